@@ -1,0 +1,120 @@
+"""Markov-head draft sampler and confidence head in fp64 — test infrastructure only.
+
+[DSpark] 方法细节, "序列阶段的依赖注入": the sequential stage induces the causal
+block distribution
+    p_k(v | x0, x<k) = exp(U_k(v) + B_k(v)) / sum_u exp(U_k(u) + B_k(u)),
+sampled left to right, x0 being the anchor (the previous round's bonus token).
+[DSpark] 方法细节, "马尔可夫头（Markov head）的实现": the Markov head restricts
+B_k to the previous token through a rank-r factorisation,
+    B(x_{k-1}, .) = W1[x_{k-1}] W2,  W1 in R^{V x r}, W2 in R^{r x V}.
+[DSpark] 方法细节, "置信度头的设计": c_k = sigmoid(w^T [h_k; W1[x_{k-1}]]).
+[DSpark] 方法细节, "并行阶段的局限与设计": the anchor is the first predicted
+position, so gamma backbone inputs give gamma base-logit rows U_1..U_gamma.
+[DeepSpec analysis] §2.2 (DFlash): markov_rank = 0 turns the head into a zero
+matrix, i.e. plain parallel drafting.
+
+Readings where the pages are silent:
+* temperature T_r per request: p_k = softmax((U_k + B_k) / T_r); T_r <= 0 (or
+  NaN) means greedy: x_k = argmax with ties to the lowest token id and p_d^k is
+  one-hot at x_k;
+* the confidence weight splits as w = [w_h (H entries); w_e (r entries)], no bias;
+* the draft draw at position k uses Philox uniform (seed, req_id, k, draw 0),
+  positions counted from 1;
+* sampling is inverse CDF in token-id order (see `oracle.sampling`).
+"""
+import numpy as np
+
+from .philox import uniform, DRAW_DRAFT
+from .sampling import inverse_cdf, argmax_first
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True):
+    """Run the draft sampler for R requests.
+
+    U [R, g, V], W1 [V, r], W2 [r, V], h [R, g, H], w [H + r]: real arrays (any
+    float dtype; read as fp64).  anchor [R] int, temp [R] float, req_id [R] int,
+    seed int.
+
+    Returns a dict:
+      tokens [R, g] int64        sampled / greedy draft tokens x_1..x_g
+      pd [R, g, V] fp64          draft probability rows (None unless keep_pd)
+      pd_tok [R, g] fp64         p_d^k(x_k)
+      conf_logit [R, g] fp64     z_k = w_h . h_k + w_e . W1[x_{k-1}]
+      conf [R, g] fp64           c_k = sigmoid(z_k)
+      margin [R, g] fp64         sampled rows: CDF margin of the draw;
+                                 greedy rows: top-2 logit gap / max(1, |l_max|)
+      greedy [R] bool
+    """
+    U = _f64(U)
+    W1 = _f64(W1)
+    W2 = _f64(W2)
+    h = _f64(h)
+    w = _f64(w)
+    R, G, V = U.shape
+    H = h.shape[2]
+    r = W1.shape[1]
+    assert W1.shape == (V, r) and W2.shape == (r, V) and w.shape == (H + r,)
+    w_h, w_e = w[:H], w[H:]
+    temp = np.asarray(temp, dtype=np.float64)
+    sampled = temp > 0
+    req_id = np.asarray(req_id, dtype=np.int64)
+    x_prev = np.asarray(anchor, dtype=np.int64).copy()
+    assert ((x_prev >= 0) & (x_prev < V)).all()
+
+    tokens = np.zeros((R, G), np.int64)
+    pd = np.zeros((R, G, V), np.float64) if keep_pd else None
+    pd_tok = np.zeros((R, G))
+    zl = np.zeros((R, G))
+    margin = np.zeros((R, G))
+    rows = np.arange(R)
+    for k in range(1, G + 1):
+        e = W1[x_prev]                              # W1[x_{k-1}]      [R, r]
+        zl[:, k - 1] = h[:, k - 1] @ w_h + e @ w_e  # confidence logit
+        logits = U[:, k - 1] + e @ W2               # U_k + B(x_{k-1}, .)
+        p = np.zeros((R, V))
+        x = np.zeros(R, np.int64)
+        if sampled.any():
+            s = sampled
+            y = logits[s] / temp[s][:, None]
+            y = y - y.max(axis=1, keepdims=True)
+            ey = np.exp(y)
+            ps = ey / ey.sum(axis=1, keepdims=True)
+            u = uniform(seed, req_id[s], k, DRAW_DRAFT)
+            xs, ms = inverse_cdf(ps, u)
+            p[s] = ps
+            x[s] = xs
+            margin[s, k - 1] = ms
+        if (~sampled).any():
+            gmask = ~sampled
+            lg = logits[gmask]
+            xg, gap = argmax_first(lg)
+            x[gmask] = xg
+            p[np.flatnonzero(gmask), xg] = 1.0
+            margin[gmask, k - 1] = gap / np.maximum(1.0, np.abs(lg.max(axis=1)))
+        tokens[:, k - 1] = x
+        pd_tok[:, k - 1] = p[rows, x]
+        if keep_pd:
+            pd[:, k - 1] = p
+        x_prev = x
+    conf = 1.0 / (1.0 + np.exp(-zl))
+    return dict(tokens=tokens, pd=pd, pd_tok=pd_tok, conf_logit=zl, conf=conf,
+                margin=margin, greedy=~sampled)
+
+
+def draft_row_distribution(U_k, W1, W2, x_prev, T):
+    """p_d^k for one request and one position, given the previous token (fp64).
+
+    Used by the statistical pins to state the conditional distribution of
+    x_k given x_{k-1}."""
+    logits = _f64(U_k) + _f64(W1)[int(x_prev)] @ _f64(W2)
+    if T > 0:
+        y = logits / T
+        ey = np.exp(y - y.max())
+        return ey / ey.sum()
+    p = np.zeros_like(logits)
+    p[int(np.argmax(logits))] = 1.0
+    return p

@@ -1,0 +1,173 @@
+"""Sequential Temperature Scaling, the hardware-aware prefix scheduler and the
+flattened verify batch — test infrastructure only.
+
+[DSpark] 方法细节, "事后校准（Post-hoc Calibration）": STS applies one
+temperature per draft position to the confidence; temperature scaling keeps the
+order of the scores.  The formula is not printed; reading: standard temperature
+scaling of the pre-sigmoid logit, c'_k = sigmoid(z_k / tau_k) (tau_k = 1 is the
+identity).
+
+[DSpark] 方法细节, "硬件感知前缀调度器": survival a_{r,j} = prod_{i<=j} c_{r,i};
+verify batch size B = sum_r (1 + l_r); expected accepted tokens
+tau = sum_r (1 + sum_{j<=l_r} a_{r,j}); objective Theta = tau * SPS(B).
+
+[DSpark] 方法细节, "贪心求解与因果性保证", Algorithm 1: candidates
+E = {(r, j) : a_{r,j} > 0} sorted by a descending; start from l_r = 0,
+B = R, tau = R, Theta_best = R * SPS(R); admit candidates in order, updating B,
+tau and Theta; keep the admission while Theta > Theta_best, stop at the first
+candidate with Theta <= Theta_best.
+
+[DSpark] 附录, "无早停机制导致的选择偏差反例": the counterexample for a
+search without the early stop (used as a pin in the tests).
+
+[DSpark] 补充细节, "高吞吐量与低延迟推理": the kept tokens of all requests are
+flattened into one batch and a marker tensor carries the intra-sequence
+dependency.
+
+Readings where the pages are silent (this library's contract):
+* c'_k is the fp32 rounding of sigmoid(z/tau) evaluated in fp64, and a_{r,j} is
+  the left-to-right fp32 product of the c'; both are sort keys, so both sides
+  must produce the same bits;
+* ties in a are broken by request index, then position (ascending), which
+  keeps every request's kept set a prefix;
+* tau and Theta are accumulated in fp64, in sorted order;
+* the SPS table is given per total verify-token count n (entries 0..R(1+g));
+* "scheduler off" verifies every draft token (l_r = g);
+* flattened layout: request-major rows, position ascending, row (r, 0) is the
+  anchor and row (r, j) the draft token x_j; marker = (request, position).
+"""
+import numpy as np
+
+MODE_OFF = 0
+MODE_GREEDY = 1
+
+
+def sts_calibrate(conf_logit, sts_temp):
+    """c' = fp32(sigmoid(z / tau)) with the sigmoid evaluated in fp64.
+
+    conf_logit [R, g] fp32 values, sts_temp [g] fp32 values.
+    Returns (c [R, g] float32, margin [R, g] fp64): margin is the relative
+    distance of the fp64 sigmoid to the nearest fp32 rounding midpoint."""
+    z = np.asarray(conf_logit, dtype=np.float32).astype(np.float64)
+    tau = np.asarray(sts_temp, dtype=np.float32).astype(np.float64)
+    t = z / tau[None, :]
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-t))
+    c = s.astype(np.float32)
+    up = np.nextafter(c, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(c, np.float32(0)).astype(np.float64)
+    cd = c.astype(np.float64)
+    mid_up = 0.5 * (cd + up)
+    mid_dn = 0.5 * (cd + dn)
+    dist = np.minimum(np.abs(s - mid_up), np.abs(s - mid_dn))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        margin = np.where(s > 0, dist / s, np.inf)
+    return c, margin
+
+
+def survival(c):
+    """a_{r,j} = c_{r,1} * ... * c_{r,j}, left to right in fp32.  c [R, g] float32."""
+    c = np.asarray(c, dtype=np.float32)
+    a = np.empty_like(c)
+    run = np.ones(c.shape[0], dtype=np.float32)
+    for j in range(c.shape[1]):
+        run = (run * c[:, j]).astype(np.float32)
+        a[:, j] = run
+    return a
+
+
+def sorted_candidates(a):
+    """E = {(r, j): a > 0} in admission order (a desc, r asc, j asc).
+
+    Returns (r_idx, j_idx) int64 arrays; j is 0-based (paper position j+1)."""
+    a = np.asarray(a, dtype=np.float32)
+    R, G = a.shape
+    rr, jj = np.nonzero(a > 0)
+    vals = a[rr, jj].astype(np.float64)
+    order = np.lexsort((jj, rr, -vals))
+    return rr[order], jj[order]
+
+
+def prefix_schedule(a, sps, mode=MODE_GREEDY, early_stop=True):
+    """Algorithm 1 on survival products a [R, g] (fp32) and the SPS table.
+
+    mode MODE_OFF returns l_r = g for every request (the "static" full-block
+    verify) with theta_best = 0.
+    With early_stop=False the search walks the whole sorted list and returns
+    the best prefix of it (the search the appendix warns about).
+
+    Returns dict(ell [R] int64, theta_best fp64, n_admit int, thetas list
+    (Theta_0, Theta_1, ... as evaluated), theta_margin fp64 = smallest relative
+    gap |Theta_i - Theta_best| / Theta_i over the comparisons made)."""
+    a = np.asarray(a, dtype=np.float32)
+    sps = np.asarray(sps, dtype=np.float64)
+    R, G = a.shape
+    if mode == MODE_OFF:
+        return dict(ell=np.full(R, G, np.int64), theta_best=0.0, n_admit=R * G,
+                    thetas=[], theta_margin=np.inf)
+    rr, jj = sorted_candidates(a)
+    B = R
+    tau = float(R)
+    theta_best = R * sps[R]
+    thetas = [theta_best]
+    ell = np.zeros(R, np.int64)
+    best_ell = ell.copy()
+    n_admit = 0
+    best_n = 0
+    margin = np.inf
+    for i, (r, j) in enumerate(zip(rr, jj)):
+        ell[r] = j + 1
+        B += 1
+        tau += float(a[r, j])
+        theta = tau * sps[B]
+        thetas.append(theta)
+        margin = min(margin, abs(theta - theta_best) / max(abs(theta), abs(theta_best)))
+        if theta > theta_best:
+            theta_best = theta
+            best_ell = ell.copy()
+            best_n = i + 1
+        elif early_stop:
+            break
+    n_admit = best_n
+    return dict(ell=best_ell, theta_best=theta_best, n_admit=n_admit, thetas=thetas,
+                theta_margin=margin)
+
+
+def flatten(ell, anchor, tokens):
+    """Flattened verify batch and marker tensor.
+
+    Returns dict(offsets [R+1], flat_tok [N], mark_req [N], mark_pos [N]) as
+    int64; N = sum_r (1 + l_r)."""
+    ell = np.asarray(ell, dtype=np.int64)
+    anchor = np.asarray(anchor, dtype=np.int64)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    R = ell.shape[0]
+    offsets = np.zeros(R + 1, np.int64)
+    offsets[1:] = np.cumsum(1 + ell)
+    N = int(offsets[-1])
+    flat_tok = np.zeros(N, np.int64)
+    mark_req = np.zeros(N, np.int64)
+    mark_pos = np.zeros(N, np.int64)
+    for r in range(R):
+        o = offsets[r]
+        L = ell[r]
+        flat_tok[o] = anchor[r]
+        flat_tok[o + 1:o + 1 + L] = tokens[r, :L]
+        mark_req[o:o + 1 + L] = r
+        mark_pos[o:o + 1 + L] = np.arange(L + 1)
+    return dict(offsets=offsets, flat_tok=flat_tok, mark_req=mark_req, mark_pos=mark_pos)
+
+
+def schedule(conf_logit, sts_temp, sps, anchor, tokens, mode=MODE_GREEDY, early_stop=True):
+    """STS -> survival -> Algorithm 1 -> flatten, as one call.
+
+    Returns the union of the dicts above plus c (calibrated, fp32), a (fp32) and
+    sts_margin (smallest rounding margin of c over the batch)."""
+    c, m = sts_calibrate(conf_logit, sts_temp)
+    a = survival(c)
+    res = prefix_schedule(a, sps, mode, early_stop)
+    res.update(flatten(res["ell"], anchor, tokens))
+    res["c"] = c
+    res["a"] = a
+    res["sts_margin"] = float(m.min()) if m.size else np.inf
+    return res

@@ -1,0 +1,120 @@
+"""Lossless rejection-sampling verification in fp64 — test infrastructure only.
+
+[DSpark] 背景知识与设计原则, "投机解码的延迟建模": at draft position k the
+target distribution p_t^k is compared with the draft distribution p_d^k and x_k
+is accepted with probability min(1, p_t^k(x_k) / p_d^k(x_k)); verification runs
+left to right and the first rejection discards every later token.
+[MTP Survey] §2.2 "拒绝采样（Rejection Sampling）：无损校验的数学": at the
+rejecting position a correction token is drawn from
+q^k = norm(max(0, p_t^k - p_d^k)); when every draft token is accepted one bonus
+token comes from the target; at temperature 0 the rule degenerates to "accept
+iff x_k = argmax p_t^k, else emit that argmax".
+
+Readings where the pages are silent (this library's contract):
+* verify rows: request r's rows in the flattened batch are [x0, x_1..x_l]; row
+  j (0-based) holds the target logits that give p_t^{j+1}.  All l accepted ->
+  the bonus comes from row l, i.e. p_t^{l+1} (the only reading consistent with
+  1 + l rows per request);
+* p_t = softmax(z / T_r) with the request's temperature T_r (same as the
+  draft's); T_r <= 0 means greedy, argmax ties to the lowest token id;
+* accept test: u * p_d(x) < p_t(x) with u = Philox(seed, req, j, draw 1), which
+  equals u < min(1, p_t/p_d) for u in [0, 1); decision margin
+  |u p_d - p_t| / max(u p_d, p_t);
+* residual: draw 2 at the rejecting position, inverse CDF of
+  max(0, p_t - p_d) / sum; if that sum is 0 in the implementation's arithmetic
+  (reachable only through rounding), sample p_t instead;
+* bonus: draw 3 at position l + 1, inverse CDF of p_t^{l+1}.
+"""
+import numpy as np
+
+from .philox import uniform, DRAW_ACCEPT, DRAW_RESIDUAL, DRAW_BONUS
+from .sampling import inverse_cdf, argmax_first
+
+
+def _softmax_rows(z, T):
+    y = z / T[:, None]
+    ey = np.exp(y - y.max(axis=1, keepdims=True))
+    return ey / ey.sum(axis=1, keepdims=True)
+
+
+def verify(target_rows, offsets, ell, tokens, pd_rows, pd_tok, temp, seed, req_id):
+    """Verify R requests.
+
+    target_rows [N, V] (row offsets[r] + j -> p_t^{j+1} of request r),
+    offsets [R+1], ell [R], tokens [R, g], pd_tok [R, g], temp [R], req_id [R];
+    pd_rows: [R, g, V] array or a callable (r, k0) -> row of p_d^{k0+1}.
+
+    Returns dict(n_accept [R], out_tok [R, g+1] (-1 after the emitted tokens),
+    n_out [R], accept_margin [R] (smallest accept-test margin met before the
+    last decision; inf if none), sample_margin [R] (CDF margin of the final
+    draw; inf for greedy rows), residual_fallback [R] bool)."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    ell = np.asarray(ell, dtype=np.int64)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    pd_tok = np.asarray(pd_tok, dtype=np.float64)
+    temp = np.asarray(temp, dtype=np.float64)
+    req_id = np.asarray(req_id, dtype=np.int64)
+    R, G = tokens.shape
+    sampled = temp > 0
+    get_pd = pd_rows if callable(pd_rows) else None
+
+    m = np.zeros(R, np.int64)
+    alive = np.ones(R, bool)  # no rejection seen yet
+    acc_margin = np.full(R, np.inf)
+    for j in range(1, G + 1):
+        act = alive & (ell >= j)
+        if not act.any():
+            break
+        idx = np.flatnonzero(act)
+        z = np.asarray(target_rows[offsets[idx] + j - 1], dtype=np.float64)
+        x = tokens[idx, j - 1]
+        acc = np.zeros(idx.size, bool)
+        s = sampled[idx]
+        if s.any():
+            pt = _softmax_rows(z[s], temp[idx[s]])
+            u = uniform(seed, req_id[idx[s]], j, DRAW_ACCEPT)
+            lhs = u * pd_tok[idx[s], j - 1]
+            rhs = pt[np.arange(pt.shape[0]), x[s]]
+            acc[s] = lhs < rhs
+            mg = np.abs(lhs - rhs) / np.maximum(np.maximum(lhs, rhs), 1e-300)
+            acc_margin[idx[s]] = np.minimum(acc_margin[idx[s]], mg)
+        if (~s).any():
+            am, _ = argmax_first(z[~s])
+            acc[~s] = x[~s] == am
+        m[idx[acc]] += 1
+        alive[idx[~acc]] = False
+
+    # final token: row m of each request (the rejecting row, or row l = m for the bonus)
+    out_tok = np.full((R, G + 1), -1, np.int64)
+    out_tok[:, :G] = np.where(np.arange(G)[None, :] < m[:, None], tokens, -1)
+    sample_margin = np.full(R, np.inf)
+    fallback = np.zeros(R, bool)
+    rejected = m < ell
+    final_rows = offsets[:R] + m
+    g = np.flatnonzero(~sampled)
+    if g.size:
+        am, _ = argmax_first(np.asarray(target_rows[final_rows[g]], dtype=np.float64))
+        out_tok[g, m[g]] = am
+    for idx, is_rej in ((np.flatnonzero(sampled & rejected), True),
+                        (np.flatnonzero(sampled & ~rejected), False)):
+        if idx.size == 0:
+            continue
+        z = np.asarray(target_rows[final_rows[idx]], dtype=np.float64)
+        pt = _softmax_rows(z, temp[idx])
+        if is_rej:
+            pdr = np.stack([get_pd(int(r), int(m[r])) for r in idx]) if callable(pd_rows) \
+                else np.asarray(pd_rows[idx, m[idx]], dtype=np.float64)
+            q = np.maximum(0.0, pt - pdr)
+            Q = q.sum(axis=1)
+            zero = ~(Q > 0)
+            q = np.where(zero[:, None], pt, q / np.where(zero, 1.0, Q)[:, None])
+            fallback[idx] = zero
+            u = uniform(seed, req_id[idx], m[idx] + 1, DRAW_RESIDUAL)
+        else:
+            q = pt
+            u = uniform(seed, req_id[idx], ell[idx] + 1, DRAW_BONUS)
+        x, mg = inverse_cdf(q, u)
+        out_tok[idx, m[idx]] = x
+        sample_margin[idx] = mg
+    return dict(n_accept=m, out_tok=out_tok, n_out=m + 1, accept_margin=acc_margin,
+                sample_margin=sample_margin, residual_fallback=fallback)

@@ -1,0 +1,86 @@
+"""The pins have teeth: plant a plausible mistake in a copy of the oracle (on the
+CPU) and check that the lossless / acceptance pins reject it.  Each mutation is a
+one-token edit of the oracle's source, executed as a throw-away module."""
+import importlib.util
+import os
+import sys
+import types
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+from oracle.draft import draft
+from oracle import schedule as S
+
+ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+
+
+def _mutant(module, old, new):
+    src = open(os.path.join(ORACLE_DIR, module + ".py")).read()
+    assert src.count(old) == 1, (module, old)
+    src = src.replace(old, new)
+    mod = types.ModuleType("oracle._mutant_" + module)
+    mod.__package__ = "oracle"
+    exec(compile(src, f"<mutant {module}>", "exec"), mod.__dict__)
+    return mod
+
+
+def _lossless_pvalues(verify_fn, draft_fn=draft, T=1.0, R=200_000):
+    rng = np.random.default_rng(1)
+    V, G, r = 8, 3, 3
+    tgt = rng.normal(size=(G + 1, V)) * 1.5
+    U = tgt[:G] + rng.normal(size=(G, V)) * 1.2
+    W1 = rng.normal(size=(V, r)) * 0.8
+    W2 = rng.normal(size=(r, V)) * 0.8
+    d = draft_fn(np.broadcast_to(U, (R, G, V)), W1, W2, np.zeros((R, G, 1)), np.zeros(1 + r),
+                 np.full(R, 2), np.full(R, T), 5, np.arange(R))
+    ell = np.full(R, G)
+    fl = S.flatten(ell, np.full(R, 2), d["tokens"])
+    v = verify_fn(tgt[fl["mark_pos"]], fl["offsets"], ell, d["tokens"], d["pd"], d["pd_tok"],
+                  np.full(R, T), 5, np.arange(R))
+    pt = special.softmax(tgt / T, axis=1)
+    ps = []
+    for j in range(G):
+        sel = v["n_out"] > j
+        obs = np.bincount(v["out_tok"][sel, j], minlength=V)
+        ps.append(stats.chisquare(obs, pt[j] * sel.sum()).pvalue)
+    return ps
+
+
+def test_unmutated_oracle_passes():
+    from oracle.verify import verify
+    assert min(_lossless_pvalues(verify)) > 1e-4
+
+
+@pytest.mark.parametrize("old,new", [
+    ("q = np.maximum(0.0, pt - pdr)", "q = np.maximum(0.0, pdr - pt)"),           # residual sign
+    ("acc[s] = lhs < rhs", "acc[s] = lhs > rhs"),                                   # accept test flipped
+    ("lhs = u * pd_tok[idx[s], j - 1]", "lhs = u * pd_tok[idx[s], j - 1] * 0.5"),   # wrong ratio
+    ("final_rows = offsets[:R] + m", "final_rows = offsets[:R] + np.maximum(m - 1, 0)"),  # off-by-one row
+    ("x = tokens[idx, j - 1]", "x = tokens[idx, np.maximum(j - 2, 0)]"),             # wrong draft index
+])
+def test_verify_mutations_are_caught(old, new):
+    mod = _mutant("verify", old, new)
+    assert min(_lossless_pvalues(mod.verify)) < 1e-6
+
+
+@pytest.mark.parametrize("old,new", [
+    ("e = W1[x_prev]  ", "e = W1[(x_prev + 1) % V]  "),                      # wrong previous token
+    ("logits = U[:, k - 1] + e @ W2", "logits = U[:, k - 1] - e @ W2"),      # wrong bias sign
+    ("y = logits[s] / temp[s][:, None]", "y = logits[s] * temp[s][:, None]"),  # temperature inverted
+])
+def test_draft_mutations_are_caught(old, new):
+    # the closed-form pin of the draft sampler: with U = 0, r = V, W1 = I and
+    # W2 = log P the head is a Markov chain with transition matrix P, so
+    # (x_1, x_2) given the anchor has law P^(1/T)[x0, a] P^(1/T)[a, b] (rows renormalised)
+    mod = _mutant("draft", old, new)
+    V, R, G, x0, T = 5, 100_000, 2, 3, 0.5
+    P = np.random.default_rng(11).dirichlet(np.full(V, 0.8), size=V)
+    out = mod.draft(np.zeros((R, G, V)), np.eye(V), np.log(P), np.zeros((R, G, 1)), np.zeros(1 + V),
+                    np.full(R, x0), np.full(R, T), 7, np.arange(R), keep_pd=False)
+    PT = P ** (1.0 / T)
+    PT /= PT.sum(axis=1, keepdims=True)
+    expect = np.outer(PT[x0], np.ones(V)) * PT
+    obs = np.bincount(out["tokens"][:, 0] * V + out["tokens"][:, 1], minlength=V * V)
+    assert stats.chisquare(obs, expect.ravel() * R).pvalue < 1e-6
