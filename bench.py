@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Benchmark of one DSpark decode step on GB300: draft sample + schedule + verify.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is dspark_draft_sample + dspark_schedule
++ dspark_verify over one batch of synthetic inputs (seeded; the shapes and value
+model of the DSpark pages' workloads).  The target model's forward on the
+flattened verify batch is not part of the path: a gather of synthetic target
+rows stands in for it and is excluded from the timed region (CUDA events around
+the two timed segments of every step).  Inputs (U alone is B*gamma*V*2 bytes,
+545 MB at the headline point) are larger than the 129 MB L2, so no flush is
+needed between steps.
+
+metric: request-positions/s = B * gamma / t_step, and the step's % of the HBM
+roofline.  --impl reference times the fp64 CPU oracle on the host cores instead
+(a bounded sample of the same workload, extrapolated per request).
+
+Multi-GPU (torchrun, one rank per GPU): the path shards by request with no
+exchange except the scheduler; this benchmark runs independent replicas (weak
+scaling), barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "spec-decode request-positions/s (draft+schedule+verify) at V=151936; % HBM peak"
+UNIT = "request-positions/s"
+
+
+# ---------------------------------------------------------------------------
+# byte model (algorithmic bytes of one step; every figure counted once)
+# ---------------------------------------------------------------------------
+def step_bytes(wl: synth.Workload, n_verify_rows: int) -> dict:
+    e = 2 if wl.dtype == "bf16" else 4
+    B, G, V, r, H = wl.B, wl.gamma, wl.V, wl.r, wl.H
+    U = B * G * V * e
+    W2_strict = r * V * e
+    W2_per_pos = G * r * V * e
+    pd = B * G * V * 4
+    target = n_verify_rows * V * e
+    resid = B * V * (e + 4)
+    small = B * G * (r * e + H * e + 24)
+    draft_strict = U + W2_strict + pd + B * G * (r * e + H * e + 16)
+    return dict(U=U, W2_strict=W2_strict, W2_per_position=W2_per_pos, pd=pd, target=target, resid=resid,
+                small=small, step_strict=U + W2_strict + pd + target + resid + small,
+                step_per_position=U + W2_per_pos + pd + target + resid + small, draft_strict=draft_strict)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from draft_sampling_lossless_markov_gb300 import build, capi
+    from draft_sampling_lossless_markov_gb300 import torch_api as T
+
+    build.build()
+    capi.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.get_workload(args.workload)
+    B, G, V = wl.B, wl.gamma, wl.V
+    inp = synth.make_inputs(wl, dev)
+    ws = T.Workspace.create(T.dims(B, G, V, wl.r, wl.H, inp["U"].dtype), device=dev)
+    cap = B * (G + 1)
+    sps_dev = torch.from_numpy(inp["sps"]).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    # outputs (allocated once)
+    d_out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
+                 pd_rows=torch.empty((B, G, V), dtype=torch.float32, device=dev),
+                 pd_tok=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 conf_logit=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 conf=torch.empty((B, G), dtype=torch.float32, device=dev))
+    s_out = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
+                 offsets=torch.empty(B + 1, dtype=torch.int32, device=dev),
+                 flat_tok=torch.empty(cap, dtype=torch.int32, device=dev),
+                 mark_req=torch.empty(cap, dtype=torch.int32, device=dev),
+                 mark_pos=torch.empty(cap, dtype=torch.int32, device=dev),
+                 n_verify=torch.empty(1, dtype=torch.int32, device=dev),
+                 theta_best=torch.empty(1, dtype=torch.float64, device=dev))
+    v_out = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
+                 out_tok=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+                 n_out=torch.empty(B, dtype=torch.int32, device=dev))
+    rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
+    tgt_flat = inp["target"].reshape(-1, V)
+
+    def seg1(st):
+        T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
+                       inp["req_id"], inp["seed"], out=d_out, stream=st)
+        T.schedule(ws, d_out["conf_logit"], inp["sts"], sps_dev, inp["anchor"], d_out["tokens"], wl.sched,
+                   out=s_out, stream=st)
+
+    def standin(st):
+        # stand-in for the target forward on the flattened batch (not timed): rows
+        # past N_v hold markers -1 and are clamped to row 0
+        with torch.cuda.stream(st):
+            idx = (s_out["mark_req"].long().clamp_min(0) * (G + 1) + s_out["mark_pos"].long().clamp_min(0))
+            torch.index_select(tgt_flat, 0, idx, out=rows)
+
+    def seg2(st):
+        T.verify(ws, rows, s_out["offsets"], s_out["ell"], d_out["tokens"], d_out["pd_rows"], d_out["pd_tok"],
+                 inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st)
+
+    use_graph = not args.no_graph
+    n0 = capi.dspark_launch_count()
+    with torch.cuda.stream(stream):
+        seg1(stream)
+        standin(stream)
+        seg2(stream)
+    stream.synchronize()
+    launches_per_step = capi.dspark_launch_count() - n0
+    if use_graph:
+        g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            seg1(torch.cuda.current_stream())
+        with torch.cuda.graph(g2, stream=stream):
+            seg2(torch.cuda.current_stream())
+        run1 = lambda: g1.replay()  # noqa: E731
+        run2 = lambda: g2.replay()  # noqa: E731
+    else:
+        run1 = lambda: seg1(stream)  # noqa: E731
+        run2 = lambda: seg2(stream)  # noqa: E731
+
+    def one_step(ev=None):
+        with torch.cuda.stream(stream):
+            if ev:
+                ev[0].record(stream)
+            run1()
+            if ev:
+                ev[1].record(stream)
+            standin(stream)
+            if ev:
+                ev[2].record(stream)
+            run2()
+            if ev:
+                ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    stream.synchronize()
+    # per-call breakdown (outside the timed loop): draft, schedule, verify separately
+    br = per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sps_dev)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    cvd = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    nv_sum = 0
+    for k in range(args.steps):
+        one_step(evs[k])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms_steps = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
+    ms = float(np.mean(ms_steps))
+    nv = int(s_out["n_verify"][0])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+        dist.barrier()
+    code, detail = ws.read_error()
+    if code != 0:
+        raise RuntimeError(f"device error word {capi.dspark_status_string(code)} ({detail})")
+
+    value = world * B * G / (ms * 1e-3)
+    peak, peak_kind = load_peaks()
+    bytes_ = step_bytes(wl, nv)
+    step_frac = bytes_["step_strict"] / (ms * 1e-3) / 1e9 / peak
+    # dominant call: the draft sampler; its strict algorithmic bytes over its measured time
+    draft_ms = br["draft_ms"]
+    draft_gbs = bytes_["draft_strict"] / (draft_ms * 1e-3) / 1e9
+    e2e = run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev) if not args.no_e2e else None
+    traffic = load_traffic(wl)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
+        "config": {"workload": wl.name, "B": B, "gamma": G, "V": V, "r": wl.r, "H": wl.H, "temp": wl.temp,
+                   "scheduler": "greedy_early_stop" if wl.sched else "off", "n_verify_rows": nv,
+                   "l2": "inputs larger than L2 (U alone %.0f MB per step), no flush" % (bytes_["U"] / 1e6),
+                   "graph": use_graph, "parallelism": "replicas" if world > 1 else "1gpu"},
+        "hbm_frac_step": step_frac,
+        "hbm_frac_step_w2_per_position": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
+        "breakdown_ms": br,
+        "roofline": {"bound": "hbm", "kernel": "dspark_draft_sample (logits passes + select)",
+                     "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
+                     "unit": "GB/s", "frac": draft_gbs / peak, "traffic": traffic,
+                     "algorithmic_bytes": bytes_["draft_strict"]},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "launches_per_step": int(launches_per_step),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_sample)
+    return res
+
+
+def per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sps_dev, reps=3):
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    acc = np.zeros(3)
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
+                           inp["req_id"], inp["seed"], out=d_out, stream=stream)
+            ev[1].record(stream)
+            T.schedule(ws, d_out["conf_logit"], inp["sts"], sps_dev, inp["anchor"], d_out["tokens"], wl.sched,
+                       out=s_out, stream=stream)
+            ev[2].record(stream)
+            standin(stream)
+            ev[3].record(stream)
+            seg2(stream)
+            ev[4].record(stream)
+        stream.synchronize()
+        acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[3].elapsed_time(ev[4])]
+    acc /= reps
+    return {"draft_ms": float(acc[0]), "schedule_ms": float(acc[1]), "verify_ms": float(acc[2])}
+
+
+def load_traffic(wl):
+    """Per-launch DRAM bytes of the dominant call from a committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d.get(wl.name)
+        except (ValueError, OSError):
+            return None
+    return None
+
+
+def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
+    """Same metric through the public API with HOST buffers: each step copies the
+    step's inputs from pinned host memory, runs the three calls, reads N_v and the
+    markers back, copies the kept target rows in, verifies, and reads the result."""
+    import torch
+    B, G, V = wl.B, wl.gamma, wl.V
+    h_U = inp["U"].cpu().pin_memory()
+    h_h = inp["h"].cpu().pin_memory()
+    h_small = {k: inp[k].cpu().pin_memory() for k in ("anchor", "temp", "req_id")}
+    h_tgt = inp["target"].cpu().pin_memory()  # [B, G+1, V]: the target model's rows live on the host here
+    d_U = torch.empty_like(inp["U"])
+    d_h = torch.empty_like(inp["h"])
+    d_small = {k: torch.empty_like(inp[k]) for k in h_small}
+    cap = B * (G + 1)
+    rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
+    h_ell = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_nv = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_out = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
+    h_nout = torch.empty(B, dtype=torch.int32).pin_memory()
+    esz = inp["U"].element_size()
+    row_bytes = V * esz
+
+    def step():
+        with torch.cuda.stream(stream):
+            d_U.copy_(h_U, non_blocking=True)
+            d_h.copy_(h_h, non_blocking=True)
+            for k in d_small:
+                d_small[k].copy_(h_small[k], non_blocking=True)
+            d = T.draft_sample(ws, d_U, inp["W1"], inp["W2"], d_h, inp["w"], d_small["anchor"], d_small["temp"],
+                               d_small["req_id"], inp["seed"], stream=stream)
+            s = T.schedule(ws, d["conf_logit"], inp["sts"], sps_dev, d_small["anchor"], d["tokens"], wl.sched,
+                           stream=stream, n_verify_host=h_nv)
+            h_ell.copy_(s["ell"], non_blocking=True)
+        stream.synchronize()
+        ell = h_ell.numpy()
+        off = 0
+        with torch.cuda.stream(stream):
+            for r in range(B):  # each request's kept rows are contiguous on both sides
+                n = int(ell[r]) + 1
+                rows[off:off + n].copy_(h_tgt[r, :n], non_blocking=True)
+                off += n
+            v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d["pd_rows"], d["pd_tok"], d_small["temp"],
+                         d_small["req_id"], inp["seed"], stream=stream)
+            h_out.copy_(v["out_tok"], non_blocking=True)
+            h_nout.copy_(v["n_out"], non_blocking=True)
+        stream.synchronize()
+        return off
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize(dev)
+    n_e2e = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    nrows = 0
+    for _ in range(n_e2e):
+        nrows += step()
+    t1 = time.perf_counter()
+    sec = (t1 - t0) / n_e2e
+    h2d = (h_U.numel() * esz + h_h.numel() * esz + sum(t.numel() * t.element_size() for t in h_small.values())
+           + nrows / n_e2e * row_bytes)
+    d2h = h_ell.numel() * 4 + 4 + h_out.numel() * 4 + h_nout.numel() * 4
+    return {"value": B * G / sec, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": n_e2e, "timer": "host wall clock around each full step (synchronised)"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample_time(wl, inp_np, n_req):
+    """fp64 oracle on the first n_req requests (draft + verify per request) plus the
+    scheduler on the full batch; returns seconds per step extrapolated to B."""
+    from oracle.draft import draft as o_draft
+    from oracle import schedule as S
+    from oracle.verify import verify as o_verify
+    B, G = wl.B, wl.gamma
+    sub = slice(0, n_req)
+    t0 = time.perf_counter()
+    d = o_draft(inp_np["U"][sub], inp_np["W1"], inp_np["W2"], inp_np["h"][sub], inp_np["w"],
+                inp_np["anchor"][sub], inp_np["temp"][sub], inp_np["seed"], inp_np["req_id"][sub])
+    t1 = time.perf_counter()
+    # scheduler over the full batch: the sampled requests' confidences tiled to B
+    zl = d["conf_logit"][np.arange(B) % n_req].astype(np.float32)
+    toks = d["tokens"][np.arange(B) % n_req]
+    sch = S.schedule(zl, inp_np["sts"], inp_np["sps"], inp_np["anchor"][np.arange(B) % n_req], toks,
+                     mode=wl.sched)
+    t2 = time.perf_counter()
+    sub_sch = S.flatten(sch["ell"][sub], inp_np["anchor"][sub], d["tokens"])
+    rows = inp_np["target"][sub][sub_sch["mark_req"], sub_sch["mark_pos"]]
+    o_verify(rows, sub_sch["offsets"], sch["ell"][sub], d["tokens"], d["pd"], d["pd_tok"], inp_np["temp"][sub],
+             inp_np["seed"], inp_np["req_id"][sub])
+    t3 = time.perf_counter()
+    per_req = (t1 - t0) + (t3 - t2)
+    return per_req / n_req * B + (t2 - t1), dict(draft_s=t1 - t0, schedule_s=t2 - t1, verify_s=t3 - t2)
+
+
+def np_inputs_for_oracle(wl, inp, n_req):
+    import torch
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    sub = slice(0, n_req)
+    return dict(U=f(inp["U"][sub]), W1=f(inp["W1"]), W2=f(inp["W2"]), h=f(inp["h"][sub]), w=f(inp["w"]),
+                anchor=inp["anchor"].cpu().numpy().astype(np.int64), temp=inp["temp"].cpu().numpy().astype(np.float64),
+                req_id=inp["req_id"].cpu().numpy().astype(np.int64), seed=inp["seed"],
+                sts=inp["sts"].cpu().numpy(), sps=inp["sps"], target=f(inp["target"][sub]))
+
+
+def cpu_baseline(wl, inp, n_req):
+    n_req = max(1, min(n_req, wl.B))
+    inp_np = np_inputs_for_oracle(wl, inp, n_req)
+    sec, parts = oracle_sample_time(wl, inp_np, n_req)
+    return {"value": wl.B * wl.gamma / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle: draft + verify of {n_req} of {wl.B} requests (extrapolated per request), "
+                      f"scheduler on the full batch; one host thread",
+            "parts_s": parts}
+
+
+def run_reference(args):
+    import torch
+    wl = synth.get_workload(args.workload)
+    inp = synth.make_inputs(wl, "cpu")
+    n_req = max(1, min(args.cpu_sample, wl.B))
+    inp_np = np_inputs_for_oracle(wl, inp, n_req)
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        oracle_sample_time(wl, inp_np, n_req)
+    secs = []
+    for _ in range(args.steps):
+        s, _ = oracle_sample_time(wl, inp_np, n_req)
+        secs.append(s)
+    sec = float(np.mean(secs))
+    value = wl.B * wl.gamma / sec
+    sample = (f"fp64 oracle per step: draft + verify of {n_req} of {wl.B} requests (extrapolated per request), "
+              f"scheduler on the full batch; one host thread")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; DSpark workload model)",
+            "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "H": wl.H},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=synth.HEADLINE.name)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=4, help="requests the oracle runs per step")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

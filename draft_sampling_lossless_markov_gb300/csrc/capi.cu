@@ -1,0 +1,163 @@
+// C ABI of the dspark library: argument checks, workspace layout, dispatch.
+// Every check happens before anything is enqueued; nothing here allocates.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "dspark.h"
+#include "internal.h"
+
+namespace dspark {
+
+size_t elem_size(int dtype) { return dtype == DSPARK_BF16 ? 2 : 4; }
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static bool dims_ok(const dspark_dims& d) {
+  if (d.B < 0 || d.gamma < 1 || d.gamma > DSPARK_MAX_GAMMA || d.V < 1) return false;
+  if (d.r < 0 || d.r > DSPARK_MAX_RANK || d.H < 0) return false;
+  if (d.dtype != DSPARK_BF16 && d.dtype != DSPARK_F32) return false;
+  // index arithmetic stays in 64 bits; per-row sizes must fit in 32 bits
+  if ((int64_t)d.B * (d.gamma + 1) > (int64_t)INT32_MAX) return false;
+  return true;
+}
+
+WsLayout ws_layout(const dspark_dims& d) {
+  WsLayout L;
+  const size_t B = (size_t)d.B, G = (size_t)d.gamma, V = (size_t)d.V, r = (size_t)d.r;
+  size_t off = sizeof(WsHeader);
+  auto take = [&](size_t bytes) {
+    off = align_up(off, 256);
+    const size_t at = off;
+    off += bytes;
+    return at;
+  };
+  // regions that depend on (B, gamma) only come first, so that dspark_schedule
+  // and dspark_verify find them at the same offsets whatever V, r, H and dtype
+  L.sk0 = take(B * G * sizeof(uint32_t));
+  L.sk1 = take(B * G * sizeof(uint32_t));
+  L.sv0 = take(B * G * sizeof(uint32_t));
+  L.sv1 = take(B * G * sizeof(uint32_t));
+  L.vrs = take(B * (G + 1) * sizeof(float4));
+  L.zh = take(B * G * sizeof(float));
+  L.rowstat = take(B * sizeof(float2));
+  L.E = take(B * r * elem_size(d.dtype));
+  const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
+  L.part = take(B * ntiles * sizeof(float4));
+  L.total = align_up(off, 256);
+  return L;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static dspark_status check_ws(const dspark_dims& d, void* ws, size_t bytes, WsLayout* L) {
+  if (!ws || ((uintptr_t)ws & 255u)) return DSPARK_INVALID_ARG;
+  *L = ws_layout(d);
+  if (bytes < L->total) return DSPARK_INVALID_ARG;
+  return DSPARK_OK;
+}
+
+static dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_CUDA_ERROR; }
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" {
+
+const char* dspark_status_string(dspark_status s) {
+  switch (s) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_INVALID_ARG: return "DSPARK_INVALID_ARG";
+    case DSPARK_UNSUPPORTED: return "DSPARK_UNSUPPORTED";
+    case DSPARK_CUDA_ERROR: return "DSPARK_CUDA_ERROR";
+    case DSPARK_TIMEOUT: return "DSPARK_TIMEOUT";
+    case DSPARK_BAD_INPUT: return "DSPARK_BAD_INPUT";
+  }
+  return "DSPARK_UNKNOWN_STATUS";
+}
+
+const char* dspark_version(void) { return "dspark-gb300 0.1 (sm_103a)"; }
+
+uint64_t dspark_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+dspark_status dspark_workspace_size(const dspark_dims* dims, size_t* bytes) {
+  if (!dims || !bytes || !dims_ok(*dims)) return DSPARK_INVALID_ARG;
+  *bytes = ws_layout(*dims).total;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < sizeof(WsHeader)) return DSPARK_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), (cudaStream_t)stream));
+}
+
+dspark_status dspark_read_error(void* workspace, int32_t* code_host, int32_t* detail_host, void* stream) {
+  if (!workspace || !code_host) return DSPARK_INVALID_ARG;
+  WsHeader h;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return DSPARK_CUDA_ERROR;
+  *code_host = h.err_code;
+  if (detail_host) *detail_host = h.err_detail;
+  e = cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return cuda_status(e);
+}
+
+dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!a || !dims_ok(a->dims)) return DSPARK_INVALID_ARG;
+  const dspark_dims& d = a->dims;
+  if (d.B == 0) return DSPARK_OK;
+  if (!a->U || !a->anchor || !a->temp || !a->req_id || !a->tokens || !a->pd_rows || !a->pd_tok ||
+      !a->conf_logit || !a->conf)
+    return DSPARK_INVALID_ARG;
+  if (d.r > 0 && (!a->W1 || !a->W2)) return DSPARK_INVALID_ARG;
+  if (d.H + d.r > 0 && !a->w) return DSPARK_INVALID_ARG;
+  if (d.H > 0 && !a->h) return DSPARK_INVALID_ARG;
+  const void* big[] = {a->U, a->W1, a->W2, a->h, a->w, a->pd_rows};
+  for (const void* p : big)
+    if (p && !aligned16(p)) return DSPARK_INVALID_ARG;
+  WsLayout L;
+  const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);
+  if (st != DSPARK_OK) return st;
+  return cuda_status(launch_draft(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
+}
+
+dspark_status dspark_schedule(const dspark_sched_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!a || a->B < 0 || a->gamma < 1 || a->gamma > DSPARK_MAX_GAMMA) return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY) return DSPARK_INVALID_ARG;
+  if ((int64_t)a->B * a->gamma > DSPARK_MAX_SCHED_KEYS) return DSPARK_UNSUPPORTED;
+  if (a->B == 0) return DSPARK_OK;
+  if (!a->conf_logit || !a->sts_temp || !a->anchor || !a->tokens || !a->ell || !a->offsets || !a->flat_tok ||
+      !a->mark_req || !a->mark_pos || !a->n_verify || !a->theta_best)
+    return DSPARK_INVALID_ARG;
+  if (a->mode == DSPARK_SCHED_GREEDY && !a->sps) return DSPARK_INVALID_ARG;
+  dspark_dims d{a->B, a->gamma, 1, 0, 0, DSPARK_F32};
+  WsLayout L;
+  const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);
+  if (st != DSPARK_OK) return st;
+  return cuda_status(launch_schedule(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
+}
+
+dspark_status dspark_verify(const dspark_verify_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!a || !dims_ok(a->dims)) return DSPARK_INVALID_ARG;
+  const dspark_dims& d = a->dims;
+  if (d.B == 0) return DSPARK_OK;
+  if (!a->target_logits || !a->offsets || !a->ell || !a->tokens || !a->pd_rows || !a->pd_tok || !a->temp ||
+      !a->req_id || !a->n_accept || !a->out_tok || !a->n_out)
+    return DSPARK_INVALID_ARG;
+  if (!aligned16(a->target_logits) || !aligned16(a->pd_rows)) return DSPARK_INVALID_ARG;
+  WsLayout L;
+  const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);
+  if (st != DSPARK_OK) return st;
+  return cuda_status(launch_verify(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,425 @@
+// Markov-head draft sampler: CUDA-core path and the per-row selection kernels.
+//
+// [DSpark] 方法细节, "序列阶段的依赖注入" / "马尔可夫头（Markov head）的实现":
+// for k = 1..gamma, l_k = U_k + W1[x_{k-1}] W2, p_d^k = softmax(l_k / T), x_k ~ p_d^k.
+// [DSpark] 方法细节, "置信度头的设计": c_k = sigmoid(w_h . h_k + w_e . W1[x_{k-1}]).
+//
+// One position k runs as
+//   k_embed        E[b] = W1[x_{k-1}], confidence of position k
+//   logits pass 1  per (row, vocabulary tile): max and sum-exp of l/T, argmax of l
+//   k_select       per row: combine the tile partials, draw u, locate the tile
+//                  that holds the draw, recompute that one tile, pick x_k
+//   logits pass 2  recompute l, write p_d = exp(l/T - m) / S and p_d(x_k)
+// The logits are recomputed rather than stored: storing them would cost a
+// 4-byte write plus a 4-byte read per element, recomputing costs a 2-byte
+// re-read of U (W2 stays in L2).  Every kernel evaluates l, l/T and exp(l/T - m)
+// with the same operations in the same order, so the recomputed tile in
+// k_select and the written row are bit-identical to pass 1's values.
+#include <float.h>
+
+#include "common.cuh"
+#include "draft_arith.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------------------
+// zh[b, k] = w_h . h[b, k, :]   (independent of the tokens: once per step)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) k_conf_hidden(const T* __restrict__ h, const T* __restrict__ w,
+                                                     float* __restrict__ zh, int BG, int H) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= BG) return;
+  float acc = 0.f;
+  if (H > 0) {
+    const T* hp = h + (size_t)warp * H;
+    if ((H & 7) == 0) {
+      for (int i = lane * 8; i < H; i += 256) {
+        float hv[8], wv[8];
+        load8_stream(hp + i, hv);
+        load8(w + i, wv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(hv[e], wv[e], acc);
+      }
+    } else {
+      for (int i = lane; i < H; i += 32) acc = fmaf(to_f32(hp[i]), to_f32(w[i]), acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) zh[warp] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// E[b] = W1[x_{k-1}], z_k = zh + w_e . E[b], c_k = sigmoid(z_k).  One warp per row.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
+                                               int k, const T* __restrict__ W1, const T* __restrict__ w,
+                                               const float* __restrict__ zh, T* __restrict__ E,
+                                               float* __restrict__ conf_logit, float* __restrict__ conf, int B, int G,
+                                               int V, int r, int H, WsHeader* hdr) {
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (b >= B) return;
+  int x = (k == 0) ? anchor[b] : tokens[(size_t)b * G + k - 1];
+  if (x < 0 || x >= V) {
+    if (lane == 0) report_error(hdr, DSPARK_BAD_INPUT, x);
+    x = 0;
+  }
+  float acc = 0.f;
+  if (r > 0) {
+    const T* row = W1 + (size_t)x * r;
+    const T* we = w + H;
+    T* dst = E + (size_t)b * r;
+    for (int i = lane; i < r; i += 32) {
+      const T v = row[i];
+      dst[i] = v;
+      acc = fmaf(to_f32(we[i]), to_f32(v), acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) {
+    const float z = zh[(size_t)b * G + k] + acc;
+    conf_logit[(size_t)b * G + k] = z;
+    conf[(size_t)b * G + k] = 1.f / (1.f + expf(-z));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core logits pass: a CTA owns CC_ROWS rows x CC_TW vocabulary columns, one
+// column per thread.  The bias is a sequential FMA chain over the rank (the same
+// chain k_select uses to recompute a tile).
+// ---------------------------------------------------------------------------
+constexpr int CC_ROWS = 16;
+constexpr int CC_TW = 256;
+
+template <typename T, bool WRITE>
+__global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, const T* __restrict__ E,
+                                                     const T* __restrict__ W2, const float* __restrict__ temp,
+                                                     int B, int G, int V, int r, int k, int ntiles,
+                                                     float4* __restrict__ part, const float2* __restrict__ rowstat,
+                                                     const int32_t* __restrict__ tokens, float* __restrict__ pd_rows,
+                                                     float* __restrict__ pd_tok) {
+  extern __shared__ float Es[];  // [CC_ROWS][r]
+  __shared__ float red_a[CC_TW / 32][CC_ROWS];
+  __shared__ float red_b[CC_TW / 32][CC_ROWS];
+  __shared__ int red_i[CC_TW / 32][CC_ROWS];
+  __shared__ float row_m[CC_ROWS];
+  __shared__ float row_invT[CC_ROWS];
+  __shared__ int row_sampled[CC_ROWS];
+
+  const int tile = blockIdx.x;
+  const int b0 = blockIdx.y * CC_ROWS;
+  const int nrows = min(CC_ROWS, B - b0);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int col = tile * CC_TW + tid;
+  const bool valid = col < V;
+
+  for (int idx = tid; idx < CC_ROWS * r; idx += CC_TW) {
+    const int i = idx / r;
+    Es[idx] = (i < nrows) ? to_f32(E[(size_t)(b0 + i) * r + (idx - i * r)]) : 0.f;
+  }
+  if (tid < CC_ROWS) {
+    const float T_ = (tid < nrows) ? temp[b0 + tid] : 1.f;
+    row_sampled[tid] = T_ > 0.f;
+    row_invT[tid] = inv_temp(T_);
+  }
+  __syncthreads();
+
+  float l[CC_ROWS];
+#pragma unroll
+  for (int i = 0; i < CC_ROWS; ++i) l[i] = 0.f;
+  if (valid) {
+    for (int kk = 0; kk < r; ++kk) {
+      const float wv = ldf(W2 + (size_t)kk * V + col);
+#pragma unroll
+      for (int i = 0; i < CC_ROWS; ++i) l[i] = fmaf(Es[i * r + kk], wv, l[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < CC_ROWS; ++i)
+      if (i < nrows) l[i] = add_base(ldf(U + ((size_t)(b0 + i) * G + k) * V + col), l[i]);
+  }
+
+  if (!WRITE) {
+    // ---- pass 1: per-row tile max of y = l/T, sum-exp, argmax of l ----
+    float y[CC_ROWS];
+#pragma unroll
+    for (int i = 0; i < CC_ROWS; ++i) {
+      y[i] = valid ? scale_logit(l[i], row_invT[i]) : -INFINITY;
+      float mv = warp_max(y[i]);
+      float av = valid ? l[i] : -INFINITY;
+      int ai = valid ? col : INT_MAX;
+      warp_argmax(av, ai);
+      if (lane == 0) {
+        red_a[wid][i] = mv;
+        red_b[wid][i] = av;
+        red_i[wid][i] = ai;
+      }
+    }
+    __syncthreads();
+    if (tid < CC_ROWS) {
+      float mv = red_a[0][tid], av = red_b[0][tid];
+      int ai = red_i[0][tid];
+      for (int w_ = 1; w_ < CC_TW / 32; ++w_) {
+        mv = fmaxf(mv, red_a[w_][tid]);
+        argmax_merge(av, ai, red_b[w_][tid], red_i[w_][tid]);
+      }
+      row_m[tid] = mv;
+      red_b[0][tid] = av;
+      red_i[0][tid] = ai;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < CC_ROWS; ++i) {
+      const float e = valid ? exp_shifted(y[i], row_m[i]) : 0.f;
+      const float sv = warp_sum(e);
+      if (lane == 0) red_a[wid][i] = sv;
+    }
+    __syncthreads();
+    if (tid < nrows) {
+      float sv = 0.f;
+      for (int w_ = 0; w_ < CC_TW / 32; ++w_) sv += red_a[w_][tid];
+      part[(size_t)(b0 + tid) * ntiles + tile] =
+          make_float4(row_m[tid], sv, red_b[0][tid], __int_as_float(red_i[0][tid]));
+    }
+  } else {
+    // ---- pass 2: p_d = exp(l/T - m) / S, one-hot for greedy rows ----
+    if (!valid) return;
+#pragma unroll
+    for (int i = 0; i < CC_ROWS; ++i) {
+      if (i >= nrows) break;
+      const int b = b0 + i;
+      const int x = tokens[(size_t)b * G + k];
+      float p;
+      if (row_sampled[i]) {
+        const float2 st = rowstat[b];
+        p = prob_from(scale_logit(l[i], row_invT[i]), st.x, st.y);
+      } else {
+        p = (col == x) ? 1.f : 0.f;
+      }
+      __stcs(pd_rows + ((size_t)b * G + k) * V + col, p);
+      if (col == x) pd_tok[(size_t)b * G + k] = p;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per-row selection.  Partials part[b, t] = (m_t, s_t, argmax value, argmax idx)
+// over tiles of `tw` columns.  Greedy rows take the global argmax.  Sampled
+// rows: m = max m_t; tile masses q_t = s_t exp(m_t - m) summed in tile order
+// give S and the prefix; target = u S; the tile where the prefix first exceeds
+// the target is recomputed column by column with the pass-1 arithmetic and
+// scanned in token order.
+// ---------------------------------------------------------------------------
+constexpr int SEL_THREADS = 256;
+
+__device__ __forceinline__ float block_excl_scan_256(float v, float* sm, float& total) {
+  // sm: >= 8 floats
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const float incl = warp_inclusive_scan(v);
+  if (lane == 31) sm[wid] = incl;
+  __syncthreads();
+  float wpre = 0.f, tot = 0.f;
+  for (int i = 0; i < SEL_THREADS / 32; ++i) {
+    if (i < wid) wpre += sm[i];
+    tot += sm[i];
+  }
+  __syncthreads();
+  total = tot;
+  return wpre + incl - v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict__ part, int ntiles, int tw,
+                                                        const T* __restrict__ U, const T* __restrict__ E,
+                                                        const T* __restrict__ W2, const float* __restrict__ temp,
+                                                        const uint32_t* __restrict__ req_id, uint64_t seed, int B,
+                                                        int G, int V, int r, int k, int32_t* __restrict__ tokens,
+                                                        float2* __restrict__ rowstat) {
+  extern __shared__ float Erow[];  // [r]
+  __shared__ float sm[32];
+  __shared__ int s_int[4];
+  __shared__ float s_flt[4];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const float4* P = part + (size_t)b * ntiles;
+  const float T_ = temp[b];
+  const bool sampled = T_ > 0.f;
+
+  if (!sampled) {
+    float av = -INFINITY;
+    int ai = INT_MAX;
+    for (int t = tid; t < ntiles; t += SEL_THREADS) argmax_merge(av, ai, P[t].z, __float_as_int(P[t].w));
+    warp_argmax(av, ai);
+    if (lane == 0) {
+      sm[wid] = av;
+      s_int[0] = 0;
+    }
+    __shared__ int sai[SEL_THREADS / 32];
+    if (lane == 0) sai[wid] = ai;
+    __syncthreads();
+    if (tid == 0) {
+      float v = sm[0];
+      int i = sai[0];
+      for (int w_ = 1; w_ < SEL_THREADS / 32; ++w_) argmax_merge(v, i, sm[w_], sai[w_]);
+      tokens[(size_t)b * G + k] = i;
+      rowstat[b] = make_float2(0.f, 1.f);
+    }
+    return;
+  }
+
+  // row max
+  float mx = -INFINITY;
+  for (int t = tid; t < ntiles; t += SEL_THREADS) mx = fmaxf(mx, P[t].x);
+  mx = warp_max(mx);
+  if (lane == 0) sm[wid] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    float v = sm[0];
+    for (int w_ = 1; w_ < SEL_THREADS / 32; ++w_) v = fmaxf(v, sm[w_]);
+    s_flt[0] = v;
+  }
+  __syncthreads();
+  const float m = s_flt[0];
+  __syncthreads();
+
+  // tile masses in tile order: each thread owns a contiguous block of tiles
+  const int cpt = (ntiles + SEL_THREADS - 1) / SEL_THREADS;
+  const int t_lo = min(tid * cpt, ntiles), t_hi = min(t_lo + cpt, ntiles);
+  float loc = 0.f;
+  for (int t = t_lo; t < t_hi; ++t) loc += tile_mass(P[t].x, P[t].y, m);
+  float S;
+  const float pre = block_excl_scan_256(loc, sm, S);
+  const float u = philox_uniform(seed, req_id[b], (uint32_t)(k + 1), 0u);
+  const float target = u * S;
+
+  // first tile whose inclusive prefix exceeds the target; also the last tile with mass
+  if (tid == 0) {
+    s_int[0] = INT_MAX;
+    s_int[1] = -1;
+  }
+  __syncthreads();
+  {
+    float run = pre;
+    int found = INT_MAX, lastpos = -1;
+    for (int t = t_lo; t < t_hi; ++t) {
+      const float q = tile_mass(P[t].x, P[t].y, m);
+      if (found == INT_MAX && run + q > target) found = t;
+      if (q > 0.f) lastpos = t;
+      run += q;
+    }
+    if (found != INT_MAX) atomicMin(&s_int[0], found);
+    if (lastpos >= 0) atomicMax(&s_int[1], lastpos);
+  }
+  __syncthreads();
+  const bool hit = s_int[0] != INT_MAX;
+  // a row without any positive mass (non-finite logits) falls back to tile 0
+  const int tstar = min(max(hit ? s_int[0] : s_int[1], 0), ntiles - 1);
+  // prefix before tstar: the owner recomputes it
+  if (tstar >= t_lo && tstar < t_hi) {
+    float run = pre;
+    for (int t = t_lo; t < tstar; ++t) run += tile_mass(P[t].x, P[t].y, m);
+    s_flt[1] = run;
+  }
+  for (int i = tid; i < r; i += SEL_THREADS) Erow[i] = to_f32(E[(size_t)b * r + i]);
+  __syncthreads();
+  const float base = s_flt[1];
+
+  // recompute the tile's columns (tw <= SEL_THREADS) with the pass-1 arithmetic
+  const float invT = inv_temp(T_);
+  const int col = tstar * tw + tid;
+  float wv = 0.f;
+  if (tid < tw && col < V) {
+    float acc = 0.f;
+    for (int kk = 0; kk < r; ++kk) acc = fmaf(Erow[kk], ldf(W2 + (size_t)kk * V + col), acc);
+    const float l = add_base(ldf(U + ((size_t)b * G + k) * V + col), acc);
+    wv = exp_shifted(scale_logit(l, invT), m);
+  }
+  float tile_tot;
+  const float excl = block_excl_scan_256(wv, sm, tile_tot);
+  if (tid == 0) {
+    s_int[2] = INT_MAX;
+    s_int[3] = -1;
+  }
+  __syncthreads();
+  if (tid < tw && col < V) {
+    if (hit && base + (excl + wv) > target) atomicMin(&s_int[2], col);
+    if (wv > 0.f) atomicMax(&s_int[3], col);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int x = (s_int[2] != INT_MAX) ? s_int[2] : s_int[3];
+    if (x < 0) x = min(tstar * tw, V - 1);  // only reachable with non-finite logits
+    tokens[(size_t)b * G + k] = x;
+    rowstat[b] = make_float2(m, S);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launcher
+// ---------------------------------------------------------------------------
+bool draft_tc_supported(const dspark_dims& d);
+cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, int k, bool write,
+                                 cudaStream_t s);
+
+template <typename T>
+static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  const int B = d.B, G = d.gamma, V = d.V, r = d.r, H = d.H;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* zh = reinterpret_cast<float*>(ws + L.zh);
+  T* E = reinterpret_cast<T*>(ws + L.E);
+  float4* part = reinterpret_cast<float4*>(ws + L.part);
+  float2* rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
+  const T* U = static_cast<const T*>(a.U);
+  const T* W1 = static_cast<const T*>(a.W1);
+  const T* W2 = static_cast<const T*>(a.W2);
+  const T* h = static_cast<const T*>(a.h);
+  const T* w = static_cast<const T*>(a.w);
+
+  const int BG = B * G;
+  k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
+  count_launches(1 + 4 * G);
+
+  const bool tc = draft_tc_supported(d);
+  const int tw = tc ? 128 : CC_TW;
+  const int ntiles = (V + tw - 1) / tw;
+  const size_t es_bytes = (size_t)CC_ROWS * r * sizeof(float);
+  if (!tc && es_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_logits_cc<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)es_bytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_logits_cc<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)es_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid_cc(ntiles, (B + CC_ROWS - 1) / CC_ROWS);
+  for (int k = 0; k < G; ++k) {
+    k_embed<T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, k, W1, w, zh, E, a.conf_logit, a.conf, B, G, V, r,
+                                             H, hdr);
+    if (tc) {
+      cudaError_t e = launch_draft_tc_pass(a, ws, L, k, false, s);
+      if (e != cudaSuccess) return e;
+    } else {
+      k_logits_cc<T, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, E, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
+                                                             a.tokens, a.pd_rows, a.pd_tok);
+    }
+    k_select<T><<<B, SEL_THREADS, (size_t)r * sizeof(float), s>>>(part, ntiles, tw, U, E, W2, a.temp, a.req_id,
+                                                                   a.seed, B, G, V, r, k, a.tokens, rowstat);
+    if (tc) {
+      cudaError_t e = launch_draft_tc_pass(a, ws, L, k, true, s);
+      if (e != cudaSuccess) return e;
+    } else {
+      k_logits_cc<T, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, E, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
+                                                            a.tokens, a.pd_rows, a.pd_tok);
+    }
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  if (a.dims.dtype == DSPARK_BF16) return launch_draft_t<__nv_bfloat16>(a, ws, L, s);
+  return launch_draft_t<float>(a, ws, L, s);
+}
+
+}  // namespace dspark

@@ -1,0 +1,38 @@
+// Host-side internals shared by the dspark translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// Vocabulary columns summarised by one (max, sum-exp, argmax) partial of the
+// draft sampler.  The CUDA-core path uses 256, the tensor-core path 128; the
+// workspace is sized for the smaller width.
+constexpr int kPartialTileMin = 128;
+
+struct WsLayout {
+  size_t zh = 0;       // [B*G] f32: w_h . h_k
+  size_t E = 0;        // [B*r] dtype: W1 rows of the previous tokens
+  size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index)
+  size_t rowstat = 0;  // [B] float2: (row max, row sum) of the current position
+  size_t sk0 = 0, sk1 = 0, sv0 = 0, sv1 = 0;  // scheduler sort buffers [B*G] u32
+  size_t vrs = 0;      // [B*(G+1)] float4: verify row stats
+  size_t total = 0;
+};
+
+WsLayout ws_layout(const dspark_dims& d);
+
+// host-side launch accounting (dspark_launch_count)
+void count_launches(int n);
+size_t elem_size(int dtype);
+
+// Launchers (argument checking happens in capi.cu before these are called).
+cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+
+}  // namespace dspark

@@ -1,0 +1,275 @@
+// Sequential Temperature Scaling, the hardware-aware prefix scheduler and the
+// flattened verify batch, as one CTA of 1024 threads.
+//
+// [DSpark] 方法细节, "事后校准（Post-hoc Calibration）": c'_k = sigmoid(z_k / tau_k).
+// [DSpark] 方法细节, "硬件感知前缀调度器" / "贪心求解与因果性保证", Algorithm 1:
+// a_{r,j} = prod_{i<=j} c'_{r,i}; candidates (a > 0) sorted by a descending;
+// Theta_i = (B + sum of the first i sorted a) * SPS[B + i]; admit until the first
+// Theta_i <= Theta_{i-1}.
+// [DSpark] 补充细节, "高吞吐量与低延迟推理": kept prefixes flattened with a
+// marker tensor.
+//
+// At most 65536 candidates (B * gamma), so one CTA does it all:
+//   1. c' (fp64 sigmoid rounded to fp32), a (fp32 running product), sort keys
+//      key = ~bits(a) for a > 0 (ascending key = descending a), 0xFFFFFFFF else,
+//      value = r * gamma + j, laid out in index order;
+//   2. stable LSD radix sort of the keys (4 passes of 8 bits); stability keeps
+//      equal a in (r, j) index order;
+//   3. fp64 block scan of the sorted a, Theta_i, first non-increase;
+//   4. l_r by atomic max over the admitted candidates;
+//   5. offsets by a block scan of 1 + l_r; flatten + markers.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+constexpr int SCH_THREADS = 1024;
+constexpr int SCH_WARPS = SCH_THREADS / 32;
+
+// calibrated confidence: fp32 rounding of the fp64 sigmoid of z / tau
+__device__ __forceinline__ float sts_conf(float z, float tau) {
+  const double t = (double)z / (double)tau;
+  const double s = 1.0 / (1.0 + exp(-t));
+  return (float)s;
+}
+
+// block-wide exclusive scan of one u32 per thread; returns the exclusive prefix
+__device__ __forceinline__ uint32_t block_excl_scan_u32(uint32_t v, uint32_t* sm, uint32_t& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) sm[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t y = sm[lane];
+    uint32_t z = y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += t;
+    }
+    sm[lane] = z - y;  // exclusive prefix of warp totals
+    if (lane == 31) sm[32] = z;
+  }
+  __syncthreads();
+  const uint32_t res = sm[wid] + x - v;
+  total = sm[32];
+  __syncthreads();
+  return res;
+}
+
+__device__ __forceinline__ double block_excl_scan_f64(double v, double* sm, double& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  double x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) sm[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    double z = sm[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double t = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += t;
+    }
+    double ze = __shfl_up_sync(0xffffffffu, z, 1);
+    sm[lane] = (lane == 0) ? 0.0 : ze;
+    if (lane == 31) sm[32] = z;
+  }
+  __syncthreads();
+  double xe = __shfl_up_sync(0xffffffffu, x, 1);  // exclusive prefix within the warp
+  if (lane == 0) xe = 0.0;
+  const double res = sm[wid] + xe;
+  total = sm[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a, uint32_t* __restrict__ k0,
+                                                             uint32_t* __restrict__ k1, uint32_t* __restrict__ v0,
+                                                             uint32_t* __restrict__ v1) {
+  __shared__ uint32_t hist[256 * SCH_WARPS];  // [digit][warp], digit-major
+  __shared__ uint32_t sm_u[40];
+  __shared__ double sm_d[40];
+  __shared__ int s_first;
+  __shared__ double s_theta_best;
+
+  const int B = a.B, G = a.gamma, n = B * G;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+  // ---- 1. calibrated survival products and sort keys ----
+  uint32_t ncand_local = 0;
+  for (int r = tid; r < B; r += SCH_THREADS) {
+    float run = 1.f;
+    for (int j = 0; j < G; ++j) {
+      const float c = sts_conf(a.conf_logit[(size_t)r * G + j], a.sts_temp[j]);
+      run = __fmul_rn(run, c);
+      const int idx = r * G + j;
+      const bool cand = run > 0.f;
+      k0[idx] = cand ? ~__float_as_uint(run) : 0xFFFFFFFFu;
+      v0[idx] = (uint32_t)idx;
+      ncand_local += cand;
+      if (a.surv) a.surv[idx] = run;
+    }
+    a.ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
+  }
+  uint32_t ncand;
+  block_excl_scan_u32(ncand_local, sm_u, ncand);
+
+  if (a.mode != DSPARK_SCHED_OFF) {
+    // ---- 2. stable LSD radix sort, 4 passes of 8 bits ----
+    const int seg = ((n + SCH_WARPS - 1) / SCH_WARPS + 31) & ~31;
+    const int w_lo = min(wid * seg, n), w_hi = min(w_lo + seg, n);
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 8 * pass;
+      const uint32_t* sk = (pass & 1) ? k1 : k0;
+      const uint32_t* sv = (pass & 1) ? v1 : v0;
+      uint32_t* dk = (pass & 1) ? k0 : k1;
+      uint32_t* dv = (pass & 1) ? v0 : v1;
+      for (int i = tid; i < 256 * SCH_WARPS; i += SCH_THREADS) hist[i] = 0;
+      __syncthreads();
+      for (int base = w_lo; base < w_hi; base += 32) {
+        const int idx = base + lane;
+        const bool valid = idx < w_hi;
+        const uint32_t d = valid ? ((sk[idx] >> shift) & 255u) : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (valid && lane == __ffs(peers) - 1) hist[d * SCH_WARPS + wid] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      // exclusive scan over (digit, warp) in digit-major order: 8 entries per thread
+      {
+        uint32_t loc[8], s = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          loc[e] = hist[tid * 8 + e];
+          s += loc[e];
+        }
+        uint32_t tot;
+        uint32_t p = block_excl_scan_u32(s, sm_u, tot);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          hist[tid * 8 + e] = p;
+          p += loc[e];
+        }
+      }
+      __syncthreads();
+      for (int base = w_lo; base < w_hi; base += 32) {
+        const int idx = base + lane;
+        const bool valid = idx < w_hi;
+        const uint32_t key = valid ? sk[idx] : 0u;
+        const uint32_t val = valid ? sv[idx] : 0u;
+        const uint32_t d = valid ? ((key >> shift) & 255u) : 256u;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (valid) {
+          const uint32_t dst = hist[d * SCH_WARPS + wid] + __popc(peers & lt_mask);
+          dk[dst] = key;
+          dv[dst] = val;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) hist[d * SCH_WARPS + wid] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+    }
+    // sorted keys / values are back in k0 / v0 (even number of passes)
+
+    // ---- 3. Theta along the sorted path, first non-increase ----
+    const int nc = (int)ncand;
+    const int ch = (nc + SCH_THREADS - 1) / SCH_THREADS;
+    const int c_lo = min(tid * ch, nc), c_hi = min(c_lo + ch, nc);
+    double loc = 0.0;
+    for (int i = c_lo; i < c_hi; ++i) loc += (double)__uint_as_float(~k0[i]);
+    double tot;
+    const double pre = block_excl_scan_f64(loc, sm_d, tot);
+    if (tid == 0) s_first = nc + 1;
+    __syncthreads();
+    {
+      double S = pre;
+      double theta_prev = ((double)B + S) * a.sps[B + c_lo];
+      for (int i = c_lo; i < c_hi; ++i) {  // sorted position i is candidate number i + 1
+        S += (double)__uint_as_float(~k0[i]);
+        const double theta = ((double)B + S) * a.sps[B + i + 1];
+        if (!(theta > theta_prev)) {
+          atomicMin(&s_first, i + 1);
+          break;
+        }
+        theta_prev = theta;
+      }
+    }
+    __syncthreads();
+    const int nstar = s_first - 1;  // admitted candidates
+    // Theta of the kept set: recomputed by the thread that owns candidate nstar
+    if (nstar == 0) {
+      if (tid == 0) s_theta_best = (double)B * a.sps[B];
+    } else if (nstar - 1 >= c_lo && nstar - 1 < c_hi) {
+      double S = pre;
+      for (int i = c_lo; i < nstar; ++i) S += (double)__uint_as_float(~k0[i]);
+      s_theta_best = ((double)B + S) * a.sps[B + nstar];
+    }
+    // ---- 4. l_r = number of admitted (r, .) candidates (= largest admitted j) ----
+    for (int i = tid; i < nstar; i += SCH_THREADS) {
+      const uint32_t v = v0[i];
+      atomicMax(&a.ell[v / G], (int)(v % G) + 1);
+    }
+    __syncthreads();
+    if (tid == 0) *a.theta_best = s_theta_best;
+  } else {
+    if (tid == 0) *a.theta_best = 0.0;
+  }
+  __syncthreads();
+
+  // ---- 5. offsets and the flattened batch ----
+  const int chb = (B + SCH_THREADS - 1) / SCH_THREADS;
+  const int b_lo = min(tid * chb, B), b_hi = min(b_lo + chb, B);
+  uint32_t cnt = 0;
+  for (int r = b_lo; r < b_hi; ++r) cnt += 1u + (uint32_t)a.ell[r];
+  uint32_t nv;
+  uint32_t off = block_excl_scan_u32(cnt, sm_u, nv);
+  for (int r = b_lo; r < b_hi; ++r) {
+    a.offsets[r] = (int)off;
+    const int L = a.ell[r];
+    a.flat_tok[off] = a.anchor[r];
+    a.mark_req[off] = r;
+    a.mark_pos[off] = 0;
+    for (int j = 1; j <= L; ++j) {
+      a.flat_tok[off + j] = a.tokens[(size_t)r * G + j - 1];
+      a.mark_req[off + j] = r;
+      a.mark_pos[off + j] = j;
+    }
+    off += 1u + (uint32_t)L;
+  }
+  const int cap = B * (1 + G);
+  for (int i = (int)nv + tid; i < cap; i += SCH_THREADS) {
+    a.flat_tok[i] = -1;
+    a.mark_req[i] = -1;
+    a.mark_pos[i] = -1;
+  }
+  if (tid == 0) {
+    a.offsets[B] = (int)nv;
+    *a.n_verify = (int)nv;
+  }
+}
+
+cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  uint32_t* k0 = reinterpret_cast<uint32_t*>(ws + L.sk0);
+  uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
+  uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
+  uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
+  k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.n_verify_host) e = cudaMemcpyAsync(a.n_verify_host, a.n_verify, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  return e;
+}
+
+}  // namespace dspark

@@ -1,0 +1,322 @@
+// Lossless rejection-sampling verification.
+//
+// [DSpark] 背景知识与设计原则, "投机解码的延迟建模": accept x_k with probability
+// min(1, p_t^k(x_k) / p_d^k(x_k)), left to right, the first rejection discards
+// the rest.  [MTP Survey] §2.2 "拒绝采样": resample the rejecting position from
+// norm(max(0, p_t - p_d)); bonus token when everything is accepted; argmax
+// compare at temperature 0.
+//
+// k_verify_rowstats  one CTA per kept row (request r, row j <= l_r): max and
+//                    sum-exp of z / T (sampled) or argmax of z (greedy), and
+//                    p_t at the draft token of that row.
+// k_verify_finish    one CTA per request: left-to-right accept scan over the row
+//                    statistics, then one inverse-CDF draw over the final row
+//                    (residual or bonus) with a two-level search: per-warp
+//                    segment sums, then a rescan of the one segment that holds
+//                    the draw.
+#include "common.cuh"
+#include "draft_arith.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+constexpr int RS_THREADS = 512;
+constexpr int FIN_THREADS = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restrict__ target,
+                                                                const int32_t* __restrict__ offsets,
+                                                                const int32_t* __restrict__ ell,
+                                                                const int32_t* __restrict__ tokens,
+                                                                const float* __restrict__ temp, int G, int V,
+                                                                float4* __restrict__ rs, WsHeader* hdr) {
+  __shared__ float sm_a[RS_THREADS / 32], sm_b[RS_THREADS / 32];
+  __shared__ int sm_i[RS_THREADS / 32];
+  const int r = blockIdx.x, j = blockIdx.y;
+  const int L = ell[r];
+  if (j > L) return;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const size_t row = (size_t)offsets[r] + j;
+  const T* z = target + row * V;
+  const float T_ = temp[r];
+  const bool sampled = T_ > 0.f;
+  const float invT = inv_temp(T_);
+  const bool vec = (V & 7) == 0;
+
+  if (sampled) {
+    float m = -INFINITY, s = 0.f;
+    if (vec) {
+      for (int i = tid * 8; i < V; i += RS_THREADS * 8) {
+        float v[8];
+        load8_stream(z + i, v);
+        float lm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          v[e] = scale_logit(v[e], invT);
+          lm = fmaxf(lm, v[e]);
+        }
+        if (lm > m) {
+          s = s * expf(m - lm);
+          m = lm;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += exp_shifted(v[e], m);
+      }
+    } else {
+      for (int i = tid; i < V; i += RS_THREADS) {
+        const float y = scale_logit(to_f32(z[i]), invT);
+        if (y > m) {
+          s = s * expf(m - y);
+          m = y;
+        }
+        s += exp_shifted(y, m);
+      }
+    }
+    warp_lse(m, s);
+    if (lane == 0) {
+      sm_a[wid] = m;
+      sm_b[wid] = s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float M = sm_a[0], S = sm_b[0];
+      for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) lse_merge(M, S, sm_a[w_], sm_b[w_]);
+      float ptok = 0.f;
+      if (j < L) {
+        int x = tokens[(size_t)r * G + j];
+        if (x < 0 || x >= V) {
+          report_error(hdr, DSPARK_BAD_INPUT, x);
+          x = 0;
+        }
+        ptok = prob_from(scale_logit(to_f32(z[x]), invT), M, S);
+      }
+      rs[row] = make_float4(M, S, __int_as_float(-1), ptok);
+    }
+  } else {
+    float av = -INFINITY;
+    int ai = INT_MAX;
+    if (vec) {
+      for (int i = tid * 8; i < V; i += RS_THREADS * 8) {
+        float v[8];
+        load8_stream(z + i, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) argmax_merge(av, ai, v[e], i + e);
+      }
+    } else {
+      for (int i = tid; i < V; i += RS_THREADS) argmax_merge(av, ai, to_f32(z[i]), i);
+    }
+    warp_argmax(av, ai);
+    if (lane == 0) {
+      sm_a[wid] = av;
+      sm_i[wid] = ai;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) argmax_merge(av, ai, sm_a[w_], sm_i[w_]);
+      rs[row] = make_float4(0.f, 1.f, __int_as_float(ai), 0.f);
+    }
+  }
+}
+
+// q(v) of the final draw: residual max(0, p_t - p_d) or the bonus weight exp(y - m)
+template <typename T, int MODE>  // MODE 0: residual, 1: target weights
+__device__ __forceinline__ float final_weight(const T* z, const float* pd, int v, float invT, float m, float S) {
+  const float y = scale_logit(to_f32(z[v]), invT);
+  if (MODE == 1) return exp_shifted(y, m);
+  return fmaxf(0.f, __fsub_rn(prob_from(y, m, S), pd[v]));
+}
+
+// one CTA: sum of q over the row in (warp segment, 256-element chunk) order and
+// the token where the running sum first exceeds u * sum
+template <typename T, int MODE>
+__device__ int final_draw(const T* z, const float* pd, int V, float invT, float m, float S, float u, float* sm_seg,
+                          int* sm_int, float* sm_flt, bool& zero_mass) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  constexpr int NW = FIN_THREADS / 32;
+  const int seg = (((V + NW - 1) / NW) + 255) & ~255;
+  const int s_lo = min(wid * seg, V), s_hi = min(s_lo + seg, V);
+  // pass 1: per-warp segment sums, chunk by chunk
+  float acc = 0.f;
+  for (int c = s_lo; c < s_hi; c += 256) {
+    float ls = 0.f;
+    const int v0 = c + lane * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (v0 + e < s_hi) ls += final_weight<T, MODE>(z, pd, v0 + e, invT, m, S);
+    acc += warp_sum(ls);
+  }
+  if (lane == 0) sm_seg[wid] = acc;
+  __syncthreads();
+  if (wid == 0) {
+    const float sv = sm_seg[lane];
+    const float incl = warp_inclusive_scan(sv);
+    const float total = __shfl_sync(0xffffffffu, incl, 31);
+    const float target = u * total;
+    const unsigned over = __ballot_sync(0xffffffffu, incl > target);
+    const unsigned pos = __ballot_sync(0xffffffffu, sv > 0.f);
+    int w_star;
+    bool hit = over != 0u && total > 0.f;
+    if (hit)
+      w_star = __ffs(over) - 1;
+    else
+      w_star = pos ? 31 - __clz(pos) : 0;
+    const float excl = __shfl_sync(0xffffffffu, incl - sv, w_star);
+    float pre = __shfl_up_sync(0xffffffffu, incl, 1);
+    pre = __shfl_sync(0xffffffffu, (lane == 0) ? 0.f : pre, w_star);
+    (void)excl;
+    if (lane == 0) {
+      sm_int[0] = w_star;
+      sm_int[1] = hit;
+      sm_flt[0] = pre;
+      sm_flt[1] = target;
+      sm_flt[2] = total;
+    }
+  }
+  __syncthreads();
+  zero_mass = !(sm_flt[2] > 0.f);
+  const int w_star = sm_int[0];
+  const bool hit = sm_int[1] != 0;
+  int result = -1;
+  if (wid == w_star) {
+    const int g_lo = min(w_star * seg, V), g_hi = min(g_lo + seg, V);
+    float run = sm_flt[0];
+    const float target = sm_flt[1];
+    int lastpos = -1;
+    for (int c = g_lo; c < g_hi && result < 0; c += 256) {
+      float q[8];
+      float ls = 0.f;
+      const int v0 = c + lane * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        q[e] = (v0 + e < g_hi) ? final_weight<T, MODE>(z, pd, v0 + e, invT, m, S) : 0.f;
+        ls += q[e];
+        if (q[e] > 0.f) lastpos = max(lastpos, v0 + e);
+      }
+      const float ctot = warp_sum(ls);
+      if (hit && run + ctot > target) {
+        const float incl = warp_inclusive_scan(ls);
+        const unsigned over = __ballot_sync(0xffffffffu, run + incl > target);
+        if (over) {
+          const int L = __ffs(over) - 1;
+          float pre = __shfl_up_sync(0xffffffffu, incl, 1);
+          pre = (lane == 0) ? 0.f : pre;
+          pre = __shfl_sync(0xffffffffu, pre, L);
+          int x = -1;
+          if (lane == L) {
+            float a = run + pre;
+            int lastp = -1;
+            for (int e = 0; e < 8; ++e) {
+              a += q[e];
+              if (q[e] > 0.f) lastp = v0 + e;
+              if (a > target) {
+                x = v0 + e;
+                break;
+              }
+            }
+            if (x < 0) x = lastp;
+          }
+          x = __shfl_sync(0xffffffffu, x, L);
+          if (x >= 0) result = x;
+        }
+      }
+      run += ctot;
+    }
+    // rounding left no crossing: last positive weight of the segment
+    for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
+    if (result < 0) result = lastpos;
+    if (lane == 0) sm_int[2] = result;
+  }
+  __syncthreads();
+  const int x = sm_int[2];
+  __syncthreads();
+  return x;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restrict__ target,
+                                                               const int32_t* __restrict__ offsets,
+                                                               const int32_t* __restrict__ ell,
+                                                               const int32_t* __restrict__ tokens,
+                                                               const float* __restrict__ pd_rows,
+                                                               const float* __restrict__ pd_tok,
+                                                               const float* __restrict__ temp,
+                                                               const uint32_t* __restrict__ req_id, uint64_t seed,
+                                                               int G, int V, const float4* __restrict__ rs,
+                                                               int32_t* __restrict__ n_accept,
+                                                               int32_t* __restrict__ out_tok,
+                                                               int32_t* __restrict__ n_out) {
+  __shared__ float sm_seg[32];
+  __shared__ int sm_int[4];
+  __shared__ float sm_flt[4];
+  __shared__ int s_m;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int L = ell[r];
+  const float T_ = temp[r];
+  const bool sampled = T_ > 0.f;
+  const uint32_t req = req_id[r];
+  const int base = offsets[r];
+  if (tid == 0) {
+    int m = 0;
+    for (int j = 1; j <= L; ++j) {
+      const float4 st = rs[base + j - 1];
+      const int x = tokens[(size_t)r * G + j - 1];
+      bool acc;
+      if (sampled) {
+        const float u = philox_uniform(seed, req, (uint32_t)j, 1u);
+        acc = __fmul_rn(u, pd_tok[(size_t)r * G + j - 1]) < st.w;
+      } else {
+        acc = x == __float_as_int(st.z);
+      }
+      if (!acc) break;
+      ++m;
+    }
+    s_m = m;
+  }
+  __syncthreads();
+  const int m = s_m;
+  for (int i = tid; i <= G; i += FIN_THREADS) out_tok[(size_t)r * (G + 1) + i] = (i < m) ? tokens[(size_t)r * G + i] : -1;
+  const float4 st = rs[base + m];
+  int x;
+  if (!sampled) {
+    x = __float_as_int(st.z);
+  } else {
+    const T* z = target + ((size_t)base + m) * V;
+    const float invT = inv_temp(T_);
+    bool zero_mass = false;
+    if (m < L) {
+      const float u = philox_uniform(seed, req, (uint32_t)(m + 1), 2u);
+      const float* pd = pd_rows + ((size_t)r * G + m) * V;
+      x = final_draw<T, 0>(z, pd, V, invT, st.x, st.y, u, sm_seg, sm_int, sm_flt, zero_mass);
+      if (zero_mass) x = final_draw<T, 1>(z, pd, V, invT, st.x, st.y, u, sm_seg, sm_int, sm_flt, zero_mass);
+    } else {
+      const float u = philox_uniform(seed, req, (uint32_t)(L + 1), 3u);
+      x = final_draw<T, 1>(z, nullptr, V, invT, st.x, st.y, u, sm_seg, sm_int, sm_flt, zero_mass);
+    }
+  }
+  if (tid == 0) {
+    out_tok[(size_t)r * (G + 1) + m] = x;
+    n_accept[r] = m;
+    n_out[r] = m + 1;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_verify_t(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  const int B = a.dims.B, G = a.dims.gamma, V = a.dims.V;
+  float4* rs = reinterpret_cast<float4*>(ws + L.vrs);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const T* tg = static_cast<const T*>(a.target_logits);
+  k_verify_rowstats<T><<<dim3(B, G + 1), RS_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.temp, G, V, rs, hdr);
+  k_verify_finish<T><<<B, FIN_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.pd_rows, a.pd_tok, a.temp,
+                                               a.req_id, a.seed, G, V, rs, a.n_accept, a.out_tok, a.n_out);
+  count_launches(2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  if (a.dims.dtype == DSPARK_BF16) return launch_verify_t<__nv_bfloat16>(a, ws, L, s);
+  return launch_verify_t<float>(a, ws, L, s);
+}
+
+}  // namespace dspark

@@ -1,0 +1,256 @@
+/*
+ * dspark.h — C ABI of the DSpark per-step hot path on one GPU (sm_103a).
+ *
+ * Three calls make one decode round's data-parallel work:
+ *   dspark_draft_sample  Markov-head draft sampler + confidence head
+ *   dspark_schedule      Sequential Temperature Scaling + hardware-aware prefix
+ *                        scheduler + flattened verify batch with marker tensor
+ *   dspark_verify        lossless rejection-sampling verification
+ *
+ * Sources (page titles; the section on each page is named at each call):
+ *   [DSpark]      "DSpark: Confidence-Scheduled Speculative Decoding with
+ *                 Semi-Autoregressive Generation" (papercache.org summary)
+ *   [MTP Survey]  "大模型推理 MTP 算法 Survey" (backyes.github.io)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer in an args struct is a DEVICE pointer unless its comment says
+ *   "host".  The caller owns every buffer; the library never allocates,
+ *   frees or keeps a pointer after the call returns.
+ * - Arrays are dense, row-major, with the shapes given in brackets.  Base
+ *   pointers of the large arrays (U, W1, W2, h, w, target_logits, pd_rows) must
+ *   be 16-byte aligned.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Calls only enqueue work on it and return; they never synchronise, except
+ *   dspark_read_error.
+ * - Argument errors return DSPARK_INVALID_ARG / DSPARK_UNSUPPORTED before any
+ *   work is enqueued.  A launch failure returns DSPARK_CUDA_ERROR.  Errors
+ *   found by a kernel while it runs (a token id outside [0, V), a bounded wait
+ *   that gave up) are written to the workspace error word and read back with
+ *   dspark_read_error.  Nothing aborts, exits or prints.
+ * - Inputs are read-only.  No state survives a call except the workspace error
+ *   word.  Random draws use Philox4x32-10 (Salmon et al., SC'11) with
+ *   key = (seed mod 2^32, seed >> 32) and counter = (req_id, position, draw, 0),
+ *   u = (out0 >> 8) * 2^-24; draw 0 = draft sample, 1 = accept test,
+ *   2 = residual, 3 = bonus.  Results therefore depend on (seed, req_id,
+ *   position) only, not on a request's slot in the batch.
+ * - Temperature T_r per request: T_r > 0 samples from softmax(logits / T_r);
+ *   anything else (0, negative, NaN) is greedy: argmax with ties to the lowest
+ *   token id.  Logits must be finite.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer      */
+  DSPARK_UNSUPPORTED = 2,   /* size beyond a limit, unknown dtype, no sm_103a  */
+  DSPARK_CUDA_ERROR = 3,    /* a CUDA call or launch failed                     */
+  DSPARK_TIMEOUT = 4,       /* a kernel's bounded wait gave up (error word)     */
+  DSPARK_BAD_INPUT = 5      /* a kernel met an out-of-range token id (error word) */
+} dspark_status;
+
+typedef enum { DSPARK_BF16 = 0, DSPARK_F32 = 1 } dspark_dtype;
+
+typedef enum {
+  DSPARK_SCHED_OFF = 0,     /* verify every draft token: l_r = gamma            */
+  DSPARK_SCHED_GREEDY = 1   /* Algorithm 1 with the early stop                  */
+} dspark_sched_mode;
+
+/* Limits checked by every call. */
+#define DSPARK_MAX_GAMMA 32
+#define DSPARK_MAX_RANK 1024
+#define DSPARK_MAX_SCHED_KEYS 65536 /* B * gamma for dspark_schedule */
+
+/* Problem sizes.  dtype applies to U, W1, W2, h, w and target_logits; every
+ * output probability / confidence is fp32. */
+typedef struct {
+  int32_t B;      /* requests in the batch, >= 0 (0 = nothing to do)        */
+  int32_t gamma;  /* draft block size, 1..DSPARK_MAX_GAMMA                   */
+  int32_t V;      /* vocabulary size, >= 1                                   */
+  int32_t r;      /* Markov rank, 0..DSPARK_MAX_RANK (0 = no head, DFlash)    */
+  int32_t H;      /* backbone hidden size, >= 0                              */
+  int32_t dtype;  /* dspark_dtype                                            */
+} dspark_dims;
+
+/* ---------------------------------------------------------------------------
+ * Workspace
+ * ---------------------------------------------------------------------------
+ * dspark_workspace_size: bytes of device scratch one set of dims needs for all
+ * three calls (they use disjoint regions, so the three calls may share one
+ * workspace while they run in order on one stream).  The caller allocates it
+ * (any 256-byte-aligned device buffer) and must call dspark_workspace_init
+ * once before first use.  Returns DSPARK_INVALID_ARG for a null pointer or
+ * invalid dims. */
+DSPARK_API dspark_status dspark_workspace_size(const dspark_dims* dims, size_t* bytes);
+
+/* dspark_workspace_init: clears the workspace error word (enqueued on stream). */
+DSPARK_API dspark_status dspark_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* dspark_read_error: synchronises `stream`, copies the workspace error word to
+ * *code_host (0 = none, else a dspark_status value) and *detail_host (the
+ * offending value, e.g. the bad token id; may be NULL), then clears the word.
+ * Returns DSPARK_CUDA_ERROR if the copy fails. */
+DSPARK_API dspark_status dspark_read_error(void* workspace, int32_t* code_host, int32_t* detail_host, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_draft_sample
+ * ---------------------------------------------------------------------------
+ * [DSpark] 方法细节, "序列阶段的依赖注入" and "马尔可夫头（Markov head）的实现":
+ * for k = 1..gamma, left to right,
+ *     l_k(v)  = U_k(v) + W1[x_{k-1}] . W2[:, v]          (x_0 = anchor)
+ *     p_d^k   = softmax(l_k / T_r)                          (one-hot if greedy)
+ *     x_k     = inverse-CDF draw from p_d^k in token-id order, u from draw 0
+ *               at position k (greedy: argmax of l_k)
+ * [DSpark] 方法细节, "置信度头的设计":
+ *     z_k = w_h . h_k + w_e . W1[x_{k-1}],  c_k = sigmoid(z_k),  w = [w_h; w_e].
+ * [DSpark] 方法细节, "并行阶段的局限与设计": the anchor is the first predicted
+ * position, so U has gamma rows per request.
+ * Inputs  U [B, gamma, V], W1 [V, r], W2 [r, V], h [B, gamma, H], w [H + r]
+ *         (all dims.dtype); anchor [B] i32 in [0, V); temp [B] f32;
+ *         req_id [B] u32; seed.  W1/W2 may be NULL when r = 0; h/w may be
+ *         NULL when H + r = 0.
+ * Outputs tokens [B, gamma] i32; pd_rows [B, gamma, V] f32 (the exact
+ *         probability row each token was drawn from); pd_tok [B, gamma] f32
+ *         (= pd_rows at the drawn token, bit for bit); conf_logit and conf
+ *         [B, gamma] f32.
+ * An anchor outside [0, V) is replaced by 0 and reported as DSPARK_BAD_INPUT
+ * through the error word. */
+typedef struct {
+  dspark_dims dims;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const void* h;
+  const void* w;
+  const int32_t* anchor;
+  const float* temp;
+  const uint32_t* req_id;
+  uint64_t seed;
+  int32_t* tokens;
+  float* pd_rows;
+  float* pd_tok;
+  float* conf_logit;
+  float* conf;
+} dspark_draft_args;
+
+DSPARK_API dspark_status dspark_draft_sample(const dspark_draft_args* args, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_schedule
+ * ---------------------------------------------------------------------------
+ * [DSpark] 方法细节, "事后校准（Post-hoc Calibration）": per-position temperature
+ * scaling of the confidence, read as c'_{r,k} = sigmoid(z_{r,k} / tau_k); this
+ * library evaluates the sigmoid in fp64 and rounds it to fp32.
+ * [DSpark] 方法细节, "硬件感知前缀调度器" / "贪心求解与因果性保证", Algorithm 1:
+ *     a_{r,j} = c'_{r,1} ... c'_{r,j}   (fp32, left to right)
+ *     E = {(r, j): a_{r,j} > 0} sorted by a descending (ties: r, then j asc.)
+ *     Theta_0 = B SPS[B];  Theta_i = (B + a_(1) + ... + a_(i)) SPS[B + i]  (fp64)
+ *     admit while Theta_i > Theta_{i-1}; stop at the first Theta_i <= Theta_{i-1}
+ *     l_r = number of admitted (r, .) candidates
+ * [DSpark] 补充细节, "高吞吐量与低延迟推理": the kept prefixes are flattened
+ * into one batch with a marker tensor.  Layout (this library's reading):
+ * request-major, position ascending; row offsets[r] + j holds the anchor for
+ * j = 0 and draft token x_j for j = 1..l_r; mark_req/mark_pos give (r, j).
+ * Inputs  conf_logit [B, gamma] f32 (z from dspark_draft_sample); sts_temp
+ *         [gamma] f32 (> 0); sps [B (1 + gamma) + 1] f64 engine steps/s indexed
+ *         by total verify tokens (may be NULL when mode = OFF); anchor [B];
+ *         tokens [B, gamma]; mode.
+ * Outputs ell [B]; offsets [B + 1]; flat_tok, mark_req, mark_pos
+ *         [B (1 + gamma)] (rows past N_v = offsets[B] are set to -1);
+ *         n_verify [1] (= N_v); theta_best [1] f64 (Theta of the kept set;
+ *         0 when mode = OFF); optional n_verify_host (pinned HOST i32, written
+ *         by a stream-ordered copy) and surv [B, gamma] f32 (the a_{r,j}).
+ * B * gamma must not exceed DSPARK_MAX_SCHED_KEYS. */
+typedef struct {
+  int32_t B;
+  int32_t gamma;
+  int32_t mode;
+  const float* conf_logit;
+  const float* sts_temp;
+  const double* sps;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  int32_t* ell;
+  int32_t* offsets;
+  int32_t* flat_tok;
+  int32_t* mark_req;
+  int32_t* mark_pos;
+  int32_t* n_verify;
+  int32_t* n_verify_host;
+  double* theta_best;
+  float* surv;
+} dspark_sched_args;
+
+DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * dspark_verify
+ * ---------------------------------------------------------------------------
+ * [DSpark] 背景知识与设计原则, "投机解码的延迟建模": x_k is accepted with
+ * probability min(1, p_t^k(x_k) / p_d^k(x_k)), left to right; the first
+ * rejection discards the rest.  Implemented as u p_d(x_k) < p_t(x_k) with u
+ * from draw 1 at position k.
+ * [MTP Survey] §2.2 "拒绝采样": at the first rejection a correction is drawn
+ * from norm(max(0, p_t^k - p_d^k)) (draw 2 at position k; if that mass is 0 in
+ * fp32, from p_t^k); when all l_r tokens are accepted the bonus is drawn from
+ * p_t^{l+1} (draw 3 at position l + 1); greedy requests accept iff
+ * x_k = argmax p_t^k and emit that argmax as the correction or bonus.
+ * p_t^j = softmax(target_logits[offsets[r] + j - 1] / T_r).
+ * Inputs  target_logits [>= offsets[B], V] (dims.dtype), the flattened rows of
+ *         dspark_schedule's layout; offsets [B + 1]; ell [B]; tokens [B, gamma];
+ *         pd_rows [B, gamma, V]; pd_tok [B, gamma]; temp [B]; req_id [B]; seed.
+ * Outputs n_accept [B]; out_tok [B, gamma + 1] (the accepted tokens, then the
+ *         correction or bonus, then -1); n_out [B] = n_accept + 1.
+ * Only dims.B, gamma, V and dtype are read. */
+typedef struct {
+  dspark_dims dims;
+  const void* target_logits;
+  const int32_t* offsets;
+  const int32_t* ell;
+  const int32_t* tokens;
+  const float* pd_rows;
+  const float* pd_tok;
+  const float* temp;
+  const uint32_t* req_id;
+  uint64_t seed;
+  int32_t* n_accept;
+  int32_t* out_tok;
+  int32_t* n_out;
+} dspark_verify_args;
+
+DSPARK_API dspark_status dspark_verify(const dspark_verify_args* args, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Number of CUDA kernels this library has enqueued since it was loaded (a
+ * host-side counter, incremented at launch time; a captured CUDA graph counts
+ * its kernels once, at capture).  For accounting only: no library behaviour
+ * depends on it. */
+DSPARK_API uint64_t dspark_launch_count(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+DSPARK_API const char* dspark_status_string(dspark_status s);
+
+/* Library build identification (static string). */
+DSPARK_API const char* dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every declared symbol; argument
+checks that return before any CUDA call (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from draft_sampling_lossless_markov_gb300 import build, capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return capi.load()
+
+
+def _declared():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            names |= set(re.findall(r"DSPARK_API\s+[\w\s\*]+?\b(dspark_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert {"dspark_draft_sample", "dspark_schedule", "dspark_verify"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(capi.EXPORTED) <= declared
+
+
+def test_status_strings_and_version(lib):
+    assert capi.dspark_status_string(capi.DSPARK_OK) == "DSPARK_OK"
+    assert capi.dspark_status_string(capi.DSPARK_TIMEOUT) == "DSPARK_TIMEOUT"
+    assert capi.dspark_status_string(99) == "DSPARK_UNKNOWN_STATUS"
+    assert "sm_103a" in capi.dspark_version()
+
+
+def test_workspace_size(lib):
+    st, n = capi.dspark_workspace_size(capi.dspark_dims(256, 7, 151936, 256, 4096, capi.DSPARK_BF16))
+    assert st == capi.DSPARK_OK and n > 0 and n % 256 == 0
+    st2, n2 = capi.dspark_workspace_size(capi.dspark_dims(256, 7, 151936, 0, 0, capi.DSPARK_BF16))
+    assert st2 == capi.DSPARK_OK and n2 < n
+    for bad in (capi.dspark_dims(4, 0, 10, 1, 1, 0), capi.dspark_dims(4, 33, 10, 1, 1, 0),
+                capi.dspark_dims(-1, 4, 10, 1, 1, 0), capi.dspark_dims(4, 4, 0, 1, 1, 0),
+                capi.dspark_dims(4, 4, 10, 1025, 1, 0), capi.dspark_dims(4, 4, 10, 1, 1, 7)):
+        assert capi.dspark_workspace_size(bad)[0] == capi.DSPARK_INVALID_ARG
+    assert lib.dspark_workspace_size(None, None) == capi.DSPARK_INVALID_ARG
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    d = capi.dspark_draft_args()
+    d.dims = capi.dspark_dims(4, 4, 64, 8, 16, capi.DSPARK_F32)
+    # null inputs
+    assert capi.dspark_draft_sample(d, 0, 0, 0) == capi.DSPARK_INVALID_ARG
+    assert lib.dspark_draft_sample(None, None, 0, None) == capi.DSPARK_INVALID_ARG
+    # empty batch: nothing to do, no CUDA call
+    d.dims = capi.dspark_dims(0, 4, 64, 8, 16, capi.DSPARK_F32)
+    assert capi.dspark_draft_sample(d, 0, 0, 0) == capi.DSPARK_OK
+    # misaligned input pointer (checked before the workspace)
+    d.dims = capi.dspark_dims(4, 4, 64, 8, 16, capi.DSPARK_F32)
+    for f in ("U", "W1", "W2", "h", "w", "anchor", "temp", "req_id", "tokens", "pd_rows", "pd_tok", "conf_logit",
+              "conf"):
+        setattr(d, f, 0x10000)
+    d.U = 0x10004
+    assert capi.dspark_draft_sample(d, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
+    # workspace too small / misaligned
+    d.U = 0x10000
+    assert capi.dspark_draft_sample(d, 0x20000, 16, 0) == capi.DSPARK_INVALID_ARG
+    assert capi.dspark_draft_sample(d, 0x20010, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
+
+    s = capi.dspark_sched_args()
+    s.B, s.gamma, s.mode = 4096, 17, capi.DSPARK_SCHED_GREEDY
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_UNSUPPORTED  # B * gamma > 65536
+    s.B, s.gamma = 4, 33
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_INVALID_ARG
+    s.gamma, s.mode = 4, 5
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_INVALID_ARG
+    s.mode = capi.DSPARK_SCHED_GREEDY
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_INVALID_ARG  # null pointers
+    s.B = 0
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_OK
+
+    v = capi.dspark_verify_args()
+    v.dims = capi.dspark_dims(4, 4, 64, 0, 0, capi.DSPARK_BF16)
+    assert capi.dspark_verify(v, 0, 0, 0) == capi.DSPARK_INVALID_ARG
+    v.dims = capi.dspark_dims(0, 4, 64, 0, 0, capi.DSPARK_BF16)
+    assert capi.dspark_verify(v, 0, 0, 0) == capi.DSPARK_OK
+
+
+def test_struct_layouts_match_header(lib):
+    # field order and sizes of the ctypes mirrors (64-bit ABI)
+    assert ctypes.sizeof(capi.dspark_dims) == 24
+    assert capi.dspark_draft_args.seed.offset == 24 + 8 * 8
+    assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8
+    assert ctypes.sizeof(capi.dspark_sched_args) == 16 + 14 * 8
+    assert capi.dspark_verify_args.seed.offset == 24 + 8 * 8

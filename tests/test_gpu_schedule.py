@@ -1,0 +1,144 @@
+"""GPU parity of dspark_schedule against the oracle (bit-exact integer outputs)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import schedule as S
+from parity import compare_schedule
+from gpu_common import check_no_error, require_gpu, to_dev_f32, to_dev_i32, workspace_for
+from draft_sampling_lossless_markov_gb300 import torch_api as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _run(z, tau, sps, anchor, tokens, mode):
+    B, G = z.shape
+    ws = workspace_for(B, G, 1, 0, 0, torch.float32)
+    host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    out = T.schedule(ws, to_dev_f32(z), to_dev_f32(tau), sps, to_dev_i32(anchor), to_dev_i32(tokens), mode,
+                     n_verify_host=host, want_surv=True)
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out.items() if isinstance(v, torch.Tensor) and k != "_sps"}
+    g["n_verify_host"] = int(host[0])
+    check_no_error(ws)
+    return g
+
+
+def _oracle(z, tau, sps, anchor, tokens, mode):
+    return S.schedule(z, tau, sps, anchor, tokens, mode=mode)
+
+
+def _case(seed, B, G, sps_kind="exp2048", z_scale=2.5, z_shift=0.5, tau=None):
+    rng = np.random.default_rng(seed)
+    z = synth.random_conf_logits(B, G, seed, scale=z_scale, shift=z_shift)
+    if tau is None:
+        tau = np.ones(G, np.float32)
+    sps = synth.sps_table(sps_kind, B, G) if sps_kind in ("tiny", "exp2048") else sps_kind
+    anchor = rng.integers(0, 1000, B).astype(np.int32)
+    tokens = synth.random_tokens(B, G, 1000, seed + 1)
+    return z, np.asarray(tau, np.float32), sps, anchor, tokens
+
+
+def _check(z, tau, sps, anchor, tokens, mode):
+    g = _run(z, tau, sps, anchor, tokens, mode)
+    o = _oracle(z, tau, sps, anchor, tokens, mode)
+    np.testing.assert_array_equal(g["surv"], o["a"])  # fp32 survival products, bit for bit
+    compared = compare_schedule(g, o)
+    assert g["n_verify_host"] == int(o["offsets"][-1]) or not compared
+    return compared, g, o
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_schedule_random_small(seed):
+    rng = np.random.default_rng(100 + seed)
+    B, G = int(rng.integers(1, 40)), int(rng.integers(1, 9))
+    tau = rng.uniform(0.8, 1.5, G).astype(np.float32)
+    kind = ["tiny", "exp2048"][seed % 2]
+    n = np.arange(B * (1 + G) + 1, dtype=np.float64)
+    if seed % 3 == 2:  # stepped cost table with cliffs
+        kind = 100.0 / (1.0 + np.floor(n / 3) * 0.05)
+    z = synth.random_conf_logits(B, G, seed)
+    sps = synth.sps_table(kind, B, G) if isinstance(kind, str) else kind
+    compared, g, o = _check(z, tau, sps, rng.integers(0, 1000, B), synth.random_tokens(B, G, 1000, seed), 1)
+    assert compared
+
+
+@pytest.mark.parametrize("B,G", [(256, 15), (256, 7), (1024, 7), (4096, 16), (65536, 1)])
+def test_schedule_workload_sizes(B, G):
+    # up to the 65536-candidate limit; config-2 STS temperatures and SPS curve
+    rng = np.random.default_rng(B + G)
+    tau = rng.uniform(0.8, 1.5, G).astype(np.float32)
+    z, _, sps, anchor, tokens = _case(B * 7 + G, B, G)
+    compared, g, o = _check(z, tau, sps, anchor, tokens, 1)
+    assert compared
+    assert 0 <= g["ell"].min() and g["ell"].max() <= G
+
+
+def test_schedule_off_mode():
+    z, tau, sps, anchor, tokens = _case(3, 50, 6)
+    compared, g, o = _check(z, tau, None, anchor, tokens, 0)
+    assert compared and np.all(g["ell"] == 6) and g["n_verify"][0] == 50 * 7
+
+
+def test_schedule_all_survival_zero():
+    z, tau, sps, anchor, tokens = _case(4, 20, 5)
+    z[:] = -1.0e4  # sigmoid underflows: c' = 0, no candidate
+    compared, g, o = _check(z, tau, sps, anchor, tokens, 1)
+    assert compared and np.all(g["ell"] == 0) and g["n_verify"][0] == 20
+
+
+def test_schedule_always_improving_admits_everything():
+    B, G = 30, 4
+    z, tau, _, anchor, tokens = _case(5, B, G)
+    sps = np.ones(B * (1 + G) + 1)  # flat cost: every candidate with a > 0 raises Theta
+    compared, g, o = _check(z, tau, sps, anchor, tokens, 1)
+    assert compared and np.all(g["ell"] == G)
+
+
+def test_schedule_ties_break_by_request_then_position():
+    B, G = 64, 4
+    z = np.full((B, G), 1.25, np.float32)  # every request identical
+    tau = np.ones(G, np.float32)
+    sps = synth.sps_table("exp2048", B, G) * 0 + 100.0 / (1.0 + np.arange(B * (1 + G) + 1) / 40.0)
+    anchor = np.arange(B, dtype=np.int32)
+    tokens = synth.random_tokens(B, G, 50, 3)
+    compared, g, o = _check(z, tau, sps, anchor, tokens, 1)
+    assert compared
+    # lengths differ by at most one and longer requests come first
+    assert g["ell"].max() - g["ell"].min() <= 1
+    assert np.all(np.diff(g["ell"]) <= 0)
+
+
+def test_schedule_appendix_a_on_gpu():
+    # [DSpark] 附录 (Appendix A): R = 1, a1 = 0.8, SPS(1..3) = 1.0, 0.5, 0.45 -> l = 0
+    golden = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "appendix_a_counterexample.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            golden[k] = float(v)
+    z1 = np.float32(np.log(golden["a1"] / (1 - golden["a1"])))
+    for c2 in (golden["c2_high"], 0.5):
+        z2 = np.float32(np.log(c2 / (1 - c2)))
+        z = np.array([[z1, z2]], np.float32)
+        sps = np.array([0.0, golden["sps1"], golden["sps2"], golden["sps3"]])
+        compared, g, o = _check(z, np.ones(2, np.float32), sps, np.array([1]), np.array([[2, 3]]), 1)
+        assert compared
+        assert g["ell"][0] == golden["early_stop_ell"]
+        assert g["theta_best"][0] == pytest.approx(golden["theta0"], rel=1e-6)
+
+
+def test_schedule_empty_batch_is_a_no_op():
+    ws = workspace_for(1, 2, 1, 0, 0, torch.float32)
+    from draft_sampling_lossless_markov_gb300 import capi
+    a = capi.dspark_sched_args()
+    a.B, a.gamma, a.mode = 0, 2, 1
+    assert capi.dspark_schedule(a, ws.ptr, ws.nbytes, 0) == capi.DSPARK_OK
