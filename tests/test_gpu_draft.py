@@ -90,7 +90,7 @@ def test_draft_full_size_sampled_requests(name, subset):
     s = out["pd_rows"].sum(dim=2)
     assert float((s - 1).abs().max()) < 5e-4
     c = out["conf"]
-    assert float(c.min()) > 0 and float(c.max()) < 1
+    assert float(c.min()) >= 0 and float(c.max()) <= 1  # fp32 sigmoid saturates to 1 for z > ~17
     check_no_error(ws)
 
 

@@ -51,7 +51,7 @@ def _check(z, tau, sps, anchor, tokens, mode):
     g = _run(z, tau, sps, anchor, tokens, mode)
     o = _oracle(z, tau, sps, anchor, tokens, mode)
     np.testing.assert_array_equal(g["surv"], o["a"])  # fp32 survival products, bit for bit
-    compared = compare_schedule(g, o)
+    compared = compare_schedule(g, o, surv_equal=True)
     assert g["n_verify_host"] == int(o["offsets"][-1]) or not compared
     return compared, g, o
 
