@@ -31,7 +31,8 @@ DSPARK_MAX_RANK = 1024
 DSPARK_MAX_SCHED_KEYS = 65536
 
 EXPORTED = ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
-            "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count")
+            "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count",
+            "dspark_schedule_noalloc")
 
 
 class dspark_dims(ctypes.Structure):
@@ -79,8 +80,9 @@ def load() -> ctypes.CDLL:
     lib.dspark_draft_sample.argtypes = [POINTER(dspark_draft_args), c_void_p, c_size_t, c_void_p]
     lib.dspark_schedule.argtypes = [POINTER(dspark_sched_args), c_void_p, c_size_t, c_void_p]
     lib.dspark_verify.argtypes = [POINTER(dspark_verify_args), c_void_p, c_size_t, c_void_p]
+    lib.dspark_schedule_noalloc.argtypes = [POINTER(dspark_sched_args), c_void_p]
     for f in ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
-              "dspark_schedule", "dspark_verify"):
+              "dspark_schedule", "dspark_verify", "dspark_schedule_noalloc"):
         getattr(lib, f).restype = c_int32
     lib.dspark_status_string.argtypes = [c_int32]
     lib.dspark_status_string.restype = c_char_p
@@ -126,6 +128,12 @@ def dspark_draft_sample(args: dspark_draft_args, workspace: int, nbytes: int, st
 
 def dspark_schedule(args: dspark_sched_args, workspace: int, nbytes: int, stream: int) -> int:
     return load().dspark_schedule(ctypes.byref(args), c_void_p(workspace), nbytes, c_void_p(stream))
+
+
+def dspark_schedule_noalloc(args: dspark_sched_args, stream: int) -> int:
+    """dspark_schedule without a workspace: scratch in a fixed 1 MiB array inside
+    the library, for callers that cannot allocate device memory."""
+    return load().dspark_schedule_noalloc(ctypes.byref(args), c_void_p(stream))
 
 
 def dspark_verify(args: dspark_verify_args, workspace: int, nbytes: int, stream: int) -> int:

@@ -200,6 +200,38 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
                               size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dspark_schedule_noalloc
+ * ---------------------------------------------------------------------------
+ * The pages have no counterpart to this entry point: it is a library
+ * convenience.  It computes exactly what dspark_schedule computes (same kernel,
+ * same outputs, bit for bit) without a caller-provided workspace, for callers
+ * that cannot allocate device memory.  Two kinds of caller are meant: code
+ * embedded in a host process whose device memory is entirely owned by that
+ * host's own pool allocator (a plug-in of a serving engine that reserves the
+ * HBM for its KV cache up front, so an extension has no allocator and no
+ * budget of its own to draw a workspace from), and latency-critical decode
+ * loops that must not call cudaMalloc / cudaFree because those calls can
+ * synchronise the device and stall the loop.
+ *
+ * Scratch: a fixed 1 MiB array compiled into the library (4 x 65536 32-bit
+ * entries).  Every GPU on which the library's device code is loaded holds its
+ * own copy until the process exits.  This call performs no cudaMalloc,
+ * cudaFree or other allocating call.
+ * Limit: B * gamma <= DSPARK_MAX_SCHED_KEYS (65536); larger batches return
+ * DSPARK_UNSUPPORTED before anything is enqueued.  Other argument errors are
+ * those of dspark_schedule.
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address once (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture begins.
+ * Sharing: every call on a device uses the same array, which keeps whatever
+ * the last call left in it.  The kernel overwrites every entry it reads, so
+ * nothing needs clearing between calls, but two calls whose kernels overlap on
+ * the same GPU (for instance on two streams without an ordering between them)
+ * race on the array and give undefined results: order them on one stream or
+ * with events. */
+DSPARK_API dspark_status dspark_schedule_noalloc(const dspark_sched_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_verify
  * ---------------------------------------------------------------------------
  * [DSpark] 背景知识与设计原则, "投机解码的延迟建模": x_k is accepted with
