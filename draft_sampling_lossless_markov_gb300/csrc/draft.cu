@@ -13,8 +13,11 @@
 // The logits are recomputed rather than stored: storing them would cost a
 // 4-byte write plus a 4-byte read per element, recomputing costs a 2-byte
 // re-read of U (W2 stays in L2).  Every kernel evaluates l, l/T and exp(l/T - m)
-// with the same operations in the same order, so the recomputed tile in
-// k_select and the written row are bit-identical to pass 1's values.
+// with the same helper functions, so the two logits passes of a path produce
+// bit-identical values.  On the CUDA-core path the one tile k_select recomputes
+// is bit-identical too (same FMA chain); on the tensor-core path (draft_tc.cu)
+// k_select's CUDA-core recompute of that tile differs from the tensor-core sum
+// only by fp32 rounding order (relative 1e-7), far inside the sampling margin.
 #include <float.h>
 
 #include "common.cuh"
@@ -360,10 +363,6 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
 // ---------------------------------------------------------------------------
 // Host launcher
 // ---------------------------------------------------------------------------
-bool draft_tc_supported(const dspark_dims& d);
-cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, int k, bool write,
-                                 cudaStream_t s);
-
 template <typename T>
 static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const dspark_dims& d = a.dims;
@@ -384,7 +383,12 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   count_launches(1 + 4 * G);
 
   const bool tc = draft_tc_supported(d);
-  const int tw = tc ? 128 : CC_TW;
+  const int tw = tc ? draft_tc_tile_width() : CC_TW;
+  TcMaps maps;
+  if (tc) {
+    const cudaError_t e = draft_tc_prepare(a, ws, L, &maps);
+    if (e != cudaSuccess) return e;
+  }
   const int ntiles = (V + tw - 1) / tw;
   const size_t es_bytes = (size_t)CC_ROWS * r * sizeof(float);
   if (!tc && es_bytes > 48 * 1024) {
@@ -398,7 +402,7 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     k_embed<T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, k, W1, w, zh, E, a.conf_logit, a.conf, B, G, V, r,
                                              H, hdr);
     if (tc) {
-      cudaError_t e = launch_draft_tc_pass(a, ws, L, k, false, s);
+      cudaError_t e = launch_draft_tc_pass(a, ws, L, maps, k, false, s);
       if (e != cudaSuccess) return e;
     } else {
       k_logits_cc<T, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, E, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
@@ -407,7 +411,7 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     k_select<T><<<B, SEL_THREADS, (size_t)r * sizeof(float), s>>>(part, ntiles, tw, U, E, W2, a.temp, a.req_id,
                                                                    a.seed, B, G, V, r, k, a.tokens, rowstat);
     if (tc) {
-      cudaError_t e = launch_draft_tc_pass(a, ws, L, k, true, s);
+      cudaError_t e = launch_draft_tc_pass(a, ws, L, maps, k, true, s);
       if (e != cudaSuccess) return e;
     } else {
       k_logits_cc<T, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, E, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,

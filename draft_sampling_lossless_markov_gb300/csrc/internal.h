@@ -1,6 +1,7 @@
 // Host-side internals shared by the dspark translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,9 +11,9 @@
 namespace dspark {
 
 // Vocabulary columns summarised by one (max, sum-exp, argmax) partial of the
-// draft sampler.  The CUDA-core path uses 256, the tensor-core path 128; the
+// draft sampler.  The CUDA-core path uses 256, the tensor-core path 64; the
 // workspace is sized for the smaller width.
-constexpr int kPartialTileMin = 128;
+constexpr int kPartialTileMin = 64;
 
 struct WsLayout {
   size_t zh = 0;       // [B*G] f32: w_h . h_k
@@ -34,5 +35,15 @@ size_t elem_size(int dtype);
 cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+
+// Tensor-core logits passes of the draft sampler (draft_tc.cu).
+struct TcMaps {
+  CUtensorMap U, W2, E, Pd;
+};
+bool draft_tc_supported(const dspark_dims& d);
+int draft_tc_tile_width();
+cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, TcMaps* maps);
+cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, const TcMaps& maps,
+                                 int k, bool write, cudaStream_t s);
 
 }  // namespace dspark
