@@ -130,7 +130,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     argmax_merge(v, i, v2, i2);
   }
 }
-// (max, sum-exp) pairs: (m1, s1) + (m2, s2) relative to the larger max
+// (max, sum) pairs of base-2 exponentials: (m1, s1) + (m2, s2) relative to the larger max
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) {
@@ -139,10 +139,10 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
     return;
   }
   if (m2 > m) {
-    s = s * expf(m - m2) + s2;
+    s = s * exp2f(m - m2) + s2;
     m = m2;
   } else {
-    s = s + s2 * expf(m2 - m);
+    s = s + s2 * exp2f(m2 - m);
   }
 }
 __device__ __forceinline__ void warp_lse(float& m, float& s) {

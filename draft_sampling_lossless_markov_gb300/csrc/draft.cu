@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, co
   if (tid < CC_ROWS) {
     const float T_ = (tid < nrows) ? temp[b0 + tid] : 1.f;
     row_sampled[tid] = T_ > 0.f;
-    row_invT[tid] = inv_temp(T_);
+    row_invT[tid] = row_scale(T_);
   }
   __syncthreads();
 
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, co
       float p;
       if (row_sampled[i]) {
         const float2 st = rowstat[b];
-        p = prob_from(scale_logit(l[i], row_invT[i]), st.x, st.y);
+        p = prob_from(scale_logit(l[i], row_invT[i]), st.x, inv_sum(st.y));
       } else {
         p = (col == x) ? 1.f : 0.f;
       }
@@ -331,12 +331,22 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
   const float base = s_flt[1];
 
   // recompute the tile's columns (tw <= SEL_THREADS) with the pass-1 arithmetic
-  const float invT = inv_temp(T_);
+  const float invT = row_scale(T_);
   const int col = tstar * tw + tid;
   float wv = 0.f;
   if (tid < tw && col < V) {
+    // the same sequential FMA chain as the CUDA-core logits pass; loads are
+    // issued eight at a time so that they overlap
     float acc = 0.f;
-    for (int kk = 0; kk < r; ++kk) acc = fmaf(Erow[kk], ldf(W2 + (size_t)kk * V + col), acc);
+    int kk = 0;
+    for (; kk + 8 <= r; kk += 8) {
+      float wv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wv[e] = ldf(W2 + (size_t)(kk + e) * V + col);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(Erow[kk + e], wv[e], acc);
+    }
+    for (; kk < r; ++kk) acc = fmaf(Erow[kk], ldf(W2 + (size_t)kk * V + col), acc);
     const float l = add_base(ldf(U + ((size_t)b * G + k) * V + col), acc);
     wv = exp_shifted(scale_logit(l, invT), m);
   }

@@ -1,24 +1,34 @@
-// The arithmetic of one draft probability, written once so that every kernel
-// that evaluates it (logits passes, tile recompute, p_d write) rounds the same
-// way.  Explicit _rn intrinsics keep the compiler from contracting a multiply
-// and an add into an FMA differently in different kernels.
+// The arithmetic of one probability, written once so that every kernel that
+// evaluates it (draft logits passes, tile recompute, p_d write, verify row
+// statistics, residual) rounds the same way.  Explicit _rn intrinsics keep the
+// compiler from contracting a multiply and an add into an FMA differently in
+// different kernels.
+//
+// softmax(l / T) is evaluated in base 2: with c = log2(e) / T,
+//     y = l * c,   m = max y,   w = 2^(y - m),   S = sum w,   p = w * (1 / S)
+// which equals exp(l/T - max l/T) / sum exp(...) up to fp32 rounding.
 #pragma once
 
 #include <cuda_runtime.h>
 
 namespace dspark {
 
-// 1/T for sampled rows (T > 0); greedy rows never use it
-__device__ __forceinline__ float inv_temp(float T) { return T > 0.f ? __frcp_rn(T) : 1.f; }
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+
+// c = log2(e) / T for sampled rows (T > 0); 1 for greedy rows, whose argmax is
+// then taken on the logits themselves (a scale could merge two distinct logits)
+__device__ __forceinline__ float row_scale(float T) { return T > 0.f ? __fmul_rn(__frcp_rn(T), kLog2e) : 1.f; }
 // l = U + bias
 __device__ __forceinline__ float add_base(float u, float bias) { return __fadd_rn(u, bias); }
-// y = l / T
-__device__ __forceinline__ float scale_logit(float l, float invT) { return __fmul_rn(l, invT); }
-// exp(y - m)
-__device__ __forceinline__ float exp_shifted(float y, float m) { return expf(__fsub_rn(y, m)); }
+// y = l * c
+__device__ __forceinline__ float scale_logit(float l, float c) { return __fmul_rn(l, c); }
+// 2^(y - m)
+__device__ __forceinline__ float exp_shifted(float y, float m) { return exp2f(__fsub_rn(y, m)); }
 // mass of a tile with partial (m_t, s_t) relative to the row max m
-__device__ __forceinline__ float tile_mass(float mt, float st, float m) { return __fmul_rn(st, expf(__fsub_rn(mt, m))); }
-// p = exp(y - m) / S
-__device__ __forceinline__ float prob_from(float y, float m, float S) { return __fdiv_rn(exp_shifted(y, m), S); }
+__device__ __forceinline__ float tile_mass(float mt, float st, float m) { return __fmul_rn(st, exp2f(__fsub_rn(mt, m))); }
+// 1 / S
+__device__ __forceinline__ float inv_sum(float S) { return __frcp_rn(S); }
+// p = 2^(y - m) / S, as 2^(y - m) * (1 / S)
+__device__ __forceinline__ float prob_from(float y, float m, float invS) { return __fmul_rn(exp_shifted(y, m), invS); }
 
 }  // namespace dspark

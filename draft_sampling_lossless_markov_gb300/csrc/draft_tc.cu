@@ -13,10 +13,12 @@
 //   warp 1    allocates TMEM, issues tcgen05.mma (A = E, K-major, resident for
 //             the whole CTA; B = W2 tile, MN-major) into one of two 64-column
 //             fp32 accumulators, commits to mbarriers
-//   warps 2-5 epilogue, one request row per thread: TMEM -> registers, + U,
-//             then either the tile's (max, sum-exp, argmax) partial (pass 1) or
-//             the probability row p_d = exp(l/T - m) / S written through a
-//             per-warp swizzled staging buffer with TMA stores (pass 2)
+//   warps 2-9 epilogue, two groups of four warps (one per TMEM lane quarter)
+//             that take alternate tiles, each with its own accumulator: one
+//             request row per thread, TMEM -> registers, + U, then either the
+//             tile's (max, sum, argmax) partial (pass 1) or the probability
+//             row p_d = 2^(y - m) / S written through a per-warp swizzled
+//             staging buffer with TMA stores (pass 2)
 //
 // A CTA owns one 128-row M-tile and a contiguous run of vocabulary tiles, so
 // its E tile is loaded once.  Every mbarrier wait gives up after two seconds:
@@ -39,8 +41,10 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BN = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiGroups = 2;                       // epilogue groups of 4 warps
+constexpr int kThreads = 64 + kEpiGroups * 128;     // producer, MMA, epilogue
 constexpr int kEpiWarp0 = 2;
+constexpr int kStagingPerWarp = 32 * 64 * 4;        // [32 rows x 64 cols] fp32
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 128;  // two 64-column accumulators
 
@@ -59,7 +63,7 @@ __host__ __device__ constexpr int num_stages(bool write) { return write ? 2 : 3;
 __host__ __device__ inline size_t smem_bytes(int r, bool write) {
   const size_t e_bytes = (size_t)r * 256;             // BM rows x r cols bf16
   const size_t stage = (size_t)r * 128 + BM * 128;    // W2 [r x 64] + U [128 x 64], bf16
-  const size_t staging = write ? 4 * 32 * 64 * 4 : 0;  // per-warp [32 x 64] fp32
+  const size_t staging = write ? (size_t)kEpiGroups * 4 * kStagingPerWarp : 0;
   return 1024 + e_bytes + num_stages(write) * stage + staging + 256;
 }
 
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sE = smem;
   uint8_t* sStage = sE + e_bytes;
   uint8_t* sStg = sStage + NS * stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + (WRITE ? 4 * 32 * 64 * 4 : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + (WRITE ? kEpiGroups * 4 * kStagingPerWarp : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + NS;
   uint64_t* tfull = bars + 2 * NS;
@@ -187,25 +191,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (count > 0 && warp >= kEpiWarp0) {
     // ------------------------------ epilogue ----------------------------------
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int g = (warp - kEpiWarp0) >> 2;  // epilogue group: tiles i with i % 2 == g
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int b = m_tile * BM + row;
     const bool vrow = b < p.B;
     const float T_ = vrow ? p.temp[b] : 1.f;
     const bool sampled = T_ > 0.f;
-    const float invT = inv_temp(T_);
-    float rm = 0.f, rS = 1.f;
+    const float c = row_scale(T_);
+    float rm = 0.f, rinvS = 1.f;
     int xb = -1;
     if (WRITE && vrow) {
       const float2 st = p.rowstat[b];
       rm = st.x;
-      rS = st.y;
+      rinvS = inv_sum(st.y);
       xb = p.tokens[(size_t)b * p.G + p.k];
     }
-    uint8_t* stg = sStg + (warp - kEpiWarp0) * (32 * 64 * 4);
+    uint8_t* stg = sStg + (warp - kEpiWarp0) * kStagingPerWarp;
     float pdtok = 0.f;
     bool have_pdtok = false;
-    for (int i = 0; i < count; ++i) {
+    for (int i = g; i < count; i += kEpiGroups) {
       const int s = i % NS, a = i & 1;
       const int n = n_lo + i;
       const int v0 = n * BN;
@@ -239,36 +244,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       // U row of this thread: 8 swizzled 16-byte chunks of 8 bf16
       const uint8_t* su = sStage + s * stage_bytes + w2_bytes + row * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(su + ((c ^ (row & 7)) << 4));
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 qv = *reinterpret_cast<const uint4*>(su + ((cc ^ (row & 7)) << 4));
         const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __bfloat1622float2(bp[e]);
-          acc[8 * c + 2 * e] = add_base(f.x, acc[8 * c + 2 * e]);
-          acc[8 * c + 2 * e + 1] = add_base(f.y, acc[8 * c + 2 * e + 1]);
+          acc[8 * cc + 2 * e] = add_base(f.x, acc[8 * cc + 2 * e]);
+          acc[8 * cc + 2 * e + 1] = add_base(f.y, acc[8 * cc + 2 * e + 1]);
         }
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[s]);
-      // acc[j] now holds the logit l of column v0 + j
+      // acc[j] now holds the logit l of column v0 + j; columns past V are masked
+      const int nvalid = min(BN, p.V - v0);
       if (!WRITE) {
-        float mt = -INFINITY, av = -INFINITY;
-        int ai = INT_MAX;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          if (v0 + j < p.V) {
-            mt = fmaxf(mt, scale_logit(acc[j], invT));
+          acc[j] = (j < nvalid) ? scale_logit(acc[j], c) : -INFINITY;  // y = l c (greedy rows: c = 1)
+          mx[j & 3] = fmaxf(mx[j & 3], acc[j]);
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mt);
+        const float st = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+        float av = -INFINITY;
+        int ai = INT_MAX;
+        if (!sampled) {
+          // greedy: argmax of y = l, ties to the lowest column
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
             if (acc[j] > av) {
               av = acc[j];
               ai = v0 + j;
             }
-          }
         }
-        float st = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j)
-          if (v0 + j < p.V) st += exp_shifted(scale_logit(acc[j], invT), mt);
         if (vrow) p.part[(size_t)b * p.ntiles + n] = make_float4(mt, st, av, __int_as_float(ai));
       } else {
         // the previous tile's TMA stores must have read the staging buffer
@@ -277,23 +289,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int cc = 0; cc < 8; ++cc) {
             float pv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int j = 32 * h + 4 * c + e;
-              float pr;
-              if (sampled)
-                pr = prob_from(scale_logit(acc[j], invT), rm, rS);
-              else
-                pr = (v0 + j == xb) ? 1.f : 0.f;
+              const int j = 32 * h + 4 * cc + e;
+              const float pr = sampled ? prob_from(scale_logit(acc[j], c), rm, rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
               if (v0 + j == xb) {
                 pdtok = pr;
                 have_pdtok = true;
               }
               pv[e] = pr;
             }
-            *reinterpret_cast<float4*>(stg + h * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<float4*>(stg + h * 4096 + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
                 make_float4(pv[0], pv[1], pv[2], pv[3]);
           }
         }

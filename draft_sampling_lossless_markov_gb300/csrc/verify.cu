@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
   const T* z = target + row * V;
   const float T_ = temp[r];
   const bool sampled = T_ > 0.f;
-  const float invT = inv_temp(T_);
+  const float invT = row_scale(T_);
   const bool vec = (V & 7) == 0;
 
   if (sampled) {
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
           lm = fmaxf(lm, v[e]);
         }
         if (lm > m) {
-          s = s * expf(m - lm);
+          s = s * exp2f(m - lm);
           m = lm;
         }
 #pragma unroll
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
       for (int i = tid; i < V; i += RS_THREADS) {
         const float y = scale_logit(to_f32(z[i]), invT);
         if (y > m) {
-          s = s * expf(m - y);
+          s = s * exp2f(m - y);
           m = y;
         }
         s += exp_shifted(y, m);
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
           report_error(hdr, DSPARK_BAD_INPUT, x);
           x = 0;
         }
-        ptok = prob_from(scale_logit(to_f32(z[x]), invT), M, S);
+        ptok = prob_from(scale_logit(to_f32(z[x]), invT), M, inv_sum(S));
       }
       rs[row] = make_float4(M, S, __int_as_float(-1), ptok);
     }
@@ -118,18 +118,18 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
   }
 }
 
-// q(v) of the final draw: residual max(0, p_t - p_d) or the bonus weight exp(y - m)
+// q(v) of the final draw: residual max(0, p_t - p_d) or the bonus weight 2^(y - m)
 template <typename T, int MODE>  // MODE 0: residual, 1: target weights
-__device__ __forceinline__ float final_weight(const T* z, const float* pd, int v, float invT, float m, float S) {
-  const float y = scale_logit(to_f32(z[v]), invT);
+__device__ __forceinline__ float final_weight(const T* z, const float* pd, int v, float c, float m, float invS) {
+  const float y = scale_logit(to_f32(z[v]), c);
   if (MODE == 1) return exp_shifted(y, m);
-  return fmaxf(0.f, __fsub_rn(prob_from(y, m, S), pd[v]));
+  return fmaxf(0.f, __fsub_rn(prob_from(y, m, invS), pd[v]));
 }
 
 // one CTA: sum of q over the row in (warp segment, 256-element chunk) order and
 // the token where the running sum first exceeds u * sum
 template <typename T, int MODE>
-__device__ int final_draw(const T* z, const float* pd, int V, float invT, float m, float S, float u, float* sm_seg,
+__device__ int final_draw(const T* z, const float* pd, int V, float invT, float m, float invS, float u, float* sm_seg,
                           int* sm_int, float* sm_flt, bool& zero_mass) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int NW = FIN_THREADS / 32;
@@ -142,7 +142,7 @@ __device__ int final_draw(const T* z, const float* pd, int V, float invT, float 
     const int v0 = c + lane * 8;
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      if (v0 + e < s_hi) ls += final_weight<T, MODE>(z, pd, v0 + e, invT, m, S);
+      if (v0 + e < s_hi) ls += final_weight<T, MODE>(z, pd, v0 + e, invT, m, invS);
     acc += warp_sum(ls);
   }
   if (lane == 0) sm_seg[wid] = acc;
@@ -188,7 +188,7 @@ __device__ int final_draw(const T* z, const float* pd, int V, float invT, float 
       const int v0 = c + lane * 8;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        q[e] = (v0 + e < g_hi) ? final_weight<T, MODE>(z, pd, v0 + e, invT, m, S) : 0.f;
+        q[e] = (v0 + e < g_hi) ? final_weight<T, MODE>(z, pd, v0 + e, invT, m, invS) : 0.f;
         ls += q[e];
         if (q[e] > 0.f) lastpos = max(lastpos, v0 + e);
       }
@@ -282,16 +282,16 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
     x = __float_as_int(st.z);
   } else {
     const T* z = target + ((size_t)base + m) * V;
-    const float invT = inv_temp(T_);
+    const float invT = row_scale(T_);
     bool zero_mass = false;
     if (m < L) {
       const float u = philox_uniform(seed, req, (uint32_t)(m + 1), 2u);
       const float* pd = pd_rows + ((size_t)r * G + m) * V;
-      x = final_draw<T, 0>(z, pd, V, invT, st.x, st.y, u, sm_seg, sm_int, sm_flt, zero_mass);
-      if (zero_mass) x = final_draw<T, 1>(z, pd, V, invT, st.x, st.y, u, sm_seg, sm_int, sm_flt, zero_mass);
+      x = final_draw<T, 0>(z, pd, V, invT, st.x, inv_sum(st.y), u, sm_seg, sm_int, sm_flt, zero_mass);
+      if (zero_mass) x = final_draw<T, 1>(z, pd, V, invT, st.x, inv_sum(st.y), u, sm_seg, sm_int, sm_flt, zero_mass);
     } else {
       const float u = philox_uniform(seed, req, (uint32_t)(L + 1), 3u);
-      x = final_draw<T, 1>(z, nullptr, V, invT, st.x, st.y, u, sm_seg, sm_int, sm_flt, zero_mass);
+      x = final_draw<T, 1>(z, nullptr, V, invT, st.x, inv_sum(st.y), u, sm_seg, sm_int, sm_flt, zero_mass);
     }
   }
   if (tid == 0) {
