@@ -29,6 +29,7 @@ DSPARK_SCHED_GREEDY = 1
 DSPARK_MAX_GAMMA = 32
 DSPARK_MAX_RANK = 1024
 DSPARK_MAX_SCHED_KEYS = 65536
+DSPARK_MAX_VOCAB = 2097152
 
 EXPORTED = ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
             "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count",

@@ -18,7 +18,7 @@ static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 static bool dims_ok(const dspark_dims& d) {
-  if (d.B < 0 || d.gamma < 1 || d.gamma > DSPARK_MAX_GAMMA || d.V < 1) return false;
+  if (d.B < 0 || d.gamma < 1 || d.gamma > DSPARK_MAX_GAMMA || d.V < 1 || d.V > DSPARK_MAX_VOCAB) return false;
   if (d.r < 0 || d.r > DSPARK_MAX_RANK || d.H < 0) return false;
   if (d.dtype != DSPARK_BF16 && d.dtype != DSPARK_F32) return false;
   // index arithmetic stays in 64 bits; per-row sizes must fit in 32 bits
@@ -45,7 +45,7 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.vrs = take(B * (G + 1) * sizeof(float4));
   L.zh = take(B * G * sizeof(float));
   L.rowstat = take(B * sizeof(float2));
-  L.E = take(B * r * elem_size(d.dtype));
+  L.E = take(2 * B * r * elem_size(d.dtype));  // two buffers: positions alternate
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
   L.part = take(B * ntiles * sizeof(float4));
   L.total = align_up(off, 256);

@@ -5,11 +5,12 @@
 // [DSpark] 方法细节, "置信度头的设计": c_k = sigmoid(w_h . h_k + w_e . W1[x_{k-1}]).
 //
 // One position k runs as
-//   k_embed        E[b] = W1[x_{k-1}], confidence of position k
-//   logits pass 1  per (row, vocabulary tile): max and sum-exp of l/T, argmax of l
+//   logits pass 1  per (row, vocabulary tile): max and sum of 2^(l c), argmax of l
 //   k_select       per row: combine the tile partials, draw u, locate the tile
-//                  that holds the draw, recompute that one tile, pick x_k
-//   logits pass 2  recompute l, write p_d = exp(l/T - m) / S and p_d(x_k)
+//                  that holds the draw, recompute that one tile, pick x_k; then
+//                  copy W1[x_k] into the other E buffer and compute the
+//                  confidence of position k + 1 (k_embed does position 1)
+//   logits pass 2  recompute l, write p_d = 2^(l c - m) / S and p_d(x_k)
 // The logits are recomputed rather than stored: storing them would cost a
 // 4-byte write plus a 4-byte read per element, recomputing costs a 2-byte
 // re-read of U (W2 stays in L2).  Every kernel evaluates l, l/T and exp(l/T - m)
@@ -234,16 +235,52 @@ __device__ __forceinline__ float block_excl_scan_256(float v, float* sm, float& 
   return wpre + incl - v;
 }
 
+// After x_k is chosen the same CTA prepares position k + 1: it copies
+// W1[x_k] into the other E buffer and evaluates that position's confidence,
+// z_{k+1} = zh + w_e . W1[x_k] (the arithmetic of k_embed).
+template <typename T>
+__device__ __forceinline__ void embed_next(int x, int b, int k, const T* __restrict__ W1, const T* __restrict__ w,
+                                           const float* __restrict__ zh, T* __restrict__ Enext,
+                                           float* __restrict__ conf_logit, float* __restrict__ conf, int G, int r,
+                                           int H) {
+  if (k + 1 >= G || threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  float acc = 0.f;
+  if (r > 0) {
+    const T* row = W1 + (size_t)x * r;
+    const T* we = w + H;
+    T* dst = Enext + (size_t)b * r;
+    for (int i = lane; i < r; i += 32) {
+      const T v = row[i];
+      dst[i] = v;
+      acc = fmaf(to_f32(we[i]), to_f32(v), acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) {
+    const float z = zh[(size_t)b * G + k + 1] + acc;
+    conf_logit[(size_t)b * G + k + 1] = z;
+    conf[(size_t)b * G + k + 1] = 1.f / (1.f + expf(-z));
+  }
+}
+
+// Bytes of shared memory k_select stages a W2 tile chunk in.
+constexpr int kSelStageBytes = 32768;
+
 template <typename T>
 __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict__ part, int ntiles, int tw,
-                                                        const T* __restrict__ U, const T* __restrict__ E,
-                                                        const T* __restrict__ W2, const float* __restrict__ temp,
+                                                        const T* __restrict__ U, const T* __restrict__ Ecur,
+                                                        const T* __restrict__ W2, const T* __restrict__ W1,
+                                                        const T* __restrict__ w, const float* __restrict__ zh,
+                                                        T* __restrict__ Enext, const float* __restrict__ temp,
                                                         const uint32_t* __restrict__ req_id, uint64_t seed, int B,
-                                                        int G, int V, int r, int k, int32_t* __restrict__ tokens,
-                                                        float2* __restrict__ rowstat) {
-  extern __shared__ float Erow[];  // [r]
+                                                        int G, int V, int r, int H, int k, int32_t* __restrict__ tokens,
+                                                        float2* __restrict__ rowstat, float* __restrict__ conf_logit,
+                                                        float* __restrict__ conf) {
+  extern __shared__ float Erow[];  // [r] floats, then a [rows x tw] W2 chunk of T
+  T* Ws = reinterpret_cast<T*>(Erow + r);
   __shared__ float sm[32];
-  __shared__ int s_int[4];
+  __shared__ int s_int[5];
   __shared__ float s_flt[4];
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -252,16 +289,15 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
   const bool sampled = T_ > 0.f;
 
   if (!sampled) {
+    __shared__ int sai[SEL_THREADS / 32];
     float av = -INFINITY;
     int ai = INT_MAX;
     for (int t = tid; t < ntiles; t += SEL_THREADS) argmax_merge(av, ai, P[t].z, __float_as_int(P[t].w));
     warp_argmax(av, ai);
     if (lane == 0) {
       sm[wid] = av;
-      s_int[0] = 0;
+      sai[wid] = ai;
     }
-    __shared__ int sai[SEL_THREADS / 32];
-    if (lane == 0) sai[wid] = ai;
     __syncthreads();
     if (tid == 0) {
       float v = sm[0];
@@ -269,7 +305,10 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
       for (int w_ = 1; w_ < SEL_THREADS / 32; ++w_) argmax_merge(v, i, sm[w_], sai[w_]);
       tokens[(size_t)b * G + k] = i;
       rowstat[b] = make_float2(0.f, 1.f);
+      s_int[4] = i;
     }
+    __syncthreads();
+    embed_next(s_int[4], b, k, W1, w, zh, Enext, conf_logit, conf, G, r, H);
     return;
   }
 
@@ -326,29 +365,46 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
     for (int t = t_lo; t < tstar; ++t) run += tile_mass(P[t].x, P[t].y, m);
     s_flt[1] = run;
   }
-  for (int i = tid; i < r; i += SEL_THREADS) Erow[i] = to_f32(E[(size_t)b * r + i]);
+  for (int i = tid; i < r; i += SEL_THREADS) Erow[i] = to_f32(Ecur[(size_t)b * r + i]);
   __syncthreads();
   const float base = s_flt[1];
 
-  // recompute the tile's columns (tw <= SEL_THREADS) with the pass-1 arithmetic
-  const float invT = row_scale(T_);
-  const int col = tstar * tw + tid;
+  // Recompute the tile's columns (tw <= SEL_THREADS) with the same sequential
+  // FMA chain as the CUDA-core logits pass.  The W2 columns are staged through
+  // shared memory in chunks of rows so that all loads of a chunk are in flight
+  // together.
+  const float c = row_scale(T_);
+  const int col0 = tstar * tw;
+  const int col = col0 + tid;
+  const int chunk = max(1, min(r, kSelStageBytes / (tw * (int)sizeof(T))));
+  float acc = 0.f;
+  for (int kk0 = 0; kk0 < r; kk0 += chunk) {
+    const int nr = min(chunk, r - kk0);
+    const int total = nr * tw;
+    // 32 independent loads per thread are in flight before any is stored
+    for (int base = 0; base < total; base += SEL_THREADS * 32) {
+      T vals[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int idx = base + j * SEL_THREADS + tid;
+        const int rr = idx / tw, cc = idx - rr * tw;
+        vals[j] = (idx < total && col0 + cc < V) ? W2[(size_t)(kk0 + rr) * V + col0 + cc] : T(0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int idx = base + j * SEL_THREADS + tid;
+        if (idx < total) Ws[idx] = vals[j];
+      }
+    }
+    __syncthreads();
+    if (tid < tw && col < V)
+      for (int rr = 0; rr < nr; ++rr) acc = fmaf(Erow[kk0 + rr], to_f32(Ws[rr * tw + tid]), acc);
+    __syncthreads();
+  }
   float wv = 0.f;
   if (tid < tw && col < V) {
-    // the same sequential FMA chain as the CUDA-core logits pass; loads are
-    // issued eight at a time so that they overlap
-    float acc = 0.f;
-    int kk = 0;
-    for (; kk + 8 <= r; kk += 8) {
-      float wv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) wv[e] = ldf(W2 + (size_t)(kk + e) * V + col);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(Erow[kk + e], wv[e], acc);
-    }
-    for (; kk < r; ++kk) acc = fmaf(Erow[kk], ldf(W2 + (size_t)kk * V + col), acc);
     const float l = add_base(ldf(U + ((size_t)b * G + k) * V + col), acc);
-    wv = exp_shifted(scale_logit(l, invT), m);
+    wv = exp_shifted(scale_logit(l, c), m);
   }
   float tile_tot;
   const float excl = block_excl_scan_256(wv, sm, tile_tot);
@@ -367,7 +423,10 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
     if (x < 0) x = min(tstar * tw, V - 1);  // only reachable with non-finite logits
     tokens[(size_t)b * G + k] = x;
     rowstat[b] = make_float2(m, S);
+    s_int[4] = x;
   }
+  __syncthreads();
+  embed_next(s_int[4], b, k, W1, w, zh, Enext, conf_logit, conf, G, r, H);
 }
 
 // ---------------------------------------------------------------------------
@@ -390,7 +449,10 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
 
   const int BG = B * G;
   k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
-  count_launches(1 + 4 * G);
+  // position 0's embedding; later positions are prepared by k_select
+  k_embed<T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, 0, W1, w, zh, E, a.conf_logit, a.conf, B, G, V, r, H,
+                                           hdr);
+  count_launches(2 + 3 * G);
 
   const bool tc = draft_tc_supported(d);
   const int tw = tc ? draft_tc_tile_width() : CC_TW;
@@ -407,24 +469,26 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     e = cudaFuncSetAttribute(k_logits_cc<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)es_bytes);
     if (e != cudaSuccess) return e;
   }
+  const size_t sel_smem = (size_t)r * sizeof(float) + kSelStageBytes;
   const dim3 grid_cc(ntiles, (B + CC_ROWS - 1) / CC_ROWS);
   for (int k = 0; k < G; ++k) {
-    k_embed<T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, k, W1, w, zh, E, a.conf_logit, a.conf, B, G, V, r,
-                                             H, hdr);
+    // E holds two buffers: W1 rows of x_{k-1} for position k are in buffer k % 2
+    T* Ecur = E + (size_t)(k & 1) * B * r;
+    T* Enext = E + (size_t)((k + 1) & 1) * B * r;
     if (tc) {
       cudaError_t e = launch_draft_tc_pass(a, ws, L, maps, k, false, s);
       if (e != cudaSuccess) return e;
     } else {
-      k_logits_cc<T, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, E, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
+      k_logits_cc<T, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
                                                              a.tokens, a.pd_rows, a.pd_tok);
     }
-    k_select<T><<<B, SEL_THREADS, (size_t)r * sizeof(float), s>>>(part, ntiles, tw, U, E, W2, a.temp, a.req_id,
-                                                                   a.seed, B, G, V, r, k, a.tokens, rowstat);
+    k_select<T><<<B, SEL_THREADS, sel_smem, s>>>(part, ntiles, tw, U, Ecur, W2, W1, w, zh, Enext, a.temp, a.req_id,
+                                                 a.seed, B, G, V, r, H, k, a.tokens, rowstat, a.conf_logit, a.conf);
     if (tc) {
       cudaError_t e = launch_draft_tc_pass(a, ws, L, maps, k, true, s);
       if (e != cudaSuccess) return e;
     } else {
-      k_logits_cc<T, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, E, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
+      k_logits_cc<T, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
                                                             a.tokens, a.pd_rows, a.pd_tok);
     }
   }

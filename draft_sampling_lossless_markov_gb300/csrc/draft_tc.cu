@@ -422,11 +422,12 @@ cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLa
     if (!tc::encode(&maps->W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  {  // E [B, r] bf16 (workspace) as (i, b)
+  for (int eb = 0; eb < 2; ++eb) {  // E [2][B, r] bf16 (workspace) as (i, b), one map per buffer
     const cuuint64_t dims[2] = {r, B};
     const cuuint64_t strides[1] = {r * 2};
     const cuuint32_t box[2] = {64, tc::BM};
-    if (!tc::encode(&maps->E, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + L.E, dims, strides, box))
+    if (!tc::encode(&maps->E[eb], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + L.E + (size_t)eb * B * r * 2, dims, strides,
+                    box))
       return cudaErrorInvalidValue;
   }
   {  // p_d rows [B, G, V] fp32 as (v, k, b); stores of 32 columns x 32 rows
@@ -470,9 +471,9 @@ cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const 
   const dim3 grid(n_mtiles * p.ctas_per_m);
   const size_t smem = tc::smem_bytes(d.r, write);
   if (write)
-    tc::k_logits_tc<true><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.E, maps.Pd, p);
+    tc::k_logits_tc<true><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.E[k & 1], maps.Pd, p);
   else
-    tc::k_logits_tc<false><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.E, maps.Pd, p);
+    tc::k_logits_tc<false><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.E[k & 1], maps.Pd, p);
   return cudaGetLastError();
 }
 

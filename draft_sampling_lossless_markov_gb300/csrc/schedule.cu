@@ -9,10 +9,12 @@
 // [DSpark] 补充细节, "高吞吐量与低延迟推理": kept prefixes flattened with a
 // marker tensor.
 //
-// At most 65536 candidates (B * gamma), so one CTA does it all:
+// Two kernels.  k_sched_prep (many CTAs, one thread per candidate, because
+// the fp64 sigmoid is slow on one SM):
 //   1. c' (fp64 sigmoid rounded to fp32), a (fp32 running product), sort keys
 //      key = ~bits(a) for a > 0 (ascending key = descending a), 0xFFFFFFFF else,
-//      value = r * gamma + j, laid out in index order;
+//      value = r * gamma + j, laid out in index order.
+// k_schedule (one CTA of 1024 threads; at most 65536 candidates):
 //   2. stable LSD radix sort of the keys (4 passes of 8 bits); stability keeps
 //      equal a in (r, j) index order;
 //   3. fp64 block scan of the sorted a, Theta_i, first non-increase;
@@ -92,6 +94,35 @@ __device__ __forceinline__ double block_excl_scan_f64(double v, double* sm, doub
   return res;
 }
 
+constexpr int PREP_THREADS = 256;
+
+// One CTA covers floor(256 / gamma) whole requests: each thread calibrates one
+// (request, position) confidence, then one thread per request forms the
+// left-to-right fp32 products and writes the sort keys.
+__global__ void __launch_bounds__(PREP_THREADS) k_sched_prep(dspark_sched_args a, uint32_t* __restrict__ k0,
+                                                             uint32_t* __restrict__ v0) {
+  __shared__ float cs[PREP_THREADS];
+  const int B = a.B, G = a.gamma;
+  const int rb = PREP_THREADS / G;
+  const int t = threadIdx.x;
+  const int lr = t / G, j = t - lr * G;
+  const int r = blockIdx.x * rb + lr;
+  const bool valid = lr < rb && r < B;
+  if (valid) cs[t] = sts_conf(a.conf_logit[(size_t)r * G + j], a.sts_temp[j]);
+  __syncthreads();
+  if (valid && j == 0) {
+    float run = 1.f;
+    for (int jj = 0; jj < G; ++jj) {
+      run = __fmul_rn(run, cs[t + jj]);
+      const int idx = r * G + jj;
+      k0[idx] = run > 0.f ? ~__float_as_uint(run) : 0xFFFFFFFFu;
+      v0[idx] = (uint32_t)idx;
+      if (a.surv) a.surv[idx] = run;
+    }
+    a.ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
+  }
+}
+
 __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a, uint32_t* __restrict__ k0,
                                                              uint32_t* __restrict__ k1, uint32_t* __restrict__ v0,
                                                              uint32_t* __restrict__ v1) {
@@ -104,22 +135,9 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a
   const int B = a.B, G = a.gamma, n = B * G;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
-  // ---- 1. calibrated survival products and sort keys ----
+  // ---- candidates: keys written by k_sched_prep; a > 0 unless the key is all ones ----
   uint32_t ncand_local = 0;
-  for (int r = tid; r < B; r += SCH_THREADS) {
-    float run = 1.f;
-    for (int j = 0; j < G; ++j) {
-      const float c = sts_conf(a.conf_logit[(size_t)r * G + j], a.sts_temp[j]);
-      run = __fmul_rn(run, c);
-      const int idx = r * G + j;
-      const bool cand = run > 0.f;
-      k0[idx] = cand ? ~__float_as_uint(run) : 0xFFFFFFFFu;
-      v0[idx] = (uint32_t)idx;
-      ncand_local += cand;
-      if (a.surv) a.surv[idx] = run;
-    }
-    a.ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
-  }
+  for (int i = tid; i < n; i += SCH_THREADS) ncand_local += (k0[i] != 0xFFFFFFFFu);
   uint32_t ncand;
   block_excl_scan_u32(ncand_local, sm_u, ncand);
 
@@ -264,8 +282,10 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
   uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
+  const int rb = PREP_THREADS / a.gamma;
+  k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0);
   k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
-  count_launches(1);
+  count_launches(2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.n_verify_host) e = cudaMemcpyAsync(a.n_verify_host, a.n_verify, sizeof(int32_t), cudaMemcpyDeviceToHost, s);

@@ -46,21 +46,28 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
   if (sampled) {
     float m = -INFINITY, s = 0.f;
     if (vec) {
-      for (int i = tid * 8; i < V; i += RS_THREADS * 8) {
-        float v[8];
-        load8_stream(z + i, v);
-        float lm = -INFINITY;
+      constexpr int STEP = RS_THREADS * 8;
+      for (int i0 = tid * 8; i0 < V; i0 += 4 * STEP) {
+        float v[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v[e] = scale_logit(v[e], invT);
-          lm = fmaxf(lm, v[e]);
-        }
-        if (lm > m) {
-          s = s * exp2f(m - lm);
-          m = lm;
-        }
+        for (int u = 0; u < 4; ++u)  // four 16-byte loads in flight per thread
+          if (i0 + u * STEP < V) load8_stream(z + i0 + u * STEP, v[u]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s += exp_shifted(v[e], m);
+        for (int u = 0; u < 4; ++u) {
+          if (i0 + u * STEP >= V) break;
+          float lm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            v[u][e] = scale_logit(v[u][e], invT);
+            lm = fmaxf(lm, v[u][e]);
+          }
+          if (lm > m) {
+            s = s * exp2f(m - lm);
+            m = lm;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s += exp_shifted(v[u][e], m);
+        }
       }
     } else {
       for (int i = tid; i < V; i += RS_THREADS) {
@@ -96,11 +103,18 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
     float av = -INFINITY;
     int ai = INT_MAX;
     if (vec) {
-      for (int i = tid * 8; i < V; i += RS_THREADS * 8) {
-        float v[8];
-        load8_stream(z + i, v);
+      constexpr int STEP = RS_THREADS * 8;
+      for (int i0 = tid * 8; i0 < V; i0 += 4 * STEP) {
+        float v[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) argmax_merge(av, ai, v[e], i + e);
+        for (int u = 0; u < 4; ++u)
+          if (i0 + u * STEP < V) load8_stream(z + i0 + u * STEP, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (i0 + u * STEP >= V) break;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) argmax_merge(av, ai, v[u][e], i0 + u * STEP + e);
+        }
       }
     } else {
       for (int i = tid; i < V; i += RS_THREADS) argmax_merge(av, ai, to_f32(z[i]), i);
@@ -126,24 +140,58 @@ __device__ __forceinline__ float final_weight(const T* z, const float* pd, int v
   return fmaxf(0.f, __fsub_rn(prob_from(y, m, invS), pd[v]));
 }
 
-// one CTA: sum of q over the row in (warp segment, 256-element chunk) order and
-// the token where the running sum first exceeds u * sum
+// Chunks of 256 tokens (8 per lane) per warp segment; a segment holds at most
+// FIN_MAXCH of them, so V <= 32 * 256 * FIN_MAXCH = DSPARK_MAX_VOCAB.
+constexpr int FIN_MAXCH = 256;
+
+// q of the 8 tokens v0..v0+7 (masked past hi), with vector loads when the row
+// allows them; both branches evaluate final_weight's formula
 template <typename T, int MODE>
-__device__ int final_draw(const T* z, const float* pd, int V, float invT, float m, float invS, float u, float* sm_seg,
-                          int* sm_int, float* sm_flt, bool& zero_mass) {
+__device__ __forceinline__ void chunk_weights(const T* z, const float* pd, int v0, int hi, bool vec, float c, float m,
+                                              float invS, float (&q)[8]) {
+  if (vec && v0 + 8 <= hi) {
+    float zv[8], pv[8];
+    load8(z + v0, zv);
+    if (MODE == 0) load8(pd + v0, pv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float y = scale_logit(zv[e], c);
+      q[e] = (MODE == 1) ? exp_shifted(y, m) : fmaxf(0.f, __fsub_rn(prob_from(y, m, invS), pv[e]));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = (v0 + e < hi) ? final_weight<T, MODE>(z, pd, v0 + e, c, m, invS) : 0.f;
+  }
+}
+
+__device__ __forceinline__ float lane_sum8(const float (&q)[8]) {
+  return ((q[0] + q[1]) + (q[2] + q[3])) + ((q[4] + q[5]) + (q[6] + q[7]));
+}
+
+// One CTA draws a token from the unnormalised weights q over the row by
+// inverse CDF in token order: the sum runs over 32 warp segments, each a
+// sequence of 256-token chunks.  Pass 1 records every chunk's total in shared
+// memory (loads of consecutive chunks overlap); the warp whose segment holds
+// u * sum then finds the chunk from those totals and re-reads only that chunk
+// to find the token.  Rounding that leaves no crossing falls back to the last
+// token with positive weight of the chosen segment or chunk.
+template <typename T, int MODE>
+__device__ int final_draw(const T* z, const float* pd, int V, float c, float m, float invS, float u, float* tot,
+                          float* sm_seg, int* sm_int, float* sm_flt, bool& zero_mass) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   constexpr int NW = FIN_THREADS / 32;
   const int seg = (((V + NW - 1) / NW) + 255) & ~255;
   const int s_lo = min(wid * seg, V), s_hi = min(s_lo + seg, V);
-  // pass 1: per-warp segment sums, chunk by chunk
+  const int nch = (s_hi - s_lo + 255) >> 8;
+  const bool vec = (V & 7) == 0;
   float acc = 0.f;
-  for (int c = s_lo; c < s_hi; c += 256) {
-    float ls = 0.f;
-    const int v0 = c + lane * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (v0 + e < s_hi) ls += final_weight<T, MODE>(z, pd, v0 + e, invT, m, invS);
-    acc += warp_sum(ls);
+#pragma unroll 4
+  for (int ci = 0; ci < nch; ++ci) {
+    float q[8];
+    chunk_weights<T, MODE>(z, pd, s_lo + ci * 256 + lane * 8, s_hi, vec, c, m, invS, q);
+    const float ct = warp_sum(lane_sum8(q));
+    if (lane == 0) tot[wid * FIN_MAXCH + ci] = ct;
+    acc += ct;
   }
   if (lane == 0) sm_seg[wid] = acc;
   __syncthreads();
@@ -154,16 +202,10 @@ __device__ int final_draw(const T* z, const float* pd, int V, float invT, float 
     const float target = u * total;
     const unsigned over = __ballot_sync(0xffffffffu, incl > target);
     const unsigned pos = __ballot_sync(0xffffffffu, sv > 0.f);
-    int w_star;
-    bool hit = over != 0u && total > 0.f;
-    if (hit)
-      w_star = __ffs(over) - 1;
-    else
-      w_star = pos ? 31 - __clz(pos) : 0;
-    const float excl = __shfl_sync(0xffffffffu, incl - sv, w_star);
+    const bool hit = over != 0u && total > 0.f;
+    const int w_star = hit ? __ffs(over) - 1 : (pos ? 31 - __clz(pos) : 0);
     float pre = __shfl_up_sync(0xffffffffu, incl, 1);
     pre = __shfl_sync(0xffffffffu, (lane == 0) ? 0.f : pre, w_star);
-    (void)excl;
     if (lane == 0) {
       sm_int[0] = w_star;
       sm_int[1] = hit;
@@ -176,55 +218,71 @@ __device__ int final_draw(const T* z, const float* pd, int V, float invT, float 
   zero_mass = !(sm_flt[2] > 0.f);
   const int w_star = sm_int[0];
   const bool hit = sm_int[1] != 0;
-  int result = -1;
   if (wid == w_star) {
     const int g_lo = min(w_star * seg, V), g_hi = min(g_lo + seg, V);
-    float run = sm_flt[0];
+    const int gch = (g_hi - g_lo + 255) >> 8;
     const float target = sm_flt[1];
-    int lastpos = -1;
-    for (int c = g_lo; c < g_hi && result < 0; c += 256) {
-      float q[8];
-      float ls = 0.f;
-      const int v0 = c + lane * 8;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        q[e] = (v0 + e < g_hi) ? final_weight<T, MODE>(z, pd, v0 + e, invT, m, invS) : 0.f;
-        ls += q[e];
-        if (q[e] > 0.f) lastpos = max(lastpos, v0 + e);
+    float run = sm_flt[0];
+    int cstar = -1, lastc = -1;
+    float cpre = 0.f;
+    for (int c0 = 0; c0 < gch; c0 += 32) {
+      const int ci = c0 + lane;
+      const float tv = ci < gch ? tot[w_star * FIN_MAXCH + ci] : 0.f;
+      const float incl = warp_inclusive_scan(tv);
+      const unsigned over = __ballot_sync(0xffffffffu, hit && run + incl > target);
+      const unsigned pos = __ballot_sync(0xffffffffu, tv > 0.f);
+      if (pos) lastc = c0 + 31 - __clz(pos);
+      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.f;
+      if (over) {
+        const int Lc = __ffs(over) - 1;
+        cstar = c0 + Lc;
+        cpre = run + __shfl_sync(0xffffffffu, excl, Lc);
+        break;
       }
-      const float ctot = warp_sum(ls);
-      if (hit && run + ctot > target) {
-        const float incl = warp_inclusive_scan(ls);
-        const unsigned over = __ballot_sync(0xffffffffu, run + incl > target);
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    const bool in_chunk = cstar >= 0;
+    if (!in_chunk) cstar = lastc;
+    int x = -1;
+    if (cstar >= 0) {
+      float q[8];
+      const int v0 = g_lo + cstar * 256 + lane * 8;
+      chunk_weights<T, MODE>(z, pd, v0, g_hi, vec, c, m, invS, q);
+      const float ls = lane_sum8(q);
+      const float incl = warp_inclusive_scan(ls);
+      int lastp = -1;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (q[e] > 0.f) lastp = v0 + e;
+      if (in_chunk) {
+        const unsigned over = __ballot_sync(0xffffffffu, cpre + incl > target);
         if (over) {
-          const int L = __ffs(over) - 1;
+          const int Ll = __ffs(over) - 1;
           float pre = __shfl_up_sync(0xffffffffu, incl, 1);
-          pre = (lane == 0) ? 0.f : pre;
-          pre = __shfl_sync(0xffffffffu, pre, L);
-          int x = -1;
-          if (lane == L) {
-            float a = run + pre;
-            int lastp = -1;
+          pre = __shfl_sync(0xffffffffu, (lane == 0) ? 0.f : pre, Ll);
+          int xl = -1;
+          if (lane == Ll) {
+            float a = cpre + pre;
             for (int e = 0; e < 8; ++e) {
               a += q[e];
-              if (q[e] > 0.f) lastp = v0 + e;
               if (a > target) {
-                x = v0 + e;
+                xl = v0 + e;
                 break;
               }
             }
-            if (x < 0) x = lastp;
+            if (xl < 0) xl = lastp;
           }
-          x = __shfl_sync(0xffffffffu, x, L);
-          if (x >= 0) result = x;
+          x = __shfl_sync(0xffffffffu, xl, Ll);
         }
       }
-      run += ctot;
+      if (x < 0) {  // rounding left no crossing: last positive weight of the chunk
+        int lp = lastp;
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+        x = lp;
+      }
     }
-    // rounding left no crossing: last positive weight of the segment
-    for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
-    if (result < 0) result = lastpos;
-    if (lane == 0) sm_int[2] = result;
+    if (lane == 0) sm_int[2] = x;
   }
   __syncthreads();
   const int x = sm_int[2];
@@ -245,6 +303,7 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
                                                                int32_t* __restrict__ n_accept,
                                                                int32_t* __restrict__ out_tok,
                                                                int32_t* __restrict__ n_out) {
+  __shared__ float tot[32 * FIN_MAXCH];
   __shared__ float sm_seg[32];
   __shared__ int sm_int[4];
   __shared__ float sm_flt[4];
@@ -256,22 +315,22 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
   const bool sampled = T_ > 0.f;
   const uint32_t req = req_id[r];
   const int base = offsets[r];
-  if (tid == 0) {
-    int m = 0;
-    for (int j = 1; j <= L; ++j) {
-      const float4 st = rs[base + j - 1];
-      const int x = tokens[(size_t)r * G + j - 1];
-      bool acc;
+  if (tid < 32) {
+    // the accept tests of positions 1..L in parallel (gamma <= 32); the first
+    // rejection ends the accepted prefix
+    const int j = tid;
+    bool acc = true;
+    if (j < L) {
+      const float4 st = rs[base + j];
       if (sampled) {
-        const float u = philox_uniform(seed, req, (uint32_t)j, 1u);
-        acc = __fmul_rn(u, pd_tok[(size_t)r * G + j - 1]) < st.w;
+        const float u = philox_uniform(seed, req, (uint32_t)(j + 1), 1u);
+        acc = __fmul_rn(u, pd_tok[(size_t)r * G + j]) < st.w;
       } else {
-        acc = x == __float_as_int(st.z);
+        acc = tokens[(size_t)r * G + j] == __float_as_int(st.z);
       }
-      if (!acc) break;
-      ++m;
     }
-    s_m = m;
+    const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+    if (tid == 0) s_m = rej ? __ffs(rej) - 1 : L;
   }
   __syncthreads();
   const int m = s_m;
@@ -282,16 +341,16 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
     x = __float_as_int(st.z);
   } else {
     const T* z = target + ((size_t)base + m) * V;
-    const float invT = row_scale(T_);
+    const float c = row_scale(T_);
     bool zero_mass = false;
     if (m < L) {
       const float u = philox_uniform(seed, req, (uint32_t)(m + 1), 2u);
       const float* pd = pd_rows + ((size_t)r * G + m) * V;
-      x = final_draw<T, 0>(z, pd, V, invT, st.x, inv_sum(st.y), u, sm_seg, sm_int, sm_flt, zero_mass);
-      if (zero_mass) x = final_draw<T, 1>(z, pd, V, invT, st.x, inv_sum(st.y), u, sm_seg, sm_int, sm_flt, zero_mass);
+      x = final_draw<T, 0>(z, pd, V, c, st.x, inv_sum(st.y), u, tot, sm_seg, sm_int, sm_flt, zero_mass);
+      if (zero_mass) x = final_draw<T, 1>(z, pd, V, c, st.x, inv_sum(st.y), u, tot, sm_seg, sm_int, sm_flt, zero_mass);
     } else {
       const float u = philox_uniform(seed, req, (uint32_t)(L + 1), 3u);
-      x = final_draw<T, 1>(z, nullptr, V, invT, st.x, inv_sum(st.y), u, sm_seg, sm_int, sm_flt, zero_mass);
+      x = final_draw<T, 1>(z, nullptr, V, c, st.x, inv_sum(st.y), u, tot, sm_seg, sm_int, sm_flt, zero_mass);
     }
   }
   if (tid == 0) {

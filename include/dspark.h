@@ -74,13 +74,14 @@ typedef enum {
 #define DSPARK_MAX_GAMMA 32
 #define DSPARK_MAX_RANK 1024
 #define DSPARK_MAX_SCHED_KEYS 65536 /* B * gamma for dspark_schedule */
+#define DSPARK_MAX_VOCAB 2097152    /* V for every call */
 
 /* Problem sizes.  dtype applies to U, W1, W2, h, w and target_logits; every
  * output probability / confidence is fp32. */
 typedef struct {
   int32_t B;      /* requests in the batch, >= 0 (0 = nothing to do)        */
   int32_t gamma;  /* draft block size, 1..DSPARK_MAX_GAMMA                   */
-  int32_t V;      /* vocabulary size, >= 1                                   */
+  int32_t V;      /* vocabulary size, 1..DSPARK_MAX_VOCAB                    */
   int32_t r;      /* Markov rank, 0..DSPARK_MAX_RANK (0 = no head, DFlash)    */
   int32_t H;      /* backbone hidden size, >= 0                              */
   int32_t dtype;  /* dspark_dtype                                            */
