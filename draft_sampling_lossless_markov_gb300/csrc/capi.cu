@@ -42,7 +42,7 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.sk1 = take(B * G * sizeof(uint32_t));
   L.sv0 = take(B * G * sizeof(uint32_t));
   L.sv1 = take(B * G * sizeof(uint32_t));
-  L.vrs = take(B * (G + 1) * sizeof(float4));
+  L.vrs = take(B * (G + 1) * RS_PARTS * sizeof(float4));
   L.zh = take(B * G * sizeof(float));
   L.rowstat = take(B * sizeof(float2));
   L.E = take(2 * B * r * elem_size(d.dtype));  // two buffers: positions alternate

@@ -4,25 +4,31 @@
 //     bias[b, v] = E[b, :] . W2[:, v],   E[b] = W1[x_{k-1}]      (B x r x V)
 // ([DSpark] 方法细节, "马尔可夫头（Markov head）的实现").  With r = 256 it is
 // 2 r = 512 flop per (b, v) against 6 bytes of U read + p_d write, i.e. far
-// above the CUDA-core ridge, so it runs on the 5th-generation tensor cores:
+// above the CUDA-core ridge, so it runs on the 5th-generation tensor cores.
 //
-//   tile      128 requests (TMEM lanes) x 64 vocabulary columns, K = r
-//   warp 0    TMA producer: W2 tile [r x 64] (L2 evict-last: W2 is re-read at
-//             every position) and U tile [128 x 64] (L2 evict-first: streamed),
-//             both 128B-swizzled, into an NS-deep ring of stages
-//   warp 1    allocates TMEM, issues tcgen05.mma (A = E, K-major, resident for
-//             the whole CTA; B = W2 tile, MN-major) into one of two 64-column
-//             fp32 accumulators, commits to mbarriers
+// Tile: 128 requests (TMEM lanes) x 192 vocabulary columns, K = r.  One
+// tcgen05.mma instruction costs about the same for N = 64 and N = 128 and
+// reaches the tensor-core peak only near N = 256, so the tile is as wide as
+// TMEM allows: E (the A operand, r/2 columns) plus two 192-column fp32
+// accumulators fill the 512 columns.
+//
+//   warp 0    TMA producer, two rings: W2 in K-chunks [64 x 192] (L2
+//             evict-last: every pass re-reads W2) and U in column chunks
+//             [128 x 64] (L2 evict-first: streamed), all 128B-swizzled
+//   warp 1    allocates TMEM, issues tcgen05.mma (A = E from TMEM, B = W2
+//             K-chunk from shared memory, MN-major, N = 192) into one of the
+//             two accumulators, commits to mbarriers
 //   warps 2-9 epilogue, two groups of four warps (one per TMEM lane quarter)
-//             that take alternate tiles, each with its own accumulator: one
-//             request row per thread, TMEM -> registers, + U, then either the
-//             tile's (max, sum, argmax) partial (pass 1) or the probability
-//             row p_d = 2^(y - m) / S written through a per-warp swizzled
-//             staging buffer with TMA stores (pass 2)
+//             on alternate tiles, one accumulator each.  Group 0 first copies
+//             the E rows into TMEM.  Per tile and 64-column chunk: TMEM ->
+//             registers, + U, then either the tile's running (max, sum, argmax)
+//             partial (pass 1) or the probability row p_d = 2^(y - m) / S
+//             written through a per-warp swizzled staging buffer with TMA
+//             stores (pass 2)
 //
-// A CTA owns one 128-row M-tile and a contiguous run of vocabulary tiles, so
-// its E tile is loaded once.  Every mbarrier wait gives up after two seconds:
-// the kernel then records DSPARK_TIMEOUT in the workspace error word, lets the
+// A CTA owns one 128-row M-tile; the vocabulary tiles of an M-tile are dealt
+// round-robin to its CTAs.  Every mbarrier wait gives up after two seconds: the
+// kernel then records DSPARK_TIMEOUT in the workspace error word, lets the
 // other roles leave their loops, waits for its own TMA loads and stores, frees
 // its TMEM and returns.
 #include <cuda.h>
@@ -39,17 +45,23 @@
 namespace dspark {
 namespace tc {
 
-constexpr int BM = 128;
-constexpr int BN = 64;
-constexpr int kEpiGroups = 2;                       // epilogue groups of 4 warps
-constexpr int kThreads = 64 + kEpiGroups * 128;     // producer, MMA, epilogue
+constexpr int BM = 128;                              // rows per tile (TMEM lanes)
+constexpr int BN = 192;                              // vocabulary columns per tile
+constexpr int CW = 64;                               // columns per swizzle atom / chunk
+constexpr int NCH = BN / CW;                         // chunks per tile
+constexpr int KC = 64;                               // W2 rows per K-chunk
+constexpr int kThreads = 64 + 2 * 128;               // producer, MMA, two epilogue groups
 constexpr int kEpiWarp0 = 2;
-constexpr int kStagingPerWarp = 32 * 64 * 4;        // [32 rows x 64 cols] fp32
+constexpr int kStagingPerWarp = 32 * CW * 4;         // [32 rows x 64 cols] fp32
+constexpr uint32_t kW2Stage = KC * BN * 2;           // 24 KB
+constexpr uint32_t kUStage = BM * CW * 2;            // 16 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kTmemCols = 128;  // two 64-column accumulators
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol0 = 128;                   // accumulators after the E columns
 
 struct Params {
   int B, G, V, r, k, ntiles, ctas_per_m;
+  const __nv_bfloat16* E;  // [B, r] W1 rows of position k
   const float* temp;
   const float2* rowstat;
   const int32_t* tokens;
@@ -58,55 +70,60 @@ struct Params {
   WsHeader* hdr;
 };
 
-__host__ __device__ constexpr int num_stages(bool write) { return write ? 2 : 3; }
+__host__ __device__ constexpr int w2_stages(bool write) { return write ? 3 : 4; }
+__host__ __device__ constexpr int u_stages(bool write) { return write ? 4 : 6; }
 
-__host__ __device__ inline size_t smem_bytes(int r, bool write) {
-  const size_t e_bytes = (size_t)r * 256;             // BM rows x r cols bf16
-  const size_t stage = (size_t)r * 128 + BM * 128;    // W2 [r x 64] + U [128 x 64], bf16
-  const size_t staging = write ? (size_t)kEpiGroups * 4 * kStagingPerWarp : 0;
-  return 1024 + e_bytes + num_stages(write) * stage + staging + 256;
+__host__ __device__ inline size_t smem_bytes(bool write) {
+  const size_t staging = write ? (size_t)8 * kStagingPerWarp : 0;
+  return 1024 + w2_stages(write) * (size_t)kW2Stage + u_stages(write) * (size_t)kUStage + staging + 512;
 }
 
 template <bool WRITE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_logits_tc(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2,
-                const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmPd, Params p) {
-  constexpr int NS = num_stages(WRITE);
+                const __grid_constant__ CUtensorMap tmPd, Params p) {
+  constexpr int NW = w2_stages(WRITE);
+  constexpr int NU = u_stages(WRITE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int r = p.r;
-  const uint32_t e_bytes = (uint32_t)r * 256;
-  const uint32_t w2_bytes = (uint32_t)r * 128;
-  const uint32_t stage_bytes = w2_bytes + BM * 128;
-  uint8_t* sE = smem;
-  uint8_t* sStage = sE + e_bytes;
-  uint8_t* sStg = sStage + NS * stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + (WRITE ? kEpiGroups * 4 * kStagingPerWarp : 0));
-  uint64_t* full = bars;
-  uint64_t* empty = bars + NS;
-  uint64_t* tfull = bars + 2 * NS;
+  const int nkc = r / KC;  // K-chunks per tile
+  uint8_t* sW = smem;
+  uint8_t* sU = sW + NW * kW2Stage;
+  uint8_t* sStg = sU + NU * kUStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + (WRITE ? 8 * kStagingPerWarp : 0));
+  uint64_t* fullW = bars;
+  uint64_t* emptyW = fullW + NW;
+  uint64_t* fullU = emptyW + NW;
+  uint64_t* emptyU = fullU + NU;
+  uint64_t* tfull = emptyU + NU;
   uint64_t* tempty = tfull + 2;
-  uint64_t* efull = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(efull + 1);
+  uint64_t* eready = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(eready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x / p.ctas_per_m;
-  const int part_i = blockIdx.x % p.ctas_per_m;
-  const int n_per = (p.ntiles + p.ctas_per_m - 1) / p.ctas_per_m;
-  const int n_lo = min(part_i * n_per, p.ntiles);
-  const int count = min(p.ntiles, n_lo + n_per) - n_lo;
+  // vocabulary tiles of this M-tile are dealt round-robin: tile n_lo + i * stride
+  const int n_lo = blockIdx.x % p.ctas_per_m;
+  const int stride = p.ctas_per_m;
+  const int count = n_lo < p.ntiles ? (p.ntiles - n_lo + stride - 1) / stride : 0;
+  const int row_base = m_tile * BM;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1 + 4);
+    for (int s = 0; s < NW; ++s) {
+      ptx::mbar_init(&fullW[s], 1);
+      ptx::mbar_init(&emptyW[s], 1);
+    }
+    for (int s = 0; s < NU; ++s) {
+      ptx::mbar_init(&fullU[s], 1);
+      ptx::mbar_init(&emptyU[s], 4);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], 4);
     }
-    ptx::mbar_init(efull, 1);
+    ptx::mbar_init(eready, 4);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -129,73 +146,110 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_last = ptx::policy_evict_last();
       const uint64_t pol_first = ptx::policy_evict_first();
-      ptx::mbar_expect_tx(efull, e_bytes);
-      for (int kb = 0; kb < r / 64; ++kb)
-        ptx::tma_load_2d(sE + kb * (BM * 128), &tmE, efull, kb * 64, m_tile * BM, pol_last);
-      int issued = 0;
-      for (int i = 0; i < count; ++i) {
-        const int s = i % NS;
-        if (!ptx::mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
-          fail();
-          break;
+      int iw = 0, iu = 0;  // items issued into each ring
+      bool ok = true;
+      for (int i = 0; i < count && ok; ++i) {
+        const int v0 = (n_lo + i * stride) * BN;
+        for (int kc = 0; kc < nkc && ok; ++kc, ++iw) {
+          const int s = iw % NW;
+          if (!ptx::mbar_wait(&emptyW[s], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = sW + s * kW2Stage;
+          ptx::mbar_expect_tx(&fullW[s], kW2Stage);
+          for (int c = 0; c < NCH; ++c)
+            ptx::tma_load_2d(st + c * (KC * CW * 2), &tmW2, &fullW[s], v0 + c * CW, kc * KC, pol_last);
         }
-        const int n = n_lo + i;
-        uint8_t* st = sStage + s * stage_bytes;
-        ptx::mbar_expect_tx(&full[s], stage_bytes);
-        ptx::tma_load_2d(st, &tmW2, &full[s], n * BN, 0, pol_last);
-        ptx::tma_load_3d(st + w2_bytes, &tmU, &full[s], n * BN, p.k, m_tile * BM, pol_first);
-        issued = i + 1;
+        for (int c = 0; c < NCH && ok; ++c, ++iu) {
+          const int s = iu % NU;
+          if (!ptx::mbar_wait(&emptyU[s], ((iu / NU) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_expect_tx(&fullU[s], kUStage);
+          ptx::tma_load_3d(sU + s * kUStage, &tmU, &fullU[s], v0 + c * CW, p.k, row_base, pol_first);
+        }
       }
+      if (!ok) fail();
       // every load this thread issued has landed before the CTA may exit
-      ptx::mbar_wait(efull, 0, abort_flag, kWaitLimitNs);
-      for (int i = max(0, issued - NS); i < issued; ++i)
-        ptx::mbar_wait(&full[i % NS], (i / NS) & 1, abort_flag, kWaitLimitNs);
+      for (int j = max(0, iw - NW); j < iw; ++j) ptx::mbar_wait(&fullW[j % NW], (j / NW) & 1, abort_flag, kWaitLimitNs);
+      for (int j = max(0, iu - NU); j < iu; ++j) ptx::mbar_wait(&fullU[j % NU], (j / NU) & 1, abort_flag, kWaitLimitNs);
     }
   } else if (count > 0 && warp == 1) {
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, true);
-      const uint32_t aE = ptx::smem_u32(sE);
-      int issued = 0;
-      if (ptx::mbar_wait(efull, 0, abort_flag, kWaitLimitNs)) {
-        for (int i = 0; i < count; ++i) {
-          const int s = i % NS, a = i & 1;
-          if (!ptx::mbar_wait(&full[s], (i / NS) & 1, abort_flag, kWaitLimitNs) ||
-              !ptx::mbar_wait(&tempty[a], ((i >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
-            fail();
+      int issued = 0, iw = 0;
+      bool ok = ptx::mbar_wait(eready, 0, abort_flag, kWaitLimitNs);
+      if (ok) ptx::tc_fence_after();
+      for (int i = 0; i < count && ok; ++i) {
+        const int a = i & 1;
+        if (!ptx::mbar_wait(&tempty[a], ((i >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + kAccCol0 + (uint32_t)(a * BN);
+        for (int kc = 0; kc < nkc; ++kc, ++iw) {
+          const int s = iw % NW;
+          if (!ptx::mbar_wait(&fullW[s], (iw / NW) & 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t aW2 = ptx::smem_u32(sStage + s * stage_bytes);
-          const uint32_t d = tmem + (uint32_t)(a * BN);
-          for (int ks = 0; ks < r / 16; ++ks) {
-            // A: E tile, K-major, 128B swizzle: 64-column blocks of BM x 128 B,
-            //    K steps of 16 advance 32 B inside a block; 8-row groups 1024 B apart
-            const uint64_t ad = ptx::smem_desc_sw128(aE + (ks >> 2) * (BM * 128) + (ks & 3) * 32, 16, 1024);
-            // B: W2 tile [r x 64], MN-major, 128B swizzle: rows of 128 B (64 columns),
-            //    8-row groups 1024 B apart along K, a K step of 16 is two groups
-            //    (the leading offset only matters for tiles wider than 64 columns)
-            const uint64_t bd = ptx::smem_desc_sw128(aW2 + ks * 2048, 16, 1024);
-            ptx::tc_mma(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+          const uint32_t aW2 = ptx::smem_u32(sW + s * kW2Stage);
+#pragma unroll
+          for (int k4 = 0; k4 < KC / 16; ++k4) {
+            const int ks = kc * (KC / 16) + k4;
+            // B: W2 K-chunk [64 x 192], MN-major, 128B swizzle: three 64-column
+            //    blocks of 64 rows x 128 B, 8 KB apart (leading offset); 8-row
+            //    groups 1024 B apart along K (stride offset); a K step of 16 is
+            //    two groups
+            const uint64_t bd = ptx::smem_desc_sw128(aW2 + k4 * 2048, KC * CW * 2, 1024);
+            // A: E in TMEM, a K step of 16 bf16 = 8 columns
+            ptx::tc_mma_tmem_a(d, tmem + (uint32_t)(ks * 8), bd, idesc, ks > 0 ? 1u : 0u);
           }
-          ptx::tc_commit(&empty[s]);
-          ptx::tc_commit(&tfull[a]);
-          issued = i + 1;
+          ptx::tc_commit(&emptyW[s]);
         }
-      } else {
-        fail();
+        if (!ok) break;
+        ptx::tc_commit(&tfull[a]);
+        issued = i + 1;
       }
+      if (!ok) fail();
       // the last commit tracks every MMA issued: TMEM is not freed under a running MMA
       if (issued > 0)
         ptx::mbar_wait(&tfull[(issued - 1) & 1], ((issued - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
     }
   } else if (count > 0 && warp >= kEpiWarp0) {
     // ------------------------------ epilogue ----------------------------------
-    const int g = (warp - kEpiWarp0) >> 2;  // epilogue group: tiles i with i % 2 == g
+    const int g = (warp - kEpiWarp0) >> 2;  // group: tiles i with i % 2 == g
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;
-    const int b = m_tile * BM + row;
+    const int row = q * 32 + lane;          // row within the M-tile
+    const int b = row_base + row;
     const bool vrow = b < p.B;
+    const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
+    if (g == 0) {
+      // E rows into TMEM columns [0, r/2): two bf16 per column, zeros past B
+      const uint4* src = reinterpret_cast<const uint4*>(p.E + (size_t)b * r);
+      for (int c0 = 0; c0 < r / 64; ++c0) {
+        uint32_t wv[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 qv = vrow ? src[c0 * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
+          wv[4 * e] = qv.x;
+          wv[4 * e + 1] = qv.y;
+          wv[4 * e + 2] = qv.z;
+          wv[4 * e + 3] = qv.w;
+        }
+        ptx::tmem_st32(tmem + lane_bits + (uint32_t)(c0 * 32), wv);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(eready);
+    }
+
     const float T_ = vrow ? p.temp[b] : 1.f;
     const bool sampled = T_ > 0.f;
     const float c = row_scale(T_);
@@ -210,110 +264,126 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = sStg + (warp - kEpiWarp0) * kStagingPerWarp;
     float pdtok = 0.f;
     bool have_pdtok = false;
-    for (int i = g; i < count; i += kEpiGroups) {
-      const int s = i % NS, a = i & 1;
-      const int n = n_lo + i;
-      const int v0 = n * BN;
+    for (int i = g; i < count; i += 2) {
+      const int a = i & 1;  // == g
+      const int n = n_lo + i * stride;
       bool ok = ptx::mbar_wait(&tfull[a], (i >> 1) & 1, abort_flag, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) fail();
         break;
       }
       ptx::tc_fence_after();
-      float acc[64];
-      {
-        float h0[32], h1[32];
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN);
-        ptx::tmem_ld32(ta, h0);
-        ptx::tmem_ld32(ta + 32, h1);
-        ptx::tmem_ld_wait();
+      // pass 1: running (max, sum) of y over the tile, argmax of l (greedy rows)
+      float tm = -INFINITY, ts = 0.f, av = -INFINITY;
+      int ai = INT_MAX;
+      bool broke = false;
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int v0 = n * BN + ch * CW;
+        float acc[64];
+        {
+          float h0[32], h1[32];
+          const uint32_t ta = tmem + lane_bits + kAccCol0 + (uint32_t)(a * BN + ch * CW);
+          ptx::tmem_ld32(ta, h0);
+          ptx::tmem_ld32(ta + 32, h1);
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = h0[j];
-          acc[32 + j] = h1[j];
-        }
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tempty[a]);
-      ok = ptx::mbar_wait(&full[s], (i / NS) & 1, abort_flag, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) {
-        if (lane == 0) fail();
-        break;
-      }
-      // U row of this thread: 8 swizzled 16-byte chunks of 8 bf16
-      const uint8_t* su = sStage + s * stage_bytes + w2_bytes + row * 128;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(su + ((cc ^ (row & 7)) << 4));
-        const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(bp[e]);
-          acc[8 * cc + 2 * e] = add_base(f.x, acc[8 * cc + 2 * e]);
-          acc[8 * cc + 2 * e + 1] = add_base(f.y, acc[8 * cc + 2 * e + 1]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&empty[s]);
-      // acc[j] now holds the logit l of column v0 + j; columns past V are masked
-      const int nvalid = min(BN, p.V - v0);
-      if (!WRITE) {
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          acc[j] = (j < nvalid) ? scale_logit(acc[j], c) : -INFINITY;  // y = l c (greedy rows: c = 1)
-          mx[j & 3] = fmaxf(mx[j & 3], acc[j]);
-        }
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mt);
-        const float st = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-        float av = -INFINITY;
-        int ai = INT_MAX;
-        if (!sampled) {
-          // greedy: argmax of y = l, ties to the lowest column
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (acc[j] > av) {
-              av = acc[j];
-              ai = v0 + j;
-            }
-        }
-        if (vrow) p.part[(size_t)b * p.ntiles + n] = make_float4(mt, st, av, __int_as_float(ai));
-      } else {
-        // the previous tile's TMA stores must have read the staging buffer
-        if (lane == 0) ptx::bulk_wait_read0();
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            float pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 32 * h + 4 * cc + e;
-              const float pr = sampled ? prob_from(scale_logit(acc[j], c), rm, rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
-              if (v0 + j == xb) {
-                pdtok = pr;
-                have_pdtok = true;
-              }
-              pv[e] = pr;
-            }
-            *reinterpret_cast<float4*>(stg + h * 4096 + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
-                make_float4(pv[0], pv[1], pv[2], pv[3]);
+          for (int j = 0; j < 32; ++j) {
+            acc[j] = h0[j];
+            acc[32 + j] = h1[j];
           }
         }
-        ptx::fence_proxy_async_smem();
+        if (ch == NCH - 1) {  // the accumulator is free for the tile after next
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&tempty[a]);
+        }
+        const int iu = i * NCH + ch, su = iu % NU;
+        ok = ptx::mbar_wait(&fullU[su], (iu / NU) & 1, abort_flag, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) fail();
+          broke = true;
+          break;
+        }
+        {
+          // U row of this thread: 8 swizzled 16-byte chunks of 8 bf16
+          const uint8_t* su_row = sU + su * kUStage + row * 128;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((cc ^ (row & 7)) << 4));
+            const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(bp[e]);
+              acc[8 * cc + 2 * e] = add_base(f.x, acc[8 * cc + 2 * e]);
+              acc[8 * cc + 2 * e + 1] = add_base(f.y, acc[8 * cc + 2 * e + 1]);
+            }
+          }
+        }
         __syncwarp();
-        const int row0 = m_tile * BM + q * 32;
-        if (lane == 0 && row0 < p.B) {  // boxes that start past B or V would write nothing
-          ptx::tma_store_3d(&tmPd, stg, v0, p.k, row0);
-          if (v0 + 32 < p.V) ptx::tma_store_3d(&tmPd, stg + 4096, v0 + 32, p.k, row0);
-          ptx::bulk_commit();
+        if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
+        // acc[j] now holds the logit l of column v0 + j; columns past V are masked
+        const int nvalid = min(CW, p.V - v0);
+        if (!WRITE) {
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            acc[j] = (j < nvalid) ? scale_logit(acc[j], c) : -INFINITY;  // y = l c (greedy rows: c = 1)
+            mx[j & 3] = fmaxf(mx[j & 3], acc[j]);
+          }
+          const float mc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          if (mc > -INFINITY) {
+            float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mc);
+            lse_merge(tm, ts, mc, (sm[0] + sm[1]) + (sm[2] + sm[3]));
+          }
+          if (!sampled) {
+            // greedy: argmax of y = l, ties to the lowest column
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (acc[j] > av) {
+                av = acc[j];
+                ai = v0 + j;
+              }
+          }
+        } else {
+          // the previous chunk's TMA stores must have read the staging buffer
+          if (lane == 0) ptx::bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              float pv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 32 * h + 4 * cc + e;
+                const float pr =
+                    sampled ? prob_from(scale_logit(acc[j], c), rm, rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
+                if (v0 + j == xb) {
+                  pdtok = pr;
+                  have_pdtok = true;
+                }
+                pv[e] = pr;
+              }
+              *reinterpret_cast<float4*>(stg + h * 4096 + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                  make_float4(pv[0], pv[1], pv[2], pv[3]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          const int row0 = row_base + q * 32;
+          if (lane == 0 && row0 < p.B && v0 < p.V) {  // boxes that start past B or V would write nothing
+            // p_d is streamed out: evict-first keeps the re-read W2 in L2
+            const uint64_t pol = ptx::policy_evict_first();
+            ptx::tma_store_3d(&tmPd, stg, v0, p.k, row0, pol);
+            if (v0 + 32 < p.V) ptx::tma_store_3d(&tmPd, stg + 4096, v0 + 32, p.k, row0, pol);
+            ptx::bulk_commit();
+          }
         }
       }
+      if (broke) break;
+      if (!WRITE && vrow) p.part[(size_t)b * p.ntiles + n] = make_float4(tm, ts, av, __int_as_float(ai));
     }
     if (WRITE) {
       if (vrow && have_pdtok) p.pd_tok[(size_t)b * p.G + p.k] = pdtok;
@@ -411,23 +481,15 @@ cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLa
   {  // U [B, G, V] bf16 as (v, k, b)
     const cuuint64_t dims[3] = {V, G, B};
     const cuuint64_t strides[2] = {V * 2, G * V * 2};
-    const cuuint32_t box[3] = {tc::BN, 1, tc::BM};
+    const cuuint32_t box[3] = {tc::CW, 1, tc::BM};
     if (!tc::encode(&maps->U, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.U, dims, strides, box))
       return cudaErrorInvalidValue;
   }
   {  // W2 [r, V] bf16 as (v, i)
     const cuuint64_t dims[2] = {V, r};
     const cuuint64_t strides[1] = {V * 2};
-    const cuuint32_t box[2] = {tc::BN, (cuuint32_t)r};
+    const cuuint32_t box[2] = {tc::CW, tc::KC};
     if (!tc::encode(&maps->W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W2, dims, strides, box))
-      return cudaErrorInvalidValue;
-  }
-  for (int eb = 0; eb < 2; ++eb) {  // E [2][B, r] bf16 (workspace) as (i, b), one map per buffer
-    const cuuint64_t dims[2] = {r, B};
-    const cuuint64_t strides[1] = {r * 2};
-    const cuuint32_t box[2] = {64, tc::BM};
-    if (!tc::encode(&maps->E[eb], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + L.E + (size_t)eb * B * r * 2, dims, strides,
-                    box))
       return cudaErrorInvalidValue;
   }
   {  // p_d rows [B, G, V] fp32 as (v, k, b); stores of 32 columns x 32 rows
@@ -441,10 +503,10 @@ cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLa
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(tc::k_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)tc::smem_bytes(256, false));
+                                    (int)tc::smem_bytes(false));
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(tc::k_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)tc::smem_bytes(256, true));
+                                      (int)tc::smem_bytes(true));
   });
   return attr_err;
 }
@@ -462,6 +524,7 @@ cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const 
   const int n_mtiles = (d.B + tc::BM - 1) / tc::BM;
   const int sms = tc::dev_info().sms > 0 ? tc::dev_info().sms : 148;
   p.ctas_per_m = max(1, min(p.ntiles, sms / n_mtiles));
+  p.E = reinterpret_cast<const __nv_bfloat16*>(ws + L.E) + (size_t)(k & 1) * d.B * d.r;
   p.temp = a.temp;
   p.rowstat = reinterpret_cast<const float2*>(ws + L.rowstat);
   p.tokens = a.tokens;
@@ -469,11 +532,11 @@ cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const 
   p.pd_tok = a.pd_tok;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   const dim3 grid(n_mtiles * p.ctas_per_m);
-  const size_t smem = tc::smem_bytes(d.r, write);
+  const size_t smem = tc::smem_bytes(write);
   if (write)
-    tc::k_logits_tc<true><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.E[k & 1], maps.Pd, p);
+    tc::k_logits_tc<true><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.Pd, p);
   else
-    tc::k_logits_tc<false><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.E[k & 1], maps.Pd, p);
+    tc::k_logits_tc<false><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.Pd, p);
   return cudaGetLastError();
 }
 

@@ -15,13 +15,16 @@ namespace dspark {
 // workspace is sized for the smaller width.
 constexpr int kPartialTileMin = 64;
 
+// Slices per kept row in the verify row statistics.
+constexpr int RS_PARTS = 4;
+
 struct WsLayout {
   size_t zh = 0;       // [B*G] f32: w_h . h_k
   size_t E = 0;        // [2][B*r] dtype: W1 rows of the previous tokens, two alternating buffers
   size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index)
   size_t rowstat = 0;  // [B] float2: (row max, row sum) of the current position
   size_t sk0 = 0, sk1 = 0, sv0 = 0, sv1 = 0;  // scheduler sort buffers [B*G] u32
-  size_t vrs = 0;      // [B*(G+1)] float4: verify row stats
+  size_t vrs = 0;      // [B*(G+1)*RS_PARTS] float4: verify row-slice statistics
   size_t total = 0;
 };
 
@@ -38,7 +41,7 @@ cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayo
 
 // Tensor-core logits passes of the draft sampler (draft_tc.cu).
 struct TcMaps {
-  CUtensorMap U, W2, E[2], Pd;
+  CUtensorMap U, W2, Pd;
 };
 bool draft_tc_supported(const dspark_dims& d);
 int draft_tc_tile_width();

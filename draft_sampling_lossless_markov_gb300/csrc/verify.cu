@@ -6,13 +6,13 @@
 // norm(max(0, p_t - p_d)); bonus token when everything is accepted; argmax
 // compare at temperature 0.
 //
-// k_verify_rowstats  one CTA per kept row (request r, row j <= l_r): max and
-//                    sum-exp of z / T (sampled) or argmax of z (greedy), and
-//                    p_t at the draft token of that row.
-// k_verify_finish    one CTA per request: left-to-right accept scan over the row
-//                    statistics, then one inverse-CDF draw over the final row
-//                    (residual or bonus) with a two-level search: per-warp
-//                    segment sums, then a rescan of the one segment that holds
+// k_verify_rowstats  one CTA per slice of a kept row (request r, row j <= l_r):
+//                    max and sum of 2^(z c) (sampled) or argmax of z (greedy)
+// k_verify_finish    one CTA per request: the accept tests of all positions in
+//                    one warp (p_t at each draft token from the combined row
+//                    statistics), the first rejection, then one inverse-CDF draw
+//                    over the final row (residual or bonus): per-chunk sums in
+//                    shared memory, then a re-read of the one chunk that holds
 //                    the draw.
 #include "common.cuh"
 #include "draft_arith.cuh"
@@ -20,19 +20,22 @@
 
 namespace dspark {
 
-constexpr int RS_THREADS = 512;
+constexpr int RS_THREADS = 256;
 constexpr int FIN_THREADS = 1024;
 
+// Each kept row is split into RS_PARTS contiguous slices, one CTA per slice, so
+// that the grid is many small CTAs instead of one wave of big ones plus a
+// nearly empty second wave.  Partial per (row, slice): sampled rows store
+// (max y, sum 2^(y - max)); greedy rows store (argmax value, argmax index).
 template <typename T>
 __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restrict__ target,
                                                                 const int32_t* __restrict__ offsets,
                                                                 const int32_t* __restrict__ ell,
-                                                                const int32_t* __restrict__ tokens,
-                                                                const float* __restrict__ temp, int G, int V,
-                                                                float4* __restrict__ rs, WsHeader* hdr) {
+                                                                const float* __restrict__ temp, int V,
+                                                                float4* __restrict__ rsp) {
   __shared__ float sm_a[RS_THREADS / 32], sm_b[RS_THREADS / 32];
   __shared__ int sm_i[RS_THREADS / 32];
-  const int r = blockIdx.x, j = blockIdx.y;
+  const int r = blockIdx.x, j = blockIdx.y, part = blockIdx.z;
   const int L = ell[r];
   if (j > L) return;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -40,38 +43,33 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
   const T* z = target + row * V;
   const float T_ = temp[r];
   const bool sampled = T_ > 0.f;
-  const float invT = row_scale(T_);
+  const float c = row_scale(T_);
   const bool vec = (V & 7) == 0;
+  const int span = ((V + RS_PARTS - 1) / RS_PARTS + 7) & ~7;  // multiple of 8: vector loads stay aligned
+  const int lo = min(part * span, V), hi = min(lo + span, V);
 
   if (sampled) {
     float m = -INFINITY, s = 0.f;
     if (vec) {
-      constexpr int STEP = RS_THREADS * 8;
-      for (int i0 = tid * 8; i0 < V; i0 += 4 * STEP) {
-        float v[4][8];
+      for (int i = lo + tid * 8; i < hi; i += RS_THREADS * 8) {
+        float v[8];
+        load8_stream(z + i, v);
+        float lm = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)  // four 16-byte loads in flight per thread
-          if (i0 + u * STEP < V) load8_stream(z + i0 + u * STEP, v[u]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (i0 + u * STEP >= V) break;
-          float lm = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v[u][e] = scale_logit(v[u][e], invT);
-            lm = fmaxf(lm, v[u][e]);
-          }
-          if (lm > m) {
-            s = s * exp2f(m - lm);
-            m = lm;
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) s += exp_shifted(v[u][e], m);
+        for (int e = 0; e < 8; ++e) {
+          v[e] = scale_logit(v[e], c);
+          lm = fmaxf(lm, v[e]);
         }
+        if (lm > m) {
+          s = s * exp2f(m - lm);
+          m = lm;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += exp_shifted(v[e], m);
       }
     } else {
-      for (int i = tid; i < V; i += RS_THREADS) {
-        const float y = scale_logit(to_f32(z[i]), invT);
+      for (int i = lo + tid; i < hi; i += RS_THREADS) {
+        const float y = scale_logit(to_f32(z[i]), c);
         if (y > m) {
           s = s * exp2f(m - y);
           m = y;
@@ -88,36 +86,20 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
     if (tid == 0) {
       float M = sm_a[0], S = sm_b[0];
       for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) lse_merge(M, S, sm_a[w_], sm_b[w_]);
-      float ptok = 0.f;
-      if (j < L) {
-        int x = tokens[(size_t)r * G + j];
-        if (x < 0 || x >= V) {
-          report_error(hdr, DSPARK_BAD_INPUT, x);
-          x = 0;
-        }
-        ptok = prob_from(scale_logit(to_f32(z[x]), invT), M, inv_sum(S));
-      }
-      rs[row] = make_float4(M, S, __int_as_float(-1), ptok);
+      rsp[row * RS_PARTS + part] = make_float4(M, S, 0.f, 0.f);
     }
   } else {
     float av = -INFINITY;
     int ai = INT_MAX;
     if (vec) {
-      constexpr int STEP = RS_THREADS * 8;
-      for (int i0 = tid * 8; i0 < V; i0 += 4 * STEP) {
-        float v[4][8];
+      for (int i = lo + tid * 8; i < hi; i += RS_THREADS * 8) {
+        float v[8];
+        load8_stream(z + i, v);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (i0 + u * STEP < V) load8_stream(z + i0 + u * STEP, v[u]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (i0 + u * STEP >= V) break;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) argmax_merge(av, ai, v[u][e], i0 + u * STEP + e);
-        }
+        for (int e = 0; e < 8; ++e) argmax_merge(av, ai, v[e], i + e);
       }
     } else {
-      for (int i = tid; i < V; i += RS_THREADS) argmax_merge(av, ai, to_f32(z[i]), i);
+      for (int i = lo + tid; i < hi; i += RS_THREADS) argmax_merge(av, ai, to_f32(z[i]), i);
     }
     warp_argmax(av, ai);
     if (lane == 0) {
@@ -127,9 +109,30 @@ __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restr
     __syncthreads();
     if (tid == 0) {
       for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) argmax_merge(av, ai, sm_a[w_], sm_i[w_]);
-      rs[row] = make_float4(0.f, 1.f, __int_as_float(ai), 0.f);
+      rsp[row * RS_PARTS + part] = make_float4(av, __int_as_float(ai), 0.f, 0.f);
     }
   }
+}
+
+// Row statistics from the slice partials, combined in slice order:
+// sampled rows -> (M, S) of the whole row; greedy rows -> argmax (in .z).
+__device__ __forceinline__ float4 row_stats(const float4* __restrict__ rsp, size_t row, bool sampled) {
+  const float4 p0 = rsp[row * RS_PARTS];
+  if (sampled) {
+    float M = p0.x, S = p0.y;
+    for (int q = 1; q < RS_PARTS; ++q) {
+      const float4 pq = rsp[row * RS_PARTS + q];
+      lse_merge(M, S, pq.x, pq.y);
+    }
+    return make_float4(M, S, __int_as_float(-1), 0.f);
+  }
+  float av = p0.x;
+  int ai = __float_as_int(p0.y);
+  for (int q = 1; q < RS_PARTS; ++q) {
+    const float4 pq = rsp[row * RS_PARTS + q];
+    argmax_merge(av, ai, pq.x, __float_as_int(pq.y));
+  }
+  return make_float4(0.f, 1.f, __int_as_float(ai), 0.f);
 }
 
 // q(v) of the final draw: residual max(0, p_t - p_d) or the bonus weight 2^(y - m)
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
                                                                int G, int V, const float4* __restrict__ rs,
                                                                int32_t* __restrict__ n_accept,
                                                                int32_t* __restrict__ out_tok,
-                                                               int32_t* __restrict__ n_out) {
+                                                               int32_t* __restrict__ n_out, WsHeader* hdr) {
   __shared__ float tot[32 * FIN_MAXCH];
   __shared__ float sm_seg[32];
   __shared__ int sm_int[4];
@@ -321,12 +324,20 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
     const int j = tid;
     bool acc = true;
     if (j < L) {
-      const float4 st = rs[base + j];
+      const size_t row = (size_t)base + j;
+      const float4 st = row_stats(rs, row, sampled);
+      int x = tokens[(size_t)r * G + j];
+      if (x < 0 || x >= V) {
+        report_error(hdr, DSPARK_BAD_INPUT, x);
+        x = 0;
+      }
       if (sampled) {
+        const float c = row_scale(T_);
+        const float ptok = prob_from(scale_logit(to_f32(target[row * V + x]), c), st.x, inv_sum(st.y));
         const float u = philox_uniform(seed, req, (uint32_t)(j + 1), 1u);
-        acc = __fmul_rn(u, pd_tok[(size_t)r * G + j]) < st.w;
+        acc = __fmul_rn(u, pd_tok[(size_t)r * G + j]) < ptok;
       } else {
-        acc = tokens[(size_t)r * G + j] == __float_as_int(st.z);
+        acc = x == __float_as_int(st.z);
       }
     }
     const unsigned rej = __ballot_sync(0xffffffffu, !acc);
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
   __syncthreads();
   const int m = s_m;
   for (int i = tid; i <= G; i += FIN_THREADS) out_tok[(size_t)r * (G + 1) + i] = (i < m) ? tokens[(size_t)r * G + i] : -1;
-  const float4 st = rs[base + m];
+  const float4 st = row_stats(rs, (size_t)base + m, sampled);
   int x;
   if (!sampled) {
     x = __float_as_int(st.z);
@@ -366,9 +377,9 @@ static cudaError_t launch_verify_t(const dspark_verify_args& a, uint8_t* ws, con
   float4* rs = reinterpret_cast<float4*>(ws + L.vrs);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const T* tg = static_cast<const T*>(a.target_logits);
-  k_verify_rowstats<T><<<dim3(B, G + 1), RS_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.temp, G, V, rs, hdr);
+  k_verify_rowstats<T><<<dim3(B, G + 1, RS_PARTS), RS_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.temp, V, rs);
   k_verify_finish<T><<<B, FIN_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.pd_rows, a.pd_tok, a.temp,
-                                               a.req_id, a.seed, G, V, rs, a.n_accept, a.out_tok, a.n_out);
+                                               a.req_id, a.seed, G, V, rs, a.n_accept, a.out_tok, a.n_out, hdr);
   count_launches(2);
   return cudaGetLastError();
 }
