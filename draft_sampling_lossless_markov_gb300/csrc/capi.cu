@@ -45,6 +45,7 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.vrs = take(B * (G + 1) * RS_PARTS * sizeof(float4));
   L.zh = take(B * G * sizeof(float));
   L.rowstat = take(B * sizeof(float2));
+  L.sel = take(B * sizeof(float4));
   L.E = take(2 * B * r * elem_size(d.dtype));  // two buffers: positions alternate
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
   L.part = take(B * ntiles * sizeof(float4));

@@ -60,13 +60,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = 128;                   // accumulators after the E columns
 
 struct Params {
-  int B, G, V, r, k, ntiles, ctas_per_m;
-  const __nv_bfloat16* E;  // [B, r] W1 rows of position k
+  int B, G, V, r, H, k, ntiles, nparts, ctas_per_m;
+  const __nv_bfloat16* W1;   // [V, r]
+  const __nv_bfloat16* w;    // [H + r] confidence weight (w_e = w + H)
+  const float* zh;           // [B, G] w_h . h
+  const int32_t* anchor;     // [B]
   const float* temp;
-  const float2* rowstat;
-  const int32_t* tokens;
-  float4* part;
+  const float2* rowstat;     // [B] (m, S) of position k (pass 2)
+  const float4* sel;         // [B] crossing chunk, prefix, target, hit (pass 2)
+  int32_t* tokens;           // [B, G]
+  float4* part;              // [B, nparts] per 64-column chunk (pass 1)
   float* pd_tok;
+  float* conf_logit;
+  float* conf;
   WsHeader* hdr;
 };
 
@@ -230,8 +236,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool vrow = b < p.B;
     const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
     if (g == 0) {
-      // E rows into TMEM columns [0, r/2): two bf16 per column, zeros past B
-      const uint4* src = reinterpret_cast<const uint4*>(p.E + (size_t)b * r);
+      // E = W1[x_{k-1}] (x_0 = anchor) into TMEM columns [0, r/2): two bf16 per
+      // column, zeros past B.  Pass 1 on the first CTA of the M-tile also forms
+      // the confidence of position k: z = w_h . h_k + w_e . W1[x_{k-1}].
+      int x = 0;
+      if (vrow) {
+        x = (p.k == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + p.k - 1];
+        if (x < 0 || x >= p.V) {
+          report_error(p.hdr, DSPARK_BAD_INPUT, x);
+          x = 0;
+        }
+      }
+      const bool do_conf = !WRITE && vrow && n_lo == 0;
+      const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r);
+      const uint4* wsrc = reinterpret_cast<const uint4*>(p.w + p.H);
+      float zacc = 0.f;
       for (int c0 = 0; c0 < r / 64; ++c0) {
         uint32_t wv[32];
 #pragma unroll
@@ -241,8 +260,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           wv[4 * e + 1] = qv.y;
           wv[4 * e + 2] = qv.z;
           wv[4 * e + 3] = qv.w;
+          if (do_conf) {
+            const uint4 we = wsrc[c0 * 8 + e];
+            const __nv_bfloat162* ev = reinterpret_cast<const __nv_bfloat162*>(&qv);
+            const __nv_bfloat162* wwv = reinterpret_cast<const __nv_bfloat162*>(&we);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 fe = __bfloat1622float2(ev[t]), fw = __bfloat1622float2(wwv[t]);
+              zacc = fmaf(fw.x, fe.x, zacc);
+              zacc = fmaf(fw.y, fe.y, zacc);
+            }
+          }
         }
         ptx::tmem_st32(tmem + lane_bits + (uint32_t)(c0 * 32), wv);
+      }
+      if (do_conf) {
+        const float z = p.zh[(size_t)b * p.G + p.k] + zacc;
+        p.conf_logit[(size_t)b * p.G + p.k] = z;
+        p.conf[(size_t)b * p.G + p.k] = 1.f / (1.f + expf(-z));
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -254,12 +289,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool sampled = T_ > 0.f;
     const float c = row_scale(T_);
     float rm = 0.f, rinvS = 1.f;
-    int xb = -1;
+    int xb = -1;          // greedy rows: the token chosen by the select kernel
+    int cstar = -1;       // sampled rows: the 64-column chunk that holds the draw
+    float sbase = 0.f, starget = 0.f;
+    bool shit = false;
     if (WRITE && vrow) {
       const float2 st = p.rowstat[b];
       rm = st.x;
       rinvS = inv_sum(st.y);
-      xb = p.tokens[(size_t)b * p.G + p.k];
+      if (sampled) {
+        const float4 sv = p.sel[b];
+        cstar = __float_as_int(sv.x);
+        sbase = sv.y;
+        starget = sv.z;
+        shit = __float_as_int(sv.w) != 0;
+      } else {
+        xb = p.tokens[(size_t)b * p.G + p.k];
+      }
     }
     uint8_t* stg = sStg + (warp - kEpiWarp0) * kStagingPerWarp;
     float pdtok = 0.f;
@@ -273,9 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      // pass 1: running (max, sum) of y over the tile, argmax of l (greedy rows)
-      float tm = -INFINITY, ts = 0.f, av = -INFINITY;
-      int ai = INT_MAX;
       bool broke = false;
       for (int ch = 0; ch < NCH; ++ch) {
         const int v0 = n * BN + ch * CW;
@@ -331,12 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx[j & 3] = fmaxf(mx[j & 3], acc[j]);
           }
           const float mc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          if (mc > -INFINITY) {
-            float sm[4] = {0.f, 0.f, 0.f, 0.f};
+          float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mc);
-            lse_merge(tm, ts, mc, (sm[0] + sm[1]) + (sm[2] + sm[3]));
-          }
+          for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mc);
+          float av = -INFINITY;
+          int ai = INT_MAX;
           if (!sampled) {
             // greedy: argmax of y = l, ties to the lowest column
 #pragma unroll
@@ -346,7 +388,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ai = v0 + j;
               }
           }
+          // one partial per 64-column chunk: (max y, sum 2^(y - max), argmax)
+          if (vrow && v0 < p.V)
+            p.part[(size_t)b * p.nparts + v0 / CW] =
+                make_float4(mc, (sm[0] + sm[1]) + (sm[2] + sm[3]), av, __int_as_float(ai));
         } else {
+          // numerators w = 2^(y - m) (sampled rows), then the draw: the row's
+          // select kernel named the chunk where the prefix sum of w crosses
+          // u S and the sum before it; the thread walks that chunk in token
+          // order with exactly the values it writes.  Rounding that leaves no
+          // crossing picks the chunk's last token with positive weight.
+          if (sampled) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = (j < nvalid) ? exp_shifted(scale_logit(acc[j], c), rm) : 0.f;
+          }
+          if (v0 / CW == cstar) {
+            float run = sbase, pf = 0.f, pl = 0.f;
+            int xf = -1, xl = -1;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              const float wj = acc[j];
+              if (wj > 0.f) {
+                xl = v0 + j;
+                pl = wj;
+              }
+              run += wj;
+              if (xf < 0 && shit && run > starget) {
+                xf = v0 + j;
+                pf = wj;
+              }
+            }
+            if (xf < 0) {
+              xf = xl;
+              pf = pl;
+            }
+            if (xf >= 0) {
+              p.tokens[(size_t)b * p.G + p.k] = xf;
+              pdtok = __fmul_rn(pf, rinvS);
+              have_pdtok = true;
+            }
+          }
           // the previous chunk's TMA stores must have read the staging buffer
           if (lane == 0) ptx::bulk_wait_read0();
           __syncwarp();
@@ -358,8 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int j = 32 * h + 4 * cc + e;
-                const float pr =
-                    sampled ? prob_from(scale_logit(acc[j], c), rm, rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
+                const float pr = sampled ? __fmul_rn(acc[j], rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
                 if (v0 + j == xb) {
                   pdtok = pr;
                   have_pdtok = true;
@@ -383,7 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (broke) break;
-      if (!WRITE && vrow) p.part[(size_t)b * p.ntiles + n] = make_float4(tm, ts, av, __int_as_float(ai));
     }
     if (WRITE) {
       if (vrow && have_pdtok) p.pd_tok[(size_t)b * p.G + p.k] = pdtok;
@@ -469,11 +548,13 @@ bool draft_tc_supported(const dspark_dims& d) {
     forced = (e && std::string(e) == "cuda_core") ? 0 : 1;
   });
   if (!forced) return false;
-  if (d.dtype != DSPARK_BF16 || d.r < 64 || d.r > 256 || (d.r % 64) != 0 || (d.V % 8) != 0) return false;
+  if (d.dtype != DSPARK_BF16 || d.r < 64 || d.r > 256 || (d.r % 64) != 0 || (d.V % 8) != 0 || (d.H % 8) != 0)
+    return false;
   return tc::dev_info().sm103 && tc::encode_fn() != nullptr;
 }
 
-int draft_tc_tile_width() { return tc::BN; }
+// vocabulary columns summarised by one partial of the tensor-core pass 1
+int draft_tc_tile_width() { return tc::CW; }
 
 cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, TcMaps* maps) {
   const dspark_dims& d = a.dims;
@@ -519,17 +600,25 @@ cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const 
   p.G = d.gamma;
   p.V = d.V;
   p.r = d.r;
+  p.H = d.H;
   p.k = k;
   p.ntiles = (d.V + tc::BN - 1) / tc::BN;
+  p.nparts = (d.V + tc::CW - 1) / tc::CW;
   const int n_mtiles = (d.B + tc::BM - 1) / tc::BM;
   const int sms = tc::dev_info().sms > 0 ? tc::dev_info().sms : 148;
   p.ctas_per_m = max(1, min(p.ntiles, sms / n_mtiles));
-  p.E = reinterpret_cast<const __nv_bfloat16*>(ws + L.E) + (size_t)(k & 1) * d.B * d.r;
+  p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  p.w = static_cast<const __nv_bfloat16*>(a.w);
+  p.zh = reinterpret_cast<const float*>(ws + L.zh);
+  p.anchor = a.anchor;
   p.temp = a.temp;
   p.rowstat = reinterpret_cast<const float2*>(ws + L.rowstat);
+  p.sel = reinterpret_cast<const float4*>(ws + L.sel);
   p.tokens = a.tokens;
   p.part = reinterpret_cast<float4*>(ws + L.part);
   p.pd_tok = a.pd_tok;
+  p.conf_logit = a.conf_logit;
+  p.conf = a.conf;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   const dim3 grid(n_mtiles * p.ctas_per_m);
   const size_t smem = tc::smem_bytes(write);

@@ -23,6 +23,7 @@ struct WsLayout {
   size_t E = 0;        // [2][B*r] dtype: W1 rows of the previous tokens, two alternating buffers
   size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index)
   size_t rowstat = 0;  // [B] float2: (row max, row sum) of the current position
+  size_t sel = 0;      // [B] float4: crossing chunk, prefix before it, target, hit (tensor-core path)
   size_t sk0 = 0, sk1 = 0, sv0 = 0, sv1 = 0;  // scheduler sort buffers [B*G] u32
   size_t vrs = 0;      // [B*(G+1)*RS_PARTS] float4: verify row-slice statistics
   size_t total = 0;
