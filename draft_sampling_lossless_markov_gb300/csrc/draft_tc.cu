@@ -18,13 +18,13 @@
 //   warp 1    allocates TMEM, issues tcgen05.mma (A = E from TMEM, B = W2
 //             K-chunk from shared memory, MN-major, N = 192) into one of the
 //             two accumulators, commits to mbarriers
-//   warps 2-9 epilogue, two groups of four warps (one per TMEM lane quarter)
-//             on alternate tiles, one accumulator each.  Group 0 first copies
-//             the E rows into TMEM.  Per tile and 64-column chunk: TMEM ->
-//             registers, + U, then either the tile's running (max, sum, argmax)
-//             partial (pass 1) or the probability row p_d = 2^(y - m) / S
-//             written through a per-warp swizzled staging buffer with TMA
-//             stores (pass 2)
+//   warps 2-13 epilogue, three groups of four warps (one per TMEM lane
+//             quarter); group g owns the g-th 64-column chunk of every tile, so
+//             all three work on a tile at once.  Group 0 first copies the E
+//             rows into TMEM.  Per tile: TMEM -> registers, + U, then either
+//             the chunk's (max, sum, argmax) partial (pass 1) or the
+//             probability row p_d = 2^(y - m) / S written through a per-warp
+//             swizzled staging buffer with TMA stores (pass 2)
 //
 // A CTA owns one 128-row M-tile; the vocabulary tiles of an M-tile are dealt
 // round-robin to its CTAs.  Every mbarrier wait gives up after two seconds: the
@@ -50,9 +50,11 @@ constexpr int BN = 192;                              // vocabulary columns per t
 constexpr int CW = 64;                               // columns per swizzle atom / chunk
 constexpr int NCH = BN / CW;                         // chunks per tile
 constexpr int KC = 64;                               // W2 rows per K-chunk
-constexpr int kThreads = 64 + 2 * 128;               // producer, MMA, two epilogue groups
+constexpr int kGroups = NCH;                         // epilogue groups: group g owns chunk g of every tile
+constexpr int kThreads = 64 + kGroups * 128;         // producer, MMA, epilogue
+constexpr int kEpiWarps = kGroups * 4;
 constexpr int kEpiWarp0 = 2;
-constexpr int kStagingPerWarp = 32 * CW * 4;         // [32 rows x 64 cols] fp32
+constexpr int kStagingPerWarp = 32 * 32 * 4;         // [32 rows x 32 cols] fp32
 constexpr uint32_t kW2Stage = KC * BN * 2;           // 24 KB
 constexpr uint32_t kUStage = BM * CW * 2;            // 16 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -77,10 +79,10 @@ struct Params {
 };
 
 __host__ __device__ constexpr int w2_stages(bool write) { return write ? 3 : 4; }
-__host__ __device__ constexpr int u_stages(bool write) { return write ? 4 : 6; }
+__host__ __device__ constexpr int u_stages(bool write) { return write ? 5 : 6; }
 
 __host__ __device__ inline size_t smem_bytes(bool write) {
-  const size_t staging = write ? (size_t)8 * kStagingPerWarp : 0;
+  const size_t staging = write ? (size_t)kEpiWarps * kStagingPerWarp : 0;
   return 1024 + w2_stages(write) * (size_t)kW2Stage + u_stages(write) * (size_t)kUStage + staging + 512;
 }
 
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sW = smem;
   uint8_t* sU = sW + NW * kW2Stage;
   uint8_t* sStg = sU + NU * kUStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + (WRITE ? 8 * kStagingPerWarp : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + (WRITE ? kEpiWarps * kStagingPerWarp : 0));
   uint64_t* fullW = bars;
   uint64_t* emptyW = fullW + NW;
   uint64_t* fullU = emptyW + NW;
@@ -110,10 +112,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x / p.ctas_per_m;
-  // vocabulary tiles of this M-tile are dealt round-robin: tile n_lo + i * stride
+  // vocabulary tiles of this M-tile are dealt round-robin, so that all CTAs
+  // sweep the vocabulary together.  Pass 1 sweeps it upward and pass 2
+  // downward: pass 2 then starts on the tiles pass 1 touched last, whose U and
+  // W2 lines are the likeliest to still be in L2 (the next position's pass 1
+  // again starts where pass 2 ended).
   const int n_lo = blockIdx.x % p.ctas_per_m;
   const int stride = p.ctas_per_m;
   const int count = n_lo < p.ntiles ? (p.ntiles - n_lo + stride - 1) / stride : 0;
+  auto tile_of = [&](int i) { return n_lo + (WRITE ? count - 1 - i : i) * stride; };
   const int row_base = m_tile * BM;
 
   if (threadIdx.x == 0) {
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 4);
+      ptx::mbar_init(&tempty[a], kEpiWarps);
     }
     ptx::mbar_init(eready, 4);
     *abort_flag = 0;
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int iw = 0, iu = 0;  // items issued into each ring
       bool ok = true;
       for (int i = 0; i < count && ok; ++i) {
-        const int v0 = (n_lo + i * stride) * BN;
+        const int v0 = tile_of(i) * BN;
         for (int kc = 0; kc < nkc && ok; ++kc, ++iw) {
           const int s = iw % NW;
           if (!ptx::mbar_wait(&emptyW[s], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
@@ -310,159 +317,151 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stg = sStg + (warp - kEpiWarp0) * kStagingPerWarp;
     float pdtok = 0.f;
     bool have_pdtok = false;
-    for (int i = g; i < count; i += 2) {
-      const int a = i & 1;  // == g
-      const int n = n_lo + i * stride;
+    const int ch = g;  // the chunk of every tile this group owns
+    for (int i = 0; i < count; ++i) {
+      const int a = i & 1;
+      const int n = tile_of(i);
+      const int v0 = n * BN + ch * CW;
       bool ok = ptx::mbar_wait(&tfull[a], (i >> 1) & 1, abort_flag, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) fail();
         break;
       }
       ptx::tc_fence_after();
-      bool broke = false;
-      for (int ch = 0; ch < NCH; ++ch) {
-        const int v0 = n * BN + ch * CW;
-        float acc[64];
-        {
-          float h0[32], h1[32];
-          const uint32_t ta = tmem + lane_bits + kAccCol0 + (uint32_t)(a * BN + ch * CW);
-          ptx::tmem_ld32(ta, h0);
-          ptx::tmem_ld32(ta + 32, h1);
-          ptx::tmem_ld_wait();
+      float acc[64];
+      {
+        float h0[32], h1[32];
+        const uint32_t ta = tmem + lane_bits + kAccCol0 + (uint32_t)(a * BN + ch * CW);
+        ptx::tmem_ld32(ta, h0);
+        ptx::tmem_ld32(ta + 32, h1);
+        ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            acc[j] = h0[j];
-            acc[32 + j] = h1[j];
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = h0[j];
+          acc[32 + j] = h1[j];
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[a]);
+      const int iu = i * NCH + ch, su = iu % NU;
+      ok = ptx::mbar_wait(&fullU[su], (iu / NU) & 1, abort_flag, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) fail();
+        break;
+      }
+      {
+        // U row of this thread: 8 swizzled 16-byte chunks of 8 bf16
+        const uint8_t* su_row = sU + su * kUStage + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((cc ^ (row & 7)) << 4));
+          const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(bp[e]);
+            acc[8 * cc + 2 * e] = add_base(f.x, acc[8 * cc + 2 * e]);
+            acc[8 * cc + 2 * e + 1] = add_base(f.y, acc[8 * cc + 2 * e + 1]);
           }
         }
-        if (ch == NCH - 1) {  // the accumulator is free for the tile after next
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&tempty[a]);
-        }
-        const int iu = i * NCH + ch, su = iu % NU;
-        ok = ptx::mbar_wait(&fullU[su], (iu / NU) & 1, abort_flag, kWaitLimitNs);
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0) fail();
-          broke = true;
-          break;
-        }
-        {
-          // U row of this thread: 8 swizzled 16-byte chunks of 8 bf16
-          const uint8_t* su_row = sU + su * kUStage + row * 128;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
+      // acc[j] now holds the logit l of column v0 + j; columns past V are masked
+      const int nvalid = min(CW, p.V - v0);
+      if (!WRITE) {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((cc ^ (row & 7)) << 4));
-            const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
+        for (int j = 0; j < 64; ++j) {
+          acc[j] = (j < nvalid) ? scale_logit(acc[j], c) : -INFINITY;  // y = l c (greedy rows: c = 1)
+          mx[j & 3] = fmaxf(mx[j & 3], acc[j]);
+        }
+        const float mc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(bp[e]);
-              acc[8 * cc + 2 * e] = add_base(f.x, acc[8 * cc + 2 * e]);
-              acc[8 * cc + 2 * e + 1] = add_base(f.y, acc[8 * cc + 2 * e + 1]);
+        for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mc);
+        float av = -INFINITY;
+        int ai = INT_MAX;
+        if (!sampled) {
+          // greedy: argmax of y = l, ties to the lowest column
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (acc[j] > av) {
+              av = acc[j];
+              ai = v0 + j;
             }
-          }
         }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
-        // acc[j] now holds the logit l of column v0 + j; columns past V are masked
-        const int nvalid = min(CW, p.V - v0);
-        if (!WRITE) {
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // one partial per 64-column chunk: (max y, sum 2^(y - max), argmax)
+        if (vrow && v0 < p.V)
+          p.part[(size_t)b * p.nparts + v0 / CW] =
+              make_float4(mc, (sm[0] + sm[1]) + (sm[2] + sm[3]), av, __int_as_float(ai));
+      } else {
+        // numerators w = 2^(y - m) (sampled rows), then the draw: the row's
+        // select kernel named the chunk where the prefix sum of w crosses u S
+        // and the sum before it; the thread walks that chunk in token order
+        // with exactly the values it writes.  Rounding that leaves no crossing
+        // picks the chunk's last token with positive weight.
+        if (sampled) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) acc[j] = (j < nvalid) ? exp_shifted(scale_logit(acc[j], c), rm) : 0.f;
+        }
+        if (v0 / CW == cstar) {
+          float run = sbase, pf = 0.f, pl = 0.f;
+          int xf = -1, xl = -1;
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
-            acc[j] = (j < nvalid) ? scale_logit(acc[j], c) : -INFINITY;  // y = l c (greedy rows: c = 1)
-            mx[j & 3] = fmaxf(mx[j & 3], acc[j]);
-          }
-          const float mc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < 64; ++j) sm[j & 3] += exp_shifted(acc[j], mc);
-          float av = -INFINITY;
-          int ai = INT_MAX;
-          if (!sampled) {
-            // greedy: argmax of y = l, ties to the lowest column
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (acc[j] > av) {
-                av = acc[j];
-                ai = v0 + j;
-              }
-          }
-          // one partial per 64-column chunk: (max y, sum 2^(y - max), argmax)
-          if (vrow && v0 < p.V)
-            p.part[(size_t)b * p.nparts + v0 / CW] =
-                make_float4(mc, (sm[0] + sm[1]) + (sm[2] + sm[3]), av, __int_as_float(ai));
-        } else {
-          // numerators w = 2^(y - m) (sampled rows), then the draw: the row's
-          // select kernel named the chunk where the prefix sum of w crosses
-          // u S and the sum before it; the thread walks that chunk in token
-          // order with exactly the values it writes.  Rounding that leaves no
-          // crossing picks the chunk's last token with positive weight.
-          if (sampled) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = (j < nvalid) ? exp_shifted(scale_logit(acc[j], c), rm) : 0.f;
-          }
-          if (v0 / CW == cstar) {
-            float run = sbase, pf = 0.f, pl = 0.f;
-            int xf = -1, xl = -1;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const float wj = acc[j];
-              if (wj > 0.f) {
-                xl = v0 + j;
-                pl = wj;
-              }
-              run += wj;
-              if (xf < 0 && shit && run > starget) {
-                xf = v0 + j;
-                pf = wj;
-              }
+            const float wj = acc[j];
+            if (wj > 0.f) {
+              xl = v0 + j;
+              pl = wj;
             }
-            if (xf < 0) {
-              xf = xl;
-              pf = pl;
-            }
-            if (xf >= 0) {
-              p.tokens[(size_t)b * p.G + p.k] = xf;
-              pdtok = __fmul_rn(pf, rinvS);
-              have_pdtok = true;
+            run += wj;
+            if (xf < 0 && shit && run > starget) {
+              xf = v0 + j;
+              pf = wj;
             }
           }
-          // the previous chunk's TMA stores must have read the staging buffer
+          if (xf < 0) {
+            xf = xl;
+            pf = pl;
+          }
+          if (xf >= 0) {
+            p.tokens[(size_t)b * p.G + p.k] = xf;
+            pdtok = __fmul_rn(pf, rinvS);
+            have_pdtok = true;
+          }
+        }
+        const int row0 = row_base + q * 32;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // the previous TMA store must have read the staging buffer
           if (lane == 0) ptx::bulk_wait_read0();
           __syncwarp();
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int cc = 0; cc < 8; ++cc) {
+            float pv[4];
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              float pv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int j = 32 * h + 4 * cc + e;
-                const float pr = sampled ? __fmul_rn(acc[j], rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
-                if (v0 + j == xb) {
-                  pdtok = pr;
-                  have_pdtok = true;
-                }
-                pv[e] = pr;
+            for (int e = 0; e < 4; ++e) {
+              const int j = 32 * h + 4 * cc + e;
+              const float pr = sampled ? __fmul_rn(acc[j], rinvS) : ((v0 + j == xb) ? 1.f : 0.f);
+              if (v0 + j == xb) {
+                pdtok = pr;
+                have_pdtok = true;
               }
-              *reinterpret_cast<float4*>(stg + h * 4096 + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
-                  make_float4(pv[0], pv[1], pv[2], pv[3]);
+              pv[e] = pr;
             }
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                make_float4(pv[0], pv[1], pv[2], pv[3]);
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
-          const int row0 = row_base + q * 32;
-          if (lane == 0 && row0 < p.B && v0 < p.V) {  // boxes that start past B or V would write nothing
+          if (lane == 0 && row0 < p.B && v0 + 32 * h < p.V) {  // boxes that start past B or V would write nothing
             // p_d is streamed out: evict-first keeps the re-read W2 in L2
-            const uint64_t pol = ptx::policy_evict_first();
-            ptx::tma_store_3d(&tmPd, stg, v0, p.k, row0, pol);
-            if (v0 + 32 < p.V) ptx::tma_store_3d(&tmPd, stg + 4096, v0 + 32, p.k, row0, pol);
+            ptx::tma_store_3d(&tmPd, stg, v0 + 32 * h, p.k, row0, ptx::policy_evict_first());
             ptx::bulk_commit();
           }
         }
       }
-      if (broke) break;
     }
     if (WRITE) {
       if (vrow && have_pdtok) p.pd_tok[(size_t)b * p.G + p.k] = pdtok;
