@@ -438,13 +438,13 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
 __global__ void __launch_bounds__(SEL_THREADS) k_select_tc(const float4* __restrict__ part, int nparts,
                                                            const float* __restrict__ temp,
                                                            const uint32_t* __restrict__ req_id, uint64_t seed, int G,
-                                                           int k, int32_t* __restrict__ tokens,
+                                                           int k, int b0, int32_t* __restrict__ tokens,
                                                            float2* __restrict__ rowstat, float4* __restrict__ sel) {
   __shared__ float sm[32];
   __shared__ int s_int[2];
   __shared__ float s_flt[2];
   __shared__ int sai[SEL_THREADS / 32];
-  const int b = blockIdx.x;
+  const int b = b0 + (int)blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const float4* P = part + (size_t)b * nparts;
   const bool sampled = temp[b] > 0.f;
@@ -549,13 +549,21 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     if (e != cudaSuccess) return e;
     const int nparts = (V + draft_tc_tile_width() - 1) / draft_tc_tile_width();
     float4* sel = reinterpret_cast<float4*>(ws + L.sel);
-    count_launches(1 + 3 * G);
+    const int n_mtiles = (B + 127) / 128;
+    const int slab = draft_tc_slab_mtiles(d);
+    const int nslabs = (n_mtiles + slab - 1) / slab;
+    count_launches(1 + 3 * G * nslabs);
     for (int k = 0; k < G; ++k) {
-      e = launch_draft_tc_pass(a, ws, L, maps, k, false, s);
-      if (e != cudaSuccess) return e;
-      k_select_tc<<<B, SEL_THREADS, 0, s>>>(part, nparts, a.temp, a.req_id, a.seed, G, k, a.tokens, rowstat, sel);
-      e = launch_draft_tc_pass(a, ws, L, maps, k, true, s);
-      if (e != cudaSuccess) return e;
+      for (int m0 = 0; m0 < n_mtiles; m0 += slab) {
+        const int mc = min(slab, n_mtiles - m0);
+        const int b0 = m0 * 128, nb = min(B - b0, mc * 128);
+        e = launch_draft_tc_pass(a, ws, L, maps, k, false, m0, mc, nslabs > 1, s);
+        if (e != cudaSuccess) return e;
+        k_select_tc<<<nb, SEL_THREADS, 0, s>>>(part, nparts, a.temp, a.req_id, a.seed, G, k, b0, a.tokens, rowstat,
+                                               sel);
+        e = launch_draft_tc_pass(a, ws, L, maps, k, true, m0, mc, false, s);
+        if (e != cudaSuccess) return e;
+      }
     }
     return cudaGetLastError();
   }

@@ -20,7 +20,7 @@
 //             two accumulators, commits to mbarriers
 //   warps 2-13 epilogue, three groups of four warps (one per TMEM lane
 //             quarter); group g owns the g-th 64-column chunk of every tile, so
-//             all three work on a tile at once.  Group 0 first copies the E
+//             all three work on a tile at once.  The groups first copy the E
 //             rows into TMEM.  Per tile: TMEM -> registers, + U, then either
 //             the chunk's (max, sum, argmax) partial (pass 1) or the
 //             probability row p_d = 2^(y - m) / S written through a per-warp
@@ -63,6 +63,8 @@ constexpr uint32_t kAccCol0 = 128;                   // accumulators after the E
 
 struct Params {
   int B, G, V, r, H, k, ntiles, nparts, ctas_per_m;
+  int m_first;   // first M-tile of this launch
+  int u_keep;    // pass 1 loads U evict-last: pass 2 of the same rows follows at once
   const __nv_bfloat16* W1;   // [V, r]
   const __nv_bfloat16* w;    // [H + r] confidence weight (w_e = w + H)
   const float* zh;           // [B, G] w_h . h
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x / p.ctas_per_m;
+  const int m_tile = p.m_first + (int)blockIdx.x / p.ctas_per_m;
   // vocabulary tiles of this M-tile are dealt round-robin, so that all CTAs
   // sweep the vocabulary together.  Pass 1 sweeps it upward and pass 2
   // downward: pass 2 then starts on the tiles pass 1 touched last, whose U and
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], kEpiWarps);
     }
-    ptx::mbar_init(eready, 4);
+    ptx::mbar_init(eready, kEpiWarps);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_last = ptx::policy_evict_last();
       const uint64_t pol_first = ptx::policy_evict_first();
+      const uint64_t pol_u = (!WRITE && p.u_keep) ? pol_last : pol_first;
       int iw = 0, iu = 0;  // items issued into each ring
       bool ok = true;
       for (int i = 0; i < count && ok; ++i) {
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::mbar_expect_tx(&fullU[s], kUStage);
-          ptx::tma_load_3d(sU + s * kUStage, &tmU, &fullU[s], v0 + c * CW, p.k, row_base, pol_first);
+          ptx::tma_load_3d(sU + s * kUStage, &tmU, &fullU[s], v0 + c * CW, p.k, row_base, pol_u);
         }
       }
       if (!ok) fail();
@@ -242,54 +245,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = row_base + row;
     const bool vrow = b < p.B;
     const uint32_t lane_bits = (uint32_t)(q * 32) << 16;
-    if (g == 0) {
+    const int npieces = r / 64;  // 64-element pieces of an E row (32 TMEM columns each)
+    {
       // E = W1[x_{k-1}] (x_0 = anchor) into TMEM columns [0, r/2): two bf16 per
-      // column, zeros past B.  Pass 1 on the first CTA of the M-tile also forms
-      // the confidence of position k: z = w_h . h_k + w_e . W1[x_{k-1}].
+      // column, zeros past B.  Group g copies pieces g and g + 3 of its rows, so
+      // every load of a row is in flight at once before the first MMA may start.
       int x = 0;
       if (vrow) {
         x = (p.k == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + p.k - 1];
         if (x < 0 || x >= p.V) {
-          report_error(p.hdr, DSPARK_BAD_INPUT, x);
+          if (g == 0) report_error(p.hdr, DSPARK_BAD_INPUT, x);
           x = 0;
         }
       }
-      const bool do_conf = !WRITE && vrow && n_lo == 0;
       const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r);
-      const uint4* wsrc = reinterpret_cast<const uint4*>(p.w + p.H);
-      float zacc = 0.f;
-      for (int c0 = 0; c0 < r / 64; ++c0) {
-        uint32_t wv[32];
+      uint32_t wv[2][32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint4 qv = vrow ? src[c0 * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
-          wv[4 * e] = qv.x;
-          wv[4 * e + 1] = qv.y;
-          wv[4 * e + 2] = qv.z;
-          wv[4 * e + 3] = qv.w;
-          if (do_conf) {
-            const uint4 we = wsrc[c0 * 8 + e];
-            const __nv_bfloat162* ev = reinterpret_cast<const __nv_bfloat162*>(&qv);
-            const __nv_bfloat162* wwv = reinterpret_cast<const __nv_bfloat162*>(&we);
+      for (int s = 0; s < 2; ++s) {
+        const int pc = g + kGroups * s;
+        if (pc < npieces) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float2 fe = __bfloat1622float2(ev[t]), fw = __bfloat1622float2(wwv[t]);
-              zacc = fmaf(fw.x, fe.x, zacc);
-              zacc = fmaf(fw.y, fe.y, zacc);
-            }
+          for (int e = 0; e < 8; ++e) {
+            const uint4 qv = vrow ? src[pc * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
+            wv[s][4 * e] = qv.x;
+            wv[s][4 * e + 1] = qv.y;
+            wv[s][4 * e + 2] = qv.z;
+            wv[s][4 * e + 3] = qv.w;
           }
         }
-        ptx::tmem_st32(tmem + lane_bits + (uint32_t)(c0 * 32), wv);
       }
-      if (do_conf) {
-        const float z = p.zh[(size_t)b * p.G + p.k] + zacc;
-        p.conf_logit[(size_t)b * p.G + p.k] = z;
-        p.conf[(size_t)b * p.G + p.k] = 1.f / (1.f + expf(-z));
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int pc = g + kGroups * s;
+        if (pc < npieces) ptx::tmem_st32(tmem + lane_bits + (uint32_t)(pc * 32), wv[s]);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(eready);
+    }
+    if (!WRITE && g == 0 && n_lo == 0) {
+      // pass 1 on the first CTA of the M-tile also forms the confidence of
+      // position k: z = w_h . h_k + w_e . W1[x_{k-1}], reading the E row back
+      // from TMEM once every group has stored its pieces
+      bool ok = ptx::mbar_wait(eready, 0, abort_flag, kWaitLimitNs);
+      if (__all_sync(0xffffffffu, ok)) {
+        ptx::tc_fence_after();
+        const uint4* wsrc = reinterpret_cast<const uint4*>(p.w + p.H);
+        float zacc = 0.f;
+        for (int pc = 0; pc < npieces; ++pc) {
+          float ev[32];  // bf16 pairs, as raw bits
+          ptx::tmem_ld32(tmem + lane_bits + (uint32_t)(pc * 32), ev);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint4 we = wsrc[pc * 8 + e];
+            const uint32_t wq[4] = {we.x, we.y, we.z, we.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const uint32_t eb = __float_as_uint(ev[4 * e + t]);
+              const float2 fe = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&eb));
+              const float2 fw = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[t]));
+              zacc = fmaf(fw.x, fe.x, zacc);
+              zacc = fmaf(fw.y, fe.y, zacc);
+            }
+          }
+        }
+        if (vrow) {
+          const float z = p.zh[(size_t)b * p.G + p.k] + zacc;
+          p.conf_logit[(size_t)b * p.G + p.k] = z;
+          p.conf[(size_t)b * p.G + p.k] = 1.f / (1.f + expf(-z));
+        }
+      } else if (lane == 0) {
+        fail();
+      }
     }
 
     const float T_ = vrow ? p.temp[b] : 1.f;
@@ -511,6 +540,7 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
 
 struct DevInfo {
   int sms = 0;
+  int l2_bytes = 0;
   bool sm103 = false;
 };
 
@@ -526,6 +556,7 @@ static DevInfo dev_info() {
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&cache[dev].l2_bytes, cudaDevAttrL2CacheSize, dev);
     cache[dev].sms = sms;
     cache[dev].sm103 = (major == 10 && minor == 3);
     have[dev] = true;
@@ -591,8 +622,31 @@ cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLa
   return attr_err;
 }
 
+// M-tiles per slab.  The passes of one position run slab by slab (pass 1,
+// select, pass 2 of the slab's rows, then the next slab) when a slab's U rows
+// and all of W2 fit in about a third of L2: pass 2 then finds both there and
+// reads HBM only for the p_d rows it writes.  (On GB300 a buffer read again
+// after one pass is found in L2 only up to about 48 MB, and not at all once a
+// stream of p_d writes has passed through, whatever the eviction hints.)
+// Otherwise a single slab covers the whole batch.  DSPARK_TC_SLAB=<n> forces
+// n M-tiles per slab.
+int draft_tc_slab_mtiles(const dspark_dims& d) {
+  static int forced = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* e = getenv("DSPARK_TC_SLAB");
+    forced = e ? atoi(e) : -1;
+  });
+  const int n_mtiles = (d.B + tc::BM - 1) / tc::BM;
+  if (forced > 0) return min(forced, n_mtiles);
+  const double w2 = 2.0 * d.r * d.V, u_tile = 2.0 * tc::BM * d.V;
+  const double budget = 0.35 * (double)tc::dev_info().l2_bytes;
+  const int fit = (int)((budget - w2) / u_tile);
+  return fit >= 1 ? min(fit, n_mtiles) : n_mtiles;
+}
+
 cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, const TcMaps& maps,
-                                 int k, bool write, cudaStream_t s) {
+                                 int k, bool write, int m_first, int m_count, bool u_keep, cudaStream_t s) {
   const dspark_dims& d = a.dims;
   tc::Params p;
   p.B = d.B;
@@ -603,9 +657,10 @@ cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const 
   p.k = k;
   p.ntiles = (d.V + tc::BN - 1) / tc::BN;
   p.nparts = (d.V + tc::CW - 1) / tc::CW;
-  const int n_mtiles = (d.B + tc::BM - 1) / tc::BM;
   const int sms = tc::dev_info().sms > 0 ? tc::dev_info().sms : 148;
-  p.ctas_per_m = max(1, min(p.ntiles, sms / n_mtiles));
+  p.ctas_per_m = max(1, min(p.ntiles, sms / m_count));
+  p.m_first = m_first;
+  p.u_keep = u_keep ? 1 : 0;
   p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
   p.w = static_cast<const __nv_bfloat16*>(a.w);
   p.zh = reinterpret_cast<const float*>(ws + L.zh);
@@ -619,7 +674,7 @@ cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const 
   p.conf_logit = a.conf_logit;
   p.conf = a.conf;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  const dim3 grid(n_mtiles * p.ctas_per_m);
+  const dim3 grid(m_count * p.ctas_per_m);
   const size_t smem = tc::smem_bytes(write);
   if (write)
     tc::k_logits_tc<true><<<grid, tc::kThreads, smem, s>>>(maps.U, maps.W2, maps.Pd, p);

@@ -47,7 +47,8 @@ struct TcMaps {
 bool draft_tc_supported(const dspark_dims& d);
 int draft_tc_tile_width();
 cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, TcMaps* maps);
+int draft_tc_slab_mtiles(const dspark_dims& d);
 cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, const TcMaps& maps,
-                                 int k, bool write, cudaStream_t s);
+                                 int k, bool write, int m_first, int m_count, bool u_keep, cudaStream_t s);
 
 }  // namespace dspark
