@@ -33,7 +33,7 @@ DSPARK_MAX_VOCAB = 2097152
 
 EXPORTED = ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
             "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count",
-            "dspark_schedule_noalloc")
+            "dspark_last_cuda_error", "dspark_schedule_noalloc")
 
 
 class dspark_dims(ctypes.Structure):
@@ -91,6 +91,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_version.restype = c_char_p
     lib.dspark_launch_count.argtypes = []
     lib.dspark_launch_count.restype = c_uint64
+    lib.dspark_last_cuda_error.argtypes = []
+    lib.dspark_last_cuda_error.restype = c_int32
     _lib = lib
     return lib
 
@@ -105,6 +107,10 @@ def dspark_version() -> str:
 
 def dspark_launch_count() -> int:
     return int(load().dspark_launch_count())
+
+
+def dspark_last_cuda_error() -> int:
+    return int(load().dspark_last_cuda_error())
 
 
 def dspark_workspace_size(dims: dspark_dims) -> tuple[int, int]:

@@ -49,6 +49,10 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.E = take(2 * B * r * elem_size(d.dtype));  // two buffers: positions alternate
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
   L.part = take(B * ntiles * sizeof(float4));
+  L.segpart = take(B * kDraftMaxSeg * sizeof(float4));
+  // grid-barrier counter, then one pass-2 tile counter per (position, M-tile);
+  // all zeroed by one memset per draft call
+  L.gbar = take(16 + G * ((B + 127) / 128) * sizeof(uint32_t));
   L.total = align_up(off, 256);
   return L;
 }
@@ -62,7 +66,14 @@ static dspark_status check_ws(const dspark_dims& d, void* ws, size_t bytes, WsLa
   return DSPARK_OK;
 }
 
-static dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_CUDA_ERROR; }
+// the CUDA error behind the last DSPARK_CUDA_ERROR returned on this thread
+static thread_local int t_last_cuda_error = 0;
+
+static dspark_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DSPARK_OK;
+  t_last_cuda_error = (int)e;
+  return DSPARK_CUDA_ERROR;
+}
 
 }  // namespace dspark
 
@@ -85,6 +96,8 @@ const char* dspark_status_string(dspark_status s) {
 const char* dspark_version(void) { return "dspark-gb300 0.1 (sm_103a)"; }
 
 uint64_t dspark_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int dspark_last_cuda_error(void) { return t_last_cuda_error; }
 
 dspark_status dspark_workspace_size(const dspark_dims* dims, size_t* bytes) {
   if (!dims || !bytes || !dims_ok(*dims)) return DSPARK_INVALID_ARG;

@@ -429,97 +429,6 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
   embed_next(s_int[4], b, k, W1, w, zh, Enext, conf_logit, conf, G, r, H);
 }
 
-// Tensor-core path: the select kernel only locates the draw.  From the
-// per-chunk partials (64 columns each) it forms m, S and the prefix sums of
-// the chunk masses in token order, and records the chunk where the prefix
-// first exceeds u S, the sum before that chunk and the target u S; the write
-// pass, which recomputes those logits on the tensor cores anyway, then walks
-// that one chunk and picks the token.  Greedy rows take the argmax here.
-__global__ void __launch_bounds__(SEL_THREADS) k_select_tc(const float4* __restrict__ part, int nparts,
-                                                           const float* __restrict__ temp,
-                                                           const uint32_t* __restrict__ req_id, uint64_t seed, int G,
-                                                           int k, int b0, int32_t* __restrict__ tokens,
-                                                           float2* __restrict__ rowstat, float4* __restrict__ sel) {
-  __shared__ float sm[32];
-  __shared__ int s_int[2];
-  __shared__ float s_flt[2];
-  __shared__ int sai[SEL_THREADS / 32];
-  const int b = b0 + (int)blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const float4* P = part + (size_t)b * nparts;
-  const bool sampled = temp[b] > 0.f;
-
-  if (!sampled) {
-    float av = -INFINITY;
-    int ai = INT_MAX;
-    for (int t = tid; t < nparts; t += SEL_THREADS) argmax_merge(av, ai, P[t].z, __float_as_int(P[t].w));
-    warp_argmax(av, ai);
-    if (lane == 0) {
-      sm[wid] = av;
-      sai[wid] = ai;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float v = sm[0];
-      int i = sai[0];
-      for (int w_ = 1; w_ < SEL_THREADS / 32; ++w_) argmax_merge(v, i, sm[w_], sai[w_]);
-      tokens[(size_t)b * G + k] = i;
-      rowstat[b] = make_float2(0.f, 1.f);
-      sel[b] = make_float4(__int_as_float(-1), 0.f, 0.f, __int_as_float(0));
-    }
-    return;
-  }
-
-  float mx = -INFINITY;
-  for (int t = tid; t < nparts; t += SEL_THREADS) mx = fmaxf(mx, P[t].x);
-  mx = warp_max(mx);
-  if (lane == 0) sm[wid] = mx;
-  __syncthreads();
-  if (tid == 0) {
-    float v = sm[0];
-    for (int w_ = 1; w_ < SEL_THREADS / 32; ++w_) v = fmaxf(v, sm[w_]);
-    s_flt[0] = v;
-  }
-  __syncthreads();
-  const float m = s_flt[0];
-  __syncthreads();
-
-  const int cpt = (nparts + SEL_THREADS - 1) / SEL_THREADS;
-  const int t_lo = min(tid * cpt, nparts), t_hi = min(t_lo + cpt, nparts);
-  float loc = 0.f;
-  for (int t = t_lo; t < t_hi; ++t) loc += tile_mass(P[t].x, P[t].y, m);
-  float S;
-  const float pre = block_excl_scan_256(loc, sm, S);
-  const float u = philox_uniform(seed, req_id[b], (uint32_t)(k + 1), 0u);
-  const float target = u * S;
-  if (tid == 0) {
-    s_int[0] = INT_MAX;
-    s_int[1] = -1;
-  }
-  __syncthreads();
-  {
-    float run = pre;
-    int found = INT_MAX, lastpos = -1;
-    for (int t = t_lo; t < t_hi; ++t) {
-      const float q = tile_mass(P[t].x, P[t].y, m);
-      if (found == INT_MAX && run + q > target) found = t;
-      if (q > 0.f) lastpos = t;
-      run += q;
-    }
-    if (found != INT_MAX) atomicMin(&s_int[0], found);
-    if (lastpos >= 0) atomicMax(&s_int[1], lastpos);
-  }
-  __syncthreads();
-  const bool hit = s_int[0] != INT_MAX;
-  const int cstar = min(max(hit ? s_int[0] : s_int[1], 0), nparts - 1);
-  if (cstar >= t_lo && cstar < t_hi) {
-    float run = pre;
-    for (int t = t_lo; t < cstar; ++t) run += tile_mass(P[t].x, P[t].y, m);
-    rowstat[b] = make_float2(m, S);
-    sel[b] = make_float4(__int_as_float(cstar), run, target, __int_as_float(hit ? 1 : 0));
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Host launcher
 // ---------------------------------------------------------------------------
@@ -542,30 +451,9 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
 
   if (draft_tc_supported(d)) {
-    // tensor-core path: pass 1 (E gather, confidence, chunk partials), select
-    // (locate the draw), pass 2 (p_d, and the token of sampled rows)
-    TcMaps maps;
-    cudaError_t e = draft_tc_prepare(a, ws, L, &maps);
-    if (e != cudaSuccess) return e;
-    const int nparts = (V + draft_tc_tile_width() - 1) / draft_tc_tile_width();
-    float4* sel = reinterpret_cast<float4*>(ws + L.sel);
-    const int n_mtiles = (B + 127) / 128;
-    const int slab = draft_tc_slab_mtiles(d);
-    const int nslabs = (n_mtiles + slab - 1) / slab;
-    count_launches(1 + 3 * G * nslabs);
-    for (int k = 0; k < G; ++k) {
-      for (int m0 = 0; m0 < n_mtiles; m0 += slab) {
-        const int mc = min(slab, n_mtiles - m0);
-        const int b0 = m0 * 128, nb = min(B - b0, mc * 128);
-        e = launch_draft_tc_pass(a, ws, L, maps, k, false, m0, mc, nslabs > 1, s);
-        if (e != cudaSuccess) return e;
-        k_select_tc<<<nb, SEL_THREADS, 0, s>>>(part, nparts, a.temp, a.req_id, a.seed, G, k, b0, a.tokens, rowstat,
-                                               sel);
-        e = launch_draft_tc_pass(a, ws, L, maps, k, true, m0, mc, false, s);
-        if (e != cudaSuccess) return e;
-      }
-    }
-    return cudaGetLastError();
+    // tensor-core path: one persistent kernel for all positions
+    count_launches(1);
+    return launch_draft_tc(a, ws, L, s);
   }
 
   // CUDA-core path

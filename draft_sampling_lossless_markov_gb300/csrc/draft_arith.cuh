@@ -22,10 +22,18 @@ __device__ __forceinline__ float row_scale(float T) { return T > 0.f ? __fmul_rn
 __device__ __forceinline__ float add_base(float u, float bias) { return __fadd_rn(u, bias); }
 // y = l * c
 __device__ __forceinline__ float scale_logit(float l, float c) { return __fmul_rn(l, c); }
+// 2^x by the hardware's approximate base-2 exponential (relative error about
+// 2^-22; results below 2^-126 flush to zero, far under every probability
+// tolerance of the library)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 // 2^(y - m)
-__device__ __forceinline__ float exp_shifted(float y, float m) { return exp2f(__fsub_rn(y, m)); }
+__device__ __forceinline__ float exp_shifted(float y, float m) { return ex2_ftz(__fsub_rn(y, m)); }
 // mass of a tile with partial (m_t, s_t) relative to the row max m
-__device__ __forceinline__ float tile_mass(float mt, float st, float m) { return __fmul_rn(st, exp2f(__fsub_rn(mt, m))); }
+__device__ __forceinline__ float tile_mass(float mt, float st, float m) { return __fmul_rn(st, ex2_ftz(__fsub_rn(mt, m))); }
 // 1 / S
 __device__ __forceinline__ float inv_sum(float S) { return __frcp_rn(S); }
 // p = 2^(y - m) / S, as 2^(y - m) * (1 / S)

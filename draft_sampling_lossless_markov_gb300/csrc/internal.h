@@ -18,12 +18,18 @@ constexpr int kPartialTileMin = 64;
 // Slices per kept row in the verify row statistics.
 constexpr int RS_PARTS = 4;
 
+// Most vocabulary segments (CTAs per M-tile) of the tensor-core draft kernel.
+constexpr int kDraftMaxSeg = 160;
+
 struct WsLayout {
   size_t zh = 0;       // [B*G] f32: w_h . h_k
   size_t E = 0;        // [2][B*r] dtype: W1 rows of the previous tokens, two alternating buffers
   size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index)
   size_t rowstat = 0;  // [B] float2: (row max, row sum) of the current position
   size_t sel = 0;      // [B] float4: crossing chunk, prefix before it, target, hit (tensor-core path)
+  size_t segpart = 0;  // [B*kDraftMaxSeg] float4: per vocabulary segment partials (tensor-core path)
+  size_t gbar = 0;     // u32 grid-barrier counter of the persistent draft kernel, then
+                       // [G * ceil(B/128)] u32 pass-2 tile counters (16 bytes in)
   size_t sk0 = 0, sk1 = 0, sv0 = 0, sv1 = 0;  // scheduler sort buffers [B*G] u32
   size_t vrs = 0;      // [B*(G+1)*RS_PARTS] float4: verify row-slice statistics
   size_t total = 0;
@@ -40,15 +46,8 @@ cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
-// Tensor-core logits passes of the draft sampler (draft_tc.cu).
-struct TcMaps {
-  CUtensorMap U, W2, Pd;
-};
+// Tensor-core draft sampler (draft_tc.cu).
 bool draft_tc_supported(const dspark_dims& d);
-int draft_tc_tile_width();
-cudaError_t draft_tc_prepare(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, TcMaps* maps);
-int draft_tc_slab_mtiles(const dspark_dims& d);
-cudaError_t launch_draft_tc_pass(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, const TcMaps& maps,
-                                 int k, bool write, int m_first, int m_count, bool u_keep, cudaStream_t s);
+cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
 }  // namespace dspark

@@ -18,7 +18,10 @@ from . import capi
 
 class DsparkError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} returned {capi.dspark_status_string(status)}")
+        msg = f"{fn} returned {capi.dspark_status_string(status)}"
+        if status == capi.DSPARK_CUDA_ERROR:
+            msg += f" (cudaError {capi.dspark_last_cuda_error()})"
+        super().__init__(msg)
         self.status = status
 
 

@@ -276,6 +276,11 @@ DSPARK_API dspark_status dspark_verify(const dspark_verify_args* args, void* wor
  * depends on it. */
 DSPARK_API uint64_t dspark_launch_count(void);
 
+/* The cudaError_t value behind the most recent DSPARK_CUDA_ERROR that a call
+ * on the calling thread returned (0 if none has).  Thread-local; no call
+ * resets it. */
+DSPARK_API int dspark_last_cuda_error(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 DSPARK_API const char* dspark_status_string(dspark_status s);
 
