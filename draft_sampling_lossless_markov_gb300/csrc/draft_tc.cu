@@ -82,7 +82,10 @@ constexpr int kStagingPerWarp = 32 * 32 * 4;         // [32 rows x 32 cols] fp32
 constexpr uint32_t kW2Stage = KC * BN * 2;           // 24 KB
 constexpr uint32_t kUChunk = BM * CW * 2;            // 16 KB: one 64-column chunk of U rows
 constexpr uint32_t kUStage = NCH * kUChunk;          // 48 KB: the U rows of one tile
-constexpr int NW = 3;                                // W2 ring stages
+constexpr int NW = 3;                                // W2 ring stages of the W2 region
+// Pass 1 writes no p_d, so its W2 ring also takes the two 24 KB halves of the
+// (then idle) p_d staging area: five stages, more than a tile of W2 in flight.
+constexpr int NW_S = 5;
 // U ring stages.  A stage holds a whole tile and every epilogue warp waits on
 // every use of it, in order: a mbarrier parity wait is only sound when the
 // waiter has seen the previous phase complete, which a ring of chunk-sized
@@ -97,6 +100,7 @@ constexpr size_t kSmemBytes =
     1024 + NW * (size_t)kW2Stage + NU * (size_t)kUStage + (size_t)kEpiWarps * kStagingPerWarp + kTailBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kGroups * BM * 16 <= kEpiWarps * kStagingPerWarp, "segment merge fits in the staging buffers");
+static_assert((NW_S - NW) * kW2Stage <= (uint32_t)(kEpiWarps * kStagingPerWarp), "pass-1 W2 stages fit in the staging area");
 
 struct Params {
   int B, G, V, r, H;
@@ -300,16 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sW = smem;
   uint8_t* sU = sW + NW * kW2Stage;
   uint8_t* sStg = sU + NU * kUStage;
+  auto w2_slot = [&](int s) { return s < NW ? sW + s * kW2Stage : sStg + (s - NW) * kW2Stage; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + kEpiWarps * kStagingPerWarp);
   uint64_t* fullW = bars;
-  uint64_t* emptyW = fullW + NW;
-  uint64_t* fullU = emptyW + NW;
+  uint64_t* emptyW = fullW + NW_S;
+  uint64_t* fullU = emptyW + NW_S;
   uint64_t* emptyU = fullU + NU;
   uint64_t* tfull = emptyU + NU;
   uint64_t* tempty = tfull + 2;
   uint64_t* eready = tempty + 2;
   uint64_t* mma_done = eready + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* stg_free = mma_done + 1;  // the epilogue's stores of a pass 2 have read the staging area
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stg_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = abort_flag + 1;
   // vocabulary tile of each item the producer hands on, in order; -1 ends a pass
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pass_of = [&](int pi) { return persist ? pi : p.pass_only; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NW; ++s) {
+    for (int s = 0; s < NW_S; ++s) {
       ptx::mbar_init(&fullW[s], 1);
       ptx::mbar_init(&emptyW[s], 1);
     }
@@ -340,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(eready, kEpiWarps);
     ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(stg_free, kEpiWarps);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -362,11 +369,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_last = ptx::policy_evict_last();
       const uint64_t pol_first = ptx::policy_evict_first();
-      int iw = 0, iu = 0, jt = 0;  // W2 stages, U stages, tile queue items
+      int iu = 0, jt = 0;            // U stages, tile queue items
+      uint32_t wpar = 0, wused = 0;  // per W2 slot: parity of its uses so far; used at all
       bool ok = true;
       for (int k = p.k_begin; k < p.k_end && ok; ++k)
         for (int pi = 0; pi < npass && ok; ++pi) {
           const int wr = pass_of(pi);
+          const int nsl = wr == 0 ? NW_S : NW;
+          int cs = 0;  // each pass cycles its W2 slots from slot 0
+          // pass 1 after a pass 2 of this launch: its two extra slots are the
+          // staging area, free once every epilogue warp's stores have read it
+          bool stg_ok = !(wr == 0 && persist && k > p.k_begin);
+          auto take_slot = [&](int& s) -> bool {
+            s = cs;
+            cs = cs + 1 == nsl ? 0 : cs + 1;
+            if (s >= NW && !stg_ok) {
+              if (!ptx::mbar_wait(stg_free, (uint32_t)((k - 1 - p.k_begin) & 1), abort_flag, kWaitLimitNs))
+                return false;
+              stg_ok = true;
+            }
+            const bool r = ptx::mbar_wait(&emptyW[s], ((wpar >> s) & 1) ^ 1, abort_flag, kWaitLimitNs);
+            wpar ^= 1u << s;
+            wused |= 1u << s;
+            return r;
+          };
           for (int i = 0; ok; ++i) {
             // the next tile: pass 1 walks this CTA's segment upward (the select
             // needs one partial per contiguous segment); pass 2 takes the M-tile's
@@ -379,26 +405,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               const unsigned t = atomicAdd(&p.sched[(size_t)k * p.n_mtiles + m_tile], 1u);
               if (t < (unsigned)p.ntiles) n = p.ntiles - 1 - (int)t;
             }
-            if (!ptx::mbar_wait(&emptyW[iw % NW], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            int s0;
+            if (!take_slot(s0)) {
               ok = false;
               break;
             }
             tq[jt % kTq] = n;
             ++jt;
             if (n < 0) {
-              // end of the pass: a W2 stage that carries no data
-              ptx::mbar_arrive(&fullW[iw % NW]);
-              ++iw;
+              // end of the pass: a W2 slot that carries no data
+              ptx::mbar_arrive(&fullW[s0]);
               break;
             }
             const int v0 = n * BN;
-            for (int kc = 0; kc < nkc; ++kc, ++iw) {
-              const int s = iw % NW;
-              if (kc > 0 && !ptx::mbar_wait(&emptyW[s], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+            for (int kc = 0; kc < nkc; ++kc) {
+              int s = s0;
+              if (kc > 0 && !take_slot(s)) {
                 ok = false;
                 break;
               }
-              uint8_t* st = sW + s * kW2Stage;
+              uint8_t* st = w2_slot(s);
               ptx::mbar_expect_tx(&fullW[s], kW2Stage);
               for (int c = 0; c < NCH; ++c)
                 ptx::tma_load_2d(st + c * (KC * CW * 2), &tmW2, &fullW[s], v0 + c * CW, kc * KC, pol_last);
@@ -418,15 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       if (!ok) fail();
-      // every load this thread issued has landed before the CTA may exit
-      for (int j = max(0, iw - NW); j < iw; ++j) ptx::mbar_wait(&fullW[j % NW], (j / NW) & 1, abort_flag, kWaitLimitNs);
+      // every load this thread issued has landed before the CTA may exit: the
+      // last use of each W2 slot and of each U stage
+      for (int s = 0; s < NW_S; ++s)
+        if ((wused >> s) & 1) ptx::mbar_wait(&fullW[s], ((wpar >> s) & 1) ^ 1, abort_flag, kWaitLimitNs);
       for (int j = max(0, iu - NU); j < iu; ++j) ptx::mbar_wait(&fullU[j % NU], (j / NU) & 1, abort_flag, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, true);
-      int it = 0, iw = 0, jt = 0;  // accumulator uses, W2 stages, tile queue items
+      int it = 0, jt = 0;  // accumulator uses, tile queue items
+      uint32_t fpar = 0;   // per W2 slot: parity of its uses so far
       bool ok = true;
       for (int k = p.k_begin; k < p.k_end && ok; ++k) {
         // E of this position is in TMEM
@@ -435,11 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        for (int pi = 0; pi < npass && ok; ++pi)
+        for (int pi = 0; pi < npass && ok; ++pi) {
+          const int nsl = pass_of(pi) == 0 ? NW_S : NW;
+          int cs = 0;  // the producer's slot order
+          auto next_slot = [&](int& s) -> bool {
+            s = cs;
+            cs = cs + 1 == nsl ? 0 : cs + 1;
+            const bool r = ptx::mbar_wait(&fullW[s], (fpar >> s) & 1, abort_flag, kWaitLimitNs);
+            fpar ^= 1u << s;
+            return r;
+          };
           for (;;) {
             const int a = it & 1;
-            if (!ptx::mbar_wait(&tempty[a], ((it >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs) ||
-                !ptx::mbar_wait(&fullW[iw % NW], (iw / NW) & 1, abort_flag, kWaitLimitNs)) {
+            int s0;
+            if (!ptx::mbar_wait(&tempty[a], ((it >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs) || !next_slot(s0)) {
               ok = false;
               break;
             }
@@ -448,24 +486,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++jt;
             ++it;
             if (n < 0) {
-              // end of the pass: release the empty W2 stage and hand the marker on
-              ptx::mbar_arrive(&emptyW[iw % NW]);
-              ++iw;
+              // end of the pass: release the empty W2 slot and hand the marker on
+              ptx::mbar_arrive(&emptyW[s0]);
               ptx::mbar_arrive(&tfull[a]);
               ptx::mbar_arrive(&tfull[a]);
               break;
             }
             const uint32_t d = tmem + kAccCol0 + (uint32_t)(a * BN);
-            for (int kc = 0; kc < nkc; ++kc, ++iw) {
-              const int s = iw % NW;
+            for (int kc = 0; kc < nkc; ++kc) {
+              int s = s0;
               if (kc > 0) {
-                if (!ptx::mbar_wait(&fullW[s], (iw / NW) & 1, abort_flag, kWaitLimitNs)) {
+                if (!next_slot(s)) {
                   ok = false;
                   break;
                 }
                 ptx::tc_fence_after();
               }
-              const uint32_t aW2 = ptx::smem_u32(sW + s * kW2Stage);
+              const uint32_t aW2 = ptx::smem_u32(w2_slot(s));
 #pragma unroll
               for (int k4 = 0; k4 < KC / 16; ++k4) {
                 const int ks = kc * (KC / 16) + k4;
@@ -485,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // before the epilogue's
             ptx::mbar_arrive(&tfull[a]);
           }
+        }
       }
       if (!ok) fail();
       // TMEM is not freed under a running MMA
@@ -830,6 +868,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             if (vrow && have_pdtok && !*abort_flag) p.pd_tok[(size_t)b * p.G + k] = pdtok;
+            // this warp's stores have read the staging area: the next pass 1 may
+            // load W2 into it
+            if (lane == 0) ptx::bulk_wait_read0();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(stg_free);
           }
         };
         if (wr == 0)
