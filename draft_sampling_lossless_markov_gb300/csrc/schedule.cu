@@ -14,12 +14,16 @@
 //   1. c' (fp64 sigmoid rounded to fp32), a (fp32 running product), sort keys
 //      key = ~bits(a) for a > 0 (ascending key = descending a), 0xFFFFFFFF else,
 //      value = r * gamma + j, laid out in index order.
-// k_schedule (one CTA of 1024 threads; at most 65536 candidates):
+// k_schedule_smem (one CTA, up to 8192 candidates: everything in shared memory,
+// bitonic sort of (key, index)) or k_schedule (one CTA of 1024 threads; at
+// most 65536 candidates, through global memory):
 //   2. stable LSD radix sort of the keys (4 passes of 8 bits); stability keeps
 //      equal a in (r, j) index order;
 //   3. fp64 block scan of the sorted a, Theta_i, first non-increase;
 //   4. l_r by atomic max over the admitted candidates;
 //   5. offsets by a block scan of 1 + l_r; flatten + markers.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -277,6 +281,192 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a
   }
 }
 
+// Up to kSmemSortMax candidates the whole schedule runs out of shared memory:
+// a bitonic sort of (key, index) pairs, whose 64-bit order is the radix sort's
+// stable order (ties in a stay in (r, j) index order), then the same Theta
+// scan, l_r and flatten as k_schedule.
+constexpr int kSmemSortMax = 8192;
+
+__device__ __forceinline__ float key_to_a(uint64_t kv) { return __uint_as_float(~(uint32_t)(kv >> 32)); }
+
+// Ascending bitonic sort of kv[0, n_pad) (n_pad a power of two, 64 <= n_pad <=
+// 1024 E) by the CTA: thread t holds elements t E .. t E + E - 1 in registers.
+// A compare-exchange at distance j runs in registers (j < E), across lanes
+// with shuffles (j < 32 E) or through shared memory (larger j).
+template <int E>
+__device__ void bitonic_sort(uint64_t* kv, int n_pad) {
+  const int t = threadIdx.x;
+  const bool active = t * E < n_pad;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = active ? kv[t * E + e] : ~0ull;
+  for (int size = 2; size <= n_pad; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      if (j >= 32 * E) {
+        __syncthreads();
+        if (active) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) kv[t * E + e] = v[e];
+        }
+        __syncthreads();
+        if (active) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int x = t * E + e;
+            const uint64_t y = kv[x ^ j];
+            const bool keep_min = ((x & size) == 0) == ((x & j) == 0);
+            v[e] = keep_min ? min(v[e], y) : max(v[e], y);
+          }
+        }
+      } else if (j >= E) {
+        if (t < ((n_pad / E + 31) & ~31)) {  // whole warps
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int x = t * E + e;
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, v[e], j / E);
+            const bool keep_min = ((x & size) == 0) == ((x & j) == 0);
+            v[e] = keep_min ? min(v[e], y) : max(v[e], y);
+          }
+        }
+      } else {
+        // j < E: pick the compile-time distance so that v stays in registers
+#pragma unroll
+        for (int jc = E / 2; jc >= 1; jc /= 2) {
+          if (jc != j) continue;
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            if ((e & jc) == 0) {
+              const int x = t * E + e;
+              const uint64_t a = v[e], b = v[e | jc];
+              const bool up = (x & size) == 0;
+              v[e] = up ? min(a, b) : max(a, b);
+              v[e | jc] = up ? max(a, b) : min(a, b);
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (active) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) kv[t * E + e] = v[e];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_args a, const uint32_t* __restrict__ k0,
+                                                                  const uint32_t* __restrict__ v0, int n_pad) {
+  extern __shared__ uint64_t kv[];  // [n_pad >= 64] sorted candidates, then [B] l_r
+  int* s_ell = reinterpret_cast<int*>(kv + n_pad);
+  __shared__ uint32_t sm_u[40];
+  __shared__ double sm_d[40];
+  __shared__ int s_first;
+  __shared__ double s_theta_best;
+
+  const int B = a.B, G = a.gamma, n = B * G;
+  const int tid = threadIdx.x;
+  for (int r = tid; r < B; r += SCH_THREADS) s_ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
+  uint32_t ncand_local = 0;
+  for (int i = tid; i < n_pad; i += SCH_THREADS) {
+    uint64_t e = ~0ull;
+    if (i < n) {
+      const uint32_t key = k0[i];
+      ncand_local += key != 0xFFFFFFFFu;
+      e = ((uint64_t)key << 32) | v0[i];
+    }
+    kv[i] = e;
+  }
+  uint32_t ncand;
+  block_excl_scan_u32(ncand_local, sm_u, ncand);  // ends with __syncthreads
+
+  if (a.mode != DSPARK_SCHED_OFF) {
+    // ---- 2. bitonic sort, ascending (key, index) = descending a, ties by index ----
+    if (n_pad <= SCH_THREADS)
+      bitonic_sort<1>(kv, n_pad);
+    else if (n_pad <= 2 * SCH_THREADS)
+      bitonic_sort<2>(kv, n_pad);
+    else if (n_pad <= 4 * SCH_THREADS)
+      bitonic_sort<4>(kv, n_pad);
+    else
+      bitonic_sort<8>(kv, n_pad);
+    // ---- 3. Theta along the sorted path, first non-increase ----
+    const int nc = (int)ncand;
+    const int ch = (nc + SCH_THREADS - 1) / SCH_THREADS;
+    const int c_lo = min(tid * ch, nc), c_hi = min(c_lo + ch, nc);
+    double loc = 0.0;
+    for (int i = c_lo; i < c_hi; ++i) loc += (double)key_to_a(kv[i]);
+    double tot;
+    const double pre = block_excl_scan_f64(loc, sm_d, tot);
+    if (tid == 0) s_first = nc + 1;
+    __syncthreads();
+    {
+      double S = pre;
+      double theta_prev = ((double)B + S) * a.sps[B + c_lo];
+      for (int i = c_lo; i < c_hi; ++i) {  // sorted position i is candidate number i + 1
+        S += (double)key_to_a(kv[i]);
+        const double theta = ((double)B + S) * a.sps[B + i + 1];
+        if (!(theta > theta_prev)) {
+          atomicMin(&s_first, i + 1);
+          break;
+        }
+        theta_prev = theta;
+      }
+    }
+    __syncthreads();
+    const int nstar = s_first - 1;  // admitted candidates
+    if (nstar == 0) {
+      if (tid == 0) s_theta_best = (double)B * a.sps[B];
+    } else if (nstar - 1 >= c_lo && nstar - 1 < c_hi) {
+      double S = pre;
+      for (int i = c_lo; i < nstar; ++i) S += (double)key_to_a(kv[i]);
+      s_theta_best = ((double)B + S) * a.sps[B + nstar];
+    }
+    // ---- 4. l_r = number of admitted (r, .) candidates (= largest admitted j) ----
+    for (int i = tid; i < nstar; i += SCH_THREADS) {
+      const uint32_t v = (uint32_t)kv[i];
+      atomicMax(&s_ell[v / G], (int)(v % G) + 1);
+    }
+    __syncthreads();
+    if (tid == 0) *a.theta_best = s_theta_best;
+  } else {
+    if (tid == 0) *a.theta_best = 0.0;
+  }
+  __syncthreads();
+
+  // ---- 5. offsets and the flattened batch ----
+  const int chb = (B + SCH_THREADS - 1) / SCH_THREADS;
+  const int b_lo = min(tid * chb, B), b_hi = min(b_lo + chb, B);
+  uint32_t cnt = 0;
+  for (int r = b_lo; r < b_hi; ++r) cnt += 1u + (uint32_t)s_ell[r];
+  uint32_t nv;
+  uint32_t off = block_excl_scan_u32(cnt, sm_u, nv);
+  for (int r = b_lo; r < b_hi; ++r) {
+    const int L = s_ell[r];
+    a.ell[r] = L;
+    a.offsets[r] = (int)off;
+    a.flat_tok[off] = a.anchor[r];
+    a.mark_req[off] = r;
+    a.mark_pos[off] = 0;
+    for (int j = 1; j <= L; ++j) {
+      a.flat_tok[off + j] = a.tokens[(size_t)r * G + j - 1];
+      a.mark_req[off + j] = r;
+      a.mark_pos[off + j] = j;
+    }
+    off += 1u + (uint32_t)L;
+  }
+  const int cap = B * (1 + G);
+  for (int i = (int)nv + tid; i < cap; i += SCH_THREADS) {
+    a.flat_tok[i] = -1;
+    a.mark_req[i] = -1;
+    a.mark_pos[i] = -1;
+  }
+  if (tid == 0) {
+    a.offsets[B] = (int)nv;
+    *a.n_verify = (int)nv;
+  }
+}
+
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   uint32_t* k0 = reinterpret_cast<uint32_t*>(ws + L.sk0);
   uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
@@ -284,7 +474,22 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
   const int rb = PREP_THREADS / a.gamma;
   k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0);
-  k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
+  const int n = a.B * a.gamma;
+  if (n <= kSmemSortMax) {
+    int n_pad = 64;
+    while (n_pad < n) n_pad <<= 1;
+    const size_t smem = (size_t)n_pad * sizeof(uint64_t) + (size_t)a.B * sizeof(int);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(k_schedule_smem, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)(kSmemSortMax * sizeof(uint64_t) + kSmemSortMax * sizeof(int)));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, k0, v0, n_pad);
+  } else {
+    k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
+  }
   count_launches(2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
