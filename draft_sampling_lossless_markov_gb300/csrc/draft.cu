@@ -21,6 +21,9 @@
 // only by fp32 rounding order (relative 1e-7), far inside the sampling margin.
 #include <float.h>
 
+#include <mutex>
+#include <string>
+#include <cstdlib>
 #include "common.cuh"
 #include "draft_arith.cuh"
 #include "internal.h"
@@ -451,8 +454,19 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
 
   if (draft_tc_supported(d)) {
-    // tensor-core path: one persistent kernel for all positions
+    // tensor-core path: the fused-sweep persistent kernel, else the two-pass
+    // kernel (DSPARK_DRAFT_LAUNCH=two_pass or per_pass selects the latter)
     count_launches(1);
+    static int fused = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+      const char* e = getenv("DSPARK_DRAFT_LAUNCH");
+      fused = (e && (std::string(e) == "per_pass" || std::string(e) == "two_pass")) ? 0 : 1;
+    });
+    if (fused) {
+      const cudaError_t e = launch_draft_fused(a, ws, L, s);
+      if (e != cudaErrorNotSupported) return e;
+    }
     return launch_draft_tc(a, ws, L, s);
   }
 

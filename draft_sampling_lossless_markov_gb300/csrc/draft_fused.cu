@@ -1,0 +1,956 @@
+// Fused-sweep tensor-core draft sampler of the Markov head, sm_103a.
+//
+// Position k of the draft needs two passes over the vocabulary: one for the
+// row normaliser of p_d^k, one that writes p_d^k ([DSpark] 方法细节, "马尔可夫头
+// （Markov head）的实现"; the logits of a position do not fit on chip).  The
+// second pass of position k and the first pass of position k + 1 read the
+// same W2 tiles, so this kernel runs them as ONE sweep: every W2 tile it
+// loads serves two tcgen05.mma products,
+//     W item  l = U_k     + E_k     . W2   -> p_d^k written (needs m_k, S_k)
+//     S item  l = U_{k+1} + E_{k+1} . W2   -> (max, sum 2^(y - max), argmax)
+//                                             partials of position k + 1
+// which halves the W2 traffic of the two-pass scheme.  The sweep needs E_{k+1}
+// = W1[x_k] at its start, so the token x_k is chosen before it: the select,
+// from the partials of the previous sweep, finds the 64-column chunk where the
+// inverse CDF crosses u S and recomputes that chunk's logits on the CUDA cores
+// (the E_k . W2 dot products in fp32) to walk it.  One persistent cooperative
+// launch runs all sweeps: S(0), then W(k) + S(k + 1) for k = 0 .. gamma - 1,
+// with grid barriers around each select.
+//
+// Tile 128 requests x 128 vocabulary columns.  TMEM: E_k and E_{k+1} in two
+// slots of r/2 columns, then two 128-column fp32 accumulators.
+//   warp 0    TMA producer: W2 K-chunks [64 x 128] (six stages), U tiles
+//             [128 x 128] per item (three stages)
+//   warp 1    tcgen05.mma issuer: per tile the W item then the S item on the
+//             same W2 stages, alternating accumulators
+//   warps 2-9 epilogue, two groups of four warps; group g owns the g-th
+//             64-column chunk of every item.  They also gather E, run the
+//             select and the grid barriers.
+// Every wait gives up after two seconds and the kernel records DSPARK_TIMEOUT.
+#include <cuda.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+#include <type_traits>
+
+#include "common.cuh"
+#include "draft_arith.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace dspark {
+namespace fz {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int CW = 64;
+constexpr int NCH = BN / CW;
+constexpr int KC = 64;
+constexpr int kGroups = NCH;
+constexpr int kEpiWarps = kGroups * 4;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kEpiWarp0 = 2;
+constexpr int kStagingPerWarp = 32 * 32 * 4;
+constexpr uint32_t kW2Stage = KC * BN * 2;     // 16 KB
+constexpr uint32_t kUChunk = BM * CW * 2;      // 16 KB
+constexpr uint32_t kUStage = NCH * kUChunk;    // 32 KB: the U rows of one item
+constexpr int NW = 6;                          // W2 stages (1.5 tiles at r = 256)
+constexpr int NU = 3;                          // U stages, one item each
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kESlotCols = 128;           // r / 2 columns, r <= 256
+constexpr uint32_t kAccCol0 = 2 * kESlotCols;
+constexpr int kTailBytes = 1024;
+constexpr size_t kSmemBytes =
+    1024 + NW * (size_t)kW2Stage + NU * (size_t)kUStage + (size_t)kEpiWarps * kStagingPerWarp + kTailBytes;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// select scratch in the (idle) staging area: 8 warps x 64 partial logits, 8 row records
+static_assert(kEpiWarps * 64 * 4 + 8 * 8 * 4 <= kEpiWarps * kStagingPerWarp, "select scratch");
+
+struct Params {
+  int B, G, V, r, H;
+  int ntiles, nparts, ctas_per_m, n_ctas;
+  uint64_t seed;
+  const __nv_bfloat16* U;    // [B, G, V] (the select's chunk recompute)
+  const __nv_bfloat16* W1;   // [V, r]
+  const __nv_bfloat16* W2;   // [r, V]
+  const __nv_bfloat16* w;    // [H + r]
+  const float* zh;           // [B, G]
+  const int32_t* anchor;     // [B]
+  const float* temp;         // [B]
+  const uint32_t* req_id;    // [B]
+  float2* rowstat;           // [B] (m, S) of the last selected position
+  int32_t* tokens;           // [B, G]
+  float4* part;              // [B, nparts]
+  float4* segpart;           // [B, kDraftMaxSeg]
+  float* pd_tok;
+  float* conf_logit;
+  float* conf;
+  unsigned* gbar;            // grid barrier counter, zero at launch
+  WsHeader* hdr;
+};
+
+__host__ __device__ __forceinline__ int seg_begin(int j, int ntiles, int nseg) {
+  return (int)(((long long)j * ntiles) / nseg);
+}
+
+__device__ __forceinline__ void epi_sync() {
+  __syncwarp();
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void prefetch_row(const __nv_bfloat16* row, int r) {
+  for (int o = 0; o < r * 2; o += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(row) + o));
+}
+
+// grid-wide barrier of the epilogue threads of every (resident) CTA
+__device__ bool grid_barrier(const Params& p, unsigned target, volatile int* abort_flag, volatile int* s_ok,
+                             int epi_tid) {
+  epi_sync();
+  if (epi_tid == 0) {
+    int ok = *abort_flag ? 0 : 1;
+    __threadfence();
+    if (ok) atomicAdd(p.gbar, 1u);
+    if (ok && ld_acquire(p.gbar) < target) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ld_acquire(p.gbar) < target) {
+        if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    *s_ok = ok;
+  }
+  epi_sync();
+  return *s_ok != 0;
+}
+
+// Row record of the select, in shared memory between its steps.
+struct SelRec {
+  int cstar;      // crossing chunk (sampled rows), -1 for greedy rows / no row
+  int hit;        // 1 if the running sum crossed u S
+  float sbase;    // sum of 2^(y - m) over the chunks before cstar
+  float target;   // u S
+  float m, S;
+  int b, pad;
+};
+
+// Levels 1 and 2 of the select of row b at position k (one warp): the row max m
+// and sum S from the segment partials, u = Philox(seed, req, k + 1, draw 0),
+// the segment and then the 64-column chunk where the running sum first exceeds
+// u S ([DSpark] 方法细节, 草稿采样: inverse CDF in token-id order).  Greedy rows
+// get their token (argmax, lowest id on ties) here.
+__device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* rec) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int nseg = p.ctas_per_m;
+  const float4* SP = p.segpart + (size_t)b * kDraftMaxSeg;
+  if (!(p.temp[b] > 0.f)) {
+    float av = -INFINITY;
+    int ai = INT_MAX;
+    for (int j = lane; j < nseg; j += 32) {
+      const float4 s = __ldcg(&SP[j]);
+      argmax_merge(av, ai, s.z, __float_as_int(s.w));
+    }
+    warp_argmax(av, ai);
+    if (lane == 0) {
+      p.tokens[(size_t)b * p.G + k] = ai;
+      p.rowstat[b] = make_float2(0.f, 1.f);
+      if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);
+      rec->cstar = -1;
+      rec->b = b;
+    }
+    return;
+  }
+  constexpr int MAXT = kDraftMaxSeg / 32;
+  float sm_[MAXT], ss_[MAXT];
+  float m = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < MAXT; ++t) {
+    const int j = t * 32 + lane;
+    float4 s = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    if (j < nseg) s = __ldcg(&SP[j]);
+    sm_[t] = s.x;
+    ss_[t] = s.y;
+    m = fmaxf(m, s.x);
+  }
+  m = warp_max(m);
+  float q[MAXT], incl[MAXT], excl[MAXT];
+  float carry = 0.f;
+#pragma unroll
+  for (int t = 0; t < MAXT; ++t) {
+    const int j = t * 32 + lane;
+    q[t] = (j < nseg) ? tile_mass(sm_[t], ss_[t], m) : 0.f;
+    incl[t] = __fadd_rn(carry, warp_inclusive_scan(q[t]));
+    const float up = __shfl_up_sync(FULL, incl[t], 1);
+    excl[t] = lane == 0 ? carry : up;
+    carry = __shfl_sync(FULL, incl[t], 31);
+  }
+  const float S = carry;
+  const float u = philox_uniform(p.seed, p.req_id[b], (uint32_t)(k + 1), 0u);
+  const float target = u * S;
+  int js = -1, jlast = -1;
+  float base = 0.f;
+#pragma unroll
+  for (int t = 0; t < MAXT; ++t) {
+    const int j = t * 32 + lane;
+    const unsigned bal = __ballot_sync(FULL, j < nseg && incl[t] > target);
+    if (js < 0 && bal) {
+      const int L = __ffs(bal) - 1;
+      js = t * 32 + L;
+      base = __shfl_sync(FULL, excl[t], L);
+    }
+    const unsigned bp = __ballot_sync(FULL, j < nseg && q[t] > 0.f);
+    if (bp) jlast = t * 32 + 31 - __clz(bp);
+  }
+  bool hit = js >= 0;
+  if (!hit) js = max(jlast, 0);
+  // level 2: the 64-column chunks of segment js (tiles of 128 columns)
+  const int c_lo = seg_begin(js, p.ntiles, nseg) * NCH;
+  const int c_hi = min(seg_begin(js + 1, p.ntiles, nseg) * NCH, p.nparts);
+  const float4* P = p.part + (size_t)b * p.nparts;
+  int cstar = -1, clast = -1;
+  float cbase = 0.f, run = base;
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+    const int cc = c0 + lane;
+    float qc = 0.f;
+    if (cc < c_hi) {
+      const float4 pc = __ldcg(&P[cc]);
+      qc = tile_mass(pc.x, pc.y, m);
+    }
+    const float inc = __fadd_rn(run, warp_inclusive_scan(qc));
+    const float up = __shfl_up_sync(FULL, inc, 1);
+    const float ex = lane == 0 ? run : up;
+    if (hit && cstar < 0) {
+      const unsigned bal = __ballot_sync(FULL, cc < c_hi && inc > target);
+      if (bal) {
+        const int L = __ffs(bal) - 1;
+        cstar = c0 + L;
+        cbase = __shfl_sync(FULL, ex, L);
+      }
+    }
+    const unsigned bp = __ballot_sync(FULL, cc < c_hi && qc > 0.f);
+    if (bp) clast = c0 + 31 - __clz(bp);
+    run = __shfl_sync(FULL, inc, 31);
+  }
+  if (cstar < 0) {
+    hit = false;
+    cstar = clast >= 0 ? clast : c_lo;
+  }
+  if (lane == 0) {
+    p.rowstat[b] = make_float2(m, S);
+    rec->cstar = cstar;
+    rec->hit = hit ? 1 : 0;
+    rec->sbase = cbase;
+    rec->target = target;
+    rec->m = m;
+    rec->S = S;
+    rec->b = b;
+  }
+}
+
+// The E_k . W2 part of the logits of chunk cstar of row b, split over the
+// eight epilogue warps by rows of W2: warp w sums its r/8 products for the two
+// columns of each lane (fp32 fma in order) into red[w][64].
+__device__ void chunk_dot(const Params& p, int b, int k, int cstar, int ew, int lane, float* red) {
+  const int x = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+  const int xs = (x < 0 || x >= p.V) ? 0 : x;
+  const __nv_bfloat16* e = p.W1 + (size_t)xs * p.r;
+  const int v = cstar * CW + 2 * lane;
+  const bool in = v < p.V;  // V % 8 == 0: both columns of a lane are in or out together
+  const int per = p.r / kEpiWarps;
+  const int i0 = ew * per;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < per; ++i) {
+    const float ei = __bfloat162float(e[i0 + i]);
+    if (in) {
+      const __nv_bfloat162 wv = *reinterpret_cast<const __nv_bfloat162*>(p.W2 + (size_t)(i0 + i) * p.V + v);
+      const float2 f = __bfloat1622float2(wv);
+      a0 = fmaf(ei, f.x, a0);
+      a1 = fmaf(ei, f.y, a1);
+    }
+  }
+  red[ew * 64 + 2 * lane] = a0;
+  red[ew * 64 + 2 * lane + 1] = a1;
+}
+
+// The walk of the crossing chunk (one warp): l = U + sum of the warps' partial
+// dot products, y = l c, w = 2^(y - m); the token is the first column whose
+// running sum from sbase exceeds u S, else the chunk's last column with
+// positive weight.  Writes the token and prefetches its W1 row.
+__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int b = rec->b;
+  const int v = rec->cstar * CW + 2 * lane;
+  const bool in = v < p.V;
+  const float c = row_scale(p.temp[b]);
+  float w0 = 0.f, w1 = 0.f;
+  if (in) {
+    float d0 = 0.f, d1 = 0.f;
+    for (int w = 0; w < kEpiWarps; ++w) {
+      d0 = __fadd_rn(d0, red[w * 64 + 2 * lane]);
+      d1 = __fadd_rn(d1, red[w * 64 + 2 * lane + 1]);
+    }
+    const __nv_bfloat162 uv =
+        *reinterpret_cast<const __nv_bfloat162*>(p.U + ((size_t)b * p.G + k) * p.V + v);
+    const float2 fu = __bfloat1622float2(uv);
+    w0 = exp_shifted(scale_logit(add_base(fu.x, d0), c), rec->m);
+    w1 = exp_shifted(scale_logit(add_base(fu.y, d1), c), rec->m);
+  }
+  const float pair = __fadd_rn(w0, w1);
+  const float incl = __fadd_rn(rec->sbase, warp_inclusive_scan(pair));
+  const float up = __shfl_up_sync(FULL, incl, 1);
+  const float ex = lane == 0 ? rec->sbase : up;
+  int tok = -1;
+  const unsigned over = __ballot_sync(FULL, rec->hit && incl > rec->target);
+  if (over) {
+    const int L = __ffs(over) - 1;
+    if (lane == L) tok = (__fadd_rn(ex, w0) > rec->target) ? v : v + 1;
+    tok = __shfl_sync(FULL, tok, L);
+  } else {
+    const unsigned pos = __ballot_sync(FULL, w0 > 0.f || w1 > 0.f);
+    if (pos) {
+      const int L = 31 - __clz(pos);
+      if (lane == L) tok = (w1 > 0.f) ? v + 1 : v;
+      tok = __shfl_sync(FULL, tok, L);
+    } else {
+      tok = rec->cstar * CW;  // no positive weight at all (unreachable for a crossing chunk)
+    }
+  }
+  if (lane == 0) {
+    p.tokens[(size_t)b * p.G + k] = tok;
+    prefetch_row(p.W1 + (size_t)tok * p.r, p.r);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_draft_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2,
+                  const __grid_constant__ CUtensorMap tmPd, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int r = p.r;
+  const int nkc = r / KC;
+  uint8_t* sW = smem;
+  uint8_t* sU = sW + NW * kW2Stage;
+  uint8_t* sStg = sU + NU * kUStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + kEpiWarps * kStagingPerWarp);
+  uint64_t* fullW = bars;
+  uint64_t* emptyW = fullW + NW;
+  uint64_t* fullU = emptyW + NW;
+  uint64_t* emptyU = fullU + NU;
+  uint64_t* tfull = emptyU + NU;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* eready = tempty + 2;
+  uint64_t* mma_done = eready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_ok = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = (int)blockIdx.x / p.ctas_per_m;
+  const int n_lo = (int)blockIdx.x % p.ctas_per_m;
+  const int t_begin = seg_begin(n_lo, p.ntiles, p.ctas_per_m);
+  const int count = seg_begin(n_lo + 1, p.ntiles, p.ctas_per_m) - t_begin;
+  const int row_base = m_tile * BM;
+  const int G = p.G;
+  // sweep q = 0 .. G: q = 0 is S(0) alone; q >= 1 is W(q - 1) + S(q) (no S in
+  // the last).  Sweeps alternate direction over the segment, so that each
+  // starts on the tiles the previous one read last.
+  auto tile_of = [&](int i, int q) { return (q & 1) ? t_begin + count - 1 - i : t_begin + i; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NW; ++s) {
+      ptx::mbar_init(&fullW[s], 1);
+      ptx::mbar_init(&emptyW[s], 1);
+    }
+    for (int s = 0; s < NU; ++s) {
+      ptx::mbar_init(&fullU[s], 1);
+      ptx::mbar_init(&emptyU[s], kEpiWarps);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], kEpiWarps);
+    }
+    ptx::mbar_init(eready, kEpiWarps);
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    report_error(p.hdr, DSPARK_TIMEOUT, (int)blockIdx.x);
+  };
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      const uint64_t pol_last = ptx::policy_evict_last();
+      const uint64_t pol_first = ptx::policy_evict_first();
+      int iw = 0, iu = 0;
+      bool ok = true;
+      for (int q = 0; q <= G && ok; ++q) {
+        const int s = q - 1;
+        const bool hasW = s >= 0, hasS = s + 1 < G;
+        for (int i = 0; i < count && ok; ++i) {
+          const int v0 = tile_of(i, q) * BN;
+          for (int kc = 0; kc < nkc; ++kc, ++iw) {
+            const int st = iw % NW;
+            if (!ptx::mbar_wait(&emptyW[st], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = sW + st * kW2Stage;
+            ptx::mbar_expect_tx(&fullW[st], kW2Stage);
+            for (int c = 0; c < NCH; ++c)
+              ptx::tma_load_2d(dst + c * (KC * CW * 2), &tmW2, &fullW[st], v0 + c * CW, kc * KC, pol_last);
+          }
+          for (int item = 0; item < 2 && ok; ++item) {
+            if (item == 0 ? !hasW : !hasS) continue;
+            const int kk = item == 0 ? s : s + 1;
+            const int su = iu % NU;
+            if (!ptx::mbar_wait(&emptyU[su], ((iu / NU) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_expect_tx(&fullU[su], kUStage);
+            for (int c = 0; c < NCH; ++c)
+              ptx::tma_load_3d(sU + su * kUStage + c * kUChunk, &tmU, &fullU[su], v0 + c * CW, kk, row_base,
+                               pol_first);
+            ++iu;
+          }
+        }
+      }
+      if (!ok) fail();
+      for (int j = max(0, iw - NW); j < iw; ++j) ptx::mbar_wait(&fullW[j % NW], (j / NW) & 1, abort_flag, kWaitLimitNs);
+      for (int j = max(0, iu - NU); j < iu; ++j) ptx::mbar_wait(&fullU[j % NU], (j / NU) & 1, abort_flag, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, true);
+      int it = 0, iw = 0;
+      bool ok = true;
+      for (int q = 0; q <= G && ok; ++q) {
+        const int s = q - 1;
+        const bool hasW = s >= 0, hasS = s + 1 < G;
+        bool e_ok = false;
+        for (int i = 0; i < count && ok; ++i) {
+          bool staged = false;  // this tile's W2 stages waited for
+          for (int item = 0; item < 2 && ok; ++item) {
+            if (item == 0 ? !hasW : !hasS) continue;
+            if (item == 1 && !e_ok) {
+              // E_{q} of this sweep's S items: the q-th gather
+              if (!ptx::mbar_wait(eready, (uint32_t)(q & 1), abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              e_ok = true;
+            }
+            const int a = it & 1;
+            if (!ptx::mbar_wait(&tempty[a], ((it >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const int kk = item == 0 ? s : s + 1;
+            const uint32_t a_base = tmem + (uint32_t)((kk & 1) * kESlotCols);
+            const uint32_t d = tmem + kAccCol0 + (uint32_t)(a * BN);
+            for (int kc = 0; kc < nkc; ++kc) {
+              const int st = (iw + kc) % NW;
+              if (!staged) {
+                if (!ptx::mbar_wait(&fullW[st], ((iw + kc) / NW) & 1, abort_flag, kWaitLimitNs)) {
+                  ok = false;
+                  break;
+                }
+                ptx::tc_fence_after();
+              }
+              const uint32_t aW2 = ptx::smem_u32(sW + st * kW2Stage);
+#pragma unroll
+              for (int k4 = 0; k4 < KC / 16; ++k4) {
+                const int ks = kc * (KC / 16) + k4;
+                // B: W2 K-chunk [64 x 128], MN-major, 128B swizzle: two 64-column
+                //    blocks 8 KB apart; 8-row groups 1024 B apart along K
+                const uint64_t bd = ptx::smem_desc_sw128(aW2 + k4 * 2048, KC * CW * 2, 1024);
+                ptx::tc_mma_tmem_a(d, a_base + (uint32_t)(ks * 8), bd, idesc, ks > 0 ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
+            staged = true;
+            ptx::tc_commit(&tfull[a]);
+            ++it;
+          }
+          if (!ok) break;
+          // the tile's W2 stages are free once both of its products are done
+          for (int kc = 0; kc < nkc; ++kc) ptx::tc_commit(&emptyW[(iw + kc) % NW]);
+          iw += nkc;
+        }
+      }
+      if (!ok) fail();
+      ptx::tc_commit(mma_done);
+      ptx::mbar_wait(mma_done, 0, abort_flag, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------ epilogue ----------------------------------
+    const int ew = warp - kEpiWarp0;
+    const int epi_tid = ew * 32 + lane;
+    const int g = ew >> 2;
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
+    const int b = row_base + row;
+    const bool vrow = b < p.B;
+    const uint32_t lane_bits = (uint32_t)(qd * 32) << 16;
+    const int npieces = r / 64;
+    const float T_ = vrow ? p.temp[b] : 1.f;
+    const bool sampled = T_ > 0.f;
+    const float c = row_scale(T_);
+    uint8_t* stg = sStg + ew * kStagingPerWarp;
+    unsigned nbar = 0;
+    int it = 0, iu = 0, ngather = 0;
+    bool alive = true;
+
+    // E_k = W1[x_{k-1}] (x_0 = anchor) into TMEM slot k & 1; then, on the
+    // first CTA of the M-tile, the confidence of position k from it
+    auto gather = [&](int k) {
+      int x = 0;
+      if (vrow) {
+        x = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+        if (x < 0 || x >= p.V) {
+          if (g == 0) report_error(p.hdr, DSPARK_BAD_INPUT, x);
+          x = 0;
+        }
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r);
+      const uint32_t slot = tmem + lane_bits + (uint32_t)((k & 1) * kESlotCols);
+      // group g copies the 64-element pieces g, g + 2 of its rows
+#pragma unroll 1
+      for (int pc = g; pc < npieces; pc += kGroups) {
+        uint32_t wv[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 qv = vrow ? src[pc * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
+          wv[4 * e] = qv.x;
+          wv[4 * e + 1] = qv.y;
+          wv[4 * e + 2] = qv.z;
+          wv[4 * e + 3] = qv.w;
+        }
+        __syncwarp();
+        ptx::tmem_st32(slot + (uint32_t)(pc * 32), wv);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(eready);
+      const int phase = ngather++;
+      if (g == 0 && n_lo == 0) {
+        const bool ok = ptx::mbar_wait(eready, (uint32_t)(phase & 1), abort_flag, kWaitLimitNs);
+        if (__all_sync(0xffffffffu, ok)) {
+          ptx::tc_fence_after();
+          const uint4* wsrc = reinterpret_cast<const uint4*>(p.w + p.H);
+          float zacc = 0.f;
+          for (int pc = 0; pc < npieces; ++pc) {
+            float ev[32];
+            __syncwarp();
+            ptx::tmem_ld32(slot + (uint32_t)(pc * 32), ev);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint4 we = wsrc[pc * 8 + e];
+              const uint32_t wq[4] = {we.x, we.y, we.z, we.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const uint32_t eb = __float_as_uint(ev[4 * e + t]);
+                const float2 fe = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&eb));
+                const float2 fw = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[t]));
+                zacc = fmaf(fw.x, fe.x, zacc);
+                zacc = fmaf(fw.y, fe.y, zacc);
+              }
+            }
+          }
+          if (vrow) {
+            const float z = p.zh[(size_t)b * p.G + k] + zacc;
+            p.conf_logit[(size_t)b * p.G + k] = z;
+            p.conf[(size_t)b * p.G + k] = 1.f / (1.f + expf(-z));
+          }
+        } else if (lane == 0) {
+          fail();
+        }
+      }
+    };
+
+    // the select of position k for the rows this CTA serves: levels 1 and 2 one
+    // warp per row (up to eight rows at a time), then the chunk recompute and
+    // walk of each sampled row with all eight warps
+    auto select = [&](int k) {
+      SelRec* recs = reinterpret_cast<SelRec*>(sStg);
+      float* red = reinterpret_cast<float*>(sStg + 8 * sizeof(SelRec));
+      for (int base = (int)blockIdx.x; base < p.B; base += p.n_ctas * kEpiWarps) {
+        const int rb = base + p.n_ctas * ew;
+        if (lane == 0) recs[ew].cstar = -2;  // no row
+        __syncwarp();
+        if (rb < p.B) select_levels(p, rb, k, lane, &recs[ew]);
+        epi_sync();
+        for (int w = 0; w < kEpiWarps; ++w) {
+          const int cst = recs[w].cstar;
+          if (cst < 0) continue;  // greedy row (done) or none
+          chunk_dot(p, recs[w].b, k, cst, ew, lane, red);
+          epi_sync();
+          if (ew == 0) chunk_walk(p, &recs[w], k, lane, red);
+          epi_sync();
+        }
+        // every warp has read the round's records before the next round writes them
+        epi_sync();
+      }
+    };
+
+    if (!*abort_flag) gather(0);
+    for (int q = 0; q <= G && alive; ++q) {
+      const int s = q - 1;
+      const bool hasW = s >= 0, hasS = s + 1 < G;
+      // W(s) row data: (m, 1/S) and the token x_s (chosen by the select)
+      float rm = 0.f, rinvS = 1.f;
+      int xs = -1;
+      if (hasW && vrow) {
+        const float2 st = __ldcg(&p.rowstat[b]);
+        rm = st.x;
+        rinvS = inv_sum(st.y);
+        xs = __ldcg(&p.tokens[(size_t)b * p.G + s]);
+      }
+      float gm = -INFINITY, gs = 0.f, gav = -INFINITY;
+      int gai = INT_MAX;
+      float pdtok = 0.f;
+      bool have_pdtok = false;
+      const int ch = g;
+      bool tiles_ok = true;
+      for (int i = 0; i < count && tiles_ok; ++i) {
+        const int n = tile_of(i, q);
+        const int v0 = n * BN + ch * CW;
+        const int nvalid = min(CW, p.V - v0);
+        for (int item = 0; item < 2; ++item) {
+          if (item == 0 ? !hasW : !hasS) continue;
+          const int a = it & 1;
+          bool ok = ptx::mbar_wait(&tfull[a], (it >> 1) & 1, abort_flag, kWaitLimitNs);
+          const int su = iu % NU;
+          if (ok) ok = ptx::mbar_wait(&fullU[su], (iu / NU) & 1, abort_flag, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) fail();
+            tiles_ok = false;
+            break;
+          }
+          ++it;
+          ++iu;
+          ptx::tc_fence_after();
+          const uint32_t ta = tmem + lane_bits + kAccCol0 + (uint32_t)(a * BN + ch * CW);
+          const uint8_t* su_row = sU + su * kUStage + ch * kUChunk + row * 128;
+          // logits of columns v0 + 32 h .. + 31: accumulator + U; the last read
+          // releases the accumulator and the U stage
+          auto load_half = [&](int h, float(&x)[32], bool last) {
+            __syncwarp();
+            ptx::tmem_ld32(ta + 32 * h, x);
+            ptx::tmem_ld_wait();
+            if (last) {
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&tempty[a]);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const int c8 = 4 * h + cc;
+              const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((c8 ^ (row & 7)) << 4));
+              const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(bp[e]);
+                x[8 * cc + 2 * e] = add_base(f.x, x[8 * cc + 2 * e]);
+                x[8 * cc + 2 * e + 1] = add_base(f.y, x[8 * cc + 2 * e + 1]);
+              }
+            }
+            if (last) {
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
+            }
+          };
+          if (item == 1) {
+            // S item: chunk partial of position s + 1
+            float mc = -INFINITY, cs = 0.f, av = -INFINITY;
+            int ai = INT_MAX;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float x[32];
+              load_half(h, x, h == 1);
+              if (sampled) {
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  x[j] = (32 * h + j < nvalid) ? scale_logit(x[j], c) : -INFINITY;
+                  mx[j & 3] = fmaxf(mx[j & 3], x[j]);
+                }
+                const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                if (mh != -INFINITY) {
+                  float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) sm[j & 3] += exp_shifted(x[j], mh);
+                  const float sh = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                  const float nm = fmaxf(mc, mh);
+                  cs = __fadd_rn(tile_mass(mc, cs, nm), tile_mass(mh, sh, nm));
+                  mc = nm;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (32 * h + j < nvalid && x[j] > av) {
+                    av = x[j];
+                    ai = v0 + 32 * h + j;
+                  }
+              }
+            }
+            if (!sampled) {
+              mc = av;
+              cs = 1.f;
+            }
+            if (v0 < p.V) {
+              if (vrow) p.part[(size_t)b * p.nparts + v0 / CW] = make_float4(mc, cs, av, __int_as_float(ai));
+              const float nm = fmaxf(gm, mc);
+              gs = __fadd_rn(tile_mass(gm, gs, nm), tile_mass(mc, cs, nm));
+              gm = nm;
+              argmax_merge(gav, gai, av, ai);
+            }
+          } else {
+            // W item: p_d^s = 2^(y - m) / S (one-hot for greedy rows)
+            const int row0 = row_base + qd * 32;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float x[32];
+              load_half(h, x, h == 1);
+              if (sampled) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  x[j] = (32 * h + j < nvalid) ? prob_from(scale_logit(x[j], c), rm, rinvS) : 0.f;
+              }
+              const int jx = xs - (v0 + 32 * h);
+              if (jx >= 0 && jx < 32) {
+                float pv = 1.f;
+                if (sampled) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (j == jx) pv = x[j];
+                }
+                pdtok = pv;
+                have_pdtok = true;
+              }
+              if (lane == 0) ptx::bulk_wait_read0();
+              __syncwarp();
+              if (sampled) {
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                  *reinterpret_cast<float4*>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                      make_float4(x[4 * cc], x[4 * cc + 1], x[4 * cc + 2], x[4 * cc + 3]);
+              } else {
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                  *reinterpret_cast<float4*>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                      make_float4(jx == 4 * cc ? 1.f : 0.f, jx == 4 * cc + 1 ? 1.f : 0.f,
+                                  jx == 4 * cc + 2 ? 1.f : 0.f, jx == 4 * cc + 3 ? 1.f : 0.f);
+              }
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0 < p.B && v0 + 32 * h < p.V) {
+                ptx::tma_store_3d(&tmPd, stg, v0 + 32 * h, s, row0, ptx::policy_evict_first());
+                ptx::bulk_commit();
+              }
+            }
+          }
+        }
+      }
+      if (hasW && vrow && have_pdtok && !*abort_flag) p.pd_tok[(size_t)b * p.G + s] = pdtok;
+      if (!hasS) break;  // the last sweep
+
+      // segment partial of position q = s + 1, through the idle staging area
+      if (lane == 0) ptx::bulk_wait_read0();
+      __syncwarp();
+      float4* xch = reinterpret_cast<float4*>(sStg);
+      epi_sync();
+      xch[g * BM + row] = make_float4(gm, gs, gav, __int_as_float(gai));
+      epi_sync();
+      if (g == 0 && vrow && !*abort_flag) {
+        float m = gm;
+        for (int gg = 1; gg < kGroups; ++gg) m = fmaxf(m, xch[gg * BM + row].x);
+        float sum = 0.f, av = -INFINITY;
+        int ai = INT_MAX;
+        for (int gg = 0; gg < kGroups; ++gg) {
+          const float4 e = xch[gg * BM + row];
+          if (m != -INFINITY) sum = __fadd_rn(sum, tile_mass(e.x, e.y, m));
+          argmax_merge(av, ai, e.z, __float_as_int(e.w));
+        }
+        p.segpart[(size_t)b * kDraftMaxSeg + n_lo] = make_float4(m, sum, av, __int_as_float(ai));
+      }
+      if (!grid_barrier(p, ++nbar * (unsigned)p.n_ctas, abort_flag, s_ok, epi_tid)) {
+        if (epi_tid == 0) fail();
+        alive = false;
+        break;
+      }
+      select(q);
+      if (!grid_barrier(p, ++nbar * (unsigned)p.n_ctas, abort_flag, s_ok, epi_tid)) {
+        if (epi_tid == 0) fail();
+        alive = false;
+        break;
+      }
+      // E of the next sweep's S items (slot (q + 1) & 1 held E_{q-1}, whose
+      // products all finished in this sweep)
+      if (q + 1 < G) gather(q + 1);
+    }
+    if (lane == 0) ptx::bulk_wait0();
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fz
+
+// The fused-sweep kernel needs every CTA resident (cooperative launch, one
+// CTA per SM) and at most one CTA's worth of M-tiles per SM; returns
+// cudaErrorNotSupported when it cannot run, so that the caller falls back.
+cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  int dev = 0, sms = 0, coop = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  const int n_mtiles = (d.B + fz::BM - 1) / fz::BM;
+  if (!coop || sms <= 0 || n_mtiles > sms || d.r > 2 * (int)fz::kESlotCols || (d.r % (8 * 8)) != 0)
+    return cudaErrorNotSupported;
+  const cuuint64_t V = (cuuint64_t)d.V, G = (cuuint64_t)d.gamma, B = (cuuint64_t)d.B, r = (cuuint64_t)d.r;
+  CUtensorMap tmU, tmW2, tmPd;
+  {
+    const cuuint64_t dims[3] = {V, G, B};
+    const cuuint64_t strides[2] = {V * 2, G * V * 2};
+    const cuuint32_t box[3] = {fz::CW, 1, fz::BM};
+    if (!fz::encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.U, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {V, r};
+    const cuuint64_t strides[1] = {V * 2};
+    const cuuint32_t box[2] = {fz::CW, fz::KC};
+    if (!fz::encode(&tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {V, G, B};
+    const cuuint64_t strides[2] = {V * 4, G * V * 4};
+    const cuuint32_t box[3] = {32, 1, 32};
+    if (!fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(fz::k_draft_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)fz::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+
+  fz::Params p;
+  p.B = d.B;
+  p.G = d.gamma;
+  p.V = d.V;
+  p.r = d.r;
+  p.H = d.H;
+  p.seed = a.seed;
+  p.ntiles = (d.V + fz::BN - 1) / fz::BN;
+  p.nparts = (d.V + fz::CW - 1) / fz::CW;
+  p.ctas_per_m = std::max(1, std::min(std::min(p.ntiles, sms / n_mtiles), kDraftMaxSeg));
+  p.n_ctas = n_mtiles * p.ctas_per_m;
+  p.U = static_cast<const __nv_bfloat16*>(a.U);
+  p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  p.W2 = static_cast<const __nv_bfloat16*>(a.W2);
+  p.w = static_cast<const __nv_bfloat16*>(a.w);
+  p.zh = reinterpret_cast<const float*>(ws + L.zh);
+  p.anchor = a.anchor;
+  p.temp = a.temp;
+  p.req_id = a.req_id;
+  p.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
+  p.tokens = a.tokens;
+  p.part = reinterpret_cast<float4*>(ws + L.part);
+  p.segpart = reinterpret_cast<float4*>(ws + L.segpart);
+  p.pd_tok = a.pd_tok;
+  p.conf_logit = a.conf_logit;
+  p.conf = a.conf;
+  p.gbar = reinterpret_cast<unsigned*>(ws + L.gbar);
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_ctas);
+  cfg.blockDim = dim3(fz::kThreads);
+  cfg.dynamicSmemBytes = fz::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  return cudaLaunchKernelEx(&cfg, fz::k_draft_fused, tmU, tmW2, tmPd, p);
+}
+
+}  // namespace dspark

@@ -49,5 +49,7 @@ cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayo
 // Tensor-core draft sampler (draft_tc.cu).
 bool draft_tc_supported(const dspark_dims& d);
 cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+// Fused-sweep kernel (draft_fused.cu); cudaErrorNotSupported when it cannot run.
+cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
 }  // namespace dspark
