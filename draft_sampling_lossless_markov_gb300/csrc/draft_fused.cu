@@ -139,14 +139,41 @@ __device__ bool grid_barrier(const Params& p, unsigned target, volatile int* abo
   return *s_ok != 0;
 }
 
+// Confidence of position k of row b (one warp): z = w_h . h_k + w_e . W1[x]
+// with x = x_{k-1} (the anchor for k = 0) and c = sigmoid(z) ([DSpark] 方法细节,
+// 置信度头); lane l takes elements 8 l .. 8 l + 7 (r <= 256).
+__device__ void conf_of(const Params& p, int b, int k, int x, int lane) {
+  if (x < 0 || x >= p.V) x = 0;
+  float acc = 0.f;
+  if (8 * lane < p.r) {
+    const uint4 eq = *reinterpret_cast<const uint4*>(p.W1 + (size_t)x * p.r + 8 * lane);
+    const uint4 wq = *reinterpret_cast<const uint4*>(p.w + p.H + 8 * lane);
+    const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&eq);
+    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wq);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 fe = __bfloat1622float2(e2[t]), fw = __bfloat1622float2(w2[t]);
+      acc = fmaf(fw.x, fe.x, acc);
+      acc = fmaf(fw.y, fe.y, acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) {
+    const float z = p.zh[(size_t)b * p.G + k] + acc;
+    p.conf_logit[(size_t)b * p.G + k] = z;
+    p.conf[(size_t)b * p.G + k] = 1.f / (1.f + expf(-z));
+  }
+}
+
 // Row record of the select, in shared memory between its steps.
 struct SelRec {
-  int cstar;      // crossing chunk (sampled rows), -1 for greedy rows / no row
+  int cstar;      // crossing chunk (sampled rows), -1 for greedy rows, -2 no row
   int hit;        // 1 if the running sum crossed u S
   float sbase;    // sum of 2^(y - m) over the chunks before cstar
   float target;   // u S
   float m, S;
-  int b, pad;
+  int b;
+  int tok;        // the chosen token
 };
 
 // Levels 1 and 2 of the select of row b at position k (one warp): the row max m
@@ -172,6 +199,7 @@ __device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* r
       if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);
       rec->cstar = -1;
       rec->b = b;
+      rec->tok = ai;
     }
     return;
   }
@@ -249,6 +277,11 @@ __device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* r
   if (cstar < 0) {
     hit = false;
     cstar = clast >= 0 ? clast : c_lo;
+  }
+  // the chunk recompute reads these W2 columns next: start them towards L2
+  for (int i = lane; i < 2 * p.r; i += 32) {  // the chunk's 128 bytes of a row span at most two lines
+    const char* a = reinterpret_cast<const char*>(p.W2 + (size_t)(i >> 1) * p.V + (size_t)cstar * CW);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a + (i & 1) * 127));
   }
   if (lane == 0) {
     p.rowstat[b] = make_float2(m, S);
@@ -334,6 +367,7 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   if (lane == 0) {
     p.tokens[(size_t)b * p.G + k] = tok;
     prefetch_row(p.W1 + (size_t)tok * p.r, p.r);
+    const_cast<SelRec*>(rec)->tok = tok;
   }
 }
 
@@ -528,11 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = row_scale(T_);
     uint8_t* stg = sStg + ew * kStagingPerWarp;
     unsigned nbar = 0;
-    int it = 0, iu = 0, ngather = 0;
+    int it = 0, iu = 0;
     bool alive = true;
 
-    // E_k = W1[x_{k-1}] (x_0 = anchor) into TMEM slot k & 1; then, on the
-    // first CTA of the M-tile, the confidence of position k from it
+    // E_k = W1[x_{k-1}] (x_0 = anchor) into TMEM slot k & 1
     auto gather = [&](int k) {
       int x = 0;
       if (vrow) {
@@ -563,41 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(eready);
-      const int phase = ngather++;
-      if (g == 0 && n_lo == 0) {
-        const bool ok = ptx::mbar_wait(eready, (uint32_t)(phase & 1), abort_flag, kWaitLimitNs);
-        if (__all_sync(0xffffffffu, ok)) {
-          ptx::tc_fence_after();
-          const uint4* wsrc = reinterpret_cast<const uint4*>(p.w + p.H);
-          float zacc = 0.f;
-          for (int pc = 0; pc < npieces; ++pc) {
-            float ev[32];
-            __syncwarp();
-            ptx::tmem_ld32(slot + (uint32_t)(pc * 32), ev);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint4 we = wsrc[pc * 8 + e];
-              const uint32_t wq[4] = {we.x, we.y, we.z, we.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const uint32_t eb = __float_as_uint(ev[4 * e + t]);
-                const float2 fe = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&eb));
-                const float2 fw = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[t]));
-                zacc = fmaf(fw.x, fe.x, zacc);
-                zacc = fmaf(fw.y, fe.y, zacc);
-              }
-            }
-          }
-          if (vrow) {
-            const float z = p.zh[(size_t)b * p.G + k] + zacc;
-            p.conf_logit[(size_t)b * p.G + k] = z;
-            p.conf[(size_t)b * p.G + k] = 1.f / (1.f + expf(-z));
-          }
-        } else if (lane == 0) {
-          fail();
-        }
-      }
     };
 
     // the select of position k for the rows this CTA serves: levels 1 and 2 one
@@ -620,11 +618,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ew == 0) chunk_walk(p, &recs[w], k, lane, red);
           epi_sync();
         }
+        // the confidence of position k + 1 of each row, from its chosen token
+        if (k + 1 < p.G && recs[ew].cstar != -2) conf_of(p, recs[ew].b, k + 1, recs[ew].tok, lane);
         // every warp has read the round's records before the next round writes them
         epi_sync();
       }
     };
 
+    // confidence of position 0 (from the anchors); later positions' come from
+    // the select that chooses their previous token
+    for (int rb = (int)blockIdx.x + p.n_ctas * ew; rb < p.B; rb += p.n_ctas * kEpiWarps)
+      conf_of(p, rb, 0, p.anchor[rb], lane);
     if (!*abort_flag) gather(0);
     for (int q = 0; q <= G && alive; ++q) {
       const int s = q - 1;
