@@ -267,7 +267,7 @@ def run_ours(args, rank, world, local_rank):
         "hbm_frac_step": step_frac,
         "hbm_frac_step_w2_per_position": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
         "breakdown_ms": br,
-        "roofline": {"bound": "hbm", "kernel": "dspark_draft_sample (logits passes + select)",
+        "roofline": {"bound": "hbm", "kernel": "dspark_draft_sample (fz::k_draft_fused, one launch, + k_conf_hidden)",
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
                      "unit": "GB/s", "frac": draft_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": bytes_["draft_strict"]},
