@@ -51,6 +51,7 @@ constexpr int NCH = BN / CW;
 constexpr int KC = 64;
 constexpr int kGroups = NCH;
 constexpr int kEpiWarps = kGroups * 4;
+constexpr int kTeamWarps = kEpiWarps / 2;  // the select recomputes two rows at a time
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kEpiWarp0 = 2;
@@ -109,30 +110,63 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
+__device__ __forceinline__ int ld_acquire_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_s32(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A token not yet chosen in this launch: every CTA sets the tokens of the rows
+// it selects to this before the first grid barrier; a select publishes the
+// chosen token (after the row's (m, S)) with a release store.
+constexpr int kTokPending = -1;
+
+// Waits (bounded) for the token at t; kTokPending if the wait gave up.
+__device__ int token_wait(const int* t, volatile int* abort_flag) {
+  int v = ld_acquire_s32(t);
+  if (v != kTokPending) return v;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while ((v = ld_acquire_s32(t)) == kTokPending) {
+    if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) return kTokPending;
+    __nanosleep(32);
+  }
+  return v;
+}
+
 __device__ __forceinline__ void prefetch_row(const __nv_bfloat16* row, int r) {
   for (int o = 0; o < r * 2; o += 128)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(row) + o));
 }
 
 // grid-wide barrier of the epilogue threads of every (resident) CTA
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 __device__ bool grid_barrier(const Params& p, unsigned target, volatile int* abort_flag, volatile int* s_ok,
                              int epi_tid) {
   epi_sync();
   if (epi_tid == 0) {
     int ok = *abort_flag ? 0 : 1;
-    __threadfence();
-    if (ok) atomicAdd(p.gbar, 1u);
-    if (ok && ld_acquire(p.gbar) < target) {
+    // release: the CTA's writes (ordered before by the named barrier) become
+    // visible with the arrival; acquire: the other CTAs' writes are visible
+    // after it
+    if (ok && atom_add_acq_rel(p.gbar, 1u) + 1u < target) {
       const uint64_t t0 = ptx::globaltimer_ns();
       while (ld_acquire(p.gbar) < target) {
         if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
           ok = 0;
           break;
         }
-        __nanosleep(64);
+        __nanosleep(32);
       }
     }
-    __threadfence();
     *s_ok = ok;
   }
   epi_sync();
@@ -173,6 +207,7 @@ struct SelRec {
   float target;   // u S
   float m, S;
   int b;
+  int x;          // x_{k-1}, the token the logits condition on
   int tok;        // the chosen token
 };
 
@@ -185,55 +220,64 @@ __device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* r
   constexpr unsigned FULL = 0xffffffffu;
   const int nseg = p.ctas_per_m;
   const float4* SP = p.segpart + (size_t)b * kDraftMaxSeg;
+  constexpr int MAXT = kDraftMaxSeg / 32;
+  // the segment partials first: both kinds of row need them
+  float4 sp[MAXT];
+#pragma unroll
+  for (int t = 0; t < MAXT; ++t) {
+    if (t * 32 >= nseg) break;  // warp-uniform
+    const int j = t * 32 + lane;
+    sp[t] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));
+    if (j < nseg) sp[t] = __ldcg(&SP[j]);
+  }
   if (!(p.temp[b] > 0.f)) {
     float av = -INFINITY;
     int ai = INT_MAX;
-    for (int j = lane; j < nseg; j += 32) {
-      const float4 s = __ldcg(&SP[j]);
-      argmax_merge(av, ai, s.z, __float_as_int(s.w));
+#pragma unroll
+    for (int t = 0; t < MAXT; ++t) {
+      if (t * 32 >= nseg) break;
+      argmax_merge(av, ai, sp[t].z, __float_as_int(sp[t].w));
     }
     warp_argmax(av, ai);
     if (lane == 0) {
-      p.tokens[(size_t)b * p.G + k] = ai;
       p.rowstat[b] = make_float2(0.f, 1.f);
-      if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);
+      if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);  // for the E gathers
+      st_release_s32(&p.tokens[(size_t)b * p.G + k], ai);
       rec->cstar = -1;
       rec->b = b;
       rec->tok = ai;
     }
     return;
   }
-  constexpr int MAXT = kDraftMaxSeg / 32;
-  float sm_[MAXT], ss_[MAXT];
+  const int xprev = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+  const uint32_t req = (uint32_t)p.req_id[b];
   float m = -INFINITY;
 #pragma unroll
   for (int t = 0; t < MAXT; ++t) {
-    const int j = t * 32 + lane;
-    float4 s = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-    if (j < nseg) s = __ldcg(&SP[j]);
-    sm_[t] = s.x;
-    ss_[t] = s.y;
-    m = fmaxf(m, s.x);
+    if (t * 32 >= nseg) break;
+    m = fmaxf(m, sp[t].x);
   }
   m = warp_max(m);
   float q[MAXT], incl[MAXT], excl[MAXT];
   float carry = 0.f;
 #pragma unroll
   for (int t = 0; t < MAXT; ++t) {
+    if (t * 32 >= nseg) break;  // warp-uniform
     const int j = t * 32 + lane;
-    q[t] = (j < nseg) ? tile_mass(sm_[t], ss_[t], m) : 0.f;
+    q[t] = (j < nseg) ? tile_mass(sp[t].x, sp[t].y, m) : 0.f;
     incl[t] = __fadd_rn(carry, warp_inclusive_scan(q[t]));
     const float up = __shfl_up_sync(FULL, incl[t], 1);
     excl[t] = lane == 0 ? carry : up;
     carry = __shfl_sync(FULL, incl[t], 31);
   }
   const float S = carry;
-  const float u = philox_uniform(p.seed, p.req_id[b], (uint32_t)(k + 1), 0u);
+  const float u = philox_uniform(p.seed, req, (uint32_t)(k + 1), 0u);
   const float target = u * S;
   int js = -1, jlast = -1;
   float base = 0.f;
 #pragma unroll
   for (int t = 0; t < MAXT; ++t) {
+    if (t * 32 >= nseg) break;  // warp-uniform
     const int j = t * 32 + lane;
     const unsigned bal = __ballot_sync(FULL, j < nseg && incl[t] > target);
     if (js < 0 && bal) {
@@ -284,6 +328,9 @@ __device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* r
     asm volatile("prefetch.global.L2 [%0];" ::"l"(a + (i & 1) * 127));
   }
   if (lane == 0) {
+    // and the walk the chunk's 64 U values of position k
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.U + ((size_t)b * p.G + k) * p.V + (size_t)cstar * CW));
+    // (m, S) now: the walk's release of the token, after a CTA barrier, publishes it
     p.rowstat[b] = make_float2(m, S);
     rec->cstar = cstar;
     rec->hit = hit ? 1 : 0;
@@ -292,40 +339,65 @@ __device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* r
     rec->m = m;
     rec->S = S;
     rec->b = b;
+    rec->x = xprev;
   }
 }
 
-// The E_k . W2 part of the logits of chunk cstar of row b, split over the
-// eight epilogue warps by rows of W2: warp w sums its r/8 products for the two
-// columns of each lane (fp32 fma in order) into red[w][64].
-__device__ void chunk_dot(const Params& p, int b, int k, int cstar, int ew, int lane, float* red) {
-  const int x = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+// The E_k . W2 part of the logits of chunk cstar of row b, split by rows of W2
+// over a team of four warps: lane (j, c) of team warp tw takes columns
+// 8 c .. 8 c + 7 of the rows tw r/4 + 4 i + j (128-bit loads, sixteen in flight),
+// the four row phases j are added by shuffles, and red[tw][64] receives the
+// warp's sums (fp32 fma in order within a phase).
+__device__ void chunk_dot(const Params& p, int x, int cstar, int tw, int lane, float* red) {
+  constexpr unsigned FULL = 0xffffffffu;
   const int xs = (x < 0 || x >= p.V) ? 0 : x;
-  const __nv_bfloat16* e = p.W1 + (size_t)xs * p.r;
-  const int v = cstar * CW + 2 * lane;
-  const bool in = v < p.V;  // V % 8 == 0: both columns of a lane are in or out together
-  const int per = p.r / kEpiWarps;
-  const int i0 = ew * per;
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < per; ++i) {
-    const float ei = __bfloat162float(e[i0 + i]);
-    if (in) {
-      const __nv_bfloat162 wv = *reinterpret_cast<const __nv_bfloat162*>(p.W2 + (size_t)(i0 + i) * p.V + v);
-      const float2 f = __bfloat1622float2(wv);
-      a0 = fmaf(ei, f.x, a0);
-      a1 = fmaf(ei, f.y, a1);
+  const int c8 = lane & 7, j = lane >> 3;
+  const int v = cstar * CW + 8 * c8;
+  const bool in = v < p.V;  // V % 8 == 0: the lane's eight columns are in or out together
+  const int per = p.r / kTeamWarps;
+  const int nt = per / 4;
+  const int i0 = tw * per + j;
+  const __nv_bfloat16* e = p.W1 + (size_t)xs * p.r + i0;
+  const __nv_bfloat16* w2 = p.W2 + (size_t)i0 * p.V + v;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int t0 = 0; t0 < nt; t0 += 16) {
+    uint4 wv[16];
+    float ev[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const bool ok = in && t0 + t < nt;
+      wv[t] = ok ? __ldcg(reinterpret_cast<const uint4*>(w2 + (size_t)(4 * (t0 + t)) * p.V))
+                 : make_uint4(0u, 0u, 0u, 0u);
+      ev[t] = ok ? __bfloat162float(e[4 * (t0 + t)]) : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&wv[t]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(bp[q]);
+        a[2 * q] = fmaf(ev[t], f.x, a[2 * q]);
+        a[2 * q + 1] = fmaf(ev[t], f.y, a[2 * q + 1]);
+      }
     }
   }
-  red[ew * 64 + 2 * lane] = a0;
-  red[ew * 64 + 2 * lane + 1] = a1;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    a[q] = __fadd_rn(a[q], __shfl_xor_sync(FULL, a[q], 8));
+    a[q] = __fadd_rn(a[q], __shfl_xor_sync(FULL, a[q], 16));
+  }
+  if (j == 0) {
+    float4* d = reinterpret_cast<float4*>(red + tw * 64 + 8 * c8);
+    d[0] = make_float4(a[0], a[1], a[2], a[3]);
+    d[1] = make_float4(a[4], a[5], a[6], a[7]);
+  }
 }
 
 // The walk of the crossing chunk (one warp): l = U + sum of the warps' partial
 // dot products, y = l c, w = 2^(y - m); the token is the first column whose
 // running sum from sbase exceeds u S, else the chunk's last column with
 // positive weight.  Writes the token and prefetches its W1 row.
-__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red) {
+__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red, uint32_t upair) {
   constexpr unsigned FULL = 0xffffffffu;
   const int b = rec->b;
   const int v = rec->cstar * CW + 2 * lane;
@@ -333,13 +405,12 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   const float c = row_scale(p.temp[b]);
   float w0 = 0.f, w1 = 0.f;
   if (in) {
+    const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&upair);
     float d0 = 0.f, d1 = 0.f;
-    for (int w = 0; w < kEpiWarps; ++w) {
+    for (int w = 0; w < kTeamWarps; ++w) {
       d0 = __fadd_rn(d0, red[w * 64 + 2 * lane]);
       d1 = __fadd_rn(d1, red[w * 64 + 2 * lane + 1]);
     }
-    const __nv_bfloat162 uv =
-        *reinterpret_cast<const __nv_bfloat162*>(p.U + ((size_t)b * p.G + k) * p.V + v);
     const float2 fu = __bfloat1622float2(uv);
     w0 = exp_shifted(scale_logit(add_base(fu.x, d0), c), rec->m);
     w1 = exp_shifted(scale_logit(add_base(fu.y, d1), c), rec->m);
@@ -365,8 +436,8 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
     }
   }
   if (lane == 0) {
-    p.tokens[(size_t)b * p.G + k] = tok;
-    prefetch_row(p.W1 + (size_t)tok * p.r, p.r);
+    prefetch_row(p.W1 + (size_t)tok * p.r, p.r);  // for the E gathers
+    st_release_s32(&p.tokens[(size_t)b * p.G + k], tok);
     const_cast<SelRec*>(rec)->tok = tok;
   }
 }
@@ -569,7 +640,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto gather = [&](int k) {
       int x = 0;
       if (vrow) {
-        x = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+        if (k == 0) {
+          x = p.anchor[b];
+        } else {
+          x = token_wait(&p.tokens[(size_t)b * p.G + k - 1], abort_flag);
+          if (x == kTokPending) {
+            fail();
+            x = 0;
+          }
+        }
         if (x < 0 || x >= p.V) {
           if (g == 0) report_error(p.hdr, DSPARK_BAD_INPUT, x);
           x = 0;
@@ -577,20 +656,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r);
       const uint32_t slot = tmem + lane_bits + (uint32_t)((k & 1) * kESlotCols);
-      // group g copies the 64-element pieces g, g + 2 of its rows
-#pragma unroll 1
-      for (int pc = g; pc < npieces; pc += kGroups) {
-        uint32_t wv[32];
+      // group g copies the 64-element pieces g, g + 2 of its rows (all loads
+      // in flight before the first store)
+      constexpr int kPer = 2 * kESlotCols / 64 / kGroups;
+      uint32_t wv[kPer][32];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int pc = g + i * kGroups;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const uint4 qv = vrow ? src[pc * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
-          wv[4 * e] = qv.x;
-          wv[4 * e + 1] = qv.y;
-          wv[4 * e + 2] = qv.z;
-          wv[4 * e + 3] = qv.w;
+          const uint4 qv = (vrow && pc < npieces) ? src[pc * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
+          wv[i][4 * e] = qv.x;
+          wv[i][4 * e + 1] = qv.y;
+          wv[i][4 * e + 2] = qv.z;
+          wv[i][4 * e + 3] = qv.w;
         }
-        __syncwarp();
-        ptx::tmem_st32(slot + (uint32_t)(pc * 32), wv);
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int pc = g + i * kGroups;
+        if (pc < npieces) {  // warp-uniform
+          __syncwarp();
+          ptx::tmem_st32(slot + (uint32_t)(pc * 32), wv[i]);
+        }
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -600,35 +688,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // the select of position k for the rows this CTA serves: levels 1 and 2 one
     // warp per row (up to eight rows at a time), then the chunk recompute and
-    // walk of each sampled row with all eight warps
+    // walk of the sampled rows, two at a time (one per team of four warps)
     auto select = [&](int k) {
       SelRec* recs = reinterpret_cast<SelRec*>(sStg);
       float* red = reinterpret_cast<float*>(sStg + 8 * sizeof(SelRec));
+      const int team = ew / kTeamWarps, tw = ew % kTeamWarps;
       for (int base = (int)blockIdx.x; base < p.B; base += p.n_ctas * kEpiWarps) {
         const int rb = base + p.n_ctas * ew;
         if (lane == 0) recs[ew].cstar = -2;  // no row
         __syncwarp();
         if (rb < p.B) select_levels(p, rb, k, lane, &recs[ew]);
         epi_sync();
-        for (int w = 0; w < kEpiWarps; ++w) {
-          const int cst = recs[w].cstar;
-          if (cst < 0) continue;  // greedy row (done) or none
-          chunk_dot(p, recs[w].b, k, cst, ew, lane, red);
+        unsigned pend = 0;  // sampled records still to walk
+        for (int w = 0; w < kEpiWarps; ++w)
+          if (recs[w].cstar >= 0) pend |= 1u << w;
+        while (pend) {
+          int wm = __ffs(pend) - 1;
+          pend &= pend - 1;
+          if (team == 1) {
+            wm = pend ? __ffs(pend) - 1 : -1;
+          }
+          if (pend) pend &= pend - 1;
+          // the walking warp fetches the chunk's U pairs before the recompute
+          uint32_t upair = 0u;
+          if (wm >= 0 && tw == 0) {
+            const int v = recs[wm].cstar * CW + 2 * lane;
+            if (v < p.V)
+              upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)recs[wm].b * G + k) * p.V + v));
+          }
+          if (wm >= 0) chunk_dot(p, recs[wm].x, recs[wm].cstar, tw, lane, red + team * kTeamWarps * 64);
           epi_sync();
-          if (ew == 0) chunk_walk(p, &recs[w], k, lane, red);
+          if (wm >= 0 && tw == 0) chunk_walk(p, &recs[wm], k, lane, red + team * kTeamWarps * 64, upair);
           epi_sync();
         }
-        // the confidence of position k + 1 of each row, from its chosen token
-        if (k + 1 < p.G && recs[ew].cstar != -2) conf_of(p, recs[ew].b, k + 1, recs[ew].tok, lane);
         // every warp has read the round's records before the next round writes them
         epi_sync();
       }
     };
 
-    // confidence of position 0 (from the anchors); later positions' come from
-    // the select that chooses their previous token
+    // tokens of the rows this CTA selects: not chosen yet (ordered before
+    // every wait on them by the first grid barrier)
     for (int rb = (int)blockIdx.x + p.n_ctas * ew; rb < p.B; rb += p.n_ctas * kEpiWarps)
-      conf_of(p, rb, 0, p.anchor[rb], lane);
+      for (int k = lane; k < G; k += 32) p.tokens[(size_t)rb * G + k] = kTokPending;
     if (!*abort_flag) gather(0);
     for (int q = 0; q <= G && alive; ++q) {
       const int s = q - 1;
@@ -637,10 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rm = 0.f, rinvS = 1.f;
       int xs = -1;
       if (hasW && vrow) {
+        // the select of another CTA publishes (m, S) and then x_s
+        xs = token_wait(&p.tokens[(size_t)b * p.G + s], abort_flag);
+        if (xs == kTokPending) fail();
         const float2 st = __ldcg(&p.rowstat[b]);
         rm = st.x;
         rinvS = inv_sum(st.y);
-        xs = __ldcg(&p.tokens[(size_t)b * p.G + s]);
       }
       float gm = -INFINITY, gs = 0.f, gav = -INFINITY;
       int gai = INT_MAX;
@@ -816,14 +919,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       select(q);
-      if (!grid_barrier(p, ++nbar * (unsigned)p.n_ctas, abort_flag, s_ok, epi_tid)) {
-        if (epi_tid == 0) fail();
-        alive = false;
-        break;
-      }
       // E of the next sweep's S items (slot (q + 1) & 1 held E_{q-1}, whose
-      // products all finished in this sweep)
+      // products all finished in this sweep); the gather waits for each row's
+      // token, so no grid barrier follows the select: a CTA's next writes of a
+      // row's partials come after it has seen the row's token, i.e. after the
+      // select finished reading them
       if (q + 1 < G) gather(q + 1);
+    }
+    // the confidences c_k = sigmoid(w_h . h_k + w_e . W1[x_{k-1}]) of every
+    // row and position, once all tokens are chosen (nothing above reads them)
+    if (alive && !*abort_flag) {
+      for (int t = (int)blockIdx.x * kEpiWarps + ew; t < p.B * G; t += p.n_ctas * kEpiWarps) {
+        const int rb = t / G, k = t % G;
+        const int x = (k == 0) ? p.anchor[rb] : token_wait(&p.tokens[(size_t)rb * G + k - 1], abort_flag);
+        conf_of(p, rb, k, x, lane);
+      }
     }
     if (lane == 0) ptx::bulk_wait0();
   }
