@@ -1,5 +1,6 @@
 // C ABI of the dspark library: argument checks, workspace layout, dispatch.
 // Every check happens before anything is enqueued; nothing here allocates.
+#include <algorithm>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -48,11 +49,14 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.sel = take(B * sizeof(float4));
   L.E = take(2 * B * r * elem_size(d.dtype));  // two buffers: positions alternate
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
-  L.part = take(B * ntiles * sizeof(float4));
+  // (the fused draft kernel keeps float2 partials of 64-column chunks, rows
+  // padded to a multiple of 128)
+  const size_t fused_row = ((V + 64 * 128 - 1) / (64 * 128)) * 128 * sizeof(float2);
+  L.part = take(B * std::max(ntiles * sizeof(float4), fused_row));
   L.segpart = take(B * kDraftMaxSeg * sizeof(float4));
-  // grid-barrier counter, then one pass-2 tile counter per (position, M-tile);
-  // all zeroed by one memset per draft call
-  L.gbar = take(16 + G * ((B + 127) / 128) * sizeof(uint32_t));
+  // grid-barrier counter, then one tile counter per (sweep, M-tile) (gamma + 1
+  // sweeps); all zeroed by one memset per draft call
+  L.gbar = take(16 + (G + 1) * ((B + 127) / 128) * sizeof(uint32_t));
   L.total = align_up(off, 256);
   return L;
 }

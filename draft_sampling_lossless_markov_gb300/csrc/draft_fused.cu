@@ -11,11 +11,14 @@
 //                                             partials of position k + 1
 // which halves the W2 traffic of the two-pass scheme.  The sweep needs E_{k+1}
 // = W1[x_k] at its start, so the token x_k is chosen before it: the select,
-// from the partials of the previous sweep, finds the 64-column chunk where the
-// inverse CDF crosses u S and recomputes that chunk's logits on the CUDA cores
-// (the E_k . W2 dot products in fp32) to walk it.  One persistent cooperative
-// launch runs all sweeps: S(0), then W(k) + S(k + 1) for k = 0 .. gamma - 1,
-// with grid barriers around each select.
+// from the chunk partials of the previous sweep, finds the 64-column chunk
+// where the inverse CDF crosses u S and recomputes that chunk's logits on the
+// CUDA cores (the E_k . W2 dot products in fp32) to walk it.  One persistent
+// cooperative launch runs all sweeps: S(0), then W(k) + S(k + 1) for
+// k = 0 .. gamma - 1.  A grid barrier separates a sweep from its select; the
+// next sweep waits only for the tokens of its own rows (release/acquire).
+// The CTAs serving an M-tile claim its vocabulary tiles one by one, so that
+// they finish a sweep together whatever their memory bandwidth.
 //
 // Tile 128 requests x 128 vocabulary columns.  TMEM: E_k and E_{k+1} in two
 // slots of r/2 columns, then two 128-column fp32 accumulators.
@@ -24,8 +27,8 @@
 //   warp 1    tcgen05.mma issuer: per tile the W item then the S item on the
 //             same W2 stages, alternating accumulators
 //   warps 2-9 epilogue, two groups of four warps; group g owns the g-th
-//             64-column chunk of every item.  They also gather E, run the
-//             select and the grid barriers.
+//             64-column chunk of every item.  They also gather E and run
+//             the select (two teams of four warps, one row each).
 // Every wait gives up after two seconds and the kernel records DSPARK_TIMEOUT.
 #include <cuda.h>
 
@@ -66,15 +69,21 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kESlotCols = 128;           // r / 2 columns, r <= 256
 constexpr uint32_t kAccCol0 = 2 * kESlotCols;
 constexpr int kTailBytes = 1024;
+constexpr int kTQ = 16;                        // tile-queue slots (the producer runs < 8 tiles ahead)
+constexpr int kMaxE = 20;                      // chunk partials per lane in the select (V <= 20 * 128 * 64)
 constexpr size_t kSmemBytes =
     1024 + NW * (size_t)kW2Stage + NU * (size_t)kUStage + (size_t)kEpiWarps * kStagingPerWarp + kTailBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-// select scratch in the (idle) staging area: 8 warps x 64 partial logits, 8 row records
-static_assert(kEpiWarps * 64 * 4 + 8 * 8 * 4 <= kEpiWarps * kStagingPerWarp, "select scratch");
+// select scratch in the (idle) staging area: per team a row record, 16 words of
+// exchange and four warps' 64 partial logits
+constexpr int kSelRecOff = 0, kSelXwOff = 128, kSelRedOff = 256;
+static_assert(kSelRedOff + 2 * kTeamWarps * 64 * 4 <= kEpiWarps * kStagingPerWarp, "select scratch");
 
 struct Params {
   int B, G, V, r, H;
-  int ntiles, nparts, ctas_per_m, n_ctas;
+  int ntiles, nparts, ctas_per_m, n_ctas, n_mtiles;
+  int ept;                   // chunk partials per select lane: E = ceil(nparts / 128)
+  int pstride;               // row stride of part: 128 E
   uint64_t seed;
   const __nv_bfloat16* U;    // [B, G, V] (the select's chunk recompute)
   const __nv_bfloat16* W1;   // [V, r]
@@ -86,18 +95,16 @@ struct Params {
   const uint32_t* req_id;    // [B]
   float2* rowstat;           // [B] (m, S) of the last selected position
   int32_t* tokens;           // [B, G]
-  float4* part;              // [B, nparts]
-  float4* segpart;           // [B, kDraftMaxSeg]
+  float2* part;              // [B, pstride] (max, sum) of a sampled row's chunk j, (value, index) of a
+                             // greedy row's, at (j % E) 128 + j / E: the select's lanes read it coalesced
   float* pd_tok;
   float* conf_logit;
   float* conf;
   unsigned* gbar;            // grid barrier counter, zero at launch
+  unsigned* sched;           // [G + 1, n_mtiles] tile claims of each sweep, zero at launch
   WsHeader* hdr;
 };
 
-__host__ __device__ __forceinline__ int seg_begin(int j, int ntiles, int nseg) {
-  return (int)(((long long)j * ntiles) / nseg);
-}
 
 __device__ __forceinline__ void epi_sync() {
   __syncwarp();
@@ -211,35 +218,50 @@ struct SelRec {
   int tok;        // the chosen token
 };
 
-// Levels 1 and 2 of the select of row b at position k (one warp): the row max m
-// and sum S from the segment partials, u = Philox(seed, req, k + 1, draw 0),
-// the segment and then the 64-column chunk where the running sum first exceeds
-// u S ([DSpark] 方法细节, 草稿采样: inverse CDF in token-id order).  Greedy rows
-// get their token (argmax, lowest id on ties) here.
-__device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* rec) {
+__device__ __forceinline__ void team_sync(int team) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + team), "n"(kTeamWarps * 32) : "memory");
+}
+
+// The pass of the select of row b at position k over its chunk partials, by
+// one team of four warps: lane tl = 32 tw + lane holds the partials
+// [tl E, tl E + E) in token order.  Sampled rows: the row max m, the sum S of
+// 2^(y - m), u = Philox(seed, req, k + 1, draw 0) and the 64-column chunk where
+// the running sum in token order first exceeds u S ([DSpark] 方法细节, 草稿采样:
+// inverse CDF), recorded for the recompute; (m, S) goes to rowstat.  Greedy
+// rows get their token here (argmax, lowest id on ties), published with a
+// release store.  The caller syncs the team before it reads the record.
+__device__ void team_levels(const Params& p, int b, int k, int team, int tw, int lane, SelRec* rec, float* xw) {
   constexpr unsigned FULL = 0xffffffffu;
-  const int nseg = p.ctas_per_m;
-  const float4* SP = p.segpart + (size_t)b * kDraftMaxSeg;
-  constexpr int MAXT = kDraftMaxSeg / 32;
-  // the segment partials first: both kinds of row need them
-  float4 sp[MAXT];
+  const int E = p.ept;
+  const int j0 = (tw * 32 + lane) * E;
+  // partial j0 + t sits at t 128 + tl: each load is one coalesced row of the team
+  const float2* P = p.part + (size_t)b * p.pstride + tw * 32 + lane;
+  float2 e[kMaxE];
 #pragma unroll
-  for (int t = 0; t < MAXT; ++t) {
-    if (t * 32 >= nseg) break;  // warp-uniform
-    const int j = t * 32 + lane;
-    sp[t] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));
-    if (j < nseg) sp[t] = __ldcg(&SP[j]);
+  for (int t = 0; t < kMaxE; ++t) {
+    if (t >= E) break;  // uniform
+    e[t] = (j0 + t < p.nparts) ? __ldcg(&P[t * 128]) : make_float2(-INFINITY, 0.f);
   }
-  if (!(p.temp[b] > 0.f)) {
+  const float T = p.temp[b];
+  const int xprev = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+  const uint32_t req = p.req_id[b];
+  if (!(T > 0.f)) {
     float av = -INFINITY;
     int ai = INT_MAX;
 #pragma unroll
-    for (int t = 0; t < MAXT; ++t) {
-      if (t * 32 >= nseg) break;
-      argmax_merge(av, ai, sp[t].z, __float_as_int(sp[t].w));
+    for (int t = 0; t < kMaxE; ++t) {
+      if (t >= E) break;
+      if (j0 + t < p.nparts) argmax_merge(av, ai, e[t].x, __float_as_int(e[t].y));
     }
     warp_argmax(av, ai);
     if (lane == 0) {
+      xw[2 * tw] = av;
+      xw[2 * tw + 1] = __int_as_float(ai);
+    }
+    team_sync(team);
+    if (tw == 0 && lane == 0) {
+      for (int w = 1; w < kTeamWarps; ++w) argmax_merge(av, ai, xw[2 * w], __float_as_int(xw[2 * w + 1]));
       p.rowstat[b] = make_float2(0.f, 1.f);
       if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);  // for the E gathers
       st_release_s32(&p.tokens[(size_t)b * p.G + k], ai);
@@ -249,88 +271,82 @@ __device__ void select_levels(const Params& p, int b, int k, int lane, SelRec* r
     }
     return;
   }
-  const int xprev = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
-  const uint32_t req = (uint32_t)p.req_id[b];
-  float m = -INFINITY;
+  float ml = -INFINITY;
 #pragma unroll
-  for (int t = 0; t < MAXT; ++t) {
-    if (t * 32 >= nseg) break;
-    m = fmaxf(m, sp[t].x);
+  for (int t = 0; t < kMaxE; ++t) {
+    if (t >= E) break;
+    ml = fmaxf(ml, e[t].x);
   }
-  m = warp_max(m);
-  float q[MAXT], incl[MAXT], excl[MAXT];
-  float carry = 0.f;
+  ml = warp_max(ml);
+  if (lane == 0) xw[tw] = ml;
+  team_sync(team);
+  const float m = fmaxf(fmaxf(xw[0], xw[1]), fmaxf(xw[2], xw[3]));
+  float sl = 0.f;
+  int tlast = -1;
 #pragma unroll
-  for (int t = 0; t < MAXT; ++t) {
-    if (t * 32 >= nseg) break;  // warp-uniform
-    const int j = t * 32 + lane;
-    q[t] = (j < nseg) ? tile_mass(sp[t].x, sp[t].y, m) : 0.f;
-    incl[t] = __fadd_rn(carry, warp_inclusive_scan(q[t]));
-    const float up = __shfl_up_sync(FULL, incl[t], 1);
-    excl[t] = lane == 0 ? carry : up;
-    carry = __shfl_sync(FULL, incl[t], 31);
+  for (int t = 0; t < kMaxE; ++t) {
+    if (t >= E) break;
+    const float qm = tile_mass(e[t].x, e[t].y, m);
+    sl = __fadd_rn(sl, qm);
+    if (qm > 0.f) tlast = t;
   }
-  const float S = carry;
+  const float incl = warp_inclusive_scan(sl);
+  const float up = __shfl_up_sync(FULL, incl, 1);
+  const float excl = lane == 0 ? 0.f : up;
+  const int jl = __reduce_max_sync(FULL, (unsigned)(tlast >= 0 ? j0 + tlast + 1 : 0));  // last positive + 1
+  if (lane == 31) xw[4 + tw] = incl;
+  if (lane == 0) xw[12 + tw] = __int_as_float(jl);
+  team_sync(team);
+  float wbase = 0.f, S = 0.f;
+#pragma unroll
+  for (int w = 0; w < kTeamWarps; ++w) {
+    if (w == tw) wbase = S;
+    S = __fadd_rn(S, xw[4 + w]);
+  }
+  int jlast = 0;
+#pragma unroll
+  for (int w = 0; w < kTeamWarps; ++w) jlast = max(jlast, __float_as_int(xw[12 + w]));
+  jlast = max(jlast - 1, 0);
   const float u = philox_uniform(p.seed, req, (uint32_t)(k + 1), 0u);
   const float target = u * S;
-  int js = -1, jlast = -1;
-  float base = 0.f;
+  const float ex = __fadd_rn(wbase, excl);
+  const unsigned bal = __ballot_sync(FULL, j0 < p.nparts && __fadd_rn(wbase, incl) > target);
+  if (lane == 0) xw[8 + tw] = __int_as_float(bal ? __ffs(bal) - 1 : 32);
+  team_sync(team);
+  int cw = -1, cl = 32;
 #pragma unroll
-  for (int t = 0; t < MAXT; ++t) {
-    if (t * 32 >= nseg) break;  // warp-uniform
-    const int j = t * 32 + lane;
-    const unsigned bal = __ballot_sync(FULL, j < nseg && incl[t] > target);
-    if (js < 0 && bal) {
-      const int L = __ffs(bal) - 1;
-      js = t * 32 + L;
-      base = __shfl_sync(FULL, excl[t], L);
+  for (int w = kTeamWarps - 1; w >= 0; --w) {
+    const int L = __float_as_int(xw[8 + w]);
+    if (L < 32) {
+      cw = w;
+      cl = L;
     }
-    const unsigned bp = __ballot_sync(FULL, j < nseg && q[t] > 0.f);
-    if (bp) jlast = t * 32 + 31 - __clz(bp);
   }
-  bool hit = js >= 0;
-  if (!hit) js = max(jlast, 0);
-  // level 2: the 64-column chunks of segment js (tiles of 128 columns)
-  const int c_lo = seg_begin(js, p.ntiles, nseg) * NCH;
-  const int c_hi = min(seg_begin(js + 1, p.ntiles, nseg) * NCH, p.nparts);
-  const float4* P = p.part + (size_t)b * p.nparts;
-  int cstar = -1, clast = -1;
-  float cbase = 0.f, run = base;
-  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-    const int cc = c0 + lane;
-    float qc = 0.f;
-    if (cc < c_hi) {
-      const float4 pc = __ldcg(&P[cc]);
-      qc = tile_mass(pc.x, pc.y, m);
-    }
-    const float inc = __fadd_rn(run, warp_inclusive_scan(qc));
-    const float up = __shfl_up_sync(FULL, inc, 1);
-    const float ex = lane == 0 ? run : up;
-    if (hit && cstar < 0) {
-      const unsigned bal = __ballot_sync(FULL, cc < c_hi && inc > target);
-      if (bal) {
-        const int L = __ffs(bal) - 1;
-        cstar = c0 + L;
-        cbase = __shfl_sync(FULL, ex, L);
+  const bool writer = cw < 0 ? (tw == 0 && lane == 0) : (tw == cw && lane == cl);
+  if (writer) {
+    int cstar = -1;
+    float cbase = 0.f;
+    if (cw >= 0) {
+      // the crossing lane walks its own chunks
+      float run = ex;
+#pragma unroll
+      for (int t = 0; t < kMaxE; ++t) {
+        if (t >= E) break;
+        const float qm = tile_mass(e[t].x, e[t].y, m);
+        const float nr = __fadd_rn(run, qm);
+        if (cstar < 0 && j0 + t < p.nparts && nr > target) {
+          cstar = j0 + t;
+          cbase = run;
+        }
+        run = nr;
       }
     }
-    const unsigned bp = __ballot_sync(FULL, cc < c_hi && qc > 0.f);
-    if (bp) clast = c0 + 31 - __clz(bp);
-    run = __shfl_sync(FULL, inc, 31);
-  }
-  if (cstar < 0) {
-    hit = false;
-    cstar = clast >= 0 ? clast : c_lo;
-  }
-  // the chunk recompute reads these W2 columns next: start them towards L2
-  for (int i = lane; i < 2 * p.r; i += 32) {  // the chunk's 128 bytes of a row span at most two lines
-    const char* a = reinterpret_cast<const char*>(p.W2 + (size_t)(i >> 1) * p.V + (size_t)cstar * CW);
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(a + (i & 1) * 127));
-  }
-  if (lane == 0) {
-    // and the walk the chunk's 64 U values of position k
+    const bool hit = cstar >= 0;
+    // no crossing (reachable only through rounding): the last chunk with weight
+    if (!hit) cstar = (cw >= 0 && tlast >= 0) ? j0 + tlast : jlast;
+    // the walk reads the chunk's 64 U values of position k
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.U + ((size_t)b * p.G + k) * p.V + (size_t)cstar * CW));
-    // (m, S) now: the walk's release of the token, after a CTA barrier, publishes it
+    // (m, S) now: the walk's release of the token, after a team barrier, publishes it
     p.rowstat[b] = make_float2(m, S);
     rec->cstar = cstar;
     rec->hit = hit ? 1 : 0;
@@ -461,21 +477,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* eready = tempty + 2;
   uint64_t* mma_done = eready + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* tqfull = mma_done + 1;  // [kTQ]
+  volatile int* tq = reinterpret_cast<volatile int*>(tqfull + kTQ);  // [kTQ] tile of each queue entry, -1 ends a sweep
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tq) + kTQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = abort_flag + 1;
+  volatile int* e_seen = s_ok + 1;  // gathers the MMA issuer has waited for
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = (int)blockIdx.x / p.ctas_per_m;
-  const int n_lo = (int)blockIdx.x % p.ctas_per_m;
-  const int t_begin = seg_begin(n_lo, p.ntiles, p.ctas_per_m);
-  const int count = seg_begin(n_lo + 1, p.ntiles, p.ctas_per_m) - t_begin;
   const int row_base = m_tile * BM;
   const int G = p.G;
   // sweep q = 0 .. G: q = 0 is S(0) alone; q >= 1 is W(q - 1) + S(q) (no S in
-  // the last).  Sweeps alternate direction over the segment, so that each
-  // starts on the tiles the previous one read last.
-  auto tile_of = [&](int i, int q) { return (q & 1) ? t_begin + count - 1 - i : t_begin + i; };
+  // the last).  The CTAs of an M-tile claim its vocabulary tiles one at a time
+  // from a counter per sweep (the producer claims, and hands each tile to the
+  // MMA issuer and the epilogue through the tile queue); sweeps alternate the
+  // claim order, so that each starts on the tiles the previous one read last.
+  auto tile_of = [&](unsigned i, int q) {
+    return i >= (unsigned)p.ntiles ? -1 : ((q & 1) ? p.ntiles - 1 - (int)i : (int)i);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NW; ++s) {
@@ -492,7 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(eready, kEpiWarps);
     ptx::mbar_init(mma_done, 1);
+    for (int j = 0; j < kTQ; ++j) ptx::mbar_init(&tqfull[j], 1);
     *abort_flag = 0;
+    *e_seen = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -514,13 +536,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_last = ptx::policy_evict_last();
       const uint64_t pol_first = ptx::policy_evict_first();
-      int iw = 0, iu = 0;
+      int iw = 0, iu = 0, jq = 0;
       bool ok = true;
       for (int q = 0; q <= G && ok; ++q) {
         const int s = q - 1;
         const bool hasW = s >= 0, hasS = s + 1 < G;
-        for (int i = 0; i < count && ok; ++i) {
-          const int v0 = tile_of(i, q) * BN;
+        unsigned* claim = p.sched + (size_t)q * p.n_mtiles + m_tile;
+        int n = tile_of(atomicAdd(claim, 1u), q);
+        while (ok) {
+          // hand the tile (or the end of the sweep) to the MMA issuer and the
+          // epilogue; the arrive releases the queue entry
+          tq[jq % kTQ] = n;
+          ptx::mbar_arrive(&tqfull[jq % kTQ]);
+          ++jq;
+          if (n < 0) break;
+          const int v0 = n * BN;
+          n = tile_of(atomicAdd(claim, 1u), q);  // the next claim, in flight during the loads
           for (int kc = 0; kc < nkc; ++kc, ++iw) {
             const int st = iw % NW;
             if (!ptx::mbar_wait(&emptyW[st], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
@@ -556,19 +587,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, true);
-      int it = 0, iw = 0;
+      int it = 0, iw = 0, jq = 0;
       bool ok = true;
+      // E_q of sweep q's S items: the q-th gather.  Waited for in every such
+      // sweep, with tiles or without, so that no phase of eready is skipped.
+      auto wait_e = [&](int q) {
+        if (!ptx::mbar_wait(eready, (uint32_t)(q & 1), abort_flag, kWaitLimitNs)) return false;
+        *e_seen = q + 1;
+        return true;
+      };
       for (int q = 0; q <= G && ok; ++q) {
         const int s = q - 1;
         const bool hasW = s >= 0, hasS = s + 1 < G;
         bool e_ok = false;
-        for (int i = 0; i < count && ok; ++i) {
+        while (ok) {
+          if (!ptx::mbar_wait(&tqfull[jq % kTQ], (jq / kTQ) & 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const int n = tq[jq % kTQ];
+          ++jq;
+          if (n < 0) {
+            if (hasS && !e_ok) ok = wait_e(q);
+            break;
+          }
           bool staged = false;  // this tile's W2 stages waited for
           for (int item = 0; item < 2 && ok; ++item) {
             if (item == 0 ? !hasW : !hasS) continue;
             if (item == 1 && !e_ok) {
-              // E_{q} of this sweep's S items: the q-th gather
-              if (!ptx::mbar_wait(eready, (uint32_t)(q & 1), abort_flag, kWaitLimitNs)) {
+              if (!wait_e(q)) {
                 ok = false;
                 break;
               }
@@ -633,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = row_scale(T_);
     uint8_t* stg = sStg + ew * kStagingPerWarp;
     unsigned nbar = 0;
-    int it = 0, iu = 0;
+    int it = 0, iu = 0, jq = 0;
     bool alive = true;
 
     // E_k = W1[x_{k-1}] (x_0 = anchor) into TMEM slot k & 1
@@ -683,47 +730,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(eready);
+      if (lane == 0) {
+        // the MMA issuer has waited for the previous gather, so that no phase
+        // of eready runs ahead of it (a CTA may get no tile in a sweep)
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (*e_seen < k) {
+          if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            fail();
+            break;
+          }
+          __nanosleep(32);
+        }
+        ptx::mbar_arrive(eready);
+      }
     };
 
-    // the select of position k for the rows this CTA serves: levels 1 and 2 one
-    // warp per row (up to eight rows at a time), then the chunk recompute and
-    // walk of the sampled rows, two at a time (one per team of four warps)
+    // the select of position k for the rows this CTA serves (rows blockIdx.x +
+    // n_ctas j): team t of four warps takes j = t, t + 2, ...: the pass over the
+    // row's chunk partials, then for a sampled row the recompute of the
+    // crossing chunk and its walk
+    const int team = ew / kTeamWarps, tw = ew % kTeamWarps;
     auto select = [&](int k) {
-      SelRec* recs = reinterpret_cast<SelRec*>(sStg);
-      float* red = reinterpret_cast<float*>(sStg + 8 * sizeof(SelRec));
-      const int team = ew / kTeamWarps, tw = ew % kTeamWarps;
-      for (int base = (int)blockIdx.x; base < p.B; base += p.n_ctas * kEpiWarps) {
-        const int rb = base + p.n_ctas * ew;
-        if (lane == 0) recs[ew].cstar = -2;  // no row
-        __syncwarp();
-        if (rb < p.B) select_levels(p, rb, k, lane, &recs[ew]);
-        epi_sync();
-        unsigned pend = 0;  // sampled records still to walk
-        for (int w = 0; w < kEpiWarps; ++w)
-          if (recs[w].cstar >= 0) pend |= 1u << w;
-        while (pend) {
-          int wm = __ffs(pend) - 1;
-          pend &= pend - 1;
-          if (team == 1) {
-            wm = pend ? __ffs(pend) - 1 : -1;
-          }
-          if (pend) pend &= pend - 1;
+      SelRec* rec = reinterpret_cast<SelRec*>(sStg + kSelRecOff) + team;
+      float* xw = reinterpret_cast<float*>(sStg + kSelXwOff) + team * 16;
+      float* red = reinterpret_cast<float*>(sStg + kSelRedOff) + team * kTeamWarps * 64;
+      for (int j = team;; j += 2) {
+        const int rb = (int)blockIdx.x + p.n_ctas * j;
+        if (rb >= p.B) break;
+        team_levels(p, rb, k, team, tw, lane, rec, xw);
+        team_sync(team);
+        const int cstar = rec->cstar;
+        if (cstar >= 0) {
           // the walking warp fetches the chunk's U pairs before the recompute
           uint32_t upair = 0u;
-          if (wm >= 0 && tw == 0) {
-            const int v = recs[wm].cstar * CW + 2 * lane;
-            if (v < p.V)
-              upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)recs[wm].b * G + k) * p.V + v));
-          }
-          if (wm >= 0) chunk_dot(p, recs[wm].x, recs[wm].cstar, tw, lane, red + team * kTeamWarps * 64);
-          epi_sync();
-          if (wm >= 0 && tw == 0) chunk_walk(p, &recs[wm], k, lane, red + team * kTeamWarps * 64, upair);
-          epi_sync();
+          if (tw == 0 && cstar * CW + 2 * lane < p.V)
+            upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)rb * G + k) * p.V + cstar * CW + 2 * lane));
+          chunk_dot(p, rec->x, cstar, tw, lane, red);
+          team_sync(team);
+          if (tw == 0) chunk_walk(p, rec, k, lane, red, upair);
         }
-        // every warp has read the round's records before the next round writes them
-        epi_sync();
+        // the record, exchange words and partial logits are free for the next row
+        team_sync(team);
       }
+      // every warp is done with the scratch before the staging area is reused
+      epi_sync();
     };
 
     // tokens of the rows this CTA selects: not chosen yet (ordered before
@@ -745,14 +795,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         rm = st.x;
         rinvS = inv_sum(st.y);
       }
-      float gm = -INFINITY, gs = 0.f, gav = -INFINITY;
-      int gai = INT_MAX;
       float pdtok = 0.f;
       bool have_pdtok = false;
       const int ch = g;
       bool tiles_ok = true;
-      for (int i = 0; i < count && tiles_ok; ++i) {
-        const int n = tile_of(i, q);
+      while (tiles_ok) {
+        // the next tile this CTA claimed, or the end of the sweep
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tqfull[jq % kTQ], (jq / kTQ) & 1, abort_flag, kWaitLimitNs))) {
+          if (lane == 0) fail();
+          tiles_ok = false;
+          break;
+        }
+        const int n = tq[jq % kTQ];
+        ++jq;
+        if (n < 0) break;
         const int v0 = n * BN + ch * CW;
         const int nvalid = min(CW, p.V - v0);
         for (int item = 0; item < 2; ++item) {
@@ -833,17 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
               }
             }
-            if (!sampled) {
-              mc = av;
-              cs = 1.f;
-            }
-            if (v0 < p.V) {
-              if (vrow) p.part[(size_t)b * p.nparts + v0 / CW] = make_float4(mc, cs, av, __int_as_float(ai));
-              const float nm = fmaxf(gm, mc);
-              gs = __fadd_rn(tile_mass(gm, gs, nm), tile_mass(mc, cs, nm));
-              gm = nm;
-              argmax_merge(gav, gai, av, ai);
-            }
+            if (v0 < p.V && vrow)
+              p.part[(size_t)b * p.pstride + (v0 / CW) % p.ept * 128 + (v0 / CW) / p.ept] = sampled ? make_float2(mc, cs) : make_float2(av, __int_as_float(ai));
           } else {
             // W item: p_d^s = 2^(y - m) / S (one-hot for greedy rows)
             const int row0 = row_base + qd * 32;
@@ -894,25 +941,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (hasW && vrow && have_pdtok && !*abort_flag) p.pd_tok[(size_t)b * p.G + s] = pdtok;
       if (!hasS) break;  // the last sweep
 
-      // segment partial of position q = s + 1, through the idle staging area
+      // the staging area is free for the select's scratch once this warp's
+      // stores have read it; the grid barrier makes every chunk partial of
+      // position q visible
       if (lane == 0) ptx::bulk_wait_read0();
       __syncwarp();
-      float4* xch = reinterpret_cast<float4*>(sStg);
-      epi_sync();
-      xch[g * BM + row] = make_float4(gm, gs, gav, __int_as_float(gai));
-      epi_sync();
-      if (g == 0 && vrow && !*abort_flag) {
-        float m = gm;
-        for (int gg = 1; gg < kGroups; ++gg) m = fmaxf(m, xch[gg * BM + row].x);
-        float sum = 0.f, av = -INFINITY;
-        int ai = INT_MAX;
-        for (int gg = 0; gg < kGroups; ++gg) {
-          const float4 e = xch[gg * BM + row];
-          if (m != -INFINITY) sum = __fadd_rn(sum, tile_mass(e.x, e.y, m));
-          argmax_merge(av, ai, e.z, __float_as_int(e.w));
-        }
-        p.segpart[(size_t)b * kDraftMaxSeg + n_lo] = make_float4(m, sum, av, __int_as_float(ai));
-      }
       if (!grid_barrier(p, ++nbar * (unsigned)p.n_ctas, abort_flag, s_ok, epi_tid)) {
         if (epi_tid == 0) fail();
         alive = false;
@@ -1032,8 +1065,12 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.seed = a.seed;
   p.ntiles = (d.V + fz::BN - 1) / fz::BN;
   p.nparts = (d.V + fz::CW - 1) / fz::CW;
-  p.ctas_per_m = std::max(1, std::min(std::min(p.ntiles, sms / n_mtiles), kDraftMaxSeg));
+  p.ctas_per_m = std::max(1, std::min(p.ntiles, sms / n_mtiles));
   p.n_ctas = n_mtiles * p.ctas_per_m;
+  p.n_mtiles = n_mtiles;
+  p.ept = (p.nparts + fz::kTeamWarps * 32 - 1) / (fz::kTeamWarps * 32);
+  p.pstride = p.ept * fz::kTeamWarps * 32;
+  if (p.ept > fz::kMaxE) return cudaErrorNotSupported;
   p.U = static_cast<const __nv_bfloat16*>(a.U);
   p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
   p.W2 = static_cast<const __nv_bfloat16*>(a.W2);
@@ -1044,14 +1081,15 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.req_id = a.req_id;
   p.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
   p.tokens = a.tokens;
-  p.part = reinterpret_cast<float4*>(ws + L.part);
-  p.segpart = reinterpret_cast<float4*>(ws + L.segpart);
+  p.part = reinterpret_cast<float2*>(ws + L.part);
   p.pd_tok = a.pd_tok;
   p.conf_logit = a.conf_logit;
   p.conf = a.conf;
   p.gbar = reinterpret_cast<unsigned*>(ws + L.gbar);
+  p.sched = reinterpret_cast<unsigned*>(ws + L.gbar + 16);
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  cudaError_t e = cudaMemsetAsync(p.gbar, 0, sizeof(unsigned), s);
+  // the grid-barrier counter and the tile claims of every sweep
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, 16 + sizeof(unsigned) * (size_t)(d.gamma + 1) * n_mtiles, s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_ctas);
