@@ -44,6 +44,10 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.sv0 = take(B * G * sizeof(uint32_t));
   L.sv1 = take(B * G * sizeof(uint32_t));
   L.vrs = take(B * (G + 1) * RS_PARTS * sizeof(float4));
+  L.vm = take(B * sizeof(int32_t));
+  L.vrowT = take(B * (G + 1) * sizeof(float));
+  L.vfmeta = take(B * 4 * sizeof(int32_t));
+  L.vfstat = take(B * 4 * sizeof(float));
   L.zh = take(B * G * sizeof(float));
   L.rowstat = take(B * sizeof(float2));
   L.sel = take(B * sizeof(float4));
@@ -57,6 +61,7 @@ WsLayout ws_layout(const dspark_dims& d) {
   // grid-barrier counter, then one tile counter per (sweep, M-tile) (gamma + 1
   // sweeps); all zeroed by one memset per draft call
   L.gbar = take(16 + (G + 1) * ((B + 127) / 128) * sizeof(uint32_t));
+  L.vfin = take(B * 32 * ((((V + 255) / 256) + 31) / 32) * sizeof(float2));
   L.total = align_up(off, 256);
   return L;
 }

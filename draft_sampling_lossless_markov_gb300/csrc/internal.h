@@ -24,14 +24,20 @@ constexpr int kDraftMaxSeg = 160;
 struct WsLayout {
   size_t zh = 0;       // [B*G] f32: w_h . h_k
   size_t E = 0;        // [2][B*r] dtype: W1 rows of the previous tokens, two alternating buffers
-  size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index)
+  size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index);
+                       // the fused kernel keeps float2 partials of 64-column chunks there
   size_t rowstat = 0;  // [B] float2: (row max, row sum) of the current position
   size_t sel = 0;      // [B] float4: crossing chunk, prefix before it, target, hit (tensor-core path)
   size_t segpart = 0;  // [B*kDraftMaxSeg] float4: per vocabulary segment partials (tensor-core path)
-  size_t gbar = 0;     // u32 grid-barrier counter of the persistent draft kernel, then
-                       // [G * ceil(B/128)] u32 pass-2 tile counters (16 bytes in)
+  size_t gbar = 0;     // u32 grid-barrier counter of the persistent draft kernels, then
+                       // [(G+1) * ceil(B/128)] u32 tile counters (16 bytes in)
   size_t sk0 = 0, sk1 = 0, sv0 = 0, sv1 = 0;  // scheduler sort buffers [B*G] u32
   size_t vrs = 0;      // [B*(G+1)*RS_PARTS] float4: verify row-slice statistics
+  size_t vm = 0;       // [B] i32: verify accepted count
+  size_t vrowT = 0;    // [B*(G+1)] f32: temperature of each kept verify row
+  size_t vfmeta = 0;   // [B] int4: final row, rejecting?, sampled?, accepted count
+  size_t vfstat = 0;   // [B] float4: final row's max, 1/sum, scale
+  size_t vfin = 0;     // [B * 32 ceil(ceil(V/256)/32)] float2: verify chunk sums of the final draw
   size_t total = 0;
 };
 

@@ -8,12 +8,16 @@
 //
 // k_verify_rowstats  one CTA per slice of a kept row (request r, row j <= l_r):
 //                    max and sum of 2^(z c) (sampled) or argmax of z (greedy)
-// k_verify_finish    one CTA per request: the accept tests of all positions in
-//                    one warp (p_t at each draft token from the combined row
-//                    statistics), the first rejection, then one inverse-CDF draw
-//                    over the final row (residual or bonus): per-chunk sums in
-//                    shared memory, then a re-read of the one chunk that holds
-//                    the draw.
+// k_verify_final     one CTA per slice of a request's final row: the accept
+//                    tests (one warp, p_t at each draft token from the row
+//                    statistics), the first rejection m, then the weights of
+//                    the final draw (residual max(0, p_t - p_d), or the bonus
+//                    2^(y - max)) summed per 256-token chunk
+// k_verify_pick      one warp per request: inverse CDF over the chunk sums in
+//                    token order, then a re-read of the one chunk that holds
+//                    the draw
+#include <algorithm>
+
 #include "common.cuh"
 #include "draft_arith.cuh"
 #include "internal.h"
@@ -21,118 +25,118 @@
 namespace dspark {
 
 constexpr int RS_THREADS = 256;
-constexpr int FIN_THREADS = 1024;
+constexpr int RS_UNROLL = 2;            // 16-byte loads in flight per thread
 
-// Each kept row is split into RS_PARTS contiguous slices, one CTA per slice, so
-// that the grid is many small CTAs instead of one wave of big ones plus a
-// nearly empty second wave.  Partial per (row, slice): sampled rows store
-// (max y, sum 2^(y - max)); greedy rows store (argmax value, argmax index).
+// The temperature of every kept row (flattened row offsets[r] + j, j <= l_r),
+// so that the row statistics need one load per row.
+__global__ void k_verify_rowmap(const int32_t* __restrict__ offsets, const int32_t* __restrict__ ell,
+                                const float* __restrict__ temp, int B, int G, float* __restrict__ rowT) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = idx / (G + 1), j = idx % (G + 1);
+  if (r < B && j <= ell[r]) rowT[offsets[r] + j] = temp[r];
+}
+
+// Each kept row is split into RS_PARTS contiguous slices, one CTA per (row,
+// slice) item of the N_v = offsets[B] kept rows (flattened row order, so that
+// the CTAs past N_v, the grid's tail, return at once), RS_UNROLL 16-byte loads
+// in flight per thread.  Partial per (row, slice): sampled rows store (max y,
+// sum 2^(y - max)); greedy rows store (argmax value, argmax index).
 template <typename T>
 __global__ void __launch_bounds__(RS_THREADS) k_verify_rowstats(const T* __restrict__ target,
                                                                 const int32_t* __restrict__ offsets,
-                                                                const int32_t* __restrict__ ell,
-                                                                const float* __restrict__ temp, int V,
+                                                                const float* __restrict__ rowT, int B, int V,
                                                                 float4* __restrict__ rsp) {
   __shared__ float sm_a[RS_THREADS / 32], sm_b[RS_THREADS / 32];
   __shared__ int sm_i[RS_THREADS / 32];
-  const int r = blockIdx.x, j = blockIdx.y, part = blockIdx.z;
-  const int L = ell[r];
-  if (j > L) return;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const size_t row = (size_t)offsets[r] + j;
-  const T* z = target + row * V;
-  const float T_ = temp[r];
-  const bool sampled = T_ > 0.f;
-  const float c = row_scale(T_);
+  const int w = (int)blockIdx.x;
+  if (w >= offsets[B] * RS_PARTS) return;
   const bool vec = (V & 7) == 0;
   const int span = ((V + RS_PARTS - 1) / RS_PARTS + 7) & ~7;  // multiple of 8: vector loads stay aligned
-  const int lo = min(part * span, V), hi = min(lo + span, V);
-
-  if (sampled) {
-    float m = -INFINITY, s = 0.f;
+  {
+    const int n = w / RS_PARTS, part = w % RS_PARTS;
+    const float T_ = rowT[n];
+    const T* z = target + (size_t)n * V;
+    const bool sampled = T_ > 0.f;
+    const float c = row_scale(T_);
+    const int lo = min(part * span, V), hi = min(lo + span, V);
+    float m = -INFINITY, s = 0.f, av = -INFINITY;
+    int ai = INT_MAX;
     if (vec) {
-      for (int i = lo + tid * 8; i < hi; i += RS_THREADS * 8) {
-        float v[8];
-        load8_stream(z + i, v);
-        float lm = -INFINITY;
+      for (int i0 = lo + tid * 8; i0 < hi; i0 += RS_THREADS * 8 * RS_UNROLL) {
+        float v[RS_UNROLL][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v[e] = scale_logit(v[e], c);
-          lm = fmaxf(lm, v[e]);
-        }
-        if (lm > m) {
-          s = s * exp2f(m - lm);
-          m = lm;
-        }
+        for (int u = 0; u < RS_UNROLL; ++u)
+          if (i0 + u * RS_THREADS * 8 < hi) load8_stream(z + i0 + u * RS_THREADS * 8, v[u]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s += exp_shifted(v[e], m);
+        for (int u = 0; u < RS_UNROLL; ++u) {
+          if (i0 + u * RS_THREADS * 8 >= hi) break;
+          if (sampled) {
+            // c > 0: the max of z c is c times the max of z; each weight is
+            // 2^(z c - m) with one rounding (fma)
+            float zm = v[u][0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q) zm = fmaxf(zm, v[u][q]);
+            const float lm = scale_logit(zm, c);
+            if (lm > m) {
+              s = s * ex2_ftz(__fsub_rn(m, lm));
+              m = lm;
+            }
+            const float nm = -m;
+            float s2[2] = {0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) s2[q & 1] += ex2_ftz(fmaf(v[u][q], c, nm));
+            s += s2[0] + s2[1];
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) argmax_merge(av, ai, v[u][q], i0 + u * RS_THREADS * 8 + q);
+          }
+        }
       }
     } else {
       for (int i = lo + tid; i < hi; i += RS_THREADS) {
-        const float y = scale_logit(to_f32(z[i]), c);
-        if (y > m) {
-          s = s * exp2f(m - y);
-          m = y;
+        const float y0 = to_f32(z[i]);
+        if (sampled) {
+          const float y = scale_logit(y0, c);
+          if (y > m) {
+            s = s * exp2f(m - y);
+            m = y;
+          }
+          s += exp_shifted(y, m);
+        } else {
+          argmax_merge(av, ai, y0, i);
         }
-        s += exp_shifted(y, m);
       }
     }
-    warp_lse(m, s);
-    if (lane == 0) {
-      sm_a[wid] = m;
-      sm_b[wid] = s;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float M = sm_a[0], S = sm_b[0];
-      for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) lse_merge(M, S, sm_a[w_], sm_b[w_]);
-      rsp[row * RS_PARTS + part] = make_float4(M, S, 0.f, 0.f);
-    }
-  } else {
-    float av = -INFINITY;
-    int ai = INT_MAX;
-    if (vec) {
-      for (int i = lo + tid * 8; i < hi; i += RS_THREADS * 8) {
-        float v[8];
-        load8_stream(z + i, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) argmax_merge(av, ai, v[e], i + e);
+    if (sampled) {
+      warp_lse(m, s);
+      if (lane == 0) {
+        sm_a[wid] = m;
+        sm_b[wid] = s;
       }
     } else {
-      for (int i = lo + tid; i < hi; i += RS_THREADS) argmax_merge(av, ai, to_f32(z[i]), i);
-    }
-    warp_argmax(av, ai);
-    if (lane == 0) {
-      sm_a[wid] = av;
-      sm_i[wid] = ai;
+      warp_argmax(av, ai);
+      if (lane == 0) {
+        sm_a[wid] = av;
+        sm_i[wid] = ai;
+      }
     }
     __syncthreads();
     if (tid == 0) {
-      for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) argmax_merge(av, ai, sm_a[w_], sm_i[w_]);
-      rsp[row * RS_PARTS + part] = make_float4(av, __int_as_float(ai), 0.f, 0.f);
+      float4 out;
+      if (sampled) {
+        float M = sm_a[0], S = sm_b[0];
+        for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) lse_merge(M, S, sm_a[w_], sm_b[w_]);
+        out = make_float4(M, S, 0.f, 0.f);
+      } else {
+        float A = sm_a[0];
+        int I = sm_i[0];
+        for (int w_ = 1; w_ < RS_THREADS / 32; ++w_) argmax_merge(A, I, sm_a[w_], sm_i[w_]);
+        out = make_float4(A, __int_as_float(I), 0.f, 0.f);
+      }
+      rsp[(size_t)n * RS_PARTS + part] = out;
     }
   }
-}
-
-// Row statistics from the slice partials, combined in slice order:
-// sampled rows -> (M, S) of the whole row; greedy rows -> argmax (in .z).
-__device__ __forceinline__ float4 row_stats(const float4* __restrict__ rsp, size_t row, bool sampled) {
-  const float4 p0 = rsp[row * RS_PARTS];
-  if (sampled) {
-    float M = p0.x, S = p0.y;
-    for (int q = 1; q < RS_PARTS; ++q) {
-      const float4 pq = rsp[row * RS_PARTS + q];
-      lse_merge(M, S, pq.x, pq.y);
-    }
-    return make_float4(M, S, __int_as_float(-1), 0.f);
-  }
-  float av = p0.x;
-  int ai = __float_as_int(p0.y);
-  for (int q = 1; q < RS_PARTS; ++q) {
-    const float4 pq = rsp[row * RS_PARTS + q];
-    argmax_merge(av, ai, pq.x, __float_as_int(pq.y));
-  }
-  return make_float4(0.f, 1.f, __int_as_float(ai), 0.f);
 }
 
 // q(v) of the final draw: residual max(0, p_t - p_d) or the bonus weight 2^(y - m)
@@ -143,9 +147,12 @@ __device__ __forceinline__ float final_weight(const T* z, const float* pd, int v
   return fmaxf(0.f, __fsub_rn(prob_from(y, m, invS), pd[v]));
 }
 
-// Chunks of 256 tokens (8 per lane) per warp segment; a segment holds at most
-// FIN_MAXCH of them, so V <= 32 * 256 * FIN_MAXCH = DSPARK_MAX_VOCAB.
-constexpr int FIN_MAXCH = 256;
+// The final draw works on 256-token chunks (8 tokens per lane of a warp).
+constexpr int FN_THREADS = 256;
+constexpr int FN_SLICES = 8;        // CTAs per request's final row
+constexpr int PK_WARPS = 4;         // requests per CTA of k_verify_pick
+constexpr int AC_WARPS = 8;         // warps per request in k_verify_accept
+constexpr int PK_REG = 24;          // chunk sums per lane the pick keeps in registers (V <= 196608)
 
 // q of the 8 tokens v0..v0+7 (masked past hi), with vector loads when the row
 // allows them; both branches evaluate final_weight's formula
@@ -171,200 +178,320 @@ __device__ __forceinline__ float lane_sum8(const float (&q)[8]) {
   return ((q[0] + q[1]) + (q[2] + q[3])) + ((q[4] + q[5]) + (q[6] + q[7]));
 }
 
-// One CTA draws a token from the unnormalised weights q over the row by
-// inverse CDF in token order: the sum runs over 32 warp segments, each a
-// sequence of 256-token chunks.  Pass 1 records every chunk's total in shared
-// memory (loads of consecutive chunks overlap); the warp whose segment holds
-// u * sum then finds the chunk from those totals and re-reads only that chunk
-// to find the token.  Rounding that leaves no crossing falls back to the last
-// token with positive weight of the chosen segment or chunk.
-template <typename T, int MODE>
-__device__ int final_draw(const T* z, const float* pd, int V, float c, float m, float invS, float u, float* tot,
-                          float* sm_seg, int* sm_int, float* sm_flt, bool& zero_mass) {
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  constexpr int NW = FIN_THREADS / 32;
-  const int seg = (((V + NW - 1) / NW) + 255) & ~255;
-  const int s_lo = min(wid * seg, V), s_hi = min(s_lo + seg, V);
-  const int nch = (s_hi - s_lo + 255) >> 8;
-  const bool vec = (V & 7) == 0;
-  float acc = 0.f;
-#pragma unroll 4
-  for (int ci = 0; ci < nch; ++ci) {
-    float q[8];
-    chunk_weights<T, MODE>(z, pd, s_lo + ci * 256 + lane * 8, s_hi, vec, c, m, invS, q);
-    const float ct = warp_sum(lane_sum8(q));
-    if (lane == 0) tot[wid * FIN_MAXCH + ci] = ct;
-    acc += ct;
-  }
-  if (lane == 0) sm_seg[wid] = acc;
+// One CTA per request: warp w takes the rows j = w, w + AC_WARPS, .. <= L of
+// the request; the row statistics come from its RS_PARTS slice partials (one
+// per lane, merged across the warp); for j < L the accept test of position
+// j + 1 (p_t at the draft token from the statistics, u * p_d < p_t, or the
+// argmax compare at temperature 0).  The first rejection ends the accepted
+// prefix: vm[r] = m, and the final row's record goes to fmeta / fstat.
+template <typename T>
+__global__ void __launch_bounds__(AC_WARPS * 32) k_verify_accept(const T* __restrict__ target,
+                                                                 const int32_t* __restrict__ offsets,
+                                                                 const int32_t* __restrict__ ell,
+                                                                 const int32_t* __restrict__ tokens,
+                                                                 const float* __restrict__ pd_tok,
+                                                                 const float* __restrict__ temp,
+                                                                 const uint32_t* __restrict__ req_id, uint64_t seed,
+                                                                 int G, int V, const float4* __restrict__ rs,
+                                                                 int32_t* __restrict__ vm, int4* __restrict__ fmeta,
+                                                                 float4* __restrict__ fstat, WsHeader* hdr) {
+  static_assert(RS_PARTS <= 32, "one slice partial per lane");
+  __shared__ float4 s_st[DSPARK_MAX_GAMMA + 1];
+  __shared__ unsigned s_rej[(DSPARK_MAX_GAMMA + 31) / 32 + 1];
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int L = ell[r];
+  const float T_ = temp[r];
+  const bool sampled = T_ > 0.f;
+  const float c = row_scale(T_);
+  const int base = offsets[r];
+  if (threadIdx.x < (DSPARK_MAX_GAMMA + 31) / 32 + 1) s_rej[threadIdx.x] = 0u;
   __syncthreads();
-  if (wid == 0) {
-    const float sv = sm_seg[lane];
-    const float incl = warp_inclusive_scan(sv);
-    const float total = __shfl_sync(0xffffffffu, incl, 31);
-    const float target = u * total;
-    const unsigned over = __ballot_sync(0xffffffffu, incl > target);
-    const unsigned pos = __ballot_sync(0xffffffffu, sv > 0.f);
-    const bool hit = over != 0u && total > 0.f;
-    const int w_star = hit ? __ffs(over) - 1 : (pos ? 31 - __clz(pos) : 0);
-    float pre = __shfl_up_sync(0xffffffffu, incl, 1);
-    pre = __shfl_sync(0xffffffffu, (lane == 0) ? 0.f : pre, w_star);
+  for (int j = wid; j <= L; j += AC_WARPS) {
+    const size_t row = (size_t)base + j;
+    const float4 p = lane < RS_PARTS ? rs[row * RS_PARTS + lane]
+                                     : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(INT_MAX));
+    int x = 0;
+    float ztok = 0.f;
+    if (j < L) {
+      x = tokens[(size_t)r * G + j];
+      if (x < 0 || x >= V) {
+        if (lane == 0) report_error(hdr, DSPARK_BAD_INPUT, x);
+        x = 0;
+      }
+      if (sampled) ztok = to_f32(target[row * V + x]);  // the same address in every lane
+    }
+    float4 st;
+    if (sampled) {
+      float M = p.x, S = p.y;
+      warp_lse(M, S);
+      st = make_float4(M, S, 0.f, 0.f);
+    } else {
+      float av = p.x;
+      int ai = __float_as_int(p.y);
+      warp_argmax(av, ai);
+      st = make_float4(0.f, 1.f, __int_as_float(ai), 0.f);
+    }
     if (lane == 0) {
-      sm_int[0] = w_star;
-      sm_int[1] = hit;
-      sm_flt[0] = pre;
-      sm_flt[1] = target;
-      sm_flt[2] = total;
+      s_st[j] = st;
+      if (j < L) {
+        bool acc;
+        if (sampled) {
+          const float ptok = prob_from(scale_logit(ztok, c), st.x, inv_sum(st.y));
+          const float u = philox_uniform(seed, req_id[r], (uint32_t)(j + 1), 1u);
+          acc = __fmul_rn(u, pd_tok[(size_t)r * G + j]) < ptok;
+        } else {
+          acc = x == __float_as_int(st.z);
+        }
+        if (!acc) atomicOr(&s_rej[j >> 5], 1u << (j & 31));
+      }
     }
   }
   __syncthreads();
-  zero_mass = !(sm_flt[2] > 0.f);
-  const int w_star = sm_int[0];
-  const bool hit = sm_int[1] != 0;
-  if (wid == w_star) {
-    const int g_lo = min(w_star * seg, V), g_hi = min(g_lo + seg, V);
-    const int gch = (g_hi - g_lo + 255) >> 8;
-    const float target = sm_flt[1];
-    float run = sm_flt[0];
-    int cstar = -1, lastc = -1;
-    float cpre = 0.f;
-    for (int c0 = 0; c0 < gch; c0 += 32) {
-      const int ci = c0 + lane;
-      const float tv = ci < gch ? tot[w_star * FIN_MAXCH + ci] : 0.f;
-      const float incl = warp_inclusive_scan(tv);
-      const unsigned over = __ballot_sync(0xffffffffu, hit && run + incl > target);
-      const unsigned pos = __ballot_sync(0xffffffffu, tv > 0.f);
-      if (pos) lastc = c0 + 31 - __clz(pos);
-      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) excl = 0.f;
-      if (over) {
-        const int Lc = __ffs(over) - 1;
-        cstar = c0 + Lc;
-        cpre = run + __shfl_sync(0xffffffffu, excl, Lc);
+  if (threadIdx.x == 0) {
+    int m = L;
+    for (int q = 0; q * 32 < L; ++q)
+      if (s_rej[q]) {
+        m = q * 32 + __ffs(s_rej[q]) - 1;
         break;
       }
-      run += __shfl_sync(0xffffffffu, incl, 31);
+    vm[r] = m;
+    const float4 st = s_st[m];
+    // sampled: (max, 1/sum, scale); greedy: the argmax of the final row, the
+    // output token
+    fmeta[r] = make_int4(base + m, m < L ? 1 : 0, sampled ? 1 : 0, m);
+    fstat[r] = sampled ? make_float4(st.x, inv_sum(st.y), c, 0.f) : make_float4(st.z, 0.f, 0.f, 0.f);
+  }
+}
+
+// Chunk sums of the final draw's weights, one CTA per slice of a sampled
+// request's final row (the accepted count and the row's statistics come from
+// k_verify_accept): chunk c of request r goes to fin[r][(c % E) 32 + c / E]
+// (E = ceil(nch / 32), the pick's lane-major order) as (mode weight, bonus
+// weight): the mode weight is the residual for a rejecting row and the bonus
+// weight otherwise; the bonus weight also serves a residual of zero mass.
+template <typename T>
+__global__ void __launch_bounds__(FN_THREADS) k_verify_final(const T* __restrict__ target,
+                                                             const float* __restrict__ pd_rows, int G, int V,
+                                                             const int4* __restrict__ fmeta,
+                                                             const float4* __restrict__ fstat,
+                                                             float2* __restrict__ fin) {
+  const int r = blockIdx.x, slice = blockIdx.y;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int4 fm = fmeta[r];
+  if (!fm.z) return;  // greedy: no draw
+  const float4 fs = fstat[r];
+  const bool resid = fm.y != 0;
+  const int m = fm.w;
+  const float M = fs.x, invS = fs.y, c = fs.z;
+  const T* z = target + (size_t)fm.x * V;
+  const float* pd = pd_rows + ((size_t)r * G + m) * V;
+  const bool vec = (V & 7) == 0;
+  const int nch = (V + 255) >> 8, E = (nch + 31) >> 5;
+  const int cps = (nch + FN_SLICES - 1) / FN_SLICES;
+  const int c_lo = slice * cps, c_hi = min(c_lo + cps, nch);
+  float2* F = fin + (size_t)r * E * 32;
+#pragma unroll 2
+  for (int ch = c_lo + wid; ch < c_hi; ch += FN_THREADS / 32) {
+    const int v0 = ch * 256 + lane * 8;
+    float qb[8], qm[8];
+    if (resid) {
+      // one read of the chunk: e = 2^(y - max) is the bonus weight, e / S - p_d
+      // the residual's
+      if (vec && v0 + 8 <= V) {
+        float zv[8], pv[8];
+        load8_stream(z + v0, zv);
+        load8_stream(pd + v0, pv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qb[e] = exp_shifted(scale_logit(zv[e], c), M);
+          qm[e] = fmaxf(0.f, __fsub_rn(__fmul_rn(qb[e], invS), pv[e]));
+        }
+      } else {
+        chunk_weights<T, 1>(z, nullptr, v0, V, vec, c, M, invS, qb);
+        chunk_weights<T, 0>(z, pd, v0, V, vec, c, M, invS, qm);
+      }
+    } else {
+      chunk_weights<T, 1>(z, nullptr, v0, V, vec, c, M, invS, qb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qm[e] = qb[e];
     }
-    const bool in_chunk = cstar >= 0;
-    if (!in_chunk) cstar = lastc;
-    int x = -1;
+    const float tm = warp_sum(lane_sum8(qm));
+    const float tb = warp_sum(lane_sum8(qb));
+    if (lane == 0) F[(ch % E) * 32 + ch / E] = make_float2(tm, tb);
+  }
+}
+
+// One warp per request: the outputs, and for a sampled row the inverse-CDF
+// draw over the final row in token order: lane l holds the chunk sums
+// [l E, l E + E) (in registers up to PK_REG of them), a warp scan finds the
+// lane, a scan of that lane's sums the chunk whose running sum first exceeds
+// u * total, and a re-read of that chunk the token.  Rounding that leaves no
+// crossing falls back to the last positive weight.  A residual of zero mass
+// (reachable only through rounding) draws from p_t instead, with the same u.
+template <typename T>
+__global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restrict__ target,
+                                                               const int32_t* __restrict__ ell,
+                                                               const int32_t* __restrict__ tokens,
+                                                               const float* __restrict__ pd_rows,
+                                                               const uint32_t* __restrict__ req_id, uint64_t seed,
+                                                               int B, int G, int V, const int4* __restrict__ fmeta,
+                                                               const float4* __restrict__ fstat,
+                                                               const float2* __restrict__ fin,
+                                                               int32_t* __restrict__ n_accept,
+                                                               int32_t* __restrict__ out_tok,
+                                                               int32_t* __restrict__ n_out) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * PK_WARPS + (threadIdx.x >> 5);
+  if (r >= B) return;
+  const int nch = (V + 255) >> 8, E = (nch + 31) >> 5;
+  const int c0 = lane * E;
+  const float2* F = fin + (size_t)r * E * 32;
+  // the chunk sums do not depend on the record: their loads go out with it
+  float2 f[PK_REG];
+  if (E <= PK_REG) {
+#pragma unroll
+    for (int t = 0; t < PK_REG; ++t) {
+      if (t >= E) break;
+      f[t] = c0 + t < nch ? F[t * 32 + lane] : make_float2(0.f, 0.f);
+    }
+  }
+  const int4 fm = fmeta[r];
+  const float4 fs = fstat[r];
+  const int m = fm.w, L = ell[r];
+  for (int i = lane; i <= G; i += 32) out_tok[(size_t)r * (G + 1) + i] = (i < m) ? tokens[(size_t)r * G + i] : -1;
+  int x;
+  if (!fm.z) {
+    x = __float_as_int(fs.x);
+  } else {
+    const bool resid = fm.y != 0;
+    const float u = resid ? philox_uniform(seed, req_id[r], (uint32_t)(m + 1), 2u)
+                          : philox_uniform(seed, req_id[r], (uint32_t)(L + 1), 3u);
+    auto entry = [&](int t) { return E <= PK_REG ? f[t] : F[t * 32 + lane]; };
+    // lane sums of its chunks (both kinds of weight), and its last chunk with
+    // positive weight of each kind
+    float sm = 0.f, sb = 0.f;
+    int lm = -1, lb = -1;
+#pragma unroll
+    for (int t = 0; t < PK_REG; ++t) {
+      if (t >= E || c0 + t >= nch) break;
+      const float2 e = entry(t);
+      sm = __fadd_rn(sm, e.x);
+      sb = __fadd_rn(sb, e.y);
+      if (e.x > 0.f) lm = c0 + t;
+      if (e.y > 0.f) lb = c0 + t;
+    }
+    for (int t = PK_REG; t < E; ++t) {  // beyond the register window
+      if (c0 + t >= nch) break;
+      const float2 e = F[t * 32 + lane];
+      sm = __fadd_rn(sm, e.x);
+      sb = __fadd_rn(sb, e.y);
+      if (e.x > 0.f) lm = c0 + t;
+      if (e.y > 0.f) lb = c0 + t;
+    }
+    const float tot_m = warp_sum(sm);
+    // the mode's weights, or p_t for a residual of zero mass
+    const bool use_b = resid && !(tot_m > 0.f);
+    const float sl = use_b ? sb : sm;
+    const float incl = warp_inclusive_scan(sl);
+    const float total = __shfl_sync(FULL, incl, 31);
+    const float tgt = u * total;
+    float ex = __shfl_up_sync(FULL, incl, 1);
+    if (lane == 0) ex = 0.f;
+    const unsigned over = __ballot_sync(FULL, total > 0.f && incl > tgt);
+    // the crossing lane walks its own chunks
+    int cstar = -1, clast = -1;
+    float cpre = 0.f, run = ex;
+#pragma unroll
+    for (int t = 0; t < PK_REG; ++t) {
+      if (t >= E || c0 + t >= nch) break;
+      const float2 e = entry(t);
+      const float w = use_b ? e.y : e.x;
+      const float nr = __fadd_rn(run, w);
+      if (w > 0.f) clast = c0 + t;
+      if (cstar < 0 && nr > tgt) {
+        cstar = c0 + t;
+        cpre = run;
+      }
+      run = nr;
+    }
+    for (int t = PK_REG; t < E; ++t) {
+      if (c0 + t >= nch) break;
+      const float2 e = F[t * 32 + lane];
+      const float w = use_b ? e.y : e.x;
+      const float nr = __fadd_rn(run, w);
+      if (w > 0.f) clast = c0 + t;
+      if (cstar < 0 && nr > tgt) {
+        cstar = c0 + t;
+        cpre = run;
+      }
+      run = nr;
+    }
+    bool in_chunk = false;
+    if (over) {
+      const int Lw = __ffs(over) - 1;
+      in_chunk = __shfl_sync(FULL, cstar >= 0 ? 1 : 0, Lw) != 0;
+      const int cs = __shfl_sync(FULL, cstar, Lw), cl = __shfl_sync(FULL, clast, Lw);
+      cpre = __shfl_sync(FULL, cpre, Lw);
+      cstar = in_chunk ? cs : cl;
+    } else {
+      cstar = -1;
+    }
+    if (cstar < 0) {
+      // no crossing: the last chunk with positive weight
+      int lc = use_b ? lb : lm;
+      for (int o = 16; o > 0; o >>= 1) lc = max(lc, __shfl_xor_sync(FULL, lc, o));
+      cstar = lc;
+      in_chunk = false;
+    }
+    x = -1;
     if (cstar >= 0) {
+      const T* z = target + (size_t)fm.x * V;
+      const float* pd = pd_rows + ((size_t)r * G + m) * V;
+      const float M = fs.x, invS = fs.y, c = fs.z;
+      const bool vec = (V & 7) == 0;
+      const int v0 = cstar * 256 + lane * 8;
       float q[8];
-      const int v0 = g_lo + cstar * 256 + lane * 8;
-      chunk_weights<T, MODE>(z, pd, v0, g_hi, vec, c, m, invS, q);
+      if (resid && !use_b)
+        chunk_weights<T, 0>(z, pd, v0, V, vec, c, M, invS, q);
+      else
+        chunk_weights<T, 1>(z, nullptr, v0, V, vec, c, M, invS, q);
       const float ls = lane_sum8(q);
-      const float incl = warp_inclusive_scan(ls);
+      const float li = warp_inclusive_scan(ls);
       int lastp = -1;
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         if (q[e] > 0.f) lastp = v0 + e;
       if (in_chunk) {
-        const unsigned over = __ballot_sync(0xffffffffu, cpre + incl > target);
-        if (over) {
-          const int Ll = __ffs(over) - 1;
-          float pre = __shfl_up_sync(0xffffffffu, incl, 1);
-          pre = __shfl_sync(0xffffffffu, (lane == 0) ? 0.f : pre, Ll);
+        const unsigned ov = __ballot_sync(FULL, cpre + li > tgt);
+        if (ov) {
+          const int Ll = __ffs(ov) - 1;
+          float pre = __shfl_up_sync(FULL, li, 1);
+          pre = __shfl_sync(FULL, (lane == 0) ? 0.f : pre, Ll);
           int xl = -1;
           if (lane == Ll) {
-            float a = cpre + pre;
+            float acc = cpre + pre;
             for (int e = 0; e < 8; ++e) {
-              a += q[e];
-              if (a > target) {
+              acc += q[e];
+              if (acc > tgt) {
                 xl = v0 + e;
                 break;
               }
             }
             if (xl < 0) xl = lastp;
           }
-          x = __shfl_sync(0xffffffffu, xl, Ll);
+          x = __shfl_sync(FULL, xl, Ll);
         }
       }
       if (x < 0) {  // rounding left no crossing: last positive weight of the chunk
         int lp = lastp;
-        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
         x = lp;
       }
     }
-    if (lane == 0) sm_int[2] = x;
   }
-  __syncthreads();
-  const int x = sm_int[2];
-  __syncthreads();
-  return x;
-}
-
-template <typename T>
-__global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restrict__ target,
-                                                               const int32_t* __restrict__ offsets,
-                                                               const int32_t* __restrict__ ell,
-                                                               const int32_t* __restrict__ tokens,
-                                                               const float* __restrict__ pd_rows,
-                                                               const float* __restrict__ pd_tok,
-                                                               const float* __restrict__ temp,
-                                                               const uint32_t* __restrict__ req_id, uint64_t seed,
-                                                               int G, int V, const float4* __restrict__ rs,
-                                                               int32_t* __restrict__ n_accept,
-                                                               int32_t* __restrict__ out_tok,
-                                                               int32_t* __restrict__ n_out, WsHeader* hdr) {
-  __shared__ float tot[32 * FIN_MAXCH];
-  __shared__ float sm_seg[32];
-  __shared__ int sm_int[4];
-  __shared__ float sm_flt[4];
-  __shared__ int s_m;
-  const int r = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int L = ell[r];
-  const float T_ = temp[r];
-  const bool sampled = T_ > 0.f;
-  const uint32_t req = req_id[r];
-  const int base = offsets[r];
-  if (tid < 32) {
-    // the accept tests of positions 1..L in parallel (gamma <= 32); the first
-    // rejection ends the accepted prefix
-    const int j = tid;
-    bool acc = true;
-    if (j < L) {
-      const size_t row = (size_t)base + j;
-      const float4 st = row_stats(rs, row, sampled);
-      int x = tokens[(size_t)r * G + j];
-      if (x < 0 || x >= V) {
-        report_error(hdr, DSPARK_BAD_INPUT, x);
-        x = 0;
-      }
-      if (sampled) {
-        const float c = row_scale(T_);
-        const float ptok = prob_from(scale_logit(to_f32(target[row * V + x]), c), st.x, inv_sum(st.y));
-        const float u = philox_uniform(seed, req, (uint32_t)(j + 1), 1u);
-        acc = __fmul_rn(u, pd_tok[(size_t)r * G + j]) < ptok;
-      } else {
-        acc = x == __float_as_int(st.z);
-      }
-    }
-    const unsigned rej = __ballot_sync(0xffffffffu, !acc);
-    if (tid == 0) s_m = rej ? __ffs(rej) - 1 : L;
-  }
-  __syncthreads();
-  const int m = s_m;
-  for (int i = tid; i <= G; i += FIN_THREADS) out_tok[(size_t)r * (G + 1) + i] = (i < m) ? tokens[(size_t)r * G + i] : -1;
-  const float4 st = row_stats(rs, (size_t)base + m, sampled);
-  int x;
-  if (!sampled) {
-    x = __float_as_int(st.z);
-  } else {
-    const T* z = target + ((size_t)base + m) * V;
-    const float c = row_scale(T_);
-    bool zero_mass = false;
-    if (m < L) {
-      const float u = philox_uniform(seed, req, (uint32_t)(m + 1), 2u);
-      const float* pd = pd_rows + ((size_t)r * G + m) * V;
-      x = final_draw<T, 0>(z, pd, V, c, st.x, inv_sum(st.y), u, tot, sm_seg, sm_int, sm_flt, zero_mass);
-      if (zero_mass) x = final_draw<T, 1>(z, pd, V, c, st.x, inv_sum(st.y), u, tot, sm_seg, sm_int, sm_flt, zero_mass);
-    } else {
-      const float u = philox_uniform(seed, req, (uint32_t)(L + 1), 3u);
-      x = final_draw<T, 1>(z, nullptr, V, c, st.x, inv_sum(st.y), u, tot, sm_seg, sm_int, sm_flt, zero_mass);
-    }
-  }
-  if (tid == 0) {
+  if (lane == 0) {
     out_tok[(size_t)r * (G + 1) + m] = x;
     n_accept[r] = m;
     n_out[r] = m + 1;
@@ -374,13 +501,24 @@ __global__ void __launch_bounds__(FIN_THREADS) k_verify_finish(const T* __restri
 template <typename T>
 static cudaError_t launch_verify_t(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const int B = a.dims.B, G = a.dims.gamma, V = a.dims.V;
+  if (B == 0) return cudaSuccess;
   float4* rs = reinterpret_cast<float4*>(ws + L.vrs);
+  float2* fin = reinterpret_cast<float2*>(ws + L.vfin);
+  int32_t* vm = reinterpret_cast<int32_t*>(ws + L.vm);
+  float* rowT = reinterpret_cast<float*>(ws + L.vrowT);
+  int4* fmeta = reinterpret_cast<int4*>(ws + L.vfmeta);
+  float4* fstat = reinterpret_cast<float4*>(ws + L.vfstat);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const T* tg = static_cast<const T*>(a.target_logits);
-  k_verify_rowstats<T><<<dim3(B, G + 1, RS_PARTS), RS_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.temp, V, rs);
-  k_verify_finish<T><<<B, FIN_THREADS, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.pd_rows, a.pd_tok, a.temp,
-                                               a.req_id, a.seed, G, V, rs, a.n_accept, a.out_tok, a.n_out, hdr);
-  count_launches(2);
+  const int nw = (B + PK_WARPS - 1) / PK_WARPS;
+  k_verify_rowmap<<<(B * (G + 1) + 255) / 256, 256, 0, s>>>(a.offsets, a.ell, a.temp, B, G, rowT);
+  k_verify_rowstats<T><<<B * (G + 1) * RS_PARTS, RS_THREADS, 0, s>>>(tg, a.offsets, rowT, B, V, rs);
+  k_verify_accept<T><<<B, AC_WARPS * 32, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.pd_tok, a.temp, a.req_id,
+                                                  a.seed, G, V, rs, vm, fmeta, fstat, hdr);
+  k_verify_final<T><<<dim3(B, FN_SLICES), FN_THREADS, 0, s>>>(tg, a.pd_rows, G, V, fmeta, fstat, fin);
+  k_verify_pick<T><<<nw, PK_WARPS * 32, 0, s>>>(tg, a.ell, a.tokens, a.pd_rows, a.req_id, a.seed, B, G, V, fmeta,
+                                                fstat, fin, a.n_accept, a.out_tok, a.n_out);
+  count_launches(5);
   return cudaGetLastError();
 }
 
