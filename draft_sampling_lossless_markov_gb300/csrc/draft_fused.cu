@@ -827,42 +827,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const uint32_t ta = tmem + lane_bits + kAccCol0 + (uint32_t)(a * BN + ch * CW);
           const uint8_t* su_row = sU + su * kUStage + ch * kUChunk + row * 128;
-          // logits of columns v0 + 32 h .. + 31: accumulator + U; the last read
-          // releases the accumulator and the U stage
-          auto load_half = [&](int h, float(&x)[32], bool last) {
+          // logits of the chunk's 64 columns: accumulator + U, both TMEM halves
+          // in flight at once; the reads release the accumulator and the U stage
+          float xa[32], xb[32];
+          {
             __syncwarp();
-            ptx::tmem_ld32(ta + 32 * h, x);
+            ptx::tmem_ld32(ta, xa);
+            ptx::tmem_ld32(ta + 32, xb);
             ptx::tmem_ld_wait();
-            if (last) {
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(&tempty[a]);
-            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&tempty[a]);
+            auto add_u = [&](float(&x)[32], int h) {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const int c8 = 4 * h + cc;
-              const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((c8 ^ (row & 7)) << 4));
-              const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
+              for (int cc = 0; cc < 4; ++cc) {
+                const int c8 = 4 * h + cc;
+                const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((c8 ^ (row & 7)) << 4));
+                const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(bp[e]);
-                x[8 * cc + 2 * e] = add_base(f.x, x[8 * cc + 2 * e]);
-                x[8 * cc + 2 * e + 1] = add_base(f.y, x[8 * cc + 2 * e + 1]);
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = __bfloat1622float2(bp[e]);
+                  x[8 * cc + 2 * e] = add_base(f.x, x[8 * cc + 2 * e]);
+                  x[8 * cc + 2 * e + 1] = add_base(f.y, x[8 * cc + 2 * e + 1]);
+                }
               }
-            }
-            if (last) {
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
-            }
-          };
+            };
+            add_u(xa, 0);
+            add_u(xb, 1);
+            // the stage's next fill is an async-proxy (TMA) write: order this
+            // warp's generic reads before it
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
+          }
           if (item == 1) {
             // S item: chunk partial of position s + 1
             float mc = -INFINITY, cs = 0.f, av = -INFINITY;
             int ai = INT_MAX;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float x[32];
-              load_half(h, x, h == 1);
+            auto s_half = [&](float(&x)[32], int h) {
               if (sampled) {
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -888,16 +890,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ai = v0 + 32 * h + j;
                   }
               }
-            }
+            };
+            s_half(xa, 0);
+            s_half(xb, 1);
             if (v0 < p.V && vrow)
               p.part[(size_t)b * p.pstride + (v0 / CW) % p.ept * 128 + (v0 / CW) / p.ept] = sampled ? make_float2(mc, cs) : make_float2(av, __int_as_float(ai));
           } else {
             // W item: p_d^s = 2^(y - m) / S (one-hot for greedy rows)
             const int row0 = row_base + qd * 32;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float x[32];
-              load_half(h, x, h == 1);
+            auto w_half = [&](float(&x)[32], int h) {
               if (sampled) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -934,7 +935,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_store_3d(&tmPd, stg, v0 + 32 * h, s, row0, ptx::policy_evict_first());
                 ptx::bulk_commit();
               }
-            }
+            };
+            w_half(xa, 0);
+            w_half(xb, 1);
           }
         }
       }

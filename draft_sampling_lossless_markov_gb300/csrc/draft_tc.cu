@@ -715,6 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
               if (last) {
+                // the stage's next fill is an async-proxy (TMA) write: order
+                // this warp's generic reads before it
+                ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
               }
