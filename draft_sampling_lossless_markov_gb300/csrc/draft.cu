@@ -451,12 +451,10 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   const T* w = static_cast<const T*>(a.w);
 
   const int BG = B * G;
-  k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
-
   if (draft_tc_supported(d)) {
-    // tensor-core path: the fused-sweep persistent kernel, else the two-pass
-    // kernel (DSPARK_DRAFT_LAUNCH=two_pass or per_pass selects the latter)
-    count_launches(1);
+    // tensor-core path: the fused-sweep persistent kernel (which forms w_h . h
+    // itself), else the two-pass kernel (DSPARK_DRAFT_LAUNCH=two_pass or
+    // per_pass selects the latter)
     static int fused = -1;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -467,8 +465,11 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
       const cudaError_t e = launch_draft_fused(a, ws, L, s);
       if (e != cudaErrorNotSupported) return e;
     }
+    k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
+    count_launches(1);
     return launch_draft_tc(a, ws, L, s);
   }
+  k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
 
   // CUDA-core path
   // position 0's embedding; later positions are prepared by k_select

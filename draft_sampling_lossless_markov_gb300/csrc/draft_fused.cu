@@ -89,7 +89,7 @@ struct Params {
   const __nv_bfloat16* W1;   // [V, r]
   const __nv_bfloat16* W2;   // [r, V]
   const __nv_bfloat16* w;    // [H + r]
-  const float* zh;           // [B, G]
+  const __nv_bfloat16* h;    // [B, G, H] hidden states of the confidence head
   const int32_t* anchor;     // [B]
   const float* temp;         // [B]
   const uint32_t* req_id;    // [B]
@@ -182,9 +182,28 @@ __device__ bool grid_barrier(const Params& p, unsigned target, volatile int* abo
 
 // Confidence of position k of row b (one warp): z = w_h . h_k + w_e . W1[x]
 // with x = x_{k-1} (the anchor for k = 0) and c = sigmoid(z) ([DSpark] 方法细节,
-// 置信度头); lane l takes elements 8 l .. 8 l + 7 (r <= 256).
+// 置信度头).  w_h . h_k: lane l takes the 8-element groups l, l + 32, ..
+// (H % 8 == 0); w_e . W1[x]: lane l takes elements 8 l .. 8 l + 7 (r <= 256).
 __device__ void conf_of(const Params& p, int b, int k, int x, int lane) {
   if (x < 0 || x >= p.V) x = 0;
+  float zh = 0.f;
+  {
+    const uint4* hq = reinterpret_cast<const uint4*>(p.h + ((size_t)b * p.G + k) * p.H);
+    const uint4* wq = reinterpret_cast<const uint4*>(p.w);
+#pragma unroll 4
+    for (int i = lane; i < p.H / 8; i += 32) {
+      const uint4 hv = __ldcs(hq + i), wv = wq[i];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
+      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 fh = __bfloat1622float2(h2[t]), fw = __bfloat1622float2(w2[t]);
+        zh = fmaf(fh.x, fw.x, zh);
+        zh = fmaf(fh.y, fw.y, zh);
+      }
+    }
+    zh = warp_sum(zh);
+  }
   float acc = 0.f;
   if (8 * lane < p.r) {
     const uint4 eq = *reinterpret_cast<const uint4*>(p.W1 + (size_t)x * p.r + 8 * lane);
@@ -200,7 +219,7 @@ __device__ void conf_of(const Params& p, int b, int k, int x, int lane) {
   }
   acc = warp_sum(acc);
   if (lane == 0) {
-    const float z = p.zh[(size_t)b * p.G + k] + acc;
+    const float z = zh + acc;
     p.conf_logit[(size_t)b * p.G + k] = z;
     p.conf[(size_t)b * p.G + k] = 1.f / (1.f + expf(-z));
   }
@@ -1078,7 +1097,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
   p.W2 = static_cast<const __nv_bfloat16*>(a.W2);
   p.w = static_cast<const __nv_bfloat16*>(a.w);
-  p.zh = reinterpret_cast<const float*>(ws + L.zh);
+  p.h = static_cast<const __nv_bfloat16*>(a.h);
   p.anchor = a.anchor;
   p.temp = a.temp;
   p.req_id = a.req_id;
