@@ -281,99 +281,129 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a
   }
 }
 
-// Up to kSmemSortMax candidates the whole schedule runs out of shared memory:
-// a bitonic sort of (key, index) pairs, whose 64-bit order is the radix sort's
-// stable order (ties in a stay in (r, j) index order), then the same Theta
-// scan, l_r and flatten as k_schedule.
+// Up to kSmemSortMax slots the whole schedule runs out of shared memory.  A
+// request's candidates are already in sort order (its survival products only
+// shrink along the prefix, so their keys only grow, and its indices grow), so
+// the (key, index) pairs are laid out as one sorted run per request, padded to
+// R = 2^ceil(log2 gamma) slots, and merged pairwise (merge path: an element's
+// place is its rank in its own run plus its rank in the partner run) until one
+// run remains; the 64-bit (key, index) order is the radix sort's stable order
+// (ties in a stay in (r, j) index order).  Then the same Theta scan, l_r and
+// flatten as k_schedule.
 constexpr int kSmemSortMax = 8192;
+constexpr size_t kSmemSchedMax = 200 * 1024;  // dynamic shared memory of k_schedule_smem
 
 __device__ __forceinline__ float key_to_a(uint64_t kv) { return __uint_as_float(~(uint32_t)(kv >> 32)); }
 
-// Ascending bitonic sort of kv[0, n_pad) (n_pad a power of two, 64 <= n_pad <=
-// 1024 E) by the CTA: thread t holds elements t E .. t E + E - 1 in registers.
-// A compare-exchange at distance j runs in registers (j < E), across lanes
-// with shuffles (j < 32 E) or through shared memory (larger j).
-template <int E>
-__device__ void bitonic_sort(uint64_t* kv, int n_pad) {
-  const int t = threadIdx.x;
-  const bool active = t * E < n_pad;
-  uint64_t v[E];
+// a (in (0, 1], from the sort key) as a fixed-point integer with 52 fraction
+// bits, by integer operations on its fp32 fields: exact for a >= 2^-28,
+// truncated below (at most 2^-52 per candidate), 0 for subnormals.  Sums of
+// these are exact, so the running survival sum of the Theta scan needs no fp64
+// adds.
+__device__ __forceinline__ long long key_to_fix52(uint64_t kv) {
+  const uint32_t bits = ~(uint32_t)(kv >> 32);
+  const int e = (int)((bits >> 23) & 0xFFu);
+  if (e == 0) return 0;
+  const long long m = (long long)((bits & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 98;  // m 2^(e - 150) 2^52
+  return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0);
+}
+constexpr double kFix52 = 2.220446049250313080847263336181640625e-16;  // 2^-52
+
+__device__ __forceinline__ long long block_excl_scan_i64(long long v, long long* sm, long long& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  long long x = v;
 #pragma unroll
-  for (int e = 0; e < E; ++e) v[e] = active ? kv[t * E + e] : ~0ull;
-  for (int size = 2; size <= n_pad; size <<= 1) {
-    for (int j = size >> 1; j > 0; j >>= 1) {
-      if (j >= 32 * E) {
-        __syncthreads();
-        if (active) {
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  if (lane == 31) sm[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    long long z = sm[lane];
 #pragma unroll
-          for (int e = 0; e < E; ++e) kv[t * E + e] = v[e];
-        }
-        __syncthreads();
-        if (active) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const int x = t * E + e;
-            const uint64_t y = kv[x ^ j];
-            const bool keep_min = ((x & size) == 0) == ((x & j) == 0);
-            v[e] = keep_min ? min(v[e], y) : max(v[e], y);
-          }
-        }
-      } else if (j >= E) {
-        if (t < ((n_pad / E + 31) & ~31)) {  // whole warps
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const int x = t * E + e;
-            const uint64_t y = __shfl_xor_sync(0xffffffffu, v[e], j / E);
-            const bool keep_min = ((x & size) == 0) == ((x & j) == 0);
-            v[e] = keep_min ? min(v[e], y) : max(v[e], y);
-          }
-        }
-      } else {
-        // j < E: pick the compile-time distance so that v stays in registers
-#pragma unroll
-        for (int jc = E / 2; jc >= 1; jc /= 2) {
-          if (jc != j) continue;
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            if ((e & jc) == 0) {
-              const int x = t * E + e;
-              const uint64_t a = v[e], b = v[e | jc];
-              const bool up = (x & size) == 0;
-              v[e] = up ? min(a, b) : max(a, b);
-              v[e | jc] = up ? max(a, b) : min(a, b);
-            }
-          }
-        }
-      }
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += t;
     }
+    const long long ze = __shfl_up_sync(0xffffffffu, z, 1);
+    sm[lane] = (lane == 0) ? 0 : ze;
+    if (lane == 31) sm[32] = z;
   }
   __syncthreads();
-  if (active) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) kv[t * E + e] = v[e];
-  }
+  long long xe = __shfl_up_sync(0xffffffffu, x, 1);  // exclusive prefix within the warp
+  if (lane == 0) xe = 0;
+  const long long res = sm[wid] + xe;
+  total = sm[32];
   __syncthreads();
+  return res;
+}
+
+// Merges sorted runs of length run0 (a power of two) in a[0, n_pad) (n_pad /
+// run0 a power of two, all values distinct) into one sorted run; b is scratch
+// of the same size.  Returns the buffer that holds the result.
+__device__ uint64_t* merge_runs(uint64_t* a, uint64_t* b, int n_pad, int run0) {
+  for (int w = run0; w < n_pad; w <<= 1) {
+    for (int i = threadIdx.x; i < n_pad; i += SCH_THREADS) {
+      const uint64_t x = a[i];
+      const int base = i & ~(2 * w - 1);
+      const int own = i & (w - 1);
+      const uint64_t* other = a + base + ((i & w) ? 0 : w);
+      // rank of x in the partner run (elements below it), by halving steps
+      int lo = 0;
+      for (int step = w >> 1; step > 0; step >>= 1) lo += other[lo + step - 1] < x ? step : 0;
+      lo += other[lo] < x ? 1 : 0;
+      b[base + own + lo] = x;
+    }
+    __syncthreads();
+    uint64_t* t = a;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// slots of the shared-memory schedule: one run of R slots per request, the
+// number of runs a power of two
+__host__ __device__ inline int sched_run_len(int G) {
+  int R = 1;
+  while (R < G) R <<= 1;
+  return R;
+}
+__host__ __device__ inline int sched_slots(int B, int G) {
+  int nb = 1;
+  while (nb < B) nb <<= 1;
+  return nb * sched_run_len(G);
 }
 
 __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_args a, const uint32_t* __restrict__ k0,
                                                                   const uint32_t* __restrict__ v0, int n_pad) {
-  extern __shared__ uint64_t kv[];  // [n_pad >= 64] sorted candidates, then [B] l_r
-  int* s_ell = reinterpret_cast<int*>(kv + n_pad);
+  // [n_pad] slots, [n_pad] scratch, [B (1 + gamma) + 1] SPS table, [B] l_r
+  extern __shared__ uint64_t kv[];
+  uint64_t* kv2 = kv + n_pad;
+  const int B = a.B, G = a.gamma;
+  double* s_sps = reinterpret_cast<double*>(kv2 + n_pad);
+  int* s_ell = reinterpret_cast<int*>(s_sps + B * (1 + G) + 1);
   __shared__ uint32_t sm_u[40];
-  __shared__ double sm_d[40];
+  __shared__ long long sm_l[40];
   __shared__ int s_first;
   __shared__ double s_theta_best;
 
-  const int B = a.B, G = a.gamma, n = B * G;
   const int tid = threadIdx.x;
+  const int R = sched_run_len(G);
   for (int r = tid; r < B; r += SCH_THREADS) s_ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
+  if (a.mode != DSPARK_SCHED_OFF)
+    for (int i = tid; i <= B * (1 + G); i += SCH_THREADS) s_sps[i] = a.sps[i];
   uint32_t ncand_local = 0;
   for (int i = tid; i < n_pad; i += SCH_THREADS) {
-    uint64_t e = ~0ull;
-    if (i < n) {
-      const uint32_t key = k0[i];
+    const int r = i / R, j = i - r * R;
+    // padding sorts after every candidate and non-candidate, each slot distinct
+    uint64_t e = (0xFFFFFFFFull << 32) | (0x80000000u + (uint32_t)i);
+    if (r < B && j < G) {
+      const uint32_t key = k0[r * G + j];
       ncand_local += key != 0xFFFFFFFFu;
-      e = ((uint64_t)key << 32) | v0[i];
+      e = ((uint64_t)key << 32) | v0[r * G + j];
     }
     kv[i] = e;
   }
@@ -381,31 +411,25 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   block_excl_scan_u32(ncand_local, sm_u, ncand);  // ends with __syncthreads
 
   if (a.mode != DSPARK_SCHED_OFF) {
-    // ---- 2. bitonic sort, ascending (key, index) = descending a, ties by index ----
-    if (n_pad <= SCH_THREADS)
-      bitonic_sort<1>(kv, n_pad);
-    else if (n_pad <= 2 * SCH_THREADS)
-      bitonic_sort<2>(kv, n_pad);
-    else if (n_pad <= 4 * SCH_THREADS)
-      bitonic_sort<4>(kv, n_pad);
-    else
-      bitonic_sort<8>(kv, n_pad);
+    // ---- 2. one sorted run: ascending (key, index) = descending a, ties by index ----
+    const uint64_t* srt = merge_runs(kv, kv2, n_pad, R);
     // ---- 3. Theta along the sorted path, first non-increase ----
     const int nc = (int)ncand;
     const int ch = (nc + SCH_THREADS - 1) / SCH_THREADS;
     const int c_lo = min(tid * ch, nc), c_hi = min(c_lo + ch, nc);
-    double loc = 0.0;
-    for (int i = c_lo; i < c_hi; ++i) loc += (double)key_to_a(kv[i]);
-    double tot;
-    const double pre = block_excl_scan_f64(loc, sm_d, tot);
+    // survival sums in 52-bit fixed point (exact adds); Theta in fp64
+    long long loc = 0;
+    for (int i = c_lo; i < c_hi; ++i) loc += key_to_fix52(srt[i]);
+    long long tot;
+    const long long pre = block_excl_scan_i64(loc, sm_l, tot);
     if (tid == 0) s_first = nc + 1;
     __syncthreads();
     {
-      double S = pre;
-      double theta_prev = ((double)B + S) * a.sps[B + c_lo];
+      long long S = pre;
+      double theta_prev = ((double)B + (double)S * kFix52) * s_sps[B + c_lo];
       for (int i = c_lo; i < c_hi; ++i) {  // sorted position i is candidate number i + 1
-        S += (double)key_to_a(kv[i]);
-        const double theta = ((double)B + S) * a.sps[B + i + 1];
+        S += key_to_fix52(srt[i]);
+        const double theta = ((double)B + (double)S * kFix52) * s_sps[B + i + 1];
         if (!(theta > theta_prev)) {
           atomicMin(&s_first, i + 1);
           break;
@@ -416,15 +440,15 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     __syncthreads();
     const int nstar = s_first - 1;  // admitted candidates
     if (nstar == 0) {
-      if (tid == 0) s_theta_best = (double)B * a.sps[B];
+      if (tid == 0) s_theta_best = (double)B * s_sps[B];
     } else if (nstar - 1 >= c_lo && nstar - 1 < c_hi) {
-      double S = pre;
-      for (int i = c_lo; i < nstar; ++i) S += (double)key_to_a(kv[i]);
-      s_theta_best = ((double)B + S) * a.sps[B + nstar];
+      long long S = pre;
+      for (int i = c_lo; i < nstar; ++i) S += key_to_fix52(srt[i]);
+      s_theta_best = ((double)B + (double)S * kFix52) * s_sps[B + nstar];
     }
     // ---- 4. l_r = number of admitted (r, .) candidates (= largest admitted j) ----
     for (int i = tid; i < nstar; i += SCH_THREADS) {
-      const uint32_t v = (uint32_t)kv[i];
+      const uint32_t v = (uint32_t)srt[i];
       atomicMax(&s_ell[v / G], (int)(v % G) + 1);
     }
     __syncthreads();
@@ -474,16 +498,15 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
   const int rb = PREP_THREADS / a.gamma;
   k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0);
-  const int n = a.B * a.gamma;
-  if (n <= kSmemSortMax) {
-    int n_pad = 64;
-    while (n_pad < n) n_pad <<= 1;
-    const size_t smem = (size_t)n_pad * sizeof(uint64_t) + (size_t)a.B * sizeof(int);
+  const int n_pad = sched_slots(a.B, a.gamma);
+  // slots, merge scratch, the SPS table and l_r
+  const size_t smem = 2 * (size_t)n_pad * sizeof(uint64_t) + ((size_t)a.B * (1 + a.gamma) + 1) * sizeof(double) +
+                      (size_t)a.B * sizeof(int);
+  if (n_pad <= kSmemSortMax && smem <= kSmemSchedMax) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(k_schedule_smem, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)(kSmemSortMax * sizeof(uint64_t) + kSmemSortMax * sizeof(int)));
+      attr_err = cudaFuncSetAttribute(k_schedule_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemSchedMax);
     });
     if (attr_err != cudaSuccess) return attr_err;
     k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, k0, v0, n_pad);
