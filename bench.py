@@ -267,7 +267,7 @@ def run_ours(args, rank, world, local_rank):
         "hbm_frac_step": step_frac,
         "hbm_frac_step_w2_per_position": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
         "breakdown_ms": br,
-        "roofline": {"bound": "hbm", "kernel": "dspark_draft_sample (fz::k_draft_fused, one launch, + k_conf_hidden)",
+        "roofline": {"bound": "hbm", "kernel": "dspark_draft_sample (fz::k_draft_fused, one launch)",
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
                      "unit": "GB/s", "frac": draft_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": bytes_["draft_strict"]},
@@ -318,8 +318,10 @@ def load_traffic(wl):
 
 def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     """Same metric through the public API with HOST buffers: each step copies the
-    step's inputs from pinned host memory, runs the three calls, reads N_v and the
-    markers back, copies the kept target rows in, verifies, and reads the result."""
+    step's inputs from pinned host memory (U and h on the compute stream; the
+    target model's rows, all B(gamma+1) of them, on a second stream while the
+    draft runs), runs the three calls, places the kept rows by the scheduler's
+    marker tensor on the device, verifies, and reads the result back."""
     import torch
     B, G, V = wl.B, wl.gamma, wl.V
     h_U = inp["U"].cpu().pin_memory()
@@ -329,16 +331,21 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     d_U = torch.empty_like(inp["U"])
     d_h = torch.empty_like(inp["h"])
     d_small = {k: torch.empty_like(inp[k]) for k in h_small}
+    d_tgt = torch.empty_like(inp["target"])
+    tgt_flat = d_tgt.reshape(-1, V)
     cap = B * (G + 1)
     rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
-    h_ell = torch.empty(B, dtype=torch.int32).pin_memory()
     h_nv = torch.empty(1, dtype=torch.int32).pin_memory()
     h_out = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
     h_nout = torch.empty(B, dtype=torch.int32).pin_memory()
     esz = inp["U"].element_size()
-    row_bytes = V * esz
+    side = torch.cuda.Stream(device=dev)
+    tgt_ready = torch.cuda.Event()
 
     def step():
+        with torch.cuda.stream(side):
+            d_tgt.copy_(h_tgt, non_blocking=True)
+            tgt_ready.record(side)
         with torch.cuda.stream(stream):
             d_U.copy_(h_U, non_blocking=True)
             d_h.copy_(h_h, non_blocking=True)
@@ -348,35 +355,29 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
                                d_small["req_id"], inp["seed"], stream=stream)
             s = T.schedule(ws, d["conf_logit"], inp["sts"], sps_dev, d_small["anchor"], d["tokens"], wl.sched,
                            stream=stream, n_verify_host=h_nv)
-            h_ell.copy_(s["ell"], non_blocking=True)
-        stream.synchronize()
-        ell = h_ell.numpy()
-        off = 0
-        with torch.cuda.stream(stream):
-            for r in range(B):  # each request's kept rows are contiguous on both sides
-                n = int(ell[r]) + 1
-                rows[off:off + n].copy_(h_tgt[r, :n], non_blocking=True)
-                off += n
+            # the kept rows in flattened verify order, from the marker tensor
+            # (rows past N_v hold markers -1 and take row 0)
+            stream.wait_event(tgt_ready)
+            idx = s["mark_req"].long().clamp_min(0) * (G + 1) + s["mark_pos"].long().clamp_min(0)
+            torch.index_select(tgt_flat, 0, idx, out=rows)
             v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d["pd_rows"], d["pd_tok"], d_small["temp"],
                          d_small["req_id"], inp["seed"], stream=stream)
             h_out.copy_(v["out_tok"], non_blocking=True)
             h_nout.copy_(v["n_out"], non_blocking=True)
         stream.synchronize()
-        return off
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
     torch.cuda.synchronize(dev)
     n_e2e = max(1, min(args.steps, 5))
     t0 = time.perf_counter()
-    nrows = 0
     for _ in range(n_e2e):
-        nrows += step()
+        step()
     t1 = time.perf_counter()
     sec = (t1 - t0) / n_e2e
     h2d = (h_U.numel() * esz + h_h.numel() * esz + sum(t.numel() * t.element_size() for t in h_small.values())
-           + nrows / n_e2e * row_bytes)
-    d2h = h_ell.numel() * 4 + 4 + h_out.numel() * 4 + h_nout.numel() * 4
+           + h_tgt.numel() * esz)
+    d2h = 4 + h_out.numel() * 4 + h_nout.numel() * 4
     return {"value": B * G / sec, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n_e2e, "timer": "host wall clock around each full step (synchronised)"}
 
