@@ -46,6 +46,10 @@ def test_draft_tiny(temp, seed):
     (17, 3, 1031, 7, 5, "f32"),    # odd sizes everywhere
     (5, 4, 4104, 64, 24, "bf16"),  # several tiles plus a ragged tail, bf16
     (33, 2, 2056, 1, 8, "bf16"),   # rank 1, more rows than one row block
+    # tensor-core shapes (bf16, r a multiple of 64, V and H multiples of 8)
+    (130, 5, 8200, 128, 16, "bf16"),   # two M-tiles (the second with 2 rows), an 8-column last tile
+    (40, 3, 1024, 256, 8, "bf16"),     # 8 vocabulary tiles for many CTAs: most claim no tile
+    (260, 16, 2048, 192, 32, "bf16"),  # gamma 16, rank 192, three M-tiles
 ])
 def test_draft_ragged_shapes(B, G, V, r, H, dt):
     wl = synth.Workload("ragged", B, G, V, H, r, dt, "mixed", synth.SCHED_GREEDY, "tiny", seed=5)
