@@ -126,3 +126,19 @@ def test_verify_zero_length_and_draft_equal_target():
     g, o, st = _verify_both(to_np64(rows), rows, fl["offsets"], ell, tok_np, pdrow.contiguous(),
                             pdtok.cpu().numpy(), temp, 78, np.arange(B))
     assert np.all(g["n_accept"][temp > 0] == G)
+
+
+@pytest.mark.parametrize("V,dt", [(1001, torch.float32), (1003, torch.bfloat16), (4099, torch.float32)])
+def test_verify_vocabulary_not_a_multiple_of_8(V, dt):
+    # rows that are not 16-byte aligned take the scalar paths of every verify kernel
+    rng = np.random.default_rng(V)
+    B, G = 24, 3
+    tgt = (torch.randn((B, G + 1, V), device="cuda") * 3).to(dt)
+    tokens = rng.integers(0, V, (B, G)).astype(np.int32)
+    ell = rng.integers(0, G + 1, B).astype(np.int64)
+    fl = S.flatten(ell, np.zeros(B), tokens)
+    rows = tgt[torch.from_numpy(fl["mark_req"]).cuda(), torch.from_numpy(fl["mark_pos"]).cuda()].contiguous()
+    temp = np.where(np.arange(B) % 4 == 0, 0.0, 0.8).astype(np.float32)
+    pd = rng.dirichlet(np.full(V, 0.3), size=(B, G)).astype(np.float32)
+    pdt = np.take_along_axis(pd, tokens[:, :, None].astype(np.int64), axis=2)[:, :, 0]
+    _verify_both(to_np64(rows), rows, fl["offsets"], ell, tokens, pd, pdt, temp, 91, np.arange(B))
