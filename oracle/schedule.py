@@ -24,7 +24,22 @@ search without the early stop (used as a pin in the tests).
 flattened into one batch and a marker tensor carries the intra-sequence
 dependency.
 
+[DSpark] 补充细节, "生产环境中的硬件感知前缀调度器" (and the engineering
+compromise of section 4.2.5 / 8.5 of the MTP survey page): in production the
+scheduler runs asynchronously.  The confidences of two steps earlier fix the
+verify capacity K by a global search over their sorted path (no early stop,
+because the real SPS curve steps down in cliffs); the current step still ranks
+its candidates by their current cumulative confidence and admits the top K.
+K depends only on the earlier information, which is the causal barrier that
+keeps the search lossless.
+
 Readings where the pages are silent (this library's contract):
+* asynchronous mode: the earlier confidences are given as a [R, g] array for
+  the current batch's requests (the caller maps its history onto them); K is the
+  number of admissions of the best prefix of their sorted path (the first
+  maximum of Theta_i, i = 0 .. n_prev); the current step admits its first
+  min(K, n_now) candidates in the usual order; theta_best reports Theta of that
+  admission with the current survivals;
 * c'_k is the fp32 rounding of sigmoid(z/tau) evaluated in fp64, and a_{r,j} is
   the left-to-right fp32 product of the c'; both are sort keys, so both sides
   must produce the same bits;
@@ -40,6 +55,7 @@ import numpy as np
 
 MODE_OFF = 0
 MODE_GREEDY = 1
+MODE_ASYNC_TOPK = 2
 
 
 def sts_calibrate(conf_logit, sts_temp):
@@ -133,6 +149,35 @@ def prefix_schedule(a, sps, mode=MODE_GREEDY, early_stop=True):
                 theta_margin=margin)
 
 
+def async_topk_schedule(a_now, a_prev, sps):
+    """The production variant: capacity K from a_prev, top-K admission of a_now.
+
+    a_now, a_prev [R, g] fp32 survival products; sps the SPS table.
+    Returns dict(ell [R] int64, theta_best fp64 (Theta of the admission with the
+    current survivals), n_admit int, K int, cap_theta fp64 (Theta_K on the
+    earlier path), cap_margin fp64 = relative gap between Theta_K and the best
+    Theta at any other prefix length of the earlier path (inf if there is no
+    other), thetas (Theta_0 .. Theta_{n_prev} of the earlier path))."""
+    a_now = np.asarray(a_now, dtype=np.float32)
+    sps = np.asarray(sps, dtype=np.float64)
+    R, G = a_now.shape
+    cap = prefix_schedule(a_prev, sps, MODE_GREEDY, early_stop=False)
+    K = cap["n_admit"]
+    th = np.asarray(cap["thetas"], dtype=np.float64)
+    others = np.delete(th, K)
+    cap_margin = (float(np.min(np.abs(th[K] - others)) / abs(th[K])) if others.size else np.inf)
+    rr, jj = sorted_candidates(a_now)
+    n_admit = min(K, rr.size)
+    ell = np.zeros(R, np.int64)
+    tau = float(R)
+    for i in range(n_admit):
+        r, j = rr[i], jj[i]
+        ell[r] = max(ell[r], j + 1)
+        tau += float(a_now[r, j])
+    return dict(ell=ell, theta_best=tau * sps[R + n_admit], n_admit=n_admit, K=K, cap_theta=float(th[K]),
+                cap_margin=cap_margin, thetas=list(th), theta_margin=np.inf)
+
+
 def flatten(ell, anchor, tokens):
     """Flattened verify batch and marker tensor.
 
@@ -158,14 +203,21 @@ def flatten(ell, anchor, tokens):
     return dict(offsets=offsets, flat_tok=flat_tok, mark_req=mark_req, mark_pos=mark_pos)
 
 
-def schedule(conf_logit, sts_temp, sps, anchor, tokens, mode=MODE_GREEDY, early_stop=True):
-    """STS -> survival -> Algorithm 1 -> flatten, as one call.
+def schedule(conf_logit, sts_temp, sps, anchor, tokens, mode=MODE_GREEDY, early_stop=True, conf_logit_prev=None):
+    """STS -> survival -> Algorithm 1 (or the asynchronous top-K variant, which
+    takes the earlier confidences conf_logit_prev) -> flatten, as one call.
 
     Returns the union of the dicts above plus c (calibrated, fp32), a (fp32) and
-    sts_margin (smallest rounding margin of c over the batch)."""
+    sts_margin (smallest rounding margin of c over the batch, and of the earlier
+    confidences in the asynchronous mode)."""
     c, m = sts_calibrate(conf_logit, sts_temp)
     a = survival(c)
-    res = prefix_schedule(a, sps, mode, early_stop)
+    if mode == MODE_ASYNC_TOPK:
+        c_prev, m_prev = sts_calibrate(conf_logit_prev, sts_temp)
+        res = async_topk_schedule(a, survival(c_prev), sps)
+        m = np.minimum(m, m_prev)
+    else:
+        res = prefix_schedule(a, sps, mode, early_stop)
     res.update(flatten(res["ell"], anchor, tokens))
     res["c"] = c
     res["a"] = a

@@ -84,3 +84,28 @@ def test_draft_mutations_are_caught(old, new):
     expect = np.outer(PT[x0], np.ones(V)) * PT
     obs = np.bincount(out["tokens"][:, 0] * V + out["tokens"][:, 1], minlength=V * V)
     assert stats.chisquare(obs, expect.ravel() * R).pvalue < 1e-6
+
+
+@pytest.mark.parametrize("old,new", [
+    ("cap = prefix_schedule(a_prev, sps, MODE_GREEDY, early_stop=False)",
+     "cap = prefix_schedule(a_prev, sps, MODE_GREEDY, early_stop=True)"),       # capacity with the early stop
+    ("cap = prefix_schedule(a_prev, sps, MODE_GREEDY, early_stop=False)",
+     "cap = prefix_schedule(a_now, sps, MODE_GREEDY, early_stop=False)"),       # capacity from the current step
+    ("n_admit = min(K, rr.size)", "n_admit = min(K + 1, rr.size)"),            # one admission too many
+])
+def test_async_scheduler_mutations_are_caught(old, new):
+    # the brute-force and appendix pins of the asynchronous scheduler reject each
+    mod = _mutant("schedule", old, new)
+    import test_oracle_schedule as T
+    failed = 0
+    for fn, args in [(T.test_async_appendix_a, ())] + [(T.test_async_capacity_is_the_brute_force_optimum, (s,))
+                                                        for s in range(30)]:
+        saved = T.S
+        T.S = mod
+        try:
+            fn(*args)
+        except AssertionError:
+            failed += 1
+        finally:
+            T.S = saved
+    assert failed > 0

@@ -156,3 +156,79 @@ def test_schedule_end_to_end_invariants():
     assert res["offsets"][-1] == R + res["ell"].sum()
     assert 0 <= res["ell"].min() and res["ell"].max() <= G
     assert res["theta_best"] >= R * sps[R]
+
+
+# ---- the asynchronous production variant (capacity from earlier confidences) ----
+
+def test_async_appendix_a():
+    # with the earlier survivals equal to the current ones the capacity is the
+    # global (no early stop) optimum of the appendix: l = 2 when c2 = 0.9, 0 when c2 = 0
+    g = _golden()
+    sps = np.array([0.0, g["sps1"], g["sps2"], g["sps3"]])
+    a1 = np.float32(g["a1"])
+    a_hi = np.array([[a1, np.float32(a1 * np.float32(g["c2_high"]))]], np.float32)
+    a_lo = np.array([[a1, np.float32(0.0)]], np.float32)
+    res = S.async_topk_schedule(a_hi, a_hi, sps)
+    assert res["K"] == 2 and res["ell"][0] == g["no_stop_ell_high"]
+    assert res["cap_theta"] == pytest.approx(g["theta2_high"], rel=1e-7)
+    res = S.async_topk_schedule(a_lo, a_lo, sps)
+    assert res["K"] == 0 and res["ell"][0] == g["no_stop_ell_low"]
+    # the causal barrier: the capacity comes from the earlier step only; a current
+    # step whose x1 ends the candidates admits what it has, up to K
+    res = S.async_topk_schedule(a_lo, a_hi, sps)
+    assert res["K"] == 2 and res["ell"][0] == 1 and res["n_admit"] == 1
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_async_capacity_is_the_brute_force_optimum(seed):
+    rng = np.random.default_rng(100 + seed)
+    R, G = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+    a_prev, sps = _random_case(rng, R, G)
+    a_now, _ = _random_case(rng, R, G)
+    res = S.async_topk_schedule(a_now, a_prev, sps)
+    best = max(_theta_of(ell, a_prev, sps) for ell in itertools.product(range(G + 1), repeat=R))
+    assert res["cap_theta"] == pytest.approx(best, rel=1e-12)
+    # K is the first prefix length reaching the optimum on the earlier path
+    assert res["K"] == int(np.argmax(np.asarray(res["thetas"]) >= res["cap_theta"]))
+    # the admission is the top min(K, n_now) current candidates, prefix-closed
+    rr, jj = S.sorted_candidates(a_now)
+    n = min(res["K"], rr.size)
+    assert res["n_admit"] == n
+    np.testing.assert_array_equal(np.bincount(rr[:n], minlength=R), res["ell"])
+    assert res["theta_best"] == pytest.approx(_theta_of(res["ell"], a_now, sps), rel=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_async_depends_on_current_values_only_through_their_order(seed):
+    rng = np.random.default_rng(200 + seed)
+    R, G = 6, 4
+    a_prev, sps = _random_case(rng, R, G)
+    a_now, _ = _random_case(rng, R, G)
+    res = S.async_topk_schedule(a_now, a_prev, sps)
+    # an order-preserving change of the current values (positive ones stay
+    # positive) leaves the admitted set alone
+    warped = np.where(a_now > 0, np.sqrt(a_now.astype(np.float64)) * 0.5 + 0.25, 0.0).astype(np.float32)
+    res2 = S.async_topk_schedule(warped, a_prev, sps)
+    np.testing.assert_array_equal(res["ell"], res2["ell"])
+
+
+def test_async_equals_algorithm_1_on_a_unimodal_path():
+    # same survivals in both steps and a smooth curve: the global optimum is the
+    # first local maximum, so the asynchronous and greedy schedules agree
+    rng = np.random.default_rng(7)
+    for _ in range(20):
+        R, G = 5, 4
+        c = rng.uniform(0.05, 1.0, size=(R, G)).astype(np.float32)
+        a = S.survival(c)
+        n = np.arange(R * (1 + G) + 1, dtype=np.float64)
+        sps = 100.0 / (1.0 + n / rng.uniform(2, 20))
+        sps[0] = 0.0
+        path = S.prefix_schedule(a, sps, S.MODE_GREEDY, early_stop=False)["thetas"]
+        i = int(np.argmax(path))
+        if not all(path[k + 1] > path[k] for k in range(i)) or not all(
+                path[k + 1] <= path[k] for k in range(i, len(path) - 1)):
+            continue
+        res = S.async_topk_schedule(a, a, sps)
+        es = S.prefix_schedule(a, sps, S.MODE_GREEDY, early_stop=True)
+        np.testing.assert_array_equal(res["ell"], es["ell"])
+        assert res["theta_best"] == pytest.approx(es["theta_best"], rel=1e-12)
