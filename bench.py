@@ -141,6 +141,11 @@ def run_ours(args, rank, world, local_rank):
     wl = synth.get_workload(args.workload)
     B, G, V = wl.B, wl.gamma, wl.V
     inp = synth.make_inputs(wl, dev)
+    inp["sched_mode"], inp["zprev"] = wl.sched, None
+    if args.sched == "async":
+        # the production mode: capacity from synthetic confidences of an earlier step
+        inp["sched_mode"] = synth.SCHED_ASYNC_TOPK
+        inp["zprev"] = torch.from_numpy(synth.random_conf_logits(B, G, wl.seed + 77)).to(dev)
     ws = T.Workspace.create(T.dims(B, G, V, wl.r, wl.H, inp["U"].dtype), device=dev)
     cap = B * (G + 1)
     sps_dev = torch.from_numpy(inp["sps"]).to(dev)
@@ -167,8 +172,7 @@ def run_ours(args, rank, world, local_rank):
     def seg1(st):
         T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
                        inp["req_id"], inp["seed"], out=d_out, stream=st)
-        T.schedule(ws, d_out["conf_logit"], inp["sts"], sps_dev, inp["anchor"], d_out["tokens"], wl.sched,
-                   out=s_out, stream=st)
+        sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=st)
 
     def standin(st):
         # stand-in for the target forward on the flattened batch (not timed): rows
@@ -261,7 +265,8 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
         "config": {"workload": wl.name, "B": B, "gamma": G, "V": V, "r": wl.r, "H": wl.H, "temp": wl.temp,
-                   "scheduler": "greedy_early_stop" if wl.sched else "off", "n_verify_rows": nv,
+                   "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]],
+                   "n_verify_rows": nv,
                    "l2": "inputs larger than L2 (U alone %.0f MB per step), no flush" % (bytes_["U"] / 1e6),
                    "graph": use_graph, "parallelism": "replicas" if world > 1 else "1gpu"},
         "hbm_frac_step": step_frac,
@@ -291,8 +296,7 @@ def per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sp
             T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
                            inp["req_id"], inp["seed"], out=d_out, stream=stream)
             ev[1].record(stream)
-            T.schedule(ws, d_out["conf_logit"], inp["sts"], sps_dev, inp["anchor"], d_out["tokens"], wl.sched,
-                       out=s_out, stream=stream)
+            sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=stream)
             ev[2].record(stream)
             standin(stream)
             ev[3].record(stream)
@@ -314,6 +318,13 @@ def load_traffic(wl):
         except (ValueError, OSError):
             return None
     return None
+
+
+def sched(T, ws, conf_logit, inp, sps_dev, anchor, tokens, **kw):
+    """dspark_schedule in the bench's scheduler mode (the workload's, or the
+    asynchronous production mode with synthetic earlier confidences)."""
+    return T.schedule(ws, conf_logit, inp["sts"], sps_dev, anchor, tokens, inp["sched_mode"],
+                      conf_logit_prev=inp.get("zprev"), **kw)
 
 
 def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
@@ -353,8 +364,8 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
                 d_small[k].copy_(h_small[k], non_blocking=True)
             d = T.draft_sample(ws, d_U, inp["W1"], inp["W2"], d_h, inp["w"], d_small["anchor"], d_small["temp"],
                                d_small["req_id"], inp["seed"], stream=stream)
-            s = T.schedule(ws, d["conf_logit"], inp["sts"], sps_dev, d_small["anchor"], d["tokens"], wl.sched,
-                           stream=stream, n_verify_host=h_nv)
+            s = sched(T, ws, d["conf_logit"], inp, sps_dev, d_small["anchor"], d["tokens"], stream=stream,
+                      n_verify_host=h_nv)
             # the kept rows in flattened verify order, from the marker tensor
             # (rows past N_v hold markers -1 and take row 0)
             stream.wait_event(tgt_ready)
@@ -401,7 +412,7 @@ def oracle_sample_time(wl, inp_np, n_req):
     zl = d["conf_logit"][np.arange(B) % n_req].astype(np.float32)
     toks = d["tokens"][np.arange(B) % n_req]
     sch = S.schedule(zl, inp_np["sts"], inp_np["sps"], inp_np["anchor"][np.arange(B) % n_req], toks,
-                     mode=wl.sched)
+                     mode=inp_np["sched_mode"], conf_logit_prev=inp_np["zprev"])
     t2 = time.perf_counter()
     sub_sch = S.flatten(sch["ell"][sub], inp_np["anchor"][sub], d["tokens"])
     rows = inp_np["target"][sub][sub_sch["mark_req"], sub_sch["mark_pos"]]
@@ -419,7 +430,9 @@ def np_inputs_for_oracle(wl, inp, n_req):
     return dict(U=f(inp["U"][sub]), W1=f(inp["W1"]), W2=f(inp["W2"]), h=f(inp["h"][sub]), w=f(inp["w"]),
                 anchor=inp["anchor"].cpu().numpy().astype(np.int64), temp=inp["temp"].cpu().numpy().astype(np.float64),
                 req_id=inp["req_id"].cpu().numpy().astype(np.int64), seed=inp["seed"],
-                sts=inp["sts"].cpu().numpy(), sps=inp["sps"], target=f(inp["target"][sub]))
+                sts=inp["sts"].cpu().numpy(), sps=inp["sps"], target=f(inp["target"][sub]),
+                sched_mode=inp["sched_mode"],
+                zprev=inp["zprev"].cpu().numpy() if inp.get("zprev") is not None else None)
 
 
 def cpu_baseline(wl, inp, n_req):
@@ -436,6 +449,10 @@ def run_reference(args):
     import torch
     wl = synth.get_workload(args.workload)
     inp = synth.make_inputs(wl, "cpu")
+    inp["sched_mode"], inp["zprev"] = wl.sched, None
+    if args.sched == "async":
+        inp["sched_mode"] = synth.SCHED_ASYNC_TOPK
+        inp["zprev"] = torch.from_numpy(synth.random_conf_logits(wl.B, wl.gamma, wl.seed + 77))
     n_req = max(1, min(args.cpu_sample, wl.B))
     inp_np = np_inputs_for_oracle(wl, inp, n_req)
     for _ in range(args.warmup if args.warmup < 2 else 1):
@@ -451,7 +468,8 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; DSpark workload model)",
-            "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "H": wl.H},
+            "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "H": wl.H,
+                       "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]]},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -464,6 +482,8 @@ def main():
     ap.add_argument("--workload", default=synth.HEADLINE.name)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--sched", default="workload", choices=["workload", "async"],
+                    help="the workload's scheduler mode, or the asynchronous production mode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=4, help="requests the oracle runs per step")

@@ -25,6 +25,7 @@ DSPARK_F32 = 1
 
 DSPARK_SCHED_OFF = 0
 DSPARK_SCHED_GREEDY = 1
+DSPARK_SCHED_ASYNC_TOPK = 2
 
 DSPARK_MAX_GAMMA = 32
 DSPARK_MAX_RANK = 1024
@@ -53,7 +54,7 @@ class dspark_sched_args(ctypes.Structure):
                 ("sts_temp", c_void_p), ("sps", c_void_p), ("anchor", c_void_p), ("tokens", c_void_p),
                 ("ell", c_void_p), ("offsets", c_void_p), ("flat_tok", c_void_p), ("mark_req", c_void_p),
                 ("mark_pos", c_void_p), ("n_verify", c_void_p), ("n_verify_host", c_void_p),
-                ("theta_best", c_void_p), ("surv", c_void_p)]
+                ("theta_best", c_void_p), ("surv", c_void_p), ("conf_logit_prev", c_void_p)]
 
 
 class dspark_verify_args(ctypes.Structure):

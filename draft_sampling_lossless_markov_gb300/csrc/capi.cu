@@ -155,13 +155,18 @@ dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, s
 
 dspark_status dspark_schedule(const dspark_sched_args* a, void* workspace, size_t workspace_bytes, void* stream) {
   if (!a || a->B < 0 || a->gamma < 1 || a->gamma > DSPARK_MAX_GAMMA) return DSPARK_INVALID_ARG;
-  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY) return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY && a->mode != DSPARK_SCHED_ASYNC_TOPK)
+    return DSPARK_INVALID_ARG;
   if ((int64_t)a->B * a->gamma > DSPARK_MAX_SCHED_KEYS) return DSPARK_UNSUPPORTED;
   if (a->B == 0) return DSPARK_OK;
   if (!a->conf_logit || !a->sts_temp || !a->anchor || !a->tokens || !a->ell || !a->offsets || !a->flat_tok ||
       !a->mark_req || !a->mark_pos || !a->n_verify || !a->theta_best)
     return DSPARK_INVALID_ARG;
-  if (a->mode == DSPARK_SCHED_GREEDY && !a->sps) return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && !a->sps) return DSPARK_INVALID_ARG;
+  if (a->mode == DSPARK_SCHED_ASYNC_TOPK) {
+    if (!a->conf_logit_prev) return DSPARK_INVALID_ARG;
+    if (!schedule_async_supported(a->B, a->gamma)) return DSPARK_UNSUPPORTED;
+  }
   dspark_dims d{a->B, a->gamma, 1, 0, 0, DSPARK_F32};
   WsLayout L;
   const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);

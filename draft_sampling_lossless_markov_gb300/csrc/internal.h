@@ -50,6 +50,8 @@ size_t elem_size(int dtype);
 // Launchers (argument checking happens in capi.cu before these are called).
 cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+// whether the asynchronous top-K mode can run at this size (one CTA's shared memory)
+bool schedule_async_supported(int B, int G);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
 // Tensor-core draft sampler (draft_tc.cu).

@@ -103,8 +103,11 @@ constexpr int PREP_THREADS = 256;
 // One CTA covers floor(256 / gamma) whole requests: each thread calibrates one
 // (request, position) confidence, then one thread per request forms the
 // left-to-right fp32 products and writes the sort keys.
+// In the asynchronous mode the earlier step's confidences get the same
+// treatment into (k1, v1).
 __global__ void __launch_bounds__(PREP_THREADS) k_sched_prep(dspark_sched_args a, uint32_t* __restrict__ k0,
-                                                             uint32_t* __restrict__ v0) {
+                                                             uint32_t* __restrict__ v0, uint32_t* __restrict__ k1,
+                                                             uint32_t* __restrict__ v1) {
   __shared__ float cs[PREP_THREADS];
   const int B = a.B, G = a.gamma;
   const int rb = PREP_THREADS / G;
@@ -112,18 +115,25 @@ __global__ void __launch_bounds__(PREP_THREADS) k_sched_prep(dspark_sched_args a
   const int lr = t / G, j = t - lr * G;
   const int r = blockIdx.x * rb + lr;
   const bool valid = lr < rb && r < B;
-  if (valid) cs[t] = sts_conf(a.conf_logit[(size_t)r * G + j], a.sts_temp[j]);
-  __syncthreads();
-  if (valid && j == 0) {
-    float run = 1.f;
-    for (int jj = 0; jj < G; ++jj) {
-      run = __fmul_rn(run, cs[t + jj]);
-      const int idx = r * G + jj;
-      k0[idx] = run > 0.f ? ~__float_as_uint(run) : 0xFFFFFFFFu;
-      v0[idx] = (uint32_t)idx;
-      if (a.surv) a.surv[idx] = run;
+  const int sets = a.mode == DSPARK_SCHED_ASYNC_TOPK ? 2 : 1;
+  for (int set = 0; set < sets; ++set) {
+    const float* z = set == 0 ? a.conf_logit : a.conf_logit_prev;
+    uint32_t* kk = set == 0 ? k0 : k1;
+    uint32_t* vv = set == 0 ? v0 : v1;
+    if (set) __syncthreads();  // the products of the first set have read cs
+    if (valid) cs[t] = sts_conf(z[(size_t)r * G + j], a.sts_temp[j]);
+    __syncthreads();
+    if (valid && j == 0) {
+      float run = 1.f;
+      for (int jj = 0; jj < G; ++jj) {
+        run = __fmul_rn(run, cs[t + jj]);
+        const int idx = r * G + jj;
+        kk[idx] = run > 0.f ? ~__float_as_uint(run) : 0xFFFFFFFFu;
+        vv[idx] = (uint32_t)idx;
+        if (set == 0 && a.surv) a.surv[idx] = run;
+      }
+      if (set == 0) a.ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
     }
-    a.ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
   }
 }
 
@@ -377,8 +387,37 @@ __host__ __device__ inline int sched_slots(int B, int G) {
   return nb * sched_run_len(G);
 }
 
+// Largest value, first index on ties, over the CTA (every thread gets it).
+__device__ __forceinline__ void block_argmax_f64(double& v, int& i, double* smv, int* smi) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    if (v2 > v || (v2 == v && i2 < i)) {
+      v = v2;
+      i = i2;
+    }
+  }
+  if (lane == 0) {
+    smv[wid] = v;
+    smi[wid] = i;
+  }
+  __syncthreads();
+  v = smv[0];
+  i = smi[0];
+  for (int w = 1; w < SCH_THREADS / 32; ++w)
+    if (smv[w] > v || (smv[w] == v && smi[w] < i)) {
+      v = smv[w];
+      i = smi[w];
+    }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_args a, const uint32_t* __restrict__ k0,
-                                                                  const uint32_t* __restrict__ v0, int n_pad) {
+                                                                  const uint32_t* __restrict__ v0,
+                                                                  const uint32_t* __restrict__ k1,
+                                                                  const uint32_t* __restrict__ v1, int n_pad) {
   // [n_pad] slots, [n_pad] scratch, [B (1 + gamma) + 1] SPS table, [B] l_r
   extern __shared__ uint64_t kv[];
   uint64_t* kv2 = kv + n_pad;
@@ -387,6 +426,8 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   int* s_ell = reinterpret_cast<int*>(s_sps + B * (1 + G) + 1);
   __shared__ uint32_t sm_u[40];
   __shared__ long long sm_l[40];
+  __shared__ double sm_v[32];
+  __shared__ int sm_i[32];
   __shared__ int s_first;
   __shared__ double s_theta_best;
 
@@ -395,22 +436,62 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   for (int r = tid; r < B; r += SCH_THREADS) s_ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
   if (a.mode != DSPARK_SCHED_OFF)
     for (int i = tid; i <= B * (1 + G); i += SCH_THREADS) s_sps[i] = a.sps[i];
-  uint32_t ncand_local = 0;
-  for (int i = tid; i < n_pad; i += SCH_THREADS) {
-    const int r = i / R, j = i - r * R;
-    // padding sorts after every candidate and non-candidate, each slot distinct
-    uint64_t e = (0xFFFFFFFFull << 32) | (0x80000000u + (uint32_t)i);
-    if (r < B && j < G) {
-      const uint32_t key = k0[r * G + j];
-      ncand_local += key != 0xFFFFFFFFu;
-      e = ((uint64_t)key << 32) | v0[r * G + j];
+  // one sorted run per request in kv, padded; returns the number of candidates
+  auto load_runs = [&](const uint32_t* kk, const uint32_t* vv) {
+    uint32_t ncand_local = 0;
+    for (int i = tid; i < n_pad; i += SCH_THREADS) {
+      const int r = i / R, j = i - r * R;
+      // padding sorts after every candidate and non-candidate, each slot distinct
+      uint64_t e = (0xFFFFFFFFull << 32) | (0x80000000u + (uint32_t)i);
+      if (r < B && j < G) {
+        const uint32_t key = kk[r * G + j];
+        ncand_local += key != 0xFFFFFFFFu;
+        e = ((uint64_t)key << 32) | vv[r * G + j];
+      }
+      kv[i] = e;
     }
-    kv[i] = e;
-  }
-  uint32_t ncand;
-  block_excl_scan_u32(ncand_local, sm_u, ncand);  // ends with __syncthreads
+    uint32_t nc;
+    block_excl_scan_u32(ncand_local, sm_u, nc);  // ends with __syncthreads
+    return nc;
+  };
 
-  if (a.mode != DSPARK_SCHED_OFF) {
+  if (a.mode == DSPARK_SCHED_ASYNC_TOPK) {
+    // ---- capacity: the best prefix of the earlier step's sorted path (global search) ----
+    const int nprev = (int)load_runs(k1, v1);
+    const uint64_t* prv = merge_runs(kv, kv2, n_pad, R);
+    const int chp = (nprev + SCH_THREADS - 1) / SCH_THREADS;
+    const int p_lo = min(tid * chp, nprev), p_hi = min(p_lo + chp, nprev);
+    long long loc = 0;
+    for (int i = p_lo; i < p_hi; ++i) loc += key_to_fix52(prv[i]);
+    long long tot;
+    long long S = block_excl_scan_i64(loc, sm_l, tot);
+    double bv = tid == 0 ? (double)B * s_sps[B] : -INFINITY;  // Theta_0: nothing admitted
+    int bi = tid == 0 ? 0 : INT_MAX;
+    for (int i = p_lo; i < p_hi; ++i) {
+      S += key_to_fix52(prv[i]);
+      const double theta = ((double)B + (double)S * kFix52) * s_sps[B + i + 1];
+      if (theta > bv) {
+        bv = theta;
+        bi = i + 1;
+      }
+    }
+    block_argmax_f64(bv, bi, sm_v, sm_i);
+    const int K = bi;
+    // ---- this step: its candidates in order, the first min(K, n) admitted ----
+    const int ncur = (int)load_runs(k0, v0);  // every read of the earlier path ended before the scan's barriers
+    const uint64_t* cur = merge_runs(kv, kv2, n_pad, R);
+    const int nadm = min(K, ncur);
+    long long sl = 0;
+    for (int i = tid; i < nadm; i += SCH_THREADS) {
+      const uint32_t v = (uint32_t)cur[i];
+      atomicMax(&s_ell[v / G], (int)(v % G) + 1);
+      sl += key_to_fix52(cur[i]);
+    }
+    long long sadm;
+    block_excl_scan_i64(sl, sm_l, sadm);
+    if (tid == 0) *a.theta_best = ((double)B + (double)sadm * kFix52) * s_sps[B + nadm];
+  } else if (a.mode != DSPARK_SCHED_OFF) {
+    const uint32_t ncand = load_runs(k0, v0);
     // ---- 2. one sorted run: ascending (key, index) = descending a, ties by index ----
     const uint64_t* srt = merge_runs(kv, kv2, n_pad, R);
     // ---- 3. Theta along the sorted path, first non-increase ----
@@ -491,17 +572,26 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   }
 }
 
+static size_t schedule_smem_bytes(int B, int G) {
+  // slots, merge scratch, the SPS table and l_r
+  return 2 * (size_t)sched_slots(B, G) * sizeof(uint64_t) + ((size_t)B * (1 + G) + 1) * sizeof(double) +
+         (size_t)B * sizeof(int);
+}
+
+bool schedule_async_supported(int B, int G) {
+  return sched_slots(B, G) <= kSmemSortMax && schedule_smem_bytes(B, G) <= kSmemSchedMax;
+}
+
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   uint32_t* k0 = reinterpret_cast<uint32_t*>(ws + L.sk0);
   uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
   uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
   const int rb = PREP_THREADS / a.gamma;
-  k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0);
+  k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1);
   const int n_pad = sched_slots(a.B, a.gamma);
-  // slots, merge scratch, the SPS table and l_r
-  const size_t smem = 2 * (size_t)n_pad * sizeof(uint64_t) + ((size_t)a.B * (1 + a.gamma) + 1) * sizeof(double) +
-                      (size_t)a.B * sizeof(int);
+  const size_t smem = schedule_smem_bytes(a.B, a.gamma);
+  if (a.mode == DSPARK_SCHED_ASYNC_TOPK && !schedule_async_supported(a.B, a.gamma)) return cudaErrorNotSupported;
   if (n_pad <= kSmemSortMax && smem <= kSmemSchedMax) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -509,7 +599,7 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
       attr_err = cudaFuncSetAttribute(k_schedule_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemSchedMax);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, k0, v0, n_pad);
+    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, k0, v0, k1, v1, n_pad);
   } else {
     k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
   }

@@ -59,13 +59,18 @@ using namespace dspark;
 extern "C" dspark_status dspark_schedule_noalloc(const dspark_sched_args* a, void* stream) {
   // the same argument checks as dspark_schedule
   if (!a || a->B < 0 || a->gamma < 1 || a->gamma > DSPARK_MAX_GAMMA) return DSPARK_INVALID_ARG;
-  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY) return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY && a->mode != DSPARK_SCHED_ASYNC_TOPK)
+    return DSPARK_INVALID_ARG;
   if ((int64_t)a->B * a->gamma > kNoallocKeys) return DSPARK_UNSUPPORTED;  // beyond the static array
   if (a->B == 0) return DSPARK_OK;
   if (!a->conf_logit || !a->sts_temp || !a->anchor || !a->tokens || !a->ell || !a->offsets || !a->flat_tok ||
       !a->mark_req || !a->mark_pos || !a->n_verify || !a->theta_best)
     return DSPARK_INVALID_ARG;
-  if (a->mode == DSPARK_SCHED_GREEDY && !a->sps) return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && !a->sps) return DSPARK_INVALID_ARG;
+  if (a->mode == DSPARK_SCHED_ASYNC_TOPK) {
+    if (!a->conf_logit_prev) return DSPARK_INVALID_ARG;
+    if (!schedule_async_supported(a->B, a->gamma)) return DSPARK_UNSUPPORTED;
+  }
 
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return DSPARK_CUDA_ERROR;

@@ -109,7 +109,8 @@ def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int
 
 
 def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int, out: Optional[dict] = None,
-             stream=None, n_verify_host: Optional[torch.Tensor] = None, want_surv=False) -> dict:
+             stream=None, n_verify_host: Optional[torch.Tensor] = None, want_surv=False,
+             conf_logit_prev=None) -> dict:
     B, G = conf_logit.shape
     dev = conf_logit.device
     cap = B * (1 + G)
@@ -136,6 +137,7 @@ def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int
     a.theta_best = _ptr(out["theta_best"], torch.float64)
     a.n_verify_host = n_verify_host.data_ptr() if n_verify_host is not None else None
     a.surv = _ptr(out.get("surv"), torch.float32)
+    a.conf_logit_prev = _ptr(conf_logit_prev, torch.float32) if conf_logit_prev is not None else None
     out["_sps"] = sps  # keep the table alive while the call is in flight
     _check("dspark_schedule", capi.dspark_schedule(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out

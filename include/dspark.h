@@ -66,8 +66,10 @@ typedef enum {
 typedef enum { DSPARK_BF16 = 0, DSPARK_F32 = 1 } dspark_dtype;
 
 typedef enum {
-  DSPARK_SCHED_OFF = 0,     /* verify every draft token: l_r = gamma            */
-  DSPARK_SCHED_GREEDY = 1   /* Algorithm 1 with the early stop                  */
+  DSPARK_SCHED_OFF = 0,        /* verify every draft token: l_r = gamma            */
+  DSPARK_SCHED_GREEDY = 1,     /* Algorithm 1 with the early stop                  */
+  DSPARK_SCHED_ASYNC_TOPK = 2  /* production variant: capacity from earlier
+                                  confidences, top-K of the current candidates    */
 } dspark_sched_mode;
 
 /* Limits checked by every call. */
@@ -176,7 +178,21 @@ DSPARK_API dspark_status dspark_draft_sample(const dspark_draft_args* args, void
  *         n_verify [1] (= N_v); theta_best [1] f64 (Theta of the kept set;
  *         0 when mode = OFF); optional n_verify_host (pinned HOST i32, written
  *         by a stream-ordered copy) and surv [B, gamma] f32 (the a_{r,j}).
- * B * gamma must not exceed DSPARK_MAX_SCHED_KEYS. */
+ * B * gamma must not exceed DSPARK_MAX_SCHED_KEYS.
+ *
+ * Mode DSPARK_SCHED_ASYNC_TOPK ([DSpark] 补充细节, "生产环境中的硬件感知前缀
+ * 调度器"): the scheduler runs one step behind the draft.  conf_logit_prev
+ * [B, gamma] f32 holds the confidence logits of two steps earlier, mapped by the
+ * caller onto this batch's requests; their survival products, sorted as above,
+ * give the capacity K = the number of admissions of the best prefix of that path
+ * (the first maximum of Theta_i over i = 0 .. n_prev: a global search, no early
+ * stop).  This step's candidates are sorted as above and the first min(K, n)
+ * are admitted; theta_best is Theta of that admission with the current
+ * survivals.  K depends only on the earlier step, which is what keeps the
+ * search lossless.  Needs sps and conf_logit_prev; supported while the
+ * schedule fits one CTA's shared memory (B rounded up to a power of two times
+ * gamma rounded up to a power of two at most 8192 slots), else
+ * DSPARK_UNSUPPORTED. */
 typedef struct {
   int32_t B;
   int32_t gamma;
@@ -195,6 +211,7 @@ typedef struct {
   int32_t* n_verify_host;
   double* theta_best;
   float* surv;
+  const float* conf_logit_prev;  /* mode DSPARK_SCHED_ASYNC_TOPK only; may be NULL otherwise */
 } dspark_sched_args;
 
 DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* workspace,

@@ -32,6 +32,7 @@ import torch
 
 SCHED_OFF = 0
 SCHED_GREEDY = 1
+SCHED_ASYNC_TOPK = 2
 
 
 @dataclass(frozen=True)

@@ -85,6 +85,17 @@ def test_argument_errors_return_before_any_launch(lib):
     assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_INVALID_ARG  # null pointers
     s.B = 0
     assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_OK
+    # asynchronous mode: needs the earlier confidences and the cost table, and
+    # one CTA's shared memory
+    for f in ("conf_logit", "sts_temp", "sps", "anchor", "tokens", "ell", "offsets", "flat_tok", "mark_req",
+              "mark_pos", "n_verify", "theta_best"):
+        setattr(s, f, 0x10000)
+    s.B, s.gamma, s.mode = 64, 7, capi.DSPARK_SCHED_ASYNC_TOPK
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_INVALID_ARG  # no conf_logit_prev
+    s.conf_logit_prev = 0x10000
+    s.B = 4096
+    assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_UNSUPPORTED  # 32768 slots
+    assert capi.dspark_schedule_noalloc(s, 0) == capi.DSPARK_UNSUPPORTED
 
     v = capi.dspark_verify_args()
     v.dims = capi.dspark_dims(4, 4, 64, 0, 0, capi.DSPARK_BF16)
@@ -98,5 +109,5 @@ def test_struct_layouts_match_header(lib):
     assert ctypes.sizeof(capi.dspark_dims) == 24
     assert capi.dspark_draft_args.seed.offset == 24 + 8 * 8
     assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8
-    assert ctypes.sizeof(capi.dspark_sched_args) == 16 + 14 * 8
+    assert ctypes.sizeof(capi.dspark_sched_args) == 16 + 15 * 8
     assert capi.dspark_verify_args.seed.offset == 24 + 8 * 8

@@ -142,3 +142,70 @@ def test_schedule_empty_batch_is_a_no_op():
     a = capi.dspark_sched_args()
     a.B, a.gamma, a.mode = 0, 2, 1
     assert capi.dspark_schedule(a, ws.ptr, ws.nbytes, 0) == capi.DSPARK_OK
+
+
+# ---- the asynchronous production mode ----
+
+def _run_async(z, zp, tau, sps, anchor, tokens):
+    B, G = z.shape
+    ws = workspace_for(B, G, 1, 0, 0, torch.float32)
+    out = T.schedule(ws, to_dev_f32(z), to_dev_f32(tau), sps, to_dev_i32(anchor), to_dev_i32(tokens),
+                     S.MODE_ASYNC_TOPK, want_surv=True, conf_logit_prev=to_dev_f32(zp))
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out.items() if isinstance(v, torch.Tensor) and k != "_sps"}
+    check_no_error(ws)
+    return g
+
+
+def _check_async(z, zp, tau, sps, anchor, tokens):
+    g = _run_async(z, zp, tau, sps, anchor, tokens)
+    o = S.schedule(z, tau, sps, anchor, tokens, mode=S.MODE_ASYNC_TOPK, conf_logit_prev=zp)
+    np.testing.assert_array_equal(g["surv"], o["a"])
+    if o["cap_margin"] <= 1e-12:  # the capacity's argmax is a near tie: exempt
+        return False, g, o
+    return compare_schedule(g, o, surv_equal=True), g, o
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_schedule_async_random_small(seed):
+    rng = np.random.default_rng(300 + seed)
+    B, G = int(rng.integers(1, 40)), int(rng.integers(1, 9))
+    tau = rng.uniform(0.8, 1.5, G).astype(np.float32)
+    n = np.arange(B * (1 + G) + 1, dtype=np.float64)
+    kind = ["tiny", "exp2048"][seed % 2]
+    sps = synth.sps_table(kind, B, G) if seed % 3 != 2 else 100.0 / (1.0 + np.floor(n / 3) * 0.05)
+    z = synth.random_conf_logits(B, G, seed)
+    zp = synth.random_conf_logits(B, G, seed + 1000)
+    compared, g, o = _check_async(z, zp, tau, sps, rng.integers(0, 1000, B), synth.random_tokens(B, G, 1000, seed))
+    assert compared
+
+
+@pytest.mark.parametrize("B,G", [(256, 7), (256, 15), (1024, 7), (64, 32)])
+def test_schedule_async_workload_sizes(B, G):
+    rng = np.random.default_rng(B * 3 + G)
+    tau = rng.uniform(0.8, 1.5, G).astype(np.float32)
+    z, _, sps, anchor, tokens = _case(B * 11 + G, B, G)
+    zp = synth.random_conf_logits(B, G, B * 13 + G, scale=2.5, shift=0.5)
+    compared, g, o = _check_async(z, zp, tau, sps, anchor, tokens)
+    assert compared
+    assert int(g["ell"].sum()) == o["n_admit"] <= o["K"]
+
+
+def test_schedule_async_same_confidences_is_the_global_search():
+    # earlier = current confidences on a stepped cost table: the admission is the
+    # best prefix of the whole path, past the first local maximum
+    B, G = 40, 6
+    z, tau, _, anchor, tokens = _case(77, B, G)
+    n = np.arange(B * (1 + G) + 1, dtype=np.float64)
+    sps = 100.0 / (1.0 + np.floor(n / 4) * 0.08)
+    compared, g, o = _check_async(z, z, tau, sps, anchor, tokens)
+    assert compared
+    full = S.prefix_schedule(o["a"], sps, S.MODE_GREEDY, early_stop=False)
+    np.testing.assert_array_equal(g["ell"], full["ell"])
+
+
+def test_schedule_async_unsupported_beyond_shared_memory():
+    B, G = 4096, 7
+    z, tau, sps, anchor, tokens = _case(5, B, G)
+    with pytest.raises(Exception, match="UNSUPPORTED|unsupported|2"):
+        _run_async(z, z, tau, sps, anchor, tokens)
