@@ -172,3 +172,65 @@ def random_conf_logits(B: int, gamma: int, seed: int, scale: float = 2.5, shift:
 def random_tokens(B: int, gamma: int, V: int, seed: int) -> np.ndarray:
     rng = np.random.default_rng(seed)
     return rng.integers(0, V, size=(B, gamma), dtype=np.int64).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# held-out blocks for fitting the STS temperatures
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class StsWorkload:
+    name: str
+    N: int          # held-out draft blocks
+    gamma: int
+    n_grid: int     # candidate temperatures, geometric between grid_lo and grid_hi
+    n_bins: int
+    grid_lo: float = 0.25
+    grid_hi: float = 4.0
+    seed: int = 0
+
+
+STS_WORKLOADS = {
+    # small case the oracle finishes in seconds
+    "sts_small": StsWorkload("sts_small", 3000, 5, 24, 15, seed=11),
+    # held-out set of a production-sized calibration run
+    "sts_N131072_g7_G128_M15": StsWorkload("sts_N131072_g7_G128_M15", 131072, 7, 128, 15, seed=12),
+}
+
+
+def sts_grid(n_grid: int, lo: float = 0.25, hi: float = 4.0) -> np.ndarray:
+    """fp32 candidate temperatures, geometric from lo to hi (one value: lo)."""
+    if n_grid == 1:
+        return np.array([lo], np.float32)
+    return np.geomspace(lo, hi, n_grid).astype(np.float32)
+
+
+def sts_heldout(N: int, gamma: int, seed: int, kappa=None, mu0: float = 2.2, mu_step: float = 0.25,
+                spread: float = 1.5, noise: float = 0.0):
+    """Held-out draft blocks with a known calibration.
+
+    Data model: the chance that draft position k is accepted, given that the
+    positions before it were, is q = 1 / (1 + exp(-u)) with u ~ N(mu0 -
+    mu_step (k-1), spread^2); a block's accept length is the number of leading
+    accepted positions drawn that way.  The confidence head reports the
+    over-confident logit z = kappa_k u (+ noise N(0, noise^2)), so that the
+    temperature kappa_k calibrates position k exactly when noise = 0.
+    Returns (conf_logit [N, gamma] float32, accept_len [N] int32, kappa [gamma])."""
+    rng = np.random.default_rng(seed)
+    if kappa is None:
+        kappa = 1.6 + 0.08 * np.arange(gamma)
+    kappa = np.asarray(kappa, dtype=np.float64)
+    mu = mu0 - mu_step * np.arange(gamma)
+    u = mu[None, :] + spread * rng.standard_normal((N, gamma))
+    q = 1.0 / (1.0 + np.exp(-u))
+    acc = rng.random((N, gamma)) < q
+    accept_len = np.cumprod(acc, axis=1).sum(axis=1).astype(np.int32)
+    z = kappa[None, :] * u + noise * rng.standard_normal((N, gamma))
+    return z.astype(np.float32), accept_len, kappa
+
+
+def sts_inputs(wl: StsWorkload, noise: float = 0.6):
+    """conf_logit, accept_len and grid of a held-out workload (the head is noisy:
+    its discrimination is imperfect, as the pages' ROC-AUC of 0.81-0.90 says)."""
+    z, L, kappa = sts_heldout(wl.N, wl.gamma, wl.seed, noise=noise)
+    return dict(conf_logit=z, accept_len=L, grid=sts_grid(wl.n_grid, wl.grid_lo, wl.grid_hi),
+                n_bins=wl.n_bins, kappa=kappa)

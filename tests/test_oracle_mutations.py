@@ -109,3 +109,46 @@ def test_async_scheduler_mutations_are_caught(old, new):
         finally:
             T.S = saved
     assert failed > 0
+
+
+def _sts_pins_hold(mod):
+    """The STS-fitting pins run against a (possibly mutated) oracle module."""
+    import synth
+    ok = True
+    # hand-worked ECEs (bin edges, weights)
+    ok &= abs(mod.ece([0.125, 0.1875, 0.5, 0.5625, 0.875, 0.9375, 1.0], [0, 1, 1, 0, 1, 1, 1], 5) - 15 / 112) < 1e-15
+    ok &= abs(mod.ece([0.25, 0.125, 0.5, 1.0, 0.75], [0, 1, 1, 1, 0], 4) - 19 / 40) < 1e-15
+    # all accepted: the sharpest temperature everywhere
+    rng = np.random.default_rng(2)
+    z = (0.5 + 3 * rng.random((400, 4))).astype(np.float32)
+    o = mod.sts_fit(z, np.full(400, 4, np.int32), np.array([0.5, 0.8, 1.0, 1.7, 3.0], np.float32), 10)
+    ok &= list(o["grid_index"]) == [0, 0, 0, 0]
+    # ties go to the first entry
+    o = mod.sts_fit(np.full((50, 2), 60.0, np.float32), np.full(50, 2, np.int32),
+                    np.array([2.0, 0.5, 1.0], np.float32), 15)
+    ok &= list(o["grid_index"]) == [0, 0]
+    # recovery of a known over-confidence
+    kappa = np.array([1.5, 2.0, 1.25, 2.5])
+    z, L, _ = synth.sts_heldout(200_000, 4, 8, kappa=kappa, mu0=1.5, mu_step=0.2)
+    o = mod.sts_fit(z, L, synth.sts_grid(97, 0.5, 4.0), 15)
+    ok &= bool(np.all(np.abs(o["sts_temp"] / kappa - 1) < 0.08))
+    return bool(ok)
+
+
+def test_unmutated_sts_fit_passes():
+    from oracle import sts_fit
+    assert _sts_pins_hold(sts_fit)
+
+
+@pytest.mark.parametrize("old,new", [
+    ("label = L >= k + 1", "label = L > k + 1"),                                        # label off by one
+    ("p = (prev * c[:, 0]).astype(np.float32)", "p = (prev_raw * c[:, 0]).astype(np.float32)"),  # earlier positions not held at their fit
+    ("np.floor(p * n_bins)", "(np.ceil(p * n_bins) - 1).clip(0)"),                      # right-closed bins
+    ("return float(np.sum(np.abs(gap)) / N)", "return float(np.mean(np.abs(gap)))"),   # bins not weighted by size
+    ("index[k] = int(np.argmin(table[k]))",
+     "index[k] = int(n_grid - 1 - np.argmin(table[k][::-1]))"),                        # ties to the last entry
+    ("gap = np.bincount(m, weights=y - p, minlength=n_bins)",
+     "gap = np.bincount(m, weights=np.abs(y - p), minlength=n_bins)"),                 # per-sample instead of per-bin gap
+])
+def test_sts_fit_mutations_are_caught(old, new):
+    assert not _sts_pins_hold(_mutant("sts_fit", old, new))
