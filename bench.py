@@ -16,6 +16,11 @@ metric: request-positions/s = B * gamma / t_step, and the step's % of the HBM
 roofline.  --impl reference times the fp64 CPU oracle on the host cores instead
 (a bounded sample of the same workload, extrapolated per request).
 
+--workload sts_small | sts_N131072_g7_G128_M15 times dspark_sts_fit instead
+(fitting the STS temperatures on a held-out set): metric = sigmoid evaluations
+per second (every block x candidate x position), roofline against the fp64
+issue rate, L2 flushed between fits.
+
 Multi-GPU (torchrun, one rank per GPU): the path shards by request with no
 exchange except the scheduler; this benchmark runs independent replicas (weak
 scaling), barrier + max-over-ranks timing.
@@ -474,6 +479,176 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------------------
+# STS temperature fitting (dspark_sts_fit) on a held-out set
+# ---------------------------------------------------------------------------
+STS_METRIC = "STS fit (block, candidate, position) sigmoid evaluations/s"
+STS_UNIT = "evaluations/s"
+# fp64 arithmetic operations of one calibrated confidence c' (the written-out
+# sigmoid: division 3, exponential 19, reciprocal 5, select 1)
+STS_FP64_OPS_PER_EVAL = 28
+# fp64 issue rate: 2 operations per clock per SM, 152 SMs, 2070 MHz (the part's
+# nominal 1.25 TFLOP/s of FP64 counts a fused multiply-add as two)
+FP64_OPS_PEAK = 152 * 2 * 2.07e9
+
+
+def sts_evals(wl) -> int:
+    # every (block, candidate, position), plus the chosen candidate's products
+    return wl.N * wl.gamma * wl.n_grid + wl.N * (wl.gamma - 1)
+
+
+def run_sts_ours(args, rank, world, local_rank):
+    import torch
+    from draft_sampling_lossless_markov_gb300 import build, capi
+    from draft_sampling_lossless_markov_gb300 import torch_api as T
+
+    build.build()
+    capi.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.STS_WORKLOADS[args.workload]
+    inp = synth.sts_inputs(replace_seed(wl, wl.seed + rank))
+    z = torch.from_numpy(inp["conf_logit"]).to(dev)
+    L = torch.from_numpy(inp["accept_len"]).to(dev)
+    grid = torch.from_numpy(inp["grid"]).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    ws = T.sts_fit_workspace(wl.N, wl.gamma, wl.n_grid, wl.n_bins, device=dev)
+    out = dict(sts_temp=torch.empty(wl.gamma, dtype=torch.float32, device=dev),
+               grid_index=torch.empty(wl.gamma, dtype=torch.int32, device=dev),
+               ece=torch.empty((wl.gamma, wl.n_grid), dtype=torch.float64, device=dev))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the L2
+
+    def fit():
+        T.sts_fit(ws, z, L, grid, wl.n_bins, out=out, stream=stream)
+
+    n0 = capi.dspark_launch_count()
+    with torch.cuda.stream(stream):
+        fit()
+    stream.synchronize()
+    launches_per_fit = capi.dspark_launch_count() - n0
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            fit()
+    stream.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    cvd = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(k & 0xFF)  # L2 flushed between fits, outside the events
+            evs[k][0].record(stream)
+            fit()
+            evs[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+        dist.barrier()
+    code, detail = ws.read_error()
+    if code != 0:
+        raise RuntimeError(f"device error word {capi.dspark_status_string(code)} ({detail})")
+
+    evals = sts_evals(wl)
+    value = world * evals / (ms * 1e-3)
+    achieved = evals * STS_FP64_OPS_PER_EVAL / (ms * 1e-3) / 1e9
+    peak = FP64_OPS_PEAK / 1e9
+
+    # end to end through the public call: pinned host inputs in, temperatures and ECE table out
+    h_z = torch.from_numpy(inp["conf_logit"]).pin_memory()
+    h_L = torch.from_numpy(inp["accept_len"]).pin_memory()
+    h_grid = torch.from_numpy(inp["grid"]).pin_memory()
+    h_temp = torch.empty(wl.gamma, dtype=torch.float32).pin_memory()
+    h_ece = torch.empty((wl.gamma, wl.n_grid), dtype=torch.float64).pin_memory()
+    e2e_ms = []
+    for k in range(max(3, min(args.steps, 10))):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            z.copy_(h_z, non_blocking=True)
+            L.copy_(h_L, non_blocking=True)
+            grid.copy_(h_grid, non_blocking=True)
+            fit()
+            h_temp.copy_(out["sts_temp"], non_blocking=True)
+            h_ece.copy_(out["ece"], non_blocking=True)
+        stream.synchronize()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_t = float(np.median(e2e_ms[1:]))
+    h2d = h_z.numel() * 4 + h_L.numel() * 4 + h_grid.numel() * 4
+    d2h = h_temp.numel() * 4 + h_ece.numel() * 8
+
+    res = {
+        "metric": STS_METRIC, "value": value, "unit": STS_UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic held-out blocks (seeded logistic acceptance model)",
+        "config": {"workload": wl.name, "N": wl.N, "gamma": wl.gamma, "n_grid": wl.n_grid, "n_bins": wl.n_bins,
+                   "l2": "flushed between fits (256 MB write outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "1gpu"},
+        "roofline": {"bound": "alu", "kernel": "dspark_sts_fit (k_sts_hist + k_sts_select per position)",
+                     "achieved": achieved, "peak": peak,
+                     "peak_kind": "fp64 issue rate from the nominal table (2 op/clk/SM x 152 SMs x 2070 MHz)",
+                     "unit": "G fp64-op/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_ops": evals * STS_FP64_OPS_PER_EVAL},
+        "gpu_launches": int(launches_per_fit * args.steps),
+        "launches_per_step": int(launches_per_fit),
+        "clocks": clk,
+        "e2e": {"value": world * evals / (e2e_t * 1e-3), "unit": STS_UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": len(e2e_ms) - 1,
+                "timer": "host wall clock around each full fit (synchronised)"},
+        "result": {"sts_temp": [float(x) for x in out["sts_temp"].cpu()],
+                   "ece_best": [float(out["ece"][k, int(out["grid_index"][k])]) for k in range(wl.gamma)]},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = sts_cpu_baseline(wl, inp)
+    return res
+
+
+def replace_seed(wl, seed):
+    from dataclasses import replace
+    return replace(wl, seed=seed)
+
+
+def sts_oracle_time(wl, inp) -> float:
+    from oracle.sts_fit import sts_fit
+    t0 = time.perf_counter()
+    sts_fit(inp["conf_logit"], inp["accept_len"], inp["grid"], wl.n_bins)
+    return time.perf_counter() - t0
+
+
+def sts_cpu_baseline(wl, inp):
+    sec = sts_oracle_time(wl, inp)
+    return {"value": sts_evals(wl) / sec, "unit": STS_UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"the whole fit ({wl.N} blocks x {wl.n_grid} candidates x {wl.gamma} positions), "
+                      "vectorised NumPy fp64, one host thread"}
+
+
+def run_sts_reference(args):
+    wl = synth.STS_WORKLOADS[args.workload]
+    inp = synth.sts_inputs(wl)
+    for _ in range(min(args.warmup, 1)):
+        sts_oracle_time(wl, inp)
+    secs = [sts_oracle_time(wl, inp) for _ in range(args.steps)]
+    sec = float(np.mean(secs))
+    value = sts_evals(wl) / sec
+    sample = (f"fp64 oracle per step: the whole fit ({wl.N} blocks x {wl.n_grid} candidates x {wl.gamma} "
+              "positions), vectorised NumPy, one host thread")
+    return {"impl": "reference", "metric": STS_METRIC, "value": value, "unit": STS_UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic held-out blocks (seeded logistic acceptance model)",
+            "config": {"workload": wl.name, "N": wl.N, "gamma": wl.gamma, "n_grid": wl.n_grid, "n_bins": wl.n_bins},
+            "cpu_baseline": {"value": value, "unit": STS_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": STS_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,16 +666,17 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    sts = args.workload in synth.STS_WORKLOADS
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_sts_reference(args) if sts else run_reference(args)), flush=True)
         return 0
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    res = run_ours(args, rank, world, local_rank)
+    res = run_sts_ours(args, rank, world, local_rank) if sts else run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

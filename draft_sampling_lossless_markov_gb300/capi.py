@@ -31,10 +31,12 @@ DSPARK_MAX_GAMMA = 32
 DSPARK_MAX_RANK = 1024
 DSPARK_MAX_SCHED_KEYS = 65536
 DSPARK_MAX_VOCAB = 2097152
+DSPARK_STS_MAX_SAMPLES = 8388607
+DSPARK_STS_MAX_TABLE = 16384
 
 EXPORTED = ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
             "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count",
-            "dspark_last_cuda_error", "dspark_schedule_noalloc")
+            "dspark_last_cuda_error", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size", "dspark_sts_fit")
 
 
 class dspark_dims(ctypes.Structure):
@@ -64,6 +66,12 @@ class dspark_verify_args(ctypes.Structure):
                 ("n_out", c_void_p)]
 
 
+class dspark_sts_fit_args(ctypes.Structure):
+    _fields_ = [("N", c_int32), ("gamma", c_int32), ("n_grid", c_int32), ("n_bins", c_int32),
+                ("conf_logit", c_void_p), ("accept_len", c_void_p), ("grid", c_void_p), ("sts_temp", c_void_p),
+                ("grid_index", c_void_p), ("ece", c_void_p)]
+
+
 _lib = None
 
 
@@ -83,8 +91,11 @@ def load() -> ctypes.CDLL:
     lib.dspark_schedule.argtypes = [POINTER(dspark_sched_args), c_void_p, c_size_t, c_void_p]
     lib.dspark_verify.argtypes = [POINTER(dspark_verify_args), c_void_p, c_size_t, c_void_p]
     lib.dspark_schedule_noalloc.argtypes = [POINTER(dspark_sched_args), c_void_p]
+    lib.dspark_sts_fit_workspace_size.argtypes = [c_int32, c_int32, c_int32, c_int32, POINTER(c_size_t)]
+    lib.dspark_sts_fit.argtypes = [POINTER(dspark_sts_fit_args), c_void_p, c_size_t, c_void_p]
     for f in ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
-              "dspark_schedule", "dspark_verify", "dspark_schedule_noalloc"):
+              "dspark_schedule", "dspark_verify", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size",
+              "dspark_sts_fit"):
         getattr(lib, f).restype = c_int32
     lib.dspark_status_string.argtypes = [c_int32]
     lib.dspark_status_string.restype = c_char_p
@@ -146,3 +157,13 @@ def dspark_schedule_noalloc(args: dspark_sched_args, stream: int) -> int:
 
 def dspark_verify(args: dspark_verify_args, workspace: int, nbytes: int, stream: int) -> int:
     return load().dspark_verify(ctypes.byref(args), c_void_p(workspace), nbytes, c_void_p(stream))
+
+
+def dspark_sts_fit_workspace_size(N: int, gamma: int, n_grid: int, n_bins: int) -> tuple[int, int]:
+    n = c_size_t(0)
+    st = load().dspark_sts_fit_workspace_size(N, gamma, n_grid, n_bins, ctypes.byref(n))
+    return st, n.value
+
+
+def dspark_sts_fit(args: dspark_sts_fit_args, workspace: int, nbytes: int, stream: int) -> int:
+    return load().dspark_sts_fit(ctypes.byref(args), c_void_p(workspace), nbytes, c_void_p(stream))

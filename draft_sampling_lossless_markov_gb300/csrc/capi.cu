@@ -188,4 +188,27 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* workspace, size_t
   return cuda_status(launch_verify(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
 }
 
+static bool sts_dims_ok(int32_t N, int32_t gamma, int32_t n_grid, int32_t n_bins) {
+  if (N < 0 || N > DSPARK_STS_MAX_SAMPLES || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return false;
+  if (n_grid < 1 || n_bins < 1) return false;
+  return (int64_t)n_bins * std::max<int32_t>(n_grid, 128) <= DSPARK_STS_MAX_TABLE;
+}
+
+dspark_status dspark_sts_fit_workspace_size(int32_t N, int32_t gamma, int32_t n_grid, int32_t n_bins,
+                                            size_t* bytes) {
+  if (!bytes || !sts_dims_ok(N, gamma, n_grid, n_bins)) return DSPARK_INVALID_ARG;
+  *bytes = sts_layout(N, gamma, n_grid, n_bins).total;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_sts_fit(const dspark_sts_fit_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!a || !sts_dims_ok(a->N, a->gamma, a->n_grid, a->n_bins)) return DSPARK_INVALID_ARG;
+  if ((a->N > 0 && (!a->conf_logit || !a->accept_len)) || !a->grid || !a->sts_temp || !a->ece)
+    return DSPARK_INVALID_ARG;
+  if (!workspace || ((uintptr_t)workspace & 255u)) return DSPARK_INVALID_ARG;
+  const StsLayout L = sts_layout(a->N, a->gamma, a->n_grid, a->n_bins);
+  if (workspace_bytes < L.total) return DSPARK_INVALID_ARG;
+  return cuda_status(launch_sts_fit(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -54,6 +54,18 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
 bool schedule_async_supported(int B, int G);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
+// STS fitting (sts_fit.cu): its own workspace, after a WsHeader.
+struct StsLayout {
+  size_t hp = 0;         // [gamma * n_bins * n_grid] u64 fixed-point prediction sums
+  size_t hy = 0;         // [gamma * n_bins * n_grid] u32 accepted-prefix counts
+  size_t table_end = 0;  // end of the two tables (zeroed per call)
+  size_t P = 0;          // [gamma * N] f32 calibrated running products
+  size_t gidx = 0;       // [gamma] i32 chosen candidates
+  size_t total = 0;
+};
+StsLayout sts_layout(int N, int G, int n_grid, int n_bins);
+cudaError_t launch_sts_fit(const dspark_sts_fit_args& a, uint8_t* ws, const StsLayout& L, cudaStream_t s);
+
 // Tensor-core draft sampler (draft_tc.cu).
 bool draft_tc_supported(const dspark_dims& d);
 cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sts_sigmoid.cuh"
 
 namespace dspark {
 
@@ -34,9 +35,8 @@ constexpr int SCH_WARPS = SCH_THREADS / 32;
 
 // calibrated confidence: fp32 rounding of the fp64 sigmoid of z / tau
 __device__ __forceinline__ float sts_conf(float z, float tau) {
-  const double t = (double)z / (double)tau;
-  const double s = 1.0 / (1.0 + exp(-t));
-  return (float)s;
+  const double td = (double)tau;
+  return sts_sigmoid(z, td, 1.0 / td);
 }
 
 // block-wide exclusive scan of one u32 per thread; returns the exclusive prefix

@@ -164,3 +164,34 @@ def verify(ws: Workspace, target_logits, offsets, ell, tokens, pd_rows, pd_tok, 
                                       _ptr(out["n_out"], torch.int32))
     _check("dspark_verify", capi.dspark_verify(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out
+
+
+def sts_fit_workspace(N: int, gamma: int, n_grid: int, n_bins: int, device="cuda", stream=None) -> Workspace:
+    """Workspace of dspark_sts_fit (separate from the step workspace)."""
+    st, n = capi.dspark_sts_fit_workspace_size(int(N), int(gamma), int(n_grid), int(n_bins))
+    _check("dspark_sts_fit_workspace_size", st)
+    ws = Workspace(torch.empty(max(n, 256), dtype=torch.uint8, device=device))
+    _check("dspark_workspace_init", capi.dspark_workspace_init(ws.ptr, ws.nbytes, _stream(stream)))
+    return ws
+
+
+def sts_fit(ws: Workspace, conf_logit, accept_len, grid, n_bins: int, out: Optional[dict] = None, stream=None):
+    """dspark_sts_fit: conf_logit [N, gamma] f32, accept_len [N] i32, grid [G] f32.
+    Returns dict(sts_temp [gamma] f32, grid_index [gamma] i32, ece [gamma, G] f64)."""
+    N, G = conf_logit.shape
+    n_grid = grid.numel()
+    dev = conf_logit.device
+    if out is None:
+        out = dict(sts_temp=torch.empty(G, dtype=torch.float32, device=dev),
+                   grid_index=torch.empty(G, dtype=torch.int32, device=dev),
+                   ece=torch.empty((G, n_grid), dtype=torch.float64, device=dev))
+    a = capi.dspark_sts_fit_args()
+    a.N, a.gamma, a.n_grid, a.n_bins = int(N), int(G), int(n_grid), int(n_bins)
+    a.conf_logit = _ptr(conf_logit, torch.float32)
+    a.accept_len = _ptr(accept_len, torch.int32)
+    a.grid = _ptr(grid, torch.float32)
+    a.sts_temp = _ptr(out["sts_temp"], torch.float32)
+    a.grid_index = _ptr(out.get("grid_index"), torch.int32)
+    a.ece = _ptr(out["ece"], torch.float64)
+    _check("dspark_sts_fit", capi.dspark_sts_fit(a, ws.ptr, ws.nbytes, _stream(stream)))
+    return out

@@ -287,6 +287,56 @@ typedef struct {
 DSPARK_API dspark_status dspark_verify(const dspark_verify_args* args, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * dspark_sts_fit
+ * ---------------------------------------------------------------------------
+ * [DSpark] 方法细节, "事后校准（Post-hoc Calibration）" (also the MTP survey's
+ * §4.2.3 on STS): the per-position temperatures of Sequential Temperature
+ * Scaling are fitted on held-out draft blocks left to right.  At position k a
+ * 1-D grid search over the candidates picks the one whose calibrated
+ * cumulative product P_k = c'_1 ... c'_k (c'_i = fp32(sigmoid(z_i / tau_i)),
+ * fp32 products as in dspark_schedule) has the smallest expected calibration
+ * error, positions before k held at their chosen temperatures.
+ *   ECE = (1/N) sum_m |sum_{n in bin m} (y_n - P_k,n)|, with n_bins equal-width
+ *   bins on [0, 1] (bin floor(P n_bins), P = 1 in the last) and y_n = 1 when
+ *   accept_len[n] >= k.
+ * Ties go to the first candidate; N = 0 gives ECE 0 and the first candidate.
+ * Inputs  conf_logit [N, gamma] f32 (the confidence head's logits of each
+ *         held-out block); accept_len [N] i32 in 0..gamma (draft tokens of the
+ *         block accepted by a verification of the full block); grid [n_grid]
+ *         f32 candidate temperatures, finite and > 0.
+ * Outputs sts_temp [gamma] f32 (the fitted temperatures, ready for
+ *         dspark_sched_args.sts_temp); grid_index [gamma] i32 (may be NULL);
+ *         ece [gamma, n_grid] f64, the ECE of every candidate at every position.
+ * The ECE sums are exact in 2^-40 fixed point: every ECE is within 2^-41 of
+ * its exact value for these fp32 products.  accept_len outside 0..gamma or a
+ * grid value that is not finite and positive is reported in the workspace
+ * error word (DSPARK_BAD_INPUT, detail = the block or candidate index); the
+ * outputs are then unspecified.  All pointers are device pointers; every
+ * output is written on the stream.  The workspace (size from
+ * dspark_sts_fit_workspace_size, 256-byte aligned, header zeroed once by
+ * dspark_workspace_init) is separate from the step workspace. */
+#define DSPARK_STS_MAX_SAMPLES 8388607 /* N < 2^23: the fixed-point sums fit in 63 bits */
+#define DSPARK_STS_MAX_TABLE 16384     /* n_bins * max(n_grid, 128) */
+
+typedef struct {
+  int32_t N;
+  int32_t gamma;
+  int32_t n_grid;
+  int32_t n_bins;
+  const float* conf_logit;
+  const int32_t* accept_len;
+  const float* grid;
+  float* sts_temp;
+  int32_t* grid_index;
+  double* ece;
+} dspark_sts_fit_args;
+
+DSPARK_API dspark_status dspark_sts_fit_workspace_size(int32_t N, int32_t gamma, int32_t n_grid, int32_t n_bins,
+                                                       size_t* bytes);
+DSPARK_API dspark_status dspark_sts_fit(const dspark_sts_fit_args* args, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* Number of CUDA kernels this library has enqueued since it was loaded (a
  * host-side counter, incremented at launch time; a captured CUDA graph counts
  * its kernels once, at capture).  For accounting only: no library behaviour

@@ -111,3 +111,23 @@ def test_struct_layouts_match_header(lib):
     assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8
     assert ctypes.sizeof(capi.dspark_sched_args) == 16 + 15 * 8
     assert capi.dspark_verify_args.seed.offset == 24 + 8 * 8
+
+
+def test_sts_fit_argument_checks(lib):
+    st, n = capi.dspark_sts_fit_workspace_size(131072, 7, 128, 15)
+    assert st == capi.DSPARK_OK and n >= 7 * 15 * 128 * 12 + 7 * 131072 * 4
+    assert capi.dspark_sts_fit_workspace_size(0, 7, 128, 15)[0] == capi.DSPARK_OK
+    for bad in [(-1, 7, 128, 15), (10, 0, 128, 15), (10, 33, 128, 15), (10, 7, 0, 15), (10, 7, 128, 0),
+                (capi.DSPARK_STS_MAX_SAMPLES + 1, 7, 128, 15), (10, 7, 128, 129), (10, 7, 1024, 17)]:
+        assert capi.dspark_sts_fit_workspace_size(*bad)[0] == capi.DSPARK_INVALID_ARG, bad
+    assert capi.dspark_sts_fit_workspace_size(10, 7, 1024, 16)[0] == capi.DSPARK_OK
+    a = capi.dspark_sts_fit_args()
+    a.N, a.gamma, a.n_grid, a.n_bins = 10, 3, 8, 15
+    assert capi.dspark_sts_fit(a, 0, 0, 0) == capi.DSPARK_INVALID_ARG  # null pointers
+    a.conf_logit = a.accept_len = a.grid = a.sts_temp = a.ece = 256
+    assert capi.dspark_sts_fit(a, 0, 0, 0) == capi.DSPARK_INVALID_ARG  # no workspace
+    assert capi.dspark_sts_fit(a, 256 + 16, 1 << 20, 0) == capi.DSPARK_INVALID_ARG  # misaligned
+    assert capi.dspark_sts_fit(a, 256, 16, 0) == capi.DSPARK_INVALID_ARG  # too small
+    a.n_bins = 200
+    assert capi.dspark_sts_fit(a, 256, 1 << 20, 0) == capi.DSPARK_INVALID_ARG  # table limit
+    assert ctypes.sizeof(capi.dspark_sts_fit_args) == 16 + 6 * 8
