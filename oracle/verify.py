@@ -118,3 +118,27 @@ def verify(target_rows, offsets, ell, tokens, pd_rows, pd_tok, temp, seed, req_i
         sample_margin[idx] = mg
     return dict(n_accept=m, out_tok=out_tok, n_out=m + 1, accept_margin=acc_margin,
                 sample_margin=sample_margin, residual_fallback=fallback)
+
+
+def cap_accept(v, cap):
+    """Cap-accept verification ([MTP Survey] §8, the SGLang integration notes:
+    three verify modes, static (full block), compact (truncated by the
+    scheduler) and cap-accept: the full block is verified but only the
+    scheduled window is committed, to observe the upper bound).
+
+    Reading: with m draft tokens accepted by the full-block verification `v`
+    (the output of verify() with every l_r = gamma) and a window of cap_r
+    tokens, the engine commits the first min(m, cap_r) + 1 emitted tokens.
+    When m > cap_r the last committed token is the accepted draft token
+    x_{cap_r + 1}, itself a sample of p_t^{cap_r + 1} given the prefix, so the
+    commit is lossless like compact verification; n_accept keeps the
+    full-block count m as the observation.
+
+    Returns dict(n_accept [R] (m), n_out [R] (committed tokens),
+    out_tok [R, g+1] (committed tokens, then -1))."""
+    m = np.asarray(v["n_accept"], dtype=np.int64)
+    G1 = v["out_tok"].shape[1]
+    cap = np.clip(np.asarray(cap, dtype=np.int64), 0, G1 - 1)
+    n_out = np.minimum(m, cap) + 1
+    out = np.where(np.arange(G1)[None, :] < n_out[:, None], v["out_tok"], -1)
+    return dict(n_accept=m, n_out=n_out, out_tok=out)

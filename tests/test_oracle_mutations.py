@@ -152,3 +152,42 @@ def test_unmutated_sts_fit_passes():
 ])
 def test_sts_fit_mutations_are_caught(old, new):
     assert not _sts_pins_hold(_mutant("sts_fit", old, new))
+
+
+def _cap_accept_pvalues(cap_fn):
+    from oracle.verify import verify
+    rng = np.random.default_rng(1)
+    V, G, r, R, T = 8, 3, 3, 300_000, 1.0
+    tgt = rng.normal(size=(G + 1, V)) * 1.5
+    U = tgt[:G] + rng.normal(size=(G, V)) * 1.2
+    W1 = rng.normal(size=(V, r)) * 0.8
+    W2 = rng.normal(size=(r, V)) * 0.8
+    d = draft(np.broadcast_to(U, (R, G, V)), W1, W2, np.zeros((R, G, 1)), np.zeros(1 + r),
+              np.full(R, 2), np.full(R, T), 5, np.arange(R))
+    ell = np.full(R, G)
+    fl = S.flatten(ell, np.full(R, 2), d["tokens"])
+    v = verify(tgt[fl["mark_pos"]], fl["offsets"], ell, d["tokens"], d["pd"], d["pd_tok"], np.full(R, T), 5,
+               np.arange(R))
+    c = cap_fn(v, np.random.default_rng(9).integers(0, G + 1, R))
+    pt = special.softmax(tgt / T, axis=1)
+    ps = []
+    for j in range(G):
+        sel = c["n_out"] > j
+        ps.append(stats.chisquare(np.bincount(c["out_tok"][sel, j], minlength=V), pt[j] * sel.sum()).pvalue)
+    return ps
+
+
+def test_unmutated_cap_accept_passes():
+    from oracle.verify import cap_accept
+    assert min(_cap_accept_pvalues(cap_accept)) > 1e-4
+
+
+@pytest.mark.parametrize("old,new", [
+    # the window's last slot takes the full output's final token (a later correction or bonus)
+    ("out = np.where(np.arange(G1)[None, :] < n_out[:, None], v[\"out_tok\"], -1)",
+     "out = np.where(np.arange(G1)[None, :] < n_out[:, None], v[\"out_tok\"], -1)\n"
+     "    out[np.arange(m.size), n_out - 1] = v[\"out_tok\"][np.arange(m.size), m]"),
+])
+def test_cap_accept_mutations_are_caught(old, new):
+    mod = _mutant("verify", old, new)
+    assert min(_cap_accept_pvalues(mod.cap_accept)) < 1e-6

@@ -8,14 +8,18 @@
   ([DSpark] 置信度头的设计, the soft label c* = 1 - ||p_d - p_t||_1 / 2);
 * greedy verification of a draft equal to the target accepts everything and
   emits the argmax chain plus the argmax bonus;
-* degenerate cases: p_d = p_t never rejects, l = 0 emits one target sample.
+* degenerate cases: p_d = p_t never rejects, l = 0 emits one target sample;
+* cap-accept (full-block verification, a committed window): the committed
+  tokens follow p_t^j, the committed length has the law of compact
+  verification with the same window, and a window of gamma or more commits
+  the full output.
 """
 import numpy as np
 import pytest
 from scipy import special, stats
 
 from oracle.draft import draft, draft_row_distribution
-from oracle.verify import verify
+from oracle.verify import cap_accept, verify
 from oracle import schedule as S
 
 SEED = 0xDEC0DE
@@ -170,3 +174,49 @@ def test_residual_zero_mass_falls_back_to_target():
                np.array([[1e9]]), np.array([T]), SEED, np.array([0]))
     assert v["n_accept"][0] == 0 and v["residual_fallback"][0]
     assert 0 <= v["out_tok"][0, 0] < V
+
+
+@pytest.mark.slow
+def test_cap_accept_is_lossless():
+    V, G, R, T = 8, 3, 600_000, 1.0
+    st = _setup(V, G, 3, 5, R)
+    _, v = _run(st, T, np.full(R, G))
+    cap = np.random.default_rng(17).integers(0, G + 1, R)
+    c = cap_accept(v, cap)
+    _check_output_marginals(st, c, T, G)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("window", [0, 1, 2])
+def test_cap_accept_commits_like_compact_verification(window):
+    # the committed length under cap-accept and the emitted length under compact
+    # verification with l = window have the same law (two independent samples)
+    V, G, R, T = 8, 3, 200_000, 1.0
+    st = _setup(V, G, 3, 6, R)
+    _, full = _run(st, T, np.full(R, G), seed=SEED)
+    c = cap_accept(full, np.full(R, window))
+    _, compact = _run(st, T, np.full(R, window), seed=SEED + 1)
+    a = np.bincount(c["n_out"], minlength=window + 2)[1:window + 2]
+    b = np.bincount(compact["n_out"], minlength=window + 2)[1:window + 2]
+    if window == 0:
+        assert a.sum() == b.sum() == R
+    else:
+        assert stats.chi2_contingency(np.stack([a, b])).pvalue > 1e-4
+
+
+def test_cap_accept_structure():
+    V, G, R, T = 8, 4, 2000, 1.0
+    st = _setup(V, G, 3, 7, R)
+    _, v = _run(st, T, np.full(R, G))
+    same = cap_accept(v, np.full(R, G + 3))
+    assert np.array_equal(same["n_out"], v["n_out"]) and np.array_equal(same["out_tok"], v["out_tok"])
+    cap = np.random.default_rng(3).integers(0, G + 1, R)
+    c = cap_accept(v, cap)
+    assert np.array_equal(c["n_accept"], v["n_accept"])  # the observation: the full-block count
+    assert np.array_equal(c["n_out"], np.minimum(v["n_accept"], cap) + 1)
+    for r in range(R):
+        k = c["n_out"][r]
+        assert np.array_equal(c["out_tok"][r, :k], v["out_tok"][r, :k]) and np.all(c["out_tok"][r, k:] == -1)
+    # a window of 0 commits one token: x_1 if it was accepted, else the correction
+    z = cap_accept(v, np.zeros(R))
+    assert np.all(z["n_out"] == 1) and np.array_equal(z["out_tok"][:, 0], v["out_tok"][:, 0])
