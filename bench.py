@@ -186,9 +186,20 @@ def run_ours(args, rank, world, local_rank):
             idx = (s_out["mark_req"].long().clamp_min(0) * (G + 1) + s_out["mark_pos"].long().clamp_min(0))
             torch.index_select(tgt_flat, 0, idx, out=rows)
 
+    cap_accept = args.verify == "cap_accept"
+    if cap_accept:
+        # cap-accept: every request's whole block is verified (its gamma+1 rows in
+        # place), the scheduler's lengths are the committed windows
+        full_offsets = (torch.arange(B + 1, device=dev, dtype=torch.int32) * (G + 1)).contiguous()
+        full_ell = torch.full((B,), G, dtype=torch.int32, device=dev)
+
     def seg2(st):
-        T.verify(ws, rows, s_out["offsets"], s_out["ell"], d_out["tokens"], d_out["pd_rows"], d_out["pd_tok"],
-                 inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st)
+        if cap_accept:
+            T.verify(ws, tgt_flat, full_offsets, full_ell, d_out["tokens"], d_out["pd_rows"], d_out["pd_tok"],
+                     inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st, commit_cap=s_out["ell"])
+        else:
+            T.verify(ws, rows, s_out["offsets"], s_out["ell"], d_out["tokens"], d_out["pd_rows"], d_out["pd_tok"],
+                     inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st)
 
     use_graph = not args.no_graph
     n0 = capi.dspark_launch_count()
@@ -245,7 +256,7 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     ms_steps = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
     ms = float(np.mean(ms_steps))
-    nv = int(s_out["n_verify"][0])
+    nv = B * (G + 1) if cap_accept else int(s_out["n_verify"][0])
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms], device=dev, dtype=torch.float64)
@@ -271,7 +282,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
         "config": {"workload": wl.name, "B": B, "gamma": G, "V": V, "r": wl.r, "H": wl.H, "temp": wl.temp,
                    "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]],
-                   "n_verify_rows": nv,
+                   "verify": args.verify, "n_verify_rows": nv,
                    "l2": "inputs larger than L2 (U alone %.0f MB per step), no flush" % (bytes_["U"] / 1e6),
                    "graph": use_graph, "parallelism": "replicas" if world > 1 else "1gpu"},
         "hbm_frac_step": step_frac,
@@ -355,6 +366,8 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     h_out = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
     h_nout = torch.empty(B, dtype=torch.int32).pin_memory()
     esz = inp["U"].element_size()
+    full_offsets = (torch.arange(B + 1, device=dev, dtype=torch.int32) * (G + 1)).contiguous()
+    full_ell = torch.full((B,), G, dtype=torch.int32, device=dev)
     side = torch.cuda.Stream(device=dev)
     tgt_ready = torch.cuda.Event()
 
@@ -376,8 +389,12 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
             stream.wait_event(tgt_ready)
             idx = s["mark_req"].long().clamp_min(0) * (G + 1) + s["mark_pos"].long().clamp_min(0)
             torch.index_select(tgt_flat, 0, idx, out=rows)
-            v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d["pd_rows"], d["pd_tok"], d_small["temp"],
-                         d_small["req_id"], inp["seed"], stream=stream)
+            if args.verify == "cap_accept":
+                v = T.verify(ws, tgt_flat, full_offsets, full_ell, d["tokens"], d["pd_rows"], d["pd_tok"],
+                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"])
+            else:
+                v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d["pd_rows"], d["pd_tok"],
+                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream)
             h_out.copy_(v["out_tok"], non_blocking=True)
             h_nout.copy_(v["n_out"], non_blocking=True)
         stream.synchronize()
@@ -659,6 +676,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--sched", default="workload", choices=["workload", "async"],
                     help="the workload's scheduler mode, or the asynchronous production mode")
+    ap.add_argument("--verify", default="compact", choices=["compact", "cap_accept"],
+                    help="verify the scheduled prefixes (compact), or the full blocks committing the scheduled "
+                         "windows (cap_accept)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=4, help="requests the oracle runs per step")

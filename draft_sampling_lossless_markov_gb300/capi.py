@@ -63,7 +63,7 @@ class dspark_verify_args(ctypes.Structure):
     _fields_ = [("dims", dspark_dims), ("target_logits", c_void_p), ("offsets", c_void_p), ("ell", c_void_p),
                 ("tokens", c_void_p), ("pd_rows", c_void_p), ("pd_tok", c_void_p), ("temp", c_void_p),
                 ("req_id", c_void_p), ("seed", c_uint64), ("n_accept", c_void_p), ("out_tok", c_void_p),
-                ("n_out", c_void_p)]
+                ("n_out", c_void_p), ("commit_cap", c_void_p)]
 
 
 class dspark_sts_fit_args(ctypes.Structure):

@@ -340,7 +340,9 @@ __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restri
                                                                const float2* __restrict__ fin,
                                                                int32_t* __restrict__ n_accept,
                                                                int32_t* __restrict__ out_tok,
-                                                               int32_t* __restrict__ n_out) {
+                                                               int32_t* __restrict__ n_out,
+                                                               const int32_t* __restrict__ commit_cap,
+                                                               WsHeader* __restrict__ hdr) {
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * PK_WARPS + (threadIdx.x >> 5);
@@ -360,7 +362,19 @@ __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restri
   const int4 fm = fmeta[r];
   const float4 fs = fstat[r];
   const int m = fm.w, L = ell[r];
-  for (int i = lane; i <= G; i += 32) out_tok[(size_t)r * (G + 1) + i] = (i < m) ? tokens[(size_t)r * G + i] : -1;
+  // cap-accept: commit the first min(m, window) + 1 emitted tokens; past the
+  // window the last committed token is the accepted draft token
+  int nout = m + 1;
+  if (commit_cap) {
+    int c = commit_cap[r];
+    if (c < 0 || c > G) {
+      if (lane == 0) report_error(hdr, DSPARK_BAD_INPUT, r);
+      c = c < 0 ? 0 : G;
+    }
+    nout = min(m, c) + 1;
+  }
+  for (int i = lane; i <= G; i += 32)
+    out_tok[(size_t)r * (G + 1) + i] = (i < m && i < nout) ? tokens[(size_t)r * G + i] : -1;
   int x;
   if (!fm.z) {
     x = __float_as_int(fs.x);
@@ -492,9 +506,9 @@ __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restri
     }
   }
   if (lane == 0) {
-    out_tok[(size_t)r * (G + 1) + m] = x;
+    if (nout == m + 1) out_tok[(size_t)r * (G + 1) + m] = x;
     n_accept[r] = m;
-    n_out[r] = m + 1;
+    n_out[r] = nout;
   }
 }
 
@@ -517,7 +531,7 @@ static cudaError_t launch_verify_t(const dspark_verify_args& a, uint8_t* ws, con
                                                   a.seed, G, V, rs, vm, fmeta, fstat, hdr);
   k_verify_final<T><<<dim3(B, FN_SLICES), FN_THREADS, 0, s>>>(tg, a.pd_rows, G, V, fmeta, fstat, fin);
   k_verify_pick<T><<<nw, PK_WARPS * 32, 0, s>>>(tg, a.ell, a.tokens, a.pd_rows, a.req_id, a.seed, B, G, V, fmeta,
-                                                fstat, fin, a.n_accept, a.out_tok, a.n_out);
+                                                fstat, fin, a.n_accept, a.out_tok, a.n_out, a.commit_cap, hdr);
   count_launches(5);
   return cudaGetLastError();
 }

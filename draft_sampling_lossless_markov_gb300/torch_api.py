@@ -144,7 +144,8 @@ def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int
 
 
 def verify(ws: Workspace, target_logits, offsets, ell, tokens, pd_rows, pd_tok, temp, req_id, seed: int,
-           out: Optional[dict] = None, stream=None) -> dict:
+           out: Optional[dict] = None, stream=None, commit_cap=None) -> dict:
+    """dspark_verify; commit_cap [B] i32 (the scheduled windows) selects cap-accept."""
     B, G = tokens.shape
     V = target_logits.shape[-1]
     dev = tokens.device
@@ -162,6 +163,7 @@ def verify(ws: Workspace, target_logits, offsets, ell, tokens, pd_rows, pd_tok, 
     a.seed = int(seed)
     a.n_accept, a.out_tok, a.n_out = (_ptr(out["n_accept"], torch.int32), _ptr(out["out_tok"], torch.int32),
                                       _ptr(out["n_out"], torch.int32))
+    a.commit_cap = _ptr(commit_cap, torch.int32) if commit_cap is not None else None
     _check("dspark_verify", capi.dspark_verify(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out
 

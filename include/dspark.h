@@ -267,6 +267,15 @@ DSPARK_API dspark_status dspark_schedule_noalloc(const dspark_sched_args* args, 
  *         pd_rows [B, gamma, V]; pd_tok [B, gamma]; temp [B]; req_id [B]; seed.
  * Outputs n_accept [B]; out_tok [B, gamma + 1] (the accepted tokens, then the
  *         correction or bonus, then -1); n_out [B] = n_accept + 1.
+ * Cap-accept ([MTP Survey] §8, the SGLang notes' third verify mode: the full
+ * block is verified, only the scheduled window is committed): when
+ * commit_cap [B] (device, 0..gamma) is not NULL, n_out = min(n_accept,
+ * commit_cap) + 1 tokens are committed and out_tok holds -1 after them; when
+ * n_accept > commit_cap the last committed token is the accepted draft token
+ * x_{commit_cap + 1}.  n_accept stays the count the full verification
+ * accepted (the observation).  Pass ell = gamma rows per request for the
+ * full block.  A window outside 0..gamma is clamped and reported in the
+ * workspace error word (DSPARK_BAD_INPUT, detail = request).
  * Only dims.B, gamma, V and dtype are read. */
 typedef struct {
   dspark_dims dims;
@@ -282,6 +291,7 @@ typedef struct {
   int32_t* n_accept;
   int32_t* out_tok;
   int32_t* n_out;
+  const int32_t* commit_cap;
 } dspark_verify_args;
 
 DSPARK_API dspark_status dspark_verify(const dspark_verify_args* args, void* workspace,

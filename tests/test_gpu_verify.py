@@ -142,3 +142,75 @@ def test_verify_vocabulary_not_a_multiple_of_8(V, dt):
     pd = rng.dirichlet(np.full(V, 0.3), size=(B, G)).astype(np.float32)
     pdt = np.take_along_axis(pd, tokens[:, :, None].astype(np.int64), axis=2)[:, :, 0]
     _verify_both(to_np64(rows), rows, fl["offsets"], ell, tokens, pd, pdt, temp, 91, np.arange(B))
+
+
+def _cap_accept_both(inp, tokens, pd32, pdtok32, tempv, req_id, anchor, cap):
+    from oracle.verify import cap_accept
+    B, G = tokens.shape
+    full = S.flatten(np.full(B, G), anchor, tokens)  # the whole block is verified
+    rows = inp["target"][torch.from_numpy(full["mark_req"]).cuda(), torch.from_numpy(full["mark_pos"]).cuda()]
+    rows = rows.contiguous()
+    V = rows.shape[1]
+    ws = workspace_for(B, G, V, 0, 0, rows.dtype)
+    out = T.verify(ws, rows, to_dev_i32(full["offsets"]), to_dev_i32(np.full(B, G)), to_dev_i32(tokens),
+                   to_dev_f32(pd32), to_dev_f32(pdtok32), to_dev_f32(tempv), to_dev_i32(req_id), inp["seed"],
+                   commit_cap=to_dev_i32(cap))
+    torch.cuda.synchronize()
+    check_no_error(ws)
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+    o_full = oracle_verify(to_np64(rows), full["offsets"], np.full(B, G), tokens, pd32, pdtok32, tempv, inp["seed"],
+                           req_id)
+    o = dict(cap_accept(o_full, cap), accept_margin=o_full["accept_margin"], sample_margin=o_full["sample_margin"])
+    st = compare_verify(g, o, ~(np.asarray(tempv) > 0))
+    assert np.all(g["n_out"] == np.minimum(g["n_accept"], cap) + 1)
+    for r in range(B):
+        k = g["n_out"][r]
+        assert np.all(g["out_tok"][r, k:] == -1) and np.all(g["out_tok"][r, :k] >= 0)
+    return g, o, st
+
+
+@pytest.mark.parametrize("temp", ["mixed", "1.0", "0"])
+def test_verify_cap_accept_tiny(temp):
+    wl = synth.WORKLOADS["tiny"]
+    tot = dict(n=0, ex=0)
+    for seed in range(6):
+        inp, tokens, pd32, pdtok32, zl32, tempv, req_id, anchor = _pipeline_inputs(wl, seed, temp=temp)
+        # windows from the scheduler on even seeds, uniform 0..gamma on odd ones
+        if seed % 2 == 0:
+            cap = S.schedule(zl32, np.ones(wl.gamma, np.float32), synth.sps_table(wl.sps, wl.B, wl.gamma), anchor,
+                             tokens, mode=1)["ell"]
+        else:
+            cap = np.random.default_rng(seed).integers(0, wl.gamma + 1, wl.B)
+        g, o, st = _cap_accept_both(inp, tokens, pd32, pdtok32, tempv, req_id, anchor, cap.astype(np.int32))
+        tot["n"] += st["n_requests"]
+        tot["ex"] += st["n_exempt"]
+    assert tot["ex"] <= 0.25 * tot["n"]
+
+
+def test_verify_cap_accept_full_size():
+    wl = synth.get_workload("sweep_B256_g7")
+    inp, tokens, pd32, pdtok32, zl32, tempv, req_id, anchor = _pipeline_inputs(wl, 0, n_oracle=8)
+    cap = S.schedule(zl32, inp["sts"].cpu().numpy(), synth.sps_table(wl.sps, wl.B, wl.gamma), anchor, tokens,
+                     mode=1)["ell"].astype(np.int32)
+    cap[:3] = [0, wl.gamma, 1]
+    g, o, st = _cap_accept_both(inp, tokens, pd32, pdtok32, tempv, req_id, anchor, cap)
+    assert st["n_exempt"] <= 0.3 * st["n_requests"]
+
+
+def test_verify_cap_accept_reports_a_window_out_of_range():
+    wl = synth.WORKLOADS["tiny"]
+    inp, tokens, pd32, pdtok32, zl32, tempv, req_id, anchor = _pipeline_inputs(wl, 1)
+    B, G = tokens.shape
+    full = S.flatten(np.full(B, G), anchor, tokens)
+    rows = inp["target"][torch.from_numpy(full["mark_req"]).cuda(), torch.from_numpy(full["mark_pos"]).cuda()]
+    ws = workspace_for(B, G, rows.shape[1], 0, 0, rows.dtype)
+    cap = np.full(B, 1, np.int32)
+    cap[2] = G + 1
+    out = T.verify(ws, rows.contiguous(), to_dev_i32(full["offsets"]), to_dev_i32(np.full(B, G)), to_dev_i32(tokens),
+                   to_dev_f32(pd32), to_dev_f32(pdtok32), to_dev_f32(tempv), to_dev_i32(req_id), inp["seed"],
+                   commit_cap=to_dev_i32(cap))
+    torch.cuda.synchronize()
+    from draft_sampling_lossless_markov_gb300 import capi
+    assert ws.read_error() == (capi.DSPARK_BAD_INPUT, 2)
+    # clamped to gamma: the full output for that request
+    assert int(out["n_out"][2]) == int(out["n_accept"][2]) + 1
