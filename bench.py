@@ -387,8 +387,9 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
             # the kept rows in flattened verify order, from the marker tensor
             # (rows past N_v hold markers -1 and take row 0)
             stream.wait_event(tgt_ready)
-            idx = s["mark_req"].long().clamp_min(0) * (G + 1) + s["mark_pos"].long().clamp_min(0)
-            torch.index_select(tgt_flat, 0, idx, out=rows)
+            if args.verify != "cap_accept":
+                idx = s["mark_req"].long().clamp_min(0) * (G + 1) + s["mark_pos"].long().clamp_min(0)
+                torch.index_select(tgt_flat, 0, idx, out=rows)
             if args.verify == "cap_accept":
                 v = T.verify(ws, tgt_flat, full_offsets, full_ell, d["tokens"], d["pd_rows"], d["pd_tok"],
                              d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"])
