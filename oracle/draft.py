@@ -8,6 +8,13 @@ sampled left to right, x0 being the anchor (the previous round's bonus token).
 B_k to the previous token through a rank-r factorisation,
     B(x_{k-1}, .) = W1[x_{k-1}] W2,  W1 in R^{V x r}, W2 in R^{r x V}.
 [DSpark] 方法细节, "置信度头的设计": c_k = sigmoid(w^T [h_k; W1[x_{k-1}]]).
+[DSpark] 方法细节, "RNN头的实现" (the optional head): a recurrent state s_k
+(s_0 = 0) carries the block's whole prefix.  With z_k = [s_{k-1}; W1[x_{k-1}];
+h_k] in R^{2r+H} and one linear map split into gate, candidate and output parts
+W_g, W_c, W_o in R^{r x (2r+H)}:
+    s_k = sigmoid(W_g z_k) * s_{k-1} + (1 - sigmoid(W_g z_k)) * tanh(W_c z_k),
+    B_k(x_{<k}, .) = W2^T tanh(W_o z_k),
+i.e. the Markov head's row W1[x_{k-1}] is replaced by tanh(W_o z_k).
 [DSpark] 方法细节, "并行阶段的局限与设计": the anchor is the first predicted
 position, so gamma backbone inputs give gamma base-logit rows U_1..U_gamma.
 [DeepSpec analysis] §2.2 (DFlash): markov_rank = 0 turns the head into a zero
@@ -20,7 +27,9 @@ Readings where the pages are silent:
 * the confidence weight splits as w = [w_h (H entries); w_e (r entries)], no bias;
 * the draft draw at position k uses Philox uniform (seed, req_id, k, draw 0),
   positions counted from 1;
-* sampling is inverse CDF in token-id order (see `oracle.sampling`).
+* sampling is inverse CDF in token-id order (see `oracle.sampling`);
+* RNN head: the map is one [3r, 2r+H] matrix, rows W_g, then W_c, then W_o;
+  the confidence head keeps its definition (w_e . W1[x_{k-1}]).
 """
 import numpy as np
 
@@ -32,12 +41,12 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True):
+def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True, W_rnn=None):
     """Run the draft sampler for R requests.
 
     U [R, g, V], W1 [V, r], W2 [r, V], h [R, g, H], w [H + r]: real arrays (any
     float dtype; read as fp64).  anchor [R] int, temp [R] float, req_id [R] int,
-    seed int.
+    seed int.  W_rnn [3r, 2r + H] selects the RNN head (None: Markov head).
 
     Returns a dict:
       tokens [R, g] int64        sampled / greedy draft tokens x_1..x_g
@@ -64,6 +73,11 @@ def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True):
     req_id = np.asarray(req_id, dtype=np.int64)
     x_prev = np.asarray(anchor, dtype=np.int64).copy()
     assert ((x_prev >= 0) & (x_prev < V)).all()
+    rnn = W_rnn is not None
+    if rnn:
+        W_rnn = _f64(W_rnn)
+        assert W_rnn.shape == (3 * r, 2 * r + H)
+        state = np.zeros((R, r))                    # s_0 = 0
 
     tokens = np.zeros((R, G), np.int64)
     pd = np.zeros((R, G, V), np.float64) if keep_pd else None
@@ -74,7 +88,14 @@ def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True):
     for k in range(1, G + 1):
         e = W1[x_prev]                              # W1[x_{k-1}]      [R, r]
         zl[:, k - 1] = h[:, k - 1] @ w_h + e @ w_e  # confidence logit
-        logits = U[:, k - 1] + e @ W2               # U_k + B(x_{k-1}, .)
+        if rnn:
+            zk = np.concatenate([state, e, h[:, k - 1]], axis=1)   # [s_{k-1}; W1[x_{k-1}]; h_k]
+            pre = zk @ W_rnn.T
+            gate = 1.0 / (1.0 + np.exp(-pre[:, :r]))
+            cand = np.tanh(pre[:, r:2 * r])
+            e = np.tanh(pre[:, 2 * r:])             # tanh(W_o z_k) takes the place of W1[x_{k-1}]
+            state = gate * state + (1.0 - gate) * cand
+        logits = U[:, k - 1] + e @ W2               # U_k + B_k
         p = np.zeros((R, V))
         x = np.zeros(R, np.int64)
         if sampled.any():

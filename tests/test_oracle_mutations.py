@@ -191,3 +191,37 @@ def test_unmutated_cap_accept_passes():
 def test_cap_accept_mutations_are_caught(old, new):
     mod = _mutant("verify", old, new)
     assert min(_cap_accept_pvalues(mod.cap_accept)) < 1e-6
+
+
+def _rnn_pins_hold(mod):
+    """The RNN-head pins (tests/test_oracle_rnn_head.py) run against a draft module."""
+    import test_oracle_rnn_head as P
+    saved = P.draft
+    P.draft = mod.draft
+    try:
+        P.test_embedding_only_output_is_a_markov_head(1.0)
+        P.test_hidden_only_output_is_a_token_independent_softmax()
+        P.test_open_gate_keeps_the_zero_state()
+        P.test_closed_gate_holds_the_previous_embedding()
+        P.test_half_open_gate_remembers_two_tokens_back()
+        return True
+    except AssertionError:
+        return False
+    finally:
+        P.draft = saved
+
+
+def test_unmutated_rnn_head_passes():
+    import oracle.draft as D
+    assert _rnn_pins_hold(D)
+
+
+@pytest.mark.parametrize("old,new", [
+    ("state = gate * state + (1.0 - gate) * cand", "state = (1.0 - gate) * state + gate * cand"),  # gate inverted
+    ("zk = np.concatenate([state, e, h[:, k - 1]], axis=1)",
+     "zk = np.concatenate([np.zeros_like(state), e, h[:, k - 1]], axis=1)"),                   # state not carried
+    ("e = np.tanh(pre[:, 2 * r:])", "e = np.tanh(pre[:, r:2 * r])"),                          # output from the candidate rows
+    ("gate = 1.0 / (1.0 + np.exp(-pre[:, :r]))", "gate = 1.0 / (1.0 + np.exp(pre[:, :r]))"),  # gate sign
+])
+def test_rnn_head_mutations_are_caught(old, new):
+    assert not _rnn_pins_hold(_mutant("draft", old, new))
