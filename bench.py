@@ -151,6 +151,9 @@ def run_ours(args, rank, world, local_rank):
         # the production mode: capacity from synthetic confidences of an earlier step
         inp["sched_mode"] = synth.SCHED_ASYNC_TOPK
         inp["zprev"] = torch.from_numpy(synth.random_conf_logits(B, G, wl.seed + 77)).to(dev)
+    if args.head == "rnn":
+        # the optional RNN sequential head (fp32 recurrent rows, CUDA-core bias product)
+        inp["W_rnn"] = synth.rnn_weights(wl.r, wl.H, wl.dtype, wl.seed, dev)
     ws = T.Workspace.create(T.dims(B, G, V, wl.r, wl.H, inp["U"].dtype), device=dev)
     cap = B * (G + 1)
     sps_dev = torch.from_numpy(inp["sps"]).to(dev)
@@ -176,7 +179,7 @@ def run_ours(args, rank, world, local_rank):
 
     def seg1(st):
         T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
-                       inp["req_id"], inp["seed"], out=d_out, stream=st)
+                       inp["req_id"], inp["seed"], out=d_out, stream=st, W_rnn=inp.get("W_rnn"))
         sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=st)
 
     def standin(st):
@@ -282,15 +285,18 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
         "config": {"workload": wl.name, "B": B, "gamma": G, "V": V, "r": wl.r, "H": wl.H, "temp": wl.temp,
                    "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]],
-                   "verify": args.verify, "n_verify_rows": nv,
+                   "head": args.head, "verify": args.verify, "n_verify_rows": nv,
                    "l2": "inputs larger than L2 (U alone %.0f MB per step), no flush" % (bytes_["U"] / 1e6),
                    "graph": use_graph, "parallelism": "replicas" if world > 1 else "1gpu"},
         "hbm_frac_step": step_frac,
         "hbm_frac_step_w2_per_position": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
         "breakdown_ms": br,
-        "roofline": {"bound": "hbm", "kernel": "dspark_draft_sample (fz::k_draft_fused, one launch)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("dspark_draft_sample (fz::k_draft_fused, one launch)" if args.head == "markov" else
+                                "dspark_draft_sample, RNN head (k_rnn_step + CUDA-core k_logits_cc x2 + k_select "
+                                "per position)"),
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
-                     "unit": "GB/s", "frac": draft_gbs / peak, "traffic": traffic,
+                     "unit": "GB/s", "frac": draft_gbs / peak, "traffic": traffic if args.head == "markov" else None,
                      "algorithmic_bytes": bytes_["draft_strict"]},
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
@@ -310,7 +316,7 @@ def per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sp
         with torch.cuda.stream(stream):
             ev[0].record(stream)
             T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
-                           inp["req_id"], inp["seed"], out=d_out, stream=stream)
+                           inp["req_id"], inp["seed"], out=d_out, stream=stream, W_rnn=inp.get("W_rnn"))
             ev[1].record(stream)
             sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=stream)
             ev[2].record(stream)
@@ -381,7 +387,7 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
             for k in d_small:
                 d_small[k].copy_(h_small[k], non_blocking=True)
             d = T.draft_sample(ws, d_U, inp["W1"], inp["W2"], d_h, inp["w"], d_small["anchor"], d_small["temp"],
-                               d_small["req_id"], inp["seed"], stream=stream)
+                               d_small["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"))
             s = sched(T, ws, d["conf_logit"], inp, sps_dev, d_small["anchor"], d["tokens"], stream=stream,
                       n_verify_host=h_nv)
             # the kept rows in flattened verify order, from the marker tensor
@@ -677,6 +683,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--sched", default="workload", choices=["workload", "async"],
                     help="the workload's scheduler mode, or the asynchronous production mode")
+    ap.add_argument("--head", default="markov", choices=["markov", "rnn"],
+                    help="the Markov head (default), or the optional RNN sequential head")
     ap.add_argument("--verify", default="compact", choices=["compact", "cap_accept"],
                     help="verify the scheduled prefixes (compact), or the full blocks committing the scheduled "
                          "windows (cap_accept)")

@@ -23,6 +23,9 @@ DSPARK_BAD_INPUT = 5
 DSPARK_BF16 = 0
 DSPARK_F32 = 1
 
+DSPARK_HEAD_MARKOV = 0
+DSPARK_HEAD_RNN = 1
+
 DSPARK_SCHED_OFF = 0
 DSPARK_SCHED_GREEDY = 1
 DSPARK_SCHED_ASYNC_TOPK = 2
@@ -48,7 +51,7 @@ class dspark_draft_args(ctypes.Structure):
     _fields_ = [("dims", dspark_dims), ("U", c_void_p), ("W1", c_void_p), ("W2", c_void_p), ("h", c_void_p),
                 ("w", c_void_p), ("anchor", c_void_p), ("temp", c_void_p), ("req_id", c_void_p),
                 ("seed", c_uint64), ("tokens", c_void_p), ("pd_rows", c_void_p), ("pd_tok", c_void_p),
-                ("conf_logit", c_void_p), ("conf", c_void_p)]
+                ("conf_logit", c_void_p), ("conf", c_void_p), ("W_rnn", c_void_p), ("head", c_int32)]
 
 
 class dspark_sched_args(ctypes.Structure):

@@ -51,7 +51,10 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.zh = take(B * G * sizeof(float));
   L.rowstat = take(B * sizeof(float2));
   L.sel = take(B * sizeof(float4));
-  L.E = take(2 * B * r * elem_size(d.dtype));  // two buffers: positions alternate
+  // two buffers, positions alternate; fp32-sized so that the RNN head's computed
+  // rows fit whatever the dtype
+  L.E = take(2 * B * r * sizeof(float));
+  L.rnn_s = take(2 * B * r * sizeof(float));  // RNN head state s_{k-1}, s_k
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
   // (the fused draft kernel keeps float2 partials of 64-column chunks, rows
   // padded to a multiple of 128)
@@ -144,7 +147,9 @@ dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, s
   if (d.r > 0 && (!a->W1 || !a->W2)) return DSPARK_INVALID_ARG;
   if (d.H + d.r > 0 && !a->w) return DSPARK_INVALID_ARG;
   if (d.H > 0 && !a->h) return DSPARK_INVALID_ARG;
-  const void* big[] = {a->U, a->W1, a->W2, a->h, a->w, a->pd_rows};
+  if (a->head != DSPARK_HEAD_MARKOV && a->head != DSPARK_HEAD_RNN) return DSPARK_INVALID_ARG;
+  if (a->head == DSPARK_HEAD_RNN && (d.r < 1 || !a->W_rnn)) return DSPARK_INVALID_ARG;
+  const void* big[] = {a->U, a->W1, a->W2, a->h, a->w, a->pd_rows, a->head == DSPARK_HEAD_RNN ? a->W_rnn : nullptr};
   for (const void* p : big)
     if (p && !aligned16(p)) return DSPARK_INVALID_ARG;
   WsLayout L;

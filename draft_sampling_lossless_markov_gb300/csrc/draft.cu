@@ -24,6 +24,7 @@
 #include <mutex>
 #include <string>
 #include <cstdlib>
+#include <type_traits>
 #include "common.cuh"
 #include "draft_arith.cuh"
 #include "internal.h"
@@ -61,10 +62,19 @@ __global__ void __launch_bounds__(256) k_conf_hidden(const T* __restrict__ h, co
 // ---------------------------------------------------------------------------
 // E[b] = W1[x_{k-1}], z_k = zh + w_e . E[b], c_k = sigmoid(z_k).  One warp per row.
 // ---------------------------------------------------------------------------
-template <typename T>
+// The row copy is skipped when E is null (the RNN head computes its own rows).
+template <typename T, typename TE>
+__device__ __forceinline__ void store_e(TE* dst, T v) {
+  if constexpr (std::is_same<T, TE>::value)
+    *dst = v;
+  else
+    *dst = to_f32(v);
+}
+
+template <typename T, typename TE>
 __global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
                                                int k, const T* __restrict__ W1, const T* __restrict__ w,
-                                               const float* __restrict__ zh, T* __restrict__ E,
+                                               const float* __restrict__ zh, TE* __restrict__ E,
                                                float* __restrict__ conf_logit, float* __restrict__ conf, int B, int G,
                                                int V, int r, int H, WsHeader* hdr) {
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -79,10 +89,9 @@ __global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ ancho
   if (r > 0) {
     const T* row = W1 + (size_t)x * r;
     const T* we = w + H;
-    T* dst = E + (size_t)b * r;
     for (int i = lane; i < r; i += 32) {
       const T v = row[i];
-      dst[i] = v;
+      if (E) store_e(E + (size_t)b * r + i, v);
       acc = fmaf(to_f32(we[i]), to_f32(v), acc);
     }
   }
@@ -102,8 +111,8 @@ __global__ void __launch_bounds__(256) k_embed(const int32_t* __restrict__ ancho
 constexpr int CC_ROWS = 16;
 constexpr int CC_TW = 256;
 
-template <typename T, bool WRITE>
-__global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, const T* __restrict__ E,
+template <typename T, typename TE, bool WRITE>
+__global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, const TE* __restrict__ E,
                                                      const T* __restrict__ W2, const float* __restrict__ temp,
                                                      int B, int G, int V, int r, int k, int ntiles,
                                                      float4* __restrict__ part, const float2* __restrict__ rowstat,
@@ -241,9 +250,9 @@ __device__ __forceinline__ float block_excl_scan_256(float v, float* sm, float& 
 // After x_k is chosen the same CTA prepares position k + 1: it copies
 // W1[x_k] into the other E buffer and evaluates that position's confidence,
 // z_{k+1} = zh + w_e . W1[x_k] (the arithmetic of k_embed).
-template <typename T>
+template <typename T, typename TE>
 __device__ __forceinline__ void embed_next(int x, int b, int k, const T* __restrict__ W1, const T* __restrict__ w,
-                                           const float* __restrict__ zh, T* __restrict__ Enext,
+                                           const float* __restrict__ zh, TE* __restrict__ Enext,
                                            float* __restrict__ conf_logit, float* __restrict__ conf, int G, int r,
                                            int H) {
   if (k + 1 >= G || threadIdx.x >= 32) return;
@@ -252,10 +261,9 @@ __device__ __forceinline__ void embed_next(int x, int b, int k, const T* __restr
   if (r > 0) {
     const T* row = W1 + (size_t)x * r;
     const T* we = w + H;
-    T* dst = Enext + (size_t)b * r;
     for (int i = lane; i < r; i += 32) {
       const T v = row[i];
-      dst[i] = v;
+      if (Enext) store_e(Enext + (size_t)b * r + i, v);
       acc = fmaf(to_f32(we[i]), to_f32(v), acc);
     }
   }
@@ -270,12 +278,12 @@ __device__ __forceinline__ void embed_next(int x, int b, int k, const T* __restr
 // Bytes of shared memory k_select stages a W2 tile chunk in.
 constexpr int kSelStageBytes = 32768;
 
-template <typename T>
+template <typename T, typename TE>
 __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict__ part, int ntiles, int tw,
-                                                        const T* __restrict__ U, const T* __restrict__ Ecur,
+                                                        const T* __restrict__ U, const TE* __restrict__ Ecur,
                                                         const T* __restrict__ W2, const T* __restrict__ W1,
                                                         const T* __restrict__ w, const float* __restrict__ zh,
-                                                        T* __restrict__ Enext, const float* __restrict__ temp,
+                                                        TE* __restrict__ Enext, const float* __restrict__ temp,
                                                         const uint32_t* __restrict__ req_id, uint64_t seed, int B,
                                                         int G, int V, int r, int H, int k, int32_t* __restrict__ tokens,
                                                         float2* __restrict__ rowstat, float* __restrict__ conf_logit,
@@ -435,13 +443,18 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
 // ---------------------------------------------------------------------------
 // Host launcher
 // ---------------------------------------------------------------------------
-template <typename T>
-static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+// CUDA-core path, per position: logits pass 1, k_select, logits pass 2.  The
+// rows of the bias product are W1 rows (TE = T, copied by k_embed / k_select)
+// or, for the RNN head, fp32 rows computed by k_rnn_step before each position.
+template <typename T, typename TE>
+static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const dspark_dims& d = a.dims;
   const int B = d.B, G = d.gamma, V = d.V, r = d.r, H = d.H;
+  const bool rnn = a.head == DSPARK_HEAD_RNN;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   float* zh = reinterpret_cast<float*>(ws + L.zh);
-  T* E = reinterpret_cast<T*>(ws + L.E);
+  TE* E = reinterpret_cast<TE*>(ws + L.E);
+  float* S = reinterpret_cast<float*>(ws + L.rnn_s);
   float4* part = reinterpret_cast<float4*>(ws + L.part);
   float2* rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
   const T* U = static_cast<const T*>(a.U);
@@ -449,8 +462,52 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   const T* W2 = static_cast<const T*>(a.W2);
   const T* h = static_cast<const T*>(a.h);
   const T* w = static_cast<const T*>(a.w);
-
   const int BG = B * G;
+
+  k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
+  // position 1's confidence (and, for the Markov head, its W1 rows); later
+  // positions are prepared by k_select
+  k_embed<T, TE><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, 0, W1, w, zh, rnn ? nullptr : E, a.conf_logit,
+                                               a.conf, B, G, V, r, H, hdr);
+  count_launches(2 + 3 * G);
+  const int tw = CC_TW;
+  const int ntiles = (V + tw - 1) / tw;
+  const size_t es_bytes = (size_t)CC_ROWS * r * sizeof(float);
+  if (es_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_logits_cc<T, TE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)es_bytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_logits_cc<T, TE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)es_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  const size_t sel_smem = (size_t)r * sizeof(float) + kSelStageBytes;
+  const dim3 grid_cc(ntiles, (B + CC_ROWS - 1) / CC_ROWS);
+  for (int k = 0; k < G; ++k) {
+    // E holds two buffers: the rows of position k are in buffer k % 2
+    TE* Ecur = E + (size_t)(k & 1) * B * r;
+    TE* Enext = E + (size_t)((k + 1) & 1) * B * r;
+    if (rnn) {
+      // position k + 1 (1-based): s_k from s_{k-1}, e_{k+1} into Ecur
+      const cudaError_t e = launch_rnn_step(a, k + 1, S + (size_t)(k & 1) * B * r, S + (size_t)((k + 1) & 1) * B * r,
+                                            reinterpret_cast<float*>(Ecur), s);
+      if (e != cudaSuccess) return e;
+    }
+    k_logits_cc<T, TE, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part,
+                                                                rowstat, a.tokens, a.pd_rows, a.pd_tok);
+    k_select<T, TE><<<B, SEL_THREADS, sel_smem, s>>>(part, ntiles, tw, U, Ecur, W2, W1, w, zh, rnn ? nullptr : Enext,
+                                                     a.temp, a.req_id, a.seed, B, G, V, r, H, k, a.tokens, rowstat,
+                                                     a.conf_logit, a.conf);
+    k_logits_cc<T, TE, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part,
+                                                               rowstat, a.tokens, a.pd_rows, a.pd_tok);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  // the RNN head computes fp32 rows: CUDA-core bias product
+  if (a.head == DSPARK_HEAD_RNN) return launch_cuda_core<T, float>(a, ws, L, s);
   if (draft_tc_supported(d)) {
     // tensor-core path: the fused-sweep persistent kernel (which forms w_h . h
     // itself), else the two-pass kernel (DSPARK_DRAFT_LAUNCH=two_pass or
@@ -465,44 +522,13 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
       const cudaError_t e = launch_draft_fused(a, ws, L, s);
       if (e != cudaErrorNotSupported) return e;
     }
-    k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
+    const int BG = d.B * d.gamma;
+    k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(static_cast<const T*>(a.h), static_cast<const T*>(a.w),
+                                                  reinterpret_cast<float*>(ws + L.zh), BG, d.H);
     count_launches(1);
     return launch_draft_tc(a, ws, L, s);
   }
-  k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(h, w, zh, BG, H);
-
-  // CUDA-core path
-  // position 0's embedding; later positions are prepared by k_select
-  k_embed<T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, 0, W1, w, zh, E, a.conf_logit, a.conf, B, G, V, r, H,
-                                           hdr);
-  count_launches(2 + 3 * G);
-  const int tw = CC_TW;
-  const int ntiles = (V + tw - 1) / tw;
-  const size_t es_bytes = (size_t)CC_ROWS * r * sizeof(float);
-  if (es_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_logits_cc<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)es_bytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_logits_cc<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)es_bytes);
-    if (e != cudaSuccess) return e;
-  }
-  const size_t sel_smem = (size_t)r * sizeof(float) + kSelStageBytes;
-  const dim3 grid_cc(ntiles, (B + CC_ROWS - 1) / CC_ROWS);
-  for (int k = 0; k < G; ++k) {
-    // E holds two buffers: W1 rows of x_{k-1} for position k are in buffer k % 2
-    T* Ecur = E + (size_t)(k & 1) * B * r;
-    T* Enext = E + (size_t)((k + 1) & 1) * B * r;
-    {
-      k_logits_cc<T, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
-                                                             a.tokens, a.pd_rows, a.pd_tok);
-    }
-    k_select<T><<<B, SEL_THREADS, sel_smem, s>>>(part, ntiles, tw, U, Ecur, W2, W1, w, zh, Enext, a.temp, a.req_id,
-                                                 a.seed, B, G, V, r, H, k, a.tokens, rowstat, a.conf_logit, a.conf);
-    {
-      k_logits_cc<T, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part, rowstat,
-                                                            a.tokens, a.pd_rows, a.pd_tok);
-    }
-  }
-  return cudaGetLastError();
+  return launch_cuda_core<T, T>(a, ws, L, s);
 }
 
 cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {

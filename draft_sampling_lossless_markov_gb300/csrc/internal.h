@@ -23,7 +23,7 @@ constexpr int kDraftMaxSeg = 160;
 
 struct WsLayout {
   size_t zh = 0;       // [B*G] f32: w_h . h_k
-  size_t E = 0;        // [2][B*r] dtype: W1 rows of the previous tokens, two alternating buffers
+  size_t E = 0;        // [2][B*r] (f32-sized): the rows the bias product uses, W1 rows (dtype) or RNN rows (f32)
   size_t part = 0;     // [B*ntiles] float4: (tile max, tile sum-exp, argmax value, argmax index);
                        // the fused kernel keeps float2 partials of 64-column chunks there
   size_t rowstat = 0;  // [B] float2: (row max, row sum) of the current position
@@ -38,6 +38,7 @@ struct WsLayout {
   size_t vfmeta = 0;   // [B] int4: final row, rejecting?, sampled?, accepted count
   size_t vfstat = 0;   // [B] float4: final row's max, 1/sum, scale
   size_t vfin = 0;     // [B * 32 ceil(ceil(V/256)/32)] float2: verify chunk sums of the final draw
+  size_t rnn_s = 0;    // [2][B*r] f32: RNN head state, positions alternate
   size_t total = 0;
 };
 
@@ -53,6 +54,11 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
 // whether the asynchronous top-K mode can run at this size (one CTA's shared memory)
 bool schedule_async_supported(int B, int G);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+
+// RNN head (rnn_head.cu): the recurrent step of position j (1-based): s_j and
+// the fp32 row e_j from s_{j-1} (ignored for j = 1), x_{j-1} and h_j.
+cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* s_prev, float* s_new, float* E,
+                            cudaStream_t s);
 
 // STS fitting (sts_fit.cu): its own workspace, after a WsHeader.
 struct StsLayout {

@@ -83,7 +83,8 @@ class Workspace:
 
 
 def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int, out: Optional[dict] = None,
-                 stream=None) -> dict:
+                 stream=None, W_rnn=None) -> dict:
+    """dspark_draft_sample; W_rnn [3r, 2r + H] (the dtype of U) selects the RNN head."""
     B, G, V = U.shape
     r = W1.shape[1] if W1 is not None else 0
     H = h.shape[2] if h is not None else 0
@@ -104,6 +105,8 @@ def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int
     a.tokens, a.pd_rows = _ptr(out["tokens"], torch.int32), _ptr(out["pd_rows"], torch.float32)
     a.pd_tok, a.conf_logit = _ptr(out["pd_tok"], torch.float32), _ptr(out["conf_logit"], torch.float32)
     a.conf = _ptr(out["conf"], torch.float32)
+    if W_rnn is not None:
+        a.W_rnn, a.head = _ptr(W_rnn, dt), capi.DSPARK_HEAD_RNN
     _check("dspark_draft_sample", capi.dspark_draft_sample(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out
 

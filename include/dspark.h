@@ -131,7 +131,18 @@ DSPARK_API dspark_status dspark_read_error(void* workspace, int32_t* code_host, 
  *         (= pd_rows at the drawn token, bit for bit); conf_logit and conf
  *         [B, gamma] f32.
  * An anchor outside [0, V) is replaced by 0 and reported as DSPARK_BAD_INPUT
- * through the error word. */
+ * through the error word.
+ *
+ * head = DSPARK_HEAD_RNN ([DSpark] 方法细节, "RNN头的实现", the optional head)
+ * replaces the row W1[x_{k-1}] of the bias product by e_k = tanh(W_o z_k),
+ * z_k = [s_{k-1}; W1[x_{k-1}]; h_k] in R^{2r+H}, with the recurrent state
+ *     s_k = g * s_{k-1} + (1 - g) * tanh(W_c z_k),  g = sigmoid(W_g z_k),  s_0 = 0.
+ * W_rnn [3r, 2r + H] (dims.dtype) holds the rows of W_g, then W_c, then W_o.
+ * The confidence head is unchanged.  e_k and s_k are fp32, and the RNN head
+ * runs the CUDA-core bias product (fp32 FMA) for either dtype.  It needs
+ * r >= 1; head = DSPARK_HEAD_MARKOV (0) ignores W_rnn. */
+typedef enum { DSPARK_HEAD_MARKOV = 0, DSPARK_HEAD_RNN = 1 } dspark_head;
+
 typedef struct {
   dspark_dims dims;
   const void* U;
@@ -148,6 +159,8 @@ typedef struct {
   float* pd_tok;
   float* conf_logit;
   float* conf;
+  const void* W_rnn;
+  int32_t head;
 } dspark_draft_args;
 
 DSPARK_API dspark_status dspark_draft_sample(const dspark_draft_args* args, void* workspace,

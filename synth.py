@@ -234,3 +234,12 @@ def sts_inputs(wl: StsWorkload, noise: float = 0.6):
     z, L, kappa = sts_heldout(wl.N, wl.gamma, wl.seed, noise=noise)
     return dict(conf_logit=z, accept_len=L, grid=sts_grid(wl.n_grid, wl.grid_lo, wl.grid_hi),
                 n_bins=wl.n_bins, kappa=kappa)
+
+
+def rnn_weights(r: int, H: int, dtype: str, seed: int, device="cpu", gain: float = 1.5) -> torch.Tensor:
+    """W_rnn [3r, 2r + H] (rows W_g, W_c, W_o) of the RNN head, N(0, gain^2 / (2r + H)):
+    pre-activations of order gain for unit-scale inputs."""
+    g = torch.Generator(device="cpu").manual_seed(7700 + seed)
+    K = 2 * r + H
+    w = gain / math.sqrt(K) * torch.randn((3 * r, K), generator=g, dtype=torch.float32)
+    return w.to(_torch_dtype(dtype)).to(device)

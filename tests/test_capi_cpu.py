@@ -108,7 +108,7 @@ def test_struct_layouts_match_header(lib):
     # field order and sizes of the ctypes mirrors (64-bit ABI)
     assert ctypes.sizeof(capi.dspark_dims) == 24
     assert capi.dspark_draft_args.seed.offset == 24 + 8 * 8
-    assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8
+    assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8 + 8 + 8
     assert ctypes.sizeof(capi.dspark_sched_args) == 16 + 15 * 8
     assert capi.dspark_verify_args.seed.offset == 24 + 8 * 8
     assert ctypes.sizeof(capi.dspark_verify_args) == 24 + 8 * 8 + 8 + 4 * 8

@@ -1,0 +1,100 @@
+"""GPU parity of the RNN sequential head (dspark_draft_sample, head = RNN)
+against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle.draft import draft as oracle_draft
+from parity import compare_draft, gpu_np, np_inputs, rtol_for, to_np64
+from gpu_common import check_no_error, require_gpu, workspace_for
+from draft_sampling_lossless_markov_gb300 import torch_api as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _run(inp, W_rnn):
+    U = inp["U"]
+    B, G, V = U.shape
+    r, H = inp["W1"].shape[1], inp["h"].shape[2]
+    ws = workspace_for(B, G, V, r, H, U.dtype)
+    out = T.draft_sample(ws, U, inp["W1"], inp["W2"], inp["h"] if H else None, inp["w"], inp["anchor"],
+                         inp["temp"], inp["req_id"], inp["seed"], W_rnn=W_rnn)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+def _invariants(g, V):
+    assert g["tokens"].min() >= 0 and g["tokens"].max() < V
+    pick = np.take_along_axis(g["pd_rows"], g["tokens"][:, :, None].astype(np.int64), axis=2)[:, :, 0]
+    np.testing.assert_array_equal(pick, g["pd_tok"])
+    np.testing.assert_allclose(g["pd_rows"].sum(axis=2), 1.0, rtol=0, atol=5e-5)
+
+
+@pytest.mark.parametrize("temp", ["mixed", "0", "1.0", "0.7"])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_rnn_head_tiny(temp, seed):
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, "cuda", seed=seed, temp=temp, with_target=False)
+    Wr = synth.rnn_weights(wl.r, wl.H, wl.dtype, seed, "cuda")
+    out, ws = _run(inp, Wr)
+    g = gpu_np(out)
+    _invariants(g, wl.V)
+    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr))
+    st = compare_draft(g, o, rtol_for(wl.dtype))
+    assert st["n_tokens_compared"] >= 0.5 * wl.B * wl.gamma
+    check_no_error(ws)
+
+
+@pytest.mark.parametrize("B,G,V,r,H,dt", [
+    (3, 5, 1000, 16, 40, "f32"),    # vocabulary not a multiple of the tile width
+    (17, 3, 1031, 7, 5, "f32"),     # rank below one column tile, odd sizes
+    (130, 4, 2000, 48, 0, "f32"),   # no hidden state, ragged request and column tiles
+    (5, 4, 4104, 64, 24, "bf16"),   # bf16 inputs, fp32 recurrent rows
+    (33, 2, 2056, 1, 8, "bf16"),    # rank 1
+    (40, 6, 1024, 256, 8, "bf16"),  # rank 256 over six positions
+])
+def test_rnn_head_ragged_shapes(B, G, V, r, H, dt):
+    wl = synth.Workload("rnn", B, G, V, H, r, dt, "mixed", synth.SCHED_GREEDY, "tiny", seed=5)
+    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    Wr = synth.rnn_weights(r, H, dt, 3, "cuda")
+    out, ws = _run(inp, Wr)
+    g = gpu_np(out)
+    _invariants(g, V)
+    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr))
+    compare_draft(g, o, rtol_for(dt))
+    check_no_error(ws)
+
+
+def test_rnn_head_full_size_sampled_requests():
+    # the whole B256 batch at V151936, r256, H4096; the oracle recomputes three requests
+    wl = synth.get_workload("sweep_B256_g7")
+    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    Wr = synth.rnn_weights(wl.r, wl.H, wl.dtype, 0, "cuda")
+    out, ws = _run(inp, Wr)
+    subset = [0, 100, 255]
+    idx = torch.tensor(subset, device="cuda")
+    g = {k: v.index_select(0, idx).cpu().numpy() for k, v in out.items()}
+    _invariants(g, wl.V)
+    o = oracle_draft(**np_inputs(inp, idx), W_rnn=to_np64(Wr))
+    compare_draft(g, o, rtol_for(wl.dtype))
+    check_no_error(ws)
+
+
+def test_rnn_head_differs_from_the_markov_head():
+    # same inputs: the recurrent rows change the draft distribution
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, "cuda", seed=4, temp="1.0", with_target=False)
+    inp["W2"] = inp["W2"] * 50  # a bias large enough to move the rows visibly
+    Wr = synth.rnn_weights(wl.r, wl.H, wl.dtype, 4, "cuda")
+    rnn, _ = _run(inp, Wr)
+    ws = workspace_for(wl.B, wl.gamma, wl.V, wl.r, wl.H, inp["U"].dtype)
+    mk = T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
+                        inp["req_id"], inp["seed"])
+    torch.cuda.synchronize()
+    assert float((rnn["pd_rows"][:, 0] - mk["pd_rows"][:, 0]).abs().max()) > 1e-3
