@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, co
                                                      float4* __restrict__ part, const float2* __restrict__ rowstat,
                                                      const int32_t* __restrict__ tokens, float* __restrict__ pd_rows,
                                                      float* __restrict__ pd_tok) {
-  extern __shared__ float Es[];  // [CC_ROWS][r]
+  extern __shared__ float Es[];  // [CC_ROWS][r rounded up to 4]
   __shared__ float red_a[CC_TW / 32][CC_ROWS];
   __shared__ float red_b[CC_TW / 32][CC_ROWS];
   __shared__ int red_i[CC_TW / 32][CC_ROWS];
@@ -133,9 +133,12 @@ __global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, co
   const int col = tile * CC_TW + tid;
   const bool valid = col < V;
 
-  for (int idx = tid; idx < CC_ROWS * r; idx += CC_TW) {
-    const int i = idx / r;
-    Es[idx] = (i < nrows) ? to_f32(E[(size_t)(b0 + i) * r + (idx - i * r)]) : 0.f;
+  // rows padded to a multiple of 4 floats, so that the loop below reads four
+  // rank entries of a row with one 16-byte shared-memory load
+  const int rs = (r + 3) & ~3;
+  for (int idx = tid; idx < CC_ROWS * rs; idx += CC_TW) {
+    const int i = idx / rs, kk = idx - i * rs;
+    Es[idx] = (i < nrows && kk < r) ? to_f32(E[(size_t)(b0 + i) * r + kk]) : 0.f;
   }
   if (tid < CC_ROWS) {
     const float T_ = (tid < nrows) ? temp[b0 + tid] : 1.f;
@@ -148,10 +151,26 @@ __global__ void __launch_bounds__(CC_TW) k_logits_cc(const T* __restrict__ U, co
 #pragma unroll
   for (int i = 0; i < CC_ROWS; ++i) l[i] = 0.f;
   if (valid) {
-    for (int kk = 0; kk < r; ++kk) {
+    // each l[i] is one fma chain over the rank in ascending order (k_select
+    // recomputes a tile with the same chain); four rank steps per shared-memory
+    // load keep the loop on the FMA pipe
+    const int r4 = r & ~3;
+    for (int kk = 0; kk < r4; kk += 4) {
+      const float w0 = ldf(W2 + (size_t)kk * V + col), w1 = ldf(W2 + (size_t)(kk + 1) * V + col);
+      const float w2 = ldf(W2 + (size_t)(kk + 2) * V + col), w3 = ldf(W2 + (size_t)(kk + 3) * V + col);
+#pragma unroll
+      for (int i = 0; i < CC_ROWS; ++i) {
+        const float4 e = *reinterpret_cast<const float4*>(&Es[i * rs + kk]);
+        l[i] = fmaf(e.x, w0, l[i]);
+        l[i] = fmaf(e.y, w1, l[i]);
+        l[i] = fmaf(e.z, w2, l[i]);
+        l[i] = fmaf(e.w, w3, l[i]);
+      }
+    }
+    for (int kk = r4; kk < r; ++kk) {
       const float wv = ldf(W2 + (size_t)kk * V + col);
 #pragma unroll
-      for (int i = 0; i < CC_ROWS; ++i) l[i] = fmaf(Es[i * r + kk], wv, l[i]);
+      for (int i = 0; i < CC_ROWS; ++i) l[i] = fmaf(Es[i * rs + kk], wv, l[i]);
     }
 #pragma unroll
     for (int i = 0; i < CC_ROWS; ++i)
@@ -472,7 +491,7 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
   count_launches(2 + 3 * G);
   const int tw = CC_TW;
   const int ntiles = (V + tw - 1) / tw;
-  const size_t es_bytes = (size_t)CC_ROWS * r * sizeof(float);
+  const size_t es_bytes = (size_t)CC_ROWS * ((r + 3) & ~3) * sizeof(float);
   if (es_bytes > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_logits_cc<T, TE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)es_bytes);
