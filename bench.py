@@ -183,11 +183,9 @@ def run_ours(args, rank, world, local_rank):
         sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=st)
 
     def standin(st):
-        # stand-in for the target forward on the flattened batch (not timed): rows
-        # past N_v hold markers -1 and are clamped to row 0
-        with torch.cuda.stream(st):
-            idx = (s_out["mark_req"].long().clamp_min(0) * (G + 1) + s_out["mark_pos"].long().clamp_min(0))
-            torch.index_select(tgt_flat, 0, idx, out=rows)
+        # stand-in for the target forward on the flattened batch (not timed): the
+        # kept rows of the synthetic target logits, packed by the marker tensor
+        T.pack_rows(inp["target"], s_out["mark_req"], s_out["mark_pos"], s_out["n_verify"], rows, ws, stream=st)
 
     cap_accept = args.verify == "cap_accept"
     if cap_accept:
@@ -351,10 +349,12 @@ def sched(T, ws, conf_logit, inp, sps_dev, anchor, tokens, **kw):
 
 def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     """Same metric through the public API with HOST buffers: each step copies the
-    step's inputs from pinned host memory (U and h on the compute stream; the
-    target model's rows, all B(gamma+1) of them, on a second stream while the
-    draft runs), runs the three calls, places the kept rows by the scheduler's
-    marker tensor on the device, verifies, and reads the result back."""
+    step's inputs from pinned host memory (U, h and the per-request scalars),
+    runs the draft and the scheduler, packs the kept target rows straight from
+    the pinned host buffer by the marker tensor (dspark_pack_rows: only the N_v
+    kept rows cross the host link), verifies, and reads the result back.  With
+    cap-accept every row is verified: the whole target buffer is copied on a
+    second stream while the draft runs."""
     import torch
     B, G, V = wl.B, wl.gamma, wl.V
     h_U = inp["U"].cpu().pin_memory()
@@ -364,8 +364,9 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     d_U = torch.empty_like(inp["U"])
     d_h = torch.empty_like(inp["h"])
     d_small = {k: torch.empty_like(inp[k]) for k in h_small}
-    d_tgt = torch.empty_like(inp["target"])
-    tgt_flat = d_tgt.reshape(-1, V)
+    # cap-accept verifies every row: the whole target buffer moves to the device
+    d_tgt = torch.empty_like(inp["target"]) if args.verify == "cap_accept" else None
+    tgt_flat = d_tgt.reshape(-1, V) if d_tgt is not None else None
     cap = B * (G + 1)
     rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
     h_nv = torch.empty(1, dtype=torch.int32).pin_memory()
@@ -377,10 +378,13 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     side = torch.cuda.Stream(device=dev)
     tgt_ready = torch.cuda.Event()
 
+    cap_accept = args.verify == "cap_accept"
+
     def step():
-        with torch.cuda.stream(side):
-            d_tgt.copy_(h_tgt, non_blocking=True)
-            tgt_ready.record(side)
+        if cap_accept:
+            with torch.cuda.stream(side):
+                d_tgt.copy_(h_tgt, non_blocking=True)
+                tgt_ready.record(side)
         with torch.cuda.stream(stream):
             d_U.copy_(h_U, non_blocking=True)
             d_h.copy_(h_h, non_blocking=True)
@@ -390,13 +394,12 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
                                d_small["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"))
             s = sched(T, ws, d["conf_logit"], inp, sps_dev, d_small["anchor"], d["tokens"], stream=stream,
                       n_verify_host=h_nv)
-            # the kept rows in flattened verify order, from the marker tensor
-            # (rows past N_v hold markers -1 and take row 0)
-            stream.wait_event(tgt_ready)
-            if args.verify != "cap_accept":
-                idx = s["mark_req"].long().clamp_min(0) * (G + 1) + s["mark_pos"].long().clamp_min(0)
-                torch.index_select(tgt_flat, 0, idx, out=rows)
-            if args.verify == "cap_accept":
+            if cap_accept:
+                stream.wait_event(tgt_ready)
+            else:
+                # the kept rows in flattened verify order, pulled from the host
+                T.pack_rows(h_tgt, s["mark_req"], s["mark_pos"], s["n_verify"], rows, ws, stream=stream)
+            if cap_accept:
                 v = T.verify(ws, tgt_flat, full_offsets, full_ell, d["tokens"], d["pd_rows"], d["pd_tok"],
                              d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"])
             else:
@@ -410,13 +413,16 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
         step()
     torch.cuda.synchronize(dev)
     n_e2e = max(1, min(args.steps, 5))
+    nv_rows = 0
     t0 = time.perf_counter()
     for _ in range(n_e2e):
         step()
+        nv_rows += int(h_nv[0])
     t1 = time.perf_counter()
     sec = (t1 - t0) / n_e2e
+    tgt_bytes = h_tgt.numel() * esz if cap_accept else nv_rows / n_e2e * V * esz
     h2d = (h_U.numel() * esz + h_h.numel() * esz + sum(t.numel() * t.element_size() for t in h_small.values())
-           + h_tgt.numel() * esz)
+           + tgt_bytes)
     d2h = 4 + h_out.numel() * 4 + h_nout.numel() * 4
     return {"value": B * G / sec, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n_e2e, "timer": "host wall clock around each full step (synchronised)"}

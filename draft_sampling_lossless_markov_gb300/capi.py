@@ -39,7 +39,8 @@ DSPARK_STS_MAX_TABLE = 16384
 
 EXPORTED = ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
             "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count",
-            "dspark_last_cuda_error", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size", "dspark_sts_fit")
+            "dspark_last_cuda_error", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size", "dspark_sts_fit",
+            "dspark_pack_rows")
 
 
 class dspark_dims(ctypes.Structure):
@@ -69,6 +70,12 @@ class dspark_verify_args(ctypes.Structure):
                 ("n_out", c_void_p), ("commit_cap", c_void_p)]
 
 
+class dspark_pack_args(ctypes.Structure):
+    _fields_ = [("V", c_int32), ("dtype", c_int32), ("rows_per_request", c_int32), ("max_rows", c_int32),
+                ("n_src_rows", ctypes.c_int64), ("src", c_void_p), ("mark_req", c_void_p), ("mark_pos", c_void_p),
+                ("n_rows", c_void_p), ("dst", c_void_p)]
+
+
 class dspark_sts_fit_args(ctypes.Structure):
     _fields_ = [("N", c_int32), ("gamma", c_int32), ("n_grid", c_int32), ("n_bins", c_int32),
                 ("conf_logit", c_void_p), ("accept_len", c_void_p), ("grid", c_void_p), ("sts_temp", c_void_p),
@@ -96,9 +103,10 @@ def load() -> ctypes.CDLL:
     lib.dspark_schedule_noalloc.argtypes = [POINTER(dspark_sched_args), c_void_p]
     lib.dspark_sts_fit_workspace_size.argtypes = [c_int32, c_int32, c_int32, c_int32, POINTER(c_size_t)]
     lib.dspark_sts_fit.argtypes = [POINTER(dspark_sts_fit_args), c_void_p, c_size_t, c_void_p]
+    lib.dspark_pack_rows.argtypes = [POINTER(dspark_pack_args), c_void_p, c_void_p]
     for f in ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
               "dspark_schedule", "dspark_verify", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size",
-              "dspark_sts_fit"):
+              "dspark_sts_fit", "dspark_pack_rows"):
         getattr(lib, f).restype = c_int32
     lib.dspark_status_string.argtypes = [c_int32]
     lib.dspark_status_string.restype = c_char_p
@@ -170,3 +178,7 @@ def dspark_sts_fit_workspace_size(N: int, gamma: int, n_grid: int, n_bins: int) 
 
 def dspark_sts_fit(args: dspark_sts_fit_args, workspace: int, nbytes: int, stream: int) -> int:
     return load().dspark_sts_fit(ctypes.byref(args), c_void_p(workspace), nbytes, c_void_p(stream))
+
+
+def dspark_pack_rows(args: dspark_pack_args, workspace: int, stream: int) -> int:
+    return load().dspark_pack_rows(ctypes.byref(args), c_void_p(workspace) if workspace else None, c_void_p(stream))

@@ -193,6 +193,15 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* workspace, size_t
   return cuda_status(launch_verify(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
 }
 
+dspark_status dspark_pack_rows(const dspark_pack_args* a, void* workspace, void* stream) {
+  if (!a || a->V < 1 || a->V > DSPARK_MAX_VOCAB || (a->dtype != DSPARK_BF16 && a->dtype != DSPARK_F32)) return DSPARK_INVALID_ARG;
+  if (a->rows_per_request < 1 || a->max_rows < 0 || a->n_src_rows < 0) return DSPARK_INVALID_ARG;
+  if (a->max_rows == 0) return DSPARK_OK;
+  if (!a->src || !a->mark_req || !a->mark_pos || !a->n_rows || !a->dst) return DSPARK_INVALID_ARG;
+  if (workspace && ((uintptr_t)workspace & 255u)) return DSPARK_INVALID_ARG;
+  return cuda_status(launch_pack_rows(*a, static_cast<WsHeader*>(workspace), (cudaStream_t)stream));
+}
+
 static bool sts_dims_ok(int32_t N, int32_t gamma, int32_t n_grid, int32_t n_bins) {
   if (N < 0 || N > DSPARK_STS_MAX_SAMPLES || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return false;
   if (n_grid < 1 || n_bins < 1) return false;

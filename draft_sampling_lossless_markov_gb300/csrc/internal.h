@@ -60,6 +60,9 @@ cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayo
 cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* s_prev, float* s_new, float* E,
                             cudaStream_t s);
 
+// Verify-batch packing (pack.cu).
+cudaError_t launch_pack_rows(const dspark_pack_args& a, WsHeader* hdr, cudaStream_t s);
+
 // STS fitting (sts_fit.cu): its own workspace, after a WsHeader.
 struct StsLayout {
   size_t hp = 0;         // [gamma * n_bins * n_grid] u64 fixed-point prediction sums

@@ -200,3 +200,24 @@ def sts_fit(ws: Workspace, conf_logit, accept_len, grid, n_bins: int, out: Optio
     a.ece = _ptr(out["ece"], torch.float64)
     _check("dspark_sts_fit", capi.dspark_sts_fit(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out
+
+
+def pack_rows(src, mark_req, mark_pos, n_rows, dst, ws: Optional[Workspace] = None, stream=None):
+    """dspark_pack_rows: dst[i] = src[mark_req[i], mark_pos[i]] for i < n_rows[0].
+
+    src [R, rows_per_request, V]: a CUDA tensor or a pinned CPU tensor (read by
+    the GPU in place); mark_req, mark_pos [max_rows] and n_rows [1] int32 CUDA
+    tensors; dst [max_rows, V] CUDA tensor of src's dtype."""
+    if not src.is_contiguous() or not (src.is_cuda or src.is_pinned()):
+        raise ValueError("src must be a contiguous CUDA tensor or a pinned CPU tensor")
+    if src.dtype != dst.dtype:
+        raise TypeError("src and dst dtypes differ")
+    R, G1, V = src.shape
+    a = capi.dspark_pack_args()
+    a.V, a.dtype, a.rows_per_request, a.max_rows = int(V), _DT[src.dtype], int(G1), int(dst.shape[0])
+    a.n_src_rows = int(R * G1)
+    a.src = src.data_ptr()
+    a.mark_req, a.mark_pos = _ptr(mark_req, torch.int32), _ptr(mark_pos, torch.int32)
+    a.n_rows, a.dst = _ptr(n_rows, torch.int32), _ptr(dst)
+    _check("dspark_pack_rows", capi.dspark_pack_rows(a, ws.ptr if ws is not None else 0, _stream(stream)))
+    return dst

@@ -263,6 +263,36 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
 DSPARK_API dspark_status dspark_schedule_noalloc(const dspark_sched_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dspark_pack_rows
+ * ---------------------------------------------------------------------------
+ * [DSpark] 补充细节, "高吞吐量与低延迟推理" (flattened prefixes + marker tensor;
+ * the SGLang notes pack ragged requests into a compact buffer): gathers the
+ * verify batch.  Row i of dst is row (mark_req[i], mark_pos[i]) of src
+ * [R, rows_per_request, V] (dtype) for i < *n_rows, where n_rows is a device
+ * count (dspark_schedule's n_verify); rows of dst past the count are not
+ * written.  src may be device memory or pinned host memory the GPU addresses
+ * directly (only the kept rows then cross the host link).  mark_req,
+ * mark_pos, n_rows are device arrays ([max_rows] each, one count); dst is
+ * [max_rows, V] device memory; max_rows bounds the count (B * (gamma + 1) for
+ * a dspark_schedule batch) and sizes the launch.  A marker outside the source
+ * skips its row and is reported in the error word of `workspace` (any dspark
+ * workspace; NULL: not reported) as DSPARK_BAD_INPUT, detail = the row. */
+typedef struct {
+  int32_t V;
+  int32_t dtype;
+  int32_t rows_per_request;
+  int32_t max_rows;
+  int64_t n_src_rows;
+  const void* src;
+  const int32_t* mark_req;
+  const int32_t* mark_pos;
+  const int32_t* n_rows;
+  void* dst;
+} dspark_pack_args;
+
+DSPARK_API dspark_status dspark_pack_rows(const dspark_pack_args* args, void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_verify
  * ---------------------------------------------------------------------------
  * [DSpark] 背景知识与设计原则, "投机解码的延迟建模": x_k is accepted with

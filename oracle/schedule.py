@@ -223,3 +223,17 @@ def schedule(conf_logit, sts_temp, sps, anchor, tokens, mode=MODE_GREEDY, early_
     res["a"] = a
     res["sts_margin"] = float(m.min()) if m.size else np.inf
     return res
+
+
+def pack_rows(target, mark_req, mark_pos, n_rows=None):
+    """The packed verify batch ([DSpark] 补充细节, "高吞吐量与低延迟推理": the
+    variable-length prefixes are flattened into one buffer; the SGLang notes
+    pack the ragged requests into a compact buffer before the target forward):
+    row i is target[mark_req[i], mark_pos[i]] for i < n_rows.
+
+    target [R, g+1, V]; mark_req, mark_pos [>= n_rows] int.  Returns [n_rows, V]."""
+    target = np.asarray(target)
+    n = len(mark_req) if n_rows is None else int(n_rows)
+    req = np.asarray(mark_req, dtype=np.int64)[:n]
+    pos = np.asarray(mark_pos, dtype=np.int64)[:n]
+    return target[req, pos]

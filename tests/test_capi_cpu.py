@@ -132,3 +132,19 @@ def test_sts_fit_argument_checks(lib):
     a.n_bins = 200
     assert capi.dspark_sts_fit(a, 256, 1 << 20, 0) == capi.DSPARK_INVALID_ARG  # table limit
     assert ctypes.sizeof(capi.dspark_sts_fit_args) == 16 + 6 * 8
+
+
+def test_pack_rows_argument_checks(lib):
+    a = capi.dspark_pack_args()
+    a.V, a.dtype, a.rows_per_request, a.max_rows, a.n_src_rows = 64, capi.DSPARK_BF16, 5, 10, 50
+    assert capi.dspark_pack_rows(a, 0, 0) == capi.DSPARK_INVALID_ARG  # null pointers
+    a.src = a.mark_req = a.mark_pos = a.n_rows = a.dst = 256
+    assert capi.dspark_pack_rows(a, 256 + 8, 0) == capi.DSPARK_INVALID_ARG  # misaligned workspace
+    for field, bad in [("V", 0), ("dtype", 7), ("rows_per_request", 0), ("max_rows", -1), ("n_src_rows", -1)]:
+        b = capi.dspark_pack_args.from_buffer_copy(a)
+        setattr(b, field, bad)
+        assert capi.dspark_pack_rows(b, 0, 0) == capi.DSPARK_INVALID_ARG, field
+    b = capi.dspark_pack_args.from_buffer_copy(a)
+    b.max_rows = 0
+    assert capi.dspark_pack_rows(b, 0, 0) == capi.DSPARK_OK  # nothing to launch
+    assert ctypes.sizeof(capi.dspark_pack_args) == 16 + 8 + 5 * 8

@@ -232,3 +232,18 @@ def test_async_equals_algorithm_1_on_a_unimodal_path():
         es = S.prefix_schedule(a, sps, S.MODE_GREEDY, early_stop=True)
         np.testing.assert_array_equal(res["ell"], es["ell"])
         assert res["theta_best"] == pytest.approx(es["theta_best"], rel=1e-12)
+
+
+def test_pack_rows_is_the_marker_gather():
+    # brute force: walk the requests and their kept positions in order
+    rng = np.random.default_rng(5)
+    R, G, V = 6, 4, 5
+    target = rng.normal(size=(R, G + 1, V))
+    ell = rng.integers(0, G + 1, R)
+    fl = S.flatten(ell, rng.integers(0, 9, R), rng.integers(0, 9, (R, G)))
+    expect = []
+    for r in range(R):
+        for j in range(ell[r] + 1):
+            expect.append(target[r, j])
+    np.testing.assert_array_equal(S.pack_rows(target, fl["mark_req"], fl["mark_pos"]), np.array(expect))
+    np.testing.assert_array_equal(S.pack_rows(target, fl["mark_req"], fl["mark_pos"], 3), np.array(expect[:3]))
