@@ -55,6 +55,7 @@ WsLayout ws_layout(const dspark_dims& d) {
   // rows fit whatever the dtype
   L.E = take(2 * B * r * sizeof(float));
   L.rnn_s = take(2 * B * r * sizeof(float));  // RNN head state s_{k-1}, s_k
+  L.rnn_p = take(B * G * 3 * r * sizeof(float));  // RNN head: W_rnn[:, 2r:] . h_k of every position
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
   // (the fused draft kernel keeps float2 partials of 64-column chunks, rows
   // padded to a multiple of 128)

@@ -489,6 +489,11 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
   k_embed<T, TE><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, 0, W1, w, zh, rnn ? nullptr : E, a.conf_logit,
                                                a.conf, B, G, V, r, H, hdr);
   count_launches(2 + 3 * G);
+  float* P = reinterpret_cast<float*>(ws + L.rnn_p);
+  if (rnn) {
+    const cudaError_t e = launch_rnn_hproj(a, P, s);
+    if (e != cudaSuccess) return e;
+  }
   const int tw = CC_TW;
   const int ntiles = (V + tw - 1) / tw;
   const size_t es_bytes = (size_t)CC_ROWS * ((r + 3) & ~3) * sizeof(float);
@@ -507,8 +512,8 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
     TE* Enext = E + (size_t)((k + 1) & 1) * B * r;
     if (rnn) {
       // position k + 1 (1-based): s_k from s_{k-1}, e_{k+1} into Ecur
-      const cudaError_t e = launch_rnn_step(a, k + 1, S + (size_t)(k & 1) * B * r, S + (size_t)((k + 1) & 1) * B * r,
-                                            reinterpret_cast<float*>(Ecur), s);
+      const cudaError_t e = launch_rnn_step(a, k + 1, P, S + (size_t)(k & 1) * B * r,
+                                            S + (size_t)((k + 1) & 1) * B * r, reinterpret_cast<float*>(Ecur), s);
       if (e != cudaSuccess) return e;
     }
     k_logits_cc<T, TE, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part,

@@ -39,6 +39,7 @@ struct WsLayout {
   size_t vfstat = 0;   // [B] float4: final row's max, 1/sum, scale
   size_t vfin = 0;     // [B * 32 ceil(ceil(V/256)/32)] float2: verify chunk sums of the final draw
   size_t rnn_s = 0;    // [2][B*r] f32: RNN head state, positions alternate
+  size_t rnn_p = 0;    // [B*gamma][3r] f32: RNN head projections of h
   size_t total = 0;
 };
 
@@ -55,10 +56,13 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
 bool schedule_async_supported(int B, int G);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
-// RNN head (rnn_head.cu): the recurrent step of position j (1-based): s_j and
-// the fp32 row e_j from s_{j-1} (ignored for j = 1), x_{j-1} and h_j.
-cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* s_prev, float* s_new, float* E,
-                            cudaStream_t s);
+// RNN head (rnn_head.cu): P [B gamma, 3r] = the h_j part of every position's
+// projection (once per draft call), then the recurrent step of position j
+// (1-based): s_j and the fp32 row e_j from s_{j-1} (ignored for j = 1),
+// x_{j-1} and P.
+cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, cudaStream_t s);
+cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
+                            float* E, cudaStream_t s);
 
 // Verify-batch packing (pack.cu).
 cudaError_t launch_pack_rows(const dspark_pack_args& a, WsHeader* hdr, cudaStream_t s);

@@ -7,11 +7,14 @@
 //     e_j = tanh(W_o z_j),     the row that multiplies W2 in the bias of position j;
 // s_0 = 0 and x_0 is the anchor.
 //
-// One launch per position: a tiled fp32 GEMM [B x (2r+H)] . [(2r+H) x 3r] whose
-// epilogue applies the gates.  A CTA holds 16 requests x 32 state columns and
-// accumulates the three rows of each column (gate, candidate, output) together,
-// so the gate arithmetic needs no second pass.  z is assembled on the fly from
-// the state, the embedding row and the hidden state.
+// The h_j part of z does not depend on the recurrence, so one GEMM per draft
+// call (k_rnn_hproj) forms P[b, j, :] = W_rnn[:, 2r:] . h_j for every position:
+// [B gamma x H] . [H x 3r], 64 x 64 tiles, 4 x 4 outputs per thread.  Each
+// position then takes one launch (k_rnn_step): a tiled fp32 GEMM
+// [B x 2r] . [2r x 3r] over z' = [s_{j-1}; W1[x_{j-1}]], plus P, whose epilogue
+// applies the gates.  A CTA of k_rnn_step holds 16 requests x 32 state columns
+// and accumulates the three rows of each column (gate, candidate, output)
+// together, so the gate arithmetic needs no second pass.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,9 +31,62 @@ constexpr int RN_BN = 32;  // state columns per CTA
 constexpr int RN_KC = 32;  // z entries per shared-memory chunk
 constexpr int RN_THREADS = 256;
 
+constexpr int HP_TM = 64, HP_TN = 64, HP_TK = 16;  // k_rnn_hproj tile
+
+// P[m, q] = sum_i h[m, i] W_rnn[q, 2r + i]  (m = b gamma + j - 1, q < 3r)
+template <typename T>
+__global__ void __launch_bounds__(256) k_rnn_hproj(const T* __restrict__ Wr, const T* __restrict__ h,
+                                                   float* __restrict__ P, int M, int N, int H, int ldw, int woff) {
+  __shared__ __align__(16) float As[2][HP_TK][HP_TM];  // h tile, k-major
+  __shared__ __align__(16) float Bs[2][HP_TK][HP_TN];  // W tile, k-major
+  const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+  const int m0 = blockIdx.y * HP_TM, n0 = blockIdx.x * HP_TN;
+  float acc[4][4] = {};
+  // each thread loads 4 elements of each tile per chunk: row tid / 4, k (tid % 4) * 4 .. + 3
+  const int lr = tid >> 2, lk = (tid & 3) * 4;
+  auto load = [&](int buf, int k0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = k0 + lk + e;
+      const int m = m0 + lr, n = n0 + lr;
+      As[buf][lk + e][lr] = (m < M && k < H) ? to_f32(h[(size_t)m * H + k]) : 0.f;
+      Bs[buf][lk + e][lr] = (n < N && k < H) ? to_f32(Wr[(size_t)n * ldw + woff + k]) : 0.f;
+    }
+  };
+  load(0, 0);
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = 0; k0 < H; k0 += HP_TK) {
+    if (k0 + HP_TK < H) load(buf ^ 1, k0 + HP_TK);
+#pragma unroll
+    for (int kk = 0; kk < HP_TK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][tr * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][kk][tc * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int m = m0 + tr * 4 + u;
+    if (m >= M) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int n = n0 + tc * 4 + v;
+      if (n < N) P[(size_t)m * N + n] = acc[u][v];
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ Wr, const T* __restrict__ W1,
-                                                         const T* __restrict__ h, const int32_t* __restrict__ anchor,
+                                                         const float* __restrict__ P,
+                                                         const int32_t* __restrict__ anchor,
                                                          const int32_t* __restrict__ tokens,
                                                          const float* __restrict__ s_prev, float* __restrict__ s_new,
                                                          float* __restrict__ E, int B, int G, int V, int r, int H,
@@ -38,7 +94,7 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
   __shared__ float zs[RN_BM][RN_KC + 1];
   __shared__ float ws[3][RN_BN][RN_KC + 1];
   __shared__ int xs[RN_BM];
-  const int K = 2 * r + H;
+  const int K = 2 * r, ldw = 2 * r + H;  // the h_j part comes from P
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   const int c0 = blockIdx.x * RN_BN, b0 = blockIdx.y * RN_BM;
   if (tid < RN_BM) {
@@ -57,10 +113,8 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
       if (b < B && i < K) {
         if (i < r)
           v = (j == 1) ? 0.f : s_prev[(size_t)b * r + i];
-        else if (i < 2 * r)
-          v = to_f32(W1[(size_t)xs[m] * r + (i - r)]);
         else
-          v = to_f32(h[((size_t)b * G + (j - 1)) * H + (i - 2 * r)]);
+          v = to_f32(W1[(size_t)xs[m] * r + (i - r)]);
       }
       zs[m][kk] = v;
     }
@@ -69,7 +123,7 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
       const int rem = idx - g * RN_BN * RN_KC;
       const int c = rem / RN_KC, kk = rem - c * RN_KC;
       const int col = c0 + c, i = i0 + kk;
-      ws[g][c][kk] = (col < r && i < K) ? to_f32(Wr[((size_t)g * r + col) * K + i]) : 0.f;
+      ws[g][c][kk] = (col < r && i < K) ? to_f32(Wr[((size_t)g * r + col) * ldw + i]) : 0.f;
     }
     __syncthreads();
 #pragma unroll 8
@@ -89,27 +143,51 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
   for (int q = 0; q < 2; ++q) {
     const int b = b0 + ty + 8 * q;
     if (b >= B || col >= r) continue;
-    const float g = 1.f / (1.f + expf(-ag[q]));
+    float pg = ag[q], pc = ac[q], po = ao[q];
+    if (H > 0) {
+      const float* pr = P + ((size_t)b * G + (j - 1)) * 3 * r;
+      pg += pr[col];
+      pc += pr[r + col];
+      po += pr[2 * r + col];
+    }
+    const float g = 1.f / (1.f + expf(-pg));
     const float sp = (j == 1) ? 0.f : s_prev[(size_t)b * r + col];
-    s_new[(size_t)b * r + col] = g * sp + (1.f - g) * tanhf(ac[q]);
-    E[(size_t)b * r + col] = tanhf(ao[q]);
+    s_new[(size_t)b * r + col] = g * sp + (1.f - g) * tanhf(pc);
+    E[(size_t)b * r + col] = tanhf(po);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* s_prev, float* s_new, float* E,
-                            cudaStream_t s) {
+template <typename T>
+static cudaError_t launch_hproj_t(const dspark_draft_args& a, float* P, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  const int M = d.B * d.gamma, N = 3 * d.r;
+  const dim3 grid((N + HP_TN - 1) / HP_TN, (M + HP_TM - 1) / HP_TM);
+  k_rnn_hproj<T><<<grid, 256, 0, s>>>(static_cast<const T*>(a.W_rnn), static_cast<const T*>(a.h), P, M, N, d.H,
+                                      2 * d.r + d.H, 2 * d.r);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, cudaStream_t s) {
+  if (a.dims.H == 0 || a.dims.B == 0) return cudaSuccess;
+  if (a.dims.dtype == DSPARK_BF16) return launch_hproj_t<__nv_bfloat16>(a, P, s);
+  return launch_hproj_t<float>(a, P, s);
+}
+
+cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
+                            float* E, cudaStream_t s) {
   const dspark_dims& d = a.dims;
   const dim3 grid((d.r + RN_BN - 1) / RN_BN, (d.B + RN_BM - 1) / RN_BM);
   if (d.dtype == DSPARK_BF16)
     k_rnn_step<__nv_bfloat16><<<grid, RN_THREADS, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.W_rnn), static_cast<const __nv_bfloat16*>(a.W1),
-        static_cast<const __nv_bfloat16*>(a.h), a.anchor, a.tokens, s_prev, s_new, E, d.B, d.gamma, d.V, d.r, d.H, j);
+        static_cast<const __nv_bfloat16*>(a.W_rnn), static_cast<const __nv_bfloat16*>(a.W1), P, a.anchor, a.tokens,
+        s_prev, s_new, E, d.B, d.gamma, d.V, d.r, d.H, j);
   else
     k_rnn_step<float><<<grid, RN_THREADS, 0, s>>>(static_cast<const float*>(a.W_rnn), static_cast<const float*>(a.W1),
-                                                  static_cast<const float*>(a.h), a.anchor, a.tokens, s_prev, s_new, E,
-                                                  d.B, d.gamma, d.V, d.r, d.H, j);
+                                                  P, a.anchor, a.tokens, s_prev, s_new, E, d.B, d.gamma, d.V, d.r,
+                                                  d.H, j);
   count_launches(1);
   return cudaGetLastError();
 }
