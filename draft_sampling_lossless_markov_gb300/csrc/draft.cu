@@ -463,8 +463,8 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
 // Host launcher
 // ---------------------------------------------------------------------------
 // CUDA-core path, per position: logits pass 1, k_select, logits pass 2.  The
-// rows of the bias product are W1 rows (TE = T, copied by k_embed / k_select)
-// or, for the RNN head, fp32 rows computed by k_rnn_step before each position.
+// rows of the bias product are W1 rows (copied by k_embed / k_select) or, for
+// the RNN head, the rows k_rnn_step computes before each position.
 template <typename T, typename TE>
 static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const dspark_dims& d = a.dims;
@@ -513,7 +513,7 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
     if (rnn) {
       // position k + 1 (1-based): s_k from s_{k-1}, e_{k+1} into Ecur
       const cudaError_t e = launch_rnn_step(a, k + 1, P, S + (size_t)(k & 1) * B * r,
-                                            S + (size_t)((k + 1) & 1) * B * r, reinterpret_cast<float*>(Ecur), s);
+                                            S + (size_t)((k + 1) & 1) * B * r, Ecur, s);
       if (e != cudaSuccess) return e;
     }
     k_logits_cc<T, TE, false><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part,
@@ -530,8 +530,33 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
 template <typename T>
 static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const dspark_dims& d = a.dims;
-  // the RNN head computes fp32 rows: CUDA-core bias product
-  if (a.head == DSPARK_HEAD_RNN) return launch_cuda_core<T, float>(a, ws, L, s);
+  if (a.head == DSPARK_HEAD_RNN) {
+    if (!draft_tc_supported(d)) return launch_cuda_core<T, T>(a, ws, L, s);
+    // tensor-core passes, one launch per pass; before each position the
+    // recurrent step writes its rows (bf16) and k_embed its confidences
+    const int B = d.B, r = d.r, BG = B * d.gamma;
+    float* zh = reinterpret_cast<float*>(ws + L.zh);
+    float* P = reinterpret_cast<float*>(ws + L.rnn_p);
+    float* S = reinterpret_cast<float*>(ws + L.rnn_s);
+    T* Erows = reinterpret_cast<T*>(ws + L.E);
+    const T* W1 = static_cast<const T*>(a.W1);
+    const T* w = static_cast<const T*>(a.w);
+    k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(static_cast<const T*>(a.h), w, zh, BG, d.H);
+    count_launches(1);
+    cudaError_t e = launch_rnn_hproj(a, P, s);
+    if (e != cudaSuccess) return e;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    const std::function<cudaError_t(int)> hook = [&](int k) {
+      const cudaError_t e2 = launch_rnn_step(a, k + 1, P, S + (size_t)(k & 1) * B * r,
+                                             S + (size_t)((k + 1) & 1) * B * r, Erows, s);
+      if (e2 != cudaSuccess) return e2;
+      k_embed<T, T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, k, W1, w, zh, nullptr, a.conf_logit, a.conf, B,
+                                                d.gamma, d.V, r, d.H, hdr);
+      count_launches(1);
+      return cudaGetLastError();
+    };
+    return launch_draft_tc(a, ws, L, s, &hook, Erows);
+  }
   if (draft_tc_supported(d)) {
     // tensor-core path: the fused-sweep persistent kernel (which forms w_h . h
     // itself), else the two-pass kernel (DSPARK_DRAFT_LAUNCH=two_pass or

@@ -109,6 +109,7 @@ struct Params {
   int ntiles, nparts, ctas_per_m, n_ctas;
   uint64_t seed;
   const __nv_bfloat16* W1;   // [V, r]
+  const __nv_bfloat16* Erows;  // [B, r] rows of the bias product (RNN head), or null: W1[x_{k-1}]
   const __nv_bfloat16* w;    // [H + r] confidence weight (w_e = w + H)
   const float* zh;           // [B, G] w_h . h
   const int32_t* anchor;     // [B]
@@ -565,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             x = 0;
           }
         }
-        const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r);
+        const uint4* src = reinterpret_cast<const uint4*>(p.Erows ? p.Erows + (size_t)(vrow ? b : 0) * r
+                                                                  : p.W1 + (size_t)x * r);
         // one 32-column piece at a time keeps the gather within the register
         // budget; the token's writer prefetched the row into L2
 #pragma unroll 1
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(eready);
       }
-      if (pass_of(0) == 0 && g == 0 && n_lo == 0) {
+      if (pass_of(0) == 0 && g == 0 && n_lo == 0 && !p.Erows) {
         // the first CTA of the M-tile also forms the confidence of position k:
         // z = w_h . h_k + w_e . W1[x_{k-1}], reading the E row back from TMEM
         // once every group has stored its pieces
@@ -1011,7 +1013,8 @@ bool draft_tc_supported(const dspark_dims& d) {
   return tc::dev_info().sm103 && tc::encode_fn() != nullptr;
 }
 
-cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                            const std::function<cudaError_t(int)>* hook, const void* Erows) {
   const dspark_dims& d = a.dims;
   const cuuint64_t V = (cuuint64_t)d.V, G = (cuuint64_t)d.gamma, B = (cuuint64_t)d.B, r = (cuuint64_t)d.r;
   CUtensorMap tmU, tmW2, tmPd;
@@ -1056,6 +1059,7 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
   p.ctas_per_m = std::max(1, std::min(std::min(p.ntiles, sms / n_mtiles), kDraftMaxSeg));
   p.n_ctas = n_mtiles * p.ctas_per_m;
   p.W1 = static_cast<const __nv_bfloat16*>(a.W1);
+  p.Erows = static_cast<const __nv_bfloat16*>(Erows);
   p.w = static_cast<const __nv_bfloat16*>(a.w);
   p.zh = reinterpret_cast<const float*>(ws + L.zh);
   p.anchor = a.anchor;
@@ -1080,7 +1084,7 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
   // than run with CTAs waiting for an SM.
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sync_bytes, s);
   if (e != cudaSuccess) return e;
-  if (!tc::per_pass_forced() && di.coop && n_mtiles <= sms) {
+  if (!hook && !tc::per_pass_forced() && di.coop && n_mtiles <= sms) {
     p.k_begin = 0;
     p.k_end = d.gamma;
     p.pass_only = -1;
@@ -1099,6 +1103,10 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
   }
   count_launches(3 * d.gamma);
   for (int k = 0; k < d.gamma; ++k) {
+    if (hook) {
+      e = (*hook)(k);
+      if (e != cudaSuccess) return e;
+    }
     p.k_begin = k;
     p.k_end = k + 1;
     p.pass_only = 0;

@@ -1,6 +1,8 @@
 // Host-side internals shared by the dspark translation units.
 #pragma once
 
+#include <functional>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -61,8 +63,9 @@ cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayo
 // (1-based): s_j and the fp32 row e_j from s_{j-1} (ignored for j = 1),
 // x_{j-1} and P.
 cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, cudaStream_t s);
+// (E: [B, r] rows in dims.dtype)
 cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
-                            float* E, cudaStream_t s);
+                            void* E, cudaStream_t s);
 
 // Verify-batch packing (pack.cu).
 cudaError_t launch_pack_rows(const dspark_pack_args& a, WsHeader* hdr, cudaStream_t s);
@@ -81,7 +84,12 @@ cudaError_t launch_sts_fit(const dspark_sts_fit_args& a, uint8_t* ws, const StsL
 
 // Tensor-core draft sampler (draft_tc.cu).
 bool draft_tc_supported(const dspark_dims& d);
-cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+// With a hook, one launch per pass and hook(k) before each position k, whose
+// rows the kernel then reads from Erows [B, r] instead of gathering W1 rows
+// (the hook also forms the confidences).
+cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                            const std::function<cudaError_t(int)>* hook = nullptr,
+                            const void* Erows = nullptr);
 // Fused-sweep kernel (draft_fused.cu); cudaErrorNotSupported when it cannot run.
 cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 

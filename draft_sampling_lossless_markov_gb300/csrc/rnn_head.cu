@@ -5,7 +5,9 @@
 // parts (W_rnn = [W_g; W_c; W_o], [3r, 2r+H]),
 //     g   = sigmoid(W_g z_j),  s_j = g * s_{j-1} + (1 - g) * tanh(W_c z_j),
 //     e_j = tanh(W_o z_j),     the row that multiplies W2 in the bias of position j;
-// s_0 = 0 and x_0 is the anchor.
+// s_0 = 0 and x_0 is the anchor.  e_j is stored in the dtype of W2 (the bias
+// product's operand precision, as the Markov head's W1 rows are), rounded to
+// nearest-even from fp32; s_j stays fp32.
 //
 // The h_j part of z does not depend on the recurrence, so one GEMM per draft
 // call (k_rnn_hproj) forms P[b, j, :] = W_rnn[:, 2r:] . h_j for every position:
@@ -83,13 +85,16 @@ __global__ void __launch_bounds__(256) k_rnn_hproj(const T* __restrict__ Wr, con
   }
 }
 
+__device__ __forceinline__ void store_row(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_row(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
 template <typename T>
 __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ Wr, const T* __restrict__ W1,
                                                          const float* __restrict__ P,
                                                          const int32_t* __restrict__ anchor,
                                                          const int32_t* __restrict__ tokens,
                                                          const float* __restrict__ s_prev, float* __restrict__ s_new,
-                                                         float* __restrict__ E, int B, int G, int V, int r, int H,
+                                                         T* __restrict__ E, int B, int G, int V, int r, int H,
                                                          int j) {
   __shared__ float zs[RN_BM][RN_KC + 1];
   __shared__ float ws[3][RN_BN][RN_KC + 1];
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
     const float g = 1.f / (1.f + expf(-pg));
     const float sp = (j == 1) ? 0.f : s_prev[(size_t)b * r + col];
     s_new[(size_t)b * r + col] = g * sp + (1.f - g) * tanhf(pc);
-    E[(size_t)b * r + col] = tanhf(po);
+    store_row(E + (size_t)b * r + col, tanhf(po));
   }
 }
 
@@ -177,17 +182,17 @@ cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, cudaStream_t 
 }
 
 cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
-                            float* E, cudaStream_t s) {
+                            void* E, cudaStream_t s) {
   const dspark_dims& d = a.dims;
   const dim3 grid((d.r + RN_BN - 1) / RN_BN, (d.B + RN_BM - 1) / RN_BM);
   if (d.dtype == DSPARK_BF16)
     k_rnn_step<__nv_bfloat16><<<grid, RN_THREADS, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.W_rnn), static_cast<const __nv_bfloat16*>(a.W1), P, a.anchor, a.tokens,
-        s_prev, s_new, E, d.B, d.gamma, d.V, d.r, d.H, j);
+        s_prev, s_new, static_cast<__nv_bfloat16*>(E), d.B, d.gamma, d.V, d.r, d.H, j);
   else
     k_rnn_step<float><<<grid, RN_THREADS, 0, s>>>(static_cast<const float*>(a.W_rnn), static_cast<const float*>(a.W1),
-                                                  P, a.anchor, a.tokens, s_prev, s_new, E, d.B, d.gamma, d.V, d.r,
-                                                  d.H, j);
+                                                  P, a.anchor, a.tokens, s_prev, s_new, static_cast<float*>(E), d.B,
+                                                  d.gamma, d.V, d.r, d.H, j);
   count_launches(1);
   return cudaGetLastError();
 }

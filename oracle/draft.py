@@ -29,7 +29,10 @@ Readings where the pages are silent:
   positions counted from 1;
 * sampling is inverse CDF in token-id order (see `oracle.sampling`);
 * RNN head: the map is one [3r, 2r+H] matrix, rows W_g, then W_c, then W_o;
-  the confidence head keeps its definition (w_e . W1[x_{k-1}]).
+  the confidence head keeps its definition (w_e . W1[x_{k-1}]); the row
+  tanh(W_o z_k) enters the bias product in that product's operand precision
+  (rnn_row_dtype "bf16" or "f32", as the Markov head's W1 rows do; None keeps
+  fp64), i.e. it is rounded to nearest-even in that format.
 """
 import numpy as np
 
@@ -41,12 +44,25 @@ def _f64(a):
     return np.asarray(a, dtype=np.float64)
 
 
-def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True, W_rnn=None):
+def round_to(x, fmt):
+    """Round fp64 values to nearest-even in fp32 or bfloat16 (bf16 through fp32,
+    which is how a kernel holding the fp32 value rounds it)."""
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    if fmt == "f32":
+        return x32.astype(np.float64)
+    assert fmt == "bf16"
+    b = x32.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True, W_rnn=None, rnn_row_dtype=None):
     """Run the draft sampler for R requests.
 
     U [R, g, V], W1 [V, r], W2 [r, V], h [R, g, H], w [H + r]: real arrays (any
     float dtype; read as fp64).  anchor [R] int, temp [R] float, req_id [R] int,
-    seed int.  W_rnn [3r, 2r + H] selects the RNN head (None: Markov head).
+    seed int.  W_rnn [3r, 2r + H] selects the RNN head (None: Markov head);
+    rnn_row_dtype ("bf16", "f32" or None) is the precision its rows take.
 
     Returns a dict:
       tokens [R, g] int64        sampled / greedy draft tokens x_1..x_g
@@ -94,6 +110,8 @@ def draft(U, W1, W2, h, w, anchor, temp, seed, req_id, keep_pd=True, W_rnn=None)
             gate = 1.0 / (1.0 + np.exp(-pre[:, :r]))
             cand = np.tanh(pre[:, r:2 * r])
             e = np.tanh(pre[:, 2 * r:])             # tanh(W_o z_k) takes the place of W1[x_{k-1}]
+            if rnn_row_dtype is not None:
+                e = round_to(e, rnn_row_dtype)
             state = gate * state + (1.0 - gate) * cand
         logits = U[:, k - 1] + e @ W2               # U_k + B_k
         p = np.zeros((R, V))

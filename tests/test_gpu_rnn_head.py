@@ -1,5 +1,8 @@
 """GPU parity of the RNN sequential head (dspark_draft_sample, head = RNN)
-against the fp64 oracle, through the C ABI."""
+against the fp64 oracle, through the C ABI.  The oracle takes the rows
+tanh(W_o z_k) in the bias product's operand precision (the workload's dtype),
+as the library does; bf16 tensor-core shapes run the tensor-core passes, the
+others the CUDA-core path (a child process forces the latter for bf16 too)."""
 import numpy as np
 import pytest
 import torch
@@ -45,7 +48,7 @@ def test_rnn_head_tiny(temp, seed):
     out, ws = _run(inp, Wr)
     g = gpu_np(out)
     _invariants(g, wl.V)
-    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr))
+    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr), rnn_row_dtype=wl.dtype)
     st = compare_draft(g, o, rtol_for(wl.dtype))
     assert st["n_tokens_compared"] >= 0.5 * wl.B * wl.gamma
     check_no_error(ws)
@@ -57,7 +60,8 @@ def test_rnn_head_tiny(temp, seed):
     (130, 4, 2000, 48, 0, "f32"),   # no hidden state, ragged request and column tiles
     (5, 4, 4104, 64, 24, "bf16"),   # bf16 inputs, fp32 recurrent rows
     (33, 2, 2056, 1, 8, "bf16"),    # rank 1
-    (40, 6, 1024, 256, 8, "bf16"),  # rank 256 over six positions
+    (40, 6, 1024, 256, 8, "bf16"),  # rank 256 over six positions: tensor-core passes
+    (130, 5, 8200, 128, 16, "bf16"),  # two M-tiles, an 8-column last tile: tensor-core passes
 ])
 def test_rnn_head_ragged_shapes(B, G, V, r, H, dt):
     wl = synth.Workload("rnn", B, G, V, H, r, dt, "mixed", synth.SCHED_GREEDY, "tiny", seed=5)
@@ -66,7 +70,7 @@ def test_rnn_head_ragged_shapes(B, G, V, r, H, dt):
     out, ws = _run(inp, Wr)
     g = gpu_np(out)
     _invariants(g, V)
-    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr))
+    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr), rnn_row_dtype=dt)
     compare_draft(g, o, rtol_for(dt))
     check_no_error(ws)
 
@@ -81,7 +85,7 @@ def test_rnn_head_full_size_sampled_requests():
     idx = torch.tensor(subset, device="cuda")
     g = {k: v.index_select(0, idx).cpu().numpy() for k, v in out.items()}
     _invariants(g, wl.V)
-    o = oracle_draft(**np_inputs(inp, idx), W_rnn=to_np64(Wr))
+    o = oracle_draft(**np_inputs(inp, idx), W_rnn=to_np64(Wr), rnn_row_dtype=wl.dtype)
     compare_draft(g, o, rtol_for(wl.dtype))
     check_no_error(ws)
 
@@ -98,3 +102,37 @@ def test_rnn_head_differs_from_the_markov_head():
                         inp["req_id"], inp["seed"])
     torch.cuda.synchronize()
     assert float((rnn["pd_rows"][:, 0] - mk["pd_rows"][:, 0]).abs().max()) > 1e-3
+
+
+CHILD = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import synth, torch
+from oracle.draft import draft as oracle_draft
+from parity import compare_draft, gpu_np, np_inputs, rtol_for, to_np64
+from gpu_common import check_no_error, workspace_for
+from draft_sampling_lossless_markov_gb300 import torch_api as T
+for B, G, V, r, H in [(130, 5, 8200, 128, 16), (5, 4, 4104, 64, 24)]:
+    wl = synth.Workload("paths", B, G, V, H, r, "bf16", "mixed", synth.SCHED_GREEDY, "tiny", seed=11)
+    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    Wr = synth.rnn_weights(r, H, "bf16", 2, "cuda")
+    ws = workspace_for(B, G, V, r, H, torch.bfloat16)
+    out = T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
+                         inp["req_id"], inp["seed"], W_rnn=Wr)
+    torch.cuda.synchronize()
+    o = oracle_draft(**np_inputs(inp), W_rnn=to_np64(Wr), rnn_row_dtype="bf16")
+    compare_draft(gpu_np(out), o, rtol_for("bf16"))
+    check_no_error(ws)
+print("ok")
+"""
+
+
+def test_rnn_head_on_the_cuda_core_path_for_bf16():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = CHILD.format(root=root, tests=os.path.join(root, "tests"))
+    res = subprocess.run([sys.executable, "-c", code], env={**os.environ, "DSPARK_DRAFT_PATH": "cuda_core"}, cwd=root,
+                         capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0 and res.stdout.strip().endswith("ok"), res.stdout[-2000:] + res.stderr[-4000:]

@@ -125,3 +125,28 @@ def test_half_open_gate_remembers_two_tokens_back():
     firsts = [np.flatnonzero(x1 == a)[0] for a in range(V) if np.any(x1 == a)]
     seen_x1_variation = len({tuple(np.round(p3[i], 12)) for i in firsts}) == len(firsts) > 1
     assert seen_x2_variation and seen_x1_variation
+
+
+def test_row_rounding_matches_the_library_conversions():
+    import torch
+    from oracle.draft import round_to
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.normal(size=20000), rng.uniform(-1, 1, 20000) * 1e-3, [0.0, -0.0, 1.0, -1.0]])
+    np.testing.assert_array_equal(round_to(x, "f32"), x.astype(np.float32).astype(np.float64))
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(round_to(x, "bf16"), ref)
+
+
+def test_rounded_rows_change_only_the_row_precision():
+    # with rounding the rows are the bf16 values of the fp64 rows: the same head with
+    # W_o reading only the embedding equals a Markov head with bf16-rounded tanh rows
+    from oracle.draft import round_to
+    rng = np.random.default_rng(12)
+    A = rng.normal(size=(r, r))
+    Wo = np.zeros((r, 2 * r + H))
+    Wo[:, r:2 * r] = A
+    inp = _inputs(13, 200)
+    rnn = draft(**inp, W_rnn=_blocks(rng, o=Wo), rnn_row_dtype="bf16")
+    markov = draft(**dict(inp, W1=round_to(np.tanh(inp["W1"] @ A.T), "bf16")))
+    assert np.array_equal(rnn["tokens"], markov["tokens"])
+    np.testing.assert_allclose(rnn["pd"], markov["pd"], rtol=0, atol=1e-12)
