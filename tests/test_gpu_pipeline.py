@@ -109,3 +109,75 @@ def test_qwen3_4b_step_sampled_requests():
     # acceptance statistics of the whole batch: the output lengths are plausible
     n_out = v["n_out"].cpu().numpy()
     assert n_out.min() >= 1 and n_out.max() <= wl.gamma + 1
+
+
+def _step_modes(inp, head, sched, verify_mode, Wr, zprev, ws=None):
+    """GPU step in the requested modes, and the oracle's step in the same modes."""
+    from oracle.verify import cap_accept
+    B, G, V = inp["U"].shape
+    if ws is None:
+        from gpu_common import workspace_for
+        ws = workspace_for(B, G, V, inp["W1"].shape[1], inp["h"].shape[2], inp["U"].dtype)
+    d = T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
+                       inp["req_id"], inp["seed"], W_rnn=Wr if head == "rnn" else None)
+    zp = torch.from_numpy(zprev).cuda() if sched == S.MODE_ASYNC_TOPK else None
+    sch = T.schedule(ws, d["conf_logit"], inp["sts"], inp["sps"], inp["anchor"], d["tokens"], sched,
+                     conf_logit_prev=zp)
+    cap_rows = B * (G + 1)
+    if verify_mode == "cap_accept":
+        full = torch.arange(B + 1, device="cuda", dtype=torch.int32) * (G + 1)
+        v = T.verify(ws, inp["target"].reshape(-1, V), full, torch.full((B,), G, dtype=torch.int32, device="cuda"),
+                     d["tokens"], d["pd_rows"], d["pd_tok"], inp["temp"], inp["req_id"], inp["seed"],
+                     commit_cap=sch["ell"])
+    else:
+        rows = torch.empty((cap_rows, V), dtype=inp["target"].dtype, device="cuda")
+        T.pack_rows(inp["target"], sch["mark_req"], sch["mark_pos"], sch["n_verify"], rows, ws)
+        v = T.verify(ws, rows, sch["offsets"], sch["ell"], d["tokens"], d["pd_rows"], d["pd_tok"], inp["temp"],
+                     inp["req_id"], inp["seed"])
+    torch.cuda.synchronize()
+    check_no_error(ws)
+
+    ni = np_inputs(inp)
+    od = oracle_draft(**ni, W_rnn=to_np64(Wr) if head == "rnn" else None,
+                      rnn_row_dtype=("bf16" if inp["U"].dtype == torch.bfloat16 else "f32") if head == "rnn" else None)
+    osch = S.schedule(od["conf_logit"].astype(np.float32), inp["sts"].cpu().numpy(), inp["sps"], ni["anchor"],
+                      od["tokens"], mode=sched, conf_logit_prev=zprev)
+    tgt = to_np64(inp["target"])
+    if verify_mode == "cap_accept":
+        fl = S.flatten(np.full(B, G), ni["anchor"], od["tokens"])
+        ofull = oracle_verify(tgt[fl["mark_req"], fl["mark_pos"]], fl["offsets"], np.full(B, G), od["tokens"],
+                              od["pd"], od["pd_tok"], ni["temp"], ni["seed"], ni["req_id"])
+        ov = dict(cap_accept(ofull, osch["ell"]), accept_margin=ofull["accept_margin"],
+                  sample_margin=ofull["sample_margin"])
+    else:
+        ov = oracle_verify(tgt[osch["mark_req"], osch["mark_pos"]], osch["offsets"], osch["ell"], od["tokens"],
+                           od["pd"], od["pd_tok"], ni["temp"], ni["seed"], ni["req_id"])
+    return (d, sch, v), (od, osch, ov)
+
+
+@pytest.mark.parametrize("head,sched,verify_mode", [
+    ("rnn", S.MODE_GREEDY, "compact"),
+    ("markov", S.MODE_ASYNC_TOPK, "compact"),
+    ("markov", S.MODE_GREEDY, "cap_accept"),
+    ("rnn", S.MODE_ASYNC_TOPK, "cap_accept"),
+])
+def test_tiny_step_in_the_other_modes(head, sched, verify_mode):
+    # the RNN head, the asynchronous scheduler and cap-accept verification, alone and together
+    wl = synth.WORKLOADS["tiny"]
+    full = 0
+    for seed in range(24):
+        inp = synth.make_inputs(wl, "cuda", seed=seed)
+        Wr = synth.rnn_weights(wl.r, wl.H, wl.dtype, seed, "cuda")
+        zprev = synth.random_conf_logits(wl.B, wl.gamma, 500 + seed)
+        (d, sch, v), (od, osch, ov) = _step_modes(inp, head, sched, verify_mode, Wr, zprev)
+        st = compare_draft(gpu_np(d), od, rtol_for(wl.dtype))
+        if st["n_exempt_requests"]:
+            continue
+        if osch["theta_margin"] < 1e-4 or _cut_gap(osch) < 1e-4 or osch.get("cap_margin", np.inf) <= 1e-12:
+            continue
+        g_s = gpu_np(sch)
+        np.testing.assert_array_equal(g_s["ell"], osch["ell"])
+        np.testing.assert_array_equal(g_s["offsets"], osch["offsets"])
+        compare_verify(gpu_np(v), ov, ~(inp["temp"].cpu().numpy() > 0))
+        full += 1
+    assert full >= 8
