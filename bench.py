@@ -302,7 +302,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_sample)
+        res["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_sample, d_out["tokens"].cpu().numpy())
     return res
 
 
@@ -441,7 +441,8 @@ def oracle_sample_time(wl, inp_np, n_req):
     sub = slice(0, n_req)
     t0 = time.perf_counter()
     d = o_draft(inp_np["U"][sub], inp_np["W1"], inp_np["W2"], inp_np["h"][sub], inp_np["w"],
-                inp_np["anchor"][sub], inp_np["temp"][sub], inp_np["seed"], inp_np["req_id"][sub])
+                inp_np["anchor"][sub], inp_np["temp"][sub], inp_np["seed"], inp_np["req_id"][sub],
+                W_rnn=inp_np.get("W_rnn"), rnn_row_dtype=wl.dtype if inp_np.get("W_rnn") is not None else None)
     t1 = time.perf_counter()
     # scheduler over the full batch: the sampled requests' confidences tiled to B
     zl = d["conf_logit"][np.arange(B) % n_req].astype(np.float32)
@@ -455,7 +456,9 @@ def oracle_sample_time(wl, inp_np, n_req):
              inp_np["seed"], inp_np["req_id"][sub])
     t3 = time.perf_counter()
     per_req = (t1 - t0) + (t3 - t2)
-    return per_req / n_req * B + (t2 - t1), dict(draft_s=t1 - t0, schedule_s=t2 - t1, verify_s=t3 - t2)
+    parts = dict(draft_s=t1 - t0, schedule_s=t2 - t1, verify_s=t3 - t2)
+    parts["_draft"] = d
+    return per_req / n_req * B + (t2 - t1), parts
 
 
 def np_inputs_for_oracle(wl, inp, n_req):
@@ -467,17 +470,35 @@ def np_inputs_for_oracle(wl, inp, n_req):
                 req_id=inp["req_id"].cpu().numpy().astype(np.int64), seed=inp["seed"],
                 sts=inp["sts"].cpu().numpy(), sps=inp["sps"], target=f(inp["target"][sub]),
                 sched_mode=inp["sched_mode"],
-                zprev=inp["zprev"].cpu().numpy() if inp.get("zprev") is not None else None)
+                zprev=inp["zprev"].cpu().numpy() if inp.get("zprev") is not None else None,
+                W_rnn=f(inp["W_rnn"]) if inp.get("W_rnn") is not None else None)
 
 
-def cpu_baseline(wl, inp, n_req):
+def cpu_baseline(wl, inp, n_req, gpu_tokens=None):
     n_req = max(1, min(n_req, wl.B))
     inp_np = np_inputs_for_oracle(wl, inp, n_req)
     sec, parts = oracle_sample_time(wl, inp_np, n_req)
-    return {"value": wl.B * wl.gamma / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"fp64 oracle: draft + verify of {n_req} of {wl.B} requests (extrapolated per request), "
-                      f"scheduler on the full batch; one host thread",
-            "parts_s": parts}
+    d = parts.pop("_draft")
+    res = {"value": wl.B * wl.gamma / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"fp64 oracle: draft + verify of {n_req} of {wl.B} requests (extrapolated per request), "
+                     f"scheduler on the full batch; one host thread",
+           "parts_s": parts}
+    if gpu_tokens is not None:
+        # the sampled requests' draft tokens against the oracle's, position by position up
+        # to the first draw inside the margin (later positions depend on that draw)
+        g = np.asarray(gpu_tokens)[:n_req]
+        agree = {}
+        for name, mg in (("margin_1e-5", 1e-5), ("margin_1e-7", 1e-7)):
+            n_cmp = n_ok = 0
+            for r in range(n_req):
+                for k in range(wl.gamma):
+                    if d["margin"][r, k] < mg:
+                        break
+                    n_cmp += 1
+                    n_ok += int(g[r, k] == d["tokens"][r, k])
+            agree[name] = {"compared": n_cmp, "equal": n_ok}
+        res["token_agreement"] = agree
+    return res
 
 
 def run_reference(args):
