@@ -82,3 +82,16 @@ def test_pack_rows_full_size_from_pinned_host():
     torch.cuda.synchronize()
     idx = torch.from_numpy(req[:n].astype(np.int64) * (G + 1) + pos[:n])
     assert torch.equal(dst[:n].cpu(), src.view(-1, V).index_select(0, idx))
+
+
+def test_pack_rows_empty_count_and_empty_launch():
+    B, G, V = 4, 2, 64
+    src = torch.randn((B, G + 1, V), dtype=torch.bfloat16, device="cuda")
+    req, pos, n = _markers(B, G, 2)
+    dst = torch.full((B * (G + 1), V), 3.0, dtype=torch.bfloat16, device="cuda")
+    T.pack_rows(src, to_dev_i32(req), to_dev_i32(pos), to_dev_i32([0]), dst)  # a count of zero
+    torch.cuda.synchronize()
+    assert bool((dst == 3.0).all())
+    empty = torch.empty((0, V), dtype=torch.bfloat16, device="cuda")
+    T.pack_rows(src, to_dev_i32(req), to_dev_i32(pos), to_dev_i32([n]), empty)  # max_rows = 0: no launch
+    torch.cuda.synchronize()

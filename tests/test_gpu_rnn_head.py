@@ -55,6 +55,7 @@ def test_rnn_head_tiny(temp, seed):
 
 
 @pytest.mark.parametrize("B,G,V,r,H,dt", [
+    (1, 1, 7, 1, 0, "f32"),         # one request, one position, rank 1, no hidden state
     (3, 5, 1000, 16, 40, "f32"),    # vocabulary not a multiple of the tile width
     (17, 3, 1031, 7, 5, "f32"),     # rank below one column tile, odd sizes
     (130, 4, 2000, 48, 0, "f32"),   # no hidden state, ragged request and column tiles
