@@ -18,7 +18,7 @@ roofline.  --impl reference times the fp64 CPU oracle on the host cores instead
 
 --workload sts_small | sts_N131072_g7_G128_M15 times dspark_sts_fit instead
 (fitting the STS temperatures on a held-out set): metric = sigmoid evaluations
-per second (every block x candidate x position), roofline against the fp64
+per second (every block x candidate x position), roofline against the fp32
 issue rate, L2 flushed between fits.
 
 Multi-GPU (torchrun, one rank per GPU): the path shards by request with no
@@ -535,12 +535,12 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 STS_METRIC = "STS fit (block, candidate, position) sigmoid evaluations/s"
 STS_UNIT = "evaluations/s"
-# fp64 arithmetic operations of one calibrated confidence c' (the written-out
-# sigmoid: division 3, exponential 19, reciprocal 5, select 1)
-STS_FP64_OPS_PER_EVAL = 28
-# fp64 issue rate: 2 operations per clock per SM, 152 SMs, 2070 MHz (the part's
-# nominal 1.25 TFLOP/s of FP64 counts a fused multiply-add as two)
-FP64_OPS_PEAK = 152 * 2 * 2.07e9
+# fp32 arithmetic operations of one calibrated confidence c' in the fit (the
+# double-float sigmoid as written: 63 for t >= 0, 67 for t < 0; the reciprocal
+# counted as one)
+STS_FP32_OPS_PER_EVAL = 65
+# fp32 issue rate: 128 lanes per SM, 152 SMs, 2070 MHz
+FP32_OPS_PEAK = 152 * 128 * 2.07e9
 
 
 def sts_evals(wl) -> int:
@@ -610,8 +610,8 @@ def run_sts_ours(args, rank, world, local_rank):
 
     evals = sts_evals(wl)
     value = world * evals / (ms * 1e-3)
-    achieved = evals * STS_FP64_OPS_PER_EVAL / (ms * 1e-3) / 1e9
-    peak = FP64_OPS_PEAK / 1e9
+    achieved = evals * STS_FP32_OPS_PER_EVAL / (ms * 1e-3) / 1e9
+    peak = FP32_OPS_PEAK / 1e9
 
     # end to end through the public call: pinned host inputs in, temperatures and ECE table out
     h_z = torch.from_numpy(inp["conf_logit"]).pin_memory()
@@ -645,9 +645,9 @@ def run_sts_ours(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "1gpu"},
         "roofline": {"bound": "alu", "kernel": "dspark_sts_fit (k_sts_hist + k_sts_select per position)",
                      "achieved": achieved, "peak": peak,
-                     "peak_kind": "fp64 issue rate from the nominal table (2 op/clk/SM x 152 SMs x 2070 MHz)",
-                     "unit": "G fp64-op/s", "frac": achieved / peak, "traffic": None,
-                     "algorithmic_ops": evals * STS_FP64_OPS_PER_EVAL},
+                     "peak_kind": "fp32 issue rate from the unit counts (128 lanes x 152 SMs x 2070 MHz)",
+                     "unit": "G fp32-op/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_ops": evals * STS_FP32_OPS_PER_EVAL},
         "gpu_launches": int(launches_per_fit * args.steps),
         "launches_per_step": int(launches_per_fit),
         "clocks": clk,

@@ -22,6 +22,25 @@
 // The prediction sums are kept in 2^-40 fixed point, so the table adds are exact
 // and order-free: the ECE of every candidate is within 2^-41 of the exact value
 // for the fp32 predictions, and the choice is deterministic.
+//
+// c' here comes from a double-float (pairs of fp32) sigmoid on the fp32 pipe,
+// with relative error about 2^-47 |t| + 2^-46 against the exact sigmoid (|t| =
+// |z| / tau <= 64; beyond, and for non-finite input, the fp64 sigmoid the
+// scheduler uses).  Its fp32 rounding is the correctly rounded value except
+// where the exact sigmoid lies within that error of an fp32 rounding midpoint:
+// a changed c' moves one prediction by one ulp (an ECE change below 1e-7 / N),
+// and moves it across a bin edge only if it also sits within an ulp of that
+// edge.  Steps (the exponential by Tang's table method, "Table-driven
+// implementation of the exponential function in IEEE floating-point
+// arithmetic", ACM TOMS 1989):
+//   t = z (1/tau)                 1/tau as a double-float, product exact in hi
+//   |t| = n ln2/64 + r            n = rint(|t| 64/ln2), ln2/64 split in three
+//                                 fp32 parts (the first with 11 bits: n times it
+//                                 is exact), |r| <= ln2/128
+//   e^-|t| = 2^-(n div 64) 2^-(n mod 64)/64 e^-r, the middle factor from a
+//                                 64-entry double-float table, e^-r by its Taylor
+//                                 series to degree 5 (the r^2 term in double-float)
+//   1/(1 + w) by an fp32 reciprocal and one correction with e + e^2.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,6 +55,81 @@
 namespace dspark {
 
 namespace {
+
+// ln2/64 = kC1 + kC2 + kC3 (kC1 has 11 significant bits: n kC1 is exact for n < 2^13)
+constexpr float kC1 = 0x1.62cp-7f;
+constexpr float kC2 = 0x1.217f7ep-18f;
+constexpr float kC3 = -0x1.c610cap-43f;
+constexpr float kInvC = 0x1.715476p+6f;  // 64/ln2, only picks n
+constexpr float kDfMaxArg = 64.f;
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// |a| >= |b|
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+  p = __fmul_rn(a, b);
+  e = fmaf(a, b, -p);
+}
+
+// c' = fp32(sigmoid(z / tau)); (bh, bl) = 1/tau as a double-float, rt = fp64 1/tau,
+// T[j] = 2^(-j/64) as (hi, lo)
+__device__ __forceinline__ float sigmoid_df(float z, float tau, float bh, float bl, double rt,
+                                            const float2* __restrict__ T) {
+  float th, tl;
+  two_prod(z, bh, th, tl);
+  tl = fmaf(z, bl, tl);
+  const bool neg = th < 0.f;
+  const float ah = fabsf(th), al = neg ? -tl : tl;
+  if (!(ah <= kDfMaxArg)) return sts_sigmoid(z, (double)tau, rt);  // large or non-finite
+  const float nf = rintf(ah * kInvC);
+  const int n = (int)nf;
+  // r = |t| - n ln2/64 as a double-float
+  const float r1 = fmaf(-nf, kC1, ah);  // exact
+  float p, pe;
+  two_prod(nf, kC2, p, pe);
+  float rh, rl;
+  two_sum(r1, -p, rh, rl);
+  rl = __fadd_rn(__fsub_rn(rl, pe), __fsub_rn(al, __fmul_rn(nf, kC3)));
+  fast_two_sum(rh, rl, rh, rl);
+  // e^-r = 1 - r + r^2/2 + c3,  c3 = r^3 (-1/6 + r/24 - r^2/120)
+  float sq, sqe;
+  two_prod(rh, rh, sq, sqe);
+  sqe = fmaf(2.f * rh, rl, sqe);
+  const float c3 = __fmul_rn(__fmul_rn(rh, sq), fmaf(rh, fmaf(rh, -1.f / 120.f, 1.f / 24.f), -1.f / 6.f));
+  float Ph, Pl, q2, q2e;
+  fast_two_sum(1.f, -rh, Ph, Pl);
+  fast_two_sum(Ph, 0.5f * sq, q2, q2e);
+  Pl = __fadd_rn(__fadd_rn(Pl, q2e), __fadd_rn(__fsub_rn(0.5f * sqe, rl), c3));
+  Ph = q2;
+  // w = e^-|t| = 2^-(n>>6) T[n & 63] (Ph + Pl)
+  const float2 Tj = T[n & 63];
+  float wh, wl;
+  two_prod(Tj.x, Ph, wh, wl);
+  wl = fmaf(Tj.x, Pl, fmaf(Tj.y, Ph, wl));
+  const float sc = __int_as_float((127 - (n >> 6)) << 23);  // 2^-(n>>6), n>>6 <= 92
+  wh = __fmul_rn(wh, sc);
+  wl = __fmul_rn(wl, sc);
+  // 1 / (1 + w): y0 (1 + e + e^2) with e = 1 - (1 + w) y0
+  float dh, dl;
+  fast_two_sum(1.f, wh, dh, dl);
+  dl = __fadd_rn(dl, wl);
+  const float y0 = __frcp_rn(dh);
+  const float e = __fsub_rn(fmaf(-dh, y0, 1.f), __fmul_rn(dl, y0));
+  const float ye = __fmul_rn(y0, fmaf(e, e, e));
+  if (!neg) return __fadd_rn(y0, ye);
+  // w / (1 + w)
+  float ph, pl;
+  two_prod(wh, y0, ph, pl);
+  pl = fmaf(wh, ye, fmaf(wl, y0, pl));
+  return __fadd_rn(ph, pl);
+}
 
 constexpr int SF_THREADS = 128;
 constexpr int SF_SLAB = 256;     // blocks staged in shared memory at a time
@@ -98,19 +192,27 @@ __global__ void __launch_bounds__(SF_THREADS) k_sts_hist(StsParams a) {
   float* zs = reinterpret_cast<float*>(hist_y + entries);
   float* ps = zs + SF_SLAB;
   unsigned int* ys = reinterpret_cast<unsigned int*>(ps + SF_SLAB);
+  __shared__ float2 T64[64];  // 2^(-j/64) as (hi, lo)
   const int t = threadIdx.x;
   for (int e = t; e < entries; e += SF_THREADS) {
     hist_p[e] = 0;
     hist_y[e] = 0;
   }
+  if (t < 64) {
+    const double v = exp2(-(double)t / 64.0);
+    const float hi = (float)v;
+    T64[t] = make_float2(hi, (float)(v - (double)hi));
+  }
 
   const int k = a.k, G = a.G, N = a.N;
   // the temperature position k-1 received (written by the previous selection)
-  float tau_prev = 1.f;
+  float tau_prev = 1.f, bh_prev = 1.f, bl_prev = 0.f;
   double rtau_prev = 1.0;
   if (k > 0) {
     tau_prev = a.grid[a.gidx[k - 1]];
     rtau_prev = 1.0 / (double)tau_prev;
+    bh_prev = (float)rtau_prev;
+    bl_prev = (float)(rtau_prev - (double)bh_prev);
   }
   const bool active = t < lanes * cols;
   const int lane = active ? t / cols : 0;
@@ -132,7 +234,7 @@ __global__ void __launch_bounds__(SF_THREADS) k_sts_hist(StsParams a) {
       float pp = 1.f;
       if (k > 0) {
         const float before = k >= 2 ? a.P[(size_t)(k - 2) * N + n] : 1.f;
-        pp = __fmul_rn(before, sts_sigmoid(a.z[row + k - 1], (double)tau_prev, rtau_prev));
+        pp = __fmul_rn(before, sigmoid_df(a.z[row + k - 1], tau_prev, bh_prev, bl_prev, rtau_prev, T64));
         a.P[(size_t)(k - 1) * N + n] = pp;
       }
       zs[i] = a.z[row + k];
@@ -143,11 +245,12 @@ __global__ void __launch_bounds__(SF_THREADS) k_sts_hist(StsParams a) {
     if (active) {
       for (int g = col; g < NG; g += cols) {
         const float tau = a.grid[g];
-        const double td = (double)tau, rt = 1.0 / td;
+        const double rt = 1.0 / (double)tau;
+        const float bh = (float)rt, bl = (float)(rt - (double)bh);
         unsigned long long* hp = hist_p + (size_t)lane * M * NG + g;
         unsigned int* hy = hist_y + (size_t)lane * M * NG + g;
         for (int i = lane; i < cnt; i += lanes) {
-          const float c = sts_sigmoid(zs[i], td, rt);
+          const float c = sigmoid_df(zs[i], tau, bh, bl, rt, T64);
           const float p = __fmul_rn(ps[i], c);
           int m;
           unsigned long long fx;
