@@ -40,7 +40,8 @@
 //   e^-|t| = 2^-(n div 64) 2^-(n mod 64)/64 e^-r, the middle factor from a
 //                                 64-entry double-float table, e^-r by its Taylor
 //                                 series to degree 5 (the r^2 term in double-float)
-//   1/(1 + w) by an fp32 reciprocal and one correction with e + e^2.
+//   1/(1 + w) by an approximate fp32 reciprocal y0 and the correction
+//                                 y0 (1 + e + e^2), e = 1 - (1 + w) y0.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -120,7 +121,8 @@ __device__ __forceinline__ float sigmoid_df(float z, float tau, float bh, float 
   float dh, dl;
   fast_two_sum(1.f, wh, dh, dl);
   dl = __fadd_rn(dl, wl);
-  const float y0 = __frcp_rn(dh);
+  float y0;  // |1 - dh y0| <= 2^-22; the correction below absorbs it
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(dh));
   const float e = __fsub_rn(fmaf(-dh, y0, 1.f), __fmul_rn(dl, y0));
   const float ye = __fmul_rn(y0, fmaf(e, e, e));
   if (!neg) return __fadd_rn(y0, ye);
@@ -154,38 +156,26 @@ struct StsParams {
   WsHeader* hdr;
 };
 
-// bin floor(p * M) (p = 1 -> M - 1) and round(p * 2^40), from the bits of a fp32
-// p in [0, 1]; anything at or above 1.0f (also inf / NaN) counts as 1, anything
-// with the sign bit as 0
-__device__ __forceinline__ void bin_and_fixed(float p, int M, int& m, unsigned long long& fx) {
-  const uint32_t b = __float_as_uint(p);
-  if (b & 0x80000000u) {
-    m = 0;
-    fx = 0;
-    return;
-  }
-  if (b >= 0x3f800000u) {
+// bin floor(p * M) (p = 1 -> M - 1) and round(p * 2^40) of an fp32 p in [0, 1];
+// anything not below 1.0f (also inf / NaN) counts as 1.  p M is rounded once;
+// when that rounding reached the next integer, the exact p M - m (one fma)
+// is negative and the bin steps back.  p 2^40 is exact.
+__device__ __forceinline__ void bin_and_fixed(float p, float Mf, int M, int& m, unsigned long long& fx) {
+  if (!(p < 1.f)) {
     m = M - 1;
     fx = 1ull << SF_FX_BITS;
     return;
   }
-  const int e = (int)(b >> 23);                                     // 0..126
-  const uint64_t mant = (b & 0x7fffffu) | (e ? 0x800000u : 0u);    // p = mant 2^(max(e,1) - 150)
-  const int eb = e ? e : 1;
-  const int sh_bin = 150 - eb;                                      // >= 24
-  m = sh_bin >= 64 ? 0 : (int)((mant * (uint64_t)M) >> sh_bin);
-  const int sh = 150 - SF_FX_BITS - eb;                             // p 2^40 = mant 2^-sh
-  if (sh <= 0)
-    fx = mant << (-sh);
-  else if (sh >= 40)
-    fx = 0;  // mant < 2^24 <= 2^(sh - 1): rounds to 0
-  else
-    fx = (mant + (1ull << (sh - 1))) >> sh;
+  int q = (int)__fmul_rn(p, Mf);
+  if (q > 0 && fmaf(p, Mf, -(float)q) < 0.f) --q;
+  m = q;
+  fx = (unsigned long long)__float2ll_rn(__fmul_rn(p, 0x1p40f));
 }
 
 __global__ void __launch_bounds__(SF_THREADS) k_sts_hist(StsParams a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int M = a.n_bins, NG = a.n_grid, lanes = a.lanes, cols = a.cols;
+  const float Mf = (float)M;
   const int entries = lanes * M * NG;
   unsigned long long* hist_p = reinterpret_cast<unsigned long long*>(smem);
   unsigned int* hist_y = reinterpret_cast<unsigned int*>(hist_p + entries);
@@ -249,12 +239,28 @@ __global__ void __launch_bounds__(SF_THREADS) k_sts_hist(StsParams a) {
         const float bh = (float)rt, bl = (float)(rt - (double)bh);
         unsigned long long* hp = hist_p + (size_t)lane * M * NG + g;
         unsigned int* hy = hist_y + (size_t)lane * M * NG + g;
-        for (int i = lane; i < cnt; i += lanes) {
+        // two samples per iteration: their sigmoids are independent; the
+        // histogram updates then go in sample order (they may hit one bin)
+        int i = lane;
+#pragma unroll 1
+        for (; i + lanes < cnt; i += 2 * lanes) {
+          const int i1 = i + lanes;
+          const float c0 = sigmoid_df(zs[i], tau, bh, bl, rt, T64);
+          const float c1 = sigmoid_df(zs[i1], tau, bh, bl, rt, T64);
+          int m0, m1;
+          unsigned long long f0, f1;
+          bin_and_fixed(__fmul_rn(ps[i], c0), Mf, M, m0, f0);
+          bin_and_fixed(__fmul_rn(ps[i1], c1), Mf, M, m1, f1);
+          hp[(size_t)m0 * NG] += f0;
+          hy[(size_t)m0 * NG] += ys[i];
+          hp[(size_t)m1 * NG] += f1;
+          hy[(size_t)m1 * NG] += ys[i1];
+        }
+        if (i < cnt) {
           const float c = sigmoid_df(zs[i], tau, bh, bl, rt, T64);
-          const float p = __fmul_rn(ps[i], c);
           int m;
           unsigned long long fx;
-          bin_and_fixed(p, M, m, fx);
+          bin_and_fixed(__fmul_rn(ps[i], c), Mf, M, m, fx);
           hp[(size_t)m * NG] += fx;
           hy[(size_t)m * NG] += ys[i];
         }
