@@ -491,7 +491,7 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
   count_launches(2 + 3 * G);
   float* P = reinterpret_cast<float*>(ws + L.rnn_p);
   if (rnn) {
-    const cudaError_t e = launch_rnn_hproj(a, P, s);
+    const cudaError_t e = launch_rnn_hproj(a, P, reinterpret_cast<WsHeader*>(ws), s);
     if (e != cudaSuccess) return e;
   }
   const int tw = CC_TW;
@@ -543,7 +543,7 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     const T* w = static_cast<const T*>(a.w);
     k_conf_hidden<T><<<(BG + 7) / 8, 256, 0, s>>>(static_cast<const T*>(a.h), w, zh, BG, d.H);
     count_launches(1);
-    cudaError_t e = launch_rnn_hproj(a, P, s);
+    cudaError_t e = launch_rnn_hproj(a, P, reinterpret_cast<WsHeader*>(ws), s);
     if (e != cudaSuccess) return e;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     const std::function<cudaError_t(int)> hook = [&](int k) {

@@ -1000,6 +1000,158 @@ static bool per_pass_forced() {
 // the tile (bf16, r a multiple of 64 up to 256, V a multiple of 8) on an
 // sm_103 device; otherwise the CUDA-core path.  DSPARK_DRAFT_PATH=cuda_core
 // forces the CUDA-core path (used by the tests to cover both paths).
+// ---------------------------------------------------------------------------
+// RNN head: P [B gamma, 3r] = h [B gamma, H] . W_rnn[:, 2r:]^T on the tensor cores
+// ([DSpark] 方法细节, "RNN头的实现": the h_k part of W z_k does not depend on the
+// recurrence, so every position's share is one bf16 GEMM with fp32
+// accumulation).  128 x 128 tiles, K in 64-element chunks through a ring of
+// four stages (A and B both K-major, 128B-swizzled by TMA), the accumulator in
+// 128 TMEM columns.  Warp 0 loads, warp 1 issues the MMAs, all four warps
+// read TMEM lane quarters and store fp32 rows.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+namespace hp {
+constexpr int TM = 128, TN = 128, TK = 64, NS = 4;
+constexpr uint32_t kTileBytes = TM * TK * 2;  // 16 KB, A and B tiles alike
+constexpr uint32_t kSmem = NS * 2 * kTileBytes + 1024;
+}  // namespace hp
+
+__global__ void __launch_bounds__(128, 1) k_rnn_hproj_tc(const __grid_constant__ CUtensorMap tmA,
+                                                        const __grid_constant__ CUtensorMap tmB, float* P, int M,
+                                                        int N, int K, WsHeader* hdr) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[hp::NS], empty[hp::NS], done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * hp::TM, n0 = blockIdx.x * hp::TN;
+  const int nk = (K + hp::TK - 1) / hp::TK;
+  volatile int* abort_flag = &abort_s;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < hp::NS; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    ptx::mbar_init(&done, 1);
+    ptx::fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&tmem_slot, 128);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  auto fail = [&]() {
+    if (hdr) report_error(hdr, DSPARK_TIMEOUT, (int)blockIdx.x);
+    *abort_flag = 1;
+  };
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol = ptx::policy_evict_last();
+    for (int kc = 0; kc < nk && !*abort_flag; ++kc) {
+      const int st = kc % hp::NS;
+      if (kc >= hp::NS && !ptx::mbar_wait(&empty[st], ((kc / hp::NS) - 1) & 1, abort_flag, tc::kWaitLimitNs)) {
+        fail();
+        break;
+      }
+      uint8_t* a = sm + st * 2 * hp::kTileBytes;
+      ptx::mbar_expect_tx(&full[st], 2 * hp::kTileBytes);
+      ptx::tma_load_2d(a, &tmA, &full[st], kc * hp::TK, m0, pol);
+      ptx::tma_load_2d(a + hp::kTileBytes, &tmB, &full[st], kc * hp::TK, n0, pol);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(hp::TM, hp::TN, false, false);
+    bool ok = true;
+    for (int kc = 0; kc < nk && ok; ++kc) {
+      const int st = kc % hp::NS;
+      if (!ptx::mbar_wait(&full[st], (kc / hp::NS) & 1, abort_flag, tc::kWaitLimitNs)) {
+        fail();
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t a = ptx::smem_u32(sm + st * 2 * hp::kTileBytes);
+#pragma unroll
+      for (int kk = 0; kk < hp::TK / 16; ++kk) {
+        // K-major, 128B swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart;
+        // the 16-element K step is 32 bytes inside the atom
+        const uint64_t ad = ptx::smem_desc_sw128(a + kk * 32, 16, 1024);
+        const uint64_t bd = ptx::smem_desc_sw128(a + hp::kTileBytes + kk * 32, 16, 1024);
+        ptx::tc_mma(tmem, ad, bd, idesc, (kc | kk) ? 1u : 0u);
+      }
+      ptx::tc_commit(&empty[st]);
+    }
+    ptx::tc_commit(&done);
+  }
+  __syncwarp();
+  // epilogue: TMEM lane quarter of this warp, 128 columns in four loads
+  const bool ok = ptx::mbar_wait(&done, 0, abort_flag, tc::kWaitLimitNs);
+  if (__all_sync(0xffffffffu, ok)) {
+    ptx::tc_fence_after();
+    const int row = m0 + warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < hp::TN / 32; ++c) {
+      float v[32];
+      ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), v);
+      ptx::tmem_ld_wait();
+      if (row < M) {
+        float* dst = P + (size_t)row * N + n0 + c * 32;
+        const int nv = min(32, N - (n0 + c * 32));
+        if (nv == 32 && (((uintptr_t)dst) & 15) == 0) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            if (q < nv) dst[q] = v[q];
+        }
+      }
+    }
+  } else if (lane == 0) {
+    fail();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) ptx::tmem_dealloc(tmem, 128);
+}
+
+bool rnn_hproj_tc_supported(const dspark_dims& d) {
+  return d.dtype == DSPARK_BF16 && d.H >= 8 && (d.H % 8) == 0 && (d.r % 8) == 0 && tc::dev_info().sm103 &&
+         tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_rnn_hproj_tc(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  const int M = d.B * d.gamma, N = 3 * d.r, K = d.H;
+  CUtensorMap tmA, tmB;
+  {  // h [M, H] bf16 as (k, m)
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {hp::TK, hp::TM};
+    if (!tc::encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {  // W_rnn[:, 2r:] [3r, H] bf16 (row stride 2r + H) as (k, n)
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(2 * d.r + d.H) * 2};
+    const cuuint32_t box[2] = {hp::TK, hp::TN};
+    const void* base = static_cast<const __nv_bfloat16*>(a.W_rnn) + 2 * d.r;
+    if (!tc::encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(k_rnn_hproj_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hp::kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const dim3 grid((N + hp::TN - 1) / hp::TN, (M + hp::TM - 1) / hp::TM);
+  k_rnn_hproj_tc<<<grid, 128, hp::kSmem, s>>>(tmA, tmB, P, M, N, K, hdr);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 bool draft_tc_supported(const dspark_dims& d) {
   static int forced = -1;
   static std::once_flag once;

@@ -62,7 +62,10 @@ cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayo
 // projection (once per draft call), then the recurrent step of position j
 // (1-based): s_j and the fp32 row e_j from s_{j-1} (ignored for j = 1),
 // x_{j-1} and P.
-cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, cudaStream_t s);
+cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s);
+// the same product on the tensor cores (draft_tc.cu): bf16, H and r multiples of 8
+bool rnn_hproj_tc_supported(const dspark_dims& d);
+cudaError_t launch_rnn_hproj_tc(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s);
 // (E: [B, r] rows in dims.dtype)
 cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
                             void* E, cudaStream_t s);

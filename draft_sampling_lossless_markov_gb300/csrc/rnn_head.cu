@@ -10,8 +10,9 @@
 // nearest-even from fp32; s_j stays fp32.
 //
 // The h_j part of z does not depend on the recurrence, so one GEMM per draft
-// call (k_rnn_hproj) forms P[b, j, :] = W_rnn[:, 2r:] . h_j for every position:
-// [B gamma x H] . [H x 3r], 64 x 64 tiles, 4 x 4 outputs per thread.  Each
+// call forms P[b, j, :] = W_rnn[:, 2r:] . h_j for every position:
+// [B gamma x H] . [H x 3r], on the tensor cores for bf16 (k_rnn_hproj_tc in
+// draft_tc.cu), else here (k_rnn_hproj: 64 x 64 tiles, 4 x 4 outputs per thread).  Each
 // position then takes one launch (k_rnn_step): a tiled fp32 GEMM
 // [B x 2r] . [2r x 3r] over z' = [s_{j-1}; W1[x_{j-1}]], plus P, whose epilogue
 // applies the gates.  A CTA of k_rnn_step holds 16 requests x 32 state columns
@@ -96,6 +97,8 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
                                                          const float* __restrict__ s_prev, float* __restrict__ s_new,
                                                          T* __restrict__ E, int B, int G, int V, int r, int H,
                                                          int j) {
+  constexpr int ZPT = RN_BM * RN_KC / RN_THREADS;      // z entries each thread stages per chunk
+  constexpr int WPT = 3 * RN_BN * RN_KC / RN_THREADS;  // W entries each thread stages per chunk
   __shared__ float zs[RN_BM][RN_KC + 1];
   __shared__ float ws[3][RN_BN][RN_KC + 1];
   __shared__ int xs[RN_BM];
@@ -108,29 +111,48 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
     if (b < B) x = (j == 1) ? anchor[b] : tokens[(size_t)b * G + j - 2];
     xs[tid] = (x >= 0 && x < V) ? x : 0;  // out-of-range anchors are reported by the confidence kernel
   }
-  float ag[2] = {0.f, 0.f}, ac[2] = {0.f, 0.f}, ao[2] = {0.f, 0.f};
-  for (int i0 = 0; i0 < K; i0 += RN_KC) {
-    __syncthreads();  // the previous chunk is consumed (and xs is written)
-    for (int idx = tid; idx < RN_BM * RN_KC; idx += RN_THREADS) {
+  __syncthreads();
+  // the next chunk's entries are loaded into registers while the current one is used
+  float zr[ZPT], wr[WPT];
+  auto fetch = [&](int i0) {
+#pragma unroll
+    for (int u = 0; u < ZPT; ++u) {
+      const int idx = tid + u * RN_THREADS;
       const int m = idx / RN_KC, kk = idx - m * RN_KC;
       const int b = b0 + m, i = i0 + kk;
       float v = 0.f;
-      if (b < B && i < K) {
-        if (i < r)
-          v = (j == 1) ? 0.f : s_prev[(size_t)b * r + i];
-        else
-          v = to_f32(W1[(size_t)xs[m] * r + (i - r)]);
-      }
-      zs[m][kk] = v;
+      if (b < B && i < K) v = (i < r) ? ((j == 1) ? 0.f : s_prev[(size_t)b * r + i])
+                                       : to_f32(W1[(size_t)xs[m] * r + (i - r)]);
+      zr[u] = v;
     }
-    for (int idx = tid; idx < 3 * RN_BN * RN_KC; idx += RN_THREADS) {
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const int idx = tid + u * RN_THREADS;
       const int g = idx / (RN_BN * RN_KC);
       const int rem = idx - g * RN_BN * RN_KC;
       const int c = rem / RN_KC, kk = rem - c * RN_KC;
       const int col = c0 + c, i = i0 + kk;
-      ws[g][c][kk] = (col < r && i < K) ? to_f32(Wr[((size_t)g * r + col) * ldw + i]) : 0.f;
+      wr[u] = (col < r && i < K) ? to_f32(Wr[((size_t)g * r + col) * ldw + i]) : 0.f;
+    }
+  };
+  fetch(0);
+  float ag[2] = {0.f, 0.f}, ac[2] = {0.f, 0.f}, ao[2] = {0.f, 0.f};
+  for (int i0 = 0; i0 < K; i0 += RN_KC) {
+    __syncthreads();  // the previous chunk is consumed
+#pragma unroll
+    for (int u = 0; u < ZPT; ++u) {
+      const int idx = tid + u * RN_THREADS;
+      zs[idx / RN_KC][idx % RN_KC] = zr[u];
+    }
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const int idx = tid + u * RN_THREADS;
+      const int g = idx / (RN_BN * RN_KC);
+      const int rem = idx - g * RN_BN * RN_KC;
+      ws[g][rem / RN_KC][rem % RN_KC] = wr[u];
     }
     __syncthreads();
+    if (i0 + RN_KC < K) fetch(i0 + RN_KC);
 #pragma unroll 8
     for (int kk = 0; kk < RN_KC; ++kk) {
       const float wg = ws[0][tx][kk], wc = ws[1][tx][kk], wo = ws[2][tx][kk];
@@ -175,8 +197,9 @@ static cudaError_t launch_hproj_t(const dspark_draft_args& a, float* P, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, cudaStream_t s) {
+cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s) {
   if (a.dims.H == 0 || a.dims.B == 0) return cudaSuccess;
+  if (rnn_hproj_tc_supported(a.dims)) return launch_rnn_hproj_tc(a, P, hdr, s);
   if (a.dims.dtype == DSPARK_BF16) return launch_hproj_t<__nv_bfloat16>(a, P, s);
   return launch_hproj_t<float>(a, P, s);
 }
