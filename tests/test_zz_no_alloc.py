@@ -48,7 +48,8 @@ def _outputs(B, G):
 
 def _args(c, out):
     a = capi.dspark_sched_args()
-    a.B, a.gamma, a.mode = c["B"], c["G"], capi.DSPARK_SCHED_GREEDY
+    a.B, a.gamma, a.mode = c["B"], c["G"], c.get("mode", capi.DSPARK_SCHED_GREEDY)
+    a.conf_logit_prev = c["prev"].data_ptr() if "prev" in c else None
     a.conf_logit, a.sts_temp, a.sps = c["conf_logit"].data_ptr(), c["sts"].data_ptr(), c["sps"].data_ptr()
     a.anchor, a.tokens = c["anchor"].data_ptr(), c["tokens"].data_ptr()
     for k in ("ell", "offsets", "flat_tok", "mark_req", "mark_pos", "n_verify", "theta_best", "surv"):
@@ -99,3 +100,15 @@ def test_noalloc_schedule_rejects_batches_beyond_the_array():
     a = capi.dspark_sched_args()
     a.B, a.gamma, a.mode = 4097, 16, capi.DSPARK_SCHED_GREEDY  # 65552 candidates > 65536
     assert capi.dspark_schedule_noalloc(a, 0) == capi.DSPARK_UNSUPPORTED
+
+
+def test_noalloc_schedule_in_the_asynchronous_mode():
+    # the production variant through the fixed array: capacity from earlier confidences
+    require_gpu()
+    c = _case(256, 7, 31)
+    c["mode"] = capi.DSPARK_SCHED_ASYNC_TOPK
+    c["prev"] = to_dev_f32(synth.random_conf_logits(256, 7, 32))
+    ref = _with_workspace(c)
+    got = _without_workspace(c)
+    torch.cuda.synchronize()
+    _same(ref, got)
