@@ -132,6 +132,21 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank timing: every rank times its own replica, the slowest one counts
+# ---------------------------------------------------------------------------
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The largest per-rank step time (the job's step time), then a barrier."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t[0])
+
+
+# ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
@@ -258,12 +273,7 @@ def run_ours(args, rank, world, local_rank):
     ms_steps = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
     ms = float(np.mean(ms_steps))
     nv = B * (G + 1) if cap_accept else int(s_out["n_verify"][0])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-        dist.barrier()
+    ms = max_over_ranks(ms, world, dev)
     code, detail = ws.read_error()
     if code != 0:
         raise RuntimeError(f"device error word {capi.dspark_status_string(code)} ({detail})")
@@ -598,12 +608,7 @@ def run_sts_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-        dist.barrier()
+    ms = max_over_ranks(ms, world, dev)
     code, detail = ws.read_error()
     if code != 0:
         raise RuntimeError(f"device error word {capi.dspark_status_string(code)} ({detail})")
