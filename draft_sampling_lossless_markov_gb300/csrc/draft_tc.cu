@@ -1236,22 +1236,39 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
   // than run with CTAs waiting for an SM.
   cudaError_t e = cudaMemsetAsync(p.gbar, 0, sync_bytes, s);
   if (e != cudaSuccess) return e;
-  if (!hook && !tc::per_pass_forced() && di.coop && n_mtiles <= sms) {
-    p.k_begin = 0;
-    p.k_end = d.gamma;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_ctas);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!tc::per_pass_forced() && di.coop && n_mtiles <= sms) {
+    if (!hook) {
+      p.k_begin = 0;
+      p.k_end = d.gamma;
+      p.pass_only = -1;
+      count_launches(1);
+      return cudaLaunchKernelEx(&cfg, tc::k_draft_tc, tmU, tmW2, tmPd, p);
+    }
+    // with a hook: one persistent launch per position (both passes and the
+    // select inside), the hook before it; the grid-barrier counter restarts
+    // at zero for every launch, the pass-2 tile counters are per position
     p.pass_only = -1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.n_ctas);
-    cfg.blockDim = dim3(tc::kThreads);
-    cfg.dynamicSmemBytes = tc::kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    count_launches(1);
-    return cudaLaunchKernelEx(&cfg, tc::k_draft_tc, tmU, tmW2, tmPd, p);
+    for (int k = 0; k < d.gamma; ++k) {
+      e = (*hook)(k);
+      if (e == cudaSuccess && k > 0) e = cudaMemsetAsync(p.gbar, 0, 16, s);
+      if (e != cudaSuccess) return e;
+      p.k_begin = k;
+      p.k_end = k + 1;
+      e = cudaLaunchKernelEx(&cfg, tc::k_draft_tc, tmU, tmW2, tmPd, p);
+      if (e != cudaSuccess) return e;
+    }
+    count_launches(d.gamma);
+    return cudaSuccess;
   }
   count_launches(3 * d.gamma);
   for (int k = 0; k < d.gamma; ++k) {

@@ -128,12 +128,14 @@ print("ok")
 """
 
 
-def test_rnn_head_on_the_cuda_core_path_for_bf16():
+@pytest.mark.parametrize("env", [{"DSPARK_DRAFT_PATH": "cuda_core"}, {"DSPARK_DRAFT_LAUNCH": "per_pass"}])
+def test_rnn_head_on_the_other_launch_paths(env):
+    # bf16 tensor-core shapes on the CUDA-core path, and with one launch per pass
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = CHILD.format(root=root, tests=os.path.join(root, "tests"))
-    res = subprocess.run([sys.executable, "-c", code], env={**os.environ, "DSPARK_DRAFT_PATH": "cuda_core"}, cwd=root,
+    res = subprocess.run([sys.executable, "-c", code], env={**os.environ, **env}, cwd=root,
                          capture_output=True, text=True, timeout=600)
     assert res.returncode == 0 and res.stdout.strip().endswith("ok"), res.stdout[-2000:] + res.stderr[-4000:]
