@@ -10,10 +10,12 @@ Between rounds the key is bumped by the two Weyl constants (mod 2^32).
 
 Uniform contract of this library (the pages specify no RNG):
     key     = (seed mod 2^32, seed >> 32)
-    counter = (req_id, position, draw, 0)
+    counter = (req_id, position, draw, trial)
     u       = (out0 >> 8) * 2^-24   in [0, 1), exact in fp32 and fp64
 Draw ids: 0 draft sample at position k, 1 accept test at k, 2 residual at the
-rejecting k, 3 bonus at l+1; ids >= 16 are free for synthetic data.
+rejecting k, 3 bonus at l+1, 4 the acceptance test of a residual proposal;
+trial numbers the proposals of the rejection-sampled residual (0 otherwise);
+ids >= 16 are free for synthetic data.
 """
 import numpy as np
 
@@ -27,6 +29,7 @@ DRAW_DRAFT = 0
 DRAW_ACCEPT = 1
 DRAW_RESIDUAL = 2
 DRAW_BONUS = 3
+DRAW_RESID_ACCEPT = 4
 
 
 def philox4x32_10(c0, c1, c2, c3, k0, k1):
@@ -54,10 +57,10 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
     return c0, c1, c2, c3
 
 
-def uniform(seed: int, req_id, position, draw):
-    """u in [0,1) for (seed, request id, position, draw id); fp64 array (exact 24-bit values)."""
+def uniform(seed: int, req_id, position, draw, trial=0):
+    """u in [0,1) for (seed, request id, position, draw id, trial); fp64 array (exact 24-bit values)."""
     seed = int(seed)
     k0 = seed & MASK32
     k1 = (seed >> 32) & MASK32
-    out0, _, _, _ = philox4x32_10(req_id, position, draw, 0, k0, k1)
+    out0, _, _, _ = philox4x32_10(req_id, position, draw, trial, k0, k1)
     return (out0 >> np.uint64(8)).astype(np.float64) * (2.0 ** -24)

@@ -24,10 +24,20 @@ Readings where the pages are silent (this library's contract):
   max(0, p_t - p_d) / sum; if that sum is 0 in the implementation's arithmetic
   (reachable only through rounding), sample p_t instead;
 * bonus: draw 3 at position l + 1, inverse CDF of p_t^{l+1}.
+* residual by rejection (residual="rejection", the p_d-row-free mode): the
+  same distribution norm(max(0, p_t - p_d)) sampled by rejection from p_t.
+  Trial t proposes v = InvCDF(p_t, u) with u from draw 2, trial t, and accepts
+  it iff w p_t(v) < p_t(v) - p_d(v) with w from draw 4, trial t, i.e. with
+  probability max(0, 1 - p_d(v)/p_t(v)); the accepted v is a sample of the
+  residual, so only p_d at the proposed tokens is needed.  After max_trials
+  rejected proposals the residual is sampled by inverse CDF with u from draw
+  2, trial max_trials (max_trials = 0 is the inverse-CDF rule above).
 """
 import numpy as np
 
-from .philox import uniform, DRAW_ACCEPT, DRAW_RESIDUAL, DRAW_BONUS
+from .philox import uniform, DRAW_ACCEPT, DRAW_RESIDUAL, DRAW_BONUS, DRAW_RESID_ACCEPT
+
+MAX_TRIALS = 256  # residual proposals before the inverse-CDF fallback
 from .sampling import inverse_cdf, argmax_first
 
 
@@ -37,17 +47,57 @@ def _softmax_rows(z, T):
     return ey / ey.sum(axis=1, keepdims=True)
 
 
-def verify(target_rows, offsets, ell, tokens, pd_rows, pd_tok, temp, seed, req_id):
+def _residual_by_rejection(pt, pdr, seed, req, j, max_trials):
+    """Rejecting requests: (tokens, margins, fell_back) of the residual drawn by
+    rejection from p_t (see the module notes), trial by trial over the requests
+    still pending.  pt, pdr [n, V] fp64; req, j [n] int."""
+    n = pt.shape[0]
+    tok = np.full(n, -1, np.int64)
+    margin = np.full(n, np.inf)
+    pend = np.arange(n)
+    for t in range(max_trials):
+        if pend.size == 0:
+            break
+        u = uniform(seed, req[pend], j[pend], DRAW_RESIDUAL, t)
+        v, mg = inverse_cdf(pt[pend], u)
+        margin[pend] = np.minimum(margin[pend], mg)
+        w = uniform(seed, req[pend], j[pend], DRAW_RESID_ACCEPT, t)
+        lhs, rhs = w * pt[pend, v], pt[pend, v] - pdr[pend, v]
+        margin[pend] = np.minimum(margin[pend], np.abs(lhs - rhs) / np.maximum(pt[pend, v], 1e-300))
+        acc = lhs < rhs
+        tok[pend[acc]] = v[acc]
+        pend = pend[~acc]
+    fell = np.zeros(n, bool)
+    if pend.size:
+        q = np.maximum(0.0, pt[pend] - pdr[pend])
+        Q = q.sum(axis=1)
+        zero = ~(Q > 0)
+        q = np.where(zero[:, None], pt[pend], q / np.where(zero, 1.0, Q)[:, None])
+        u = uniform(seed, req[pend], j[pend], DRAW_RESIDUAL, max_trials)
+        v, mg = inverse_cdf(q, u)
+        tok[pend] = v
+        margin[pend] = np.minimum(margin[pend], mg)
+        fell[pend] = True
+    return tok, margin, fell
+
+
+def verify(target_rows, offsets, ell, tokens, pd_rows, pd_tok, temp, seed, req_id, residual="inverse_cdf",
+           max_trials=MAX_TRIALS):
     """Verify R requests.
 
     target_rows [N, V] (row offsets[r] + j -> p_t^{j+1} of request r),
     offsets [R+1], ell [R], tokens [R, g], pd_tok [R, g], temp [R], req_id [R];
     pd_rows: [R, g, V] array or a callable (r, k0) -> row of p_d^{k0+1}.
 
+    residual: "inverse_cdf" or "rejection" (see the module notes).
+
     Returns dict(n_accept [R], out_tok [R, g+1] (-1 after the emitted tokens),
     n_out [R], accept_margin [R] (smallest accept-test margin met before the
     last decision; inf if none), sample_margin [R] (CDF margin of the final
-    draw; inf for greedy rows), residual_fallback [R] bool)."""
+    draw, or the smallest margin of any proposal and acceptance decision of a
+    rejection-sampled residual; inf for greedy rows), residual_fallback [R]
+    bool (inverse-CDF rule: zero residual mass; rejection: no proposal
+    accepted))."""
     offsets = np.asarray(offsets, dtype=np.int64)
     ell = np.asarray(ell, dtype=np.int64)
     tokens = np.asarray(tokens, dtype=np.int64)
@@ -101,6 +151,14 @@ def verify(target_rows, offsets, ell, tokens, pd_rows, pd_tok, temp, seed, req_i
             continue
         z = np.asarray(target_rows[final_rows[idx]], dtype=np.float64)
         pt = _softmax_rows(z, temp[idx])
+        if is_rej and residual == "rejection":
+            pdr = np.stack([get_pd(int(r), int(m[r])) for r in idx]) if callable(pd_rows) \
+                else np.asarray(pd_rows[idx, m[idx]], dtype=np.float64)
+            x, mg, fb = _residual_by_rejection(pt, pdr, seed, req_id[idx], m[idx] + 1, max_trials)
+            out_tok[idx, m[idx]] = x
+            sample_margin[idx] = mg
+            fallback[idx] = fb
+            continue
         if is_rej:
             pdr = np.stack([get_pd(int(r), int(m[r])) for r in idx]) if callable(pd_rows) \
                 else np.asarray(pd_rows[idx, m[idx]], dtype=np.float64)

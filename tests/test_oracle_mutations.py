@@ -225,3 +225,27 @@ def test_unmutated_rnn_head_passes():
 ])
 def test_rnn_head_mutations_are_caught(old, new):
     assert not _rnn_pins_hold(_mutant("draft", old, new))
+
+
+def _rejection_residual_pvalue(mod):
+    import test_oracle_verify as P
+    counts, n, pt, pd_row = P._residual_counts(mod.verify, 9, 60_000, 4, residual="rejection")
+    q = np.maximum(0.0, pt - pd_row)
+    q /= q.sum()
+    pos = q > 0
+    return stats.chisquare(counts[pos], q[pos] * counts[pos].sum()).pvalue if counts[~pos].sum() == 0 else 0.0
+
+
+def test_unmutated_rejection_residual_passes():
+    import oracle.verify as Vm
+    assert _rejection_residual_pvalue(Vm) > 1e-4
+
+
+@pytest.mark.parametrize("old,new", [
+    ("v, mg = inverse_cdf(pt[pend], u)", "v, mg = inverse_cdf(pdr[pend], u)"),          # proposals from the draft
+    ("acc = lhs < rhs", "acc = lhs > rhs"),                                               # acceptance inverted
+    ("lhs, rhs = w * pt[pend, v], pt[pend, v] - pdr[pend, v]",
+     "lhs, rhs = w * pt[pend, v], pt[pend, v]"),                                          # p_d left out of the test
+])
+def test_rejection_residual_mutations_are_caught(old, new):
+    assert _rejection_residual_pvalue(_mutant("verify", old, new)) < 1e-6

@@ -220,3 +220,58 @@ def test_cap_accept_structure():
     # a window of 0 commits one token: x_1 if it was accepted, else the correction
     z = cap_accept(v, np.zeros(R))
     assert np.all(z["n_out"] == 1) and np.array_equal(z["out_tok"][:, 0], v["out_tok"][:, 0])
+
+
+def _rejecting_requests(V, R, seed):
+    """R one-position requests with the same p_t and p_d rows, draft tokens drawn from p_d."""
+    rng = np.random.default_rng(seed)
+    zt = rng.normal(size=(2, V)) * 0.8
+    pd_row = special.softmax(rng.normal(size=V) * 0.8)  # independent of the target: p_t > p_d at several tokens
+    pt = special.softmax(zt[0])
+    tok = rng.choice(V, size=R, p=pd_row)[:, None]
+    pd = np.broadcast_to(pd_row, (R, 1, V))
+    return zt, pt, pd_row, tok, pd
+
+
+def _residual_counts(verify_fn, V, R, seed, **kw):
+    zt, pt, pd_row, tok, pd = _rejecting_requests(V, R, seed)
+    rows = np.tile(zt, (R, 1))
+    offsets = np.arange(R + 1) * 2
+    v = verify_fn(rows, offsets, np.ones(R, np.int64), tok, pd, pd_row[tok[:, 0]][:, None], np.ones(R), 99,
+                  np.arange(R), **kw)
+    rej = v["n_accept"] == 0
+    return np.bincount(v["out_tok"][rej, 0], minlength=V), rej.sum(), pt, pd_row
+
+
+def test_residual_by_rejection_samples_the_residual():
+    counts, n, pt, pd_row = _residual_counts(verify, 9, 120_000, 4, residual="rejection")
+    q = np.maximum(0.0, pt - pd_row)
+    q /= q.sum()
+    pos = q > 0
+    assert n > 20_000 and pos.sum() >= 3
+    assert stats.chisquare(counts[pos], q[pos] * n).pvalue > 1e-4
+    assert counts[~pos].sum() == 0  # tokens where p_d >= p_t are never the correction
+
+
+def test_rejection_residual_without_trials_is_the_inverse_cdf_rule():
+    zt, pt, pd_row, tok, pd = _rejecting_requests(9, 3000, 4)
+    R = tok.shape[0]
+    args = (np.tile(zt, (R, 1)), np.arange(R + 1) * 2, np.ones(R, np.int64), tok, pd, pd_row[tok[:, 0]][:, None],
+            np.ones(R), 5, np.arange(R))
+    a = verify(*args)
+    b = verify(*args, residual="rejection", max_trials=0)
+    assert np.array_equal(a["out_tok"], b["out_tok"]) and np.array_equal(a["n_accept"], b["n_accept"])
+    assert b["residual_fallback"][a["n_accept"] == 0].all()
+
+
+@pytest.mark.slow
+def test_lossless_with_the_rejection_residual():
+    V, G, R, T = 8, 3, 300_000, 1.0
+    st = _setup(V, G, 3, 8, R)
+    d = draft(np.broadcast_to(st["U"], (R, G, V)), st["W1"], st["W2"], np.broadcast_to(st["h"], (R,) + st["h"].shape),
+              st["w"], np.full(R, st["x0"]), np.full(R, T), SEED, np.arange(R))
+    ell = np.full(R, G)
+    fl = S.flatten(ell, np.full(R, st["x0"]), d["tokens"])
+    v = verify(st["tgt"][fl["mark_pos"]], fl["offsets"], ell, d["tokens"], d["pd"], d["pd_tok"], np.full(R, T), SEED,
+               np.arange(R), residual="rejection")
+    _check_output_marginals(st, v, T, G)
