@@ -23,6 +23,10 @@ DSPARK_BAD_INPUT = 5
 DSPARK_BF16 = 0
 DSPARK_F32 = 1
 
+DSPARK_RESIDUAL_INVERSE_CDF = 0
+DSPARK_RESIDUAL_REJECTION = 1
+DSPARK_RESIDUAL_TRIALS = 256
+
 DSPARK_HEAD_MARKOV = 0
 DSPARK_HEAD_RNN = 1
 
@@ -52,7 +56,8 @@ class dspark_draft_args(ctypes.Structure):
     _fields_ = [("dims", dspark_dims), ("U", c_void_p), ("W1", c_void_p), ("W2", c_void_p), ("h", c_void_p),
                 ("w", c_void_p), ("anchor", c_void_p), ("temp", c_void_p), ("req_id", c_void_p),
                 ("seed", c_uint64), ("tokens", c_void_p), ("pd_rows", c_void_p), ("pd_tok", c_void_p),
-                ("conf_logit", c_void_p), ("conf", c_void_p), ("W_rnn", c_void_p), ("head", c_int32)]
+                ("conf_logit", c_void_p), ("conf", c_void_p), ("W_rnn", c_void_p), ("head", c_int32),
+                ("pd_stat", c_void_p)]
 
 
 class dspark_sched_args(ctypes.Structure):
@@ -67,7 +72,8 @@ class dspark_verify_args(ctypes.Structure):
     _fields_ = [("dims", dspark_dims), ("target_logits", c_void_p), ("offsets", c_void_p), ("ell", c_void_p),
                 ("tokens", c_void_p), ("pd_rows", c_void_p), ("pd_tok", c_void_p), ("temp", c_void_p),
                 ("req_id", c_void_p), ("seed", c_uint64), ("n_accept", c_void_p), ("out_tok", c_void_p),
-                ("n_out", c_void_p), ("commit_cap", c_void_p)]
+                ("n_out", c_void_p), ("commit_cap", c_void_p), ("residual_mode", c_int32), ("U", c_void_p),
+                ("W1", c_void_p), ("W2", c_void_p), ("anchor", c_void_p), ("pd_stat", c_void_p)]
 
 
 class dspark_pack_args(ctypes.Structure):

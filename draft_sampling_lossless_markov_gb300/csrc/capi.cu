@@ -142,9 +142,9 @@ dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, s
   if (!a || !dims_ok(a->dims)) return DSPARK_INVALID_ARG;
   const dspark_dims& d = a->dims;
   if (d.B == 0) return DSPARK_OK;
-  if (!a->U || !a->anchor || !a->temp || !a->req_id || !a->tokens || !a->pd_rows || !a->pd_tok ||
-      !a->conf_logit || !a->conf)
+  if (!a->U || !a->anchor || !a->temp || !a->req_id || !a->tokens || !a->pd_tok || !a->conf_logit || !a->conf)
     return DSPARK_INVALID_ARG;
+  if (!a->pd_rows && (!a->pd_stat || a->head != DSPARK_HEAD_MARKOV)) return DSPARK_INVALID_ARG;
   if (d.r > 0 && (!a->W1 || !a->W2)) return DSPARK_INVALID_ARG;
   if (d.H + d.r > 0 && !a->w) return DSPARK_INVALID_ARG;
   if (d.H > 0 && !a->h) return DSPARK_INVALID_ARG;
@@ -156,7 +156,9 @@ dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, s
   WsLayout L;
   const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);
   if (st != DSPARK_OK) return st;
-  return cuda_status(launch_draft(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream));
+  const cudaError_t e = launch_draft(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported && !a->pd_rows) return DSPARK_UNSUPPORTED;  // no fused path for the row-free mode
+  return cuda_status(e);
 }
 
 dspark_status dspark_schedule(const dspark_sched_args* a, void* workspace, size_t workspace_bytes, void* stream) {
@@ -184,10 +186,16 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* workspace, size_t
   if (!a || !dims_ok(a->dims)) return DSPARK_INVALID_ARG;
   const dspark_dims& d = a->dims;
   if (d.B == 0) return DSPARK_OK;
-  if (!a->target_logits || !a->offsets || !a->ell || !a->tokens || !a->pd_rows || !a->pd_tok || !a->temp ||
-      !a->req_id || !a->n_accept || !a->out_tok || !a->n_out)
+  if (!a->target_logits || !a->offsets || !a->ell || !a->tokens || !a->pd_tok || !a->temp || !a->req_id ||
+      !a->n_accept || !a->out_tok || !a->n_out)
     return DSPARK_INVALID_ARG;
-  if (!aligned16(a->target_logits) || !aligned16(a->pd_rows)) return DSPARK_INVALID_ARG;
+  if (a->residual_mode != DSPARK_RESIDUAL_INVERSE_CDF && a->residual_mode != DSPARK_RESIDUAL_REJECTION)
+    return DSPARK_INVALID_ARG;
+  if (a->residual_mode == DSPARK_RESIDUAL_INVERSE_CDF && !a->pd_rows) return DSPARK_INVALID_ARG;
+  if (a->residual_mode == DSPARK_RESIDUAL_REJECTION &&
+      (d.r < 1 || !a->U || !a->W1 || !a->W2 || !a->anchor || !a->pd_stat))
+    return DSPARK_INVALID_ARG;
+  if (!aligned16(a->target_logits) || (a->pd_rows && !aligned16(a->pd_rows))) return DSPARK_INVALID_ARG;
   WsLayout L;
   const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);
   if (st != DSPARK_OK) return st;

@@ -48,9 +48,10 @@ __device__ __forceinline__ uint32_t philox_u32(uint64_t seed, uint32_t c0, uint3
   return c0;
 }
 
-// u in [0,1) on the 2^-24 grid for (seed, request id, position, draw).
-__device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t req, uint32_t pos, uint32_t draw) {
-  return (float)(philox_u32(seed, req, pos, draw, 0u) >> 8) * 5.9604644775390625e-08f;
+// u in [0,1) on the 2^-24 grid for (seed, request id, position, draw[, trial]).
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t req, uint32_t pos, uint32_t draw,
+                                                uint32_t trial = 0u) {
+  return (float)(philox_u32(seed, req, pos, draw, trial) >> 8) * 5.9604644775390625e-08f;
 }
 
 // ---------------------------------------------------------------------------

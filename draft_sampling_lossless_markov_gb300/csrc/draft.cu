@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
                                                         const uint32_t* __restrict__ req_id, uint64_t seed, int B,
                                                         int G, int V, int r, int H, int k, int32_t* __restrict__ tokens,
                                                         float2* __restrict__ rowstat, float* __restrict__ conf_logit,
-                                                        float* __restrict__ conf) {
+                                                        float* __restrict__ conf, float2* __restrict__ pd_stat) {
   extern __shared__ float Erow[];  // [r] floats, then a [rows x tw] W2 chunk of T
   T* Ws = reinterpret_cast<T*>(Erow + r);
   __shared__ float sm[32];
@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
       for (int w_ = 1; w_ < SEL_THREADS / 32; ++w_) argmax_merge(v, i, sm[w_], sai[w_]);
       tokens[(size_t)b * G + k] = i;
       rowstat[b] = make_float2(0.f, 1.f);
+      if (pd_stat) pd_stat[(size_t)b * G + k] = make_float2(0.f, 1.f);
       s_int[4] = i;
     }
     __syncthreads();
@@ -453,6 +454,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(const float4* __restrict
     if (x < 0) x = min(tstar * tw, V - 1);  // only reachable with non-finite logits
     tokens[(size_t)b * G + k] = x;
     rowstat[b] = make_float2(m, S);
+    if (pd_stat) pd_stat[(size_t)b * G + k] = make_float2(m, S);
     s_int[4] = x;
   }
   __syncthreads();
@@ -520,7 +522,7 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
                                                                 rowstat, a.tokens, a.pd_rows, a.pd_tok);
     k_select<T, TE><<<B, SEL_THREADS, sel_smem, s>>>(part, ntiles, tw, U, Ecur, W2, W1, w, zh, rnn ? nullptr : Enext,
                                                      a.temp, a.req_id, a.seed, B, G, V, r, H, k, a.tokens, rowstat,
-                                                     a.conf_logit, a.conf);
+                                                     a.conf_logit, a.conf, reinterpret_cast<float2*>(a.pd_stat));
     k_logits_cc<T, TE, true><<<grid_cc, CC_TW, es_bytes, s>>>(U, Ecur, W2, a.temp, B, G, V, r, k, ntiles, part,
                                                                rowstat, a.tokens, a.pd_rows, a.pd_tok);
   }
@@ -530,6 +532,8 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
 template <typename T>
 static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const dspark_dims& d = a.dims;
+  // without p_d rows: the fused-sweep kernel only (its select yields p_d(x) and (m, S))
+  if (!a.pd_rows) return draft_tc_supported(d) ? launch_draft_fused(a, ws, L, s) : cudaErrorNotSupported;
   if (a.head == DSPARK_HEAD_RNN) {
     if (!draft_tc_supported(d)) return launch_cuda_core<T, T>(a, ws, L, s);
     // tensor-core passes, one launch per pass; before each position the

@@ -98,6 +98,8 @@ struct Params {
   float2* part;              // [B, pstride] (max, sum) of a sampled row's chunk j, (value, index) of a
                              // greedy row's, at (j % E) 128 + j / E: the select's lanes read it coalesced
   float* pd_tok;
+  int write_pd;              // 0: no p_d rows (no W items; p_d(x) and (m, S) come from the select)
+  float2* pd_stat;           // [B, G] (m, S) of every drawn row, or null
   float* conf_logit;
   float* conf;
   unsigned* gbar;            // grid barrier counter, zero at launch
@@ -282,6 +284,8 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
     if (tw == 0 && lane == 0) {
       for (int w = 1; w < kTeamWarps; ++w) argmax_merge(av, ai, xw[2 * w], __float_as_int(xw[2 * w + 1]));
       p.rowstat[b] = make_float2(0.f, 1.f);
+      if (p.pd_stat) p.pd_stat[(size_t)b * p.G + k] = make_float2(0.f, 1.f);
+      if (!p.write_pd) p.pd_tok[(size_t)b * p.G + k] = 1.f;  // the one-hot row at the argmax
       if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);  // for the E gathers
       st_release_s32(&p.tokens[(size_t)b * p.G + k], ai);
       rec->cstar = -1;
@@ -367,6 +371,7 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p.U + ((size_t)b * p.G + k) * p.V + (size_t)cstar * CW));
     // (m, S) now: the walk's release of the token, after a team barrier, publishes it
     p.rowstat[b] = make_float2(m, S);
+    if (p.pd_stat) p.pd_stat[(size_t)b * p.G + k] = make_float2(m, S);
     rec->cstar = cstar;
     rec->hit = hit ? 1 : 0;
     rec->sbase = cbase;
@@ -455,22 +460,33 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   const float up = __shfl_up_sync(FULL, incl, 1);
   const float ex = lane == 0 ? rec->sbase : up;
   int tok = -1;
+  float wsel = 0.f;  // the chosen token's weight 2^(y - m)
   const unsigned over = __ballot_sync(FULL, rec->hit && incl > rec->target);
   if (over) {
     const int L = __ffs(over) - 1;
-    if (lane == L) tok = (__fadd_rn(ex, w0) > rec->target) ? v : v + 1;
+    if (lane == L) {
+      tok = (__fadd_rn(ex, w0) > rec->target) ? v : v + 1;
+      wsel = tok == v ? w0 : w1;
+    }
     tok = __shfl_sync(FULL, tok, L);
+    wsel = __shfl_sync(FULL, wsel, L);
   } else {
     const unsigned pos = __ballot_sync(FULL, w0 > 0.f || w1 > 0.f);
     if (pos) {
       const int L = 31 - __clz(pos);
-      if (lane == L) tok = (w1 > 0.f) ? v + 1 : v;
+      if (lane == L) {
+        tok = (w1 > 0.f) ? v + 1 : v;
+        wsel = (w1 > 0.f) ? w1 : w0;
+      }
       tok = __shfl_sync(FULL, tok, L);
+      wsel = __shfl_sync(FULL, wsel, L);
     } else {
       tok = rec->cstar * CW;  // no positive weight at all (unreachable for a crossing chunk)
     }
   }
   if (lane == 0) {
+    // without p_d rows, p_d(x_k) comes from this walk (the W item writes it otherwise)
+    if (!p.write_pd) p.pd_tok[(size_t)b * p.G + k] = __fmul_rn(wsel, inv_sum(rec->S));
     prefetch_row(p.W1 + (size_t)tok * p.r, p.r);  // for the E gathers
     st_release_s32(&p.tokens[(size_t)b * p.G + k], tok);
     const_cast<SelRec*>(rec)->tok = tok;
@@ -557,9 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_first = ptx::policy_evict_first();
       int iw = 0, iu = 0, jq = 0;
       bool ok = true;
-      for (int q = 0; q <= G && ok; ++q) {
+      for (int q = 0; q < G + p.write_pd && ok; ++q) {
         const int s = q - 1;
-        const bool hasW = s >= 0, hasS = s + 1 < G;
+        const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
         unsigned* claim = p.sched + (size_t)q * p.n_mtiles + m_tile;
         int n = tile_of(atomicAdd(claim, 1u), q);
         while (ok) {
@@ -615,9 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *e_seen = q + 1;
         return true;
       };
-      for (int q = 0; q <= G && ok; ++q) {
+      for (int q = 0; q < G + p.write_pd && ok; ++q) {
         const int s = q - 1;
-        const bool hasW = s >= 0, hasS = s + 1 < G;
+        const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
         bool e_ok = false;
         while (ok) {
           if (!ptx::mbar_wait(&tqfull[jq % kTQ], (jq / kTQ) & 1, abort_flag, kWaitLimitNs)) {
@@ -800,9 +816,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rb = (int)blockIdx.x + p.n_ctas * ew; rb < p.B; rb += p.n_ctas * kEpiWarps)
       for (int k = lane; k < G; k += 32) p.tokens[(size_t)rb * G + k] = kTokPending;
     if (!*abort_flag) gather(0);
-    for (int q = 0; q <= G && alive; ++q) {
+    for (int q = 0; q < G + p.write_pd && alive; ++q) {
       const int s = q - 1;
-      const bool hasW = s >= 0, hasS = s + 1 < G;
+      const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
       // W(s) row data: (m, 1/S) and the token x_s (chosen by the select)
       float rm = 0.f, rinvS = 1.f;
       int xs = -1;
@@ -1049,7 +1065,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   if (!coop || sms <= 0 || n_mtiles > sms || d.r > 2 * (int)fz::kESlotCols || (d.r % (8 * 8)) != 0)
     return cudaErrorNotSupported;
   const cuuint64_t V = (cuuint64_t)d.V, G = (cuuint64_t)d.gamma, B = (cuuint64_t)d.B, r = (cuuint64_t)d.r;
-  CUtensorMap tmU, tmW2, tmPd;
+  CUtensorMap tmU, tmW2, tmPd = {};  // tmPd stays unused without p_d rows
   {
     const cuuint64_t dims[3] = {V, G, B};
     const cuuint64_t strides[2] = {V * 2, G * V * 2};
@@ -1067,7 +1083,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     const cuuint64_t dims[3] = {V, G, B};
     const cuuint64_t strides[2] = {V * 4, G * V * 4};
     const cuuint32_t box[3] = {32, 1, 32};
-    if (!fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
+    if (a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
   static std::once_flag once;
@@ -1105,6 +1121,8 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.tokens = a.tokens;
   p.part = reinterpret_cast<float2*>(ws + L.part);
   p.pd_tok = a.pd_tok;
+  p.write_pd = a.pd_rows ? 1 : 0;
+  p.pd_stat = reinterpret_cast<float2*>(a.pd_stat);
   p.conf_logit = a.conf_logit;
   p.conf = a.conf;
   p.gbar = reinterpret_cast<unsigned*>(ws + L.gbar);

@@ -119,6 +119,7 @@ struct Params {
   float4* sel;               // [B] crossing chunk, sum before it, target u S, hit
   int32_t* tokens;           // [B, G]
   float4* part;              // [B, nparts] per 64-column chunk
+  float2* pd_stat;           // [B, G] (m, S) of every drawn row, or null
   float4* segpart;           // [B, kDraftMaxSeg] per CTA segment
   float* pd_tok;
   float* conf_logit;
@@ -204,6 +205,7 @@ __device__ __noinline__ void select_row(const Params& p, int b, int k, int lane)
       p.tokens[(size_t)b * p.G + k] = ai;
       if (ai >= 0 && ai < p.V) prefetch_row(p.W1 + (size_t)ai * p.r, p.r);  // E of position k + 1
       p.rowstat[b] = make_float2(0.f, 1.f);
+      if (p.pd_stat) p.pd_stat[(size_t)b * p.G + k] = make_float2(0.f, 1.f);
       p.sel[b] = make_float4(__int_as_float(-1), 0.f, 0.f, __int_as_float(0));
     }
     return;
@@ -286,6 +288,7 @@ __device__ __noinline__ void select_row(const Params& p, int b, int k, int lane)
   }
   if (lane == 0) {
     p.rowstat[b] = make_float2(m, S);
+    if (p.pd_stat) p.pd_stat[(size_t)b * p.G + k] = make_float2(m, S);
     p.sel[b] = make_float4(__int_as_float(cstar), cbase, target, __int_as_float(hit ? 1 : 0));
   }
 }
@@ -1221,6 +1224,7 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
   p.sel = reinterpret_cast<float4*>(ws + L.sel);
   p.tokens = a.tokens;
   p.part = reinterpret_cast<float4*>(ws + L.part);
+  p.pd_stat = reinterpret_cast<float2*>(a.pd_stat);
   p.segpart = reinterpret_cast<float4*>(ws + L.segpart);
   p.pd_tok = a.pd_tok;
   p.conf_logit = a.conf_logit;

@@ -275,17 +275,18 @@ __global__ void __launch_bounds__(FN_THREADS) k_verify_final(const T* __restrict
                                                              const float* __restrict__ pd_rows, int G, int V,
                                                              const int4* __restrict__ fmeta,
                                                              const float4* __restrict__ fstat,
-                                                             float2* __restrict__ fin) {
+                                                             float2* __restrict__ fin, bool row_free) {
   const int r = blockIdx.x, slice = blockIdx.y;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int4 fm = fmeta[r];
   if (!fm.z) return;  // greedy: no draw
   const float4 fs = fstat[r];
-  const bool resid = fm.y != 0;
+  // without p_d rows the residual is drawn by rejection from p_t: p_t's weights only
+  const bool resid = fm.y != 0 && !row_free;
   const int m = fm.w;
   const float M = fs.x, invS = fs.y, c = fs.z;
   const T* z = target + (size_t)fm.x * V;
-  const float* pd = pd_rows + ((size_t)r * G + m) * V;
+  const float* pd = resid ? pd_rows + ((size_t)r * G + m) * V : nullptr;
   const bool vec = (V & 7) == 0;
   const int nch = (V + 255) >> 8, E = (nch + 31) >> 5;
   const int cps = (nch + FN_SLICES - 1) / FN_SLICES;
@@ -329,6 +330,17 @@ __global__ void __launch_bounds__(FN_THREADS) k_verify_final(const T* __restrict
 // u * total, and a re-read of that chunk the token.  Rounding that leaves no
 // crossing falls back to the last positive weight.  A residual of zero mass
 // (reachable only through rounding) draws from p_t instead, with the same u.
+// what the row-free (rejection) residual reads
+struct RowFree {
+  bool on;
+  int r;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const int32_t* anchor;
+  const float* pd_stat;
+};
+
 template <typename T>
 __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restrict__ target,
                                                                const int32_t* __restrict__ ell,
@@ -342,7 +354,7 @@ __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restri
                                                                int32_t* __restrict__ out_tok,
                                                                int32_t* __restrict__ n_out,
                                                                const int32_t* __restrict__ commit_cap,
-                                                               WsHeader* __restrict__ hdr) {
+                                                               WsHeader* __restrict__ hdr, RowFree rf) {
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * PK_WARPS + (threadIdx.x >> 5);
@@ -380,8 +392,7 @@ __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restri
     x = __float_as_int(fs.x);
   } else {
     const bool resid = fm.y != 0;
-    const float u = resid ? philox_uniform(seed, req_id[r], (uint32_t)(m + 1), 2u)
-                          : philox_uniform(seed, req_id[r], (uint32_t)(L + 1), 3u);
+    const bool rejection = resid && rf.on;  // residual by rejection from p_t
     auto entry = [&](int t) { return E <= PK_REG ? f[t] : F[t * 32 + lane]; };
     // lane sums of its chunks (both kinds of weight), and its last chunk with
     // positive weight of each kind
@@ -405,103 +416,168 @@ __global__ void __launch_bounds__(PK_WARPS * 32) k_verify_pick(const T* __restri
       if (e.y > 0.f) lb = c0 + t;
     }
     const float tot_m = warp_sum(sm);
-    // the mode's weights, or p_t for a residual of zero mass
-    const bool use_b = resid && !(tot_m > 0.f);
-    const float sl = use_b ? sb : sm;
-    const float incl = warp_inclusive_scan(sl);
-    const float total = __shfl_sync(FULL, incl, 31);
-    const float tgt = u * total;
-    float ex = __shfl_up_sync(FULL, incl, 1);
-    if (lane == 0) ex = 0.f;
-    const unsigned over = __ballot_sync(FULL, total > 0.f && incl > tgt);
-    // the crossing lane walks its own chunks
-    int cstar = -1, clast = -1;
-    float cpre = 0.f, run = ex;
+    const T* zrow = target + (size_t)fm.x * V;
+    const float M = fs.x, invS = fs.y, c = fs.z;
+    // inverse-CDF draw with u over the chunk sums (use_b: p_t's weights, else the
+    // mode's), then the token by a re-read of the crossing chunk
+    auto draw = [&](float u, bool use_b) -> int {
+      int x = -1;
+      const float sl = use_b ? sb : sm;
+      const float incl = warp_inclusive_scan(sl);
+      const float total = __shfl_sync(FULL, incl, 31);
+      const float tgt = u * total;
+      float ex = __shfl_up_sync(FULL, incl, 1);
+      if (lane == 0) ex = 0.f;
+      const unsigned over = __ballot_sync(FULL, total > 0.f && incl > tgt);
+      // the crossing lane walks its own chunks
+      int cstar = -1, clast = -1;
+      float cpre = 0.f, run = ex;
 #pragma unroll
-    for (int t = 0; t < PK_REG; ++t) {
-      if (t >= E || c0 + t >= nch) break;
-      const float2 e = entry(t);
-      const float w = use_b ? e.y : e.x;
-      const float nr = __fadd_rn(run, w);
-      if (w > 0.f) clast = c0 + t;
-      if (cstar < 0 && nr > tgt) {
-        cstar = c0 + t;
-        cpre = run;
+      for (int t = 0; t < PK_REG; ++t) {
+        if (t >= E || c0 + t >= nch) break;
+        const float2 e = entry(t);
+        const float w = use_b ? e.y : e.x;
+        const float nr = __fadd_rn(run, w);
+        if (w > 0.f) clast = c0 + t;
+        if (cstar < 0 && nr > tgt) {
+          cstar = c0 + t;
+          cpre = run;
+        }
+        run = nr;
       }
-      run = nr;
-    }
-    for (int t = PK_REG; t < E; ++t) {
-      if (c0 + t >= nch) break;
-      const float2 e = F[t * 32 + lane];
-      const float w = use_b ? e.y : e.x;
-      const float nr = __fadd_rn(run, w);
-      if (w > 0.f) clast = c0 + t;
-      if (cstar < 0 && nr > tgt) {
-        cstar = c0 + t;
-        cpre = run;
+      for (int t = PK_REG; t < E; ++t) {
+        if (c0 + t >= nch) break;
+        const float2 e = F[t * 32 + lane];
+        const float w = use_b ? e.y : e.x;
+        const float nr = __fadd_rn(run, w);
+        if (w > 0.f) clast = c0 + t;
+        if (cstar < 0 && nr > tgt) {
+          cstar = c0 + t;
+          cpre = run;
+        }
+        run = nr;
       }
-      run = nr;
-    }
-    bool in_chunk = false;
-    if (over) {
-      const int Lw = __ffs(over) - 1;
-      in_chunk = __shfl_sync(FULL, cstar >= 0 ? 1 : 0, Lw) != 0;
-      const int cs = __shfl_sync(FULL, cstar, Lw), cl = __shfl_sync(FULL, clast, Lw);
-      cpre = __shfl_sync(FULL, cpre, Lw);
-      cstar = in_chunk ? cs : cl;
-    } else {
-      cstar = -1;
-    }
-    if (cstar < 0) {
-      // no crossing: the last chunk with positive weight
-      int lc = use_b ? lb : lm;
-      for (int o = 16; o > 0; o >>= 1) lc = max(lc, __shfl_xor_sync(FULL, lc, o));
-      cstar = lc;
-      in_chunk = false;
-    }
-    x = -1;
-    if (cstar >= 0) {
-      const T* z = target + (size_t)fm.x * V;
-      const float* pd = pd_rows + ((size_t)r * G + m) * V;
-      const float M = fs.x, invS = fs.y, c = fs.z;
-      const bool vec = (V & 7) == 0;
-      const int v0 = cstar * 256 + lane * 8;
-      float q[8];
-      if (resid && !use_b)
-        chunk_weights<T, 0>(z, pd, v0, V, vec, c, M, invS, q);
-      else
-        chunk_weights<T, 1>(z, nullptr, v0, V, vec, c, M, invS, q);
-      const float ls = lane_sum8(q);
-      const float li = warp_inclusive_scan(ls);
-      int lastp = -1;
+      bool in_chunk = false;
+      if (over) {
+        const int Lw = __ffs(over) - 1;
+        in_chunk = __shfl_sync(FULL, cstar >= 0 ? 1 : 0, Lw) != 0;
+        const int cs = __shfl_sync(FULL, cstar, Lw), cl = __shfl_sync(FULL, clast, Lw);
+        cpre = __shfl_sync(FULL, cpre, Lw);
+        cstar = in_chunk ? cs : cl;
+      } else {
+        cstar = -1;
+      }
+      if (cstar < 0) {
+        // no crossing: the last chunk with positive weight
+        int lc = use_b ? lb : lm;
+        for (int o = 16; o > 0; o >>= 1) lc = max(lc, __shfl_xor_sync(FULL, lc, o));
+        cstar = lc;
+        in_chunk = false;
+      }
+      if (cstar >= 0) {
+        const T* z = zrow;
+        const float* pd = (resid && !rf.on) ? pd_rows + ((size_t)r * G + m) * V : nullptr;
+        const bool vec = (V & 7) == 0;
+        const int v0 = cstar * 256 + lane * 8;
+        float q[8];
+        if (resid && !use_b && !rf.on)
+          chunk_weights<T, 0>(z, pd, v0, V, vec, c, M, invS, q);
+        else
+          chunk_weights<T, 1>(z, nullptr, v0, V, vec, c, M, invS, q);
+        const float ls = lane_sum8(q);
+        const float li = warp_inclusive_scan(ls);
+        int lastp = -1;
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (q[e] > 0.f) lastp = v0 + e;
-      if (in_chunk) {
-        const unsigned ov = __ballot_sync(FULL, cpre + li > tgt);
-        if (ov) {
-          const int Ll = __ffs(ov) - 1;
-          float pre = __shfl_up_sync(FULL, li, 1);
-          pre = __shfl_sync(FULL, (lane == 0) ? 0.f : pre, Ll);
-          int xl = -1;
-          if (lane == Ll) {
-            float acc = cpre + pre;
-            for (int e = 0; e < 8; ++e) {
-              acc += q[e];
-              if (acc > tgt) {
-                xl = v0 + e;
-                break;
+        for (int e = 0; e < 8; ++e)
+          if (q[e] > 0.f) lastp = v0 + e;
+        if (in_chunk) {
+          const unsigned ov = __ballot_sync(FULL, cpre + li > tgt);
+          if (ov) {
+            const int Ll = __ffs(ov) - 1;
+            float pre = __shfl_up_sync(FULL, li, 1);
+            pre = __shfl_sync(FULL, (lane == 0) ? 0.f : pre, Ll);
+            int xl = -1;
+            if (lane == Ll) {
+              float acc = cpre + pre;
+              for (int e = 0; e < 8; ++e) {
+                acc += q[e];
+                if (acc > tgt) {
+                  xl = v0 + e;
+                  break;
+                }
               }
+              if (xl < 0) xl = lastp;
             }
-            if (xl < 0) xl = lastp;
+            x = __shfl_sync(FULL, xl, Ll);
           }
-          x = __shfl_sync(FULL, xl, Ll);
+        }
+        if (x < 0) {  // rounding left no crossing: last positive weight of the chunk
+          int lp = lastp;
+          for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
+          x = lp;
         }
       }
-      if (x < 0) {  // rounding left no crossing: last positive weight of the chunk
-        int lp = lastp;
-        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
-        x = lp;
+      return x;
+    };
+    if (!rejection) {
+      const float u = resid ? philox_uniform(seed, req_id[r], (uint32_t)(m + 1), 2u)
+                            : philox_uniform(seed, req_id[r], (uint32_t)(L + 1), 3u);
+      x = draw(u, resid && !(tot_m > 0.f));
+    } else {
+      // proposals v ~ p_t, accepted iff u p_t(v) < p_t(v) - p_d(v); p_d(v) of the
+      // Markov head recomputed at v from U, W1[x_m] and the row's (max, sum)
+      const int xp0 = (m == 0) ? rf.anchor[r] : tokens[(size_t)r * G + m - 1];
+      const int xp = (xp0 >= 0 && xp0 < V) ? xp0 : 0;
+      const float2 st = reinterpret_cast<const float2*>(rf.pd_stat)[(size_t)r * G + m];
+      const float dinv = inv_sum(st.y);
+      const T* W1r = static_cast<const T*>(rf.W1) + (size_t)xp * rf.r;
+      const T* W2 = static_cast<const T*>(rf.W2);
+      const T* Ur = static_cast<const T*>(rf.U) + ((size_t)r * G + m) * V;
+      auto pd_at = [&](int v) -> float {  // warp-wide, the same value in every lane
+        float acc = 0.f;
+        for (int i = lane; i < rf.r; i += 32) acc = fmaf(to_f32(W1r[i]), to_f32(W2[(size_t)i * V + v]), acc);
+        acc = warp_sum(acc);
+        return prob_from(scale_logit(add_base(to_f32(Ur[v]), acc), c), st.x, dinv);
+      };
+      const uint32_t req = req_id[r];
+      x = -1;
+      for (int t = 0; t < DSPARK_RESIDUAL_TRIALS && x < 0; ++t) {
+        const int v = max(draw(philox_uniform(seed, req, (uint32_t)(m + 1), 2u, (uint32_t)t), false), 0);
+        const float pt = prob_from(scale_logit(to_f32(zrow[v]), c), M, invS);
+        const float pdv = pd_at(v);
+        const float w = philox_uniform(seed, req, (uint32_t)(m + 1), 4u, (uint32_t)t);
+        if (__fmul_rn(w, pt) < __fsub_rn(pt, pdv)) x = v;
+      }
+      if (x < 0) {
+        // no proposal accepted: the residual by inverse CDF, recomputing p_d at
+        // every token (two passes over the vocabulary; one lane per token)
+        const float u = philox_uniform(seed, req, (uint32_t)(m + 1), 2u, (uint32_t)DSPARK_RESIDUAL_TRIALS);
+        auto q_at = [&](int v) -> float {
+          if (v >= V) return 0.f;
+          float acc = 0.f;
+          for (int i = 0; i < rf.r; ++i) acc = fmaf(to_f32(W1r[i]), to_f32(W2[(size_t)i * V + v]), acc);
+          const float pdv = prob_from(scale_logit(add_base(to_f32(Ur[v]), acc), c), st.x, dinv);
+          return fmaxf(0.f, __fsub_rn(prob_from(scale_logit(to_f32(zrow[v]), c), M, invS), pdv));
+        };
+        float Q = 0.f;
+        for (int v0 = 0; v0 < V; v0 += 32) Q = __fadd_rn(Q, warp_sum(q_at(v0 + lane)));
+        if (!(Q > 0.f)) {
+          x = draw(u, false);  // zero residual mass: p_t
+        } else {
+          const float tgt = u * Q;
+          float run = 0.f;
+          int lastp = -1;
+          for (int v0 = 0; v0 < V && x < 0; v0 += 32) {
+            const float q = q_at(v0 + lane);
+            const float incl = __fadd_rn(run, warp_inclusive_scan(q));
+            const unsigned ov = __ballot_sync(FULL, incl > tgt);
+            const unsigned pos = __ballot_sync(FULL, q > 0.f);
+            if (pos) lastp = v0 + 31 - __clz(pos);
+            if (ov) x = v0 + __ffs(ov) - 1;
+            run = __shfl_sync(FULL, incl, 31);
+          }
+          if (x < 0) x = lastp;
+        }
       }
     }
   }
@@ -529,9 +605,11 @@ static cudaError_t launch_verify_t(const dspark_verify_args& a, uint8_t* ws, con
   k_verify_rowstats<T><<<B * (G + 1) * RS_PARTS, RS_THREADS, 0, s>>>(tg, a.offsets, rowT, B, V, rs);
   k_verify_accept<T><<<B, AC_WARPS * 32, 0, s>>>(tg, a.offsets, a.ell, a.tokens, a.pd_tok, a.temp, a.req_id,
                                                   a.seed, G, V, rs, vm, fmeta, fstat, hdr);
-  k_verify_final<T><<<dim3(B, FN_SLICES), FN_THREADS, 0, s>>>(tg, a.pd_rows, G, V, fmeta, fstat, fin);
+  const bool row_free = a.residual_mode == DSPARK_RESIDUAL_REJECTION;
+  const RowFree rf{row_free, a.dims.r, a.U, a.W1, a.W2, a.anchor, a.pd_stat};
+  k_verify_final<T><<<dim3(B, FN_SLICES), FN_THREADS, 0, s>>>(tg, a.pd_rows, G, V, fmeta, fstat, fin, row_free);
   k_verify_pick<T><<<nw, PK_WARPS * 32, 0, s>>>(tg, a.ell, a.tokens, a.pd_rows, a.req_id, a.seed, B, G, V, fmeta,
-                                                fstat, fin, a.n_accept, a.out_tok, a.n_out, a.commit_cap, hdr);
+                                                fstat, fin, a.n_accept, a.out_tok, a.n_out, a.commit_cap, hdr, rf);
   count_launches(5);
   return cudaGetLastError();
 }

@@ -83,8 +83,9 @@ class Workspace:
 
 
 def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int, out: Optional[dict] = None,
-                 stream=None, W_rnn=None) -> dict:
-    """dspark_draft_sample; W_rnn [3r, 2r + H] (the dtype of U) selects the RNN head."""
+                 stream=None, W_rnn=None, rows: bool = True, want_pd_stat: bool = False) -> dict:
+    """dspark_draft_sample; W_rnn [3r, 2r + H] (the dtype of U) selects the RNN head;
+    rows=False draws without p_d rows (pd_stat [B, gamma, 2] is then returned)."""
     B, G, V = U.shape
     r = W1.shape[1] if W1 is not None else 0
     H = h.shape[2] if h is not None else 0
@@ -92,17 +93,21 @@ def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int
     dev = U.device
     if out is None:
         out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
-                   pd_rows=torch.empty((B, G, V), dtype=torch.float32, device=dev),
                    pd_tok=torch.empty((B, G), dtype=torch.float32, device=dev),
                    conf_logit=torch.empty((B, G), dtype=torch.float32, device=dev),
                    conf=torch.empty((B, G), dtype=torch.float32, device=dev))
+        if rows:
+            out["pd_rows"] = torch.empty((B, G, V), dtype=torch.float32, device=dev)
+        if want_pd_stat or not rows:
+            out["pd_stat"] = torch.empty((B, G, 2), dtype=torch.float32, device=dev)
     a = capi.dspark_draft_args()
     a.dims = dims(B, G, V, r, H, dt)
     a.U, a.W1, a.W2, a.h, a.w = _ptr(U, dt), _ptr(W1, dt), _ptr(W2, dt), _ptr(h, dt), _ptr(w, dt)
     a.anchor, a.temp = _ptr(anchor, torch.int32), _ptr(temp, torch.float32)
     a.req_id = _ptr(req_id, torch.int32)
     a.seed = int(seed)
-    a.tokens, a.pd_rows = _ptr(out["tokens"], torch.int32), _ptr(out["pd_rows"], torch.float32)
+    a.tokens, a.pd_rows = _ptr(out["tokens"], torch.int32), _ptr(out.get("pd_rows"), torch.float32)
+    a.pd_stat = _ptr(out.get("pd_stat"), torch.float32)
     a.pd_tok, a.conf_logit = _ptr(out["pd_tok"], torch.float32), _ptr(out["conf_logit"], torch.float32)
     a.conf = _ptr(out["conf"], torch.float32)
     if W_rnn is not None:
@@ -147,8 +152,10 @@ def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int
 
 
 def verify(ws: Workspace, target_logits, offsets, ell, tokens, pd_rows, pd_tok, temp, req_id, seed: int,
-           out: Optional[dict] = None, stream=None, commit_cap=None) -> dict:
-    """dspark_verify; commit_cap [B] i32 (the scheduled windows) selects cap-accept."""
+           out: Optional[dict] = None, stream=None, commit_cap=None, rejection: Optional[dict] = None) -> dict:
+    """dspark_verify; commit_cap [B] i32 (the scheduled windows) selects cap-accept;
+    rejection=dict(U, W1, W2, anchor, pd_stat) draws the residual by rejection
+    from p_t (pd_rows may then be None)."""
     B, G = tokens.shape
     V = target_logits.shape[-1]
     dev = tokens.device
@@ -158,11 +165,15 @@ def verify(ws: Workspace, target_logits, offsets, ell, tokens, pd_rows, pd_tok, 
                    out_tok=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
                    n_out=torch.empty(B, dtype=torch.int32, device=dev))
     a = capi.dspark_verify_args()
-    a.dims = dims(B, G, V, 0, 0, dt)
+    a.dims = dims(B, G, V, rejection["W1"].shape[1] if rejection else 0, 0, dt)
     a.target_logits = _ptr(target_logits, dt)
     a.offsets, a.ell, a.tokens = _ptr(offsets, torch.int32), _ptr(ell, torch.int32), _ptr(tokens, torch.int32)
     a.pd_rows, a.pd_tok = _ptr(pd_rows, torch.float32), _ptr(pd_tok, torch.float32)
     a.temp, a.req_id = _ptr(temp, torch.float32), _ptr(req_id, torch.int32)
+    if rejection is not None:
+        a.residual_mode = capi.DSPARK_RESIDUAL_REJECTION
+        a.U, a.W1, a.W2 = _ptr(rejection["U"], dt), _ptr(rejection["W1"], dt), _ptr(rejection["W2"], dt)
+        a.anchor, a.pd_stat = _ptr(rejection["anchor"], torch.int32), _ptr(rejection["pd_stat"], torch.float32)
     a.seed = int(seed)
     a.n_accept, a.out_tok, a.n_out = (_ptr(out["n_accept"], torch.int32), _ptr(out["out_tok"], torch.int32),
                                       _ptr(out["n_out"], torch.int32))

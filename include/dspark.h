@@ -133,6 +133,14 @@ DSPARK_API dspark_status dspark_read_error(void* workspace, int32_t* code_host, 
  * An anchor outside [0, V) is replaced by 0 and reported as DSPARK_BAD_INPUT
  * through the error word.
  *
+ * pd_stat [B, gamma, 2] f32 (optional): each drawn row's max m and sum S of
+ * 2^(y - m) (y = l_k log2(e) / T), so that p_d(v) = 2^(y(v) - m) / S can be
+ * recomputed (dspark_verify's rejection residual).  pd_rows may be NULL (the
+ * p_d-row-free mode): then pd_stat is required, the Markov head only, and
+ * the call needs the fused tensor-core path (bf16, r in {64, 128, 192, 256},
+ * V and H multiples of 8, sm_103), else DSPARK_UNSUPPORTED; p_d(x_k) still
+ * comes back in pd_tok.
+ *
  * head = DSPARK_HEAD_RNN ([DSpark] 方法细节, "RNN头的实现", the optional head)
  * replaces the row W1[x_{k-1}] of the bias product by e_k = tanh(W_o z_k),
  * z_k = [s_{k-1}; W1[x_{k-1}]; h_k] in R^{2r+H}, with the recurrent state
@@ -161,6 +169,7 @@ typedef struct {
   float* conf;
   const void* W_rnn;
   int32_t head;
+  float* pd_stat;
 } dspark_draft_args;
 
 DSPARK_API dspark_status dspark_draft_sample(const dspark_draft_args* args, void* workspace,
@@ -319,7 +328,19 @@ DSPARK_API dspark_status dspark_pack_rows(const dspark_pack_args* args, void* wo
  * accepted (the observation).  Pass ell = gamma rows per request for the
  * full block.  A window outside 0..gamma is clamped and reported in the
  * workspace error word (DSPARK_BAD_INPUT, detail = request).
- * Only dims.B, gamma, V and dtype are read. */
+ * residual_mode = DSPARK_RESIDUAL_REJECTION samples the residual by rejection
+ * from p_t instead (trial t proposes v ~ p_t with draw 2 and Philox counter
+ * word 3 = t, and accepts iff u p_t(v) < p_t(v) - p_d(v) with u from draw 4;
+ * after DSPARK_RESIDUAL_TRIALS rejected proposals the residual is drawn by
+ * inverse CDF with draw 2, trial DSPARK_RESIDUAL_TRIALS).  It reads no p_d
+ * row: p_d(v) is recomputed at the proposed tokens of the Markov head from
+ * U [B, gamma, V], W1 [V, r], W2 [r, V] (dims.dtype, dims.r >= 1), anchor [B]
+ * and pd_stat [B, gamma, 2] (each draft row's max and sum, written by
+ * dspark_draft_sample); pd_rows may then be NULL.
+ * Only dims.B, gamma, V, dtype (and r in the rejection mode) are read. */
+#define DSPARK_RESIDUAL_INVERSE_CDF 0
+#define DSPARK_RESIDUAL_REJECTION 1
+#define DSPARK_RESIDUAL_TRIALS 256
 typedef struct {
   dspark_dims dims;
   const void* target_logits;
@@ -335,6 +356,12 @@ typedef struct {
   int32_t* out_tok;
   int32_t* n_out;
   const int32_t* commit_cap;
+  int32_t residual_mode;
+  const void* U;
+  const void* W1;
+  const void* W2;
+  const int32_t* anchor;
+  const float* pd_stat;
 } dspark_verify_args;
 
 DSPARK_API dspark_status dspark_verify(const dspark_verify_args* args, void* workspace,

@@ -108,10 +108,10 @@ def test_struct_layouts_match_header(lib):
     # field order and sizes of the ctypes mirrors (64-bit ABI)
     assert ctypes.sizeof(capi.dspark_dims) == 24
     assert capi.dspark_draft_args.seed.offset == 24 + 8 * 8
-    assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8 + 8 + 8
+    assert ctypes.sizeof(capi.dspark_draft_args) == 24 + 8 * 8 + 8 + 5 * 8 + 8 + 8 + 8
     assert ctypes.sizeof(capi.dspark_sched_args) == 16 + 15 * 8
     assert capi.dspark_verify_args.seed.offset == 24 + 8 * 8
-    assert ctypes.sizeof(capi.dspark_verify_args) == 24 + 8 * 8 + 8 + 4 * 8
+    assert ctypes.sizeof(capi.dspark_verify_args) == 24 + 8 * 8 + 8 + 4 * 8 + 8 + 5 * 8
 
 
 def test_sts_fit_argument_checks(lib):
@@ -148,3 +148,24 @@ def test_pack_rows_argument_checks(lib):
     b.max_rows = 0
     assert capi.dspark_pack_rows(b, 0, 0) == capi.DSPARK_OK  # nothing to launch
     assert ctypes.sizeof(capi.dspark_pack_args) == 16 + 8 + 5 * 8
+
+
+def test_row_free_argument_checks(lib):
+    # a draft without p_d rows needs pd_stat (and the Markov head)
+    a = capi.dspark_draft_args()
+    a.dims = capi.dspark_dims(4, 3, 1024, 64, 8, capi.DSPARK_BF16)
+    a.U = a.W1 = a.W2 = a.h = a.w = a.anchor = a.temp = a.req_id = a.tokens = a.pd_tok = 256
+    a.conf_logit = a.conf = 256
+    assert capi.dspark_draft_sample(a, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # no rows, no pd_stat
+    a.pd_stat, a.head, a.W_rnn = 256, capi.DSPARK_HEAD_RNN, 256
+    assert capi.dspark_draft_sample(a, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # RNN head without rows
+    # the rejection residual needs the draft's inputs and pd_stat; any other mode is refused
+    v = capi.dspark_verify_args()
+    v.dims = capi.dspark_dims(4, 3, 1024, 64, 0, capi.DSPARK_BF16)
+    v.target_logits = v.offsets = v.ell = v.tokens = v.pd_tok = v.temp = v.req_id = 256
+    v.n_accept = v.out_tok = v.n_out = 256
+    assert capi.dspark_verify(v, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # inverse CDF without rows
+    v.residual_mode = capi.DSPARK_RESIDUAL_REJECTION
+    assert capi.dspark_verify(v, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # no U, W1, W2, anchor, pd_stat
+    v.residual_mode = 7
+    assert capi.dspark_verify(v, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
