@@ -79,20 +79,13 @@ def test_row_free_draft_against_the_oracle():
     assert st["n_tokens_compared"] >= 0.5 * wl.B * wl.gamma
 
 
-def _cut_gap(osch):
-    rr, jj = S.sorted_candidates(osch["a"])
-    n = osch["n_admit"]
-    vals = osch["a"][rr, jj].astype(np.float64)
-    if n == 0 or n >= len(vals):
-        return np.inf
-    return (vals[n - 1] - vals[n]) / vals[n - 1]
-
-
 @pytest.mark.parametrize("temp", ["1.0", "mixed"])
 def test_row_free_step_against_the_oracle(temp):
-    # draft without rows -> schedule -> packed rows -> verify with the rejection residual
-    full = 0
-    for seed in range(8):
+    # draft without rows -> schedule -> packed rows -> verify with the rejection residual;
+    # the oracle verifies the same scheduled lengths, request by request (requests with
+    # a draft draw inside the margin are left out)
+    n_cmp = 0
+    for seed in range(6):
         wl = _workload(40, 4, 2048, 64, 16, temp=temp, seed=20 + seed)
         inp = synth.make_inputs(wl, "cuda")
         B, G, V = wl.B, wl.gamma, wl.V
@@ -108,19 +101,20 @@ def test_row_free_step_against_the_oracle(temp):
         check_no_error(ws)
         ni = np_inputs(inp)
         od = oracle_draft(**ni)
-        if compare_draft(gpu_np(d), od, rtol_for("bf16"), check_pd_rows=False)["n_exempt_requests"]:
-            continue
-        osch = S.schedule(od["conf_logit"].astype(np.float32), inp["sts"].cpu().numpy(), inp["sps"], ni["anchor"],
-                          od["tokens"], mode=wl.sched)
-        if osch["theta_margin"] < 1e-4 or _cut_gap(osch) < 1e-4:
-            continue
-        assert np.array_equal(sch["ell"].cpu().numpy(), osch["ell"])
+        ok = (od["margin"] >= MARGIN).all(axis=1)
+        np.testing.assert_array_equal(d["tokens"].cpu().numpy()[ok], od["tokens"][ok])
+        ell = sch["ell"].cpu().numpy().astype(np.int64)
+        fl = S.flatten(ell, ni["anchor"], od["tokens"])
         tgt = to_np64(inp["target"])
-        ov = oracle_verify(tgt[osch["mark_req"], osch["mark_pos"]], osch["offsets"], osch["ell"], od["tokens"],
-                           od["pd"], od["pd_tok"], ni["temp"], ni["seed"], ni["req_id"], residual="rejection")
-        compare_verify(gpu_np(v), ov, ~(ni["temp"] > 0))
-        full += 1
-    assert full >= 3
+        ov = oracle_verify(tgt[fl["mark_req"], fl["mark_pos"]], fl["offsets"], ell, od["tokens"], od["pd"],
+                           od["pd_tok"], ni["temp"], ni["seed"], ni["req_id"], residual="rejection")
+        g = gpu_np(v)
+        st = compare_verify({k: a[ok] for k, a in g.items()},
+                            {k: a[ok] for k, a in ov.items() if isinstance(a, np.ndarray)}, ~(ni["temp"][ok] > 0))
+        n_cmp += st["n_requests"] - st["n_exempt"]
+        # some of the compared requests rejected a sampled draft token: the residual ran
+        assert np.any((ov["n_accept"] < ell)[ok] & (ni["temp"][ok] > 0)) or temp == "mixed"
+    assert n_cmp >= 100
 
 
 def test_rejection_residual_fallback_after_the_trials():
