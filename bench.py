@@ -53,15 +53,17 @@ UNIT = "request-positions/s"
 # ---------------------------------------------------------------------------
 # byte model (algorithmic bytes of one step; every figure counted once)
 # ---------------------------------------------------------------------------
-def step_bytes(wl: synth.Workload, n_verify_rows: int) -> dict:
+def step_bytes(wl: synth.Workload, n_verify_rows: int, pd_rows: bool = True) -> dict:
+    """Without p_d rows the draft writes none and the final draw re-reads only the
+    target row (p_d is recomputed at a few proposed tokens)."""
     e = 2 if wl.dtype == "bf16" else 4
     B, G, V, r, H = wl.B, wl.gamma, wl.V, wl.r, wl.H
     U = B * G * V * e
     W2_strict = r * V * e
     W2_per_pos = G * r * V * e
-    pd = B * G * V * 4
+    pd = B * G * V * 4 if pd_rows else 0
     target = n_verify_rows * V * e
-    resid = B * V * (e + 4)
+    resid = B * V * (e + 4) if pd_rows else B * V * e
     small = B * G * (r * e + H * e + 24)
     draft_strict = U + W2_strict + pd + B * G * (r * e + H * e + 16)
     return dict(U=U, W2_strict=W2_strict, W2_per_position=W2_per_pos, pd=pd, target=target, resid=resid,
@@ -174,11 +176,19 @@ def run_ours(args, rank, world, local_rank):
     sps_dev = torch.from_numpy(inp["sps"]).to(dev)
     stream = torch.cuda.Stream(device=dev)
     # outputs (allocated once)
+    row_free = args.rows == "none"
     d_out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
-                 pd_rows=torch.empty((B, G, V), dtype=torch.float32, device=dev),
                  pd_tok=torch.empty((B, G), dtype=torch.float32, device=dev),
                  conf_logit=torch.empty((B, G), dtype=torch.float32, device=dev),
                  conf=torch.empty((B, G), dtype=torch.float32, device=dev))
+    if row_free:
+        # no p_d rows: the select's (max, sum) per row; verify draws the residual by
+        # rejection from p_t, recomputing p_d at the proposed tokens
+        d_out["pd_stat"] = torch.empty((B, G, 2), dtype=torch.float32, device=dev)
+    else:
+        d_out["pd_rows"] = torch.empty((B, G, V), dtype=torch.float32, device=dev)
+    rej = (dict(U=inp["U"], W1=inp["W1"], W2=inp["W2"], anchor=inp["anchor"], pd_stat=d_out["pd_stat"])
+           if row_free else None)
     s_out = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
                  offsets=torch.empty(B + 1, dtype=torch.int32, device=dev),
                  flat_tok=torch.empty(cap, dtype=torch.int32, device=dev),
@@ -211,11 +221,12 @@ def run_ours(args, rank, world, local_rank):
 
     def seg2(st):
         if cap_accept:
-            T.verify(ws, tgt_flat, full_offsets, full_ell, d_out["tokens"], d_out["pd_rows"], d_out["pd_tok"],
-                     inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st, commit_cap=s_out["ell"])
+            T.verify(ws, tgt_flat, full_offsets, full_ell, d_out["tokens"], d_out.get("pd_rows"), d_out["pd_tok"],
+                     inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st, commit_cap=s_out["ell"],
+                     rejection=rej)
         else:
-            T.verify(ws, rows, s_out["offsets"], s_out["ell"], d_out["tokens"], d_out["pd_rows"], d_out["pd_tok"],
-                     inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st)
+            T.verify(ws, rows, s_out["offsets"], s_out["ell"], d_out["tokens"], d_out.get("pd_rows"),
+                     d_out["pd_tok"], inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st, rejection=rej)
 
     use_graph = not args.no_graph
     n0 = capi.dspark_launch_count()
@@ -280,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
 
     value = world * B * G / (ms * 1e-3)
     peak, peak_kind = load_peaks()
-    bytes_ = step_bytes(wl, nv)
+    bytes_ = step_bytes(wl, nv, not row_free)
     step_frac = bytes_["step_strict"] / (ms * 1e-3) / 1e9 / peak
     # dominant call: the draft sampler; its strict algorithmic bytes over its measured time
     draft_ms = br["draft_ms"]
@@ -293,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
         "config": {"workload": wl.name, "B": B, "gamma": G, "V": V, "r": wl.r, "H": wl.H, "temp": wl.temp,
                    "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]],
-                   "head": args.head, "verify": args.verify, "n_verify_rows": nv,
+                   "head": args.head, "verify": args.verify, "pd_rows": args.rows, "n_verify_rows": nv,
                    "l2": "inputs larger than L2 (U alone %.0f MB per step), no flush" % (bytes_["U"] / 1e6),
                    "graph": use_graph, "parallelism": "replicas" if world > 1 else "1gpu"},
         "hbm_frac_step": step_frac,
@@ -304,7 +315,8 @@ def run_ours(args, rank, world, local_rank):
                                 "dspark_draft_sample, RNN head (k_rnn_step + CUDA-core k_logits_cc x2 + k_select "
                                 "per position)"),
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
-                     "unit": "GB/s", "frac": draft_gbs / peak, "traffic": traffic if args.head == "markov" else None,
+                     "unit": "GB/s", "frac": draft_gbs / peak,
+                     "traffic": traffic if args.head == "markov" and not row_free else None,
                      "algorithmic_bytes": bytes_["draft_strict"]},
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
@@ -401,7 +413,10 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
             for k in d_small:
                 d_small[k].copy_(h_small[k], non_blocking=True)
             d = T.draft_sample(ws, d_U, inp["W1"], inp["W2"], d_h, inp["w"], d_small["anchor"], d_small["temp"],
-                               d_small["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"))
+                               d_small["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"),
+                               rows=args.rows != "none")
+            rj = (dict(U=d_U, W1=inp["W1"], W2=inp["W2"], anchor=d_small["anchor"], pd_stat=d["pd_stat"])
+                  if args.rows == "none" else None)
             s = sched(T, ws, d["conf_logit"], inp, sps_dev, d_small["anchor"], d["tokens"], stream=stream,
                       n_verify_host=h_nv)
             if cap_accept:
@@ -410,11 +425,12 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
                 # the kept rows in flattened verify order, pulled from the host
                 T.pack_rows(h_tgt, s["mark_req"], s["mark_pos"], s["n_verify"], rows, ws, stream=stream)
             if cap_accept:
-                v = T.verify(ws, tgt_flat, full_offsets, full_ell, d["tokens"], d["pd_rows"], d["pd_tok"],
-                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"])
+                v = T.verify(ws, tgt_flat, full_offsets, full_ell, d["tokens"], d.get("pd_rows"), d["pd_tok"],
+                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"],
+                             rejection=rj)
             else:
-                v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d["pd_rows"], d["pd_tok"],
-                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream)
+                v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d.get("pd_rows"), d["pd_tok"],
+                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, rejection=rj)
             h_out.copy_(v["out_tok"], non_blocking=True)
             h_nout.copy_(v["n_out"], non_blocking=True)
         stream.synchronize()
@@ -720,6 +736,9 @@ def main():
     ap.add_argument("--verify", default="compact", choices=["compact", "cap_accept"],
                     help="verify the scheduled prefixes (compact), or the full blocks committing the scheduled "
                          "windows (cap_accept)")
+    ap.add_argument("--rows", default="full", choices=["full", "none"],
+                    help="write the p_d rows (full), or draft without them and draw the residual by rejection "
+                         "from p_t (none)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=4, help="requests the oracle runs per step")
