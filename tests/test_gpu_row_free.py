@@ -169,3 +169,36 @@ def test_row_free_draft_unsupported_off_the_fused_path():
     with pytest.raises(T.DsparkError) as e:
         _draft(inp, rows=False)
     assert e.value.status == capi.DSPARK_UNSUPPORTED
+
+
+def test_row_free_step_full_size_sampled_requests():
+    # the headline batch in the row-free mode; the oracle recomputes eight requests
+    # (draws are keyed by request id) on the GPU's scheduled lengths
+    wl = synth.get_workload("sweep_B256_g7")
+    inp = synth.make_inputs(wl, "cuda")
+    B, G, V = wl.B, wl.gamma, wl.V
+    d, ws = _draft(inp, rows=False)
+    sch = T.schedule(ws, d["conf_logit"], inp["sts"], inp["sps"], inp["anchor"], d["tokens"], wl.sched)
+    rows = torch.empty((B * (G + 1), V), dtype=torch.bfloat16, device="cuda")
+    T.pack_rows(inp["target"], sch["mark_req"], sch["mark_pos"], sch["n_verify"], rows, ws)
+    v = T.verify(ws, rows, sch["offsets"], sch["ell"], d["tokens"], None, d["pd_tok"], inp["temp"], inp["req_id"],
+                 inp["seed"], rejection=dict(U=inp["U"], W1=inp["W1"], W2=inp["W2"], anchor=inp["anchor"],
+                                             pd_stat=d["pd_stat"]))
+    torch.cuda.synchronize()
+    check_no_error(ws)
+    subset = [0, 1, 2, 3, 100, 101, 200, 255]
+    idx = torch.tensor(subset, device="cuda")
+    ni = np_inputs(inp, idx)
+    od = oracle_draft(**ni)
+    ok = (od["margin"] >= MARGIN).all(axis=1)
+    np.testing.assert_array_equal(d["tokens"][idx].cpu().numpy()[ok], od["tokens"][ok])
+    ell = sch["ell"][idx].cpu().numpy().astype(np.int64)
+    fl = S.flatten(ell, ni["anchor"], od["tokens"])
+    tgt = inp["target"].index_select(0, idx)
+    ov = oracle_verify(to_np64(tgt[torch.from_numpy(fl["mark_req"]).cuda(), torch.from_numpy(fl["mark_pos"]).cuda()]),
+                       fl["offsets"], ell, od["tokens"], od["pd"], od["pd_tok"], ni["temp"], ni["seed"], ni["req_id"],
+                       residual="rejection")
+    g = {k: t.index_select(0, idx).cpu().numpy() for k, t in v.items()}
+    st = compare_verify({k: a[ok] for k, a in g.items()},
+                        {k: a[ok] for k, a in ov.items() if isinstance(a, np.ndarray)}, ~(ni["temp"][ok] > 0))
+    assert st["n_requests"] - st["n_exempt"] >= 4
