@@ -172,7 +172,7 @@ def test_row_free_draft_unsupported_off_the_fused_path():
 
 
 def test_row_free_step_full_size_sampled_requests():
-    # the headline batch in the row-free mode; the oracle recomputes eight requests
+    # the headline batch in the row-free mode; the oracle recomputes 24 requests
     # (draws are keyed by request id) on the GPU's scheduled lengths
     wl = synth.get_workload("sweep_B256_g7")
     inp = synth.make_inputs(wl, "cuda")
@@ -186,7 +186,7 @@ def test_row_free_step_full_size_sampled_requests():
                                              pd_stat=d["pd_stat"]))
     torch.cuda.synchronize()
     check_no_error(ws)
-    subset = [0, 1, 2, 3, 100, 101, 200, 255]
+    subset = list(range(0, 256, 11))  # 24 requests across the batch
     idx = torch.tensor(subset, device="cuda")
     ni = np_inputs(inp, idx)
     od = oracle_draft(**ni)
@@ -201,4 +201,4 @@ def test_row_free_step_full_size_sampled_requests():
     g = {k: t.index_select(0, idx).cpu().numpy() for k, t in v.items()}
     st = compare_verify({k: a[ok] for k, a in g.items()},
                         {k: a[ok] for k, a in ov.items() if isinstance(a, np.ndarray)}, ~(ni["temp"][ok] > 0))
-    assert st["n_requests"] - st["n_exempt"] >= 4
+    assert st["n_requests"] - st["n_exempt"] >= 8
