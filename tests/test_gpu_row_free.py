@@ -41,7 +41,8 @@ def _workload(B, G, V, r, H, temp="mixed", seed=5):
     return synth.Workload("rowfree", B, G, V, H, r, "bf16", temp, synth.SCHED_GREEDY, "exp2048", seed=seed)
 
 
-@pytest.mark.parametrize("B,G,V,r,H", [(40, 3, 1024, 256, 8), (130, 5, 8200, 128, 16), (256, 7, 151936, 256, 4096)])
+@pytest.mark.parametrize("B,G,V,r,H", [(40, 3, 1024, 256, 8), (130, 5, 8200, 128, 16), (256, 7, 151936, 256, 4096),
+                                       (300, 1, 2056, 64, 8), (260, 16, 2048, 192, 32)])
 def test_row_free_draft_matches_the_row_mode(B, G, V, r, H):
     wl = _workload(B, G, V, r, H)
     inp = synth.make_inputs(wl, "cuda", with_target=False)
