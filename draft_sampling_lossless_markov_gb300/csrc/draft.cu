@@ -44,12 +44,30 @@ __global__ void __launch_bounds__(256) k_conf_hidden(const T* __restrict__ h, co
   if (H > 0) {
     const T* hp = h + (size_t)warp * H;
     if ((H & 7) == 0) {
-      for (int i = lane * 8; i < H; i += 256) {
-        float hv[8], wv[8];
-        load8_stream(hp + i, hv);
-        load8(w + i, wv);
+      // NU row loads of 16 (bf16) or 32 (fp32) bytes per lane in flight before
+      // the first fma: one warp per row keeps too few bytes in flight otherwise.
+      // The products are still added in increasing i.
+      constexpr int NU = sizeof(T) == 2 ? 8 : 4;
+      for (int i0 = lane * 8; i0 < H; i0 += 256 * NU) {
+        float hv[NU][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(hv[e], wv[e], acc);
+        for (int u = 0; u < NU; ++u) {
+          if (i0 + 256 * u < H) {
+            load8_stream(hp + i0 + 256 * u, hv[u]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hv[u][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          if (i0 + 256 * u < H) {
+            float wv[8];
+            load8(w + i0 + 256 * u, wv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(hv[u][e], wv[e], acc);
+          }
+        }
       }
     } else {
       for (int i = lane; i < H; i += 32) acc = fmaf(to_f32(hp[i]), to_f32(w[i]), acc);

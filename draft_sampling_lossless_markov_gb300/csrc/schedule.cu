@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a
 // (ties in a stay in (r, j) index order).  Then the same Theta scan, l_r and
 // flatten as k_schedule.
 constexpr int kSmemSortMax = 8192;
+constexpr int kPrefetchTok = 8;  // draft lengths whose tokens k_schedule_smem loads at its start
 constexpr size_t kSmemSchedMax = 200 * 1024;  // dynamic shared memory of k_schedule_smem
 
 __device__ __forceinline__ float key_to_a(uint64_t kv) { return __uint_as_float(~(uint32_t)(kv >> 32)); }
@@ -433,6 +434,18 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
 
   const int tid = threadIdx.x;
   const int R = sched_run_len(G);
+  // the flatten's inputs for this thread's request, loaded now so that their
+  // latency overlaps the sort (the later stores could alias them, so the
+  // compiler would not hoist the loads itself)
+  const int chb = (B + SCH_THREADS - 1) / SCH_THREADS;
+  const int b_lo = min(tid * chb, B), b_hi = min(b_lo + chb, B);
+  const bool pre = chb == 1 && G <= kPrefetchTok && b_lo < b_hi;
+  int pre_anchor = 0, pre_tok[kPrefetchTok];
+  if (pre) {
+    pre_anchor = a.anchor[b_lo];
+#pragma unroll
+    for (int j = 0; j < kPrefetchTok; ++j) pre_tok[j] = j < G ? a.tokens[(size_t)b_lo * G + j] : 0;
+  }
   for (int r = tid; r < B; r += SCH_THREADS) s_ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
   if (a.mode != DSPARK_SCHED_OFF)
     for (int i = tid; i <= B * (1 + G); i += SCH_THREADS) s_sps[i] = a.sps[i];
@@ -540,25 +553,40 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   __syncthreads();
 
   // ---- 5. offsets and the flattened batch ----
-  const int chb = (B + SCH_THREADS - 1) / SCH_THREADS;
-  const int b_lo = min(tid * chb, B), b_hi = min(b_lo + chb, B);
   uint32_t cnt = 0;
   for (int r = b_lo; r < b_hi; ++r) cnt += 1u + (uint32_t)s_ell[r];
   uint32_t nv;
   uint32_t off = block_excl_scan_u32(cnt, sm_u, nv);
-  for (int r = b_lo; r < b_hi; ++r) {
-    const int L = s_ell[r];
+  if (pre) {
+    const int r = b_lo, L = s_ell[r];
     a.ell[r] = L;
     a.offsets[r] = (int)off;
-    a.flat_tok[off] = a.anchor[r];
+    a.flat_tok[off] = pre_anchor;
     a.mark_req[off] = r;
     a.mark_pos[off] = 0;
-    for (int j = 1; j <= L; ++j) {
-      a.flat_tok[off + j] = a.tokens[(size_t)r * G + j - 1];
-      a.mark_req[off + j] = r;
-      a.mark_pos[off + j] = j;
+#pragma unroll
+    for (int j = 1; j <= kPrefetchTok; ++j) {
+      if (j <= L) {
+        a.flat_tok[off + j] = pre_tok[j - 1];
+        a.mark_req[off + j] = r;
+        a.mark_pos[off + j] = j;
+      }
     }
-    off += 1u + (uint32_t)L;
+  } else {
+    for (int r = b_lo; r < b_hi; ++r) {
+      const int L = s_ell[r];
+      a.ell[r] = L;
+      a.offsets[r] = (int)off;
+      a.flat_tok[off] = a.anchor[r];
+      a.mark_req[off] = r;
+      a.mark_pos[off] = 0;
+      for (int j = 1; j <= L; ++j) {
+        a.flat_tok[off + j] = a.tokens[(size_t)r * G + j - 1];
+        a.mark_req[off + j] = r;
+        a.mark_pos[off + j] = j;
+      }
+      off += 1u + (uint32_t)L;
+    }
   }
   const int cap = B * (1 + G);
   for (int i = (int)nv + tid; i < cap; i += SCH_THREADS) {
