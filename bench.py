@@ -297,7 +297,9 @@ def run_ours(args, rank, world, local_rank):
     draft_ms = br["draft_ms"]
     draft_gbs = bytes_["draft_strict"] / (draft_ms * 1e-3) / 1e9
     e2e = run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev) if not args.no_e2e else None
-    traffic = load_traffic(wl)
+    traffic, traffic_why = load_traffic(wl)
+    if args.head != "markov" or row_free:
+        traffic, traffic_why = None, "captured for the Markov head with p_d rows only"
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -316,7 +318,8 @@ def run_ours(args, rank, world, local_rank):
                                 "per position)"),
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
                      "unit": "GB/s", "frac": draft_gbs / peak,
-                     "traffic": traffic if args.head == "markov" and not row_free else None,
+                     "traffic": traffic,
+                     **({"traffic_null_because": traffic_why} if traffic is None else {}),
                      "algorithmic_bytes": bytes_["draft_strict"]},
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
@@ -351,15 +354,20 @@ def per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sp
 
 
 def load_traffic(wl):
-    """Per-launch DRAM bytes of the dominant call from a committed ncu summary, if any."""
+    """Per-launch DRAM bytes of the dominant call from a committed ncu summary:
+    (bytes, None), or (None, why) when there is no capture for this workload or
+    the capture was taken on another version of the kernel's source."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(p):
-        try:
-            d = json.load(open(p))
-            return d.get(wl.name)
-        except (ValueError, OSError):
-            return None
-    return None
+    try:
+        d = json.load(open(p))
+        src = open(os.path.join(ROOT, d["kernel_source"]), "rb").read()
+    except (ValueError, OSError, KeyError):
+        return None, "no ncu traffic record"
+    if hashlib.sha256(src).hexdigest() != d.get("kernel_source_sha256"):
+        return None, "the ncu traffic record was captured on another version of the kernel source"
+    b = d.get("per_launch_bytes", {}).get(wl.name)
+    return (b, None) if b is not None else (None, "no ncu traffic record for this workload")
 
 
 def sched(T, ws, conf_logit, inp, sps_dev, anchor, tokens, **kw):
