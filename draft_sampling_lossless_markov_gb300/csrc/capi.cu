@@ -6,6 +6,9 @@
 #include <string.h>
 
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "dspark.h"
@@ -68,6 +71,20 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.vfin = take(B * 32 * ((((V + 255) / 256) + 31) / 32) * sizeof(float2));
   L.total = align_up(off, 256);
   return L;
+}
+
+cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> set_to;  // (device, kernel) -> limit set
+  std::lock_guard<std::mutex> lock(mu);
+  int& cur = set_to[std::make_pair(dev, func)];
+  if (cur >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }

@@ -1086,13 +1086,9 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     if (a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fz::k_draft_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)fz::kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (const cudaError_t ae = ensure_smem_limit((const void*)fz::k_draft_fused, (int)fz::kSmemBytes);
+      ae != cudaSuccess)
+    return ae;
 
   fz::Params p;
   p.B = d.B;

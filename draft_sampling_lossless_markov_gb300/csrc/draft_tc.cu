@@ -1143,12 +1143,8 @@ cudaError_t launch_rnn_hproj_tc(const dspark_draft_args& a, float* P, WsHeader* 
     const void* base = static_cast<const __nv_bfloat16*>(a.W_rnn) + 2 * d.r;
     if (!tc::encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_rnn_hproj_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hp::kSmem);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (const cudaError_t ae = ensure_smem_limit((const void*)k_rnn_hproj_tc, (int)hp::kSmem); ae != cudaSuccess)
+    return ae;
   const dim3 grid((N + hp::TN - 1) / hp::TN, (M + hp::TM - 1) / hp::TM);
   k_rnn_hproj_tc<<<grid, 128, hp::kSmem, s>>>(tmA, tmB, P, M, N, K, hdr);
   count_launches(1);
@@ -1192,12 +1188,8 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
     if (!tc::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(tc::k_draft_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (const cudaError_t ae = ensure_smem_limit((const void*)tc::k_draft_tc, (int)tc::kSmemBytes); ae != cudaSuccess)
+    return ae;
 
   tc::Params p;
   p.B = d.B;

@@ -49,6 +49,12 @@ WsLayout ws_layout(const dspark_dims& d);
 
 // host-side launch accounting (dspark_launch_count)
 void count_launches(int n);
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute belongs to the kernel's instance in each
+// device's context, so it is recorded per (device, kernel); a process that
+// drives several GPUs gets it set on each.  Thread-safe.
+cudaError_t ensure_smem_limit(const void* func, int bytes);
 size_t elem_size(int dtype);
 
 // Launchers (argument checking happens in capi.cu before these are called).

@@ -621,12 +621,8 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   const size_t smem = schedule_smem_bytes(a.B, a.gamma);
   if (a.mode == DSPARK_SCHED_ASYNC_TOPK && !schedule_async_supported(a.B, a.gamma)) return cudaErrorNotSupported;
   if (n_pad <= kSmemSortMax && smem <= kSmemSchedMax) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(k_schedule_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemSchedMax);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (const cudaError_t ae = ensure_smem_limit((const void*)k_schedule_smem, (int)kSmemSchedMax); ae != cudaSuccess)
+      return ae;
     k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, k0, v0, k1, v1, n_pad);
   } else {
     k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);

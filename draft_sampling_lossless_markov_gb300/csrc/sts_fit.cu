@@ -46,7 +46,6 @@
 #include <stdint.h>
 
 #include <algorithm>
-#include <atomic>
 
 #include "common.cuh"
 #include "dspark.h"
@@ -368,21 +367,12 @@ size_t sts_hist_smem_bytes(int n_grid, int n_bins) {
 }
 
 cudaError_t launch_sts_fit(const dspark_sts_fit_args& a, uint8_t* ws, const StsLayout& L, cudaStream_t s) {
-  static std::atomic<int> s_sms{0};
-  static std::atomic<bool> s_attr{false};
-  cudaError_t e;
-  if (!s_attr.load()) {
-    e = cudaFuncSetAttribute(k_sts_hist, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sts_hist_smem_bytes(SF_THREADS, DSPARK_STS_MAX_TABLE / SF_THREADS));
-    if (e != cudaSuccess) return e;
-    s_attr.store(true);
-  }
-  if (s_sms.load() == 0) {
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    s_sms.store(sms);
-  }
+  cudaError_t e = ensure_smem_limit((const void*)k_sts_hist,
+                                    (int)sts_hist_smem_bytes(SF_THREADS, DSPARK_STS_MAX_TABLE / SF_THREADS));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;  // of the current device
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   StsParams p{};
   p.N = a.N;
   p.G = a.gamma;
@@ -410,7 +400,7 @@ cudaError_t launch_sts_fit(const dspark_sts_fit_args& a, uint8_t* ws, const StsL
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // every CTA resident at once, each with an equal share of the blocks (at
   // least 32 of them, so small sets do not spread over idle CTAs)
-  int ctas = s_sms.load() * per_sm;
+  int ctas = sms * per_sm;
   ctas = (int)std::min<long long>(ctas, std::max<long long>(1, ((long long)a.N + 31) / 32));
   p.chunk = (a.N + ctas - 1) / ctas;
   int launches = 0;
