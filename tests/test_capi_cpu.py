@@ -169,3 +169,42 @@ def test_row_free_argument_checks(lib):
     assert capi.dspark_verify(v, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # no U, W1, W2, anchor, pd_stat
     v.residual_mode = 7
     assert capi.dspark_verify(v, 256, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
+
+
+def _no_visible_gpu():
+    # these calls pass made-up device addresses: they must be refused by the
+    # argument checks, so they are never made where a GPU could run a kernel
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("argument-check test with made-up device addresses: CPU only")
+
+
+def test_misaligned_pointers_are_refused(lib):
+    _no_visible_gpu()
+    fields = ("U", "W1", "W2", "h", "w", "anchor", "temp", "req_id", "tokens", "pd_rows", "pd_tok", "conf_logit",
+              "conf")
+    for bad in ("W1", "W2", "h", "w", "pd_rows"):
+        a = capi.dspark_draft_args()
+        a.dims = capi.dspark_dims(4, 3, 1024, 64, 8, capi.DSPARK_BF16)
+        for f in fields:
+            setattr(a, f, 0x10000)
+        # control: with every address aligned the call passes the checks and
+        # fails only at the CUDA layer (no device here)
+        assert capi.dspark_draft_sample(a, 0x20000, 1 << 30, 0) == capi.DSPARK_CUDA_ERROR
+        setattr(a, bad, 0x10008)
+        assert capi.dspark_draft_sample(a, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG, bad
+    a.pd_rows = 0x10000
+    a.head, a.W_rnn = capi.DSPARK_HEAD_RNN, 0x10002
+    assert capi.dspark_draft_sample(a, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # W_rnn
+    a.head = 9
+    assert capi.dspark_draft_sample(a, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # unknown head
+
+    for bad in ("target_logits", "pd_rows"):
+        v = capi.dspark_verify_args()
+        v.dims = capi.dspark_dims(4, 3, 1024, 64, 0, capi.DSPARK_BF16)
+        for f in ("target_logits", "offsets", "ell", "tokens", "pd_rows", "pd_tok", "temp", "req_id", "n_accept",
+                  "out_tok", "n_out"):
+            setattr(v, f, 0x10000)
+        assert capi.dspark_verify(v, 0x20000, 1 << 30, 0) == capi.DSPARK_CUDA_ERROR  # control, as above
+        setattr(v, bad, 0x10004)
+        assert capi.dspark_verify(v, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG, bad
