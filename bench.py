@@ -44,7 +44,8 @@ import numpy as np  # noqa: E402
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-import synth  # noqa: E402
+# synth (and with it torch) is imported inside the functions that use it: the
+# oracle's worker processes start by re-importing this file and need numpy only
 
 METRIC = "spec-decode request-positions/s (draft+schedule+verify) at V=151936; % HBM peak"
 UNIT = "request-positions/s"
@@ -65,10 +66,12 @@ def step_bytes(wl: synth.Workload, n_verify_rows: int, pd_rows: bool = True) -> 
     target = n_verify_rows * V * e
     resid = B * V * (e + 4) if pd_rows else B * V * e
     small = B * G * (r * e + H * e + 24)
-    draft_strict = U + W2_strict + pd + B * G * (r * e + H * e + 16)
+    draft_small = B * G * (r * e + H * e + 16)
+    draft_strict = U + W2_strict + pd + draft_small
     return dict(U=U, W2_strict=W2_strict, W2_per_position=W2_per_pos, pd=pd, target=target, resid=resid,
                 small=small, step_strict=U + W2_strict + pd + target + resid + small,
-                step_per_position=U + W2_per_pos + pd + target + resid + small, draft_strict=draft_strict)
+                step_per_position=U + W2_per_pos + pd + target + resid + small, draft_strict=draft_strict,
+                draft_per_position=U + W2_per_pos + pd + draft_small)
 
 
 def load_peaks():
@@ -152,6 +155,7 @@ def max_over_ranks(ms: float, world: int, device) -> float:
 # the GPU arm
 # ---------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
+    import synth
     import torch
     from draft_sampling_lossless_markov_gb300 import build, capi
     from draft_sampling_lossless_markov_gb300 import torch_api as T
@@ -202,9 +206,11 @@ def run_ours(args, rank, world, local_rank):
     rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
     tgt_flat = inp["target"].reshape(-1, V)
 
-    def seg1(st):
+    def draft_call(st):
         T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
                        inp["req_id"], inp["seed"], out=d_out, stream=st, W_rnn=inp.get("W_rnn"))
+
+    def sched_call(st):
         sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=st)
 
     def standin(st):
@@ -219,7 +225,7 @@ def run_ours(args, rank, world, local_rank):
         full_offsets = (torch.arange(B + 1, device=dev, dtype=torch.int32) * (G + 1)).contiguous()
         full_ell = torch.full((B,), G, dtype=torch.int32, device=dev)
 
-    def seg2(st):
+    def verify_call(st):
         if cap_accept:
             T.verify(ws, tgt_flat, full_offsets, full_ell, d_out["tokens"], d_out.get("pd_rows"), d_out["pd_tok"],
                      inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st, commit_cap=s_out["ell"],
@@ -228,45 +234,49 @@ def run_ours(args, rank, world, local_rank):
             T.verify(ws, rows, s_out["offsets"], s_out["ell"], d_out["tokens"], d_out.get("pd_rows"),
                      d_out["pd_tok"], inp["temp"], inp["req_id"], inp["seed"], out=v_out, stream=st, rejection=rej)
 
+    calls = (draft_call, sched_call, verify_call)
     use_graph = not args.no_graph
     n0 = capi.dspark_launch_count()
     with torch.cuda.stream(stream):
-        seg1(stream)
+        draft_call(stream)
+        sched_call(stream)
         standin(stream)
-        seg2(stream)
+        verify_call(stream)
     stream.synchronize()
     launches_per_step = capi.dspark_launch_count() - n0
     if use_graph:
-        g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g1, stream=stream):
-            seg1(torch.cuda.current_stream())
-        with torch.cuda.graph(g2, stream=stream):
-            seg2(torch.cuda.current_stream())
-        run1 = lambda: g1.replay()  # noqa: E731
-        run2 = lambda: g2.replay()  # noqa: E731
+        # one graph per call, so that CUDA events between the replays time each
+        # call live inside the timed region
+        runs = []
+        for fn in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(torch.cuda.current_stream())
+            runs.append(g.replay)
     else:
-        run1 = lambda: seg1(stream)  # noqa: E731
-        run2 = lambda: seg2(stream)  # noqa: E731
+        runs = [lambda fn=fn: fn(stream) for fn in calls]
 
     def one_step(ev=None):
+        # events: 0 | draft | 1 | schedule | 2 | (stand-in, not timed) | 3 | verify | 4
         with torch.cuda.stream(stream):
             if ev:
                 ev[0].record(stream)
-            run1()
+            runs[0]()
             if ev:
                 ev[1].record(stream)
-            standin(stream)
+            runs[1]()
             if ev:
                 ev[2].record(stream)
-            run2()
+            standin(stream)
             if ev:
                 ev[3].record(stream)
+            runs[2]()
+            if ev:
+                ev[4].record(stream)
 
     for _ in range(args.warmup):
         one_step()
     stream.synchronize()
-    # per-call breakdown (outside the timed loop): draft, schedule, verify separately
-    br = per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sps_dev)
 
     if world > 1:
         import torch.distributed as dist
@@ -275,14 +285,17 @@ def run_ours(args, rank, world, local_rank):
     cvd = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    nv_sum = 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     for k in range(args.steps):
         one_step(evs[k])
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    ms_steps = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
-    ms = float(np.mean(ms_steps))
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[3].elapsed_time(e[4])] for e in evs])
+    ms_steps = per.sum(axis=1)
+    ms = float(np.median(ms_steps))
+    br = {"draft_ms": float(np.median(per[:, 0])), "schedule_ms": float(np.median(per[:, 1])),
+          "verify_ms": float(np.median(per[:, 2])),
+          "timer": "CUDA events around each call's graph replay inside the timed region; median over the steps"}
     nv = B * (G + 1) if cap_accept else int(s_out["n_verify"][0])
     ms = max_over_ranks(ms, world, dev)
     code, detail = ws.read_error()
@@ -292,10 +305,11 @@ def run_ours(args, rank, world, local_rank):
     value = world * B * G / (ms * 1e-3)
     peak, peak_kind = load_peaks()
     bytes_ = step_bytes(wl, nv, not row_free)
-    step_frac = bytes_["step_strict"] / (ms * 1e-3) / 1e9 / peak
-    # dominant call: the draft sampler; its strict algorithmic bytes over its measured time
+    # dominant call: the draft sampler, one launch of fz::k_draft_fused; its
+    # algorithmic bytes with W2 read once per position (the method's sequential
+    # structure), and the strict count (W2 once per call) beside them
     draft_ms = br["draft_ms"]
-    draft_gbs = bytes_["draft_strict"] / (draft_ms * 1e-3) / 1e9
+    draft_gbs = bytes_["draft_per_position"] / (draft_ms * 1e-3) / 1e9
     e2e = run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev) if not args.no_e2e else None
     traffic, traffic_why = load_traffic(wl)
     if args.head != "markov" or row_free:
@@ -304,23 +318,23 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
-        "config": {"workload": wl.name, "B": B, "gamma": G, "V": V, "r": wl.r, "H": wl.H, "temp": wl.temp,
-                   "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]],
-                   "head": args.head, "verify": args.verify, "pd_rows": args.rows, "n_verify_rows": nv,
-                   "l2": "inputs larger than L2 (U alone %.0f MB per step), no flush" % (bytes_["U"] / 1e6),
-                   "graph": use_graph, "parallelism": "replicas" if world > 1 else "1gpu"},
-        "hbm_frac_step": step_frac,
-        "hbm_frac_step_w2_per_position": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
+        "config": workload_config(wl, args, inp["sched_mode"], world),
+        "run": {"n_verify_rows": nv, "graph": use_graph, "ms_per_step_mean": float(np.mean(ms_steps)),
+                "ms_per_step_min": float(np.min(ms_steps)), "ms_per_step_max": float(np.max(ms_steps))},
+        "hbm_frac_step": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
+        "hbm_frac_step_strict": bytes_["step_strict"] / (ms * 1e-3) / 1e9 / peak,
+        "step_bytes": {"per_position": bytes_["step_per_position"], "strict": bytes_["step_strict"]},
         "breakdown_ms": br,
         "roofline": {"bound": "hbm",
                      "kernel": ("dspark_draft_sample (fz::k_draft_fused, one launch)" if args.head == "markov" else
-                                "dspark_draft_sample, RNN head (k_rnn_step + CUDA-core k_logits_cc x2 + k_select "
-                                "per position)"),
+                                "dspark_draft_sample, RNN head (k_rnn_step + tensor-core passes per position)"),
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
                      "unit": "GB/s", "frac": draft_gbs / peak,
                      "traffic": traffic,
                      **({"traffic_null_because": traffic_why} if traffic is None else {}),
-                     "algorithmic_bytes": bytes_["draft_strict"]},
+                     "algorithmic_bytes": bytes_["draft_per_position"],
+                     "algorithmic_bytes_strict": bytes_["draft_strict"],
+                     "frac_strict": bytes_["draft_strict"] / (draft_ms * 1e-3) / 1e9 / peak},
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
         "clocks": clk,
@@ -329,28 +343,6 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_sample, d_out["tokens"].cpu().numpy())
     return res
-
-
-def per_call_times(T, seg1, seg2, standin, ws, inp, d_out, s_out, wl, stream, sps_dev, reps=3):
-    import torch
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    acc = np.zeros(3)
-    for _ in range(reps):
-        with torch.cuda.stream(stream):
-            ev[0].record(stream)
-            T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
-                           inp["req_id"], inp["seed"], out=d_out, stream=stream, W_rnn=inp.get("W_rnn"))
-            ev[1].record(stream)
-            sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=stream)
-            ev[2].record(stream)
-            standin(stream)
-            ev[3].record(stream)
-            seg2(stream)
-            ev[4].record(stream)
-        stream.synchronize()
-        acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[3].elapsed_time(ev[4])]
-    acc /= reps
-    return {"draft_ms": float(acc[0]), "schedule_ms": float(acc[1]), "verify_ms": float(acc[2])}
 
 
 def load_traffic(wl):
@@ -463,79 +455,193 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle (baseline leg and --impl reference)
+# CPU oracle (the baseline leg and --impl reference): one worker process per
+# host core, each holding a disjoint subset of the sampled requests
 # ---------------------------------------------------------------------------
-def oracle_sample_time(wl, inp_np, n_req):
-    """fp64 oracle on the first n_req requests (draft + verify per request) plus the
-    scheduler on the full batch; returns seconds per step extrapolated to B."""
+def host_cores() -> int:
+    """Cores this process may run on (its affinity mask), else the machine's count."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(conn, shm_names, shapes, data):
+    """One worker of the oracle pool: drafts and verifies its own requests, on
+    command, with NumPy's BLAS pinned to one thread (set in the environment
+    before this process started)."""
+    from multiprocessing import shared_memory
     from oracle.draft import draft as o_draft
     from oracle import schedule as S
     from oracle.verify import verify as o_verify
-    B, G = wl.B, wl.gamma
-    sub = slice(0, n_req)
-    t0 = time.perf_counter()
-    d = o_draft(inp_np["U"][sub], inp_np["W1"], inp_np["W2"], inp_np["h"][sub], inp_np["w"],
-                inp_np["anchor"][sub], inp_np["temp"][sub], inp_np["seed"], inp_np["req_id"][sub],
-                W_rnn=inp_np.get("W_rnn"), rnn_row_dtype=wl.dtype if inp_np.get("W_rnn") is not None else None)
-    t1 = time.perf_counter()
-    # scheduler over the full batch: the sampled requests' confidences tiled to B
-    zl = d["conf_logit"][np.arange(B) % n_req].astype(np.float32)
-    toks = d["tokens"][np.arange(B) % n_req]
-    sch = S.schedule(zl, inp_np["sts"], inp_np["sps"], inp_np["anchor"][np.arange(B) % n_req], toks,
-                     mode=inp_np["sched_mode"], conf_logit_prev=inp_np["zprev"])
-    t2 = time.perf_counter()
-    sub_sch = S.flatten(sch["ell"][sub], inp_np["anchor"][sub], d["tokens"])
-    rows = inp_np["target"][sub][sub_sch["mark_req"], sub_sch["mark_pos"]]
-    o_verify(rows, sub_sch["offsets"], sch["ell"][sub], d["tokens"], d["pd"], d["pd_tok"], inp_np["temp"][sub],
-             inp_np["seed"], inp_np["req_id"][sub])
-    t3 = time.perf_counter()
-    per_req = (t1 - t0) + (t3 - t2)
-    parts = dict(draft_s=t1 - t0, schedule_s=t2 - t1, verify_s=t3 - t2)
-    parts["_draft"] = d
-    return per_req / n_req * B + (t2 - t1), parts
+    shms = [shared_memory.SharedMemory(name=n) for n in shm_names]
+    W1, W2 = (np.ndarray(s, dtype=np.float64, buffer=m.buf) for s, m in zip(shapes, shms))
+    d = None
+    try:
+        while True:
+            msg = conn.recv()
+            if msg[0] == "draft":
+                t0 = time.perf_counter()
+                d = o_draft(data["U"], W1, W2, data["h"], data["w"], data["anchor"], data["temp"], data["seed"],
+                            data["req_id"], W_rnn=data.get("W_rnn"), rnn_row_dtype=data.get("rnn_row_dtype"))
+                conn.send((d["conf_logit"], d["tokens"], d["margin"], time.perf_counter() - t0))
+            elif msg[0] == "verify":
+                t0 = time.perf_counter()
+                ell = msg[1]
+                fl = S.flatten(ell, data["anchor"], d["tokens"])
+                rows = data["target"][fl["mark_req"], fl["mark_pos"]]
+                o_verify(rows, fl["offsets"], ell, d["tokens"], d["pd"], d["pd_tok"], data["temp"], data["seed"],
+                         data["req_id"])
+                conn.send(time.perf_counter() - t0)
+            else:
+                break
+    finally:
+        del W1, W2
+        for m in shms:
+            m.close()
+        conn.close()
 
 
-def np_inputs_for_oracle(wl, inp, n_req):
-    import torch
-    f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
-    sub = slice(0, n_req)
-    return dict(U=f(inp["U"][sub]), W1=f(inp["W1"]), W2=f(inp["W2"]), h=f(inp["h"][sub]), w=f(inp["w"]),
-                anchor=inp["anchor"].cpu().numpy().astype(np.int64), temp=inp["temp"].cpu().numpy().astype(np.float64),
-                req_id=inp["req_id"].cpu().numpy().astype(np.int64), seed=inp["seed"],
-                sts=inp["sts"].cpu().numpy(), sps=inp["sps"], target=f(inp["target"][sub]),
-                sched_mode=inp["sched_mode"],
-                zprev=inp["zprev"].cpu().numpy() if inp.get("zprev") is not None else None,
-                W_rnn=f(inp["W_rnn"]) if inp.get("W_rnn") is not None else None)
+class OraclePool:
+    """The fp64 oracle over the first n_req requests of a workload, split into
+    disjoint contiguous subsets, one per worker process (one process per host
+    core, at most one per request).  A step drafts every subset in parallel,
+    runs the scheduler on the whole batch in this process (the sampled
+    requests' confidences tiled over the batch), then verifies every subset in
+    parallel with the scheduler's lengths.  W1 and W2 are shared with the
+    workers through shared memory; the per-request rows travel once, at start.
+    Workers are started with spawn, so that a pool made after the GPU is in use
+    does not fork a CUDA context."""
+
+    def __init__(self, wl, inp, n_req, cores=None):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        import torch
+        self.wl, self.n_req = wl, max(1, min(n_req, wl.B))
+        self.cores = max(1, min(cores or host_cores(), self.n_req))
+        f = lambda x: x.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+        sub = slice(0, self.n_req)
+        self.anchor_all = inp["anchor"].cpu().numpy().astype(np.int64)
+        self.sts = inp["sts"].cpu().numpy()
+        self.sps = inp["sps"]
+        self.sched_mode = inp["sched_mode"]
+        self.zprev = inp["zprev"].cpu().numpy() if inp.get("zprev") is not None else None
+        self.shms, shapes = [], []
+        for name in ("W1", "W2"):
+            a = f(inp[name])
+            m = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            np.ndarray(a.shape, dtype=np.float64, buffer=m.buf)[...] = a
+            self.shms.append(m)
+            shapes.append(a.shape)
+            del a
+        U, h, tgt = f(inp["U"][sub]), f(inp["h"][sub]), f(inp["target"][sub])
+        temp = inp["temp"].cpu().numpy().astype(np.float64)
+        req = inp["req_id"].cpu().numpy().astype(np.int64)
+        w = f(inp["w"])
+        W_rnn = f(inp["W_rnn"]) if inp.get("W_rnn") is not None else None
+        self.bounds = np.linspace(0, self.n_req, self.cores + 1).round().astype(int)
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for c in range(self.cores):
+            lo, hi = int(self.bounds[c]), int(self.bounds[c + 1])
+            data = dict(U=U[lo:hi], h=h[lo:hi], target=tgt[lo:hi], w=w, anchor=self.anchor_all[lo:hi],
+                        temp=temp[lo:hi], req_id=req[lo:hi], seed=inp["seed"], W_rnn=W_rnn,
+                        rnn_row_dtype=wl.dtype if W_rnn is not None else None)
+            pc, cc = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(cc, [m.name for m in self.shms], shapes, data), daemon=True)
+            pr.start()
+            cc.close()
+            self.conns.append(pc)
+            self.procs.append(pr)
+        self.tokens = None
+
+    def step(self) -> dict:
+        """One oracle step over the sample; wall seconds and the parts' times."""
+        from oracle import schedule as S
+        B, G, n = self.wl.B, self.wl.gamma, self.n_req
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send(("draft",))
+        res = [c.recv() for c in self.conns]
+        t1 = time.perf_counter()
+        zl = np.concatenate([r[0] for r in res])
+        self.tokens = np.concatenate([r[1] for r in res])
+        self.margin = np.concatenate([r[2] for r in res])
+        tile = np.arange(B) % n
+        sch = S.schedule(zl[tile].astype(np.float32), self.sts, self.sps, self.anchor_all[tile], self.tokens[tile],
+                         mode=self.sched_mode, conf_logit_prev=self.zprev)
+        t2 = time.perf_counter()
+        for c, lo, hi in zip(self.conns, self.bounds[:-1], self.bounds[1:]):
+            c.send(("verify", sch["ell"][lo:hi]))
+        vt = [c.recv() for c in self.conns]
+        t3 = time.perf_counter()
+        return dict(step_s=t3 - t0, draft_s=t1 - t0, schedule_s=t2 - t1, verify_s=t3 - t2,
+                    worker_draft_s=float(max(r[3] for r in res)), worker_verify_s=float(max(vt)))
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(("stop",))
+            except (BrokenPipeError, OSError):
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.terminate()
+        for m in self.shms:
+            m.close()
+            m.unlink()
+
+    def describe(self) -> str:
+        return (f"fp64 oracle: draft + verify of requests 0..{self.n_req - 1} of {self.wl.B} (all "
+                f"{self.wl.gamma} positions each), split over {self.cores} worker processes (one per host core, "
+                f"BLAS one thread each); the scheduler on the whole batch (the sample's confidences tiled) in "
+                f"the parent; value = sampled request-positions / step wall time, nothing extrapolated")
 
 
-def cpu_baseline(wl, inp, n_req, gpu_tokens=None):
-    n_req = max(1, min(n_req, wl.B))
-    inp_np = np_inputs_for_oracle(wl, inp, n_req)
-    sec, parts = oracle_sample_time(wl, inp_np, n_req)
-    d = parts.pop("_draft")
-    res = {"value": wl.B * wl.gamma / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
-           "sample": f"fp64 oracle: draft + verify of {n_req} of {wl.B} requests (extrapolated per request), "
-                     f"scheduler on the full batch; one host thread",
-           "parts_s": parts}
+def default_oracle_requests(wl, cores: int) -> int:
+    """Requests per oracle step: two per core, within the batch."""
+    return max(1, min(wl.B, 2 * cores))
+
+
+def cpu_baseline(wl, inp, n_req, gpu_tokens=None, steps=2):
+    """The oracle on the host cores, timed on a bounded sample (one untimed
+    step, then `steps` timed steps, median)."""
+    cores = host_cores()
+    n_req = n_req or default_oracle_requests(wl, cores)
+    pool = OraclePool(wl, inp, n_req, cores)
+    try:
+        pool.step()
+        runs = [pool.step() for _ in range(steps)]
+    finally:
+        pool.close()
+    sec = float(np.median([r["step_s"] for r in runs]))
+    res = {"value": pool.n_req * wl.gamma / sec, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+           "sample": pool.describe() + f"; {steps} timed steps after one untimed, median",
+           "host_cores": cores, "step_s": sec,
+           "parts_s": {k: float(np.median([r[k] for r in runs])) for k in runs[0] if k != "step_s"}}
     if gpu_tokens is not None:
         # the sampled requests' draft tokens against the oracle's, position by position up
         # to the first draw inside the margin (later positions depend on that draw)
-        g = np.asarray(gpu_tokens)[:n_req]
+        g = np.asarray(gpu_tokens)[:pool.n_req]
         agree = {}
         for name, mg in (("margin_1e-5", 1e-5), ("margin_1e-7", 1e-7)):
             n_cmp = n_ok = 0
-            for r in range(n_req):
+            for r in range(pool.n_req):
                 for k in range(wl.gamma):
-                    if d["margin"][r, k] < mg:
+                    if pool.margin[r, k] < mg:
                         break
                     n_cmp += 1
-                    n_ok += int(g[r, k] == d["tokens"][r, k])
+                    n_ok += int(g[r, k] == pool.tokens[r, k])
             agree[name] = {"compared": n_cmp, "equal": n_ok}
         res["token_agreement"] = agree
     return res
 
 
 def run_reference(args):
+    """The oracle as the reference arm: every step a bounded sample of the
+    workload (two requests per host core by default), all host cores."""
+    import synth
     import torch
     wl = synth.get_workload(args.workload)
     inp = synth.make_inputs(wl, "cpu")
@@ -543,25 +649,42 @@ def run_reference(args):
     if args.sched == "async":
         inp["sched_mode"] = synth.SCHED_ASYNC_TOPK
         inp["zprev"] = torch.from_numpy(synth.random_conf_logits(wl.B, wl.gamma, wl.seed + 77))
-    n_req = max(1, min(args.cpu_sample, wl.B))
-    inp_np = np_inputs_for_oracle(wl, inp, n_req)
-    for _ in range(args.warmup if args.warmup < 2 else 1):
-        oracle_sample_time(wl, inp_np, n_req)
-    secs = []
-    for _ in range(args.steps):
-        s, _ = oracle_sample_time(wl, inp_np, n_req)
-        secs.append(s)
-    sec = float(np.mean(secs))
-    value = wl.B * wl.gamma / sec
-    sample = (f"fp64 oracle per step: draft + verify of {n_req} of {wl.B} requests (extrapolated per request), "
-              f"scheduler on the full batch; one host thread")
+    if args.head == "rnn":
+        inp["W_rnn"] = synth.rnn_weights(wl.r, wl.H, wl.dtype, wl.seed, "cpu")
+    cores = host_cores()
+    n_req = args.cpu_sample or default_oracle_requests(wl, cores)
+    pool = OraclePool(wl, inp, n_req, cores)
+    try:
+        for _ in range(args.warmup):
+            pool.step()
+        t0 = time.perf_counter()
+        runs = [pool.step() for _ in range(args.steps)]
+        timed = time.perf_counter() - t0
+    finally:
+        pool.close()
+    sec = float(np.median([r["step_s"] for r in runs]))
+    value = pool.n_req * wl.gamma / sec
+    sample = pool.describe() + f"; median of {args.steps} steps after {args.warmup} untimed"
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; DSpark workload model)",
-            "config": {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "H": wl.H,
-                       "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[inp["sched_mode"]]},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": workload_config(wl, args, inp["sched_mode"], 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "timed_region_s": timed, "requests_per_step": pool.n_req, "host_cores": cores,
+            "parts_s": {k: float(np.median([r[k] for r in runs])) for k in runs[0] if k != "step_s"}}
+
+
+def workload_config(wl, args, sched_mode, world) -> dict:
+    """The `config` object of both arms: the workload and the modes, nothing
+    that depends on the run."""
+    u_mb = wl.B * wl.gamma * wl.V * (2 if wl.dtype == "bf16" else 4) / 1e6
+    return {"workload": wl.name, "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "H": wl.H, "temp": wl.temp,
+            "scheduler": {0: "off", 1: "greedy_early_stop", 2: "async_topk"}[sched_mode],
+            "head": args.head, "verify": args.verify, "pd_rows": args.rows,
+            "l2": (("inputs larger than L2 (U alone %.0f MB per step), no flush" if u_mb > 129 else
+                    "inputs within the 129 MB L2 (U %.1f MB per step), no flush") % u_mb),
+            "parallelism": "replicas" if world > 1 else "1gpu"}
 
 
 # ---------------------------------------------------------------------------
@@ -583,6 +706,7 @@ def sts_evals(wl) -> int:
 
 
 def run_sts_ours(args, rank, world, local_rank):
+    import synth
     import torch
     from draft_sampling_lossless_markov_gb300 import build, capi
     from draft_sampling_lossless_markov_gb300 import torch_api as T
@@ -711,6 +835,7 @@ def sts_cpu_baseline(wl, inp):
 
 
 def run_sts_reference(args):
+    import synth
     wl = synth.STS_WORKLOADS[args.workload]
     inp = synth.sts_inputs(wl)
     for _ in range(min(args.warmup, 1)):
@@ -729,7 +854,13 @@ def run_sts_reference(args):
             "e2e": {"value": value, "unit": STS_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# every point of the batch/gamma sweep, then the named full-size configs
+SWEEP_ALL = ([f"sweep_B{b}_g{g}" for b in (1, 8, 64, 256, 1024, 4096) for g in (4, 7, 15, 16)]
+             + ["qwen3_4b", "qwen3_8b_sched", "deepseek_vocab"])
+
+
 def main():
+    import synth
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -747,9 +878,13 @@ def main():
     ap.add_argument("--rows", default="full", choices=["full", "none"],
                     help="write the p_d rows (full), or draft without them and draw the residual by rejection "
                          "from p_t (none)")
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated workloads (or 'all': the batch/gamma sweep and the named configs): one "
+                         "JSON line per workload, device-timed only (no end-to-end leg, no oracle baseline)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=4, help="requests the oracle runs per step")
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="requests the oracle runs per step (default: two per host core)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -764,9 +899,20 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    res = run_sts_ours(args, rank, world, local_rank) if sts else run_ours(args, rank, world, local_rank)
-    if rank == 0:
-        print(json.dumps(res), flush=True)
+    if args.sweep:
+        import torch
+        names = (SWEEP_ALL if args.sweep == "all" else args.sweep.split(","))
+        args.no_e2e = args.no_cpu_baseline = True
+        for name in names:
+            args.workload = name
+            res = run_ours(args, rank, world, local_rank)
+            if rank == 0:
+                print(json.dumps(res), flush=True)
+            torch.cuda.empty_cache()
+    else:
+        res = run_sts_ours(args, rank, world, local_rank) if sts else run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

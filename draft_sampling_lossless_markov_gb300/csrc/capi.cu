@@ -99,10 +99,27 @@ static dspark_status check_ws(const dspark_dims& d, void* ws, size_t bytes, WsLa
 // the CUDA error behind the last DSPARK_CUDA_ERROR returned on this thread
 static thread_local int t_last_cuda_error = 0;
 
-static dspark_status cuda_status(cudaError_t e) {
+dspark_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return DSPARK_OK;
   t_last_cuda_error = (int)e;
   return DSPARK_CUDA_ERROR;
+}
+
+dspark_status check_sched_args(const dspark_sched_args* a, int64_t max_keys) {
+  if (!a || a->B < 0 || a->gamma < 1 || a->gamma > DSPARK_MAX_GAMMA) return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY && a->mode != DSPARK_SCHED_ASYNC_TOPK)
+    return DSPARK_INVALID_ARG;
+  if ((int64_t)a->B * a->gamma > max_keys) return DSPARK_UNSUPPORTED;
+  if (a->B == 0) return DSPARK_OK;
+  if (!a->conf_logit || !a->sts_temp || !a->anchor || !a->tokens || !a->ell || !a->offsets || !a->flat_tok ||
+      !a->mark_req || !a->mark_pos || !a->n_verify || !a->theta_best)
+    return DSPARK_INVALID_ARG;
+  if (a->mode != DSPARK_SCHED_OFF && !a->sps) return DSPARK_INVALID_ARG;
+  if (a->mode == DSPARK_SCHED_ASYNC_TOPK) {
+    if (!a->conf_logit_prev) return DSPARK_INVALID_ARG;
+    if (!schedule_async_supported(a->B, a->gamma)) return DSPARK_UNSUPPORTED;
+  }
+  return DSPARK_OK;
 }
 
 }  // namespace dspark
@@ -179,19 +196,8 @@ dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, s
 }
 
 dspark_status dspark_schedule(const dspark_sched_args* a, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!a || a->B < 0 || a->gamma < 1 || a->gamma > DSPARK_MAX_GAMMA) return DSPARK_INVALID_ARG;
-  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY && a->mode != DSPARK_SCHED_ASYNC_TOPK)
-    return DSPARK_INVALID_ARG;
-  if ((int64_t)a->B * a->gamma > DSPARK_MAX_SCHED_KEYS) return DSPARK_UNSUPPORTED;
-  if (a->B == 0) return DSPARK_OK;
-  if (!a->conf_logit || !a->sts_temp || !a->anchor || !a->tokens || !a->ell || !a->offsets || !a->flat_tok ||
-      !a->mark_req || !a->mark_pos || !a->n_verify || !a->theta_best)
-    return DSPARK_INVALID_ARG;
-  if (a->mode != DSPARK_SCHED_OFF && !a->sps) return DSPARK_INVALID_ARG;
-  if (a->mode == DSPARK_SCHED_ASYNC_TOPK) {
-    if (!a->conf_logit_prev) return DSPARK_INVALID_ARG;
-    if (!schedule_async_supported(a->B, a->gamma)) return DSPARK_UNSUPPORTED;
-  }
+  const dspark_status chk = check_sched_args(a, DSPARK_MAX_SCHED_KEYS);
+  if (chk != DSPARK_OK || a->B == 0) return chk;
   dspark_dims d{a->B, a->gamma, 1, 0, 0, DSPARK_F32};
   WsLayout L;
   const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);

@@ -50,6 +50,17 @@ WsLayout ws_layout(const dspark_dims& d);
 // host-side launch accounting (dspark_launch_count)
 void count_launches(int n);
 
+// DSPARK_OK for cudaSuccess; otherwise records e for dspark_last_cuda_error on
+// this thread and returns DSPARK_CUDA_ERROR.
+dspark_status cuda_status(cudaError_t e);
+
+// The argument checks of the scheduler entry points (dspark_schedule and
+// dspark_schedule_noalloc), before anything is enqueued: DSPARK_INVALID_ARG
+// for a null or malformed argument, DSPARK_UNSUPPORTED for B * gamma above
+// max_keys or an asynchronous batch beyond one CTA's shared memory.  B == 0
+// passes (the callers return at once).
+dspark_status check_sched_args(const dspark_sched_args* a, int64_t max_keys);
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device.  The attribute belongs to the kernel's instance in each
 // device's context, so it is recorded per (device, kernel); a process that

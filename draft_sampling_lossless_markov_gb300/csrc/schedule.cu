@@ -615,11 +615,12 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
   uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
+  // every refusal comes before the first launch
+  if (a.mode == DSPARK_SCHED_ASYNC_TOPK && !schedule_async_supported(a.B, a.gamma)) return cudaErrorNotSupported;
   const int rb = PREP_THREADS / a.gamma;
   k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1);
   const int n_pad = sched_slots(a.B, a.gamma);
   const size_t smem = schedule_smem_bytes(a.B, a.gamma);
-  if (a.mode == DSPARK_SCHED_ASYNC_TOPK && !schedule_async_supported(a.B, a.gamma)) return cudaErrorNotSupported;
   if (n_pad <= kSmemSortMax && smem <= kSmemSchedMax) {
     if (const cudaError_t ae = ensure_smem_limit((const void*)k_schedule_smem, (int)kSmemSchedMax); ae != cudaSuccess)
       return ae;

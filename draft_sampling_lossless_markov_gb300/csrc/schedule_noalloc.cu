@@ -10,8 +10,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "dspark.h"
 #include "internal.h"
@@ -20,7 +18,6 @@ namespace dspark {
 namespace {
 
 constexpr int kNoallocKeys = DSPARK_MAX_SCHED_KEYS;  // candidates (B * gamma) per call, at most
-constexpr int kMaxDevices = 64;
 
 // 4 x 65536 x 4 bytes = 1 MiB, present in every GPU context that loads the
 // library until the process exits.  Layout: keys copy 0, keys copy 1, values
@@ -29,25 +26,20 @@ constexpr int kMaxDevices = 64;
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) uint32_t g_sched_scratch[4 * kNoallocKeys];
 
-std::mutex g_mu;
-void* g_scratch_dev[kMaxDevices] = {};
-
-// Device address of g_sched_scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of g_sched_scratch in the current device's context.  The
+// lookup allocates nothing and runs on every call, so the address always
+// belongs to the context that is current now: a process that resets the
+// device (which reloads the library's module and may move the array), or a
+// caller that makes its own driver-API context current on the GPU, gets that
+// context's copy rather than a stale one.  The first lookup in a context can
+// load the library's device code there, which is why the first call on a
+// device should come before any stream capture.
 cudaError_t scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_sched_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_dev[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_sched_scratch);
-    if (e != cudaSuccess) return e;
-    if (p == nullptr) return cudaErrorInvalidSymbol;
-    g_scratch_dev[dev] = p;
-  }
-  *out = g_scratch_dev[dev];
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  *out = p;
   return cudaSuccess;
 }
 
@@ -57,23 +49,13 @@ cudaError_t scratch_address(void** out) {
 using namespace dspark;
 
 extern "C" dspark_status dspark_schedule_noalloc(const dspark_sched_args* a, void* stream) {
-  // the same argument checks as dspark_schedule
-  if (!a || a->B < 0 || a->gamma < 1 || a->gamma > DSPARK_MAX_GAMMA) return DSPARK_INVALID_ARG;
-  if (a->mode != DSPARK_SCHED_OFF && a->mode != DSPARK_SCHED_GREEDY && a->mode != DSPARK_SCHED_ASYNC_TOPK)
-    return DSPARK_INVALID_ARG;
-  if ((int64_t)a->B * a->gamma > kNoallocKeys) return DSPARK_UNSUPPORTED;  // beyond the static array
-  if (a->B == 0) return DSPARK_OK;
-  if (!a->conf_logit || !a->sts_temp || !a->anchor || !a->tokens || !a->ell || !a->offsets || !a->flat_tok ||
-      !a->mark_req || !a->mark_pos || !a->n_verify || !a->theta_best)
-    return DSPARK_INVALID_ARG;
-  if (a->mode != DSPARK_SCHED_OFF && !a->sps) return DSPARK_INVALID_ARG;
-  if (a->mode == DSPARK_SCHED_ASYNC_TOPK) {
-    if (!a->conf_logit_prev) return DSPARK_INVALID_ARG;
-    if (!schedule_async_supported(a->B, a->gamma)) return DSPARK_UNSUPPORTED;
-  }
+  // the checks of dspark_schedule, with the static array's capacity as the limit
+  const dspark_status chk = check_sched_args(a, kNoallocKeys);
+  if (chk != DSPARK_OK || a->B == 0) return chk;
 
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return DSPARK_CUDA_ERROR;
+  const dspark_status st = cuda_status(scratch_address(&scratch));
+  if (st != DSPARK_OK) return st;
   // The kernel writes every key and value it later reads (all B * gamma of
   // them, in every sort pass), so nothing left from an earlier call needs
   // clearing.
@@ -83,6 +65,5 @@ extern "C" dspark_status dspark_schedule_noalloc(const dspark_sched_args* a, voi
   L.sv0 = 2 * (size_t)kNoallocKeys * sizeof(uint32_t);
   L.sv1 = 3 * (size_t)kNoallocKeys * sizeof(uint32_t);
   L.total = 4 * (size_t)kNoallocKeys * sizeof(uint32_t);
-  const cudaError_t e = launch_schedule(*a, static_cast<uint8_t*>(scratch), L, (cudaStream_t)stream);
-  return e == cudaSuccess ? DSPARK_OK : DSPARK_CUDA_ERROR;
+  return cuda_status(launch_schedule(*a, static_cast<uint8_t*>(scratch), L, (cudaStream_t)stream));
 }

@@ -260,9 +260,13 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
  * Limit: B * gamma <= DSPARK_MAX_SCHED_KEYS (65536); larger batches return
  * DSPARK_UNSUPPORTED before anything is enqueued.  Other argument errors are
  * those of dspark_schedule.
- * Set-up: the first call on each device, with that device current, looks up
- * the array's device address once (cudaGetSymbolAddress) and caches it; make
- * that first call before any stream capture begins.
+ * Set-up: every call looks up the array's device address in the context that
+ * is current (cudaGetSymbolAddress, which allocates nothing), so the address
+ * stays right across a device reset or a caller-made driver-API context.  The
+ * first call in a context can load the library's device code there: make
+ * the first call on each device, with that device current, before any stream
+ * capture begins.  A failed lookup or launch returns DSPARK_CUDA_ERROR and is
+ * recorded for dspark_last_cuda_error like the other entry points' errors.
  * Sharing: every call on a device uses the same array, which keeps whatever
  * the last call left in it.  The kernel overwrites every entry it reads, so
  * nothing needs clearing between calls, but two calls whose kernels overlap on

@@ -208,3 +208,17 @@ def test_misaligned_pointers_are_refused(lib):
         assert capi.dspark_verify(v, 0x20000, 1 << 30, 0) == capi.DSPARK_CUDA_ERROR  # control, as above
         setattr(v, bad, 0x10004)
         assert capi.dspark_verify(v, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG, bad
+
+
+def test_noalloc_scheduler_source_names_no_allocating_call():
+    # dspark_schedule_noalloc exists for callers that cannot allocate device memory:
+    # neither its file nor the scheduler launcher it shares with dspark_schedule
+    # may name an allocating runtime call
+    csrc = os.path.join(ROOT, "draft_sampling_lossless_markov_gb300", "csrc")
+    noalloc = open(os.path.join(csrc, "schedule_noalloc.cu")).read()
+    sched = open(os.path.join(csrc, "schedule.cu")).read()
+    launcher = sched[sched.index("cudaError_t launch_schedule("):]
+    bad = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cuMem(?:Alloc|Free|Create|Map)\w*|cudaHostAlloc|cudaMemPool\w*)\b")
+    for name, src in (("schedule_noalloc.cu", noalloc), ("launch_schedule", launcher)):
+        code = re.sub(r"//[^\n]*", "", src)  # comments may name them
+        assert not bad.search(code), (name, bad.search(code).group(0))

@@ -95,6 +95,30 @@ def test_noalloc_schedule_matches_workspace_schedule():
     assert int(ref1["n_verify"][0]) > c1["B"]  # the scheduler admitted something: a real comparison
 
 
+def test_noalloc_schedule_allocates_no_device_memory():
+    # the property the entry point exists for: once the library's device code is
+    # loaded (the first call), further calls leave the device's free memory and
+    # torch's caching allocator untouched
+    require_gpu()
+    c = _case(256, 7, 41)
+    _without_workspace(c)
+    torch.cuda.synchronize()
+    outs = [_outputs(c["B"], c["G"]) for _ in range(3)]  # every tensor allocated before the calls
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for out in outs:
+        st = capi.dspark_schedule_noalloc(_args(c, out), torch.cuda.current_stream().cuda_stream)
+        assert st == capi.DSPARK_OK, capi.dspark_status_string(st)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0
+    for k in ("allocation.all.allocated", "segment.all.allocated", "allocated_bytes.all.allocated"):
+        assert stats1.get(k, 0) == stats0.get(k, 0), k
+    _same(outs[0], outs[2])
+
+
 def test_noalloc_schedule_rejects_batches_beyond_the_array():
     require_gpu()
     a = capi.dspark_sched_args()
