@@ -34,6 +34,11 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 __device__ __forceinline__ float exp_shifted(float y, float m) { return ex2_ftz(__fsub_rn(y, m)); }
 // mass of a tile with partial (m_t, s_t) relative to the row max m
 __device__ __forceinline__ float tile_mass(float mt, float st, float m) { return __fmul_rn(st, ex2_ftz(__fsub_rn(mt, m))); }
+// 2^(l c - m) with l c - m formed by one fma (one rounding instead of two): the
+// fused-sweep kernel's form, used by every step of that kernel that weighs a
+// logit (chunk sums, the crossing chunk's walk, the p_d rows), so that they
+// agree with each other
+__device__ __forceinline__ float exp_scaled(float l, float c, float m) { return ex2_ftz(__fmaf_rn(l, c, -m)); }
 // 1 / S
 __device__ __forceinline__ float inv_sum(float S) { return __frcp_rn(S); }
 // p = 2^(y - m) / S, as 2^(y - m) * (1 / S)

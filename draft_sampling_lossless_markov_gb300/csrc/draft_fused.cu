@@ -77,7 +77,8 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 // select scratch in the (idle) staging area: per team a row record, 16 words of
 // exchange and four warps' 64 partial logits
 constexpr int kSelRecOff = 0, kSelXwOff = 128, kSelRedOff = 256;
-static_assert(kSelRedOff + 2 * kTeamWarps * 64 * 4 <= kEpiWarps * kStagingPerWarp, "select scratch");
+constexpr int kSelConfOff = kSelRedOff + 2 * kTeamWarps * 64 * 4;  // per team four warp sums of z
+static_assert(kSelConfOff + 2 * kTeamWarps * 4 <= kEpiWarps * kStagingPerWarp, "select scratch");
 
 struct Params {
   int B, G, V, r, H;
@@ -182,49 +183,74 @@ __device__ bool grid_barrier(const Params& p, unsigned target, volatile int* abo
   return *s_ok != 0;
 }
 
-// Confidence of position k of row b (one warp): z = w_h . h_k + w_e . W1[x]
-// with x = x_{k-1} (the anchor for k = 0) and c = sigmoid(z) ([DSpark] 方法细节,
-// 置信度头).  w_h . h_k: lane l takes the 8-element groups l, l + 32, ..
-// (H % 8 == 0); w_e . W1[x]: lane l takes elements 8 l .. 8 l + 7 (r <= 256).
-__device__ void conf_of(const Params& p, int b, int k, int x, int lane) {
-  if (x < 0 || x >= p.V) x = 0;
+// named barrier of one select team (four warps)
+__device__ __forceinline__ void team_sync(int team) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + team), "n"(kTeamWarps * 32) : "memory");
+}
+
+// Confidence of position k of row b, split over a team's four warps
+// ([DSpark] 方法细节, 置信度头): z = w_h . h_k + w_e . W1[x] with x = x_{k-1}
+// (the anchor for k = 0), c = sigmoid(z).  The team's lane tl takes the
+// 8-element groups tl, tl + 128, .. of h_k and w_h (H % 8 == 0), warp 0's lane
+// l also elements 8 l .. 8 l + 7 of W1[x] and w_e (r <= 256).  The first
+// kConfPer groups of each lane are loaded when the select of the row begins
+// (conf_issue) and added after the levels pass (conf_partial), so that no load
+// of the confidence waits on the select's critical path; for H > 4096 the
+// rest are loaded there.  Nothing in the kernel reads the confidences.
+constexpr int kConfPer = 4;
+struct ConfLoads {
+  uint4 h[kConfPer], w[kConfPer];
+  uint4 e, we;  // W1[x] and w_e (team warp 0)
+};
+
+__device__ __forceinline__ void conf_issue(const Params& p, int b, int k, int tw, int lane, ConfLoads& L) {
+  const int tl = tw * 32 + lane;
+  const uint4* hq = reinterpret_cast<const uint4*>(p.h + ((size_t)b * p.G + k) * p.H);
+  const uint4* wq = reinterpret_cast<const uint4*>(p.w);
+  const int n8 = p.H / 8;
+#pragma unroll
+  for (int u = 0; u < kConfPer; ++u) {
+    const int i = tl + u * kTeamWarps * 32;
+    L.h[u] = i < n8 ? __ldcs(hq + i) : make_uint4(0u, 0u, 0u, 0u);
+    L.w[u] = i < n8 ? __ldg(wq + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  L.e = L.we = make_uint4(0u, 0u, 0u, 0u);
+  if (tw == 0 && 8 * lane < p.r) {
+    int x = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
+    if (x < 0 || x >= p.V) x = 0;
+    L.e = *reinterpret_cast<const uint4*>(p.W1 + (size_t)x * p.r + 8 * lane);
+    L.we = __ldg(reinterpret_cast<const uint4*>(p.w + p.H + 8 * lane));
+  }
+}
+
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b, float acc) {
+  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 fa = __bfloat1622float2(a2[t]), fb = __bfloat1622float2(b2[t]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+  return acc;
+}
+
+// This warp's share of z, summed over the warp (every lane holds it).
+__device__ __forceinline__ float conf_partial(const Params& p, int b, int k, int tw, int lane, const ConfLoads& L) {
+  const int tl = tw * 32 + lane;
+  const int n8 = p.H / 8;
   float zh = 0.f;
-  {
+#pragma unroll
+  for (int u = 0; u < kConfPer; ++u) zh = dot8_bf16(L.h[u], L.w[u], zh);
+  if (n8 > kConfPer * kTeamWarps * 32) {
     const uint4* hq = reinterpret_cast<const uint4*>(p.h + ((size_t)b * p.G + k) * p.H);
     const uint4* wq = reinterpret_cast<const uint4*>(p.w);
-#pragma unroll 4
-    for (int i = lane; i < p.H / 8; i += 32) {
-      const uint4 hv = __ldcs(hq + i), wv = wq[i];
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
-      const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 fh = __bfloat1622float2(h2[t]), fw = __bfloat1622float2(w2[t]);
-        zh = fmaf(fh.x, fw.x, zh);
-        zh = fmaf(fh.y, fw.y, zh);
-      }
-    }
-    zh = warp_sum(zh);
+    for (int i = tl + kConfPer * kTeamWarps * 32; i < n8; i += kTeamWarps * 32)
+      zh = dot8_bf16(__ldcs(hq + i), __ldg(wq + i), zh);
   }
-  float acc = 0.f;
-  if (8 * lane < p.r) {
-    const uint4 eq = *reinterpret_cast<const uint4*>(p.W1 + (size_t)x * p.r + 8 * lane);
-    const uint4 wq = *reinterpret_cast<const uint4*>(p.w + p.H + 8 * lane);
-    const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&eq);
-    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wq);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 fe = __bfloat1622float2(e2[t]), fw = __bfloat1622float2(w2[t]);
-      acc = fmaf(fw.x, fe.x, acc);
-      acc = fmaf(fw.y, fe.y, acc);
-    }
-  }
-  acc = warp_sum(acc);
-  if (lane == 0) {
-    const float z = zh + acc;
-    p.conf_logit[(size_t)b * p.G + k] = z;
-    p.conf[(size_t)b * p.G + k] = 1.f / (1.f + expf(-z));
-  }
+  zh = dot8_bf16(L.we, L.e, zh);  // zero outside warp 0
+  return warp_sum(zh);
 }
 
 // Row record of the select, in shared memory between its steps.
@@ -238,11 +264,6 @@ struct SelRec {
   int x;          // x_{k-1}, the token the logits condition on
   int tok;        // the chosen token
 };
-
-__device__ __forceinline__ void team_sync(int team) {
-  __syncwarp();
-  asm volatile("bar.sync %0, %1;" ::"r"(2 + team), "n"(kTeamWarps * 32) : "memory");
-}
 
 // The pass of the select of row b at position k over its chunk partials, by
 // one team of four warps: lane tl = 32 tw + lane holds the partials
@@ -290,10 +311,13 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
       st_release_s32(&p.tokens[(size_t)b * p.G + k], ai);
       rec->cstar = -1;
       rec->b = b;
+      rec->x = xprev;
       rec->tok = ai;
     }
     return;
   }
+  // the draw, while the partials are in flight
+  const float u = philox_uniform(p.seed, req, (uint32_t)(k + 1), 0u);
   float ml = -INFINITY;
 #pragma unroll
   for (int t = 0; t < kMaxE; ++t) {
@@ -306,12 +330,13 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
   const float m = fmaxf(fmaxf(xw[0], xw[1]), fmaxf(xw[2], xw[3]));
   float sl = 0.f;
   int tlast = -1;
+  float qm[kMaxE];  // each chunk's mass relative to m, reused by the walk below
 #pragma unroll
   for (int t = 0; t < kMaxE; ++t) {
     if (t >= E) break;
-    const float qm = tile_mass(e[t].x, e[t].y, m);
-    sl = __fadd_rn(sl, qm);
-    if (qm > 0.f) tlast = t;
+    qm[t] = tile_mass(e[t].x, e[t].y, m);
+    sl = __fadd_rn(sl, qm[t]);
+    if (qm[t] > 0.f) tlast = t;
   }
   const float incl = warp_inclusive_scan(sl);
   const float up = __shfl_up_sync(FULL, incl, 1);
@@ -330,7 +355,6 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
 #pragma unroll
   for (int w = 0; w < kTeamWarps; ++w) jlast = max(jlast, __float_as_int(xw[12 + w]));
   jlast = max(jlast - 1, 0);
-  const float u = philox_uniform(p.seed, req, (uint32_t)(k + 1), 0u);
   const float target = u * S;
   const float ex = __fadd_rn(wbase, excl);
   const unsigned bal = __ballot_sync(FULL, j0 < p.nparts && __fadd_rn(wbase, incl) > target);
@@ -355,8 +379,7 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
 #pragma unroll
       for (int t = 0; t < kMaxE; ++t) {
         if (t >= E) break;
-        const float qm = tile_mass(e[t].x, e[t].y, m);
-        const float nr = __fadd_rn(run, qm);
+        const float nr = __fadd_rn(run, tile_mass(e[t].x, e[t].y, m));
         if (cstar < 0 && j0 + t < p.nparts && nr > target) {
           cstar = j0 + t;
           cbase = run;
@@ -452,8 +475,8 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
       d1 = __fadd_rn(d1, red[w * 64 + 2 * lane + 1]);
     }
     const float2 fu = __bfloat1622float2(uv);
-    w0 = exp_shifted(scale_logit(add_base(fu.x, d0), c), rec->m);
-    w1 = exp_shifted(scale_logit(add_base(fu.y, d1), c), rec->m);
+    w0 = exp_scaled(add_base(fu.x, d0), c, rec->m);
+    w1 = exp_scaled(add_base(fu.y, d1), c, rec->m);
   }
   const float pair = __fadd_rn(w0, w1);
   const float incl = __fadd_rn(rec->sbase, warp_inclusive_scan(pair));
@@ -708,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = qd * 32 + lane;
     const int b = row_base + row;
     const bool vrow = b < p.B;
+    const bool wlive = row_base + qd * 32 < p.B;  // warp-uniform: some row of this warp is in the batch
     const uint32_t lane_bits = (uint32_t)(qd * 32) << 16;
     const int npieces = r / 64;
     const float T_ = vrow ? p.temp[b] : 1.f;
@@ -719,6 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool alive = true;
 
     // E_k = W1[x_{k-1}] (x_0 = anchor) into TMEM slot k & 1
+    // the next W item's row data, taken by the gather that waits for its token:
+    // x_{k-1} and (m, S) of position k - 1 (published before the token)
+    int wx = -1;
+    float2 wst = make_float2(0.f, 1.f);
     auto gather = [&](int k) {
       int x = 0;
       if (vrow) {
@@ -730,6 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail();
             x = 0;
           }
+          wx = x;
+          wst = __ldcg(&p.rowstat[b]);
         }
         if (x < 0 || x >= p.V) {
           if (g == 0) report_error(p.hdr, DSPARK_BAD_INPUT, x);
@@ -789,11 +819,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       SelRec* rec = reinterpret_cast<SelRec*>(sStg + kSelRecOff) + team;
       float* xw = reinterpret_cast<float*>(sStg + kSelXwOff) + team * 16;
       float* red = reinterpret_cast<float*>(sStg + kSelRedOff) + team * kTeamWarps * 64;
+      float* cz = reinterpret_cast<float*>(sStg + kSelConfOff) + team * kTeamWarps;
       for (int j = team;; j += 2) {
         const int rb = (int)blockIdx.x + p.n_ctas * j;
         if (rb >= p.B) break;
+        // the confidence of (rb, k) needs x_{k-1} only: its loads go out first
+        // and land during the levels pass
+        ConfLoads cl;
+        conf_issue(p, rb, k, tw, lane, cl);
         team_levels(p, rb, k, team, tw, lane, rec, xw);
+        {
+          const float zp = conf_partial(p, rb, k, tw, lane, cl);
+          if (lane == 0) cz[tw] = zp;
+        }
         team_sync(team);
+        if (tw == 1 && lane == 0) {
+          const float z = (cz[0] + cz[1]) + (cz[2] + cz[3]);
+          p.conf_logit[(size_t)rb * G + k] = z;
+          p.conf[(size_t)rb * G + k] = 1.f / (1.f + expf(-z));
+        }
         const int cstar = rec->cstar;
         if (cstar >= 0) {
           // the walking warp fetches the chunk's U pairs before the recompute
@@ -823,12 +867,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rm = 0.f, rinvS = 1.f;
       int xs = -1;
       if (hasW && vrow) {
-        // the select of another CTA publishes (m, S) and then x_s
-        xs = token_wait(&p.tokens[(size_t)b * p.G + s], abort_flag);
-        if (xs == kTokPending) fail();
-        const float2 st = __ldcg(&p.rowstat[b]);
-        rm = st.x;
-        rinvS = inv_sum(st.y);
+        // the select of another CTA published (m, S) and then x_s; the gather of
+        // E_{s+1} waited for x_s and read both
+        xs = wx;
+        rm = wst.x;
+        rinvS = inv_sum(wst.y);
       }
       float pdtok = 0.f;
       bool have_pdtok = false;
@@ -860,12 +903,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++it;
           ++iu;
           ptx::tc_fence_after();
+          if (!wlive) {
+            // every row of this warp is past the batch: release the accumulator
+            // and the U stage unread
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(&tempty[a]);
+              ptx::mbar_arrive(&emptyU[su]);
+            }
+            continue;
+          }
           const uint32_t ta = tmem + lane_bits + kAccCol0 + (uint32_t)(a * BN + ch * CW);
           const uint8_t* su_row = sU + su * kUStage + ch * kUChunk + row * 128;
-          // logits of the chunk's 64 columns: accumulator + U, both TMEM halves
-          // in flight at once; the reads release the accumulator and the U stage
-          float xa[32], xb[32];
+          // the row's 64 U values (8 x 16 B, 128-byte swizzle), loaded before the
+          // TMEM wait so that the two latencies overlap
+          uint4 uq[8];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) uq[c8] = *reinterpret_cast<const uint4*>(su_row + ((c8 ^ (row & 7)) << 4));
+          // logits of the chunk's 64 columns: accumulator + U; reading the
+          // accumulator releases it
+          float x[64];
           {
+            float (&xa)[32] = *reinterpret_cast<float(*)[32]>(&x[0]);
+            float (&xb)[32] = *reinterpret_cast<float(*)[32]>(&x[32]);
             __syncwarp();
             ptx::tmem_ld32(ta, xa);
             ptx::tmem_ld32(ta + 32, xb);
@@ -873,71 +933,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tempty[a]);
-            auto add_u = [&](float(&x)[32], int h) {
+          }
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                const int c8 = 4 * h + cc;
-                const uint4 qv = *reinterpret_cast<const uint4*>(su_row + ((c8 ^ (row & 7)) << 4));
-                const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&qv);
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(&uq[c8]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = __bfloat1622float2(bp[e]);
-                  x[8 * cc + 2 * e] = add_base(f.x, x[8 * cc + 2 * e]);
-                  x[8 * cc + 2 * e + 1] = add_base(f.y, x[8 * cc + 2 * e + 1]);
-                }
-              }
-            };
-            add_u(xa, 0);
-            add_u(xb, 1);
-            // the stage's next fill is an async-proxy (TMA) write: order this
-            // warp's generic reads before it
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(bp[e]);
+              x[8 * c8 + 2 * e] = add_base(f.x, x[8 * c8 + 2 * e]);
+              x[8 * c8 + 2 * e + 1] = add_base(f.y, x[8 * c8 + 2 * e + 1]);
+            }
+          }
+          if (item == 1) {
+            // the U stage's next fill is an async-proxy (TMA) write: order this
+            // warp's generic reads of it before the release
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&emptyU[su]);
-          }
-          if (item == 1) {
             // S item: chunk partial of position s + 1
-            float mc = -INFINITY, cs = 0.f, av = -INFINITY;
-            int ai = INT_MAX;
-            auto s_half = [&](float(&x)[32], int h) {
-              if (sampled) {
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float2 part;
+            if (sampled) {
+              // chunk max on the logits (l c is monotone in l for c > 0), then
+              // the sum of 2^(l c - m_chunk); columns past V count as -inf
+              if (nvalid < CW) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  x[j] = (32 * h + j < nvalid) ? scale_logit(x[j], c) : -INFINITY;
-                  mx[j & 3] = fmaxf(mx[j & 3], x[j]);
-                }
-                const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                if (mh != -INFINITY) {
-                  float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) sm[j & 3] += exp_shifted(x[j], mh);
-                  const float sh = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-                  const float nm = fmaxf(mc, mh);
-                  cs = __fadd_rn(tile_mass(mc, cs, nm), tile_mass(mh, sh, nm));
-                  mc = nm;
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (32 * h + j < nvalid && x[j] > av) {
-                    av = x[j];
-                    ai = v0 + 32 * h + j;
-                  }
+                for (int j = 0; j < CW; ++j)
+                  if (j >= nvalid) x[j] = -INFINITY;
               }
-            };
-            s_half(xa, 0);
-            s_half(xb, 1);
-            if (v0 < p.V && vrow)
-              p.part[(size_t)b * p.pstride + (v0 / CW) % p.ept * 128 + (v0 / CW) / p.ept] = sampled ? make_float2(mc, cs) : make_float2(av, __int_as_float(ai));
+              float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int j = 0; j < CW; ++j) mx[j & 3] = fmaxf(mx[j & 3], x[j]);
+              const float lm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+              float cs = 0.f, mh = -INFINITY;
+              if (lm != -INFINITY) {
+                mh = scale_logit(lm, c);
+                float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < CW; ++j) sm[j & 3] += exp_scaled(x[j], c, mh);
+                cs = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+              }
+              part = make_float2(mh, cs);
+            } else {
+              float av = -INFINITY;
+              int ai = INT_MAX;
+#pragma unroll
+              for (int j = 0; j < CW; ++j)
+                if (j < nvalid && x[j] > av) {
+                  av = x[j];
+                  ai = v0 + j;
+                }
+              part = make_float2(av, __int_as_float(ai));
+            }
+            if (v0 < p.V && vrow) p.part[(size_t)b * p.pstride + (v0 / CW) % p.ept * 128 + (v0 / CW) / p.ept] = part;
           } else {
-            // W item: p_d^s = 2^(y - m) / S (one-hot for greedy rows)
+            // W item: p_d^s = 2^(l c - m) / S (one-hot for greedy rows); columns
+            // past V are computed but not stored (the TMA store clips them)
             const int row0 = row_base + qd * 32;
-            auto w_half = [&](float(&x)[32], int h) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float* xh = x + 32 * h;
               if (sampled) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  x[j] = (32 * h + j < nvalid) ? prob_from(scale_logit(x[j], c), rm, rinvS) : 0.f;
+                for (int j = 0; j < 32; ++j) xh[j] = __fmul_rn(exp_scaled(xh[j], c, rm), rinvS);
               }
               const int jx = xs - (v0 + 32 * h);
               if (jx >= 0 && jx < 32) {
@@ -945,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (sampled) {
 #pragma unroll
                   for (int j = 0; j < 32; ++j)
-                    if (j == jx) pv = x[j];
+                    if (j == jx) pv = xh[j];
                 }
                 pdtok = pv;
                 have_pdtok = true;
@@ -956,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
                   *reinterpret_cast<float4*>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
-                      make_float4(x[4 * cc], x[4 * cc + 1], x[4 * cc + 2], x[4 * cc + 3]);
+                      make_float4(xh[4 * cc], xh[4 * cc + 1], xh[4 * cc + 2], xh[4 * cc + 3]);
               } else {
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
@@ -964,15 +1021,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                       make_float4(jx == 4 * cc ? 1.f : 0.f, jx == 4 * cc + 1 ? 1.f : 0.f,
                                   jx == 4 * cc + 2 ? 1.f : 0.f, jx == 4 * cc + 3 ? 1.f : 0.f);
               }
+              // orders the staging writes before the TMA store and, in the first
+              // half, this warp's reads of the U stage before its release
               ptx::fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0 && row0 < p.B && v0 + 32 * h < p.V) {
-                ptx::tma_store_3d(&tmPd, stg, v0 + 32 * h, s, row0, ptx::policy_evict_first());
-                ptx::bulk_commit();
+              if (lane == 0) {
+                if (row0 < p.B && v0 + 32 * h < p.V) {
+                  ptx::tma_store_3d(&tmPd, stg, v0 + 32 * h, s, row0, ptx::policy_evict_first());
+                  ptx::bulk_commit();
+                }
+                if (h == 0) ptx::mbar_arrive(&emptyU[su]);
               }
-            };
-            w_half(xa, 0);
-            w_half(xb, 1);
+            }
           }
         }
       }
@@ -995,15 +1055,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // token, so no grid barrier follows the select: a CTA's next writes of a
       // row's partials come after it has seen the row's token, i.e. after the
       // select finished reading them
-      if (q + 1 < G) gather(q + 1);
-    }
-    // the confidences c_k = sigmoid(w_h . h_k + w_e . W1[x_{k-1}]) of every
-    // row and position, once all tokens are chosen (nothing above reads them)
-    if (alive && !*abort_flag) {
-      for (int t = (int)blockIdx.x * kEpiWarps + ew; t < p.B * G; t += p.n_ctas * kEpiWarps) {
-        const int rb = t / G, k = t % G;
-        const int x = (k == 0) ? p.anchor[rb] : token_wait(&p.tokens[(size_t)rb * G + k - 1], abort_flag);
-        conf_of(p, rb, k, x, lane);
+      if (q + 1 < G) {
+        gather(q + 1);
+      } else if (vrow) {
+        // the last sweep has no S items, hence no gather: the W item's row data
+        wx = token_wait(&p.tokens[(size_t)b * p.G + q], abort_flag);
+        if (wx == kTokPending) fail();
+        wst = __ldcg(&p.rowstat[b]);
       }
     }
     if (lane == 0) ptx::bulk_wait0();

@@ -9,19 +9,25 @@
 // [DSpark] 补充细节, "高吞吐量与低延迟推理": kept prefixes flattened with a
 // marker tensor.
 //
-// Two kernels.  k_sched_prep (many CTAs, one thread per candidate, because
-// the fp64 sigmoid is slow on one SM):
-//   1. c' (fp64 sigmoid rounded to fp32), a (fp32 running product), sort keys
-//      key = ~bits(a) for a > 0 (ascending key = descending a), 0xFFFFFFFF else,
-//      value = r * gamma + j, laid out in index order.
-// k_schedule_smem (one CTA, up to 8192 candidates: everything in shared memory,
-// bitonic sort of (key, index)) or k_schedule (one CTA of 1024 threads; at
-// most 65536 candidates, through global memory):
-//   2. stable LSD radix sort of the keys (4 passes of 8 bits); stability keeps
-//      equal a in (r, j) index order;
-//   3. fp64 block scan of the sorted a, Theta_i, first non-increase;
+// Up to 8192 slots (B rounded up to a power of two, times gamma rounded up to
+// a power of two) the schedule runs in one CTA's shared memory,
+// k_schedule_smem:
+//   1. c' for every candidate (a double-float sigmoid on the fp32 pipe, with
+//      the fp64 sigmoid deciding the rare values that lie near an fp32
+//      rounding boundary, so c' is the fp32 rounding of the fp64 sigmoid), a
+//      (the fp32 running product), sort keys key = ~bits(a) for a > 0 (ascending
+//      key = descending a), 0xFFFFFFFF else, with the index r * gamma + j;
+//      above kFusedKeys candidates k_sched_prep (many CTAs, one thread per
+//      candidate) does this step and writes the keys to the workspace;
+//   2. one sorted run per request merged pairwise into one;
+//   3. fp64 Theta along the sorted path (exact fixed-point survival sums),
+//      first non-increase;
 //   4. l_r by atomic max over the admitted candidates;
 //   5. offsets by a block scan of 1 + l_r; flatten + markers.
+// Above 8192 slots k_sched_prep and k_schedule (one CTA of 1024 threads, at
+// most 65536 candidates) sort the keys by a stable LSD radix sort (4 passes of
+// 8 bits; stability keeps equal a in (r, j) index order) before steps 3-5.
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -33,10 +39,50 @@ namespace dspark {
 constexpr int SCH_THREADS = 1024;
 constexpr int SCH_WARPS = SCH_THREADS / 32;
 
-// calibrated confidence: fp32 rounding of the fp64 sigmoid of z / tau
-__device__ __forceinline__ float sts_conf(float z, float tau) {
-  const double td = (double)tau;
-  return sts_sigmoid(z, td, 1.0 / td);
+// 2^(-j/64), j = 0..63, as double-float (hi, lo) pairs for the double-float
+// sigmoid: built once on the host, passed by value to the kernels.
+struct DfTable {
+  float2 t[64];
+};
+
+static const DfTable& df_table() {
+  static DfTable tab;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (int j = 0; j < 64; ++j) {
+      const double v = std::exp2(-(double)j / 64.0);
+      const float hi = (float)v;
+      tab.t[j] = make_float2(hi, (float)(v - (double)hi));
+    }
+  });
+  return tab;
+}
+
+// Per-position STS constants in shared memory: tau, 1/tau as a double-float
+// (hi, lo) and in fp64, and the 2^(-j/64) table of the double-float sigmoid.
+struct StsConsts {
+  float4 tau[DSPARK_MAX_GAMMA];  // (tau, 1/tau hi, 1/tau lo, -)
+  double rt[DSPARK_MAX_GAMMA];
+  float2 T64[64];
+};
+
+// Filled by the first max(64, gamma) threads; the caller syncs before use.
+__device__ __forceinline__ void sts_consts_init(StsConsts& c, const float* sts_temp, int G, const DfTable& tab) {
+  const int t = threadIdx.x;
+  if (t < 64) c.T64[t] = tab.t[t];
+  if (t < G) {
+    const float tau = sts_temp[t];
+    const double rt = 1.0 / (double)tau;
+    const float bh = (float)rt;
+    c.tau[t] = make_float4(tau, bh, (float)(rt - (double)bh), 0.f);
+    c.rt[t] = rt;
+  }
+}
+
+// calibrated confidence of position j: the fp32 rounding of the fp64 sigmoid of z / tau_j
+__device__ __forceinline__ float sts_conf(const StsConsts& c, float z, int j) {
+  const float4 tj = c.tau[j];
+  return sts_df::sts_sigmoid_exact32(z, tj.x, tj.y, tj.z, c.rt[j], c.T64);
 }
 
 // block-wide exclusive scan of one u32 per thread; returns the exclusive prefix
@@ -107,9 +153,12 @@ constexpr int PREP_THREADS = 256;
 // treatment into (k1, v1).
 __global__ void __launch_bounds__(PREP_THREADS) k_sched_prep(dspark_sched_args a, uint32_t* __restrict__ k0,
                                                              uint32_t* __restrict__ v0, uint32_t* __restrict__ k1,
-                                                             uint32_t* __restrict__ v1) {
+                                                             uint32_t* __restrict__ v1, const __grid_constant__ DfTable tab) {
   __shared__ float cs[PREP_THREADS];
+  __shared__ StsConsts sc;
   const int B = a.B, G = a.gamma;
+  sts_consts_init(sc, a.sts_temp, G, tab);
+  __syncthreads();
   const int rb = PREP_THREADS / G;
   const int t = threadIdx.x;
   const int lr = t / G, j = t - lr * G;
@@ -121,7 +170,7 @@ __global__ void __launch_bounds__(PREP_THREADS) k_sched_prep(dspark_sched_args a
     uint32_t* kk = set == 0 ? k0 : k1;
     uint32_t* vv = set == 0 ? v0 : v1;
     if (set) __syncthreads();  // the products of the first set have read cs
-    if (valid) cs[t] = sts_conf(z[(size_t)r * G + j], a.sts_temp[j]);
+    if (valid) cs[t] = sts_conf(sc, z[(size_t)r * G + j], j);
     __syncthreads();
     if (valid && j == 0) {
       float run = 1.f;
@@ -301,6 +350,8 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a
 // (ties in a stay in (r, j) index order).  Then the same Theta scan, l_r and
 // flatten as k_schedule.
 constexpr int kSmemSortMax = 8192;
+constexpr int kFusedKeys = 2048;  // candidates up to which k_schedule_smem calibrates them itself
+static_assert(kSmemSortMax <= 8 * 1024, "merge_runs keeps eight elements per thread");
 constexpr int kPrefetchTok = 8;  // draft lengths whose tokens k_schedule_smem loads at its start
 constexpr size_t kSmemSchedMax = 200 * 1024;  // dynamic shared memory of k_schedule_smem
 
@@ -352,20 +403,41 @@ __device__ __forceinline__ long long block_excl_scan_i64(long long v, long long*
 }
 
 // Merges sorted runs of length run0 (a power of two) in a[0, n_pad) (n_pad /
-// run0 a power of two, all values distinct) into one sorted run; b is scratch
-// of the same size.  Returns the buffer that holds the result.
-__device__ uint64_t* merge_runs(uint64_t* a, uint64_t* b, int n_pad, int run0) {
+// run0 a power of two, all values distinct, n_pad <= kSmemSortMax) into one
+// sorted run; b is scratch of the same size.  Each thread places its elements
+// i = tid, tid + 1024, .. (merge path: an element's place is its rank in its
+// own run plus its rank in the partner run, found by halving steps), the
+// searches of all its elements interleaved.  Returns the buffer that holds the
+// result.
+template <int EPT>  // elements per thread: n_pad <= EPT * SCH_THREADS
+__device__ uint64_t* merge_runs_t(uint64_t* a, uint64_t* b, int n_pad, int run0) {
+  const int tid = threadIdx.x;
   for (int w = run0; w < n_pad; w <<= 1) {
-    for (int i = threadIdx.x; i < n_pad; i += SCH_THREADS) {
-      const uint64_t x = a[i];
-      const int base = i & ~(2 * w - 1);
-      const int own = i & (w - 1);
-      const uint64_t* other = a + base + ((i & w) ? 0 : w);
-      // rank of x in the partner run (elements below it), by halving steps
-      int lo = 0;
-      for (int step = w >> 1; step > 0; step >>= 1) lo += other[lo + step - 1] < x ? step : 0;
-      lo += other[lo] < x ? 1 : 0;
-      b[base + own + lo] = x;
+    uint64_t x[EPT];
+    int lo[EPT], oth[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = tid + e * SCH_THREADS;
+      lo[e] = 0;
+      oth[e] = 0;
+      x[e] = 0;
+      if (i < n_pad) {
+        x[e] = a[i];
+        oth[e] = (i & ~(2 * w - 1)) + ((i & w) ? 0 : w);  // start of the partner run
+      }
+    }
+    for (int step = w >> 1; step > 0; step >>= 1) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e)
+        if (tid + e * SCH_THREADS < n_pad) lo[e] += a[oth[e] + lo[e] + step - 1] < x[e] ? step : 0;
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int i = tid + e * SCH_THREADS;
+      if (i < n_pad) {
+        lo[e] += a[oth[e] + lo[e]] < x[e] ? 1 : 0;
+        b[(i & ~(2 * w - 1)) + (i & (w - 1)) + lo[e]] = x[e];
+      }
     }
     __syncthreads();
     uint64_t* t = a;
@@ -373,6 +445,13 @@ __device__ uint64_t* merge_runs(uint64_t* a, uint64_t* b, int n_pad, int run0) {
     b = t;
   }
   return a;
+}
+
+__device__ uint64_t* merge_runs(uint64_t* a, uint64_t* b, int n_pad, int run0) {
+  if (n_pad <= SCH_THREADS) return merge_runs_t<1>(a, b, n_pad, run0);
+  if (n_pad <= 2 * SCH_THREADS) return merge_runs_t<2>(a, b, n_pad, run0);
+  if (n_pad <= 4 * SCH_THREADS) return merge_runs_t<4>(a, b, n_pad, run0);
+  return merge_runs_t<8>(a, b, n_pad, run0);
 }
 
 // slots of the shared-memory schedule: one run of R slots per request, the
@@ -415,25 +494,31 @@ __device__ __forceinline__ void block_argmax_f64(double& v, int& i, double* smv,
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_args a, const uint32_t* __restrict__ k0,
+__global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_args a, int n_pad,
+                                                                  const __grid_constant__ DfTable tab,
+                                                                  const uint32_t* __restrict__ k0,
                                                                   const uint32_t* __restrict__ v0,
                                                                   const uint32_t* __restrict__ k1,
-                                                                  const uint32_t* __restrict__ v1, int n_pad) {
-  // [n_pad] slots, [n_pad] scratch, [B (1 + gamma) + 1] SPS table, [B] l_r
+                                                                  const uint32_t* __restrict__ v1, int fused) {
+  // [n_pad] slots, [n_pad] scratch (first holding the calibrated confidences),
+  // [B (1 + gamma) + 1] SPS table, [B] l_r
   extern __shared__ uint64_t kv[];
   uint64_t* kv2 = kv + n_pad;
   const int B = a.B, G = a.gamma;
   double* s_sps = reinterpret_cast<double*>(kv2 + n_pad);
   int* s_ell = reinterpret_cast<int*>(s_sps + B * (1 + G) + 1);
+  float* s_c = reinterpret_cast<float*>(kv2);  // [B gamma] c', until the merge reuses kv2
   __shared__ uint32_t sm_u[40];
   __shared__ long long sm_l[40];
   __shared__ double sm_v[32];
   __shared__ int sm_i[32];
   __shared__ int s_first;
   __shared__ double s_theta_best;
+  __shared__ StsConsts sc;
 
   const int tid = threadIdx.x;
   const int R = sched_run_len(G);
+  sts_consts_init(sc, a.sts_temp, G, tab);
   // the flatten's inputs for this thread's request, loaded now so that their
   // latency overlaps the sort (the later stores could alias them, so the
   // compiler would not hoist the loads itself)
@@ -449,28 +534,54 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   for (int r = tid; r < B; r += SCH_THREADS) s_ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
   if (a.mode != DSPARK_SCHED_OFF)
     for (int i = tid; i <= B * (1 + G); i += SCH_THREADS) s_sps[i] = a.sps[i];
-  // one sorted run per request in kv, padded; returns the number of candidates
-  auto load_runs = [&](const uint32_t* kk, const uint32_t* vv) {
+  __syncthreads();  // the STS constants
+  // c' of every candidate, then one sorted run per request in kv (a request's
+  // keys only grow along its prefix, so each run is sorted), padded; returns
+  // the number of candidates (a > 0)
+  auto build_runs = [&](const float* z, bool write_surv, const uint32_t* kk, const uint32_t* vv) {
+    const int n = B * G;
+    if (!fused) {
+      // keys from k_sched_prep (more candidates than one SM calibrates quickly)
+      uint32_t ncand_local = 0;
+      for (int i = tid; i < n_pad; i += SCH_THREADS) {
+        const int r = i / R, j = i - r * R;
+        uint64_t e = (0xFFFFFFFFull << 32) | (0x80000000u + (uint32_t)i);
+        if (r < B && j < G) {
+          const uint32_t key = kk[r * G + j];
+          ncand_local += key != 0xFFFFFFFFu;
+          e = ((uint64_t)key << 32) | vv[r * G + j];
+        }
+        kv[i] = e;
+      }
+      uint32_t nc;
+      block_excl_scan_u32(ncand_local, sm_u, nc);
+      return nc;
+    }
+    for (int i = tid; i < n; i += SCH_THREADS) s_c[i] = sts_conf(sc, z[i], i % G);
+    __syncthreads();
     uint32_t ncand_local = 0;
     for (int i = tid; i < n_pad; i += SCH_THREADS) {
       const int r = i / R, j = i - r * R;
       // padding sorts after every candidate and non-candidate, each slot distinct
       uint64_t e = (0xFFFFFFFFull << 32) | (0x80000000u + (uint32_t)i);
       if (r < B && j < G) {
-        const uint32_t key = kk[r * G + j];
+        // a_{r,j}: the left-to-right fp32 product, the same chain for every j
+        float run = 1.f;
+        for (int jj = 0; jj <= j; ++jj) run = __fmul_rn(run, s_c[r * G + jj]);
+        const uint32_t key = run > 0.f ? ~__float_as_uint(run) : 0xFFFFFFFFu;
         ncand_local += key != 0xFFFFFFFFu;
-        e = ((uint64_t)key << 32) | vv[r * G + j];
+        e = ((uint64_t)key << 32) | (uint32_t)(r * G + j);
+        if (write_surv && a.surv) a.surv[r * G + j] = run;
       }
       kv[i] = e;
     }
     uint32_t nc;
-    block_excl_scan_u32(ncand_local, sm_u, nc);  // ends with __syncthreads
+    block_excl_scan_u32(ncand_local, sm_u, nc);  // ends with __syncthreads: kv2 (c') is free again
     return nc;
   };
-
   if (a.mode == DSPARK_SCHED_ASYNC_TOPK) {
     // ---- capacity: the best prefix of the earlier step's sorted path (global search) ----
-    const int nprev = (int)load_runs(k1, v1);
+    const int nprev = (int)build_runs(a.conf_logit_prev, false, k1, v1);
     const uint64_t* prv = merge_runs(kv, kv2, n_pad, R);
     const int chp = (nprev + SCH_THREADS - 1) / SCH_THREADS;
     const int p_lo = min(tid * chp, nprev), p_hi = min(p_lo + chp, nprev);
@@ -491,7 +602,7 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     block_argmax_f64(bv, bi, sm_v, sm_i);
     const int K = bi;
     // ---- this step: its candidates in order, the first min(K, n) admitted ----
-    const int ncur = (int)load_runs(k0, v0);  // every read of the earlier path ended before the scan's barriers
+    const int ncur = (int)build_runs(a.conf_logit, true, k0, v0);  // every read of the earlier path ended before the scan's barriers
     const uint64_t* cur = merge_runs(kv, kv2, n_pad, R);
     const int nadm = min(K, ncur);
     long long sl = 0;
@@ -504,7 +615,7 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     block_excl_scan_i64(sl, sm_l, sadm);
     if (tid == 0) *a.theta_best = ((double)B + (double)sadm * kFix52) * s_sps[B + nadm];
   } else if (a.mode != DSPARK_SCHED_OFF) {
-    const uint32_t ncand = load_runs(k0, v0);
+    const uint32_t ncand = build_runs(a.conf_logit, true, k0, v0);
     // ---- 2. one sorted run: ascending (key, index) = descending a, ties by index ----
     const uint64_t* srt = merge_runs(kv, kv2, n_pad, R);
     // ---- 3. Theta along the sorted path, first non-increase ----
@@ -548,6 +659,7 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     __syncthreads();
     if (tid == 0) *a.theta_best = s_theta_best;
   } else {
+    if (a.surv && fused) build_runs(a.conf_logit, true, k0, v0);  // the survival products only
     if (tid == 0) *a.theta_best = 0.0;
   }
   __syncthreads();
@@ -617,18 +729,26 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
   // every refusal comes before the first launch
   if (a.mode == DSPARK_SCHED_ASYNC_TOPK && !schedule_async_supported(a.B, a.gamma)) return cudaErrorNotSupported;
-  const int rb = PREP_THREADS / a.gamma;
-  k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1);
   const int n_pad = sched_slots(a.B, a.gamma);
   const size_t smem = schedule_smem_bytes(a.B, a.gamma);
   if (n_pad <= kSmemSortMax && smem <= kSmemSchedMax) {
+    // up to kFusedKeys candidates one launch does everything (confidences, keys,
+    // sort, Theta, flatten); above, k_sched_prep calibrates on many SMs first
     if (const cudaError_t ae = ensure_smem_limit((const void*)k_schedule_smem, (int)kSmemSchedMax); ae != cudaSuccess)
       return ae;
-    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, k0, v0, k1, v1, n_pad);
+    const int fused = (int64_t)a.B * a.gamma <= kFusedKeys ? 1 : 0;
+    if (!fused) {
+      const int rb = PREP_THREADS / a.gamma;
+      k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1, df_table());
+    }
+    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, n_pad, df_table(), k0, v0, k1, v1, fused);
+    count_launches(fused ? 1 : 2);
   } else {
+    const int rb = PREP_THREADS / a.gamma;
+    k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1, df_table());
     k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
+    count_launches(2);
   }
-  count_launches(2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.n_verify_host) e = cudaMemcpyAsync(a.n_verify_host, a.n_verify, sizeof(int32_t), cudaMemcpyDeviceToHost, s);

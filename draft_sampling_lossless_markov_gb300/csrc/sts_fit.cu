@@ -56,81 +56,7 @@ namespace dspark {
 
 namespace {
 
-// ln2/64 = kC1 + kC2 + kC3 (kC1 has 11 significant bits: n kC1 is exact for n < 2^13)
-constexpr float kC1 = 0x1.62cp-7f;
-constexpr float kC2 = 0x1.217f7ep-18f;
-constexpr float kC3 = -0x1.c610cap-43f;
-constexpr float kInvC = 0x1.715476p+6f;  // 64/ln2, only picks n
-constexpr float kDfMaxArg = 64.f;
-
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-// |a| >= |b|
-__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  e = __fsub_rn(b, __fsub_rn(s, a));
-}
-__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
-  p = __fmul_rn(a, b);
-  e = fmaf(a, b, -p);
-}
-
-// c' = fp32(sigmoid(z / tau)); (bh, bl) = 1/tau as a double-float, rt = fp64 1/tau,
-// T[j] = 2^(-j/64) as (hi, lo)
-__device__ __forceinline__ float sigmoid_df(float z, float tau, float bh, float bl, double rt,
-                                            const float2* __restrict__ T) {
-  float th, tl;
-  two_prod(z, bh, th, tl);
-  tl = fmaf(z, bl, tl);
-  const bool neg = th < 0.f;
-  const float ah = fabsf(th), al = neg ? -tl : tl;
-  if (!(ah <= kDfMaxArg)) return sts_sigmoid(z, (double)tau, rt);  // large or non-finite
-  const float nf = rintf(ah * kInvC);
-  const int n = (int)nf;
-  // r = |t| - n ln2/64 as a double-float
-  const float r1 = fmaf(-nf, kC1, ah);  // exact
-  float p, pe;
-  two_prod(nf, kC2, p, pe);
-  float rh, rl;
-  two_sum(r1, -p, rh, rl);
-  rl = __fadd_rn(__fsub_rn(rl, pe), __fsub_rn(al, __fmul_rn(nf, kC3)));
-  fast_two_sum(rh, rl, rh, rl);
-  // e^-r = 1 - r + r^2/2 + c3,  c3 = r^3 (-1/6 + r/24 - r^2/120)
-  float sq, sqe;
-  two_prod(rh, rh, sq, sqe);
-  sqe = fmaf(2.f * rh, rl, sqe);
-  const float c3 = __fmul_rn(__fmul_rn(rh, sq), fmaf(rh, fmaf(rh, -1.f / 120.f, 1.f / 24.f), -1.f / 6.f));
-  float Ph, Pl, q2, q2e;
-  fast_two_sum(1.f, -rh, Ph, Pl);
-  fast_two_sum(Ph, 0.5f * sq, q2, q2e);
-  Pl = __fadd_rn(__fadd_rn(Pl, q2e), __fadd_rn(__fsub_rn(0.5f * sqe, rl), c3));
-  Ph = q2;
-  // w = e^-|t| = 2^-(n>>6) T[n & 63] (Ph + Pl)
-  const float2 Tj = T[n & 63];
-  float wh, wl;
-  two_prod(Tj.x, Ph, wh, wl);
-  wl = fmaf(Tj.x, Pl, fmaf(Tj.y, Ph, wl));
-  const float sc = __int_as_float((127 - (n >> 6)) << 23);  // 2^-(n>>6), n>>6 <= 92
-  wh = __fmul_rn(wh, sc);
-  wl = __fmul_rn(wl, sc);
-  // 1 / (1 + w): y0 (1 + e + e^2) with e = 1 - (1 + w) y0
-  float dh, dl;
-  fast_two_sum(1.f, wh, dh, dl);
-  dl = __fadd_rn(dl, wl);
-  float y0;  // |1 - dh y0| <= 2^-22; the correction below absorbs it
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(dh));
-  const float e = __fsub_rn(fmaf(-dh, y0, 1.f), __fmul_rn(dl, y0));
-  const float ye = __fmul_rn(y0, fmaf(e, e, e));
-  if (!neg) return __fadd_rn(y0, ye);
-  // w / (1 + w)
-  float ph, pl;
-  two_prod(wh, y0, ph, pl);
-  pl = fmaf(wh, ye, fmaf(wl, y0, pl));
-  return __fadd_rn(ph, pl);
-}
+using namespace sts_df;
 
 constexpr int SF_THREADS = 128;
 constexpr int SF_SLAB = 256;     // blocks staged in shared memory at a time

@@ -43,9 +43,17 @@ def _spread(B, n):
     return [int(i) for i in idx]
 
 
-def _draft_sample_parity(name, subset, min_tokens):
+def _draft_sample_parity(name, subset, min_tokens, sampling_seeds=(None,)):
+    tot = 0
+    for ss in sampling_seeds:
+        st = _draft_sample_parity_once(name, subset, ss)
+        tot += st["n_tokens_compared"]
+    assert tot >= min_tokens, (name, tot)
+
+
+def _draft_sample_parity_once(name, subset, sampling_seed):
     wl = synth.get_workload(name)
-    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    inp = synth.make_inputs(wl, "cuda", with_target=False, sampling_seed=sampling_seed)
     out, ws = gpu_draft(inp)
     check_no_error(ws)
     idx = torch.tensor(subset, device="cuda")
@@ -62,23 +70,23 @@ def _draft_sample_parity(name, subset, min_tokens):
     assert float((s - 1).abs().max()) < 5e-4
     c = out["conf"]
     assert float(c.min()) >= 0 and float(c.max()) <= 1
-    print(f"{name}: {st['n_tokens_compared']} draft tokens compared bit-exact over {len(subset)} requests "
-          f"({st['n_exempt_requests']} requests met a draw inside the margin)")
-    assert st["n_tokens_compared"] >= min_tokens, st
+    print(f"{name} (sampling seed {sampling_seed}): {st['n_tokens_compared']} draft tokens compared bit-exact over "
+          f"{len(subset)} requests ({st['n_exempt_requests']} requests met a draw inside the margin)")
     return st
 
 
-@pytest.mark.parametrize("name,n_req,min_tokens", [
-    ("sweep_B256_g7", 64, 150),     # the headline point: both M-tiles, 64 requests
-    ("qwen3_8b_sched", 48, 150),    # gamma 15, T 0.7
-    ("deepseek_vocab", 64, 150),    # V 129280, even request ids greedy, odd sampled; 8 M-tiles
-    ("sweep_B1_g7", 1, 1),          # one request
-    ("sweep_B8_g7", 8, 20),
-    ("sweep_B4096_g7", 48, 100),    # 32 M-tiles
+@pytest.mark.parametrize("name,n_req,min_tokens,n_seeds", [
+    ("sweep_B256_g7", 64, 150, 1),    # the headline point: both M-tiles, 64 requests
+    ("qwen3_8b_sched", 48, 150, 1),   # gamma 15, T 0.7
+    ("deepseek_vocab", 64, 150, 1),   # V 129280, even request ids greedy, odd sampled; 8 M-tiles
+    ("sweep_B1_g7", 1, 12, 6),        # one request: six sampling seeds (six draw sequences)
+    ("sweep_B8_g7", 8, 40, 2),
+    ("sweep_B4096_g7", 48, 100, 1),   # 32 M-tiles
 ])
-def test_draft_full_size(name, n_req, min_tokens):
+def test_draft_full_size(name, n_req, min_tokens, n_seeds):
     wl = synth.get_workload(name)
-    _draft_sample_parity(name, _spread(wl.B, n_req), min_tokens)
+    seeds = (None,) if n_seeds == 1 else tuple(1000 + i for i in range(n_seeds))
+    _draft_sample_parity(name, _spread(wl.B, n_req), min_tokens, seeds)
 
 
 def test_draft_deepseek_vocab_covers_greedy_and_sampled_requests():
