@@ -195,9 +195,10 @@ __device__ __forceinline__ void team_sync(int team) {
 // 8-element groups tl, tl + 128, .. of h_k and w_h (H % 8 == 0), warp 0's lane
 // l also elements 8 l .. 8 l + 7 of W1[x] and w_e (r <= 256).  The first
 // kConfPer groups of each lane are loaded when the select of the row begins
-// (conf_issue) and added after the levels pass (conf_partial), so that no load
-// of the confidence waits on the select's critical path; for H > 4096 the
-// rest are loaded there.  Nothing in the kernel reads the confidences.
+// (conf_issue) and added after the crossing chunk's recompute (conf_partial),
+// so that no load of the confidence waits on the select's critical path; for
+// H > 4096 the rest are loaded there.  Nothing in the kernel reads the
+// confidences.
 constexpr int kConfPer = 4;
 struct ConfLoads {
   uint4 h[kConfPer], w[kConfPer];
@@ -460,7 +461,7 @@ __device__ void chunk_dot(const Params& p, int x, int cstar, int tw, int lane, f
 // dot products, y = l c, w = 2^(y - m); the token is the first column whose
 // running sum from sbase exceeds u S, else the chunk's last column with
 // positive weight.  Writes the token and prefetches its W1 row.
-__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red, uint32_t upair) {
+__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red) {
   constexpr unsigned FULL = 0xffffffffu;
   const int b = rec->b;
   const int v = rec->cstar * CW + 2 * lane;
@@ -468,6 +469,8 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   const float c = row_scale(p.temp[b]);
   float w0 = 0.f, w1 = 0.f;
   if (in) {
+    const unsigned upair =
+        __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)b * p.G + k) * p.V + (size_t)rec->cstar * CW + 2 * lane));
     const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&upair);
     float d0 = 0.f, d1 = 0.f;
     for (int w = 0; w < kTeamWarps; ++w) {
@@ -828,25 +831,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ConfLoads cl;
         conf_issue(p, rb, k, tw, lane, cl);
         team_levels(p, rb, k, team, tw, lane, rec, xw);
+        team_sync(team);
+        const int cstar = rec->cstar;
+        if (cstar >= 0) {
+          chunk_dot(p, rec->x, cstar, tw, lane, red);
+        }
+        // this warp's share of the confidence (its loads have landed by now)
         {
           const float zp = conf_partial(p, rb, k, tw, lane, cl);
           if (lane == 0) cz[tw] = zp;
         }
         team_sync(team);
+        if (cstar >= 0 && tw == 0) chunk_walk(p, rec, k, lane, red);
         if (tw == 1 && lane == 0) {
           const float z = (cz[0] + cz[1]) + (cz[2] + cz[3]);
           p.conf_logit[(size_t)rb * G + k] = z;
           p.conf[(size_t)rb * G + k] = 1.f / (1.f + expf(-z));
-        }
-        const int cstar = rec->cstar;
-        if (cstar >= 0) {
-          // the walking warp fetches the chunk's U pairs before the recompute
-          uint32_t upair = 0u;
-          if (tw == 0 && cstar * CW + 2 * lane < p.V)
-            upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)rb * G + k) * p.V + cstar * CW + 2 * lane));
-          chunk_dot(p, rec->x, cstar, tw, lane, red);
-          team_sync(team);
-          if (tw == 0) chunk_walk(p, rec, k, lane, red, upair);
         }
         // the record, exchange words and partial logits are free for the next row
         team_sync(team);
