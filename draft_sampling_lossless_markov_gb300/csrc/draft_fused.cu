@@ -71,6 +71,7 @@ constexpr uint32_t kAccCol0 = 2 * kESlotCols;
 constexpr int kTailBytes = 1024;
 constexpr int kTQ = 16;                        // tile-queue slots (the producer runs < 8 tiles ahead)
 constexpr int kMaxE = 20;                      // chunk partials per lane in the select (V <= 20 * 128 * 64)
+constexpr int kTailDiv = 5;                    // the last fifth of a sweep's claims is kept in L2
 constexpr size_t kSmemBytes =
     1024 + NW * (size_t)kW2Stage + NU * (size_t)kUStage + (size_t)kEpiWarps * kStagingPerWarp + kTailBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -192,36 +193,28 @@ __device__ __forceinline__ void team_sync(int team) {
 // Confidence of position k of row b, split over a team's four warps
 // ([DSpark] 方法细节, 置信度头): z = w_h . h_k + w_e . W1[x] with x = x_{k-1}
 // (the anchor for k = 0), c = sigmoid(z).  The team's lane tl takes the
-// 8-element groups tl, tl + 128, .. of h_k and w_h (H % 8 == 0), warp 0's lane
+// 8-element groups tl, tl + 128, .. of h_k and w_h (H % 8 == 0), warp 1's lane
 // l also elements 8 l .. 8 l + 7 of W1[x] and w_e (r <= 256).  The first
-// kConfPer groups of each lane are loaded when the select of the row begins
-// (conf_issue) and added after the crossing chunk's recompute (conf_partial),
-// so that no load of the confidence waits on the select's critical path; for
-// H > 4096 the rest are loaded there.  Nothing in the kernel reads the
+// kConfPer groups of h_k (read once, from HBM) are loaded when the select of
+// the row begins (conf_issue), with no address that waits on another load;
+// after the crossing chunk's recompute each warp adds its share with w_h (read
+// by every row: from L2) while the walk publishes the token (conf_partial), so
+// that no load of the confidence waits on the select's critical path; for
+// H > 4096 the rest of h_k is loaded there.  Nothing in the kernel reads the
 // confidences.
 constexpr int kConfPer = 4;
 struct ConfLoads {
-  uint4 h[kConfPer], w[kConfPer];
-  uint4 e, we;  // W1[x] and w_e (team warp 0)
+  uint4 h[kConfPer];
 };
 
 __device__ __forceinline__ void conf_issue(const Params& p, int b, int k, int tw, int lane, ConfLoads& L) {
   const int tl = tw * 32 + lane;
   const uint4* hq = reinterpret_cast<const uint4*>(p.h + ((size_t)b * p.G + k) * p.H);
-  const uint4* wq = reinterpret_cast<const uint4*>(p.w);
   const int n8 = p.H / 8;
 #pragma unroll
   for (int u = 0; u < kConfPer; ++u) {
     const int i = tl + u * kTeamWarps * 32;
     L.h[u] = i < n8 ? __ldcs(hq + i) : make_uint4(0u, 0u, 0u, 0u);
-    L.w[u] = i < n8 ? __ldg(wq + i) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  L.e = L.we = make_uint4(0u, 0u, 0u, 0u);
-  if (tw == 0 && 8 * lane < p.r) {
-    int x = (k == 0) ? p.anchor[b] : __ldcg(&p.tokens[(size_t)b * p.G + k - 1]);
-    if (x < 0 || x >= p.V) x = 0;
-    L.e = *reinterpret_cast<const uint4*>(p.W1 + (size_t)x * p.r + 8 * lane);
-    L.we = __ldg(reinterpret_cast<const uint4*>(p.w + p.H + 8 * lane));
   }
 }
 
@@ -237,20 +230,38 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b, float
   return acc;
 }
 
-// This warp's share of z, summed over the warp (every lane holds it).
-__device__ __forceinline__ float conf_partial(const Params& p, int b, int k, int tw, int lane, const ConfLoads& L) {
+// This warp's share of z, summed over the warp (every lane holds it); team
+// warp 1 also adds w_e . W1[x] (x = x_{k-1}; the row is in L2: the walk that
+// chose x prefetched it).
+__device__ __forceinline__ float conf_partial(const Params& p, int b, int k, int tw, int lane, const ConfLoads& L,
+                                              int x) {
   const int tl = tw * 32 + lane;
   const int n8 = p.H / 8;
   float zh = 0.f;
+  {
+    // w_h is read by every row and position: it stays in L2
+    const uint4* wq = reinterpret_cast<const uint4*>(p.w);
+    uint4 wv[kConfPer];
 #pragma unroll
-  for (int u = 0; u < kConfPer; ++u) zh = dot8_bf16(L.h[u], L.w[u], zh);
+    for (int u = 0; u < kConfPer; ++u) {
+      const int i = tl + u * kTeamWarps * 32;
+      wv[u] = i < n8 ? __ldg(wq + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kConfPer; ++u) zh = dot8_bf16(L.h[u], wv[u], zh);
+  }
   if (n8 > kConfPer * kTeamWarps * 32) {
     const uint4* hq = reinterpret_cast<const uint4*>(p.h + ((size_t)b * p.G + k) * p.H);
     const uint4* wq = reinterpret_cast<const uint4*>(p.w);
     for (int i = tl + kConfPer * kTeamWarps * 32; i < n8; i += kTeamWarps * 32)
       zh = dot8_bf16(__ldcs(hq + i), __ldg(wq + i), zh);
   }
-  zh = dot8_bf16(L.we, L.e, zh);  // zero outside warp 0
+  if (tw == 1 && 8 * lane < p.r) {
+    if (x < 0 || x >= p.V) x = 0;
+    const uint4 e = *reinterpret_cast<const uint4*>(p.W1 + (size_t)x * p.r + 8 * lane);
+    const uint4 we = __ldg(reinterpret_cast<const uint4*>(p.w + p.H + 8 * lane));
+    zh = dot8_bf16(we, e, zh);
+  }
   return warp_sum(zh);
 }
 
@@ -461,7 +472,7 @@ __device__ void chunk_dot(const Params& p, int x, int cstar, int tw, int lane, f
 // dot products, y = l c, w = 2^(y - m); the token is the first column whose
 // running sum from sbase exceeds u S, else the chunk's last column with
 // positive weight.  Writes the token and prefetches its W1 row.
-__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red) {
+__device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, const float* red, uint32_t upair) {
   constexpr unsigned FULL = 0xffffffffu;
   const int b = rec->b;
   const int v = rec->cstar * CW + 2 * lane;
@@ -469,8 +480,6 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   const float c = row_scale(p.temp[b]);
   float w0 = 0.f, w1 = 0.f;
   if (in) {
-    const unsigned upair =
-        __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)b * p.G + k) * p.V + (size_t)rec->cstar * CW + 2 * lane));
     const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&upair);
     float d0 = 0.f, d1 = 0.f;
     for (int w = 0; w < kTeamWarps; ++w) {
@@ -595,15 +604,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
+      // L2 policies: a sweep's last kTailDiv-th of claims are the next sweep's
+      // first (the claim order alternates), so their W2 tile and the U rows of
+      // their S item (read again by the next sweep's W item) are kept
+      // (evict-last); other U rows are read for the last time (evict-first);
+      // other W2 tiles need to last only until the other M-tile's CTA has read
+      // them (evict-normal)
       const uint64_t pol_last = ptx::policy_evict_last();
       const uint64_t pol_first = ptx::policy_evict_first();
+      const uint64_t pol_normal = ptx::policy_evict_normal();
+      const unsigned tail0 = (unsigned)(p.ntiles - p.ntiles / kTailDiv);
       int iw = 0, iu = 0, jq = 0;
       bool ok = true;
       for (int q = 0; q < G + p.write_pd && ok; ++q) {
         const int s = q - 1;
         const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
         unsigned* claim = p.sched + (size_t)q * p.n_mtiles + m_tile;
-        int n = tile_of(atomicAdd(claim, 1u), q);
+        unsigned ci = atomicAdd(claim, 1u);  // claim index of the tile n
+        int n = tile_of(ci, q);
         while (ok) {
           // hand the tile (or the end of the sweep) to the MMA issuer and the
           // epilogue; the arrive releases the queue entry
@@ -612,7 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++jq;
           if (n < 0) break;
           const int v0 = n * BN;
-          n = tile_of(atomicAdd(claim, 1u), q);  // the next claim, in flight during the loads
+          const bool keep = ci >= tail0;
+          ci = atomicAdd(claim, 1u);  // the next claim, in flight during the loads
+          n = tile_of(ci, q);
           for (int kc = 0; kc < nkc; ++kc, ++iw) {
             const int st = iw % NW;
             if (!ptx::mbar_wait(&emptyW[st], ((iw / NW) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
@@ -622,7 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* dst = sW + st * kW2Stage;
             ptx::mbar_expect_tx(&fullW[st], kW2Stage);
             for (int c = 0; c < NCH; ++c)
-              ptx::tma_load_2d(dst + c * (KC * CW * 2), &tmW2, &fullW[st], v0 + c * CW, kc * KC, pol_last);
+              ptx::tma_load_2d(dst + c * (KC * CW * 2), &tmW2, &fullW[st], v0 + c * CW, kc * KC,
+                               keep ? pol_last : pol_normal);
           }
           for (int item = 0; item < 2 && ok; ++item) {
             if (item == 0 ? !hasW : !hasS) continue;
@@ -635,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_expect_tx(&fullU[su], kUStage);
             for (int c = 0; c < NCH; ++c)
               ptx::tma_load_3d(sU + su * kUStage + c * kUChunk, &tmU, &fullU[su], v0 + c * CW, kk, row_base,
-                               pol_first);
+                               (keep && item == 1) ? pol_last : pol_first);
             ++iu;
           }
         }
@@ -741,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool sampled = T_ > 0.f;
     const float c = row_scale(T_);
     uint8_t* stg = sStg + ew * kStagingPerWarp;
+    const uint64_t pol_keep = ptx::policy_evict_last();
     unsigned nbar = 0;
     int it = 0, iu = 0, jq = 0;
     bool alive = true;
@@ -833,23 +855,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         team_levels(p, rb, k, team, tw, lane, rec, xw);
         team_sync(team);
         const int cstar = rec->cstar;
+        uint32_t upair = 0u;
         if (cstar >= 0) {
+          // the walking warp fetches the chunk's U pairs (prefetched to L2 by the
+          // levels pass) with the recompute's loads
+          if (tw == 0 && cstar * CW + 2 * lane < p.V)
+            upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)rb * G + k) * p.V + cstar * CW + 2 * lane));
           chunk_dot(p, rec->x, cstar, tw, lane, red);
+          team_sync(team);
+          if (tw == 0) chunk_walk(p, rec, k, lane, red, upair);
         }
-        // this warp's share of the confidence (its loads have landed by now)
+        // this warp's share of the confidence, off the walk's path: warps 1-3
+        // while warp 0 walks, warp 0 after it (the loads have landed by now)
         {
-          const float zp = conf_partial(p, rb, k, tw, lane, cl);
+          const float zp = conf_partial(p, rb, k, tw, lane, cl, rec->x);
           if (lane == 0) cz[tw] = zp;
         }
+        // the record, exchange words and partial logits are free for the next row
         team_sync(team);
-        if (cstar >= 0 && tw == 0) chunk_walk(p, rec, k, lane, red);
         if (tw == 1 && lane == 0) {
           const float z = (cz[0] + cz[1]) + (cz[2] + cz[3]);
           p.conf_logit[(size_t)rb * G + k] = z;
           p.conf[(size_t)rb * G + k] = 1.f / (1.f + expf(-z));
         }
-        // the record, exchange words and partial logits are free for the next row
-        team_sync(team);
       }
       // every warp is done with the scratch before the staging area is reused
       epi_sync();
@@ -984,7 +1012,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               part = make_float2(av, __int_as_float(ai));
             }
-            if (v0 < p.V && vrow) p.part[(size_t)b * p.pstride + (v0 / CW) % p.ept * 128 + (v0 / CW) / p.ept] = part;
+            // the select reads the partials right after the sweep: keep them in L2
+            // (evict-last) through the sweep's streams (evict-first)
+            if (v0 < p.V && vrow)
+              ptx::st_global_hint(&p.part[(size_t)b * p.pstride + (v0 / CW) % p.ept * 128 + (v0 / CW) / p.ept], part,
+                                  pol_keep);
           } else {
             // W item: p_d^s = 2^(l c - m) / S (one-hot for greedy rows); columns
             // past V are computed but not stored (the TMA store clips them)
