@@ -50,6 +50,11 @@ def test_draft_tiny(temp, seed):
     (130, 5, 8200, 128, 16, "bf16"),   # two M-tiles (the second with 2 rows), an 8-column last tile
     (40, 3, 1024, 256, 8, "bf16"),     # 8 vocabulary tiles for many CTAs: most claim no tile
     (260, 16, 2048, 192, 32, "bf16"),  # gamma 16, rank 192, three M-tiles
+    # small batches on the tensor-core path (one M-tile, most lane quadrants idle)
+    (1, 3, 8200, 256, 16, "bf16"),     # one row, an 8-column last tile
+    (2, 5, 1032, 128, 32, "bf16"),     # two rows, rank 128, 9 tiles
+    (3, 4, 4104, 64, 24, "bf16"),      # three rows, rank 64
+    (4, 7, 16384, 256, 64, "bf16"),    # four rows
 ])
 def test_draft_ragged_shapes(B, G, V, r, H, dt):
     wl = synth.Workload("ragged", B, G, V, H, r, dt, "mixed", synth.SCHED_GREEDY, "tiny", seed=5)
