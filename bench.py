@@ -370,88 +370,117 @@ def sched(T, ws, conf_logit, inp, sps_dev, anchor, tokens, **kw):
 
 
 def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
-    """Same metric through the public API with HOST buffers: each step copies the
-    step's inputs from pinned host memory (U, h and the per-request scalars),
-    runs the draft and the scheduler, packs the kept target rows straight from
-    the pinned host buffer by the marker tensor (dspark_pack_rows: only the N_v
-    kept rows cross the host link), verifies, and reads the result back.  With
-    cap-accept every row is verified: the whole target buffer is copied on a
-    second stream while the draft runs."""
+    """Same metric through the public API with HOST buffers.  Every step copies its
+    inputs from pinned host memory (U, h and the per-request scalars) into one of
+    two device input buffers on a copy stream, runs the draft and the scheduler
+    on the compute stream once its copy is done, packs the kept target rows
+    straight from the pinned host buffer by the marker tensor (dspark_pack_rows:
+    only the N_v kept rows cross the host link), verifies, and reads its result
+    back into pinned memory.  The copies of step i + 1 overlap the compute of
+    step i, as a serving loop would run them.  With cap-accept every row is
+    verified: the whole target buffer is copied as well."""
     import torch
     B, G, V = wl.B, wl.gamma, wl.V
     h_U = inp["U"].cpu().pin_memory()
     h_h = inp["h"].cpu().pin_memory()
     h_small = {k: inp[k].cpu().pin_memory() for k in ("anchor", "temp", "req_id")}
     h_tgt = inp["target"].cpu().pin_memory()  # [B, G+1, V]: the target model's rows live on the host here
-    d_U = torch.empty_like(inp["U"])
-    d_h = torch.empty_like(inp["h"])
-    d_small = {k: torch.empty_like(inp[k]) for k in h_small}
+    nbuf = 2
+    d_U = [torch.empty_like(inp["U"]) for _ in range(nbuf)]
+    d_h = [torch.empty_like(inp["h"]) for _ in range(nbuf)]
+    d_small = [{k: torch.empty_like(inp[k]) for k in h_small} for _ in range(nbuf)]
+    cap_accept = args.verify == "cap_accept"
     # cap-accept verifies every row: the whole target buffer moves to the device
-    d_tgt = torch.empty_like(inp["target"]) if args.verify == "cap_accept" else None
-    tgt_flat = d_tgt.reshape(-1, V) if d_tgt is not None else None
+    d_tgt = [torch.empty_like(inp["target"]) for _ in range(nbuf)] if cap_accept else None
     cap = B * (G + 1)
     rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
-    h_nv = torch.empty(1, dtype=torch.int32).pin_memory()
-    h_out = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
-    h_nout = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_nv = [torch.empty(1, dtype=torch.int32).pin_memory() for _ in range(nbuf)]
+    h_out = [torch.empty((B, G + 1), dtype=torch.int32).pin_memory() for _ in range(nbuf)]
+    h_nout = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(nbuf)]
     esz = inp["U"].element_size()
     full_offsets = (torch.arange(B + 1, device=dev, dtype=torch.int32) * (G + 1)).contiguous()
     full_ell = torch.full((B,), G, dtype=torch.int32, device=dev)
-    side = torch.cuda.Stream(device=dev)
-    tgt_ready = torch.cuda.Event()
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(nbuf)]
+    consumed = [torch.cuda.Event() for _ in range(nbuf)]
+    issued = [False] * nbuf
 
-    cap_accept = args.verify == "cap_accept"
-
-    def step():
-        if cap_accept:
-            with torch.cuda.stream(side):
-                d_tgt.copy_(h_tgt, non_blocking=True)
-                tgt_ready.record(side)
-        with torch.cuda.stream(stream):
-            d_U.copy_(h_U, non_blocking=True)
-            d_h.copy_(h_h, non_blocking=True)
-            for k in d_small:
-                d_small[k].copy_(h_small[k], non_blocking=True)
-            d = T.draft_sample(ws, d_U, inp["W1"], inp["W2"], d_h, inp["w"], d_small["anchor"], d_small["temp"],
-                               d_small["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"),
-                               rows=args.rows != "none")
-            rj = (dict(U=d_U, W1=inp["W1"], W2=inp["W2"], anchor=d_small["anchor"], pd_stat=d["pd_stat"])
-                  if args.rows == "none" else None)
-            s = sched(T, ws, d["conf_logit"], inp, sps_dev, d_small["anchor"], d["tokens"], stream=stream,
-                      n_verify_host=h_nv)
+    def step(i):
+        k = i % nbuf
+        with torch.cuda.stream(copy_stream):
+            if issued[k]:
+                copy_stream.wait_event(consumed[k])  # the compute of step i - 2 is done with buffer k
+            d_U[k].copy_(h_U, non_blocking=True)
+            d_h[k].copy_(h_h, non_blocking=True)
+            for n in h_small:
+                d_small[k][n].copy_(h_small[n], non_blocking=True)
             if cap_accept:
-                stream.wait_event(tgt_ready)
+                d_tgt[k].copy_(h_tgt, non_blocking=True)
+            copied[k].record(copy_stream)
+        issued[k] = True
+        sm = d_small[k]
+        with torch.cuda.stream(stream):
+            stream.wait_event(copied[k])
+            d = T.draft_sample(ws, d_U[k], inp["W1"], inp["W2"], d_h[k], inp["w"], sm["anchor"], sm["temp"],
+                               sm["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"),
+                               rows=args.rows != "none")
+            rj = (dict(U=d_U[k], W1=inp["W1"], W2=inp["W2"], anchor=sm["anchor"], pd_stat=d["pd_stat"])
+                  if args.rows == "none" else None)
+            s = sched(T, ws, d["conf_logit"], inp, sps_dev, sm["anchor"], d["tokens"], stream=stream,
+                      n_verify_host=h_nv[k])
+            if cap_accept:
+                v = T.verify(ws, d_tgt[k].reshape(-1, V), full_offsets, full_ell, d["tokens"], d.get("pd_rows"),
+                             d["pd_tok"], sm["temp"], sm["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"],
+                             rejection=rj)
             else:
                 # the kept rows in flattened verify order, pulled from the host
                 T.pack_rows(h_tgt, s["mark_req"], s["mark_pos"], s["n_verify"], rows, ws, stream=stream)
-            if cap_accept:
-                v = T.verify(ws, tgt_flat, full_offsets, full_ell, d["tokens"], d.get("pd_rows"), d["pd_tok"],
-                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"],
-                             rejection=rj)
-            else:
                 v = T.verify(ws, rows, s["offsets"], s["ell"], d["tokens"], d.get("pd_rows"), d["pd_tok"],
-                             d_small["temp"], d_small["req_id"], inp["seed"], stream=stream, rejection=rj)
-            h_out.copy_(v["out_tok"], non_blocking=True)
-            h_nout.copy_(v["n_out"], non_blocking=True)
-        stream.synchronize()
+                             sm["temp"], sm["req_id"], inp["seed"], stream=stream, rejection=rj)
+            h_out[k].copy_(v["out_tok"], non_blocking=True)
+            h_nout[k].copy_(v["n_out"], non_blocking=True)
+            consumed[k].record(stream)
 
-    for _ in range(max(1, min(args.warmup, 2))):
-        step()
+    nw = max(1, min(args.warmup, 2))
+    for i in range(nw):
+        step(i)
     torch.cuda.synchronize(dev)
-    n_e2e = max(1, min(args.steps, 5))
-    nv_rows = 0
+    n_e2e = max(2, min(args.steps, 8))
     t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        step()
-        nv_rows += int(h_nv[0])
+    for i in range(nw, nw + n_e2e):
+        step(i)
+    torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
     sec = (t1 - t0) / n_e2e
-    tgt_bytes = h_tgt.numel() * esz if cap_accept else nv_rows / n_e2e * V * esz
+    # the same steps one at a time (each synchronised before the next starts): no overlap
+    ser = []
+    for i in range(nw + n_e2e, nw + 2 * n_e2e):
+        s0 = time.perf_counter()
+        step(i)
+        torch.cuda.synchronize(dev)
+        ser.append(time.perf_counter() - s0)
+    # the host link's own rate: one pinned-host -> device copy of U, event-timed
+    lk = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy_stream):
+            e0.record(copy_stream)
+            d_U[0].copy_(h_U, non_blocking=True)
+            e1.record(copy_stream)
+        copy_stream.synchronize()
+        lk.append(e0.elapsed_time(e1))
+    link_gbs = h_U.numel() * h_U.element_size() / (float(np.median(lk)) * 1e-3) / 1e9
+    nv_rows = float(np.mean([int(h_nv[k][0]) for k in range(nbuf)]))
+    tgt_bytes = h_tgt.numel() * esz if cap_accept else nv_rows * V * esz
     h2d = (h_U.numel() * esz + h_h.numel() * esz + sum(t.numel() * t.element_size() for t in h_small.values())
            + tgt_bytes)
-    d2h = 4 + h_out.numel() * 4 + h_nout.numel() * 4
+    d2h = 4 + h_out[0].numel() * 4 + h_nout[0].numel() * 4
     return {"value": B * G / sec, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": n_e2e, "timer": "host wall clock around each full step (synchronised)"}
+            "steps": n_e2e, "ms_per_step": sec * 1e3, "h2d_gbs": h2d / sec / 1e9,
+            "serial_ms_per_step": float(np.median(ser)) * 1e3,
+            "link_gbs": link_gbs, "link_floor_ms": h2d / link_gbs / 1e6,
+            "timer": "host wall clock around n pipelined steps (two input buffers; step i + 1's copies overlap "
+                     "step i's compute), synchronised at both ends"}
 
 
 # ---------------------------------------------------------------------------

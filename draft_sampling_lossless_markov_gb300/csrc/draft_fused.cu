@@ -100,6 +100,7 @@ struct Params {
   float2* part;              // [B, pstride] (max, sum) of a sampled row's chunk j, (value, index) of a
                              // greedy row's, at (j % E) 128 + j / E: the select's lanes read it coalesced
   float* pd_tok;
+  float* pd_rows;            // [B, G, V]: stored directly by the small-batch form (TMA stores otherwise)
   int write_pd;              // 0: no p_d rows (no W items; p_d(x) and (m, S) come from the select)
   float2* pd_stat;           // [B, G] (m, S) of every drawn row, or null
   float* conf_logit;
@@ -528,6 +529,55 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   }
 }
 
+// The select of position k for the rows this CTA serves (rows blockIdx.x +
+// n_ctas j), by the epilogue's two teams of four warps (team t takes j = t,
+// t + 2, ..): the pass over the row's chunk partials, then for a sampled row
+// the recompute of the crossing chunk and its walk, and the confidence of the
+// position.  scr: the teams' scratch in shared memory.
+__device__ __forceinline__ void select_rows(const Params& p, int k, uint8_t* scr, int team, int tw, int lane) {
+  const int G = p.G;
+  SelRec* rec = reinterpret_cast<SelRec*>(scr + kSelRecOff) + team;
+  float* xw = reinterpret_cast<float*>(scr + kSelXwOff) + team * 16;
+  float* red = reinterpret_cast<float*>(scr + kSelRedOff) + team * kTeamWarps * 64;
+  float* cz = reinterpret_cast<float*>(scr + kSelConfOff) + team * kTeamWarps;
+  for (int j = team;; j += 2) {
+    const int rb = (int)blockIdx.x + p.n_ctas * j;
+    if (rb >= p.B) break;
+    // the confidence of (rb, k) needs x_{k-1} only: its loads go out first
+    // and land during the levels pass
+    ConfLoads cl;
+    conf_issue(p, rb, k, tw, lane, cl);
+    team_levels(p, rb, k, team, tw, lane, rec, xw);
+    team_sync(team);
+    const int cstar = rec->cstar;
+    uint32_t upair = 0u;
+    if (cstar >= 0) {
+      // the walking warp fetches the chunk's U pairs (prefetched to L2 by the
+      // levels pass) with the recompute's loads
+      if (tw == 0 && cstar * CW + 2 * lane < p.V)
+        upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)rb * G + k) * p.V + cstar * CW + 2 * lane));
+      chunk_dot(p, rec->x, cstar, tw, lane, red);
+      team_sync(team);
+      if (tw == 0) chunk_walk(p, rec, k, lane, red, upair);
+    }
+    // this warp's share of the confidence, off the walk's path: warps 1-3
+    // while warp 0 walks, warp 0 after it (the loads have landed by now)
+    {
+      const float zp = conf_partial(p, rb, k, tw, lane, cl, rec->x);
+      if (lane == 0) cz[tw] = zp;
+    }
+    // the record, exchange words and partial logits are free for the next row
+    team_sync(team);
+    if (tw == 1 && lane == 0) {
+      const float z = (cz[0] + cz[1]) + (cz[2] + cz[3]);
+      p.conf_logit[(size_t)rb * G + k] = z;
+      p.conf[(size_t)rb * G + k] = 1.f / (1.f + expf(-z));
+    }
+  }
+  // every warp is done with the scratch before it is reused
+  epi_sync();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_draft_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2,
                   const __grid_constant__ CUtensorMap tmPd, Params p) {
@@ -835,53 +885,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    // the select of position k for the rows this CTA serves (rows blockIdx.x +
-    // n_ctas j): team t of four warps takes j = t, t + 2, ...: the pass over the
-    // row's chunk partials, then for a sampled row the recompute of the
-    // crossing chunk and its walk
     const int team = ew / kTeamWarps, tw = ew % kTeamWarps;
-    auto select = [&](int k) {
-      SelRec* rec = reinterpret_cast<SelRec*>(sStg + kSelRecOff) + team;
-      float* xw = reinterpret_cast<float*>(sStg + kSelXwOff) + team * 16;
-      float* red = reinterpret_cast<float*>(sStg + kSelRedOff) + team * kTeamWarps * 64;
-      float* cz = reinterpret_cast<float*>(sStg + kSelConfOff) + team * kTeamWarps;
-      for (int j = team;; j += 2) {
-        const int rb = (int)blockIdx.x + p.n_ctas * j;
-        if (rb >= p.B) break;
-        // the confidence of (rb, k) needs x_{k-1} only: its loads go out first
-        // and land during the levels pass
-        ConfLoads cl;
-        conf_issue(p, rb, k, tw, lane, cl);
-        team_levels(p, rb, k, team, tw, lane, rec, xw);
-        team_sync(team);
-        const int cstar = rec->cstar;
-        uint32_t upair = 0u;
-        if (cstar >= 0) {
-          // the walking warp fetches the chunk's U pairs (prefetched to L2 by the
-          // levels pass) with the recompute's loads
-          if (tw == 0 && cstar * CW + 2 * lane < p.V)
-            upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)rb * G + k) * p.V + cstar * CW + 2 * lane));
-          chunk_dot(p, rec->x, cstar, tw, lane, red);
-          team_sync(team);
-          if (tw == 0) chunk_walk(p, rec, k, lane, red, upair);
-        }
-        // this warp's share of the confidence, off the walk's path: warps 1-3
-        // while warp 0 walks, warp 0 after it (the loads have landed by now)
-        {
-          const float zp = conf_partial(p, rb, k, tw, lane, cl, rec->x);
-          if (lane == 0) cz[tw] = zp;
-        }
-        // the record, exchange words and partial logits are free for the next row
-        team_sync(team);
-        if (tw == 1 && lane == 0) {
-          const float z = (cz[0] + cz[1]) + (cz[2] + cz[3]);
-          p.conf_logit[(size_t)rb * G + k] = z;
-          p.conf[(size_t)rb * G + k] = 1.f / (1.f + expf(-z));
-        }
-      }
-      // every warp is done with the scratch before the staging area is reused
-      epi_sync();
-    };
+    auto select = [&](int k) { select_rows(p, k, sStg, team, tw, lane); };
 
     // tokens of the rows this CTA selects: not chosen yet (ordered before
     // every wait on them by the first grid barrier)
@@ -1110,6 +1115,598 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Small batches (B <= nrw::NB): the same sweeps with the vocabulary on the
+// MMA's M side.  A 128-request tile would carry at most NB live rows, and the
+// tensor pipe would spend the sweep on the dead ones; here each product is
+//     D[v, b] = sum_k W2[k, v] E[b, k]      M = 128 columns v, N = NB, K = r
+// with A = the staged W2 tile (the same TMA stages, read MN-major) and B = the
+// E rows in shared memory (K-major, 128-byte swizzle), so that a sweep costs
+// what its W2 tiles cost to read.  TMEM lane v of an accumulator holds column
+// v of the tile for every request b.  The epilogue's group 0 writes the W
+// items' p_d rows (a warp stores 32 consecutive columns of a row), group 1
+// forms the S items' 64-column chunk partials (warp reductions over the lanes,
+// the chunk's two warps exchanging through shared memory), in the layout the
+// select reads.  The select, the grid barrier and the tile claims are the
+// 128-row form's.
+// ---------------------------------------------------------------------------
+namespace nrw {
+constexpr int NB = 16;                          // batch columns of a product (M = 128 needs N % 16 == 0)
+constexpr int NWS = 10;                         // W2 stages (2.5 tiles at r = 256)
+constexpr int NUS = 3;                          // U stages per item
+constexpr uint32_t kUStage = NB * BN * 2;       // [NB rows][128 columns] bf16, unswizzled
+constexpr uint32_t kEAtom = NB / 8 * 1024;      // one 64-element K block of E: NB rows x 128 B
+constexpr uint32_t kESlot = 4 * kEAtom;         // E_k for r <= 256
+constexpr uint32_t kTmemCols = 4 * NB;          // two accumulators per item
+constexpr uint32_t kOffE = NWS * kW2Stage;
+constexpr uint32_t kOffUW = kOffE + 2 * kESlot;
+constexpr uint32_t kOffUS = kOffUW + NUS * kUStage;
+constexpr uint32_t kOffScr = kOffUS + NUS * kUStage;
+constexpr uint32_t kScrBytes = 4096;
+constexpr uint32_t kOffRow = kOffScr + kScrBytes;  // [NB] float4 (c, m, 1/S, x), [NB] gather token
+constexpr uint32_t kOffXa = kOffRow + 5 * NB * 4;   // [2 buffers][2 chunks][2 halves][NB] float2
+constexpr uint32_t kOffXb = kOffXa + 8 * NB * 8;    // [2][2][2][NB] float
+constexpr uint32_t kOffBar = (kOffXb + 8 * NB * 4 + 63) / 64 * 64;
+constexpr uint32_t kBarBytes = 1024;
+constexpr size_t kSmemBytes = 1024 + kOffBar + kBarBytes;
+static_assert(kSelConfOff + 2 * kTeamWarps * 4 <= (int)kScrBytes, "select scratch");
+static_assert(kOffE % 1024 == 0 && kESlot % 1024 == 0 && kOffUW % 128 == 0 && kOffUS % 128 == 0, "alignment");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr int kNBars = 2 * NWS + 4 * NUS + 8 + 2 + 4 + kTQ;
+static_assert(kNBars * 8 + kTQ * 4 + 16 <= (int)kBarBytes, "barrier area");
+}  // namespace nrw
+
+// Transpose-reductions over a warp of NB = 16 values per lane: each step
+// halves the values a lane holds (lanes with bit `off` set keep the upper half
+// and send the lower one to lane ^ off, which keeps it), so that after the
+// steps at 16, 8, 4, 2 and the final exchange at 1, lanes L and L ^ 1 hold
+// the reduction over all 32 lanes of value b = L >> 1.  (value, lowest index)
+// argmax, and the fp32 sum in a fixed tree order.
+template <int N>
+__device__ __forceinline__ void halve_argmax(const float* v, const int* ix, float* vo, int* io, int off, int lane) {
+  const bool hi = (lane & off) != 0;
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    float kv = hi ? v[N / 2 + j] : v[j];
+    int ki = hi ? ix[N / 2 + j] : ix[j];
+    const float sv = hi ? v[j] : v[N / 2 + j];
+    const int si = hi ? ix[j] : ix[N / 2 + j];
+    argmax_merge(kv, ki, __shfl_xor_sync(0xffffffffu, sv, off), __shfl_xor_sync(0xffffffffu, si, off));
+    vo[j] = kv;
+    io[j] = ki;
+  }
+}
+__device__ __forceinline__ void xpose_argmax16(const float (&v)[16], const int (&ix)[16], float& rv, int& ri,
+                                               int lane) {
+  float v8[8], v4[4], v2[2], v1[1];
+  int i8[8], i4[4], i2[2], i1[1];
+  halve_argmax<16>(v, ix, v8, i8, 16, lane);
+  halve_argmax<8>(v8, i8, v4, i4, 8, lane);
+  halve_argmax<4>(v4, i4, v2, i2, 4, lane);
+  halve_argmax<2>(v2, i2, v1, i1, 2, lane);
+  rv = v1[0];
+  ri = i1[0];
+  argmax_merge(rv, ri, __shfl_xor_sync(0xffffffffu, rv, 1), __shfl_xor_sync(0xffffffffu, ri, 1));
+}
+template <int N>
+__device__ __forceinline__ void halve_sum(const float* v, float* vo, int off, int lane) {
+  const bool hi = (lane & off) != 0;
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    const float kv = hi ? v[N / 2 + j] : v[j];
+    const float sv = hi ? v[j] : v[N / 2 + j];
+    const float ov = __shfl_xor_sync(0xffffffffu, sv, off);
+    // the lower lane's value first: both lanes of a pair add in the same order
+    vo[j] = hi ? __fadd_rn(ov, kv) : __fadd_rn(kv, ov);
+  }
+}
+__device__ __forceinline__ float xpose_sum16(const float (&v)[16], int lane) {
+  float v8[8], v4[4], v2[2], v1[1];
+  halve_sum<16>(v, v8, 16, lane);
+  halve_sum<8>(v8, v4, 8, lane);
+  halve_sum<4>(v4, v2, 4, lane);
+  halve_sum<2>(v2, v1, 2, lane);
+  const float o = __shfl_xor_sync(0xffffffffu, v1[0], 1);
+  return (lane & 1) ? __fadd_rn(o, v1[0]) : __fadd_rn(v1[0], o);
+}
+
+// exchange point of the two warps of an S-item chunk: both arrive (lane 0,
+// after the warp's shared-memory writes), then wait for the phase; bounded, so
+// that a warp whose partner left on an error gives up too.  False if it gave up.
+__device__ __forceinline__ bool pair_exchange(uint64_t* bar, uint32_t parity, int lane, volatile int* abort_flag) {
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(bar);
+  return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_draft_narrow(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int r = p.r;
+  const int nkc = r / KC;
+  const int G = p.G;
+  const int B = p.B;
+  uint8_t* sW = smem;
+  uint8_t* sE = smem + nrw::kOffE;
+  uint8_t* sUW = smem + nrw::kOffUW;
+  uint8_t* sUS = smem + nrw::kOffUS;
+  uint8_t* sScr = smem + nrw::kOffScr;
+  // per row: c = log2(e) / T, and the next W items' (m, 1/S, x_s) of the row
+  float4* sRow = reinterpret_cast<float4*>(smem + nrw::kOffRow);
+  int* sGx = reinterpret_cast<int*>(sRow + nrw::NB);
+  float2* sXa = reinterpret_cast<float2*>(smem + nrw::kOffXa);
+  float* sXb = reinterpret_cast<float*>(smem + nrw::kOffXb);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + nrw::kOffBar);
+  uint64_t* fullW = bars;
+  uint64_t* emptyW = fullW + nrw::NWS;
+  uint64_t* fullUW = emptyW + nrw::NWS;
+  uint64_t* emptyUW = fullUW + nrw::NUS;
+  uint64_t* fullUS = emptyUW + nrw::NUS;
+  uint64_t* emptyUS = fullUS + nrw::NUS;
+  uint64_t* tfull = emptyUS + nrw::NUS;  // [item][buffer]
+  uint64_t* tempty = tfull + 4;          // [item][buffer]
+  uint64_t* eready = tempty + 4;
+  uint64_t* mma_done = eready + 1;
+  uint64_t* pbar = mma_done + 1;    // [step][chunk]: the S items' exchanges
+  uint64_t* tqfull = pbar + 4;      // [kTQ]
+  volatile int* tq = reinterpret_cast<volatile int*>(tqfull + kTQ);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tq) + kTQ);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_ok = abort_flag + 1;
+  volatile int* e_seen = s_ok + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto tile_of = [&](unsigned i, int q) {
+    return i >= (unsigned)p.ntiles ? -1 : ((q & 1) ? p.ntiles - 1 - (int)i : (int)i);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < 4; ++j) ptx::mbar_init(&pbar[j], 2);
+    for (int s = 0; s < nrw::NWS; ++s) {
+      ptx::mbar_init(&fullW[s], 1);
+      ptx::mbar_init(&emptyW[s], 1);
+    }
+    for (int s = 0; s < nrw::NUS; ++s) {
+      ptx::mbar_init(&fullUW[s], 1);
+      ptx::mbar_init(&emptyUW[s], 4);
+      ptx::mbar_init(&fullUS[s], 1);
+      ptx::mbar_init(&emptyUS[s], 4);
+    }
+    for (int a = 0; a < 4; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(eready, kEpiWarps);
+    ptx::mbar_init(mma_done, 1);
+    for (int j = 0; j < kTQ; ++j) ptx::mbar_init(&tqfull[j], 1);
+    *abort_flag = 0;
+    *e_seen = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, nrw::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    report_error(p.hdr, DSPARK_TIMEOUT, (int)blockIdx.x);
+  };
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      // L2: a sweep's last kTailDiv-th of claims are the next sweep's first, so
+      // their W2 tiles are kept (evict-last), the others read for the last time
+      // in the sweep (evict-first); the S item's U rows are read again by the
+      // next sweep's W item (evict-last), the W item's for the last time
+      const uint64_t pol_last = ptx::policy_evict_last();
+      const uint64_t pol_first = ptx::policy_evict_first();
+      const unsigned tail0 = (unsigned)(p.ntiles - p.ntiles / kTailDiv);
+      int iw = 0, iuw = 0, ius = 0, jq = 0;
+      bool ok = true;
+      for (int q = 0; q < G + p.write_pd && ok; ++q) {
+        const int s = q - 1;
+        const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
+        unsigned* claim = p.sched + q;
+        unsigned ci = atomicAdd(claim, 1u);
+        int n = tile_of(ci, q);
+        while (ok) {
+          tq[jq % kTQ] = n;
+          ptx::mbar_arrive(&tqfull[jq % kTQ]);
+          ++jq;
+          if (n < 0) break;
+          const int v0 = n * BN;
+          const bool keep = ci >= tail0;
+          ci = atomicAdd(claim, 1u);
+          n = tile_of(ci, q);
+          for (int kc = 0; kc < nkc; ++kc, ++iw) {
+            const int st = iw % nrw::NWS;
+            if (!ptx::mbar_wait(&emptyW[st], ((iw / nrw::NWS) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = sW + st * kW2Stage;
+            ptx::mbar_expect_tx(&fullW[st], kW2Stage);
+            for (int c = 0; c < NCH; ++c)
+              ptx::tma_load_2d(dst + c * (KC * CW * 2), &tmW2, &fullW[st], v0 + c * CW, kc * KC,
+                               keep ? pol_last : pol_first);
+          }
+          if (ok && hasW) {
+            const int su = iuw % nrw::NUS;
+            if (!ptx::mbar_wait(&emptyUW[su], ((iuw / nrw::NUS) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+            } else {
+              // rows past the batch read as zeros (the box is NB rows)
+              ptx::mbar_expect_tx(&fullUW[su], nrw::kUStage);
+              ptx::tma_load_3d(sUW + su * nrw::kUStage, &tmU, &fullUW[su], v0, s, 0, pol_first);
+              ++iuw;
+            }
+          }
+          if (ok && hasS) {
+            const int su = ius % nrw::NUS;
+            if (!ptx::mbar_wait(&emptyUS[su], ((ius / nrw::NUS) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+            } else {
+              ptx::mbar_expect_tx(&fullUS[su], nrw::kUStage);
+              ptx::tma_load_3d(sUS + su * nrw::kUStage, &tmU, &fullUS[su], v0, s + 1, 0, pol_last);
+              ++ius;
+            }
+          }
+        }
+      }
+      if (!ok) fail();
+      for (int j = max(0, iw - nrw::NWS); j < iw; ++j)
+        ptx::mbar_wait(&fullW[j % nrw::NWS], (j / nrw::NWS) & 1, abort_flag, kWaitLimitNs);
+      for (int j = max(0, iuw - nrw::NUS); j < iuw; ++j)
+        ptx::mbar_wait(&fullUW[j % nrw::NUS], (j / nrw::NUS) & 1, abort_flag, kWaitLimitNs);
+      for (int j = max(0, ius - nrw::NUS); j < ius; ++j)
+        ptx::mbar_wait(&fullUS[j % nrw::NUS], (j / nrw::NUS) & 1, abort_flag, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer --------------------------------
+    // The whole warp runs the loop (its values stay warp-uniform); one elected
+    // lane issues the MMAs and commits.  A wait on an mbarrier queues behind
+    // the shared-memory operand reads of the MMAs in flight, so a tile takes
+    // all its waits (accumulators, E, W2 stages) before its first MMA and
+    // then issues both products back to back; the warp takes lane 0's result
+    // of each wait.
+    {
+      // A: W2 K-chunk [64 x 128], MN-major (the vocabulary contiguous); B: E
+      // [NB x r], K-major
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, nrw::NB, true, false);
+      constexpr unsigned FULL = 0xffffffffu;
+      int itk[2] = {0, 0};
+      int iw = 0, jq = 0;
+      bool ok = true;
+      auto wait0 = [&](uint64_t* bar, uint32_t parity) {
+        return __shfl_sync(FULL, ptx::mbar_wait(bar, parity, abort_flag, kWaitLimitNs), 0);
+      };
+      auto wait_e = [&](int q) {
+        if (!wait0(eready, (uint32_t)(q & 1))) return false;
+        if (lane == 0) *e_seen = q + 1;
+        return true;
+      };
+      const uint32_t sE32 = ptx::smem_u32(sE);
+      for (int q = 0; q < G + p.write_pd && ok; ++q) {
+        const int s = q - 1;
+        const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
+        bool e_ok = false;
+        while (ok) {
+          if (!wait0(&tqfull[jq % kTQ], (jq / kTQ) & 1)) {
+            ok = false;
+            break;
+          }
+          const int n = __shfl_sync(FULL, tq[jq % kTQ], 0);
+          ++jq;
+          if (n < 0) {
+            if (hasS && !e_ok) ok = wait_e(q);
+            break;
+          }
+          // every wait of the tile
+          if (hasS && !e_ok) {
+            ok = wait_e(q);
+            e_ok = ok;
+          }
+          for (int item = 0; item < 2 && ok; ++item) {
+            if (item == 0 ? !hasW : !hasS) continue;
+            ok = wait0(&tempty[item * 2 + (itk[item] & 1)], ((itk[item] >> 1) & 1) ^ 1);
+          }
+          for (int kc = 0; kc < nkc && ok; ++kc)
+            ok = wait0(&fullW[(iw + kc) % nrw::NWS], ((iw + kc) / nrw::NWS) & 1);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) {
+            for (int item = 0; item < 2; ++item) {
+              if (item == 0 ? !hasW : !hasS) continue;
+              const int ab = item * 2 + (itk[item] & 1);
+              const int kk = item == 0 ? s : s + 1;
+              const uint32_t eb = sE32 + (uint32_t)(kk & 1) * nrw::kESlot;
+              const uint32_t d = tmem + (uint32_t)(ab * nrw::NB);
+              for (int kc = 0; kc < nkc; ++kc) {
+                const uint32_t aW2 = ptx::smem_u32(sW + ((iw + kc) % nrw::NWS) * kW2Stage);
+#pragma unroll
+                for (int k4 = 0; k4 < KC / 16; ++k4) {
+                  // A: two 64-column blocks 8 KB apart, 8-row K groups 1024 B
+                  //    apart; B: E's K block kc, 16 elements (32 B) per step
+                  const uint64_t ad = ptx::smem_desc_sw128(aW2 + k4 * 2048, KC * CW * 2, 1024);
+                  const uint64_t bd = ptx::smem_desc_sw128(eb + (uint32_t)kc * nrw::kEAtom + k4 * 32, 16, 1024);
+                  ptx::tc_mma(d, ad, bd, idesc, (kc | k4) > 0 ? 1u : 0u);
+                }
+              }
+              ptx::tc_commit(&tfull[ab]);
+            }
+            // the tile's W2 stages are free once both of its products are done
+            for (int kc = 0; kc < nkc; ++kc) ptx::tc_commit(&emptyW[(iw + kc) % nrw::NWS]);
+          }
+          __syncwarp();
+          if (hasW) ++itk[0];
+          if (hasS) ++itk[1];
+          iw += nkc;
+        }
+      }
+      if (!ok && lane == 0) fail();
+      if (ptx::elect_one()) ptx::tc_commit(mma_done);
+      __syncwarp();
+      wait0(mma_done, 0);
+    }
+  } else {
+    // ------------------------------ epilogue ----------------------------------
+    const int ew = warp - kEpiWarp0;
+    const int epi_tid = ew * 32 + lane;
+    const int g = ew >> 2;       // 0: W items, 1: S items
+    const int qd = warp & 3;     // TMEM lanes 32 qd .. 32 qd + 31: columns of the tile
+    const int ch = qd >> 1;      // the 64-column chunk of those columns
+    const int half = qd & 1;     // this warp's half of the chunk
+    const uint32_t lane_bits = (uint32_t)(qd * 32) << 16;
+    const int team = ew / kTeamWarps, tw = ew % kTeamWarps;
+    unsigned nbar = 0;
+    int jq = 0, itw = 0, its = 0, iuw = 0, ius = 0, ix = 0;
+    bool alive = true;
+
+    // bit b: row b is sampled (T > 0); the others are greedy
+    uint32_t samp = 0u;
+    for (int b = 0; b < B; ++b) samp |= (p.temp[b] > 0.f ? 1u : 0u) << b;
+    if (epi_tid < B) sRow[epi_tid] = make_float4(row_scale(p.temp[epi_tid]), 0.f, 1.f, 0.f);
+    // both E slots zero: the rows past the batch stay so (their products fill
+    // accumulator columns nobody reads)
+    for (int i = epi_tid; i < (int)(2 * nrw::kESlot / 16); i += kEpiThreads)
+      reinterpret_cast<uint4*>(sE)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int rb = (int)blockIdx.x + p.n_ctas * ew; rb < B; rb += p.n_ctas * kEpiWarps)
+      for (int k = lane; k < G; k += 32) p.tokens[(size_t)rb * G + k] = kTokPending;
+    epi_sync();
+
+    // E_k = W1[x_{k-1}] (x_0 = anchor) of every row into slot k & 1, and for
+    // k >= 1 the next W items' row data: x_{k-1} and (m, S) of position k - 1
+    auto gather = [&](int k) {
+      if (epi_tid < B) {
+        const int b = epi_tid;
+        int x;
+        if (k == 0) {
+          x = p.anchor[b];
+        } else {
+          x = token_wait(&p.tokens[(size_t)b * G + k - 1], abort_flag);
+          if (x == kTokPending) {
+            fail();
+            x = 0;
+          }
+          const float2 st = __ldcg(&p.rowstat[b]);
+          sRow[b].y = st.x;
+          sRow[b].z = inv_sum(st.y);
+          sRow[b].w = __int_as_float(x);
+        }
+        if (x < 0 || x >= p.V) {
+          report_error(p.hdr, DSPARK_BAD_INPUT, x);
+          x = 0;
+        }
+        sGx[b] = x;
+      }
+      epi_sync();
+      // row b's r / 8 16-byte pieces; piece j holds K elements 8 j .. 8 j + 7:
+      // K block j / 8, 16-byte column (j % 8) ^ (b % 8) of the row's 128 bytes
+      uint8_t* slot = sE + (k & 1) * nrw::kESlot;
+      const int per = r / 8;
+      for (int i = epi_tid; i < B * per; i += kEpiThreads) {
+        const int b = i / per, j = i - b * per;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)sGx[b] * r) + j);
+        *reinterpret_cast<uint4*>(slot + (j >> 3) * nrw::kEAtom + (b >> 3) * 1024 + (b & 7) * 128 +
+                                  (((j & 7) ^ (b & 7)) << 4)) = v;
+      }
+      // the MMA reads the slot through the async proxy
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (*e_seen < k) {
+          if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            fail();
+            break;
+          }
+          __nanosleep(32);
+        }
+        ptx::mbar_arrive(eready);
+      }
+    };
+
+    if (!*abort_flag) gather(0);
+    for (int q = 0; q < G + p.write_pd && alive; ++q) {
+      const int s = q - 1;
+      const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
+      const bool mine = g == 0 ? hasW : hasS;
+      bool tiles_ok = true;
+      while (tiles_ok) {
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&tqfull[jq % kTQ], (jq / kTQ) & 1, abort_flag, kWaitLimitNs))) {
+          if (lane == 0) fail();
+          tiles_ok = false;
+          break;
+        }
+        const int n = tq[jq % kTQ];
+        ++jq;
+        if (n < 0) break;
+        if (!mine) continue;
+        const int col = 32 * qd + lane;  // this lane's column of the tile
+        const int vt = n * BN + col;
+        const bool vin = vt < p.V;
+        // the accumulator and the U stage of this warp's item
+        int& it = g == 0 ? itw : its;
+        int& iu = g == 0 ? iuw : ius;
+        const int ab = g * 2 + (it & 1);
+        const int su = iu % nrw::NUS;
+        uint64_t* fullU = g == 0 ? fullUW : fullUS;
+        uint64_t* emptyU = g == 0 ? emptyUW : emptyUS;
+        bool ok = ptx::mbar_wait(&tfull[ab], (it >> 1) & 1, abort_flag, kWaitLimitNs);
+        if (ok) ok = ptx::mbar_wait(&fullU[su], (iu / nrw::NUS) & 1, abort_flag, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) fail();
+          tiles_ok = false;
+          break;
+        }
+        ++it;
+        ++iu;
+        ptx::tc_fence_after();
+        float acc[nrw::NB];
+        __syncwarp();
+        ptx::tmem_ld16(tmem + lane_bits + (uint32_t)(ab * nrw::NB), acc);
+        const __nv_bfloat16* ur =
+            reinterpret_cast<const __nv_bfloat16*>((g == 0 ? sUW : sUS) + su * nrw::kUStage) + col;
+        float l[nrw::NB];
+#pragma unroll
+        for (int b = 0; b < nrw::NB; ++b) l[b] = b < B ? __bfloat162float(ur[b * BN]) : 0.f;
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        // the U stage's next fill is an async-proxy write: order the reads first
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&tempty[ab]);
+          ptx::mbar_arrive(&emptyU[su]);
+        }
+#pragma unroll
+        for (int b = 0; b < nrw::NB; ++b) l[b] = add_base(l[b], acc[b]);
+        if (g == 0) {
+          // W item: p_d^s = 2^(l c - m) / S, one-hot for greedy rows
+#pragma unroll
+          for (int b = 0; b < nrw::NB; ++b) {
+            if (b >= B) break;
+            const float4 rw = sRow[b];
+            const int xs = __float_as_int(rw.w);
+            const float pw = __fmul_rn(exp_scaled(l[b], rw.x, rw.y), rw.z);
+            const float pv = ((samp >> b) & 1u) ? pw : (vt == xs ? 1.f : 0.f);
+            // streaming store (read once, by verify)
+            if (vin) __stcs(p.pd_rows + ((size_t)b * G + s) * p.V + vt, pv);
+            if (vt == xs) p.pd_tok[(size_t)b * G + s] = pv;
+          }
+        } else {
+          // S item: chunk partials of position s + 1.  Step 1: each warp's
+          // (value, lowest index) argmax of the logits over its 32 columns, for
+          // every row at once (a sampled row takes the value: the max of l c
+          // is at the max of l for c > 0)
+          const int buf = ix & 1;
+          ++ix;
+          float2* xa = sXa + (size_t)((buf * 2 + ch) * 2) * nrw::NB;
+          float* xb = sXb + (size_t)((buf * 2 + ch) * 2) * nrw::NB;
+          const int bl = lane >> 1;  // the row whose reductions this lane ends with
+          {
+            int li[nrw::NB];
+#pragma unroll
+            for (int b = 0; b < nrw::NB; ++b) {
+              li[b] = (vin && b < B) ? vt : INT_MAX;
+              if (!(vin && b < B)) l[b] = -INFINITY;
+            }
+            float rv;
+            int ri;
+            xpose_argmax16(l, li, rv, ri, lane);
+            if (!(lane & 1) && bl < B) xa[half * nrw::NB + bl] = make_float2(rv, __int_as_float(ri));
+          }
+          if (!pair_exchange(&pbar[ch], (uint32_t)buf, lane, abort_flag)) {
+            if (lane == 0) fail();
+            tiles_ok = false;
+            break;
+          }
+          // step 2: the chunk max of each sampled row, then each warp's sum of
+          // 2^(l c - m_chunk) for every row at once
+          {
+            float e[nrw::NB];
+#pragma unroll
+            for (int b = 0; b < nrw::NB; ++b) {
+              e[b] = 0.f;
+              if (b < B && ((samp >> b) & 1u)) {
+                const float lm = fmaxf(xa[b].x, xa[nrw::NB + b].x);
+                const float cb = sRow[b].x;
+                // (l is -inf past V: those columns weigh nothing)
+                if (lm != -INFINITY) e[b] = exp_scaled(l[b], cb, scale_logit(lm, cb));
+              }
+            }
+            const float ws = xpose_sum16(e, lane);
+            if (!(lane & 1) && bl < B) xb[half * nrw::NB + bl] = ws;
+          }
+          if (!pair_exchange(&pbar[2 + ch], (uint32_t)buf, lane, abort_flag)) {
+            if (lane == 0) fail();
+            tiles_ok = false;
+            break;
+          }
+          const int j = n * NCH + ch;  // the chunk's index in the row
+          if (half == 0 && lane < B && j * CW < p.V) {
+            const int b = lane;
+            float2 part;
+            if ((samp >> b) & 1u) {
+              const float lm = fmaxf(xa[b].x, xa[nrw::NB + b].x);
+              part = lm == -INFINITY ? make_float2(-INFINITY, 0.f)
+                                     : make_float2(scale_logit(lm, sRow[b].x), __fadd_rn(xb[b], xb[nrw::NB + b]));
+            } else {
+              float v = xa[b].x;
+              int i = __float_as_int(xa[b].y);
+              argmax_merge(v, i, xa[nrw::NB + b].x, __float_as_int(xa[nrw::NB + b].y));
+              part = make_float2(v, __int_as_float(i));
+            }
+            // (a small batch's partials stay in L2 without a policy)
+            p.part[(size_t)b * p.pstride + (j % p.ept) * 128 + j / p.ept] = part;
+          }
+        }
+      }
+      if (!hasS) break;  // the last sweep
+      if (!grid_barrier(p, ++nbar * (unsigned)p.n_ctas, abort_flag, s_ok, epi_tid)) {
+        if (epi_tid == 0) fail();
+        alive = false;
+        break;
+      }
+      select_rows(p, q, sScr, team, tw, lane);
+      if (q + 1 < G) {
+        gather(q + 1);
+      } else {
+        // the last sweep has no S items, hence no gather: the W items' row data
+        if (epi_tid < B) {
+          const int b = epi_tid;
+          int x = token_wait(&p.tokens[(size_t)b * G + q], abort_flag);
+          if (x == kTokPending) {
+            fail();
+            x = 0;
+          }
+          const float2 st = __ldcg(&p.rowstat[b]);
+          sRow[b].y = st.x;
+          sRow[b].z = inv_sum(st.y);
+          sRow[b].w = __int_as_float(x);
+        }
+        epi_sync();
+      }
+    }
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, nrw::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1131,13 +1728,25 @@ static EncodeTiledFn encode_fn() {
 }
 
 static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
-                   const cuuint64_t* strides, const cuuint32_t* box) {
+                   const cuuint64_t* strides, const cuuint32_t* box,
+                   CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The small-batch form runs for B <= nrw::NB unless DSPARK_DRAFT_FORM=wide
+// asks for the 128-row form at every batch.
+static bool narrow_enabled() {
+  static int on = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* e = getenv("DSPARK_DRAFT_FORM");
+    on = (e && std::string(e) == "wide") ? 0 : 1;
+  });
+  return on != 0;
 }
 
 }  // namespace fz
@@ -1155,8 +1764,17 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   if (!coop || sms <= 0 || n_mtiles > sms || d.r > 2 * (int)fz::kESlotCols || (d.r % (8 * 8)) != 0)
     return cudaErrorNotSupported;
   const cuuint64_t V = (cuuint64_t)d.V, G = (cuuint64_t)d.gamma, B = (cuuint64_t)d.B, r = (cuuint64_t)d.r;
-  CUtensorMap tmU, tmW2, tmPd = {};  // tmPd stays unused without p_d rows
-  {
+  // small batches: the vocabulary on the MMA's M side (k_draft_narrow)
+  const bool narrow = d.B <= fz::nrw::NB && fz::narrow_enabled();
+  CUtensorMap tmU, tmW2, tmPd = {};  // tmPd stays unused without p_d rows and in the small-batch form
+  if (narrow) {
+    // U rows of all requests of one position, 128 columns, unswizzled
+    const cuuint64_t dims[3] = {V, G, B};
+    const cuuint64_t strides[2] = {V * 2, G * V * 2};
+    const cuuint32_t box[3] = {fz::BN, 1, fz::nrw::NB};
+    if (!fz::encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.U, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
     const cuuint64_t dims[3] = {V, G, B};
     const cuuint64_t strides[2] = {V * 2, G * V * 2};
     const cuuint32_t box[3] = {fz::CW, 1, fz::BM};
@@ -1173,12 +1791,12 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     const cuuint64_t dims[3] = {V, G, B};
     const cuuint64_t strides[2] = {V * 4, G * V * 4};
     const cuuint32_t box[3] = {32, 1, 32};
-    if (a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
+    if (!narrow && a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  if (const cudaError_t ae = ensure_smem_limit((const void*)fz::k_draft_fused, (int)fz::kSmemBytes);
-      ae != cudaSuccess)
-    return ae;
+  const void* kfn = narrow ? (const void*)fz::k_draft_narrow : (const void*)fz::k_draft_fused;
+  const size_t smem = narrow ? fz::nrw::kSmemBytes : fz::kSmemBytes;
+  if (const cudaError_t ae = ensure_smem_limit(kfn, (int)smem); ae != cudaSuccess) return ae;
 
   fz::Params p;
   p.B = d.B;
@@ -1207,6 +1825,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.tokens = a.tokens;
   p.part = reinterpret_cast<float2*>(ws + L.part);
   p.pd_tok = a.pd_tok;
+  p.pd_rows = a.pd_rows;
   p.write_pd = a.pd_rows ? 1 : 0;
   p.pd_stat = reinterpret_cast<float2*>(a.pd_stat);
   p.conf_logit = a.conf_logit;
@@ -1220,7 +1839,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_ctas);
   cfg.blockDim = dim3(fz::kThreads);
-  cfg.dynamicSmemBytes = fz::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -1228,6 +1847,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
+  if (narrow) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow, tmU, tmW2, p);
   return cudaLaunchKernelEx(&cfg, fz::k_draft_fused, tmU, tmW2, tmPd, p);
 }
 

@@ -50,7 +50,7 @@ def test_draft_tiny(temp, seed):
     (130, 5, 8200, 128, 16, "bf16"),   # two M-tiles (the second with 2 rows), an 8-column last tile
     (40, 3, 1024, 256, 8, "bf16"),     # 8 vocabulary tiles for many CTAs: most claim no tile
     (260, 16, 2048, 192, 32, "bf16"),  # gamma 16, rank 192, three M-tiles
-    # small batches on the tensor-core path (one M-tile, most lane quadrants idle)
+    # small batches on the tensor-core path (the vocabulary on the MMA's M side)
     (1, 3, 8200, 256, 16, "bf16"),     # one row, an 8-column last tile
     (2, 5, 1032, 128, 32, "bf16"),     # two rows, rank 128, 9 tiles
     (3, 4, 4104, 64, 24, "bf16"),      # three rows, rank 64
@@ -64,6 +64,27 @@ def test_draft_ragged_shapes(B, G, V, r, H, dt):
     _invariants(g, V)
     o = oracle_draft(**np_inputs(inp))
     compare_draft(g, o, rtol_for(dt))
+    check_no_error(ws)
+
+
+@pytest.mark.parametrize("temp", ["0", "1.0", "0.7", "mixed"])
+@pytest.mark.parametrize("B,G,V,r,H", [
+    (1, 4, 8200, 256, 16),     # one request, an 8-column last tile
+    (5, 4, 8200, 256, 16),
+    (16, 4, 8200, 256, 16),    # the largest batch of the small-batch form
+    (16, 16, 2048, 192, 32),   # gamma 16, rank 192 (three K blocks)
+    (9, 3, 1032, 64, 8),       # rank 64, 9 tiles for 152 CTAs
+    (17, 3, 4104, 128, 24),    # one past the small-batch form: the 128-row tile
+])
+def test_draft_small_batch_form(B, G, V, r, H, temp):
+    # small batches put the vocabulary on the MMA's M side (the batch is N = 16)
+    wl = synth.Workload("small", B, G, V, H, r, "bf16", temp, synth.SCHED_GREEDY, "tiny", seed=13)
+    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    out, ws = gpu_draft(inp)
+    g = gpu_np(out)
+    _invariants(g, V)
+    o = oracle_draft(**np_inputs(inp))
+    compare_draft(g, o, rtol_for("bf16"))
     check_no_error(ws)
 
 

@@ -1,6 +1,7 @@
 """The other draft launch paths (chosen once per process by environment
-variables): the two-pass tensor-core kernel, one launch per pass, and the
-CUDA-core path, each against the fp64 oracle in a child process."""
+variables): the two-pass tensor-core kernel, one launch per pass, the
+CUDA-core path, and the 128-row fused tile at small batches too, each against
+the fp64 oracle in a child process."""
 import os
 import subprocess
 import sys
@@ -20,7 +21,7 @@ import synth
 from oracle.draft import draft as oracle_draft
 from parity import compare_draft, gpu_np, np_inputs, rtol_for
 from gpu_common import check_no_error, gpu_draft
-for B, G, V, r, H in [(130, 5, 8200, 128, 16), (5, 4, 4104, 64, 24)]:
+for B, G, V, r, H in [(130, 5, 8200, 128, 16), (5, 4, 4104, 64, 24), (1, 3, 8200, 256, 16)]:
     wl = synth.Workload("paths", B, G, V, H, r, "bf16", "mixed", synth.SCHED_GREEDY, "tiny", seed=11)
     inp = synth.make_inputs(wl, "cuda", with_target=False)
     out, ws = gpu_draft(inp)
@@ -31,7 +32,7 @@ print("ok")
 
 
 @pytest.mark.parametrize("env", [{"DSPARK_DRAFT_LAUNCH": "two_pass"}, {"DSPARK_DRAFT_LAUNCH": "per_pass"},
-                                 {"DSPARK_DRAFT_PATH": "cuda_core"}])
+                                 {"DSPARK_DRAFT_PATH": "cuda_core"}, {"DSPARK_DRAFT_FORM": "wide"}])
 def test_draft_launch_paths(env):
     require_gpu()
     code = CHILD.format(root=ROOT, tests=os.path.join(ROOT, "tests"))

@@ -42,7 +42,9 @@ def _workload(B, G, V, r, H, temp="mixed", seed=5):
 
 
 @pytest.mark.parametrize("B,G,V,r,H", [(40, 3, 1024, 256, 8), (130, 5, 8200, 128, 16), (256, 7, 151936, 256, 4096),
-                                       (300, 1, 2056, 64, 8), (260, 16, 2048, 192, 32)])
+                                       (300, 1, 2056, 64, 8), (260, 16, 2048, 192, 32),
+                                       # small batches (the vocabulary on the MMA's M side)
+                                       (1, 7, 151936, 256, 4096), (8, 4, 8200, 256, 16), (16, 5, 4104, 64, 24)])
 def test_row_free_draft_matches_the_row_mode(B, G, V, r, H):
     wl = _workload(B, G, V, r, H)
     inp = synth.make_inputs(wl, "cuda", with_target=False)
