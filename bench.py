@@ -305,9 +305,11 @@ def run_ours(args, rank, world, local_rank):
     value = world * B * G / (ms * 1e-3)
     peak, peak_kind = load_peaks()
     bytes_ = step_bytes(wl, nv, not row_free)
-    # dominant call: the draft sampler, one launch of fz::k_draft_fused; its
-    # algorithmic bytes with W2 read once per position (the method's sequential
-    # structure), and the strict count (W2 once per call) beside them
+    # dominant call: the draft sampler, one launch of fz::k_draft_fused (the
+    # library's small-batch form fz::k_draft_narrow for B <= 16 unless
+    # DSPARK_DRAFT_FORM=wide); its algorithmic bytes with W2 read once per
+    # position (the method's sequential structure), and the strict count (W2
+    # once per call) beside them
     draft_ms = br["draft_ms"]
     draft_gbs = bytes_["draft_per_position"] / (draft_ms * 1e-3) / 1e9
     e2e = run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev) if not args.no_e2e else None
@@ -326,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
         "step_bytes": {"per_position": bytes_["step_per_position"], "strict": bytes_["step_strict"]},
         "breakdown_ms": br,
         "roofline": {"bound": "hbm",
-                     "kernel": ("dspark_draft_sample (fz::k_draft_fused, one launch)" if args.head == "markov" else
+                     "kernel": (f"dspark_draft_sample ({draft_kernel_name(wl)}, one launch)" if args.head == "markov" else
                                 "dspark_draft_sample, RNN head (k_rnn_step + tensor-core passes per position)"),
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
                      "unit": "GB/s", "frac": draft_gbs / peak,
@@ -343,6 +345,12 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_sample, d_out["tokens"].cpu().numpy())
     return res
+
+
+def draft_kernel_name(wl):
+    """The kernel that runs the draft call of a Markov-head workload."""
+    small = wl.B <= 16 and os.environ.get("DSPARK_DRAFT_FORM") != "wide"
+    return "fz::k_draft_narrow" if small else "fz::k_draft_fused"
 
 
 def load_traffic(wl):
