@@ -453,7 +453,7 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
     for i in range(nw):
         step(i)
     torch.cuda.synchronize(dev)
-    n_e2e = max(2, min(args.steps, 8))
+    n_e2e = max(4, min(args.steps, 16))
     t0 = time.perf_counter()
     for i in range(nw, nw + n_e2e):
         step(i)

@@ -17,7 +17,8 @@
 // [B x 2r] . [2r x 3r] over z' = [s_{j-1}; W1[x_{j-1}]], plus P, whose epilogue
 // applies the gates.  A CTA of k_rnn_step holds 16 requests x 32 state columns
 // and accumulates the three rows of each column (gate, candidate, output)
-// together, so the gate arithmetic needs no second pass.
+// together, so the gate arithmetic needs no second pass; each thread keeps
+// 4 requests x 2 columns x 3 rows in registers.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -29,10 +30,11 @@ namespace dspark {
 
 namespace {
 
-constexpr int RN_BM = 16;  // requests per CTA
-constexpr int RN_BN = 32;  // state columns per CTA
-constexpr int RN_KC = 32;  // z entries per shared-memory chunk
-constexpr int RN_THREADS = 256;
+constexpr int RN_BM = 16;     // requests per CTA
+constexpr int RN_BN = 32;     // state columns per CTA
+constexpr int RN_KC = 16;     // z entries per shared-memory chunk
+constexpr int RN_KG = 4;      // groups of 64 threads, each summing a quarter of z
+constexpr int RN_THREADS = 64 * RN_KG;
 
 constexpr int HP_TM = 64, HP_TN = 64, HP_TK = 16;  // k_rnn_hproj tile
 
@@ -89,7 +91,15 @@ __global__ void __launch_bounds__(256) k_rnn_hproj(const T* __restrict__ Wr, con
 __device__ __forceinline__ void store_row(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_row(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-template <typename T>
+// One CTA: RN_BM requests x RN_BN state columns, four groups of 64 threads
+// each summing a contiguous quarter of the z entries.  Thread (ty, tx) of a
+// group accumulates requests 4 ty .. 4 ty + 3 x columns 2 tx, 2 tx + 1 x the
+// three rows of each column (gate, candidate, output): 24 fma chains over its
+// quarter in ascending order; the quarters are then added in order.  z and
+// the weight rows go through shared memory k-major, RN_KC entries at a time;
+// the next chunk's global loads are in flight while the current one is used.
+// kVec: vector loads (bf16 weights and W1 rows, r % RN_KC == 0, 2r + H % 8 == 0).
+template <typename T, bool kVec>
 __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ Wr, const T* __restrict__ W1,
                                                          const float* __restrict__ P,
                                                          const int32_t* __restrict__ anchor,
@@ -97,90 +107,179 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
                                                          const float* __restrict__ s_prev, float* __restrict__ s_new,
                                                          T* __restrict__ E, int B, int G, int V, int r, int H,
                                                          int j) {
-  constexpr int ZPT = RN_BM * RN_KC / RN_THREADS;      // z entries each thread stages per chunk
-  constexpr int WPT = 3 * RN_BN * RN_KC / RN_THREADS;  // W entries each thread stages per chunk
-  __shared__ float zs[RN_BM][RN_KC + 1];
-  __shared__ float ws[3][RN_BN][RN_KC + 1];
+  // staging (z and weights per group), reused for the groups' sums after the loop
+  constexpr int kZs = RN_KG * RN_KC * RN_BM, kWs = RN_KG * 3 * RN_KC * RN_BN, kRed = (RN_KG - 1) * 3 * RN_BM * RN_BN;
+  static_assert(kRed <= kZs + kWs, "reduction buffer");
+  __shared__ __align__(16) float smem[kZs + kWs];
   __shared__ int xs[RN_BM];
+  auto zs = reinterpret_cast<float(*)[RN_KC][RN_BM]>(smem);
+  auto ws = reinterpret_cast<float(*)[3][RN_KC][RN_BN]>(smem + kZs);
+  auto red = reinterpret_cast<float(*)[3][RN_BM][RN_BN]>(smem);
   const int K = 2 * r, ldw = 2 * r + H;  // the h_j part comes from P
-  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int kg = threadIdx.x >> 6, tid = threadIdx.x & 63;
+  const int ty = tid >> 4, tx = tid & 15;
   const int c0 = blockIdx.x * RN_BN, b0 = blockIdx.y * RN_BM;
-  if (tid < RN_BM) {
-    const int b = b0 + tid;
+  if (threadIdx.x < RN_BM) {
+    const int b = b0 + threadIdx.x;
     int x = 0;
     if (b < B) x = (j == 1) ? anchor[b] : tokens[(size_t)b * G + j - 2];
-    xs[tid] = (x >= 0 && x < V) ? x : 0;  // out-of-range anchors are reported by the confidence kernel
+    xs[threadIdx.x] = (x >= 0 && x < V) ? x : 0;  // out-of-range anchors are reported by the confidence kernel
   }
   __syncthreads();
-  // the next chunk's entries are loaded into registers while the current one is used
-  float zr[ZPT], wr[WPT];
+  // this group's quarter of the z entries, in whole chunks
+  const int nch = (K + RN_KC - 1) / RN_KC;
+  const int per = (nch + RN_KG - 1) / RN_KG;
+  const int ch0 = kg * per, ch1 = min(nch, ch0 + per);
+  // staging: thread tid loads z entries kz .. kz + 3 of request mz, and entries
+  // kw .. kw + 7 of the three weight rows of column cw
+  const int mz = tid >> 2, kz = (tid & 3) * 4;
+  const int cw = tid >> 1, kw = (tid & 1) * 8;
+  float zr[4], wr[3][8];
   auto fetch = [&](int i0) {
+    const int b = b0 + mz;
+    const int col = c0 + cw;
+    if constexpr (kVec) {
+      // a chunk lies wholly in the state part or wholly in the W1 part
+      if (b < B && i0 + kz < K) {
+        if (i0 < r) {
+          if (j == 1) {
 #pragma unroll
-    for (int u = 0; u < ZPT; ++u) {
-      const int idx = tid + u * RN_THREADS;
-      const int m = idx / RN_KC, kk = idx - m * RN_KC;
-      const int b = b0 + m, i = i0 + kk;
-      float v = 0.f;
-      if (b < B && i < K) v = (i < r) ? ((j == 1) ? 0.f : s_prev[(size_t)b * r + i])
-                                       : to_f32(W1[(size_t)xs[m] * r + (i - r)]);
-      zr[u] = v;
-    }
+            for (int u = 0; u < 4; ++u) zr[u] = 0.f;
+          } else {
+            const float4 s0 = *reinterpret_cast<const float4*>(s_prev + (size_t)b * r + i0 + kz);
+            zr[0] = s0.x;
+            zr[1] = s0.y;
+            zr[2] = s0.z;
+            zr[3] = s0.w;
+          }
+        } else {
+          const uint2 q = *reinterpret_cast<const uint2*>(W1 + (size_t)xs[mz] * r + (i0 - r) + kz);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
-    for (int u = 0; u < WPT; ++u) {
-      const int idx = tid + u * RN_THREADS;
-      const int g = idx / (RN_BN * RN_KC);
-      const int rem = idx - g * RN_BN * RN_KC;
-      const int c = rem / RN_KC, kk = rem - c * RN_KC;
-      const int col = c0 + c, i = i0 + kk;
-      wr[u] = (col < r && i < K) ? to_f32(Wr[((size_t)g * r + col) * ldw + i]) : 0.f;
+          for (int u = 0; u < 2; ++u) {
+            const float2 f = __bfloat1622float2(h2[u]);
+            zr[2 * u] = f.x;
+            zr[2 * u + 1] = f.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) zr[u] = 0.f;
+      }
+#pragma unroll
+      for (int g = 0; g < 3; ++g) {
+        if (col < r && i0 + kw < K) {
+          const uint4 q = *reinterpret_cast<const uint4*>(Wr + ((size_t)g * r + col) * ldw + i0 + kw);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(h2[u]);
+            wr[g][2 * u] = f.x;
+            wr[g][2 * u + 1] = f.y;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) wr[g][u] = 0.f;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + kz + u;
+        float v = 0.f;
+        if (b < B && i < K) v = (i < r) ? ((j == 1) ? 0.f : s_prev[(size_t)b * r + i])
+                                         : to_f32(W1[(size_t)xs[mz] * r + (i - r)]);
+        zr[u] = v;
+      }
+#pragma unroll
+      for (int g = 0; g < 3; ++g)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + kw + u;
+          wr[g][u] = (col < r && i < K) ? to_f32(Wr[((size_t)g * r + col) * ldw + i]) : 0.f;
+        }
     }
   };
-  fetch(0);
-  float ag[2] = {0.f, 0.f}, ac[2] = {0.f, 0.f}, ao[2] = {0.f, 0.f};
-  for (int i0 = 0; i0 < K; i0 += RN_KC) {
-    __syncthreads();  // the previous chunk is consumed
+  auto stash = [&]() {
 #pragma unroll
-    for (int u = 0; u < ZPT; ++u) {
-      const int idx = tid + u * RN_THREADS;
-      zs[idx / RN_KC][idx % RN_KC] = zr[u];
-    }
+    for (int u = 0; u < 4; ++u) zs[kg][kz + u][mz] = zr[u];
 #pragma unroll
-    for (int u = 0; u < WPT; ++u) {
-      const int idx = tid + u * RN_THREADS;
-      const int g = idx / (RN_BN * RN_KC);
-      const int rem = idx - g * RN_BN * RN_KC;
-      ws[g][rem / RN_KC][rem % RN_KC] = wr[u];
-    }
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ws[kg][g][kw + u][cw] = wr[g][u];
+  };
+  float acc[3][4][2];
+#pragma unroll
+  for (int g = 0; g < 3; ++g)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[g][u][0] = acc[g][u][1] = 0.f;
+  // every group runs the same number of rounds, so that the CTA barriers match
+  if (ch0 < ch1) fetch(ch0 * RN_KC);
+  for (int c = 0; c < per; ++c) {
+    const int ch = ch0 + c;
+    const bool live = ch < ch1;
+    if (live) stash();
     __syncthreads();
-    if (i0 + RN_KC < K) fetch(i0 + RN_KC);
+    if (live && ch + 1 < ch1) fetch((ch + 1) * RN_KC);
+    if (live) {
 #pragma unroll 8
-    for (int kk = 0; kk < RN_KC; ++kk) {
-      const float wg = ws[0][tx][kk], wc = ws[1][tx][kk], wo = ws[2][tx][kk];
+      for (int kk = 0; kk < RN_KC; ++kk) {
+        const float4 z4 = *reinterpret_cast<const float4*>(&zs[kg][kk][4 * ty]);
+        const float zv[4] = {z4.x, z4.y, z4.z, z4.w};
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float z = zs[ty + 8 * q][kk];
-        ag[q] = fmaf(wg, z, ag[q]);
-        ac[q] = fmaf(wc, z, ac[q]);
-        ao[q] = fmaf(wo, z, ao[q]);
+        for (int g = 0; g < 3; ++g) {
+          const float2 w2 = *reinterpret_cast<const float2*>(&ws[kg][g][kk][2 * tx]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            acc[g][u][0] = fmaf(w2.x, zv[u], acc[g][u][0]);
+            acc[g][u][1] = fmaf(w2.y, zv[u], acc[g][u][1]);
+          }
+        }
       }
     }
+    __syncthreads();
   }
-  const int col = c0 + tx;
+  // groups 1..3 hand their sums to group 0, which adds them in group order
+  // (the staging area is free: the loop ended with a barrier)
+  if (kg > 0) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int b = b0 + ty + 8 * q;
-    if (b >= B || col >= r) continue;
-    float pg = ag[q], pc = ac[q], po = ao[q];
-    if (H > 0) {
-      const float* pr = P + ((size_t)b * G + (j - 1)) * 3 * r;
-      pg += pr[col];
-      pc += pr[r + col];
-      po += pr[2 * r + col];
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        red[kg - 1][g][4 * ty + u][2 * tx] = acc[g][u][0];
+        red[kg - 1][g][4 * ty + u][2 * tx + 1] = acc[g][u][1];
+      }
+  }
+  __syncthreads();
+  if (kg > 0) return;
+#pragma unroll
+  for (int q = 0; q < RN_KG - 1; ++q)
+#pragma unroll
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[g][u][0] = __fadd_rn(acc[g][u][0], red[q][g][4 * ty + u][2 * tx]);
+        acc[g][u][1] = __fadd_rn(acc[g][u][1], red[q][g][4 * ty + u][2 * tx + 1]);
+      }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int b = b0 + 4 * ty + u;
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      const int col = c0 + 2 * tx + v;
+      if (b >= B || col >= r) continue;
+      float pg = acc[0][u][v], pc = acc[1][u][v], po = acc[2][u][v];
+      if (H > 0) {
+        const float* pr = P + ((size_t)b * G + (j - 1)) * 3 * r;
+        pg += pr[col];
+        pc += pr[r + col];
+        po += pr[2 * r + col];
+      }
+      const float gt = 1.f / (1.f + expf(-pg));
+      const float sp = (j == 1) ? 0.f : s_prev[(size_t)b * r + col];
+      s_new[(size_t)b * r + col] = gt * sp + (1.f - gt) * tanhf(pc);
+      store_row(E + (size_t)b * r + col, tanhf(po));
     }
-    const float g = 1.f / (1.f + expf(-pg));
-    const float sp = (j == 1) ? 0.f : s_prev[(size_t)b * r + col];
-    s_new[(size_t)b * r + col] = g * sp + (1.f - g) * tanhf(pc);
-    store_row(E + (size_t)b * r + col, tanhf(po));
   }
 }
 
@@ -208,14 +307,26 @@ cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, c
                             void* E, cudaStream_t s) {
   const dspark_dims& d = a.dims;
   const dim3 grid((d.r + RN_BN - 1) / RN_BN, (d.B + RN_BM - 1) / RN_BM);
-  if (d.dtype == DSPARK_BF16)
-    k_rnn_step<__nv_bfloat16><<<grid, RN_THREADS, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.W_rnn), static_cast<const __nv_bfloat16*>(a.W1), P, a.anchor, a.tokens,
-        s_prev, s_new, static_cast<__nv_bfloat16*>(E), d.B, d.gamma, d.V, d.r, d.H, j);
-  else
-    k_rnn_step<float><<<grid, RN_THREADS, 0, s>>>(static_cast<const float*>(a.W_rnn), static_cast<const float*>(a.W1),
-                                                  P, a.anchor, a.tokens, s_prev, s_new, static_cast<float*>(E), d.B,
-                                                  d.gamma, d.V, d.r, d.H, j);
+  // vector loads when every chunk lies in one part of z and the rows are 16-byte aligned
+  const bool vec = d.dtype == DSPARK_BF16 && d.r % RN_KC == 0 && (2 * d.r + d.H) % 8 == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.W_rnn) % 16) == 0 && (reinterpret_cast<uintptr_t>(a.W1) % 16) == 0 &&
+                   (reinterpret_cast<uintptr_t>(s_prev) % 16) == 0;
+  if (d.dtype == DSPARK_BF16) {
+    const auto* Wr = static_cast<const __nv_bfloat16*>(a.W_rnn);
+    const auto* W1 = static_cast<const __nv_bfloat16*>(a.W1);
+    auto* Eo = static_cast<__nv_bfloat16*>(E);
+    if (vec)
+      k_rnn_step<__nv_bfloat16, true><<<grid, RN_THREADS, 0, s>>>(Wr, W1, P, a.anchor, a.tokens, s_prev, s_new, Eo,
+                                                                 d.B, d.gamma, d.V, d.r, d.H, j);
+    else
+      k_rnn_step<__nv_bfloat16, false><<<grid, RN_THREADS, 0, s>>>(Wr, W1, P, a.anchor, a.tokens, s_prev, s_new, Eo,
+                                                                  d.B, d.gamma, d.V, d.r, d.H, j);
+  } else {
+    k_rnn_step<float, false><<<grid, RN_THREADS, 0, s>>>(static_cast<const float*>(a.W_rnn),
+                                                         static_cast<const float*>(a.W1), P, a.anchor, a.tokens,
+                                                         s_prev, s_new, static_cast<float*>(E), d.B, d.gamma, d.V,
+                                                         d.r, d.H, j);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
