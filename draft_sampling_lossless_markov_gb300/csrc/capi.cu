@@ -66,8 +66,9 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.part = take(B * std::max(ntiles * sizeof(float4), fused_row));
   L.segpart = take(B * kDraftMaxSeg * sizeof(float4));
   // grid-barrier counter, then one tile counter per (sweep, M-tile) (gamma + 1
-  // sweeps); all zeroed by one memset per draft call
-  L.gbar = take(16 + (G + 1) * ((B + 127) / 128) * sizeof(uint32_t));
+  // sweeps), then the RNN head's recurrent-unit counters per (position,
+  // M-tile); all zeroed by one memset per draft call
+  L.gbar = take(16 + (2 * G + 1) * ((B + 127) / 128) * sizeof(uint32_t));
   L.vfin = take(B * 32 * ((((V + 255) / 256) + 31) / 32) * sizeof(float2));
   L.total = align_up(off, 256);
   return L;

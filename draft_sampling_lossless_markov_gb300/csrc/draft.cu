@@ -547,6 +547,18 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
   return cudaGetLastError();
 }
 
+// The fused-sweep kernel serves the tensor-core shapes unless
+// DSPARK_DRAFT_LAUNCH=two_pass or per_pass selects the pass kernels.
+static bool fused_launch_enabled() {
+  static int fused = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* e = getenv("DSPARK_DRAFT_LAUNCH");
+    fused = (e && (std::string(e) == "per_pass" || std::string(e) == "two_pass")) ? 0 : 1;
+  });
+  return fused != 0;
+}
+
 template <typename T>
 static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   const dspark_dims& d = a.dims;
@@ -554,6 +566,12 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   if (!a.pd_rows) return draft_tc_supported(d) ? launch_draft_fused(a, ws, L, s) : cudaErrorNotSupported;
   if (a.head == DSPARK_HEAD_RNN) {
     if (!draft_tc_supported(d)) return launch_cuda_core<T, T>(a, ws, L, s);
+    // the fused-sweep kernel with the recurrent step between sweeps (B > 16),
+    // unless DSPARK_DRAFT_LAUNCH asks for the pass kernels
+    if (fused_launch_enabled()) {
+      const cudaError_t fe = launch_draft_fused(a, ws, L, s);
+      if (fe != cudaErrorNotSupported) return fe;
+    }
     // tensor-core passes, one launch per pass; before each position the
     // recurrent step writes its rows (bf16) and k_embed its confidences
     const int B = d.B, r = d.r, BG = B * d.gamma;
@@ -583,13 +601,7 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     // tensor-core path: the fused-sweep persistent kernel (which forms w_h . h
     // itself), else the two-pass kernel (DSPARK_DRAFT_LAUNCH=two_pass or
     // per_pass selects the latter)
-    static int fused = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-      const char* e = getenv("DSPARK_DRAFT_LAUNCH");
-      fused = (e && (std::string(e) == "per_pass" || std::string(e) == "two_pass")) ? 0 : 1;
-    });
-    if (fused) {
+    if (fused_launch_enabled()) {
       const cudaError_t e = launch_draft_fused(a, ws, L, s);
       if (e != cudaErrorNotSupported) return e;
     }

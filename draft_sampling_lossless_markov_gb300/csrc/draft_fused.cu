@@ -108,6 +108,12 @@ struct Params {
   unsigned* gbar;            // grid barrier counter, zero at launch
   unsigned* sched;           // [G + 1, n_mtiles] tile claims of each sweep, zero at launch
   WsHeader* hdr;
+  // RNN head (rnn_E non-null): E_k = tanh(W_o z_k), z_k = [s_k; W1[x_{k-1}]; h_k]
+  const __nv_bfloat16* W_rnn;  // [3r, 2r + H]: gate, candidate and output rows
+  const float* rnn_P;          // [B, G, 3r]: W_rnn[:, 2r:] . h_k of every position
+  float* rnn_S;                // [2][B, r] fp32 state: s_k in buffer k & 1
+  __nv_bfloat16* rnn_E;        // [2][B, r] rows E_k in buffer k & 1
+  unsigned* rnn_done;          // [G, n_mtiles] recurrent units finished, zero at launch
 };
 
 
@@ -423,17 +429,17 @@ __device__ void team_levels(const Params& p, int b, int k, int team, int tw, int
 // over a team of four warps: lane (j, c) of team warp tw takes columns
 // 8 c .. 8 c + 7 of the rows tw r/4 + 4 i + j (128-bit loads, sixteen in flight),
 // the four row phases j are added by shuffles, and red[tw][64] receives the
-// warp's sums (fp32 fma in order within a phase).
-__device__ void chunk_dot(const Params& p, int x, int cstar, int tw, int lane, float* red) {
+// warp's sums (fp32 fma in order within a phase).  erow: E_k of the row
+// (W1[x_{k-1}] for the Markov head, the recurrent row for the RNN head).
+__device__ void chunk_dot(const Params& p, const __nv_bfloat16* erow, int cstar, int tw, int lane, float* red) {
   constexpr unsigned FULL = 0xffffffffu;
-  const int xs = (x < 0 || x >= p.V) ? 0 : x;
   const int c8 = lane & 7, j = lane >> 3;
   const int v = cstar * CW + 8 * c8;
   const bool in = v < p.V;  // V % 8 == 0: the lane's eight columns are in or out together
   const int per = p.r / kTeamWarps;
   const int nt = per / 4;
   const int i0 = tw * per + j;
-  const __nv_bfloat16* e = p.W1 + (size_t)xs * p.r + i0;
+  const __nv_bfloat16* e = erow + i0;
   const __nv_bfloat16* w2 = p.W2 + (size_t)i0 * p.V + v;
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int t0 = 0; t0 < nt; t0 += 16) {
@@ -444,7 +450,10 @@ __device__ void chunk_dot(const Params& p, int x, int cstar, int tw, int lane, f
       const bool ok = in && t0 + t < nt;
       wv[t] = ok ? __ldcg(reinterpret_cast<const uint4*>(w2 + (size_t)(4 * (t0 + t)) * p.V))
                  : make_uint4(0u, 0u, 0u, 0u);
-      ev[t] = ok ? __bfloat162float(e[4 * (t0 + t)]) : 0.f;
+      // (L2: the RNN head's rows are written during this launch)
+      ev[t] = ok ? __bfloat162float(__ushort_as_bfloat16(__ldcg(reinterpret_cast<const unsigned short*>(e) +
+                                                                4 * (t0 + t))))
+                 : 0.f;
     }
 #pragma unroll
     for (int t = 0; t < 16; ++t) {
@@ -529,6 +538,202 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
   }
 }
 
+// RNN head: the recurrent step of position k for the units this CTA owns
+// ([DSpark] 方法细节, "RNN头的实现").  A unit is 32 rows x kRnnCols state
+// columns; units are numbered column groups fastest, and CTA c owns the
+// contiguous range [c n / n_ctas, (c + 1) n / n_ctas), so that consecutive
+// units of a CTA mostly share their rows and z' stays in registers.  The
+// unit's 3 kRnnCols weight rows are staged in scr as fp32, [2r][12] per z'
+// entry (gate g, column c at kRnnCols g + c), each 64-entry segment offset by
+// 16 bytes so that the eight segments' reads fall in distinct banks; the next
+// unit's rows are loaded while the current one computes.  Eight epilogue
+// threads per row: thread s sums z' entries 64 s .. 64 s + 63 of
+// z' = [s_k; W1[x_{k-1}]] (fp32 fma chains in ascending order), the eight sums
+// are added by a fixed shuffle tree (the lower lane's first), then thread
+// c < kRnnCols finishes column c:
+//     pre = W_rnn[:, :2r] z' + P[b, k],  g = sigmoid(pre_g),
+//     s_{k+1} = g s_k + (1 - g) tanh(pre_c),  E_k = tanh(pre_o) (bf16),
+// s_0 = 0 and x_{-1} the anchor.  After its last unit the CTA adds, with
+// release semantics, its unit count of each M-tile m to rnn_done[k, m].
+// False if a token wait gave up.
+constexpr int kRnnCols = 4;
+constexpr int kRnnRows = 32;
+constexpr int kRnnSegBytes = 64 * 3 * kRnnCols * 4 + 16;  // one segment of staged weights (fp32), padded
+constexpr int kRnnStageLd = (3 * kRnnCols * 512 / 8 + kEpiThreads - 1) / kEpiThreads;  // 16-byte loads per thread
+__device__ bool rnn_units(const Params& p, int k, uint8_t* scr, int epi_tid, volatile int* abort_flag) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int r = p.r, K = 2 * r, ldw = 2 * r + p.H, B = p.B;
+  const int nrb = (B + kRnnRows - 1) / kRnnRows;  // row blocks
+  const int ncg = r / kRnnCols;
+  const int nunits = nrb * ncg;
+  const int u_lo = (int)((long long)nunits * blockIdx.x / p.n_ctas);
+  const int u_hi = (int)((long long)nunits * (blockIdx.x + 1) / p.n_ctas);
+  const int seg = epi_tid & 7;   // this thread's 64-entry segment of z'
+  const int rr = epi_tid >> 3;   // this thread's row of the unit
+  const int i0 = seg * 64;
+  const int nld = 3 * kRnnCols * (K / 8);  // 16-byte pieces of a unit's weight rows
+  bool ok = true;
+  // the weight rows of column group cg, piece idx = epi_tid + kEpiThreads j:
+  // row (gate g, column cc) = idx % 12, eight entries from 8 (idx / 12)
+  uint4 wq[kRnnStageLd];
+  auto load_w = [&](int cg) {
+#pragma unroll
+    for (int j = 0; j < kRnnStageLd; ++j) {
+      const int idx = epi_tid + j * kEpiThreads;
+      if (idx < nld) {
+        const int rowi = idx % (3 * kRnnCols), s8 = idx / (3 * kRnnCols);
+        const int g = rowi / kRnnCols, cc = rowi - g * kRnnCols;
+        wq[j] = __ldg(reinterpret_cast<const uint4*>(p.W_rnn + (size_t)(g * r + cg * kRnnCols + cc) * ldw) + s8);
+      }
+    }
+  };
+  for (int u = u_lo; u < u_hi;) {
+    // the units of one row block share z' = [s_k; W1[x_{k-1}]] of its rows
+    const int rb = u / ncg;
+    const int u_end = min(u_hi, (rb + 1) * ncg);
+    const int b = rb * kRnnRows + rr;
+    const bool used = b < B && i0 < K;  // a segment past 2r (r < 256) loads and adds nothing
+    float z[64];
+    if (used && i0 < r) {
+      if (k > 0) {
+        const float4* sq = reinterpret_cast<const float4*>(p.rnn_S + ((size_t)(k & 1) * B + b) * r + i0);
+        float4 v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = __ldcg(sq + q);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          z[4 * q] = v[q].x;
+          z[4 * q + 1] = v[q].y;
+          z[4 * q + 2] = v[q].z;
+          z[4 * q + 3] = v[q].w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) z[q] = 0.f;  // s_0 = 0
+      }
+    } else if (used) {
+      int x = (k == 0) ? p.anchor[b] : token_wait(&p.tokens[(size_t)b * p.G + k - 1], abort_flag);
+      if (x == kTokPending) {
+        ok = false;
+        x = 0;
+      }
+      if (x < 0 || x >= p.V) x = 0;  // reported by the gather
+      const uint4* wp = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r + (i0 - r));
+      uint4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = __ldg(wp + q);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[q]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          z[8 * q + 2 * e] = f.x;
+          z[8 * q + 2 * e + 1] = f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 64; ++q) z[q] = 0.f;
+    }
+  for (; u < u_end; ++u) {
+    const int cg = u - rb * ncg;
+    const int col0 = cg * kRnnCols;
+    load_w(cg);
+    // the finishing operands of the row's kRnnCols columns, copied by its
+    // segment-0 thread into the row's slot: P[b, k] per gate, then s_k
+    float4* fslot = reinterpret_cast<float4*>(scr + 8 * kRnnSegBytes) + 4 * rr;
+    if (seg == 0 && b < B) {
+      if (p.rnn_P) {
+        const float* pr = p.rnn_P + ((size_t)b * p.G + k) * 3 * r + col0;
+        ptx::cp_async16_cg(fslot, pr);
+        ptx::cp_async16_cg(fslot + 1, pr + r);
+        ptx::cp_async16_cg(fslot + 2, pr + 2 * r);
+      } else {
+        fslot[0] = fslot[1] = fslot[2] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (k > 0)
+        ptx::cp_async16_cg(fslot + 3, p.rnn_S + ((size_t)(k & 1) * B + b) * r + col0);
+      else
+        fslot[3] = make_float4(0.f, 0.f, 0.f, 0.f);  // s_0 = 0
+    }
+    // stage this unit's weight rows: entry (i, rowi) at segment i / 64, slot (i % 64) 12 + rowi
+#pragma unroll
+    for (int j = 0; j < kRnnStageLd; ++j) {
+      const int idx = epi_tid + j * kEpiThreads;
+      if (idx < nld) {
+        const int rowi = idx % (3 * kRnnCols), s8 = idx / (3 * kRnnCols);
+        const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&wq[j]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = s8 * 8 + e;
+          reinterpret_cast<float*>(scr + (i >> 6) * kRnnSegBytes)[(i & 63) * 3 * kRnnCols + rowi] =
+              __bfloat162float(hv[e]);
+        }
+      }
+    }
+    epi_sync();
+    float acc[3 * kRnnCols];
+#pragma unroll
+    for (int a = 0; a < 3 * kRnnCols; ++a) acc[a] = 0.f;
+    if (used) {
+      const uint8_t* wseg = scr + seg * kRnnSegBytes;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float4* w = reinterpret_cast<const float4*>(wseg + i * 3 * kRnnCols * 4);
+#pragma unroll
+        for (int h = 0; h < 3; ++h) {
+          const float4 f = w[h];
+          acc[4 * h] = fmaf(f.x, z[i], acc[4 * h]);
+          acc[4 * h + 1] = fmaf(f.y, z[i], acc[4 * h + 1]);
+          acc[4 * h + 2] = fmaf(f.z, z[i], acc[4 * h + 2]);
+          acc[4 * h + 3] = fmaf(f.w, z[i], acc[4 * h + 3]);
+        }
+      }
+    }
+    // the eight segments' sums, lower lane first at every level
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+      for (int a = 0; a < 3 * kRnnCols; ++a) {
+        const float v = __shfl_xor_sync(FULL, acc[a], o);
+        acc[a] = (seg & o) ? __fadd_rn(v, acc[a]) : __fadd_rn(acc[a], v);
+      }
+    if (seg == 0 && b < B) ptx::cp_async_wait_all();
+    __syncwarp();  // the slot's copies seen by the row's other threads
+    if (b < B && seg < kRnnCols) {
+      const float* fs = reinterpret_cast<const float*>(fslot);
+      float pg = fs[seg], pc = fs[4 + seg], po = fs[8 + seg];
+      const float sp = fs[12 + seg];
+#pragma unroll
+      for (int c = 0; c < kRnnCols; ++c)
+        if (c == seg) {
+          pg += acc[c];
+          pc += acc[kRnnCols + c];
+          po += acc[2 * kRnnCols + c];
+        }
+      const int col = col0 + seg;
+      const float gt = 1.f / (1.f + expf(-pg));
+      p.rnn_S[((size_t)((k + 1) & 1) * B + b) * r + col] = gt * sp + (1.f - gt) * tanhf(pc);
+      p.rnn_E[((size_t)(k & 1) * B + b) * r + col] = __float2bfloat16_rn(tanhf(po));
+    }
+    // every read of scr before the next unit's staging
+    epi_sync();
+  }
+  }
+  // every write of the units before the counts (the last epi_sync above
+  // orders them before thread 0's release)
+  if (epi_tid == 0 && u_lo < u_hi) {
+    constexpr int kRbPerTile = BM / kRnnRows;
+    const int m_lo = (u_lo / ncg) / kRbPerTile, m_hi = ((u_hi - 1) / ncg) / kRbPerTile;
+    for (int m = m_lo; m <= m_hi; ++m) {
+      const int a0 = max(u_lo, m * kRbPerTile * ncg), a1 = min(u_hi, (m + 1) * kRbPerTile * ncg);
+      atom_add_acq_rel(&p.rnn_done[(size_t)k * p.n_mtiles + m], (unsigned)(a1 - a0));
+    }
+  }
+  return ok;
+}
+
 // The select of position k for the rows this CTA serves (rows blockIdx.x +
 // n_ctas j), by the epilogue's two teams of four warps (team t takes j = t,
 // t + 2, ..): the pass over the row's chunk partials, then for a sampled row
@@ -556,7 +761,10 @@ __device__ __forceinline__ void select_rows(const Params& p, int k, uint8_t* scr
       // levels pass) with the recompute's loads
       if (tw == 0 && cstar * CW + 2 * lane < p.V)
         upair = __ldcg(reinterpret_cast<const unsigned*>(p.U + ((size_t)rb * G + k) * p.V + cstar * CW + 2 * lane));
-      chunk_dot(p, rec->x, cstar, tw, lane, red);
+      // E_k of the row: the recurrent row (RNN head) or W1[x_{k-1}]
+      const int xk = (rec->x < 0 || rec->x >= p.V) ? 0 : rec->x;
+      const __nv_bfloat16* erow = p.rnn_E ? p.rnn_E + ((size_t)(k & 1) * p.B + rb) * p.r : p.W1 + (size_t)xk * p.r;
+      chunk_dot(p, erow, cstar, tw, lane, red);
       team_sync(team);
       if (tw == 0) chunk_walk(p, rec, k, lane, red, upair);
     }
@@ -578,6 +786,8 @@ __device__ __forceinline__ void select_rows(const Params& p, int k, uint8_t* scr
   epi_sync();
 }
 
+// kRnn: the RNN head's rows (recurrent units in each gather); else W1 rows.
+template <bool kRnn>
 __global__ void __launch_bounds__(kThreads, 1)
     k_draft_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2,
                   const __grid_constant__ CUtensorMap tmPd, Params p) {
@@ -842,6 +1052,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint4* src = reinterpret_cast<const uint4*>(p.W1 + (size_t)x * r);
+      if constexpr (kRnn) {
+        // the recurrent units of position k, then this M-tile's rows E_k once
+        // every unit of the M-tile has finished
+        if (!rnn_units(p, k, sStg, epi_tid, abort_flag)) fail();
+        if (epi_tid == 0) {
+          // the units of this M-tile: its row blocks x the column groups
+          const int rb_hi = min((m_tile + 1) * BM, ((p.B + kRnnRows - 1) / kRnnRows) * kRnnRows);
+          const unsigned target = (unsigned)((rb_hi - m_tile * BM) / kRnnRows * (r / kRnnCols));
+          const unsigned* cnt = p.rnn_done + (size_t)k * p.n_mtiles + m_tile;
+          int okw = *abort_flag ? 0 : 1;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (okw && ld_acquire(cnt) < target) {
+            if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) okw = 0;
+            __nanosleep(32);
+          }
+          *s_ok = okw;
+        }
+        epi_sync();
+        if (!*s_ok && epi_tid == 0) fail();
+        src = reinterpret_cast<const uint4*>(p.rnn_E + ((size_t)(k & 1) * p.B + (vrow ? b : 0)) * r);
+      }
       const uint32_t slot = tmem + lane_bits + (uint32_t)((k & 1) * kESlotCols);
       // group g copies the 64-element pieces g, g + 2 of its rows (all loads
       // in flight before the first store)
@@ -852,7 +1083,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pc = g + i * kGroups;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const uint4 qv = (vrow && pc < npieces) ? src[pc * 8 + e] : make_uint4(0u, 0u, 0u, 0u);
+          // (L2 for the RNN head's rows: written during this launch)
+          const uint4 qv = (vrow && pc < npieces) ? (kRnn ? __ldcg(src + pc * 8 + e) : src[pc * 8 + e])
+                                                  : make_uint4(0u, 0u, 0u, 0u);
           wv[i][4 * e] = qv.x;
           wv[i][4 * e + 1] = qv.y;
           wv[i][4 * e + 2] = qv.z;
@@ -1766,6 +1999,12 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   const cuuint64_t V = (cuuint64_t)d.V, G = (cuuint64_t)d.gamma, B = (cuuint64_t)d.B, r = (cuuint64_t)d.r;
   // small batches: the vocabulary on the MMA's M side (k_draft_narrow)
   const bool narrow = d.B <= fz::nrw::NB && fz::narrow_enabled();
+  // the RNN head runs in the 128-row form, with p_d rows, and reads W_rnn
+  // rows with 16-byte loads
+  const bool rnn = a.head == DSPARK_HEAD_RNN;
+  if (rnn && (narrow || !a.pd_rows || !a.W_rnn || (reinterpret_cast<uintptr_t>(a.W_rnn) % 16) != 0 ||
+              ((2 * d.r + d.H) % 8) != 0))
+    return cudaErrorNotSupported;
   CUtensorMap tmU, tmW2, tmPd = {};  // tmPd stays unused without p_d rows and in the small-batch form
   if (narrow) {
     // U rows of all requests of one position, 128 columns, unswizzled
@@ -1794,7 +2033,8 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     if (!narrow && a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  const void* kfn = narrow ? (const void*)fz::k_draft_narrow : (const void*)fz::k_draft_fused;
+  const void* kfn = narrow ? (const void*)fz::k_draft_narrow
+                           : (rnn ? (const void*)fz::k_draft_fused<true> : (const void*)fz::k_draft_fused<false>);
   const size_t smem = narrow ? fz::nrw::kSmemBytes : fz::kSmemBytes;
   if (const cudaError_t ae = ensure_smem_limit(kfn, (int)smem); ae != cudaSuccess) return ae;
 
@@ -1833,8 +2073,26 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.gbar = reinterpret_cast<unsigned*>(ws + L.gbar);
   p.sched = reinterpret_cast<unsigned*>(ws + L.gbar + 16);
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  // the grid-barrier counter and the tile claims of every sweep
-  cudaError_t e = cudaMemsetAsync(p.gbar, 0, 16 + sizeof(unsigned) * (size_t)(d.gamma + 1) * n_mtiles, s);
+  p.W_rnn = nullptr;
+  p.rnn_P = nullptr;
+  p.rnn_S = nullptr;
+  p.rnn_E = nullptr;
+  p.rnn_done = p.sched + (size_t)(d.gamma + 1) * n_mtiles;
+  if (rnn) {
+    // the h part of every position's projection, one GEMM before the sweeps
+    float* P = reinterpret_cast<float*>(ws + L.rnn_p);
+    if (d.H > 0) {
+      const cudaError_t he = launch_rnn_hproj(a, P, reinterpret_cast<WsHeader*>(ws), s);
+      if (he != cudaSuccess) return he;
+      p.rnn_P = P;
+    }
+    p.W_rnn = static_cast<const __nv_bfloat16*>(a.W_rnn);
+    p.rnn_S = reinterpret_cast<float*>(ws + L.rnn_s);
+    p.rnn_E = reinterpret_cast<__nv_bfloat16*>(ws + L.E);
+  }
+  // the grid-barrier counter, the tile claims of every sweep and the
+  // recurrent-unit counters of every position
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, 16 + sizeof(unsigned) * (size_t)(2 * d.gamma + 1) * n_mtiles, s);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_ctas);
@@ -1848,7 +2106,8 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   cfg.numAttrs = 1;
   count_launches(1);
   if (narrow) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow, tmU, tmW2, p);
-  return cudaLaunchKernelEx(&cfg, fz::k_draft_fused, tmU, tmW2, tmPd, p);
+  if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true>, tmU, tmW2, tmPd, p);
+  return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false>, tmU, tmW2, tmPd, p);
 }
 
 }  // namespace dspark

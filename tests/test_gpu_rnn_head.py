@@ -91,6 +91,29 @@ def test_rnn_head_full_size_sampled_requests():
     check_no_error(ws)
 
 
+@pytest.mark.parametrize("B,G,V,r,H,subset", [
+    # about 13 recurrent units per CTA: unit ranges cross row blocks and M-tiles,
+    # a ragged last row block (8 rows) and M-tile (104 rows)
+    (1000, 3, 8200, 256, 16, [0, 31, 32, 127, 128, 300, 511, 767, 895, 896, 991, 999]),
+    # no hidden state (no h projection), rank 64: a ragged 12-row last block
+    (300, 3, 4104, 64, 0, [0, 63, 64, 127, 128, 255, 256, 287, 288, 299]),
+    # rank 192: six of the eight segments of z' in use
+    (200, 4, 8200, 192, 8, [0, 31, 32, 127, 128, 191, 192, 199]),
+])
+def test_rnn_head_many_units_per_cta(B, G, V, r, H, subset):
+    wl = synth.Workload("rnn_units", B, G, V, H, r, "bf16", "mixed", synth.SCHED_GREEDY, "tiny", seed=9)
+    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    Wr = synth.rnn_weights(r, H, "bf16", 6, "cuda")
+    out, ws = _run(inp, Wr)
+    _invariants(gpu_np(out), V)
+    idx = torch.tensor(subset, device="cuda")
+    g = {k: v.index_select(0, idx).cpu().numpy() for k, v in out.items()}
+    o = oracle_draft(**np_inputs(inp, idx), W_rnn=to_np64(Wr), rnn_row_dtype="bf16")
+    st = compare_draft(g, o, rtol_for("bf16"))
+    assert st["n_tokens_compared"] >= len(subset)
+    check_no_error(ws)
+
+
 def test_rnn_head_differs_from_the_markov_head():
     # same inputs: the recurrent rows change the draft distribution
     wl = synth.WORKLOADS["tiny"]
@@ -128,9 +151,11 @@ print("ok")
 """
 
 
-@pytest.mark.parametrize("env", [{"DSPARK_DRAFT_PATH": "cuda_core"}, {"DSPARK_DRAFT_LAUNCH": "per_pass"}])
+@pytest.mark.parametrize("env", [{"DSPARK_DRAFT_PATH": "cuda_core"}, {"DSPARK_DRAFT_LAUNCH": "per_pass"},
+                                 {"DSPARK_DRAFT_LAUNCH": "two_pass"}])
 def test_rnn_head_on_the_other_launch_paths(env):
-    # bf16 tensor-core shapes on the CUDA-core path, and with one launch per pass
+    # bf16 tensor-core shapes on the CUDA-core path, with one launch per pass, and
+    # with one launch per position (the recurrent step between launches)
     import os
     import subprocess
     import sys
