@@ -357,86 +357,134 @@ constexpr size_t kSmemSchedMax = 200 * 1024;  // dynamic shared memory of k_sche
 
 __device__ __forceinline__ float key_to_a(uint64_t kv) { return __uint_as_float(~(uint32_t)(kv >> 32)); }
 
-// a (in (0, 1], from the sort key) as a fixed-point integer with 52 fraction
-// bits, by integer operations on its fp32 fields: exact for a >= 2^-28,
-// truncated below (at most 2^-52 per candidate), 0 for subnormals.  Sums of
-// these are exact, so the running survival sum of the Theta scan needs no fp64
-// adds.
-__device__ __forceinline__ long long key_to_fix52(uint64_t kv) {
+// a (in (0, 1], from the sort key) as a fixed-point integer with 50 fraction
+// bits, by integer operations on its fp32 fields: exact for a >= 2^-27,
+// truncated below (by less than 2^-50 per candidate), 0 for subnormals.  Sums
+// of these are exact in 64 unsigned bits for up to 2^14 candidates (a <= 1), so
+// the running survival sum of the Theta scan needs no fp64 adds; the
+// truncation moves B + sum by less than gamma 2^-50 relative.
+__device__ __forceinline__ unsigned long long key_to_fix(uint64_t kv) {
   const uint32_t bits = ~(uint32_t)(kv >> 32);
   const int e = (int)((bits >> 23) & 0xFFu);
   if (e == 0) return 0;
-  const long long m = (long long)((bits & 0x7FFFFFu) | 0x800000u);
-  const int sh = e - 98;  // m 2^(e - 150) 2^52
+  const unsigned long long m = (unsigned long long)((bits & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 100;  // m 2^(e - 150) 2^50
   return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0);
 }
-constexpr double kFix52 = 2.220446049250313080847263336181640625e-16;  // 2^-52
+constexpr double kFixUnit = 8.8817841970012523233890533447265625e-16;  // 2^-50
+static_assert(kSmemSortMax <= (1 << 14), "fixed-point survival sums hold 2^14 candidates");
 
-__device__ __forceinline__ long long block_excl_scan_i64(long long v, long long* sm, long long& total) {
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned long long* sm,
+                                                                  unsigned long long& total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  long long x = v;
+  unsigned long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long t = __shfl_up_sync(0xffffffffu, x, o);
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += t;
   }
   if (lane == 31) sm[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    long long z = sm[lane];
+    unsigned long long z = sm[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const long long t = __shfl_up_sync(0xffffffffu, z, o);
+      const unsigned long long t = __shfl_up_sync(0xffffffffu, z, o);
       if (lane >= o) z += t;
     }
-    const long long ze = __shfl_up_sync(0xffffffffu, z, 1);
+    const unsigned long long ze = __shfl_up_sync(0xffffffffu, z, 1);
     sm[lane] = (lane == 0) ? 0 : ze;
     if (lane == 31) sm[32] = z;
   }
   __syncthreads();
-  long long xe = __shfl_up_sync(0xffffffffu, x, 1);  // exclusive prefix within the warp
+  unsigned long long xe = __shfl_up_sync(0xffffffffu, x, 1);  // exclusive prefix within the warp
   if (lane == 0) xe = 0;
-  const long long res = sm[wid] + xe;
+  const unsigned long long res = sm[wid] + xe;
   total = sm[32];
   __syncthreads();
   return res;
 }
 
+// Theta_j = (B + S_j 2^-50) SPS[B + j] in fp64, the value the sorted-path scan
+// compares
+__device__ __forceinline__ double theta64(int B, unsigned long long S, double sps) {
+  return ((double)B + (double)S * kFixUnit) * sps;
+}
+
+// The same in fp32, with a relative error below 2^-21 for a positive SPS
+// entry in fp32's normal range, else 0: S rounded to fp32 (one rounding), the
+// sum with B (one), the SPS entry truncated to fp32 by its bit fields (below
+// 2^-23), the product (one).  No fp64 arithmetic.
+__device__ __forceinline__ float theta32(int B, unsigned long long S, double sps) {
+  const unsigned long long b = (unsigned long long)__double_as_longlong(sps);
+  const int e = (int)((b >> 52) & 0x7FF) - 1023 + 127;
+  if ((b >> 63) || e <= 0 || e >= 255) return 0.f;
+  const float s32 = __uint_as_float(((unsigned)e << 23) | (unsigned)((b >> 29) & 0x7FFFFFu));
+  return __fmul_rn(__fadd_rn((float)B, __fmul_rn(__ull2float_rn(S), 0x1p-50f)), s32);
+}
+
+// Theta_{j+1} > Theta_j as the fp64 values compare: decided in fp32 when the
+// two fp32 values differ by more than 2^-19 relative (twice the bound on their
+// combined error), by the fp64 values otherwise
+__device__ __forceinline__ bool theta_rises(int B, unsigned long long S0, double sps0, float t0,
+                                            unsigned long long S1, double sps1, float t1) {
+  constexpr float kLo = 1e-30f, kHi = 1e30f;
+  if (t0 > kLo && t0 < kHi && t1 > kLo && t1 < kHi) {
+    if (t1 > __fmul_rn(t0, 1.f + 0x1p-19f)) return true;
+    if (t1 < __fmul_rn(t0, 1.f - 0x1p-19f)) return false;
+  }
+  return theta64(B, S1, sps1) > theta64(B, S0, sps0);
+}
+
 // Merges sorted runs of length run0 (a power of two) in a[0, n_pad) (n_pad /
 // run0 a power of two, all values distinct, n_pad <= kSmemSortMax) into one
-// sorted run; b is scratch of the same size.  Each thread places its elements
-// i = tid, tid + 1024, .. (merge path: an element's place is its rank in its
-// own run plus its rank in the partner run, found by halving steps), the
-// searches of all its elements interleaved.  Returns the buffer that holds the
-// result.
-template <int EPT>  // elements per thread: n_pad <= EPT * SCH_THREADS
+// sorted run; b is scratch of the same size.  Each pass merges pairs of runs
+// of width w into runs of 2w along the merge path: thread t writes outputs
+// t EPT .. t EPT + EPT - 1, finding by one halving search how many of the
+// outputs before its first come from the left run (its diagonal's split),
+// then taking the smaller head of the two runs EPT times.  Returns the buffer
+// that holds the result.
+template <int EPT>  // outputs per thread: n_pad <= EPT * SCH_THREADS
 __device__ uint64_t* merge_runs_t(uint64_t* a, uint64_t* b, int n_pad, int run0) {
-  const int tid = threadIdx.x;
+  const int o0 = threadIdx.x * EPT;
+  const bool act = o0 < n_pad;
   for (int w = run0; w < n_pad; w <<= 1) {
-    uint64_t x[EPT];
-    int lo[EPT], oth[EPT];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const int i = tid + e * SCH_THREADS;
-      lo[e] = 0;
-      oth[e] = 0;
-      x[e] = 0;
-      if (i < n_pad) {
-        x[e] = a[i];
-        oth[e] = (i & ~(2 * w - 1)) + ((i & w) ? 0 : w);  // start of the partner run
+    if (act) {
+      int blk = o0 & ~(2 * w - 1);  // the pair of runs: [blk, blk + w) and [blk + w, blk + 2w)
+      const int d = o0 - blk;
+      const uint64_t* L = a + blk;
+      const uint64_t* Rr = L + w;
+      int lo = max(0, d - w), hi = min(d, w);
+      while (lo < hi) {  // the split: L[0, ia) and Rr[0, d - ia) precede output d
+        const int mid = (lo + hi) >> 1;
+        if (L[mid] < Rr[d - 1 - mid])
+          lo = mid + 1;
+        else
+          hi = mid;
       }
-    }
-    for (int step = w >> 1; step > 0; step >>= 1) {
+      int ia = lo, ib = d - lo;
+      uint64_t va = ia < w ? L[ia] : ~0ull, vb = ib < w ? Rr[ib] : ~0ull;  // an empty run's head sorts last
 #pragma unroll
-      for (int e = 0; e < EPT; ++e)
-        if (tid + e * SCH_THREADS < n_pad) lo[e] += a[oth[e] + lo[e] + step - 1] < x[e] ? step : 0;
-    }
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const int i = tid + e * SCH_THREADS;
-      if (i < n_pad) {
-        lo[e] += a[oth[e] + lo[e]] < x[e] ? 1 : 0;
-        b[(i & ~(2 * w - 1)) + (i & (w - 1)) + lo[e]] = x[e];
+      for (int k = 0; k < EPT; ++k) {
+        if (k > 0 && ((o0 + k) & (2 * w - 1)) == 0) {
+          // (2w < EPT) the next pair of runs starts inside this thread's outputs
+          blk += 2 * w;
+          L = a + blk;
+          Rr = L + w;
+          ia = 0;
+          ib = 0;
+          va = L[0];
+          vb = Rr[0];
+        }
+        const bool from_l = va < vb;
+        b[o0 + k] = from_l ? va : vb;
+        if (from_l) {
+          ++ia;
+          va = ia < w ? L[ia] : ~0ull;
+        } else {
+          ++ib;
+          vb = ib < w ? Rr[ib] : ~0ull;
+        }
       }
     }
     __syncthreads();
@@ -509,7 +557,7 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   int* s_ell = reinterpret_cast<int*>(s_sps + B * (1 + G) + 1);
   float* s_c = reinterpret_cast<float*>(kv2);  // [B gamma] c', until the merge reuses kv2
   __shared__ uint32_t sm_u[40];
-  __shared__ long long sm_l[40];
+  __shared__ unsigned long long sm_l[40];
   __shared__ double sm_v[32];
   __shared__ int sm_i[32];
   __shared__ int s_first;
@@ -585,15 +633,15 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     const uint64_t* prv = merge_runs(kv, kv2, n_pad, R);
     const int chp = (nprev + SCH_THREADS - 1) / SCH_THREADS;
     const int p_lo = min(tid * chp, nprev), p_hi = min(p_lo + chp, nprev);
-    long long loc = 0;
-    for (int i = p_lo; i < p_hi; ++i) loc += key_to_fix52(prv[i]);
-    long long tot;
-    long long S = block_excl_scan_i64(loc, sm_l, tot);
+    unsigned long long loc = 0;
+    for (int i = p_lo; i < p_hi; ++i) loc += key_to_fix(prv[i]);
+    unsigned long long tot;
+    unsigned long long S = block_excl_scan_u64(loc, sm_l, tot);
     double bv = tid == 0 ? (double)B * s_sps[B] : -INFINITY;  // Theta_0: nothing admitted
     int bi = tid == 0 ? 0 : INT_MAX;
     for (int i = p_lo; i < p_hi; ++i) {
-      S += key_to_fix52(prv[i]);
-      const double theta = ((double)B + (double)S * kFix52) * s_sps[B + i + 1];
+      S += key_to_fix(prv[i]);
+      const double theta = theta64(B, S, s_sps[B + i + 1]);
       if (theta > bv) {
         bv = theta;
         bi = i + 1;
@@ -605,15 +653,15 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     const int ncur = (int)build_runs(a.conf_logit, true, k0, v0);  // every read of the earlier path ended before the scan's barriers
     const uint64_t* cur = merge_runs(kv, kv2, n_pad, R);
     const int nadm = min(K, ncur);
-    long long sl = 0;
+    unsigned long long sl = 0;
     for (int i = tid; i < nadm; i += SCH_THREADS) {
       const uint32_t v = (uint32_t)cur[i];
       atomicMax(&s_ell[v / G], (int)(v % G) + 1);
-      sl += key_to_fix52(cur[i]);
+      sl += key_to_fix(cur[i]);
     }
-    long long sadm;
-    block_excl_scan_i64(sl, sm_l, sadm);
-    if (tid == 0) *a.theta_best = ((double)B + (double)sadm * kFix52) * s_sps[B + nadm];
+    unsigned long long sadm;
+    block_excl_scan_u64(sl, sm_l, sadm);
+    if (tid == 0) *a.theta_best = theta64(B, sadm, s_sps[B + nadm]);
   } else if (a.mode != DSPARK_SCHED_OFF) {
     const uint32_t ncand = build_runs(a.conf_logit, true, k0, v0);
     // ---- 2. one sorted run: ascending (key, index) = descending a, ties by index ----
@@ -622,24 +670,28 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     const int nc = (int)ncand;
     const int ch = (nc + SCH_THREADS - 1) / SCH_THREADS;
     const int c_lo = min(tid * ch, nc), c_hi = min(c_lo + ch, nc);
-    // survival sums in 52-bit fixed point (exact adds); Theta in fp64
-    long long loc = 0;
-    for (int i = c_lo; i < c_hi; ++i) loc += key_to_fix52(srt[i]);
-    long long tot;
-    const long long pre = block_excl_scan_i64(loc, sm_l, tot);
+    // survival sums in fixed point (exact adds); Theta compared as in fp64
+    unsigned long long loc = 0;
+    for (int i = c_lo; i < c_hi; ++i) loc += key_to_fix(srt[i]);
+    unsigned long long tot;
+    const unsigned long long pre_s = block_excl_scan_u64(loc, sm_l, tot);
     if (tid == 0) s_first = nc + 1;
     __syncthreads();
-    {
-      long long S = pre;
-      double theta_prev = ((double)B + (double)S * kFix52) * s_sps[B + c_lo];
+    if (c_lo < c_hi) {
+      unsigned long long S = pre_s;
+      double sp = s_sps[B + c_lo];
+      float t_prev = theta32(B, S, sp);
       for (int i = c_lo; i < c_hi; ++i) {  // sorted position i is candidate number i + 1
-        S += key_to_fix52(srt[i]);
-        const double theta = ((double)B + (double)S * kFix52) * s_sps[B + i + 1];
-        if (!(theta > theta_prev)) {
+        const unsigned long long S1 = S + key_to_fix(srt[i]);
+        const double sp1 = s_sps[B + i + 1];
+        const float t = theta32(B, S1, sp1);
+        if (!theta_rises(B, S, sp, t_prev, S1, sp1, t)) {
           atomicMin(&s_first, i + 1);
           break;
         }
-        theta_prev = theta;
+        S = S1;
+        sp = sp1;
+        t_prev = t;
       }
     }
     __syncthreads();
@@ -647,9 +699,9 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
     if (nstar == 0) {
       if (tid == 0) s_theta_best = (double)B * s_sps[B];
     } else if (nstar - 1 >= c_lo && nstar - 1 < c_hi) {
-      long long S = pre;
-      for (int i = c_lo; i < nstar; ++i) S += key_to_fix52(srt[i]);
-      s_theta_best = ((double)B + (double)S * kFix52) * s_sps[B + nstar];
+      unsigned long long S = pre_s;
+      for (int i = c_lo; i < nstar; ++i) S += key_to_fix(srt[i]);
+      s_theta_best = theta64(B, S, s_sps[B + nstar]);
     }
     // ---- 4. l_r = number of admitted (r, .) candidates (= largest admitted j) ----
     for (int i = tid; i < nstar; i += SCH_THREADS) {

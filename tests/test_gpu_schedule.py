@@ -82,6 +82,17 @@ def test_schedule_workload_sizes(B, G):
     assert 0 <= g["ell"].min() and g["ell"].max() <= G
 
 
+def test_schedule_survival_sums_past_2048():
+    # confident drafts at B1024 gamma8 (8192 slots, the shared-memory path): the
+    # admitted survival products sum to about 7300, past 2^11, where a sum with
+    # 52 fraction bits would no longer fit a signed 64-bit integer
+    B, G = 1024, 8
+    z, tau, sps, anchor, tokens = _case(21, B, G, z_scale=0.5, z_shift=4.0)
+    compared, g, o = _check(z, tau, sps, anchor, tokens, 1)
+    assert compared
+    assert int(g["ell"].sum()) > 7000 and float(o["a"][o["a"] > 0].sum()) > 4096
+
+
 def test_schedule_off_mode():
     z, tau, sps, anchor, tokens = _case(3, 50, 6)
     compared, g, o = _check(z, tau, None, anchor, tokens, 0)
