@@ -71,9 +71,13 @@ def test_schedule_random_small(seed):
     assert compared
 
 
-@pytest.mark.parametrize("B,G", [(256, 15), (256, 7), (1024, 7), (4096, 16), (65536, 1)])
+@pytest.mark.parametrize("B,G", [(256, 15), (256, 7), (1024, 7), (4096, 16), (65536, 1),
+                                 (2500, 2), (3000, 1)])
 def test_schedule_workload_sizes(B, G):
-    # up to the 65536-candidate limit; config-2 STS temperatures and SPS curve
+    # up to the 65536-candidate limit; config-2 STS temperatures and SPS curve.
+    # B2500 gamma2 and B3000 gamma1 take the shared-memory merge with 8 and 4
+    # outputs per thread over runs of 2 and 1 slots (a thread's outputs span
+    # several run pairs in the first passes)
     rng = np.random.default_rng(B + G)
     tau = rng.uniform(0.8, 1.5, G).astype(np.float32)
     z, _, sps, anchor, tokens = _case(B * 7 + G, B, G)
