@@ -539,28 +539,37 @@ __device__ void chunk_walk(const Params& p, const SelRec* rec, int k, int lane, 
 }
 
 // RNN head: the recurrent step of position k for the units this CTA owns
-// ([DSpark] 方法细节, "RNN头的实现").  A unit is 32 rows x kRnnCols state
-// columns; units are numbered column groups fastest, and CTA c owns the
+// ([DSpark] 方法细节, "RNN头的实现").  A unit is 32 rows x C state columns
+// (C = 4 in the 128-row form, 2 in the small-batch form, whose shared memory
+// is smaller); units are numbered column groups fastest, and CTA c owns the
 // contiguous range [c n / n_ctas, (c + 1) n / n_ctas), so that consecutive
 // units of a CTA mostly share their rows and z' stays in registers.  The
-// unit's 3 kRnnCols weight rows are staged in scr as fp32, [2r][12] per z'
-// entry (gate g, column c at kRnnCols g + c), each 64-entry segment offset by
-// 16 bytes so that the eight segments' reads fall in distinct banks; the next
-// unit's rows are loaded while the current one computes.  Eight epilogue
+// unit's 3 C weight rows are staged in scr as fp32, [2r][3C] per z' entry
+// (gate g, column c at C g + c), each 64-entry segment offset by 16 bytes so
+// that the eight segments' reads fall in distinct banks.  Eight epilogue
 // threads per row: thread s sums z' entries 64 s .. 64 s + 63 of
 // z' = [s_k; W1[x_{k-1}]] (fp32 fma chains in ascending order), the eight sums
 // are added by a fixed shuffle tree (the lower lane's first), then thread
-// c < kRnnCols finishes column c:
+// c < C finishes column c:
 //     pre = W_rnn[:, :2r] z' + P[b, k],  g = sigmoid(pre_g),
 //     s_{k+1} = g s_k + (1 - g) tanh(pre_c),  E_k = tanh(pre_o) (bf16),
 // s_0 = 0 and x_{-1} the anchor.  After its last unit the CTA adds, with
 // release semantics, its unit count of each M-tile m to rnn_done[k, m].
 // False if a token wait gave up.
-constexpr int kRnnCols = 4;
 constexpr int kRnnRows = 32;
-constexpr int kRnnSegBytes = 64 * 3 * kRnnCols * 4 + 16;  // one segment of staged weights (fp32), padded
-constexpr int kRnnStageLd = (3 * kRnnCols * 512 / 8 + kEpiThreads - 1) / kEpiThreads;  // 16-byte loads per thread
+template <int C>
+struct RnnUnit {
+  static constexpr int kSegBytes = 64 * 3 * C * 4 + 16;  // one segment of staged weights (fp32), padded
+  static constexpr int kStageLd = (3 * C * 512 / 8 + kEpiThreads - 1) / kEpiThreads;  // 16-byte loads per thread
+  static constexpr int kScrBytes = 8 * kSegBytes + kRnnRows * 64;  // segments, then a float4 x 4 slot per row
+};
+constexpr int kWideRnnCols = 4;  // state columns of a unit in the 128-row form
+static_assert(RnnUnit<kWideRnnCols>::kScrBytes <= kEpiWarps * kStagingPerWarp, "unit scratch in the p_d staging");
+
+template <int kRnnCols>
 __device__ bool rnn_units(const Params& p, int k, uint8_t* scr, int epi_tid, volatile int* abort_flag) {
+  constexpr int kRnnSegBytes = RnnUnit<kRnnCols>::kSegBytes;
+  constexpr int kRnnStageLd = RnnUnit<kRnnCols>::kStageLd;
   constexpr unsigned FULL = 0xffffffffu;
   const int r = p.r, K = 2 * r, ldw = 2 * r + p.H, B = p.B;
   const int nrb = (B + kRnnRows - 1) / kRnnRows;  // row blocks
@@ -641,11 +650,13 @@ __device__ bool rnn_units(const Params& p, int k, uint8_t* scr, int epi_tid, vol
     const int col0 = cg * kRnnCols;
     load_w(cg);
     // the finishing operands of the row's kRnnCols columns, copied by its
-    // segment-0 thread into the row's slot: P[b, k] per gate, then s_k
+    // segment-0 thread into the row's slot: the aligned four columns that
+    // hold them, of P[b, k] per gate, then of s_k
     float4* fslot = reinterpret_cast<float4*>(scr + 8 * kRnnSegBytes) + 4 * rr;
+    const int c4 = col0 & ~3;
     if (seg == 0 && b < B) {
       if (p.rnn_P) {
-        const float* pr = p.rnn_P + ((size_t)b * p.G + k) * 3 * r + col0;
+        const float* pr = p.rnn_P + ((size_t)b * p.G + k) * 3 * r + c4;
         ptx::cp_async16_cg(fslot, pr);
         ptx::cp_async16_cg(fslot + 1, pr + r);
         ptx::cp_async16_cg(fslot + 2, pr + 2 * r);
@@ -653,7 +664,7 @@ __device__ bool rnn_units(const Params& p, int k, uint8_t* scr, int epi_tid, vol
         fslot[0] = fslot[1] = fslot[2] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       if (k > 0)
-        ptx::cp_async16_cg(fslot + 3, p.rnn_S + ((size_t)(k & 1) * B + b) * r + col0);
+        ptx::cp_async16_cg(fslot + 3, p.rnn_S + ((size_t)(k & 1) * B + b) * r + c4);
       else
         fslot[3] = make_float4(0.f, 0.f, 0.f, 0.f);  // s_0 = 0
     }
@@ -680,14 +691,24 @@ __device__ bool rnn_units(const Params& p, int k, uint8_t* scr, int epi_tid, vol
       const uint8_t* wseg = scr + seg * kRnnSegBytes;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float4* w = reinterpret_cast<const float4*>(wseg + i * 3 * kRnnCols * 4);
+        if constexpr (kRnnCols == 4) {
+          const float4* w = reinterpret_cast<const float4*>(wseg + i * 3 * kRnnCols * 4);
 #pragma unroll
-        for (int h = 0; h < 3; ++h) {
-          const float4 f = w[h];
-          acc[4 * h] = fmaf(f.x, z[i], acc[4 * h]);
-          acc[4 * h + 1] = fmaf(f.y, z[i], acc[4 * h + 1]);
-          acc[4 * h + 2] = fmaf(f.z, z[i], acc[4 * h + 2]);
-          acc[4 * h + 3] = fmaf(f.w, z[i], acc[4 * h + 3]);
+          for (int h = 0; h < 3; ++h) {
+            const float4 f = w[h];
+            acc[4 * h] = fmaf(f.x, z[i], acc[4 * h]);
+            acc[4 * h + 1] = fmaf(f.y, z[i], acc[4 * h + 1]);
+            acc[4 * h + 2] = fmaf(f.z, z[i], acc[4 * h + 2]);
+            acc[4 * h + 3] = fmaf(f.w, z[i], acc[4 * h + 3]);
+          }
+        } else {
+          const float2* w = reinterpret_cast<const float2*>(wseg + i * 3 * kRnnCols * 4);
+#pragma unroll
+          for (int h = 0; h < 3 * kRnnCols / 2; ++h) {
+            const float2 f = w[h];
+            acc[2 * h] = fmaf(f.x, z[i], acc[2 * h]);
+            acc[2 * h + 1] = fmaf(f.y, z[i], acc[2 * h + 1]);
+          }
         }
       }
     }
@@ -702,7 +723,7 @@ __device__ bool rnn_units(const Params& p, int k, uint8_t* scr, int epi_tid, vol
     if (seg == 0 && b < B) ptx::cp_async_wait_all();
     __syncwarp();  // the slot's copies seen by the row's other threads
     if (b < B && seg < kRnnCols) {
-      const float* fs = reinterpret_cast<const float*>(fslot);
+      const float* fs = reinterpret_cast<const float*>(fslot) + (col0 - c4);
       float pg = fs[seg], pc = fs[4 + seg], po = fs[8 + seg];
       const float sp = fs[12 + seg];
 #pragma unroll
@@ -1055,11 +1076,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kRnn) {
         // the recurrent units of position k, then this M-tile's rows E_k once
         // every unit of the M-tile has finished
-        if (!rnn_units(p, k, sStg, epi_tid, abort_flag)) fail();
+        if (!rnn_units<kWideRnnCols>(p, k, sStg, epi_tid, abort_flag)) fail();
         if (epi_tid == 0) {
           // the units of this M-tile: its row blocks x the column groups
           const int rb_hi = min((m_tile + 1) * BM, ((p.B + kRnnRows - 1) / kRnnRows) * kRnnRows);
-          const unsigned target = (unsigned)((rb_hi - m_tile * BM) / kRnnRows * (r / kRnnCols));
+          const unsigned target = (unsigned)((rb_hi - m_tile * BM) / kRnnRows * (r / kWideRnnCols));
           const unsigned* cnt = p.rnn_done + (size_t)k * p.n_mtiles + m_tile;
           int okw = *abort_flag ? 0 : 1;
           const uint64_t t0 = ptx::globaltimer_ns();
@@ -1378,7 +1399,9 @@ constexpr uint32_t kScrBytes = 4096;
 constexpr uint32_t kOffRow = kOffScr + kScrBytes;  // [NB] float4 (c, m, 1/S, x), [NB] gather token
 constexpr uint32_t kOffXa = kOffRow + 5 * NB * 4;   // [2 buffers][2 chunks][2 halves][NB] float2
 constexpr uint32_t kOffXb = kOffXa + 8 * NB * 8;    // [2][2][2][NB] float
-constexpr uint32_t kOffBar = (kOffXb + 8 * NB * 4 + 63) / 64 * 64;
+constexpr int kRnnCols = 2;                         // state columns of a recurrent unit in this form
+constexpr uint32_t kOffRnn = (kOffXb + 8 * NB * 4 + 15) / 16 * 16;  // the RNN head's unit scratch
+constexpr uint32_t kOffBar = (kOffRnn + RnnUnit<kRnnCols>::kScrBytes + 63) / 64 * 64;
 constexpr uint32_t kBarBytes = 1024;
 constexpr size_t kSmemBytes = 1024 + kOffBar + kBarBytes;
 static_assert(kSelConfOff + 2 * kTeamWarps * 4 <= (int)kScrBytes, "select scratch");
@@ -1451,6 +1474,8 @@ __device__ __forceinline__ bool pair_exchange(uint64_t* bar, uint32_t parity, in
   return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
 }
 
+// kRnn: the RNN head's rows (recurrent units in each gather); else W1 rows.
+template <bool kRnn>
 __global__ void __launch_bounds__(kThreads, 1)
     k_draft_narrow(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1464,6 +1489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sUW = smem + nrw::kOffUW;
   uint8_t* sUS = smem + nrw::kOffUS;
   uint8_t* sScr = smem + nrw::kOffScr;
+  uint8_t* sRnn = smem + nrw::kOffRnn;
   // per row: c = log2(e) / T, and the next W items' (m, 1/S, x_s) of the row
   float4* sRow = reinterpret_cast<float4*>(smem + nrw::kOffRow);
   int* sGx = reinterpret_cast<int*>(sRow + nrw::NB);
@@ -1739,13 +1765,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         sGx[b] = x;
       }
       epi_sync();
+      if constexpr (kRnn) {
+        // the recurrent units of position k, then E_k once every unit (one
+        // row block: B <= 16) has finished
+        if (!rnn_units<nrw::kRnnCols>(p, k, sRnn, epi_tid, abort_flag)) fail();
+        if (epi_tid == 0) {
+          const unsigned target = (unsigned)(r / nrw::kRnnCols);
+          const unsigned* cnt = p.rnn_done + (size_t)k * p.n_mtiles;
+          int okw = *abort_flag ? 0 : 1;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (okw && ld_acquire(cnt) < target) {
+            if (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitLimitNs) okw = 0;
+            __nanosleep(32);
+          }
+          *s_ok = okw;
+        }
+        epi_sync();
+        if (!*s_ok && epi_tid == 0) fail();
+      }
       // row b's r / 8 16-byte pieces; piece j holds K elements 8 j .. 8 j + 7:
       // K block j / 8, 16-byte column (j % 8) ^ (b % 8) of the row's 128 bytes
       uint8_t* slot = sE + (k & 1) * nrw::kESlot;
       const int per = r / 8;
       for (int i = epi_tid; i < B * per; i += kEpiThreads) {
         const int b = i / per, j = i - b * per;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)sGx[b] * r) + j);
+        // (L2 for the RNN head's rows: written during this launch)
+        const uint4 v = kRnn ? __ldcg(reinterpret_cast<const uint4*>(p.rnn_E + ((size_t)(k & 1) * B + b) * r) + j)
+                             : __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)sGx[b] * r) + j);
         *reinterpret_cast<uint4*>(slot + (j >> 3) * nrw::kEAtom + (b >> 3) * 1024 + (b & 7) * 128 +
                                   (((j & 7) ^ (b & 7)) << 4)) = v;
       }
@@ -1999,10 +2045,9 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   const cuuint64_t V = (cuuint64_t)d.V, G = (cuuint64_t)d.gamma, B = (cuuint64_t)d.B, r = (cuuint64_t)d.r;
   // small batches: the vocabulary on the MMA's M side (k_draft_narrow)
   const bool narrow = d.B <= fz::nrw::NB && fz::narrow_enabled();
-  // the RNN head runs in the 128-row form, with p_d rows, and reads W_rnn
-  // rows with 16-byte loads
+  // the RNN head runs with p_d rows and reads W_rnn rows with 16-byte loads
   const bool rnn = a.head == DSPARK_HEAD_RNN;
-  if (rnn && (narrow || !a.pd_rows || !a.W_rnn || (reinterpret_cast<uintptr_t>(a.W_rnn) % 16) != 0 ||
+  if (rnn && (!a.pd_rows || !a.W_rnn || (reinterpret_cast<uintptr_t>(a.W_rnn) % 16) != 0 ||
               ((2 * d.r + d.H) % 8) != 0))
     return cudaErrorNotSupported;
   CUtensorMap tmU, tmW2, tmPd = {};  // tmPd stays unused without p_d rows and in the small-batch form
@@ -2033,7 +2078,7 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     if (!narrow && a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  const void* kfn = narrow ? (const void*)fz::k_draft_narrow
+  const void* kfn = narrow ? (rnn ? (const void*)fz::k_draft_narrow<true> : (const void*)fz::k_draft_narrow<false>)
                            : (rnn ? (const void*)fz::k_draft_fused<true> : (const void*)fz::k_draft_fused<false>);
   const size_t smem = narrow ? fz::nrw::kSmemBytes : fz::kSmemBytes;
   if (const cudaError_t ae = ensure_smem_limit(kfn, (int)smem); ae != cudaSuccess) return ae;
@@ -2105,7 +2150,10 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
-  if (narrow) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow, tmU, tmW2, p);
+  if (narrow) {
+    if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<true>, tmU, tmW2, p);
+    return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<false>, tmU, tmW2, p);
+  }
   if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true>, tmU, tmW2, tmPd, p);
   return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false>, tmU, tmW2, tmPd, p);
 }

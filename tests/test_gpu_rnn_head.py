@@ -63,6 +63,9 @@ def test_rnn_head_tiny(temp, seed):
     (33, 2, 2056, 1, 8, "bf16"),    # rank 1
     (40, 6, 1024, 256, 8, "bf16"),  # rank 256 over six positions: tensor-core passes
     (130, 5, 8200, 128, 16, "bf16"),  # two M-tiles, an 8-column last tile: tensor-core passes
+    (1, 7, 8200, 256, 16, "bf16"),    # one request: the small-batch form with the recurrent units
+    (16, 5, 8200, 128, 8, "bf16"),    # the small-batch form's largest batch
+    (9, 3, 4104, 192, 0, "bf16"),     # small batch, rank 192, no hidden state
 ])
 def test_rnn_head_ragged_shapes(B, G, V, r, H, dt):
     wl = synth.Workload("rnn", B, G, V, H, r, dt, "mixed", synth.SCHED_GREEDY, "tiny", seed=5)
@@ -152,10 +155,11 @@ print("ok")
 
 
 @pytest.mark.parametrize("env", [{"DSPARK_DRAFT_PATH": "cuda_core"}, {"DSPARK_DRAFT_LAUNCH": "per_pass"},
-                                 {"DSPARK_DRAFT_LAUNCH": "two_pass"}])
+                                 {"DSPARK_DRAFT_LAUNCH": "two_pass"}, {"DSPARK_DRAFT_FORM": "wide"}])
 def test_rnn_head_on_the_other_launch_paths(env):
-    # bf16 tensor-core shapes on the CUDA-core path, with one launch per pass, and
-    # with one launch per position (the recurrent step between launches)
+    # bf16 tensor-core shapes on the CUDA-core path, with one launch per pass,
+    # with one launch per position (the recurrent step between launches), and a
+    # small batch on the 128-row form
     import os
     import subprocess
     import sys
