@@ -566,7 +566,7 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   if (!a.pd_rows) return draft_tc_supported(d) ? launch_draft_fused(a, ws, L, s) : cudaErrorNotSupported;
   if (a.head == DSPARK_HEAD_RNN) {
     if (!draft_tc_supported(d)) return launch_cuda_core<T, T>(a, ws, L, s);
-    // the fused-sweep kernel with the recurrent step between sweeps (B > 16),
+    // the fused-sweep kernel (either form) with the recurrent step between sweeps,
     // unless DSPARK_DRAFT_LAUNCH asks for the pass kernels
     if (fused_launch_enabled()) {
       const cudaError_t fe = launch_draft_fused(a, ws, L, s);

@@ -1,4 +1,5 @@
-// Fused-sweep tensor-core draft sampler of the Markov head, sm_103a.
+// Fused-sweep tensor-core draft sampler, sm_103a: the Markov head, and the
+// RNN head, whose recurrent step runs in each gather (rnn_units below).
 //
 // Position k of the draft needs two passes over the vocabulary: one for the
 // row normaliser of p_d^k, one that writes p_d^k ([DSpark] 方法细节, "马尔可夫头
@@ -29,6 +30,8 @@
 //   warps 2-9 epilogue, two groups of four warps; group g owns the g-th
 //             64-column chunk of every item.  They also gather E and run
 //             the select (two teams of four warps, one row each).
+// For B <= 16, k_draft_narrow (below) puts the vocabulary on the MMA's M side
+// instead, with the requests as N = 16 columns.
 // Every wait gives up after two seconds and the kernel records DSPARK_TIMEOUT.
 #include <cuda.h>
 

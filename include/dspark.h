@@ -146,9 +146,11 @@ DSPARK_API dspark_status dspark_read_error(void* workspace, int32_t* code_host, 
  * z_k = [s_{k-1}; W1[x_{k-1}]; h_k] in R^{2r+H}, with the recurrent state
  *     s_k = g * s_{k-1} + (1 - g) * tanh(W_c z_k),  g = sigmoid(W_g z_k),  s_0 = 0.
  * W_rnn [3r, 2r + H] (dims.dtype) holds the rows of W_g, then W_c, then W_o.
- * The confidence head is unchanged.  e_k and s_k are fp32, and the RNN head
- * runs the CUDA-core bias product (fp32 FMA) for either dtype.  It needs
- * r >= 1; head = DSPARK_HEAD_MARKOV (0) ignores W_rnn. */
+ * The confidence head is unchanged.  s_k is fp32; e_k enters the bias product
+ * in dims.dtype (rounded to nearest from fp32).  bf16 tensor-core shapes run
+ * the tensor-core kernels (with p_d rows, the recurrent step inside the fused
+ * draft kernel); fp32 and other shapes run the CUDA-core bias product (fp32
+ * FMA).  It needs r >= 1; head = DSPARK_HEAD_MARKOV (0) ignores W_rnn. */
 typedef enum { DSPARK_HEAD_MARKOV = 0, DSPARK_HEAD_RNN = 1 } dspark_head;
 
 typedef struct {
