@@ -79,18 +79,24 @@ def test_rnn_head_ragged_shapes(B, G, V, r, H, dt):
     check_no_error(ws)
 
 
-def test_rnn_head_full_size_sampled_requests():
-    # the whole B256 batch at V151936, r256, H4096; the oracle recomputes three requests
-    wl = synth.get_workload("sweep_B256_g7")
+@pytest.mark.parametrize("name,subset,min_tokens", [
+    # the whole B256 batch at V151936, r256, H4096 (the 128-row form); 24 requests
+    # spread over both M-tiles
+    ("sweep_B256_g7", list(range(0, 256, 11)), 40),
+    # one request at full size: the small-batch form with its recurrent units
+    ("sweep_B1_g7", [0], 1),
+])
+def test_rnn_head_full_size_sampled_requests(name, subset, min_tokens):
+    wl = synth.get_workload(name)
     inp = synth.make_inputs(wl, "cuda", with_target=False)
     Wr = synth.rnn_weights(wl.r, wl.H, wl.dtype, 0, "cuda")
     out, ws = _run(inp, Wr)
-    subset = [0, 100, 255]
     idx = torch.tensor(subset, device="cuda")
     g = {k: v.index_select(0, idx).cpu().numpy() for k, v in out.items()}
     _invariants(g, wl.V)
     o = oracle_draft(**np_inputs(inp, idx), W_rnn=to_np64(Wr), rnn_row_dtype=wl.dtype)
-    compare_draft(g, o, rtol_for(wl.dtype))
+    st = compare_draft(g, o, rtol_for(wl.dtype))
+    assert st["n_tokens_compared"] >= min_tokens
     check_no_error(ws)
 
 
