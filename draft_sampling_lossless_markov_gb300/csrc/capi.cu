@@ -59,6 +59,9 @@ WsLayout ws_layout(const dspark_dims& d) {
   L.E = take(2 * B * r * sizeof(float));
   L.rnn_s = take(2 * B * r * sizeof(float));  // RNN head state s_{k-1}, s_k
   L.rnn_p = take(B * G * 3 * r * sizeof(float));  // RNN head: W_rnn[:, 2r:] . h_k of every position
+  L.rnn_z = take(B * 4 * r * sizeof(uint16_t));     // RNN head, tensor-core recurrent step: z''
+  L.rnn_wz = take(3 * r * 4 * r * sizeof(uint16_t));  // its packed weights
+  L.rnn_pre = take(B * 3 * r * sizeof(float));      // its products
   const size_t ntiles = (V + kPartialTileMin - 1) / kPartialTileMin;
   // (the fused draft kernel keeps float2 partials of 64-column chunks, rows
   // padded to a multiple of 128)

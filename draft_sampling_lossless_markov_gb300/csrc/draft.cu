@@ -548,15 +548,36 @@ static cudaError_t launch_cuda_core(const dspark_draft_args& a, uint8_t* ws, con
 }
 
 // The fused-sweep kernel serves the tensor-core shapes unless
-// DSPARK_DRAFT_LAUNCH=two_pass or per_pass selects the pass kernels.
-static bool fused_launch_enabled() {
-  static int fused = -1;
+// DSPARK_DRAFT_LAUNCH=two_pass or per_pass selects the pass kernels;
+// DSPARK_DRAFT_LAUNCH=fused takes it for the RNN head at every batch.
+static int draft_launch_mode() {  // 0: pass kernels, 1: default, 2: fused always
+  static int mode = -1;
   static std::once_flag once;
   std::call_once(once, [] {
     const char* e = getenv("DSPARK_DRAFT_LAUNCH");
-    fused = (e && (std::string(e) == "per_pass" || std::string(e) == "two_pass")) ? 0 : 1;
+    const std::string v = e ? e : "";
+    mode = (v == "per_pass" || v == "two_pass") ? 0 : (v == "fused" ? 2 : 1);
   });
-  return fused != 0;
+  return mode;
+}
+static bool fused_launch_enabled() { return draft_launch_mode() != 0; }
+
+// The RNN head above this batch runs the pass kernels with the recurrent step
+// on the tensor cores: measured at r256 gamma 7, the fused form's recurrent
+// units (fp32, one CTA's share at a time) cost more there (B1024: 2.70 against
+// 2.46 ms; B256: 0.84 against 0.90 ms).
+constexpr int kRnnFusedMaxB = 512;
+
+// The RNN head's recurrent step on the tensor cores (bf16 tensor-core shapes)
+// unless DSPARK_RNN_STEP=cuda_core keeps k_rnn_step.
+static bool rnn_step_tc_enabled() {
+  static int tc = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* e = getenv("DSPARK_RNN_STEP");
+    tc = (e && std::string(e) == "cuda_core") ? 0 : 1;
+  });
+  return tc != 0;
 }
 
 template <typename T>
@@ -566,9 +587,9 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   if (!a.pd_rows) return draft_tc_supported(d) ? launch_draft_fused(a, ws, L, s) : cudaErrorNotSupported;
   if (a.head == DSPARK_HEAD_RNN) {
     if (!draft_tc_supported(d)) return launch_cuda_core<T, T>(a, ws, L, s);
-    // the fused-sweep kernel (either form) with the recurrent step between sweeps,
-    // unless DSPARK_DRAFT_LAUNCH asks for the pass kernels
-    if (fused_launch_enabled()) {
+    // the fused-sweep kernel (either form) with the recurrent step between
+    // sweeps, up to kRnnFusedMaxB requests unless DSPARK_DRAFT_LAUNCH says otherwise
+    if (draft_launch_mode() == 2 || (draft_launch_mode() == 1 && d.B <= kRnnFusedMaxB)) {
       const cudaError_t fe = launch_draft_fused(a, ws, L, s);
       if (fe != cudaErrorNotSupported) return fe;
     }
@@ -586,9 +607,18 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     cudaError_t e = launch_rnn_hproj(a, P, reinterpret_cast<WsHeader*>(ws), s);
     if (e != cudaSuccess) return e;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    // the recurrent step: on the tensor cores (z'' and the packed weights), or k_rnn_step
+    const bool tc_step = std::is_same<T, __nv_bfloat16>::value && rnn_step_tc_enabled();
+    auto* Z = reinterpret_cast<__nv_bfloat16*>(ws + L.rnn_z);
+    auto* Wz = reinterpret_cast<__nv_bfloat16*>(ws + L.rnn_wz);
+    float* pre = reinterpret_cast<float*>(ws + L.rnn_pre);
+    if (tc_step && (e = launch_rnn_pack_wz(a, Wz, s)) != cudaSuccess) return e;
     const std::function<cudaError_t(int)> hook = [&](int k) {
-      const cudaError_t e2 = launch_rnn_step(a, k + 1, P, S + (size_t)(k & 1) * B * r,
-                                             S + (size_t)((k + 1) & 1) * B * r, Erows, s);
+      const float* s_prev = S + (size_t)(k & 1) * B * r;
+      float* s_new = S + (size_t)((k + 1) & 1) * B * r;
+      const cudaError_t e2 = tc_step ? launch_rnn_step_tc(a, k + 1, P, s_prev, s_new,
+                                                          reinterpret_cast<__nv_bfloat16*>(Erows), Z, Wz, pre, hdr, s)
+                                     : launch_rnn_step(a, k + 1, P, s_prev, s_new, Erows, s);
       if (e2 != cudaSuccess) return e2;
       k_embed<T, T><<<(B + 7) / 8, 256, 0, s>>>(a.anchor, a.tokens, k, W1, w, zh, nullptr, a.conf_logit, a.conf, B,
                                                 d.gamma, d.V, r, d.H, hdr);

@@ -1126,29 +1126,38 @@ bool rnn_hproj_tc_supported(const dspark_dims& d) {
          tc::encode_fn() != nullptr;
 }
 
-cudaError_t launch_rnn_hproj_tc(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s) {
-  const dspark_dims& d = a.dims;
-  const int M = d.B * d.gamma, N = 3 * d.r, K = d.H;
+// C[M, N] (fp32, row stride N) = A[M, K] . B[N, K]^T for bf16 A and B with K
+// contiguous (row strides lda, ldb elements, multiples of 8; 16-byte aligned
+// bases): the k_rnn_hproj_tc tiles, K-major operands by TMA.
+cudaError_t launch_tc_gemm_nt(const void* A, int lda, const void* Bm, int ldb, float* C, int M, int N, int K,
+                              WsHeader* hdr, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
-  {  // h [M, H] bf16 as (k, m)
+  {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
     const cuuint32_t box[2] = {hp::TK, hp::TM};
-    if (!tc::encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!tc::encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  {  // W_rnn[:, 2r:] [3r, H] bf16 (row stride 2r + H) as (k, n)
+  {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(2 * d.r + d.H) * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)ldb * 2};
     const cuuint32_t box[2] = {hp::TK, hp::TN};
-    const void* base = static_cast<const __nv_bfloat16*>(a.W_rnn) + 2 * d.r;
-    if (!tc::encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!tc::encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Bm, dims, strides, box)) return cudaErrorInvalidValue;
   }
   if (const cudaError_t ae = ensure_smem_limit((const void*)k_rnn_hproj_tc, (int)hp::kSmem); ae != cudaSuccess)
     return ae;
   const dim3 grid((N + hp::TN - 1) / hp::TN, (M + hp::TM - 1) / hp::TM);
-  k_rnn_hproj_tc<<<grid, 128, hp::kSmem, s>>>(tmA, tmB, P, M, N, K, hdr);
+  k_rnn_hproj_tc<<<grid, 128, hp::kSmem, s>>>(tmA, tmB, C, M, N, K, hdr);
   count_launches(1);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_hproj_tc(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  // h [B gamma, H] . W_rnn[:, 2r:]^T (rows of stride 2r + H)
+  return launch_tc_gemm_nt(a.h, d.H, static_cast<const __nv_bfloat16*>(a.W_rnn) + 2 * d.r, 2 * d.r + d.H, P,
+                           d.B * d.gamma, 3 * d.r, d.H, hdr, s);
 }
 
 bool draft_tc_supported(const dspark_dims& d) {

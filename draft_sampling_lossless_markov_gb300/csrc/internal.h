@@ -4,6 +4,7 @@
 #include <functional>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -42,6 +43,9 @@ struct WsLayout {
   size_t vfin = 0;     // [B * 32 ceil(ceil(V/256)/32)] float2: verify chunk sums of the final draw
   size_t rnn_s = 0;    // [2][B*r] f32: RNN head state, positions alternate
   size_t rnn_p = 0;    // [B*gamma][3r] f32: RNN head projections of h
+  size_t rnn_z = 0;    // [B][4r] bf16: RNN head z'' of the tensor-core recurrent step
+  size_t rnn_wz = 0;   // [3r][4r] bf16: RNN head weights of that step
+  size_t rnn_pre = 0;  // [B][3r] f32: its products
   size_t total = 0;
 };
 
@@ -83,6 +87,16 @@ cudaError_t launch_rnn_hproj(const dspark_draft_args& a, float* P, WsHeader* hdr
 // the same product on the tensor cores (draft_tc.cu): bf16, H and r multiples of 8
 bool rnn_hproj_tc_supported(const dspark_dims& d);
 cudaError_t launch_rnn_hproj_tc(const dspark_draft_args& a, float* P, WsHeader* hdr, cudaStream_t s);
+// C[M, N] (fp32) = A[M, K] . B[N, K]^T, bf16 operands with K contiguous (draft_tc.cu)
+cudaError_t launch_tc_gemm_nt(const void* A, int lda, const void* Bm, int ldb, float* C, int M, int N, int K,
+                              WsHeader* hdr, cudaStream_t s);
+// the RNN head's recurrent step on the tensor cores (rnn_head.cu): Wz packed
+// once per draft call, then per position z'' = [s split in three bf16 parts;
+// W1[x]], the GEMM into pre, and the gates
+cudaError_t launch_rnn_pack_wz(const dspark_draft_args& a, __nv_bfloat16* Wz, cudaStream_t s);
+cudaError_t launch_rnn_step_tc(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
+                               __nv_bfloat16* E, __nv_bfloat16* Z, const __nv_bfloat16* Wz, float* pre,
+                               WsHeader* hdr, cudaStream_t s);
 // (E: [B, r] rows in dims.dtype)
 cudaError_t launch_rnn_step(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
                             void* E, cudaStream_t s);

@@ -283,7 +283,91 @@ __global__ void __launch_bounds__(RN_THREADS) k_rnn_step(const T* __restrict__ W
   }
 }
 
+// ---- the recurrent step on the tensor cores (bf16, sm_103a) ----
+// pre = W_rnn[:, :2r] . z' as one bf16 GEMM with fp32 accumulation.  s_{j-1}
+// (fp32) is split into three bf16 parts hi + mid + lo, each the nearest bf16 to
+// what the parts before it leave (the remainders are exact in fp32), so that
+// the parts carry s to about 2^-27 of its magnitude; z'' = [hi; mid; lo;
+// W1[x_{j-1}]] in R^{4r} meets Wz = [W_s, W_s, W_s, W_x] (W_s = W_rnn[:, :r],
+// W_x = W_rnn[:, r:2r]), [3r, 4r], packed once per draft call.  Products of
+// bf16 operands are exact in fp32; the GEMM adds them in fp32, in another
+// order than k_rnn_step's fma chains.
+
+// Wz row n (n < 3r): W_s row n three times, then W_x row n
+__global__ void k_rnn_pack_wz(const __nv_bfloat16* __restrict__ Wr, __nv_bfloat16* __restrict__ Wz, int r, int ldw) {
+  const int n = blockIdx.y;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 4 * r; i += gridDim.x * blockDim.x)
+    Wz[(size_t)n * 4 * r + i] = Wr[(size_t)n * ldw + (i < 3 * r ? i % r : i - 2 * r)];
+}
+
+// z'' of request b = blockIdx.y for position j (s_0 = 0, x_0 the anchor)
+__global__ void k_rnn_zsplit(const float* __restrict__ s_prev, const __nv_bfloat16* __restrict__ W1,
+                             const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
+                             __nv_bfloat16* __restrict__ Z, int G, int V, int r, int j) {
+  const int b = blockIdx.y;
+  int x = (j == 1) ? anchor[b] : tokens[(size_t)b * G + j - 2];
+  x = (x >= 0 && x < V) ? x : 0;  // out-of-range anchors are reported by the confidence kernel
+  __nv_bfloat16* z = Z + (size_t)b * 4 * r;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < r; i += gridDim.x * blockDim.x) {
+    const float s = (j == 1) ? 0.f : s_prev[(size_t)b * r + i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(s);
+    const float r1 = __fsub_rn(s, __bfloat162float(hi));
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = __fsub_rn(r1, __bfloat162float(mid));
+    z[i] = hi;
+    z[r + i] = mid;
+    z[2 * r + i] = __float2bfloat16_rn(r2);
+    z[3 * r + i] = W1[(size_t)x * r + i];
+  }
+}
+
+// the gates of position j from pre [B, 3r] (and P), as k_rnn_step's epilogue
+__global__ void k_rnn_gates(const float* __restrict__ pre, const float* __restrict__ P,
+                            const float* __restrict__ s_prev, float* __restrict__ s_new,
+                            __nv_bfloat16* __restrict__ E, int B, int G, int r, int H, int j) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= B * r) return;
+  const int b = idx / r, col = idx - b * r;
+  const float* pb = pre + (size_t)b * 3 * r;
+  float pg = pb[col], pc = pb[r + col], po = pb[2 * r + col];
+  if (H > 0) {
+    const float* pr = P + ((size_t)b * G + (j - 1)) * 3 * r;
+    pg += pr[col];
+    pc += pr[r + col];
+    po += pr[2 * r + col];
+  }
+  const float gt = 1.f / (1.f + expf(-pg));
+  const float sp = (j == 1) ? 0.f : s_prev[(size_t)b * r + col];
+  s_new[(size_t)b * r + col] = gt * sp + (1.f - gt) * tanhf(pc);
+  E[(size_t)b * r + col] = __float2bfloat16_rn(tanhf(po));
+}
+
 }  // namespace
+
+cudaError_t launch_rnn_pack_wz(const dspark_draft_args& a, __nv_bfloat16* Wz, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  const dim3 grid((4 * d.r + 255) / 256, 3 * d.r);
+  k_rnn_pack_wz<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.W_rnn), Wz, d.r, 2 * d.r + d.H);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_step_tc(const dspark_draft_args& a, int j, const float* P, const float* s_prev, float* s_new,
+                               __nv_bfloat16* E, __nv_bfloat16* Z, const __nv_bfloat16* Wz, float* pre,
+                               WsHeader* hdr, cudaStream_t s) {
+  const dspark_dims& d = a.dims;
+  const int B = d.B, r = d.r;
+  k_rnn_zsplit<<<dim3((r + 255) / 256, B), 256, 0, s>>>(s_prev, static_cast<const __nv_bfloat16*>(a.W1), a.anchor,
+                                                         a.tokens, Z, d.gamma, d.V, r, j);
+  count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_tc_gemm_nt(Z, 4 * r, Wz, 4 * r, pre, B, 3 * r, 4 * r, hdr, s);
+  if (e != cudaSuccess) return e;
+  k_rnn_gates<<<(B * r + 255) / 256, 256, 0, s>>>(pre, P, s_prev, s_new, E, B, d.gamma, r, d.H, j);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 template <typename T>
 static cudaError_t launch_hproj_t(const dspark_draft_args& a, float* P, cudaStream_t s) {

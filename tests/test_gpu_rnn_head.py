@@ -101,8 +101,10 @@ def test_rnn_head_full_size_sampled_requests(name, subset, min_tokens):
 
 
 @pytest.mark.parametrize("B,G,V,r,H,subset", [
-    # about 13 recurrent units per CTA: unit ranges cross row blocks and M-tiles,
-    # a ragged last row block (8 rows) and M-tile (104 rows)
+    # about 6 recurrent units per CTA in the fused form: unit ranges cross row
+    # blocks and M-tiles, a ragged last row block (20 rows) and M-tile (116 rows)
+    (500, 3, 8200, 256, 16, [0, 31, 32, 127, 128, 300, 383, 384, 479, 480, 499]),
+    # above 512 requests: the pass kernels with the recurrent step on the tensor cores
     (1000, 3, 8200, 256, 16, [0, 31, 32, 127, 128, 300, 511, 767, 895, 896, 991, 999]),
     # no hidden state (no h projection), rank 64: a ragged 12-row last block
     (300, 3, 4104, 64, 0, [0, 63, 64, 127, 128, 255, 256, 287, 288, 299]),
@@ -145,7 +147,7 @@ from oracle.draft import draft as oracle_draft
 from parity import compare_draft, gpu_np, np_inputs, rtol_for, to_np64
 from gpu_common import check_no_error, workspace_for
 from draft_sampling_lossless_markov_gb300 import torch_api as T
-for B, G, V, r, H in [(130, 5, 8200, 128, 16), (5, 4, 4104, 64, 24)]:
+for B, G, V, r, H in [(130, 5, 8200, 128, 16), (5, 4, 4104, 64, 24), (600, 3, 8200, 256, 16)]:
     wl = synth.Workload("paths", B, G, V, H, r, "bf16", "mixed", synth.SCHED_GREEDY, "tiny", seed=11)
     inp = synth.make_inputs(wl, "cuda", with_target=False)
     Wr = synth.rnn_weights(r, H, "bf16", 2, "cuda")
@@ -161,11 +163,14 @@ print("ok")
 
 
 @pytest.mark.parametrize("env", [{"DSPARK_DRAFT_PATH": "cuda_core"}, {"DSPARK_DRAFT_LAUNCH": "per_pass"},
-                                 {"DSPARK_DRAFT_LAUNCH": "two_pass"}, {"DSPARK_DRAFT_FORM": "wide"}])
+                                 {"DSPARK_DRAFT_LAUNCH": "two_pass"},
+                                 {"DSPARK_DRAFT_LAUNCH": "two_pass", "DSPARK_RNN_STEP": "cuda_core"},
+                                 {"DSPARK_DRAFT_FORM": "wide"}, {"DSPARK_DRAFT_LAUNCH": "fused"}])
 def test_rnn_head_on_the_other_launch_paths(env):
     # bf16 tensor-core shapes on the CUDA-core path, with one launch per pass,
-    # with one launch per position (the recurrent step between launches), and a
-    # small batch on the 128-row form
+    # with one launch per position (the recurrent step between launches, on the
+    # tensor cores or on the CUDA cores), a small batch on the 128-row form, and
+    # the fused form above 512 requests
     import os
     import subprocess
     import sys
