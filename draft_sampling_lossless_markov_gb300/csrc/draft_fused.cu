@@ -65,8 +65,17 @@ constexpr int kStagingPerWarp = 32 * 32 * 4;
 constexpr uint32_t kW2Stage = KC * BN * 2;     // 16 KB
 constexpr uint32_t kUChunk = BM * CW * 2;      // 16 KB
 constexpr uint32_t kUStage = NCH * kUChunk;    // 32 KB: the U rows of one item
-constexpr int NW = 6;                          // W2 stages (1.5 tiles at r = 256)
-constexpr int NU = 3;                          // U stages, one item each
+// Stage rings of the 128-row form, a template parameter of its kernel: the W2
+// ring (16 KB stages, four per tile at r = 256) and the U ring (32 KB stages,
+// one per item), in the shared memory the p_d staging leaves.  With few
+// M-tiles every W2 tile comes from DRAM and the deeper W2 ring pays; with many,
+// the M-tiles' CTAs find most W2 tiles in L2 and U (read from DRAM by every
+// CTA) wants the deeper U ring.
+constexpr int kRingW2Deep = 0;                 // 8 W2 stages (two tiles), 2 U stages
+constexpr int kRingUDeep = 1;                  // 6 W2 stages (1.5 tiles), 3 U stages
+__host__ __device__ constexpr int ring_nw(int ring) { return ring == kRingW2Deep ? 8 : 6; }
+__host__ __device__ constexpr int ring_nu(int ring) { return ring == kRingW2Deep ? 2 : 3; }
+constexpr int kRingW2DeepMaxMtiles = 4;        // M-tiles up to which the W2-deep ring runs (measured)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kESlotCols = 128;           // r / 2 columns, r <= 256
@@ -75,9 +84,11 @@ constexpr int kTailBytes = 1024;
 constexpr int kTQ = 16;                        // tile-queue slots (the producer runs < 8 tiles ahead)
 constexpr int kMaxE = 20;                      // chunk partials per lane in the select (V <= 20 * 128 * 64)
 constexpr int kTailDiv = 5;                    // the last fifth of a sweep's claims is kept in L2
-constexpr size_t kSmemBytes =
-    1024 + NW * (size_t)kW2Stage + NU * (size_t)kUStage + (size_t)kEpiWarps * kStagingPerWarp + kTailBytes;
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr size_t smem_bytes(int ring) {
+  return 1024 + ring_nw(ring) * (size_t)kW2Stage + ring_nu(ring) * (size_t)kUStage +
+         (size_t)kEpiWarps * kStagingPerWarp + kTailBytes;
+}
+static_assert(smem_bytes(kRingW2Deep) <= 232448 && smem_bytes(kRingUDeep) <= 232448, "shared memory per CTA");
 // select scratch in the (idle) staging area: per team a row record, 16 words of
 // exchange and four warps' 64 partial logits
 constexpr int kSelRecOff = 0, kSelXwOff = 128, kSelRedOff = 256;
@@ -811,10 +822,12 @@ __device__ __forceinline__ void select_rows(const Params& p, int k, uint8_t* scr
 }
 
 // kRnn: the RNN head's rows (recurrent units in each gather); else W1 rows.
-template <bool kRnn>
+// kRing: the stage rings (kRingW2Deep or kRingUDeep).
+template <bool kRnn, int kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     k_draft_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW2,
                   const __grid_constant__ CUtensorMap tmPd, Params p) {
+  constexpr int NW = ring_nw(kRing), NU = ring_nu(kRing);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int r = p.r;
@@ -2031,6 +2044,19 @@ static bool narrow_enabled() {
   return on != 0;
 }
 
+// The 128-row form's stage rings for a batch of n_mtiles M-tiles;
+// DSPARK_FUSED_RING=w2 or =u picks one at every batch.
+static bool ring_w2_deep(int n_mtiles) {
+  static int force = -1;  // -1: by the batch, 0: U-deep, 1: W2-deep
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* e = getenv("DSPARK_FUSED_RING");
+    if (e && std::string(e) == "w2") force = 1;
+    if (e && std::string(e) == "u") force = 0;
+  });
+  return force >= 0 ? force == 1 : n_mtiles <= kRingW2DeepMaxMtiles;
+}
+
 }  // namespace fz
 
 // The fused-sweep kernel needs every CTA resident (cooperative launch, one
@@ -2081,9 +2107,14 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     if (!narrow && a.pd_rows && !fz::encode(&tmPd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.pd_rows, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  const void* kfn = narrow ? (rnn ? (const void*)fz::k_draft_narrow<true> : (const void*)fz::k_draft_narrow<false>)
-                           : (rnn ? (const void*)fz::k_draft_fused<true> : (const void*)fz::k_draft_fused<false>);
-  const size_t smem = narrow ? fz::nrw::kSmemBytes : fz::kSmemBytes;
+  const bool w2deep = fz::ring_w2_deep(n_mtiles);
+  const void* kfn =
+      narrow ? (rnn ? (const void*)fz::k_draft_narrow<true> : (const void*)fz::k_draft_narrow<false>)
+      : w2deep ? (rnn ? (const void*)fz::k_draft_fused<true, fz::kRingW2Deep>
+                      : (const void*)fz::k_draft_fused<false, fz::kRingW2Deep>)
+               : (rnn ? (const void*)fz::k_draft_fused<true, fz::kRingUDeep>
+                      : (const void*)fz::k_draft_fused<false, fz::kRingUDeep>);
+  const size_t smem = narrow ? fz::nrw::kSmemBytes : fz::smem_bytes(w2deep ? fz::kRingW2Deep : fz::kRingUDeep);
   if (const cudaError_t ae = ensure_smem_limit(kfn, (int)smem); ae != cudaSuccess) return ae;
 
   fz::Params p;
@@ -2157,8 +2188,12 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<true>, tmU, tmW2, p);
     return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<false>, tmU, tmW2, p);
   }
-  if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true>, tmU, tmW2, tmPd, p);
-  return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false>, tmU, tmW2, tmPd, p);
+  if (w2deep) {
+    if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingW2Deep>, tmU, tmW2, tmPd, p);
+    return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingW2Deep>, tmU, tmW2, tmPd, p);
+  }
+  if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingUDeep>, tmU, tmW2, tmPd, p);
+  return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingUDeep>, tmU, tmW2, tmPd, p);
 }
 
 }  // namespace dspark
