@@ -206,12 +206,20 @@ def run_ours(args, rank, world, local_rank):
     rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
     tgt_flat = inp["target"].reshape(-1, V)
 
+    overlap = args.sched_overlap == "on"
+
     def draft_call(st):
-        T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
-                       inp["req_id"], inp["seed"], out=d_out, stream=st, W_rnn=inp.get("W_rnn"))
+        if overlap:
+            # dspark_draft_and_schedule: the scheduler beside the draft's last sweep
+            draft_and_sched(T, ws, inp, inp["U"], inp["h"], inp["anchor"], inp["temp"], inp["req_id"], sps_dev,
+                            d_out, s_out, st, rows=not row_free)
+        else:
+            T.draft_sample(ws, inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"],
+                           inp["req_id"], inp["seed"], out=d_out, stream=st, W_rnn=inp.get("W_rnn"))
 
     def sched_call(st):
-        sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=st)
+        if not overlap:
+            sched(T, ws, d_out["conf_logit"], inp, sps_dev, inp["anchor"], d_out["tokens"], out=s_out, stream=st)
 
     def standin(st):
         # stand-in for the target forward on the flattened batch (not timed): the
@@ -249,6 +257,9 @@ def run_ours(args, rank, world, local_rank):
         # call live inside the timed region
         runs = []
         for fn in calls:
+            if fn is sched_call and overlap:
+                runs.append(lambda: None)  # the schedule runs inside the draft call
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn(torch.cuda.current_stream())
@@ -296,6 +307,9 @@ def run_ours(args, rank, world, local_rank):
     br = {"draft_ms": float(np.median(per[:, 0])), "schedule_ms": float(np.median(per[:, 1])),
           "verify_ms": float(np.median(per[:, 2])),
           "timer": "CUDA events around each call's graph replay inside the timed region; median over the steps"}
+    if overlap:
+        br["schedule"] = ("inside the draft call (dspark_draft_and_schedule): beside the draft kernel's last "
+                          "sweep where the shapes allow, else right after it; draft_ms covers both")
     nv = B * (G + 1) if cap_accept else int(s_out["n_verify"][0])
     ms = max_over_ranks(ms, world, dev)
     code, detail = ws.read_error()
@@ -322,14 +336,14 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded; DSpark workload model)",
         "config": workload_config(wl, args, inp["sched_mode"], world),
         "run": {"n_verify_rows": nv, "graph": use_graph, "ms_per_step_mean": float(np.mean(ms_steps)),
-                "ms_per_step_min": float(np.min(ms_steps)), "ms_per_step_max": float(np.max(ms_steps))},
+                "ms_per_step_min": float(np.min(ms_steps)), "ms_per_step_max": float(np.max(ms_steps)),
+                "sched_overlap": args.sched_overlap},
         "hbm_frac_step": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
         "hbm_frac_step_strict": bytes_["step_strict"] / (ms * 1e-3) / 1e9 / peak,
         "step_bytes": {"per_position": bytes_["step_per_position"], "strict": bytes_["step_strict"]},
         "breakdown_ms": br,
         "roofline": {"bound": "hbm",
-                     "kernel": (f"dspark_draft_sample ({draft_kernel_name(wl)}, one launch)" if args.head == "markov" else
-                                "dspark_draft_sample, RNN head (k_rnn_step + tensor-core passes per position)"),
+                     "kernel": draft_call_label(wl, args),
                      "achieved": draft_gbs, "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}",
                      "unit": "GB/s", "frac": draft_gbs / peak,
                      "traffic": traffic,
@@ -353,6 +367,19 @@ def draft_kernel_name(wl):
     return "fz::k_draft_narrow" if small else "fz::k_draft_fused"
 
 
+def draft_call_label(wl, args):
+    """What the roofline's dominant call runs (the library's default dispatch)."""
+    call = "dspark_draft_and_schedule" if args.sched_overlap == "on" else "dspark_draft_sample"
+    if args.head == "rnn" and wl.B > 512:
+        return f"{call}, RNN head (two-pass tensor-core passes, tensor-core recurrent step per position)"
+    head = ", RNN head" if args.head == "rnn" else ""
+    beside = ""
+    if (args.sched_overlap == "on" and draft_kernel_name(wl) == "fz::k_draft_fused" and args.rows != "none"
+            and wl.B * wl.gamma <= 2048):
+        beside = ", k_schedule_smem beside its last sweep"
+    return f"{call}{head} ({draft_kernel_name(wl)}, one launch{beside})"
+
+
 def load_traffic(wl):
     """Per-launch DRAM bytes of the dominant call from a committed ncu summary:
     (bytes, None), or (None, why) when there is no capture for this workload or
@@ -368,6 +395,15 @@ def load_traffic(wl):
         return None, "the ncu traffic record was captured on another version of the kernel source"
     b = d.get("per_launch_bytes", {}).get(wl.name)
     return (b, None) if b is not None else (None, "no ncu traffic record for this workload")
+
+
+def draft_and_sched(T, ws, inp, U, h, anchor, temp, req_id, sps_dev, d_out, s_out, stream, rows=True,
+                    n_verify_host=None):
+    """dspark_draft_and_schedule in the bench's scheduler mode; returns (draft out, schedule out)."""
+    return T.draft_and_schedule(ws, U, inp["W1"], inp["W2"], h, inp["w"], anchor, temp, req_id, inp["seed"],
+                                inp["sts"], sps_dev, inp["sched_mode"], out=d_out, sched_out=s_out, stream=stream,
+                                W_rnn=inp.get("W_rnn"), rows=rows, conf_logit_prev=inp.get("zprev"),
+                                n_verify_host=n_verify_host)
 
 
 def sched(T, ws, conf_logit, inp, sps_dev, anchor, tokens, **kw):
@@ -429,13 +465,17 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
         sm = d_small[k]
         with torch.cuda.stream(stream):
             stream.wait_event(copied[k])
-            d = T.draft_sample(ws, d_U[k], inp["W1"], inp["W2"], d_h[k], inp["w"], sm["anchor"], sm["temp"],
-                               sm["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"),
-                               rows=args.rows != "none")
+            if args.sched_overlap == "on":
+                d, s = draft_and_sched(T, ws, inp, d_U[k], d_h[k], sm["anchor"], sm["temp"], sm["req_id"], sps_dev,
+                                       None, None, stream, rows=args.rows != "none", n_verify_host=h_nv[k])
+            else:
+                d = T.draft_sample(ws, d_U[k], inp["W1"], inp["W2"], d_h[k], inp["w"], sm["anchor"], sm["temp"],
+                                   sm["req_id"], inp["seed"], stream=stream, W_rnn=inp.get("W_rnn"),
+                                   rows=args.rows != "none")
+                s = sched(T, ws, d["conf_logit"], inp, sps_dev, sm["anchor"], d["tokens"], stream=stream,
+                          n_verify_host=h_nv[k])
             rj = (dict(U=d_U[k], W1=inp["W1"], W2=inp["W2"], anchor=sm["anchor"], pd_stat=d["pd_stat"])
                   if args.rows == "none" else None)
-            s = sched(T, ws, d["conf_logit"], inp, sps_dev, sm["anchor"], d["tokens"], stream=stream,
-                      n_verify_host=h_nv[k])
             if cap_accept:
                 v = T.verify(ws, d_tgt[k].reshape(-1, V), full_offsets, full_ell, d["tokens"], d.get("pd_rows"),
                              d["pd_tok"], sm["temp"], sm["req_id"], inp["seed"], stream=stream, commit_cap=s["ell"],
@@ -918,6 +958,9 @@ def main():
     ap.add_argument("--sweep", default=None,
                     help="comma-separated workloads (or 'all': the batch/gamma sweep and the named configs): one "
                          "JSON line per workload, device-timed only (no end-to-end leg, no oracle baseline)")
+    ap.add_argument("--sched-overlap", default="on", choices=["on", "off"],
+                    help="on: the step's draft and schedule as one dspark_draft_and_schedule call (the scheduler "
+                         "beside the draft kernel's last sweep); off: two calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0,

@@ -44,7 +44,7 @@ DSPARK_STS_MAX_TABLE = 16384
 EXPORTED = ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
             "dspark_schedule", "dspark_verify", "dspark_status_string", "dspark_version", "dspark_launch_count",
             "dspark_last_cuda_error", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size", "dspark_sts_fit",
-            "dspark_pack_rows")
+            "dspark_pack_rows", "dspark_draft_and_schedule")
 
 
 class dspark_dims(ctypes.Structure):
@@ -105,6 +105,8 @@ def load() -> ctypes.CDLL:
     lib.dspark_read_error.argtypes = [c_void_p, POINTER(c_int32), POINTER(c_int32), c_void_p]
     lib.dspark_draft_sample.argtypes = [POINTER(dspark_draft_args), c_void_p, c_size_t, c_void_p]
     lib.dspark_schedule.argtypes = [POINTER(dspark_sched_args), c_void_p, c_size_t, c_void_p]
+    lib.dspark_draft_and_schedule.argtypes = [POINTER(dspark_draft_args), POINTER(dspark_sched_args), c_void_p,
+                                              c_size_t, c_void_p]
     lib.dspark_verify.argtypes = [POINTER(dspark_verify_args), c_void_p, c_size_t, c_void_p]
     lib.dspark_schedule_noalloc.argtypes = [POINTER(dspark_sched_args), c_void_p]
     lib.dspark_sts_fit_workspace_size.argtypes = [c_int32, c_int32, c_int32, c_int32, POINTER(c_size_t)]
@@ -112,7 +114,7 @@ def load() -> ctypes.CDLL:
     lib.dspark_pack_rows.argtypes = [POINTER(dspark_pack_args), c_void_p, c_void_p]
     for f in ("dspark_workspace_size", "dspark_workspace_init", "dspark_read_error", "dspark_draft_sample",
               "dspark_schedule", "dspark_verify", "dspark_schedule_noalloc", "dspark_sts_fit_workspace_size",
-              "dspark_sts_fit", "dspark_pack_rows"):
+              "dspark_sts_fit", "dspark_pack_rows", "dspark_draft_and_schedule"):
         getattr(lib, f).restype = c_int32
     lib.dspark_status_string.argtypes = [c_int32]
     lib.dspark_status_string.restype = c_char_p
@@ -164,6 +166,13 @@ def dspark_draft_sample(args: dspark_draft_args, workspace: int, nbytes: int, st
 
 def dspark_schedule(args: dspark_sched_args, workspace: int, nbytes: int, stream: int) -> int:
     return load().dspark_schedule(ctypes.byref(args), c_void_p(workspace), nbytes, c_void_p(stream))
+
+
+def dspark_draft_and_schedule(dargs: dspark_draft_args, sargs: dspark_sched_args, workspace: int, nbytes: int,
+                              stream: int) -> int:
+    """dspark_draft_sample then dspark_schedule in one call that may overlap them."""
+    return load().dspark_draft_and_schedule(ctypes.byref(dargs), ctypes.byref(sargs), c_void_p(workspace), nbytes,
+                                            c_void_p(stream))
 
 
 def dspark_schedule_noalloc(args: dspark_sched_args, stream: int) -> int:

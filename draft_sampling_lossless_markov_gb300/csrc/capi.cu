@@ -175,11 +175,10 @@ dspark_status dspark_read_error(void* workspace, int32_t* code_host, int32_t* de
   return cuda_status(e);
 }
 
-dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, size_t workspace_bytes,
-                                  void* stream) {
-  if (!a || !dims_ok(a->dims)) return DSPARK_INVALID_ARG;
+// The checks of dspark_draft_sample (B > 0), with the workspace layout.
+static dspark_status check_draft_args(const dspark_draft_args* a, void* workspace, size_t workspace_bytes,
+                                      WsLayout* L) {
   const dspark_dims& d = a->dims;
-  if (d.B == 0) return DSPARK_OK;
   if (!a->U || !a->anchor || !a->temp || !a->req_id || !a->tokens || !a->pd_tok || !a->conf_logit || !a->conf)
     return DSPARK_INVALID_ARG;
   if (!a->pd_rows && (!a->pd_stat || a->head != DSPARK_HEAD_MARKOV)) return DSPARK_INVALID_ARG;
@@ -191,11 +190,42 @@ dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, s
   const void* big[] = {a->U, a->W1, a->W2, a->h, a->w, a->pd_rows, a->head == DSPARK_HEAD_RNN ? a->W_rnn : nullptr};
   for (const void* p : big)
     if (p && !aligned16(p)) return DSPARK_INVALID_ARG;
+  return check_ws(d, workspace, workspace_bytes, L);
+}
+
+dspark_status dspark_draft_sample(const dspark_draft_args* a, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!a || !dims_ok(a->dims)) return DSPARK_INVALID_ARG;
+  if (a->dims.B == 0) return DSPARK_OK;
   WsLayout L;
-  const dspark_status st = check_ws(d, workspace, workspace_bytes, &L);
+  const dspark_status st = check_draft_args(a, workspace, workspace_bytes, &L);
   if (st != DSPARK_OK) return st;
   const cudaError_t e = launch_draft(*a, static_cast<uint8_t*>(workspace), L, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported && !a->pd_rows) return DSPARK_UNSUPPORTED;  // no fused path for the row-free mode
+  return cuda_status(e);
+}
+
+dspark_status dspark_draft_and_schedule(const dspark_draft_args* da, const dspark_sched_args* sa, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (!da || !dims_ok(da->dims)) return DSPARK_INVALID_ARG;
+  const dspark_status chk = check_sched_args(sa, DSPARK_MAX_SCHED_KEYS);
+  if (chk != DSPARK_OK) return chk;
+  // the schedule reads the draft's confidences and tokens
+  if (sa->B != da->dims.B || sa->gamma != da->dims.gamma) return DSPARK_INVALID_ARG;
+  if (da->dims.B == 0) return DSPARK_OK;
+  if (sa->conf_logit != da->conf_logit || sa->tokens != da->tokens || sa->anchor != da->anchor)
+    return DSPARK_INVALID_ARG;
+  WsLayout L;
+  const dspark_status st = check_draft_args(da, workspace, workspace_bytes, &L);
+  if (st != DSPARK_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const cudaStream_t s = (cudaStream_t)stream;
+  DraftOverlap ov;
+  ov.want = schedule_one_launch(sa->B, sa->gamma);
+  cudaError_t e = launch_draft(*da, ws, L, s, &ov);
+  if (e == cudaErrorNotSupported && !da->pd_rows) return DSPARK_UNSUPPORTED;
+  if (e != cudaSuccess) return cuda_status(e);
+  e = ov.armed ? launch_schedule_behind_draft(*sa, ws, L, ov.sel_done, ov.n_ctas, s) : launch_schedule(*sa, ws, L, s);
   return cuda_status(e);
 }
 

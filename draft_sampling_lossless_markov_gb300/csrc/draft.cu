@@ -581,16 +581,17 @@ static bool rnn_step_tc_enabled() {
 }
 
 template <typename T>
-static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                                  DraftOverlap* ov) {
   const dspark_dims& d = a.dims;
   // without p_d rows: the fused-sweep kernel only (its select yields p_d(x) and (m, S))
-  if (!a.pd_rows) return draft_tc_supported(d) ? launch_draft_fused(a, ws, L, s) : cudaErrorNotSupported;
+  if (!a.pd_rows) return draft_tc_supported(d) ? launch_draft_fused(a, ws, L, s, ov) : cudaErrorNotSupported;
   if (a.head == DSPARK_HEAD_RNN) {
     if (!draft_tc_supported(d)) return launch_cuda_core<T, T>(a, ws, L, s);
     // the fused-sweep kernel (either form) with the recurrent step between
     // sweeps, up to kRnnFusedMaxB requests unless DSPARK_DRAFT_LAUNCH says otherwise
     if (draft_launch_mode() == 2 || (draft_launch_mode() == 1 && d.B <= kRnnFusedMaxB)) {
-      const cudaError_t fe = launch_draft_fused(a, ws, L, s);
+      const cudaError_t fe = launch_draft_fused(a, ws, L, s, ov);
       if (fe != cudaErrorNotSupported) return fe;
     }
     // tensor-core passes, one launch per pass; before each position the
@@ -632,7 +633,7 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
     // itself), else the two-pass kernel (DSPARK_DRAFT_LAUNCH=two_pass or
     // per_pass selects the latter)
     if (fused_launch_enabled()) {
-      const cudaError_t e = launch_draft_fused(a, ws, L, s);
+      const cudaError_t e = launch_draft_fused(a, ws, L, s, ov);
       if (e != cudaErrorNotSupported) return e;
     }
     const int BG = d.B * d.gamma;
@@ -644,9 +645,11 @@ static cudaError_t launch_draft_t(const dspark_draft_args& a, uint8_t* ws, const
   return launch_cuda_core<T, T>(a, ws, L, s);
 }
 
-cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
-  if (a.dims.dtype == DSPARK_BF16) return launch_draft_t<__nv_bfloat16>(a, ws, L, s);
-  return launch_draft_t<float>(a, ws, L, s);
+cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                         DraftOverlap* ov) {
+  if (ov) ov->armed = false;
+  if (a.dims.dtype == DSPARK_BF16) return launch_draft_t<__nv_bfloat16>(a, ws, L, s, ov);
+  return launch_draft_t<float>(a, ws, L, s, ov);
 }
 
 }  // namespace dspark

@@ -121,6 +121,14 @@ struct Params {
   float* conf;
   unsigned* gbar;            // grid barrier counter, zero at launch
   unsigned* sched;           // [G + 1, n_mtiles] tile claims of each sweep, zero at launch
+  // A scheduler launched behind this kernel (programmatic dependent launch)
+  // overlaps its last sweep: every CTA adds 1 to sel_done (release) once its
+  // selects of the last position are done, then lets the dependent grid
+  // launch; CTA `donor` leaves its share of the last sweep to the others and
+  // exits, so that the scheduler finds a free SM.  sel_done = null, donor = -1:
+  // no scheduler behind.
+  unsigned* sel_done;
+  int donor;
   WsHeader* hdr;
   // RNN head (rnn_E non-null): E_k = tanh(W_o z_k), z_k = [s_k; W1[x_{k-1}]; h_k]
   const __nv_bfloat16* W_rnn;  // [3r, 2r + H]: gate, candidate and output rows
@@ -917,7 +925,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = q - 1;
         const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
         unsigned* claim = p.sched + (size_t)q * p.n_mtiles + m_tile;
-        unsigned ci = atomicAdd(claim, 1u);  // claim index of the tile n
+        // the donor CTA claims nothing in the last sweep (q = G has W items only)
+        const bool donate = q == G && (int)blockIdx.x == p.donor;
+        unsigned ci = donate ? (unsigned)p.ntiles : atomicAdd(claim, 1u);  // claim index of the tile n
         int n = tile_of(ci, q);
         while (ok) {
           // hand the tile (or the end of the sweep) to the MMA issuer and the
@@ -1357,6 +1367,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       select(q);
+      if (q + 1 == G && p.sel_done) {
+        // every select of this CTA is done (select_rows ends with the epilogue
+        // barrier): publish, then let a dependent scheduler launch
+        if (epi_tid == 0) {
+          __threadfence();
+          atomicAdd(p.sel_done, 1u);
+          ptx::launch_dependents();
+        }
+      }
       // E of the next sweep's S items (slot (q + 1) & 1 held E_{q-1}, whose
       // products all finished in this sweep); the gather waits for each row's
       // token, so no grid barrier follows the select: a CTA's next writes of a
@@ -2062,7 +2081,8 @@ static bool ring_w2_deep(int n_mtiles) {
 // The fused-sweep kernel needs every CTA resident (cooperative launch, one
 // CTA per SM) and at most one CTA's worth of M-tiles per SM; returns
 // cudaErrorNotSupported when it cannot run, so that the caller falls back.
-cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                               DraftOverlap* ov) {
   const dspark_dims& d = a.dims;
   int dev = 0, sms = 0, coop = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
@@ -2157,6 +2177,14 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.rnn_S = nullptr;
   p.rnn_E = nullptr;
   p.rnn_done = p.sched + (size_t)(d.gamma + 1) * n_mtiles;
+  // a scheduler behind this launch: the 128-row form with p_d rows (a last
+  // sweep to run beside) and more than one CTA
+  p.sel_done = nullptr;
+  p.donor = -1;
+  if (ov && ov->want && !narrow && a.pd_rows && p.n_ctas > 1) {
+    p.sel_done = p.gbar + 1;  // in the counters' 16-byte head, zeroed below
+    p.donor = p.n_ctas - 1;
+  }
   if (rnn) {
     // the h part of every position's projection, one GEMM before the sweeps
     float* P = reinterpret_cast<float*>(ws + L.rnn_p);
@@ -2188,12 +2216,18 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
     if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<true>, tmU, tmW2, p);
     return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<false>, tmU, tmW2, p);
   }
-  if (w2deep) {
-    if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingW2Deep>, tmU, tmW2, tmPd, p);
-    return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingW2Deep>, tmU, tmW2, tmPd, p);
+  if (w2deep)
+    e = rnn ? cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingW2Deep>, tmU, tmW2, tmPd, p)
+            : cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingW2Deep>, tmU, tmW2, tmPd, p);
+  else
+    e = rnn ? cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingUDeep>, tmU, tmW2, tmPd, p)
+            : cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingUDeep>, tmU, tmW2, tmPd, p);
+  if (e == cudaSuccess && p.sel_done) {
+    ov->armed = true;
+    ov->sel_done = p.sel_done;
+    ov->n_ctas = (unsigned)p.n_ctas;
   }
-  if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingUDeep>, tmU, tmW2, tmPd, p);
-  return cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingUDeep>, tmU, tmW2, tmPd, p);
+  return e;
 }
 
 }  // namespace dspark

@@ -72,11 +72,30 @@ dspark_status check_sched_args(const dspark_sched_args* a, int64_t max_keys);
 cudaError_t ensure_smem_limit(const void* func, int bytes);
 size_t elem_size(int dtype);
 
+// A scheduler run beside the draft kernel's last sweep (dspark_draft_and_schedule).
+// want: the caller will launch it behind the draft; on return armed says that
+// the fused-sweep kernel ran with a donor CTA and publishes its selects in
+// *sel_done, which reaches n_ctas once every confidence and token is written.
+struct DraftOverlap {
+  bool want = false;
+  bool armed = false;
+  unsigned* sel_done = nullptr;
+  unsigned n_ctas = 0;
+};
+
 // Launchers (argument checking happens in capi.cu before these are called).
-cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                         DraftOverlap* ov = nullptr);
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 // whether the asynchronous top-K mode can run at this size (one CTA's shared memory)
 bool schedule_async_supported(int B, int G);
+// whether the schedule is one launch of the shared-memory kernel that also
+// calibrates the keys (the form that can run behind the draft kernel)
+bool schedule_one_launch(int B, int G);
+// that launch with programmatic stream serialization behind the draft kernel,
+// waiting for *dep >= dep_target; cudaErrorNotSupported when !schedule_one_launch
+cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L,
+                                         const unsigned* dep, unsigned dep_target, cudaStream_t s);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 
 // RNN head (rnn_head.cu): P [B gamma, 3r] = the h_j part of every position's
@@ -125,6 +144,7 @@ cudaError_t launch_draft_tc(const dspark_draft_args& a, uint8_t* ws, const WsLay
                             const std::function<cudaError_t(int)>* hook = nullptr,
                             const void* Erows = nullptr);
 // Fused-sweep kernel (draft_fused.cu); cudaErrorNotSupported when it cannot run.
-cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
+cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                               DraftOverlap* ov = nullptr);
 
 }  // namespace dspark

@@ -146,6 +146,17 @@ __device__ __forceinline__ double block_excl_scan_f64(double v, double* sm, doub
 
 constexpr int PREP_THREADS = 256;
 
+__device__ __forceinline__ unsigned sched_ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t sched_globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // One CTA covers floor(256 / gamma) whole requests: each thread calibrates one
 // (request, position) confidence, then one thread per request forms the
 // left-to-right fp32 products and writes the sort keys.
@@ -542,12 +553,20 @@ __device__ __forceinline__ void block_argmax_f64(double& v, int& i, double* smv,
   __syncthreads();
 }
 
+// dep (may be null): launched behind the draft kernel with programmatic
+// stream serialization, so that it runs beside the draft's last sweep; the
+// draft's CTAs add 1 to *dep (release) once the confidences and tokens are
+// written and let this grid launch only after that, so the wait below finds
+// *dep == dep_target at once (it gives up after a bound all the same and
+// reports DSPARK_TIMEOUT to hdr).
 __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_args a, int n_pad,
                                                                   const __grid_constant__ DfTable tab,
                                                                   const uint32_t* __restrict__ k0,
                                                                   const uint32_t* __restrict__ v0,
                                                                   const uint32_t* __restrict__ k1,
-                                                                  const uint32_t* __restrict__ v1, int fused) {
+                                                                  const uint32_t* __restrict__ v1, int fused,
+                                                                  const unsigned* dep, unsigned dep_target,
+                                                                  WsHeader* hdr) {
   // [n_pad] slots, [n_pad] scratch (first holding the calibrated confidences),
   // [B (1 + gamma) + 1] SPS table, [B] l_r
   extern __shared__ uint64_t kv[];
@@ -565,6 +584,23 @@ __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule_smem(dspark_sched_a
   __shared__ StsConsts sc;
 
   const int tid = threadIdx.x;
+  if (dep) {
+    if (tid == 0) {
+      const uint64_t t0 = sched_globaltimer_ns();
+      int ok = 1;
+      while (sched_ld_acquire(dep) < dep_target) {
+        if (sched_globaltimer_ns() - t0 > 2000000000ull) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+      if (!ok) report_error(hdr, DSPARK_TIMEOUT, -1);
+      s_first = ok;
+    }
+    __syncthreads();
+    if (!s_first) return;
+  }
   const int R = sched_run_len(G);
   sts_consts_init(sc, a.sts_temp, G, tab);
   // the flatten's inputs for this thread's request, loaded now so that their
@@ -774,6 +810,39 @@ bool schedule_async_supported(int B, int G) {
   return sched_slots(B, G) <= kSmemSortMax && schedule_smem_bytes(B, G) <= kSmemSchedMax;
 }
 
+bool schedule_one_launch(int B, int G) {
+  return schedule_async_supported(B, G) && (int64_t)B * G <= kFusedKeys;
+}
+
+cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L,
+                                         const unsigned* dep, unsigned dep_target, cudaStream_t s) {
+  if (!schedule_one_launch(a.B, a.gamma)) return cudaErrorNotSupported;
+  uint32_t* k0 = reinterpret_cast<uint32_t*>(ws + L.sk0);
+  uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
+  uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
+  uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
+  const int n_pad = sched_slots(a.B, a.gamma);
+  if (const cudaError_t ae = ensure_smem_limit((const void*)k_schedule_smem, (int)kSmemSchedMax); ae != cudaSuccess)
+    return ae;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(SCH_THREADS);
+  cfg.dynamicSmemBytes = schedule_smem_bytes(a.B, a.gamma);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_schedule_smem, a, n_pad, df_table(), (const uint32_t*)k0,
+                                     (const uint32_t*)v0, (const uint32_t*)k1, (const uint32_t*)v1, 1, dep,
+                                     dep_target, reinterpret_cast<WsHeader*>(ws));
+  if (e != cudaSuccess) return e;
+  if (a.n_verify_host) e = cudaMemcpyAsync(a.n_verify_host, a.n_verify, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  return e;
+}
+
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
   uint32_t* k0 = reinterpret_cast<uint32_t*>(ws + L.sk0);
   uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
@@ -793,7 +862,8 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
       const int rb = PREP_THREADS / a.gamma;
       k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1, df_table());
     }
-    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, n_pad, df_table(), k0, v0, k1, v1, fused);
+    k_schedule_smem<<<1, SCH_THREADS, smem, s>>>(a, n_pad, df_table(), k0, v0, k1, v1, fused, nullptr, 0u,
+                                                 reinterpret_cast<WsHeader*>(ws));
     count_launches(fused ? 1 : 2);
   } else {
     const int rb = PREP_THREADS / a.gamma;

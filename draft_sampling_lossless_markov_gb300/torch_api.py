@@ -82,10 +82,7 @@ class Workspace:
         return code, detail
 
 
-def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int, out: Optional[dict] = None,
-                 stream=None, W_rnn=None, rows: bool = True, want_pd_stat: bool = False) -> dict:
-    """dspark_draft_sample; W_rnn [3r, 2r + H] (the dtype of U) selects the RNN head;
-    rows=False draws without p_d rows (pd_stat [B, gamma, 2] is then returned)."""
+def _draft_args(U, W1, W2, h, w, anchor, temp, req_id, seed, out, W_rnn, rows, want_pd_stat):
     B, G, V = U.shape
     r = W1.shape[1] if W1 is not None else 0
     H = h.shape[2] if h is not None else 0
@@ -112,13 +109,19 @@ def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int
     a.conf = _ptr(out["conf"], torch.float32)
     if W_rnn is not None:
         a.W_rnn, a.head = _ptr(W_rnn, dt), capi.DSPARK_HEAD_RNN
+    return a, out
+
+
+def draft_sample(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int, out: Optional[dict] = None,
+                 stream=None, W_rnn=None, rows: bool = True, want_pd_stat: bool = False) -> dict:
+    """dspark_draft_sample; W_rnn [3r, 2r + H] (the dtype of U) selects the RNN head;
+    rows=False draws without p_d rows (pd_stat [B, gamma, 2] is then returned)."""
+    a, out = _draft_args(U, W1, W2, h, w, anchor, temp, req_id, seed, out, W_rnn, rows, want_pd_stat)
     _check("dspark_draft_sample", capi.dspark_draft_sample(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out
 
 
-def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int, out: Optional[dict] = None,
-             stream=None, n_verify_host: Optional[torch.Tensor] = None, want_surv=False,
-             conf_logit_prev=None) -> dict:
+def _sched_args(conf_logit, sts_temp, sps, anchor, tokens, mode, out, n_verify_host, want_surv, conf_logit_prev):
     B, G = conf_logit.shape
     dev = conf_logit.device
     cap = B * (1 + G)
@@ -147,8 +150,30 @@ def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int
     a.surv = _ptr(out.get("surv"), torch.float32)
     a.conf_logit_prev = _ptr(conf_logit_prev, torch.float32) if conf_logit_prev is not None else None
     out["_sps"] = sps  # keep the table alive while the call is in flight
+    return a, out
+
+
+def schedule(ws: Workspace, conf_logit, sts_temp, sps, anchor, tokens, mode: int, out: Optional[dict] = None,
+             stream=None, n_verify_host: Optional[torch.Tensor] = None, want_surv=False,
+             conf_logit_prev=None) -> dict:
+    a, out = _sched_args(conf_logit, sts_temp, sps, anchor, tokens, mode, out, n_verify_host, want_surv,
+                         conf_logit_prev)
     _check("dspark_schedule", capi.dspark_schedule(a, ws.ptr, ws.nbytes, _stream(stream)))
     return out
+
+
+def draft_and_schedule(ws: Workspace, U, W1, W2, h, w, anchor, temp, req_id, seed: int, sts_temp, sps, mode: int,
+                       out: Optional[dict] = None, sched_out: Optional[dict] = None, stream=None, W_rnn=None,
+                       rows: bool = True, want_pd_stat: bool = False, n_verify_host: Optional[torch.Tensor] = None,
+                       want_surv=False, conf_logit_prev=None) -> tuple:
+    """dspark_draft_and_schedule: draft_sample then schedule of its confidences
+    and tokens, in one call that may overlap them; returns (draft out, schedule out)."""
+    da, out = _draft_args(U, W1, W2, h, w, anchor, temp, req_id, seed, out, W_rnn, rows, want_pd_stat)
+    sa, sched_out = _sched_args(out["conf_logit"], sts_temp, sps, anchor, out["tokens"], mode, sched_out,
+                                n_verify_host, want_surv, conf_logit_prev)
+    _check("dspark_draft_and_schedule",
+           capi.dspark_draft_and_schedule(da, sa, ws.ptr, ws.nbytes, _stream(stream)))
+    return out, sched_out
 
 
 def verify(ws: Workspace, target_logits, offsets, ell, tokens, pd_rows, pd_tok, temp, req_id, seed: int,

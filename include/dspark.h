@@ -242,6 +242,27 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
                               size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * dspark_draft_and_schedule
+ * ---------------------------------------------------------------------------
+ * dspark_draft_sample(draft) followed by dspark_schedule(sched) on the same
+ * stream, with the same results bit for bit, in one call that may overlap the
+ * two.  The schedule needs only the confidences and the tokens, which are
+ * final once the last position is drawn; the draft then still writes that
+ * position's p_d rows.  When the draft runs the 128-row fused-sweep
+ * tensor-core kernel with p_d rows and the schedule is one launch of the
+ * shared-memory scheduler (B * gamma <= 2048), one CTA of the draft kernel
+ * leaves that last sweep to the others and the scheduler kernel starts on its
+ * SM (programmatic dependent launch) while the sweep runs.  Other shapes run
+ * the two calls one after the other.
+ * Arguments: as for the two calls, one workspace for both (sized for the
+ * draft's dims); sched->B and sched->gamma must equal draft->dims, and
+ * sched->conf_logit, sched->tokens and sched->anchor must be the draft's
+ * conf_logit, tokens and anchor pointers, else DSPARK_INVALID_ARG.  Every
+ * argument check of both calls happens before anything is enqueued. */
+DSPARK_API dspark_status dspark_draft_and_schedule(const dspark_draft_args* draft, const dspark_sched_args* sched,
+                                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * dspark_schedule_noalloc
  * ---------------------------------------------------------------------------
  * The pages have no counterpart to this entry point: it is a library

@@ -97,6 +97,26 @@ def test_argument_errors_return_before_any_launch(lib):
     assert capi.dspark_schedule(s, 0, 0, 0) == capi.DSPARK_UNSUPPORTED  # 32768 slots
     assert capi.dspark_schedule_noalloc(s, 0) == capi.DSPARK_UNSUPPORTED
 
+    # the combined draft + schedule call: its own consistency checks, then both calls' checks
+    d.dims = capi.dspark_dims(64, 7, 64, 8, 16, capi.DSPARK_F32)
+    s.B, s.gamma, s.mode, s.conf_logit_prev = 64, 7, capi.DSPARK_SCHED_GREEDY, None
+    s.conf_logit, s.tokens, s.anchor = d.conf_logit, d.tokens, d.anchor
+    assert lib.dspark_draft_and_schedule(None, ctypes.byref(s), None, 0, None) == capi.DSPARK_INVALID_ARG
+    assert lib.dspark_draft_and_schedule(ctypes.byref(d), None, None, 0, None) == capi.DSPARK_INVALID_ARG
+    d.U = 0x10004
+    assert capi.dspark_draft_and_schedule(d, s, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG  # misaligned U
+    d.U = 0x10000
+    assert capi.dspark_draft_and_schedule(d, s, 0x20000, 16, 0) == capi.DSPARK_INVALID_ARG  # workspace too small
+    s.conf_logit = 0x30000  # not the draft's confidences
+    assert capi.dspark_draft_and_schedule(d, s, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
+    s.conf_logit, s.gamma = d.conf_logit, 6  # shape differs from the draft's
+    assert capi.dspark_draft_and_schedule(d, s, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
+    s.gamma, s.mode = 7, 9
+    assert capi.dspark_draft_and_schedule(d, s, 0x20000, 1 << 30, 0) == capi.DSPARK_INVALID_ARG
+    s.mode = capi.DSPARK_SCHED_GREEDY
+    d.dims, s.B = capi.dspark_dims(0, 7, 64, 8, 16, capi.DSPARK_F32), 0
+    assert capi.dspark_draft_and_schedule(d, s, 0, 0, 0) == capi.DSPARK_OK  # empty batch
+
     v = capi.dspark_verify_args()
     v.dims = capi.dspark_dims(4, 4, 64, 0, 0, capi.DSPARK_BF16)
     assert capi.dspark_verify(v, 0, 0, 0) == capi.DSPARK_INVALID_ARG
