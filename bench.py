@@ -206,7 +206,7 @@ def run_ours(args, rank, world, local_rank):
     rows = torch.empty((cap, V), dtype=inp["U"].dtype, device=dev)
     tgt_flat = inp["target"].reshape(-1, V)
 
-    overlap = args.sched_overlap == "on"
+    overlap = sched_overlaps(wl, args)
 
     def draft_call(st):
         if overlap:
@@ -308,8 +308,8 @@ def run_ours(args, rank, world, local_rank):
           "verify_ms": float(np.median(per[:, 2])),
           "timer": "CUDA events around each call's graph replay inside the timed region; median over the steps"}
     if overlap:
-        br["schedule"] = ("inside the draft call (dspark_draft_and_schedule): beside the draft kernel's last "
-                          "sweep where the shapes allow, else right after it; draft_ms covers both")
+        br["schedule"] = ("inside the draft call (dspark_draft_and_schedule), beside the draft kernel's last "
+                          "sweep; draft_ms covers both")
     nv = B * (G + 1) if cap_accept else int(s_out["n_verify"][0])
     ms = max_over_ranks(ms, world, dev)
     code, detail = ws.read_error()
@@ -337,7 +337,7 @@ def run_ours(args, rank, world, local_rank):
         "config": workload_config(wl, args, inp["sched_mode"], world),
         "run": {"n_verify_rows": nv, "graph": use_graph, "ms_per_step_mean": float(np.mean(ms_steps)),
                 "ms_per_step_min": float(np.min(ms_steps)), "ms_per_step_max": float(np.max(ms_steps)),
-                "sched_overlap": args.sched_overlap},
+                "sched_overlap": overlap},
         "hbm_frac_step": bytes_["step_per_position"] / (ms * 1e-3) / 1e9 / peak,
         "hbm_frac_step_strict": bytes_["step_strict"] / (ms * 1e-3) / 1e9 / peak,
         "step_bytes": {"per_position": bytes_["step_per_position"], "strict": bytes_["step_strict"]},
@@ -367,17 +367,23 @@ def draft_kernel_name(wl):
     return "fz::k_draft_narrow" if small else "fz::k_draft_fused"
 
 
+def sched_overlaps(wl, args):
+    """Whether the step runs the draft and the schedule as one call: where the
+    library runs the scheduler beside the draft kernel's last sweep (the 128-row
+    fused form with p_d rows, B gamma <= 2048).  Elsewhere the two calls stay
+    apart, so that the draft call's time is the draft kernel's."""
+    fused = draft_kernel_name(wl) == "fz::k_draft_fused" and not (args.head == "rnn" and wl.B > 512)
+    return args.sched_overlap == "on" and fused and args.rows != "none" and wl.B * wl.gamma <= 2048
+
+
 def draft_call_label(wl, args):
     """What the roofline's dominant call runs (the library's default dispatch)."""
-    call = "dspark_draft_and_schedule" if args.sched_overlap == "on" else "dspark_draft_sample"
     if args.head == "rnn" and wl.B > 512:
-        return f"{call}, RNN head (two-pass tensor-core passes, tensor-core recurrent step per position)"
+        return "dspark_draft_sample, RNN head (two-pass tensor-core passes, tensor-core recurrent step per position)"
     head = ", RNN head" if args.head == "rnn" else ""
-    beside = ""
-    if (args.sched_overlap == "on" and draft_kernel_name(wl) == "fz::k_draft_fused" and args.rows != "none"
-            and wl.B * wl.gamma <= 2048):
-        beside = ", k_schedule_smem beside its last sweep"
-    return f"{call}{head} ({draft_kernel_name(wl)}, one launch{beside})"
+    if sched_overlaps(wl, args):
+        return f"dspark_draft_and_schedule{head} ({draft_kernel_name(wl)}, one launch, k_schedule_smem beside its last sweep)"
+    return f"dspark_draft_sample{head} ({draft_kernel_name(wl)}, one launch)"
 
 
 def load_traffic(wl):
@@ -465,7 +471,7 @@ def run_e2e(args, T, capi, wl, inp, ws, dev, stream, sps_dev):
         sm = d_small[k]
         with torch.cuda.stream(stream):
             stream.wait_event(copied[k])
-            if args.sched_overlap == "on":
+            if sched_overlaps(wl, args):
                 d, s = draft_and_sched(T, ws, inp, d_U[k], d_h[k], sm["anchor"], sm["temp"], sm["req_id"], sps_dev,
                                        None, None, stream, rows=args.rows != "none", n_verify_host=h_nv[k])
             else:
@@ -959,8 +965,8 @@ def main():
                     help="comma-separated workloads (or 'all': the batch/gamma sweep and the named configs): one "
                          "JSON line per workload, device-timed only (no end-to-end leg, no oracle baseline)")
     ap.add_argument("--sched-overlap", default="on", choices=["on", "off"],
-                    help="on: the step's draft and schedule as one dspark_draft_and_schedule call (the scheduler "
-                         "beside the draft kernel's last sweep); off: two calls")
+                    help="on: where the scheduler can run beside the draft kernel's last sweep, the step's draft "
+                         "and schedule are one dspark_draft_and_schedule call; off: always two calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0,
