@@ -370,10 +370,23 @@ def draft_kernel_name(wl):
 def sched_overlaps(wl, args):
     """Whether the step runs the draft and the schedule as one call: where the
     library runs the scheduler beside the draft kernel's last sweep (the 128-row
-    fused form with p_d rows, B gamma <= 2048).  Elsewhere the two calls stay
-    apart, so that the draft call's time is the draft kernel's."""
+    fused form with p_d rows, a schedule that fits one CTA's shared memory).
+    Elsewhere the two calls stay apart, so that the draft call's time is the
+    draft kernel's."""
     fused = draft_kernel_name(wl) == "fz::k_draft_fused" and not (args.head == "rnn" and wl.B > 512)
-    return args.sched_overlap == "on" and fused and args.rows != "none" and wl.B * wl.gamma <= 2048
+    return args.sched_overlap == "on" and fused and args.rows != "none" and sched_fits_one_cta(wl.B, wl.gamma)
+
+
+def sched_fits_one_cta(B, G):
+    """The library's one-CTA shared-memory scheduler: B and gamma rounded up to
+    powers of two give at most 8192 slots, and its shared memory (two u64 per
+    slot, the f64 SPS table, one i32 per request) stays within 200 KB."""
+    nb, R = 1, 1
+    while nb < B:
+        nb <<= 1
+    while R < G:
+        R <<= 1
+    return nb * R <= 8192 and 2 * nb * R * 8 + (B * (1 + G) + 1) * 8 + B * 4 <= 200 * 1024
 
 
 def draft_call_label(wl, args):

@@ -221,7 +221,7 @@ dspark_status dspark_draft_and_schedule(const dspark_draft_args* da, const dspar
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const cudaStream_t s = (cudaStream_t)stream;
   DraftOverlap ov;
-  ov.want = schedule_one_launch(sa->B, sa->gamma);
+  ov.want = schedule_behind_draft_supported(sa->B, sa->gamma);
   cudaError_t e = launch_draft(*da, ws, L, s, &ov);
   if (e == cudaErrorNotSupported && !da->pd_rows) return DSPARK_UNSUPPORTED;
   if (e != cudaSuccess) return cuda_status(e);

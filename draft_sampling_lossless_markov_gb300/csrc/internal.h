@@ -89,11 +89,12 @@ cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 // whether the asynchronous top-K mode can run at this size (one CTA's shared memory)
 bool schedule_async_supported(int B, int G);
-// whether the schedule is one launch of the shared-memory kernel that also
+// whether the schedule fits the one-CTA shared-memory kernel, which then also
 // calibrates the keys (the form that can run behind the draft kernel)
-bool schedule_one_launch(int B, int G);
+bool schedule_behind_draft_supported(int B, int G);
 // that launch with programmatic stream serialization behind the draft kernel,
-// waiting for *dep >= dep_target; cudaErrorNotSupported when !schedule_one_launch
+// waiting for *dep >= dep_target; cudaErrorNotSupported when
+// !schedule_behind_draft_supported
 cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L,
                                          const unsigned* dep, unsigned dep_target, cudaStream_t s);
 cudaError_t launch_verify(const dspark_verify_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);

@@ -810,13 +810,11 @@ bool schedule_async_supported(int B, int G) {
   return sched_slots(B, G) <= kSmemSortMax && schedule_smem_bytes(B, G) <= kSmemSchedMax;
 }
 
-bool schedule_one_launch(int B, int G) {
-  return schedule_async_supported(B, G) && (int64_t)B * G <= kFusedKeys;
-}
+bool schedule_behind_draft_supported(int B, int G) { return schedule_async_supported(B, G); }
 
 cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L,
                                          const unsigned* dep, unsigned dep_target, cudaStream_t s) {
-  if (!schedule_one_launch(a.B, a.gamma)) return cudaErrorNotSupported;
+  if (!schedule_behind_draft_supported(a.B, a.gamma)) return cudaErrorNotSupported;
   uint32_t* k0 = reinterpret_cast<uint32_t*>(ws + L.sk0);
   uint32_t* k1 = reinterpret_cast<uint32_t*>(ws + L.sk1);
   uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
@@ -835,6 +833,8 @@ cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
+  // the keys calibrated in this one CTA at every size (fused = 1): beside the
+  // draft's last sweep that costs less than a second launch on many SMs would
   cudaError_t e = cudaLaunchKernelEx(&cfg, k_schedule_smem, a, n_pad, df_table(), (const uint32_t*)k0,
                                      (const uint32_t*)v0, (const uint32_t*)k1, (const uint32_t*)v1, 1, dep,
                                      dep_target, reinterpret_cast<WsHeader*>(ws));

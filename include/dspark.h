@@ -249,8 +249,10 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
  * two.  The schedule needs only the confidences and the tokens, which are
  * final once the last position is drawn; the draft then still writes that
  * position's p_d rows.  When the draft runs the 128-row fused-sweep
- * tensor-core kernel with p_d rows and the schedule is one launch of the
- * shared-memory scheduler (B * gamma <= 2048), one CTA of the draft kernel
+ * tensor-core kernel with p_d rows and the schedule fits the one-CTA
+ * shared-memory scheduler (B rounded up to a power of two times gamma
+ * rounded up to a power of two at most 8192 slots, within 200 KB of shared
+ * memory), one CTA of the draft kernel
  * leaves that last sweep to the others and the scheduler kernel starts on its
  * SM (programmatic dependent launch) while the sweep runs.  Other shapes run
  * the two calls one after the other.
