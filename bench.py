@@ -369,11 +369,12 @@ def draft_kernel_name(wl):
 
 def sched_overlaps(wl, args):
     """Whether the step runs the draft and the schedule as one call: where the
-    library runs the scheduler beside the draft kernel's last sweep (the 128-row
-    fused form with p_d rows, a schedule that fits one CTA's shared memory).
+    library runs the scheduler beside the draft kernel's last sweep (either
+    fused tensor-core form with p_d rows, a schedule that fits one CTA's shared
+    memory).
     Elsewhere the two calls stay apart, so that the draft call's time is the
     draft kernel's."""
-    fused = draft_kernel_name(wl) == "fz::k_draft_fused" and not (args.head == "rnn" and wl.B > 512)
+    fused = not (args.head == "rnn" and wl.B > 512)  # both fused forms (k_draft_fused, k_draft_narrow)
     return args.sched_overlap == "on" and fused and args.rows != "none" and sched_fits_one_cta(wl.B, wl.gamma)
 
 

@@ -1607,7 +1607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = q - 1;
         const bool hasW = p.write_pd && s >= 0, hasS = s + 1 < G;
         unsigned* claim = p.sched + q;
-        unsigned ci = atomicAdd(claim, 1u);
+        // the donor CTA claims nothing in the last sweep (q = G has W items only)
+        const bool donate = q == G && (int)blockIdx.x == p.donor;
+        unsigned ci = donate ? (unsigned)p.ntiles : atomicAdd(claim, 1u);
         int n = tile_of(ci, q);
         while (ok) {
           tq[jq % kTQ] = n;
@@ -1989,6 +1991,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       select_rows(p, q, sScr, team, tw, lane);
+      if (q + 1 == G && p.sel_done && epi_tid == 0) {
+        // every select of this CTA is done: publish, then let a dependent
+        // scheduler launch (as in the 128-row form)
+        __threadfence();
+        atomicAdd(p.sel_done, 1u);
+        ptx::launch_dependents();
+      }
       if (q + 1 < G) {
         gather(q + 1);
       } else {
@@ -2177,11 +2186,11 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.rnn_S = nullptr;
   p.rnn_E = nullptr;
   p.rnn_done = p.sched + (size_t)(d.gamma + 1) * n_mtiles;
-  // a scheduler behind this launch: the 128-row form with p_d rows (a last
-  // sweep to run beside) and more than one CTA
+  // a scheduler behind this launch: either form with p_d rows (a last sweep
+  // to run beside) and more than one CTA
   p.sel_done = nullptr;
   p.donor = -1;
-  if (ov && ov->want && !narrow && a.pd_rows && p.n_ctas > 1) {
+  if (ov && ov->want && a.pd_rows && p.n_ctas > 1) {
     p.sel_done = p.gbar + 1;  // in the counters' 16-byte head, zeroed below
     p.donor = p.n_ctas - 1;
   }
@@ -2212,11 +2221,10 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
-  if (narrow) {
-    if (rnn) return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<true>, tmU, tmW2, p);
-    return cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<false>, tmU, tmW2, p);
-  }
-  if (w2deep)
+  if (narrow)
+    e = rnn ? cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<true>, tmU, tmW2, p)
+            : cudaLaunchKernelEx(&cfg, fz::k_draft_narrow<false>, tmU, tmW2, p);
+  else if (w2deep)
     e = rnn ? cudaLaunchKernelEx(&cfg, fz::k_draft_fused<true, fz::kRingW2Deep>, tmU, tmW2, tmPd, p)
             : cudaLaunchKernelEx(&cfg, fz::k_draft_fused<false, fz::kRingW2Deep>, tmU, tmW2, tmPd, p);
   else

@@ -248,8 +248,9 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
  * stream, with the same results bit for bit, in one call that may overlap the
  * two.  The schedule needs only the confidences and the tokens, which are
  * final once the last position is drawn; the draft then still writes that
- * position's p_d rows.  When the draft runs the 128-row fused-sweep
- * tensor-core kernel with p_d rows and the schedule fits the one-CTA
+ * position's p_d rows.  When the draft runs a fused-sweep tensor-core kernel
+ * (the 128-row form or the small-batch form) with p_d rows and the schedule
+ * fits the one-CTA
  * shared-memory scheduler (B rounded up to a power of two times gamma
  * rounded up to a power of two at most 8192 slots, within 200 KB of shared
  * memory), one CTA of the draft kernel

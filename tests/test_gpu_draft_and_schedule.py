@@ -1,6 +1,6 @@
 """dspark_draft_and_schedule: the draft and the schedule in one call, the
-scheduler running beside the draft kernel's last sweep where it can (the
-128-row fused form with p_d rows and a schedule that fits one CTA's shared
+scheduler running beside the draft kernel's last sweep where it can (either
+fused tensor-core form with p_d rows and a schedule that fits one CTA's shared
 memory), else one after the other.  Every output must equal, bit for bit, what dspark_draft_sample followed
 by dspark_schedule give on the same inputs (both checked against the oracle
 elsewhere); the schedule is also compared with the oracle's scheduler run on
@@ -31,7 +31,9 @@ CASES = [
     (64, 7, 4104, 64, 8, "bf16", "markov", synth.SCHED_ASYNC_TOPK),      # overlapped, asynchronous scheduler
     (200, 4, 8200, 128, 8, "bf16", "rnn", synth.SCHED_GREEDY),           # overlapped, RNN head in the fused form
     (256, 7, 8200, 256, 16, "bf16", "markov", synth.SCHED_OFF),          # overlapped, scheduler off
-    (8, 4, 8200, 256, 16, "bf16", "markov", synth.SCHED_GREEDY),         # small-batch form: in sequence
+    (8, 4, 8200, 256, 16, "bf16", "markov", synth.SCHED_GREEDY),         # overlapped, small-batch form
+    (1, 7, 8200, 256, 16, "bf16", "markov", synth.SCHED_GREEDY),         # overlapped, small-batch form, one request
+    (12, 3, 4104, 128, 8, "bf16", "rnn", synth.SCHED_GREEDY),            # overlapped, small-batch RNN form
     (600, 4, 4104, 128, 8, "bf16", "markov", synth.SCHED_GREEDY),        # overlapped, 2400 candidates
     (1024, 7, 2056, 64, 8, "bf16", "markov", synth.SCHED_GREEDY),        # overlapped, 8192 slots (the keys
                                                                          # calibrated in the one CTA)
