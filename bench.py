@@ -370,24 +370,11 @@ def draft_kernel_name(wl):
 def sched_overlaps(wl, args):
     """Whether the step runs the draft and the schedule as one call: where the
     library runs the scheduler beside the draft kernel's last sweep (either
-    fused tensor-core form with p_d rows, a schedule that fits one CTA's shared
-    memory).
+    fused tensor-core form with p_d rows).
     Elsewhere the two calls stay apart, so that the draft call's time is the
     draft kernel's."""
     fused = not (args.head == "rnn" and wl.B > 512)  # both fused forms (k_draft_fused, k_draft_narrow)
-    return args.sched_overlap == "on" and fused and args.rows != "none" and sched_fits_one_cta(wl.B, wl.gamma)
-
-
-def sched_fits_one_cta(B, G):
-    """The library's one-CTA shared-memory scheduler: B and gamma rounded up to
-    powers of two give at most 8192 slots, and its shared memory (two u64 per
-    slot, the f64 SPS table, one i32 per request) stays within 200 KB."""
-    nb, R = 1, 1
-    while nb < B:
-        nb <<= 1
-    while R < G:
-        R <<= 1
-    return nb * R <= 8192 and 2 * nb * R * 8 + (B * (1 + G) + 1) * 8 + B * 4 <= 200 * 1024
+    return args.sched_overlap == "on" and fused and args.rows != "none"
 
 
 def draft_call_label(wl, args):

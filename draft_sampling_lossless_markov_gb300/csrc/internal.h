@@ -89,8 +89,9 @@ cudaError_t launch_draft(const dspark_draft_args& a, uint8_t* ws, const WsLayout
 cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L, cudaStream_t s);
 // whether the asynchronous top-K mode can run at this size (one CTA's shared memory)
 bool schedule_async_supported(int B, int G);
-// whether the schedule fits the one-CTA shared-memory kernel, which then also
-// calibrates the keys (the form that can run behind the draft kernel)
+// whether the schedule can run behind the draft kernel as one CTA that also
+// calibrates the keys: the shared-memory kernel up to 8192 slots, the radix
+// kernel above (every size dspark_schedule accepts)
 bool schedule_behind_draft_supported(int B, int G);
 // that launch with programmatic stream serialization behind the draft kernel,
 // waiting for *dep >= dep_target; cudaErrorNotSupported when

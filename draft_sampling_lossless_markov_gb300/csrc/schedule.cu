@@ -197,17 +197,57 @@ __global__ void __launch_bounds__(PREP_THREADS) k_sched_prep(dspark_sched_args a
   }
 }
 
+// fused_keys: this CTA forms the keys itself (k_sched_prep's arithmetic, one
+// request per thread at a time) instead of reading k_sched_prep's; dep: as
+// for k_schedule_smem (launched behind the draft kernel, beside its last sweep).
 __global__ void __launch_bounds__(SCH_THREADS, 1) k_schedule(dspark_sched_args a, uint32_t* __restrict__ k0,
                                                              uint32_t* __restrict__ k1, uint32_t* __restrict__ v0,
-                                                             uint32_t* __restrict__ v1) {
+                                                             uint32_t* __restrict__ v1, int fused_keys,
+                                                             const __grid_constant__ DfTable tab,
+                                                             const unsigned* dep, unsigned dep_target,
+                                                             WsHeader* hdr) {
   __shared__ uint32_t hist[256 * SCH_WARPS];  // [digit][warp], digit-major
   __shared__ uint32_t sm_u[40];
   __shared__ double sm_d[40];
   __shared__ int s_first;
   __shared__ double s_theta_best;
+  __shared__ StsConsts sc;
 
   const int B = a.B, G = a.gamma, n = B * G;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (dep) {
+    if (tid == 0) {
+      const uint64_t t0 = sched_globaltimer_ns();
+      int ok = 1;
+      while (sched_ld_acquire(dep) < dep_target) {
+        if (sched_globaltimer_ns() - t0 > 2000000000ull) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+      if (!ok) report_error(hdr, DSPARK_TIMEOUT, -1);
+      s_first = ok;
+    }
+    __syncthreads();
+    if (!s_first) return;
+  }
+  if (fused_keys) {
+    sts_consts_init(sc, a.sts_temp, G, tab);
+    __syncthreads();
+    for (int r = tid; r < B; r += SCH_THREADS) {
+      float run = 1.f;
+      for (int jj = 0; jj < G; ++jj) {
+        const int idx = r * G + jj;
+        run = __fmul_rn(run, sts_conf(sc, a.conf_logit[idx], jj));
+        k0[idx] = run > 0.f ? ~__float_as_uint(run) : 0xFFFFFFFFu;
+        v0[idx] = (uint32_t)idx;
+        if (a.surv) a.surv[idx] = run;
+      }
+      a.ell[r] = (a.mode == DSPARK_SCHED_OFF) ? G : 0;
+    }
+    __syncthreads();  // the keys and l_r = 0, for every thread of the CTA
+  }
 
   // ---- candidates: keys written by k_sched_prep; a > 0 unless the key is all ones ----
   uint32_t ncand_local = 0;
@@ -810,7 +850,7 @@ bool schedule_async_supported(int B, int G) {
   return sched_slots(B, G) <= kSmemSortMax && schedule_smem_bytes(B, G) <= kSmemSchedMax;
 }
 
-bool schedule_behind_draft_supported(int B, int G) { return schedule_async_supported(B, G); }
+bool schedule_behind_draft_supported(int B, int G) { return (int64_t)B * G <= DSPARK_MAX_SCHED_KEYS; }
 
 cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws, const WsLayout& L,
                                          const unsigned* dep, unsigned dep_target, cudaStream_t s) {
@@ -820,12 +860,16 @@ cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws
   uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + L.sv0);
   uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + L.sv1);
   const int n_pad = sched_slots(a.B, a.gamma);
-  if (const cudaError_t ae = ensure_smem_limit((const void*)k_schedule_smem, (int)kSmemSchedMax); ae != cudaSuccess)
-    return ae;
+  const bool smem_path = schedule_async_supported(a.B, a.gamma);
+  if (smem_path) {
+    if (const cudaError_t ae = ensure_smem_limit((const void*)k_schedule_smem, (int)kSmemSchedMax);
+        ae != cudaSuccess)
+      return ae;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(SCH_THREADS);
-  cfg.dynamicSmemBytes = schedule_smem_bytes(a.B, a.gamma);
+  cfg.dynamicSmemBytes = smem_path ? schedule_smem_bytes(a.B, a.gamma) : 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -833,11 +877,14 @@ cudaError_t launch_schedule_behind_draft(const dspark_sched_args& a, uint8_t* ws
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
-  // the keys calibrated in this one CTA at every size (fused = 1): beside the
-  // draft's last sweep that costs less than a second launch on many SMs would
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_schedule_smem, a, n_pad, df_table(), (const uint32_t*)k0,
-                                     (const uint32_t*)v0, (const uint32_t*)k1, (const uint32_t*)v1, 1, dep,
-                                     dep_target, reinterpret_cast<WsHeader*>(ws));
+  // the keys calibrated in this one CTA at every size (no k_sched_prep on many
+  // SMs): beside the draft's last sweep only one SM is free
+  cudaError_t e = smem_path
+                      ? cudaLaunchKernelEx(&cfg, k_schedule_smem, a, n_pad, df_table(), (const uint32_t*)k0,
+                                           (const uint32_t*)v0, (const uint32_t*)k1, (const uint32_t*)v1, 1, dep,
+                                           dep_target, reinterpret_cast<WsHeader*>(ws))
+                      : cudaLaunchKernelEx(&cfg, k_schedule, a, k0, k1, v0, v1, 1, df_table(), dep, dep_target,
+                                           reinterpret_cast<WsHeader*>(ws));
   if (e != cudaSuccess) return e;
   if (a.n_verify_host) e = cudaMemcpyAsync(a.n_verify_host, a.n_verify, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   return e;
@@ -868,7 +915,8 @@ cudaError_t launch_schedule(const dspark_sched_args& a, uint8_t* ws, const WsLay
   } else {
     const int rb = PREP_THREADS / a.gamma;
     k_sched_prep<<<(a.B + rb - 1) / rb, PREP_THREADS, 0, s>>>(a, k0, v0, k1, v1, df_table());
-    k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1);
+    k_schedule<<<1, SCH_THREADS, 0, s>>>(a, k0, k1, v0, v1, 0, df_table(), nullptr, 0u,
+                                         reinterpret_cast<WsHeader*>(ws));
     count_launches(2);
   }
   cudaError_t e = cudaGetLastError();

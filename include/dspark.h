@@ -249,14 +249,12 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
  * two.  The schedule needs only the confidences and the tokens, which are
  * final once the last position is drawn; the draft then still writes that
  * position's p_d rows.  When the draft runs a fused-sweep tensor-core kernel
- * (the 128-row form or the small-batch form) with p_d rows and the schedule
- * fits the one-CTA
- * shared-memory scheduler (B rounded up to a power of two times gamma
- * rounded up to a power of two at most 8192 slots, within 200 KB of shared
- * memory), one CTA of the draft kernel
- * leaves that last sweep to the others and the scheduler kernel starts on its
- * SM (programmatic dependent launch) while the sweep runs.  Other shapes run
- * the two calls one after the other.
+ * (the 128-row form or the small-batch form) with p_d rows, one CTA of the
+ * draft kernel leaves that last sweep to the others and the scheduler (one
+ * CTA, which then also calibrates the keys that dspark_schedule calibrates on
+ * many SMs above 2048 candidates) starts on its SM by programmatic dependent
+ * launch while the sweep runs.  Other shapes (the row-free mode, the two-pass
+ * and CUDA-core paths) run the two calls one after the other.
  * Arguments: as for the two calls, one workspace for both (sized for the
  * draft's dims); sched->B and sched->gamma must equal draft->dims, and
  * sched->conf_logit, sched->tokens and sched->anchor must be the draft's

@@ -37,7 +37,10 @@ CASES = [
     (600, 4, 4104, 128, 8, "bf16", "markov", synth.SCHED_GREEDY),        # overlapped, 2400 candidates
     (1024, 7, 2056, 64, 8, "bf16", "markov", synth.SCHED_GREEDY),        # overlapped, 8192 slots (the keys
                                                                          # calibrated in the one CTA)
-    (1100, 8, 2056, 64, 8, "bf16", "markov", synth.SCHED_GREEDY),        # 16384 slots: in sequence
+    (1100, 8, 2056, 64, 8, "bf16", "markov", synth.SCHED_GREEDY),        # overlapped, 16384 slots: the radix
+                                                                         # kernel forming its own keys
+    (2100, 16, 1000, 64, 8, "bf16", "markov", synth.SCHED_GREEDY),       # overlapped, 33600 candidates
+    (1100, 8, 2056, 64, 8, "bf16", "markov", synth.SCHED_OFF),           # overlapped, radix kernel, scheduler off
     (40, 3, 1000, 16, 8, "f32", "markov", synth.SCHED_GREEDY),           # CUDA-core path: in sequence
 ]
 
