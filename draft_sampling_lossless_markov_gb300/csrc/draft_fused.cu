@@ -2187,12 +2187,15 @@ cudaError_t launch_draft_fused(const dspark_draft_args& a, uint8_t* ws, const Ws
   p.rnn_E = nullptr;
   p.rnn_done = p.sched + (size_t)(d.gamma + 1) * n_mtiles;
   // a scheduler behind this launch: either form with p_d rows (a last sweep
-  // to run beside) and more than one CTA
+  // to run beside) and more than one CTA.  It needs a free SM: a donor CTA
+  // when the grid fills every SM; otherwise an idle SM takes it and every CTA
+  // keeps its share of the last sweep (a donor would leave its M-tile one CTA
+  // short for that sweep).
   p.sel_done = nullptr;
   p.donor = -1;
   if (ov && ov->want && a.pd_rows && p.n_ctas > 1) {
     p.sel_done = p.gbar + 1;  // in the counters' 16-byte head, zeroed below
-    p.donor = p.n_ctas - 1;
+    p.donor = p.n_ctas < sms ? -1 : p.n_ctas - 1;
   }
   if (rnn) {
     // the h part of every position's projection, one GEMM before the sweeps
