@@ -249,11 +249,12 @@ DSPARK_API dspark_status dspark_schedule(const dspark_sched_args* args, void* wo
  * two.  The schedule needs only the confidences and the tokens, which are
  * final once the last position is drawn; the draft then still writes that
  * position's p_d rows.  When the draft runs a fused-sweep tensor-core kernel
- * (the 128-row form or the small-batch form) with p_d rows, one CTA of the
- * draft kernel leaves that last sweep to the others and the scheduler (one
- * CTA, which then also calibrates the keys that dspark_schedule calibrates on
- * many SMs above 2048 candidates) starts on its SM by programmatic dependent
- * launch while the sweep runs.  Other shapes (the row-free mode, the two-pass
+ * (the 128-row form or the small-batch form) with p_d rows, the scheduler
+ * (one CTA, which then also calibrates the keys that dspark_schedule
+ * calibrates on many SMs above 2048 candidates) starts by programmatic
+ * dependent launch while that sweep runs: on an SM the draft grid leaves
+ * idle, or, when the grid fills every SM, on the SM of one draft CTA that
+ * leaves the last sweep to the others.  Other shapes (the row-free mode, the two-pass
  * and CUDA-core paths) run the two calls one after the other.
  * Arguments: as for the two calls, one workspace for both (sized for the
  * draft's dims); sched->B and sched->gamma must equal draft->dims, and
