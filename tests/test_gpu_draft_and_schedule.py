@@ -102,3 +102,37 @@ def test_draft_and_schedule_repeated_on_one_workspace():
         for a, b in zip(got, first):
             np.testing.assert_array_equal(a, b)
     check_no_error(ws)
+
+
+@pytest.mark.parametrize("B,G", [(256, 7), (8, 4)])
+def test_draft_and_schedule_in_a_cuda_graph(B, G):
+    # the call captured into a CUDA graph (the programmatic dependency becomes a
+    # graph edge) and replayed: the same outputs as the eager call
+    wl = synth.Workload("ds", B, G, 8200, 16, 256, "bf16", "mixed", synth.SCHED_GREEDY, "tiny", seed=7)
+    inp = synth.make_inputs(wl, "cuda", with_target=False)
+    ws = workspace_for(B, G, 8200, 256, 16, inp["U"].dtype)
+    sps = torch.from_numpy(np.ascontiguousarray(inp["sps"], dtype=np.float64)).cuda()
+    args = (inp["U"], inp["W1"], inp["W2"], inp["h"], inp["w"], inp["anchor"], inp["temp"], inp["req_id"],
+            inp["seed"])
+    d0, s0 = T.draft_and_schedule(ws, *args, inp["sts"], sps, synth.SCHED_GREEDY)
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in list(d0.items()) + [("s_" + k, v) for k, v in s0.items() if not k.startswith("_")]}
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        T.draft_and_schedule(ws, *args, inp["sts"], sps, synth.SCHED_GREEDY, out=d0, sched_out=s0, stream=st)
+    st.synchronize()
+    with torch.cuda.graph(g, stream=st):
+        T.draft_and_schedule(ws, *args, inp["sts"], sps, synth.SCHED_GREEDY, out=d0, sched_out=s0,
+                             stream=torch.cuda.current_stream())
+    for _ in range(2):
+        for v in list(d0.values()) + [v for k, v in s0.items() if not k.startswith("_")]:
+            v.fill_(-7) if v.dtype != torch.float64 else v.fill_(-7.0)
+        g.replay()
+        st.synchronize()
+        for k, v in d0.items():
+            assert torch.equal(v, ref[k]), k
+        for k, v in s0.items():
+            if not k.startswith("_"):
+                assert torch.equal(v, ref["s_" + k]), k
+    check_no_error(ws)
